@@ -1,0 +1,304 @@
+/*
+ * Plain CPU oracle of the fused MLA attention prolog.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the test-suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code with the CUDA library.
+ *
+ * It is deliberately slow and literal: plain loops over tokens and columns,
+ * the steps in the order the pages give them, no blocking and no fusion.
+ * OpenMP splits the independent token rows over host threads; the arithmetic
+ * of one row does not depend on the thread count.
+ *
+ * Precision of each step:
+ *   - GEMM dot products: the pages fix only the output type (BF16 for the
+ *     compression and KV expansion projections), so the oracle forms the
+ *     plain definition -- the sum of exact BF16 x BF16 products -- in float64
+ *     and rounds it once to the output type.
+ *   - RMSNorm: FP32 throughout, as the pages fix it ("PyPTO-Gym 算子设计模式
+ *     AT-10", section 三, variant B: x^2, times 1/L, sum, + eps, sqrt, 1/std,
+ *     x * rstd), then * gamma in FP32 and a cast to BF16 (section 五).
+ *   - RoPE: FP32 rotate-half, out = x*cos + rotate_half(x)*sin, with
+ *     rotate_half(x1, x2) = (-x2, x1) (DeepSeek-V3.2-Exp PyPTO article,
+ *     section 3.3 QuantRope; V2-Lite migration guide, section "精度验证").
+ *   - Per-token INT8 quant: FP32 chain amax = max|y|, inv = 127/amax,
+ *     code = rint(y * inv) (round half to even), clamp to +-127,
+ *     scale = amax / 127 (DeepSeek-V3.2-Exp PyPTO article, section 3.1
+ *     PrologQuant; grouped_matmul_swiglu_quant article, sections "数学公式" and
+ *     "5. 量化流水线的数值细节").
+ *
+ * Readings where the pages are silent (also listed in the design notes):
+ *   - a zero row (amax == 0) yields codes 0 and scale 0;
+ *   - a position outside [0, max_pos) zero-fills every output of that token
+ *     and is reported in the return value;
+ *   - q is kept in FP32 after its projection and RoPE; the quant reads FP32.
+ *
+ * Build: cc -O2 -ffp-contract=off -fopenmp -fPIC -shared (no -ffast-math),
+ * so every FP32 operation below is one IEEE-754 operation, rounded to nearest.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_QUANT_Q 1u
+
+typedef struct {
+    int32_t T, D, q_lora_rank, kv_lora_rank, rope_dim, num_heads, nope_dim, v_dim, max_pos;
+    float eps;
+    uint32_t flags;
+} oracle_dims;
+
+/* ---------------------------------------------------------------- BF16 -- */
+
+/* Widen BF16 bits to FP32: the BF16 bits are the upper half of the FP32. */
+static float bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* FP32 -> BF16, round to nearest, ties to even, on the bit pattern. */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) /* NaN: keep it quiet */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* float64 -> BF16 with a single rounding: the value rounded to 8 significant
+ * bits (to nearest, ties to even), or to a multiple of 2^-133 in BF16's
+ * subnormal range. */
+uint16_t oracle_f64_to_bf16(double v) {
+    if (isnan(v)) return 0x7fc0u;
+    if (v == 0.0) return signbit(v) ? 0x8000u : 0x0000u;
+    int e;
+    (void)frexp(v, &e);                 /* v = m * 2^e, 0.5 <= |m| < 1 */
+    int q = e - 8;                      /* quantum exponent for 8 significant bits */
+    if (q < -133) q = -133;             /* BF16 subnormal spacing */
+    double r = nearbyint(ldexp(v, -q)); /* default rounding mode: to nearest even */
+    double w = ldexp(r, q);
+    if (fabs(w) >= 0x1p128) return signbit(v) ? 0xff80u : 0x7f80u; /* overflow to inf */
+    float f = (float)w;                 /* exact: w has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------ steps ----- */
+
+/* One output of a projection with weights in [N, K] layout:
+ * sum_k a[k] * w[n, k] in float64 (each BF16 x BF16 product is exact). */
+static double dot_bf16_f64(const uint16_t* a, const uint16_t* w_row, int K) {
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k)
+        acc += (double)bf16_to_f32(a[k]) * (double)bf16_to_f32(w_row[k]);
+    return acc;
+}
+
+/* Compression projection of one token row, rounded to BF16:
+ * c[n] = bf16( sum_k x[k] * W_a[n, k] ), n in [0, N). */
+void oracle_project_bf16(const uint16_t* x_row, const uint16_t* W, int N, int K, uint16_t* out) {
+    for (int n = 0; n < N; ++n)
+        out[n] = oracle_f64_to_bf16(dot_bf16_f64(x_row, W + (size_t)n * K, K));
+}
+
+/* Expansion projection of one normed row, rounded to FP32. */
+void oracle_project_f32(const uint16_t* a_row, const uint16_t* W, int N, int K, float* out) {
+    for (int n = 0; n < N; ++n)
+        out[n] = (float)dot_bf16_f64(a_row, W + (size_t)n * K, K);
+}
+
+/* RMSNorm of one row of L BF16 values with BF16 gamma, FP32 inside.
+ * y_f32 (optional) receives x * rstd * gamma before the BF16 cast. */
+void oracle_rmsnorm_row(const uint16_t* x, const uint16_t* gamma, int L, float eps,
+                        float* y_f32, uint16_t* y_bf16) {
+    const float inv_L = (float)(1.0 / (double)L);
+    float ms = 0.0f;
+    for (int i = 0; i < L; ++i) {
+        float v = bf16_to_f32(x[i]);
+        float sq = v * v;
+        ms += sq * inv_L;
+    }
+    float var = ms + eps;
+    float stdv = sqrtf(var);
+    float rstd = 1.0f / stdv;
+    for (int i = 0; i < L; ++i) {
+        float y = bf16_to_f32(x[i]) * rstd;
+        y = y * (gamma ? bf16_to_f32(gamma[i]) : 1.0f);
+        if (y_f32) y_f32[i] = y;
+        if (y_bf16) y_bf16[i] = oracle_f32_to_bf16(y);
+    }
+}
+
+/* Rotate-half RoPE of R values in FP32 with the table row (cos | sin):
+ * out[i]       = x[i] * c_i + (-x[i + R/2]) * s_i
+ * out[i + R/2] = x[i + R/2] * c_i + x[i] * s_i,   i < R/2. */
+void oracle_rope_f32(const float* x, const float* cs_row, int R, float* out) {
+    const int h = R / 2;
+    for (int i = 0; i < h; ++i) {
+        float c = cs_row[i], s = cs_row[h + i];
+        float x1 = x[i], x2 = x[h + i];
+        float a = x1 * c;
+        float b = (-x2) * s;
+        float e = x2 * c;
+        float f = x1 * s;
+        out[i] = a + b;
+        out[h + i] = e + f;
+    }
+}
+
+/* Per-token symmetric INT8 quantisation of one FP32 row. */
+void oracle_quant_row(const float* y, int n, int8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(y[i]);
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0f) {
+        for (int i = 0; i < n; ++i) codes[i] = 0;
+        *scale = 0.0f;
+        return;
+    }
+    float inv = 127.0f / amax;
+    for (int i = 0; i < n; ++i) {
+        float v = y[i] * inv;
+        float r = rintf(v); /* round half to even (default rounding mode) */
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        codes[i] = (int8_t)r;
+    }
+    *scale = amax / 127.0f;
+}
+
+/* ------------------------------------------------------------ whole op -- */
+
+/*
+ * Runs the whole prolog for the tokens listed in `tokens` (all T tokens when
+ * `tokens` is NULL, n_tokens then ignored).  Output rows are compact: row j
+ * of every output belongs to token tokens[j].
+ *
+ * Optional taps (NULL to skip), also compact by selected token:
+ *   c_out      BF16 [n, Lq+Lkv+R]  compression output after the BF16 cast
+ *   normed_out BF16 [n, Lq+Lkv]    normed c_q | c_kv after gamma and the cast
+ *   q_out      FP32 [n, H*(Dn+R)]  q after projection and RoPE (the quant input)
+ *
+ * Returns the number of selected tokens whose position was out of range
+ * (their outputs are zero-filled), or -1 on bad arguments.
+ */
+int oracle_mla_prolog(const oracle_dims* d,
+                      const uint16_t* x, const uint16_t* gamma,
+                      const uint16_t* W_a, const uint16_t* W_b,
+                      const int32_t* positions, const float* cos_sin,
+                      const int32_t* tokens, int32_t n_tokens,
+                      uint16_t* out_k, uint16_t* out_v, uint16_t* out_kpe,
+                      int8_t* out_q_int8, float* out_scale,
+                      uint16_t* c_out, uint16_t* normed_out, float* q_out) {
+    if (!d || !x || !W_a || !positions || !cos_sin || !out_k || !out_v || !out_kpe) return -1;
+    const int T = d->T, D = d->D, Lq = d->q_lora_rank, Lkv = d->kv_lora_rank, R = d->rope_dim;
+    const int H = d->num_heads, Dn = d->nope_dim, Dv = d->v_dim;
+    const int NA = Lq + Lkv + R, NQ = H * (Dn + R);
+    const int quant = (d->flags & ORACLE_QUANT_Q) != 0;
+    if (T < 0 || D <= 0 || Lq < 0 || Lkv <= 0 || R <= 0 || (R & 1) || H <= 0 || Dn < 0 || Dv < 0)
+        return -1;
+    if ((Lq + Lkv) > 0 && !gamma) return -1;
+    if (Lq > 0 && (!W_b || !quant || !out_q_int8 || !out_scale)) return -1;
+    if (!W_b) return -1;
+    const int n = tokens ? n_tokens : T;
+    if (n < 0) return -1;
+    const uint16_t* W_qb = W_b;                          /* [NQ, Lq]  */
+    const uint16_t* W_kvb = W_b + (size_t)NQ * Lq;       /* [NKV, Lkv] */
+    int bad = 0;
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+    for (int j = 0; j < n; ++j) {
+        const int t = tokens ? tokens[j] : j;
+        uint16_t* ok = out_k + (size_t)j * H * (Dn + R);
+        uint16_t* ov = out_v + (size_t)j * H * Dv;
+        uint16_t* okpe = out_kpe + (size_t)j * R;
+        if (t < 0 || t >= T) { bad += 1; continue; }
+        const int32_t pos = positions[t];
+        if (pos < 0 || pos >= d->max_pos) {
+            memset(ok, 0, sizeof(uint16_t) * (size_t)H * (Dn + R));
+            memset(ov, 0, sizeof(uint16_t) * (size_t)H * Dv);
+            memset(okpe, 0, sizeof(uint16_t) * (size_t)R);
+            if (Lq > 0) {
+                memset(out_q_int8 + (size_t)j * NQ, 0, (size_t)NQ);
+                out_scale[j] = 0.0f;
+            }
+            if (c_out) memset(c_out + (size_t)j * NA, 0, sizeof(uint16_t) * (size_t)NA);
+            if (normed_out) memset(normed_out + (size_t)j * (Lq + Lkv), 0, sizeof(uint16_t) * (size_t)(Lq + Lkv));
+            if (q_out) memset(q_out + (size_t)j * NQ, 0, sizeof(float) * (size_t)NQ);
+            bad += 1;
+            continue;
+        }
+        const float* cs = cos_sin + (size_t)pos * R;
+        uint16_t* c = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)NA);
+        uint16_t* nrm = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(Lq + Lkv));
+        float* kpe_f = (float*)malloc(sizeof(float) * (size_t)R);
+        float* kpe_r = (float*)malloc(sizeof(float) * (size_t)R);
+
+        /* Step 1: compression projection x . W_a^T, each output rounded to BF16. */
+        oracle_project_bf16(x + (size_t)t * D, W_a, NA, D, c);
+        /* Step 2: split -- c_q = c[0, Lq), c_kv = c[Lq, Lq+Lkv), k_pe = c[Lq+Lkv, NA). */
+        /* Step 3: RMSNorm of c_q and c_kv with their gammas, then BF16. */
+        if (Lq > 0) oracle_rmsnorm_row(c, gamma, Lq, d->eps, NULL, nrm);
+        oracle_rmsnorm_row(c + Lq, gamma + Lq, Lkv, d->eps, NULL, nrm + Lq);
+        /* Step 4 (k_pe RoPE): rotate-half in FP32 with this token's table row. */
+        for (int i = 0; i < R; ++i) kpe_f[i] = bf16_to_f32(c[Lq + Lkv + i]);
+        oracle_rope_f32(kpe_f, cs, R, kpe_r);
+        for (int i = 0; i < R; ++i) okpe[i] = oracle_f32_to_bf16(kpe_r[i]);
+        /* Steps 5-7: KV expansion, split per head into k_nope | value, assemble
+         * K = [k_nope | k_pe_rot] with the rotated k_pe shared by every head. */
+        for (int h = 0; h < H; ++h) {
+            const uint16_t* Wh = W_kvb + (size_t)h * (Dn + Dv) * Lkv;
+            for (int i = 0; i < Dn; ++i)
+                ok[(size_t)h * (Dn + R) + i] = oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)i * Lkv, Lkv));
+            for (int i = 0; i < Dv; ++i)
+                ov[(size_t)h * Dv + i] = oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)(Dn + i) * Lkv, Lkv));
+            for (int i = 0; i < R; ++i) ok[(size_t)h * (Dn + R) + Dn + i] = okpe[i];
+        }
+        /* q path: expansion, RoPE on each head's rope slice, per-token quant. */
+        if (Lq > 0) {
+            float* q = (float*)malloc(sizeof(float) * (size_t)NQ);
+            oracle_project_f32(nrm, W_qb, NQ, Lq, q);
+            for (int h = 0; h < H; ++h) {
+                float* qr = q + (size_t)h * (Dn + R) + Dn;
+                memcpy(kpe_f, qr, sizeof(float) * (size_t)R);
+                oracle_rope_f32(kpe_f, cs, R, qr);
+            }
+            if (q_out) memcpy(q_out + (size_t)j * NQ, q, sizeof(float) * (size_t)NQ);
+            oracle_quant_row(q, NQ, out_q_int8 + (size_t)j * NQ, out_scale + j);
+            free(q);
+        }
+        if (c_out) memcpy(c_out + (size_t)j * NA, c, sizeof(uint16_t) * (size_t)NA);
+        if (normed_out) memcpy(normed_out + (size_t)j * (Lq + Lkv), nrm, sizeof(uint16_t) * (size_t)(Lq + Lkv));
+        free(c); free(nrm); free(kpe_f); free(kpe_r);
+    }
+    return bad;
+}
+
+/* Threads OpenMP will use for the next parallel region (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
