@@ -1,0 +1,202 @@
+/*
+ * mla_prolog.h -- C ABI of the GB300 (sm_103a) fused MLA attention prolog.
+ *
+ * The prolog turns the hidden states of T tokens into the per-head K and V
+ * of Multi-head Latent Attention (and, optionally, an INT8 per-token q):
+ *
+ *   1. compression projection  C = x . W_a^T, rounded to BF16
+ *      (DeepSeek-V2-Lite-Chat MLA KV Prolog migration guide, section 背景,
+ *       step "kv_a_proj"; PyPTO-Gym AT-10 article, section 五, q_a_proj);
+ *   2. split C into c_q | c_kv | k_pe (migration guide, step "split");
+ *   3. RMSNorm of c_q and c_kv in FP32 with gamma, cast to BF16
+ *      (AT-10 article, sections 二 and 三, variant B);
+ *   4. rotate-half RoPE of k_pe with the token's row of the cos/sin table
+ *      (migration guide, step "RoPE" and section 精度验证; DeepSeek-V3.2-Exp
+ *       PyPTO article, section 3.3);
+ *   5. KV expansion projection of the normed c_kv (migration guide, "kv_b_proj");
+ *   6. reshape to [T, H, Dn + Dv], split into k_nope | value, and assemble
+ *      K = [k_nope | k_pe_rot] per head (migration guide, "reshape split" and
+ *      "assemble");
+ *   7. q path (when q_lora_rank > 0): q expansion of the normed c_q, RoPE on
+ *      each head's rope slice, then per-token symmetric INT8 quantisation:
+ *      amax = max|q_row|, code = clamp(rint_half_even(q * (127/amax)), +-127),
+ *      scale = amax/127 (DeepSeek-V3.2-Exp PyPTO article, section 3.1
+ *      PrologQuant; grouped_matmul_swiglu_quant article, section 数学公式).
+ *
+ * Notation: T tokens, D hidden size, Lq = q_lora_rank (0: no q path),
+ * Lkv = kv_lora_rank, R = rope_dim, H = num_heads, Dn = nope_dim, Dv = v_dim.
+ *
+ * Conventions for every call below
+ *   - Tensor arguments are DEVICE pointers on the handle's device, owned by
+ *     the caller, contiguous row-major, and 16-byte aligned (positions:
+ *     4-byte aligned).  BF16 tensors are passed as raw 16-bit storage.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return without synchronising, except
+ *     where a call says it synchronises.
+ *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  A failed call
+ *     enqueues nothing.  Faults found on the device (a position outside the
+ *     table, a wait that ran out) never trap: they set bits of the handle's
+ *     device status word, read with mla_prolog_device_status().
+ */
+#ifndef MLA_PROLOG_H_
+#define MLA_PROLOG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define MLA_OK                    0
+#define MLA_ERR_INVALID_ARG      -1  /* null / misaligned pointer, bad flag combination   */
+#define MLA_ERR_UNSUPPORTED_DIMS -2  /* a size rule below is broken                        */
+#define MLA_ERR_CUDA             -3  /* a CUDA runtime call or launch failed               */
+#define MLA_ERR_OOM              -4  /* workspace allocation failed                        */
+#define MLA_ERR_DEVICE           -5  /* current device is not an sm_103 (GB300) GPU       */
+
+/* ---- device status bits (mla_prolog_device_status) --------------------- */
+#define MLA_STATUS_POSITION_RANGE 0x1 /* some positions[t] was outside [0, max_pos): that
+                                         token's outputs were zero-filled                  */
+#define MLA_STATUS_WAIT_TIMEOUT   0x2 /* a bounded in-kernel wait gave up; outputs of the
+                                         affected tile are undefined                       */
+
+/* ---- dims flags --------------------------------------------------------- */
+#define MLA_PROLOG_QUANT_Q 0x1u /* q path emits INT8 codes + FP32 per-token scales.
+                                   Required exactly when q_lora_rank > 0.               */
+
+/*
+ * Problem sizes, fixed for the life of a handle.
+ * Size rules (else MLA_ERR_UNSUPPORTED_DIMS):
+ *   D, Lkv, R, Dn, Dv  positive multiples of 16;  Lq = 0 or a multiple of 16;
+ *   R <= 128;  Dn + R <= 256 when Lq > 0;  T >= 0;  H >= 1;  max_pos >= 1;
+ *   eps finite and >= 0.
+ */
+typedef struct mla_prolog_dims {
+    int32_t  T;            /* tokens per run (rows of x)                         */
+    int32_t  D;            /* hidden size                                        */
+    int32_t  q_lora_rank;  /* Lq; 0 = KV prolog only                             */
+    int32_t  kv_lora_rank; /* Lkv                                                */
+    int32_t  rope_dim;     /* R                                                  */
+    int32_t  num_heads;    /* H                                                  */
+    int32_t  nope_dim;     /* Dn                                                 */
+    int32_t  v_dim;        /* Dv                                                 */
+    int32_t  max_pos;      /* rows of the cos/sin table                          */
+    float    eps;          /* RMSNorm epsilon (1e-6 in the DeepSeek shapes)      */
+    uint32_t flags;        /* MLA_PROLOG_QUANT_Q                                 */
+} mla_prolog_dims;
+
+typedef struct mla_prolog* mla_prolog_t;
+
+/*
+ * Creates a handle for the CURRENT CUDA device: validates dims, picks the
+ * decode (small T) or prefill schedule, and allocates the handle's device
+ * workspace (split-K partials, the normed c_q | c_kv rows, the FP32 q rows,
+ * per-token amax, the status word).  *out receives the handle.
+ * Errors: INVALID_ARG (null pointers), UNSUPPORTED_DIMS, DEVICE, OOM, CUDA.
+ */
+int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out);
+
+/*
+ * Enqueues one prolog pass over T tokens on `stream`.
+ *
+ * Inputs (device, read only):
+ *   x          BF16 [T, D]
+ *   gamma      BF16 [Lq + Lkv]              = [gamma_q ; gamma_kv]
+ *   W_a        BF16 [Lq + Lkv + R, D]       = rows [W_q_a ; W_kv_a], W_kv_a rows
+ *                                             ordered [c_kv (Lkv) ; k_pe (R)]
+ *   W_b        BF16, W_q_b [H(Dn+R), Lq] followed by W_kv_b [H(Dn+Dv), Lkv]
+ *              (both [N, K] row-major; W_q_b empty when Lq = 0)
+ *   positions  int32 [T], each in [0, max_pos)
+ *   cos_sin    FP32 [max_pos, R]: columns [0, R/2) = cos(p * theta_i),
+ *              [R/2, R) = sin(p * theta_i)
+ * Outputs (device, written in full):
+ *   out_k      BF16 [T, H, Dn + R]  = [k_nope | k_pe_rot] per head
+ *   out_v      BF16 [T, H, Dv]
+ *   out_kpe    BF16 [T, R]          rotated k_pe (shared by every head)
+ *   out_q_int8 int8 [T, H, Dn + R]  q codes (NULL iff Lq == 0)
+ *   out_scale  FP32 [T]             per-token q scale (NULL iff Lq == 0)
+ * One run at a time per handle (the workspace is shared): use one handle per
+ * concurrent stream.  Inputs and outputs must not overlap.
+ * Errors: INVALID_ARG, CUDA.
+ */
+int mla_prolog_run(mla_prolog_t h,
+                   const void* x, const void* gamma, const void* W_a, const void* W_b,
+                   const int32_t* positions, const float* cos_sin,
+                   void* out_k, void* out_v, void* out_kpe,
+                   int8_t* out_q_int8, float* out_scale,
+                   void* stream);
+
+/* Frees the workspace and the handle.  NULL-safe.  Synchronises the device. */
+int mla_prolog_destroy(mla_prolog_t h);
+
+/*
+ * Synchronises `stream`, copies the handle's device status word (an OR of
+ * MLA_STATUS_* bits accumulated since the last call) into *status, and clears
+ * it.  Errors: INVALID_ARG, CUDA.
+ */
+int mla_prolog_device_status(mla_prolog_t h, void* stream, int32_t* status);
+
+/* Static English text for a return code (never NULL). */
+const char* mla_prolog_strerror(int code);
+
+/* Text of the last CUDA error seen by this library in the calling thread ("" if none). */
+const char* mla_prolog_last_cuda_error(void);
+
+/*
+ * Per-token symmetric INT8 quantisation of `rows` FP32 rows of `row_len`
+ * values (device): codes int8 [rows, row_len], scale FP32 [rows].  The same
+ * quantisation step the q path of mla_prolog_run() ends with (DeepSeek-V3.2-Exp
+ * PyPTO article, section 3.1 PrologQuant): amax = max|y|, inv = 127/amax,
+ * code = clamp(rint_half_even(y * inv), +-127), scale = amax/127; a zero row
+ * gives codes 0 and scale 0.  Every FP32 operation is correctly rounded, so
+ * the result is bit-exact for a given input.  `y` 16-byte aligned, codes
+ * 4-byte aligned.  Errors: INVALID_ARG (row_len not a multiple of 4, bad
+ * pointers), CUDA.
+ */
+int mla_prolog_quant_rows(const float* y, int32_t rows, int32_t row_len,
+                          int8_t* codes, float* scale, void* stream);
+
+/*
+ * Sets the limit, in nanoseconds, after which an in-kernel wait of this
+ * handle gives up (default 1e9 = 1 s).  A wait that gives up sets
+ * MLA_STATUS_WAIT_TIMEOUT and lets its CTA finish cleanly.
+ */
+int mla_prolog_set_wait_timeout(mla_prolog_t h, uint64_t timeout_ns);
+
+/*
+ * Self-test of the bounded-wait path: launches one CTA that waits on a
+ * barrier phase that nothing completes, for at most `timeout_ns`.  Expected
+ * result: MLA_STATUS_WAIT_TIMEOUT in the handle's status word, a clean return
+ * and a usable context.  No fault, trap or hang is involved.
+ */
+int mla_prolog_selftest_wait_timeout(mla_prolog_t h, uint64_t timeout_ns, void* stream);
+
+/*
+ * Profiling hook.  With n_events >= mla_prolog_kernel_count(h) + 1 CUDA
+ * events (cudaEvent_t passed as void*), each later run records events[0]
+ * before its first kernel and events[i + 1] after its kernel i, on the run's
+ * stream; n_events = 0 turns the hook off.  Events stay owned by the caller.
+ */
+int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_events);
+
+/* Number of kernels one run launches, and the name of kernel i. */
+int32_t mla_prolog_kernel_count(mla_prolog_t h);
+const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i);
+
+/* Bytes of device workspace the handle holds. */
+int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes);
+
+/*
+ * Schedule chosen at create time, for reports: tile widths and split-K of the
+ * two projections.  Any pointer may be NULL.
+ */
+int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a,
+                        int32_t* bn_kv, int32_t* bn_q);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_PROLOG_H_ */

@@ -1,0 +1,426 @@
+// Host side of the C ABI declared in include/mla_prolog.h: argument checks,
+// the schedule chosen at create time, the device workspace, TMA tensor maps,
+// and the kernel launches of one run.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/mla_prolog.h"
+#include "prolog.cuh"
+
+using namespace mlap;
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", where, cudaGetErrorString(e));
+    return e == cudaErrorMemoryAllocation ? MLA_ERR_OOM : MLA_ERR_CUDA;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// K-major BF16 operand [rows, cols] with row stride `stride_elems`, loaded as
+// boxes of 64 columns (one 128-byte swizzle atom) x box_rows rows.  Reads
+// outside [rows, cols] are filled with zeros.
+bool encode_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t stride_elems,
+                 uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {stride_elems * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+constexpr int kKernelCount = 4;
+const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
+                                                "mla_expand_kernel", "mla_quant_kernel"};
+
+}  // namespace
+
+struct mla_prolog {
+    mla_prolog_dims d{};
+    int device = 0;
+    int NA = 0, NQ = 0, NKV = 0;
+    // schedule
+    bool decode = false;
+    GemmShape shape_a = GemmShape::Wide, shape_b = GemmShape::Wide;
+    int bn_a = 0, splits_a = 1, bn_kv = 0, m_tiles = 0;
+    // workspace
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    float* partials = nullptr;
+    uint16_t* normed = nullptr;
+    float* qws = nullptr;
+    uint32_t* amax = nullptr;
+    int* status = nullptr;
+    uint64_t timeout_ns = 1000000000ull;
+    // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
+    CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wqb{}, tm_wkvb{};
+    const void* last_x = nullptr;
+    const void* last_wa = nullptr;
+    const void* last_wb = nullptr;
+    cudaEvent_t events[kKernelCount + 1] = {};
+    int n_events = 0;
+};
+
+namespace {
+
+int check_dims(const mla_prolog_dims& d) {
+    auto m16 = [](int v) { return v > 0 && v % 16 == 0; };
+    if (!m16(d.D) || !m16(d.kv_lora_rank) || !m16(d.rope_dim) || !m16(d.nope_dim) || !m16(d.v_dim))
+        return MLA_ERR_UNSUPPORTED_DIMS;
+    if (d.q_lora_rank < 0 || d.q_lora_rank % 16) return MLA_ERR_UNSUPPORTED_DIMS;
+    if (d.rope_dim > 128 || d.T < 0 || d.num_heads < 1 || d.max_pos < 1) return MLA_ERR_UNSUPPORTED_DIMS;
+    if (!std::isfinite(d.eps) || d.eps < 0.0f) return MLA_ERR_UNSUPPORTED_DIMS;
+    const bool quant = (d.flags & MLA_PROLOG_QUANT_Q) != 0;
+    if ((d.flags & ~MLA_PROLOG_QUANT_Q) != 0) return MLA_ERR_INVALID_ARG;
+    if (quant != (d.q_lora_rank > 0)) return MLA_ERR_INVALID_ARG;
+    if (d.q_lora_rank > 0 && d.nope_dim + d.rope_dim > 256) return MLA_ERR_UNSUPPORTED_DIMS;
+    // 32-bit index headroom of the kernels' row arithmetic
+    const double big = static_cast<double>(d.T) * d.num_heads * (d.nope_dim + d.rope_dim + d.v_dim);
+    if (big > 4.0e9 || static_cast<double>(d.T) * d.D > 4.0e9) return MLA_ERR_UNSUPPORTED_DIMS;
+    return MLA_OK;
+}
+
+// Largest width in [lo, 256] (step 16) dividing n, else 256 with a ragged tail.
+int pick_wide_bn(int n, int lo) {
+    for (int bn = 256; bn >= lo; bn -= 16)
+        if (n % bn == 0) return bn;
+    return 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_prolog_strerror(int code) {
+    switch (code) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, or bad flags)";
+        case MLA_ERR_UNSUPPORTED_DIMS: return "unsupported dims (see the size rules of mla_prolog_dims)";
+        case MLA_ERR_CUDA: return "CUDA error (see mla_prolog_last_cuda_error)";
+        case MLA_ERR_OOM: return "device memory allocation failed";
+        case MLA_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        default: return "unknown error code";
+    }
+}
+
+const char* mla_prolog_last_cuda_error(void) { return g_last_cuda_error; }
+
+int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
+    if (!dims || !out) return MLA_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = check_dims(*dims);
+    if (rc != MLA_OK) return rc;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3) return MLA_ERR_DEVICE;
+    if (!encode_fn()) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
+    if ((e = gemm_set_attributes()) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+
+    mla_prolog* h = new (std::nothrow) mla_prolog();
+    if (!h) return MLA_ERR_OOM;
+    h->d = *dims;
+    h->device = dev;
+    const mla_prolog_dims& d = h->d;
+    const int Lq = d.q_lora_rank, Lkv = d.kv_lora_rank, R = d.rope_dim;
+    h->NA = Lq + Lkv + R;
+    h->NQ = d.num_heads * (d.nope_dim + R);
+    h->NKV = d.num_heads * (d.nope_dim + d.v_dim);
+    h->m_tiles = cdiv(d.T, kBM);
+    const int sms = prop.multiProcessorCount;
+
+    // Schedule: few token tiles -> decode (weights streamed by many narrow or
+    // split-K tiles); otherwise prefill (wide tiles, tensor-core bound).
+    h->decode = h->m_tiles <= 2;
+    const int kb_a = cdiv(d.D, kBK);
+    if (h->decode) {
+        h->shape_a = GemmShape::Narrow;
+        h->bn_a = 64;
+        const int tiles = cdiv(h->NA, h->bn_a) * h->m_tiles;
+        int s = sms / (tiles > 0 ? tiles : 1);
+        if (s < 1) s = 1;
+        if (s > kb_a / 2) s = kb_a / 2 > 0 ? kb_a / 2 : 1;
+        h->splits_a = s;
+    } else {
+        h->shape_a = GemmShape::Wide;
+        h->bn_a = pick_wide_bn(h->NA, 128);
+        h->splits_a = 1;
+    }
+    // Expansion: prefill uses 256-wide kv tiles (one head of V2/V3); decode
+    // without a q path uses the narrow kernel with enough tiles to cover the
+    // SMs; decode with a q path shares the wide kernel with the q heads.
+    if (!h->decode) {
+        h->shape_b = GemmShape::Wide;
+        h->bn_kv = 256;
+    } else if (Lq == 0) {
+        h->shape_b = GemmShape::Narrow;
+        h->bn_kv = cdiv(h->NKV, 64) * h->m_tiles >= sms ? 64 : 32;
+    } else {
+        h->shape_b = GemmShape::Wide;
+        h->bn_kv = 128;
+    }
+
+    // Workspace: partials | normed | q | amax | status, each 256-byte aligned.
+    auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    const size_t T = static_cast<size_t>(d.T);
+    const size_t b_part = al(static_cast<size_t>(h->splits_a) * T * h->NA * 4);
+    const size_t b_norm = al(T * (Lq + Lkv) * 2);
+    const size_t b_q = Lq > 0 ? al(T * h->NQ * 4) : 0;
+    const size_t b_amax = al(T * 4);
+    const size_t b_stat = 256;
+    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat;
+    if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
+        delete h;
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    }
+    char* w = static_cast<char*>(h->ws);
+    h->partials = reinterpret_cast<float*>(w);
+    h->normed = reinterpret_cast<uint16_t*>(w + b_part);
+    h->qws = Lq > 0 ? reinterpret_cast<float*>(w + b_part + b_norm) : nullptr;
+    h->amax = reinterpret_cast<uint32_t*>(w + b_part + b_norm + b_q);
+    h->status = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax);
+    if ((e = cudaMemset(h->ws, 0, h->ws_bytes)) != cudaSuccess) {
+        cudaFree(h->ws);
+        delete h;
+        return cuda_fail(e, "cudaMemset(workspace)");
+    }
+    const uint64_t Tm = d.T > 0 ? static_cast<uint64_t>(d.T) : 1;
+    bool ok = encode_bf16(&h->tm_nkv, h->normed + Lq, Lkv, Tm, Lq + Lkv, kBM);
+    if (Lq > 0) ok = ok && encode_bf16(&h->tm_nq, h->normed, Lq, Tm, Lq + Lkv, kBM);
+    else h->tm_nq = h->tm_nkv;
+    if (!ok) {
+        cudaFree(h->ws);
+        delete h;
+        return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(workspace)");
+    }
+    *out = h;
+    return MLA_OK;
+}
+
+int mla_prolog_destroy(mla_prolog_t h) {
+    if (!h) return MLA_OK;
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != h->device) cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    if (h->ws) cudaFree(h->ws);
+    if (dev >= 0 && dev != h->device) cudaSetDevice(dev);
+    delete h;
+    return MLA_OK;
+}
+
+int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, const void* W_b,
+                   const int32_t* positions, const float* cos_sin, void* out_k, void* out_v, void* out_kpe,
+                   int8_t* out_q_int8, float* out_scale, void* stream) {
+    if (!h) return MLA_ERR_INVALID_ARG;
+    const mla_prolog_dims& d = h->d;
+    const int Lq = d.q_lora_rank, Lkv = d.kv_lora_rank, R = d.rope_dim;
+    if (d.T == 0) return MLA_OK;
+    const void* p16[] = {x, gamma, W_a, W_b, cos_sin, out_k, out_v, out_kpe};
+    for (const void* p : p16)
+        if (!p || !aligned(p, 16)) return MLA_ERR_INVALID_ARG;
+    if (!positions || !aligned(positions, 4)) return MLA_ERR_INVALID_ARG;
+    if (Lq > 0) {
+        if (!out_q_int8 || !out_scale || !aligned(out_q_int8, 16) || !aligned(out_scale, 4))
+            return MLA_ERR_INVALID_ARG;
+    } else if (out_q_int8 || out_scale) {
+        return MLA_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const uint16_t* wb = static_cast<const uint16_t*>(W_b);
+    if (x != h->last_x) {
+        if (!encode_bf16(&h->tm_x, x, d.D, d.T, d.D, kBM)) return cuda_fail(cudaErrorInvalidValue, "tensor map x");
+        h->last_x = x;
+    }
+    if (W_a != h->last_wa) {
+        if (!encode_bf16(&h->tm_wa, W_a, d.D, h->NA, d.D, h->bn_a))
+            return cuda_fail(cudaErrorInvalidValue, "tensor map W_a");
+        h->last_wa = W_a;
+    }
+    if (W_b != h->last_wb) {
+        const uint16_t* wkvb = wb + static_cast<size_t>(h->NQ) * Lq;
+        if (!encode_bf16(&h->tm_wkvb, wkvb, Lkv, h->NKV, Lkv, h->bn_kv))
+            return cuda_fail(cudaErrorInvalidValue, "tensor map W_kv_b");
+        if (Lq > 0) {
+            if (!encode_bf16(&h->tm_wqb, wb, Lq, h->NQ, Lq, d.nope_dim + R))
+                return cuda_fail(cudaErrorInvalidValue, "tensor map W_q_b");
+        } else {
+            h->tm_wqb = h->tm_wkvb;
+        }
+        h->last_wb = W_b;
+    }
+    const bool timed = h->n_events > 0;
+    cudaError_t e;
+    auto mark = [&](int i) {
+        if (timed) cudaEventRecord(h->events[i], st);
+    };
+
+    mark(0);
+    CompressParams pa{h->partials, d.T, h->NA, h->bn_a, cdiv(d.D, kBK), h->splits_a, h->status, h->timeout_ns};
+    dim3 ga(cdiv(h->NA, h->bn_a), h->m_tiles, h->splits_a);
+    if ((e = launch_compress(h->shape_a, ga, h->tm_x, h->tm_wa, pa, st)) != cudaSuccess)
+        return cuda_fail(e, "launch mla_compress_kernel");
+    mark(1);
+
+    NormRopeParams pn{};
+    pn.partials = h->partials;
+    pn.splits = h->splits_a;
+    pn.T = d.T;
+    pn.NA = h->NA;
+    pn.Lq = Lq;
+    pn.Lkv = Lkv;
+    pn.R = R;
+    pn.H = d.num_heads;
+    pn.Dn = d.nope_dim;
+    pn.inv_lq = Lq > 0 ? static_cast<float>(1.0 / Lq) : 0.0f;
+    pn.inv_lkv = static_cast<float>(1.0 / Lkv);
+    pn.eps = d.eps;
+    pn.gamma = static_cast<const uint16_t*>(gamma);
+    pn.positions = positions;
+    pn.cos_sin = cos_sin;
+    pn.max_pos = d.max_pos;
+    pn.normed = h->normed;
+    pn.out_k = static_cast<uint16_t*>(out_k);
+    pn.out_kpe = static_cast<uint16_t*>(out_kpe);
+    pn.amax = Lq > 0 ? h->amax : nullptr;
+    pn.status = h->status;
+    if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
+    mark(2);
+
+    ExpandParams pb{};
+    pb.T = d.T;
+    pb.H = d.num_heads;
+    pb.Dn = d.nope_dim;
+    pb.Dv = d.v_dim;
+    pb.R = R;
+    pb.NQ = h->NQ;
+    pb.NKV = h->NKV;
+    pb.nq_tiles = Lq > 0 ? d.num_heads : 0;
+    pb.bn_kv = h->bn_kv;
+    pb.kb_q = cdiv(Lq, kBK);
+    pb.kb_kv = cdiv(Lkv, kBK);
+    pb.positions = positions;
+    pb.cos_sin = cos_sin;
+    pb.max_pos = d.max_pos;
+    pb.out_k = static_cast<uint16_t*>(out_k);
+    pb.out_v = static_cast<uint16_t*>(out_v);
+    pb.qws = h->qws;
+    pb.amax = h->amax;
+    pb.status = h->status;
+    pb.timeout_ns = h->timeout_ns;
+    dim3 gb(pb.nq_tiles + cdiv(h->NKV, h->bn_kv), h->m_tiles);
+    if ((e = launch_expand(h->shape_b, gb, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb, st)) != cudaSuccess)
+        return cuda_fail(e, "launch mla_expand_kernel");
+    mark(3);
+
+    if (Lq > 0) {
+        QuantParams pq{h->qws, h->amax, d.T, h->NQ, out_q_int8, out_scale};
+        if ((e = launch_quant(pq, st)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
+    }
+    mark(4);
+    return MLA_OK;
+}
+
+int mla_prolog_device_status(mla_prolog_t h, void* stream, int32_t* status) {
+    if (!h || !status) return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    int v = 0;
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if ((e = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(status)");
+    if ((e = cudaMemset(h->status, 0, sizeof v)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    *status = v;
+    return MLA_OK;
+}
+
+int mla_prolog_quant_rows(const float* y, int32_t rows, int32_t row_len, int8_t* codes, float* scale,
+                          void* stream) {
+    if (rows < 0 || row_len <= 0 || row_len % 4) return MLA_ERR_INVALID_ARG;
+    if (rows == 0) return MLA_OK;
+    if (!y || !codes || !scale || !aligned(y, 16) || !aligned(codes, 4) || !aligned(scale, 4))
+        return MLA_ERR_INVALID_ARG;
+    QuantParams p{y, nullptr, rows, row_len, codes, scale};
+    cudaError_t e = launch_quant(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "launch mla_quant_kernel");
+}
+
+int mla_prolog_set_wait_timeout(mla_prolog_t h, uint64_t timeout_ns) {
+    if (!h || timeout_ns == 0) return MLA_ERR_INVALID_ARG;
+    h->timeout_ns = timeout_ns;
+    return MLA_OK;
+}
+
+int mla_prolog_selftest_wait_timeout(mla_prolog_t h, uint64_t timeout_ns, void* stream) {
+    if (!h || timeout_ns == 0 || timeout_ns > 10000000000ull) return MLA_ERR_INVALID_ARG;
+    cudaError_t e = launch_wait_selftest(h->status, timeout_ns, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "launch mla_wait_selftest_kernel");
+}
+
+int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_events) {
+    if (!h || n_events < 0) return MLA_ERR_INVALID_ARG;
+    if (n_events == 0) {
+        h->n_events = 0;
+        return MLA_OK;
+    }
+    if (!events || n_events < kKernelCount + 1) return MLA_ERR_INVALID_ARG;
+    for (int i = 0; i <= kKernelCount; ++i) {
+        if (!events[i]) return MLA_ERR_INVALID_ARG;
+        h->events[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    h->n_events = kKernelCount + 1;
+    return MLA_OK;
+}
+
+int32_t mla_prolog_kernel_count(mla_prolog_t h) { return h ? kKernelCount : 0; }
+
+const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
+    if (!h || i < 0 || i >= kKernelCount) return "";
+    return kKernelNames[i];
+}
+
+int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes) {
+    if (!h || !bytes) return MLA_ERR_INVALID_ARG;
+    *bytes = h->ws_bytes;
+    return MLA_OK;
+}
+
+int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a, int32_t* bn_kv, int32_t* bn_q) {
+    if (!h) return MLA_ERR_INVALID_ARG;
+    if (bn_a) *bn_a = h->bn_a;
+    if (splits_a) *splits_a = h->splits_a;
+    if (bn_kv) *bn_kv = h->bn_kv;
+    if (bn_q) *bn_q = h->d.q_lora_rank > 0 ? h->d.nope_dim + h->d.rope_dim : 0;
+    return MLA_OK;
+}
+
+}  // extern "C"

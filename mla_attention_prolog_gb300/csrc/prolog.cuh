@@ -1,0 +1,87 @@
+// Kernel parameter blocks and host-side launchers of the prolog kernels.
+// Included by the kernel translation units and by the C-ABI host code.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mlap {
+
+constexpr int kStatusPositionRange = 0x1;
+constexpr int kStatusWaitTimeout = 0x2;
+
+constexpr int kBM = 128;  // MMA M: token rows per tile (one TMEM lane per row)
+constexpr int kBK = 64;   // K per pipeline stage: one 128-byte swizzle atom of BF16
+
+// Compression projection: partial[split][t][n] = sum over the split's K range
+// of x[t, k] * W_a[n, k]  (FP32, one split per blockIdx.z).
+struct CompressParams {
+    float* partials;  // [splits][T][NA]
+    int T, NA;
+    int bn;        // tile width over the NA weight rows
+    int kb_total;  // K blocks of 64 over D
+    int splits;    // split-K factor
+    int* status;
+    uint64_t timeout_ns;
+};
+
+// Per-token reduction of the partials, BF16 cast, RMSNorm of c_q and c_kv,
+// RoPE of k_pe; writes the normed rows, out_kpe and the rope slice of out_k.
+struct NormRopeParams {
+    const float* partials;  // [splits][T][NA]
+    int splits, T, NA, Lq, Lkv, R, H, Dn;
+    float inv_lq, inv_lkv, eps;
+    const uint16_t* gamma;  // [Lq + Lkv]
+    const int32_t* positions;
+    const float* cos_sin;
+    int max_pos;
+    uint16_t* normed;   // [T][Lq + Lkv]
+    uint16_t* out_k;    // [T][H][Dn + R]
+    uint16_t* out_kpe;  // [T][R]
+    uint32_t* amax;     // [T] (cleared here when the q path is on)
+    int* status;
+};
+
+// Expansion projections.  Tiles [0, nq_tiles) are q heads (one head of
+// Dn + R columns each), the rest are kv tiles of bn_kv columns.
+struct ExpandParams {
+    int T, H, Dn, Dv, R;
+    int NQ, NKV;
+    int nq_tiles, bn_kv;
+    int kb_q, kb_kv;
+    const int32_t* positions;
+    const float* cos_sin;
+    int max_pos;
+    uint16_t* out_k;  // [T][H][Dn + R]
+    uint16_t* out_v;  // [T][H][Dv]
+    float* qws;       // [T][NQ] FP32 q after RoPE
+    uint32_t* amax;   // [T] bits of max |q| per token
+    int* status;
+    uint64_t timeout_ns;
+};
+
+struct QuantParams {
+    const float* y;          // [rows][row_len]
+    const uint32_t* amax;    // [rows] bits of max|y| (null: the kernel finds it)
+    int rows, row_len;
+    int8_t* codes;
+    float* scale;
+};
+
+// Shapes of the GEMM kernel instantiations.
+enum class GemmShape { Wide, Narrow };  // Wide: BN_MAX 256, 4 stages; Narrow: BN_MAX 64, 8 stages
+int gemm_smem_bytes(GemmShape s);
+constexpr int kGemmThreads = 192;
+
+cudaError_t gemm_set_attributes();
+cudaError_t launch_compress(GemmShape s, dim3 grid, const CUtensorMap& tm_x,
+                            const CUtensorMap& tm_wa, const CompressParams& p, cudaStream_t st);
+cudaError_t launch_expand(GemmShape s, dim3 grid, const CUtensorMap& tm_aq,
+                          const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
+                          const CUtensorMap& tm_bkv, const ExpandParams& p, cudaStream_t st);
+cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
+cudaError_t launch_quant(const QuantParams& p, cudaStream_t st);
+cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
+
+}  // namespace mlap
