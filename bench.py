@@ -1,0 +1,453 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MLA attention prolog on GB300.
+
+One step = one pass of the whole prolog (compression projection, split,
+RMSNorm, RoPE, expansion projection, split/assemble, and the q path + INT8
+quant when the workload has one) over one batch of T tokens.
+
+Default workload: the DeepSeek-V2-Lite-shaped KV prolog decode (T=64).
+Other workloads: --workload {tiny,v2lite_decode,v2lite_prefill,v3_decode,v3_prefill}.
+
+Timing: K steps are captured into one CUDA graph, each step on its own
+buffer set (inputs, weights and outputs), with enough sets that the sets
+together exceed 3x the L2 size; the graph is replayed between CUDA events on
+the launching stream after W warm-up replays.  Per-kernel durations come from
+a second graph of the same K steps with the library's timing hook on.
+`e2e` is the same metric through the public call with host buffers: each
+step copies x and positions from pinned host memory, runs, and copies every
+output back, all inside the timed region.
+Under torchrun each rank runs its own replica of the workload (no collective
+on the data path); value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mla_attention_prolog_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MLA prolog tokens/s on 1 GB300; % HBM roofline (decode) / % BF16 TC peak (prefill)"
+L2_BYTES = 126 * 1024 * 1024
+DEFAULT_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(DEFAULT_PEAKS), "fallback"
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a per-rank number over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------ per-kernel accounting
+
+def kernel_work(d: wl.Dims):
+    """Algorithmic bytes and flops attributed to each kernel of one run.
+
+    Bytes: every input a kernel must read once plus every output it must write
+    once (workspace traffic excluded); they add up to the whole op's count.
+    Flops: 2 * T * N * K of the projection the kernel computes.
+    """
+    T, H, Dn, Dv, R = d.T, d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
+    b = {
+        "mla_compress_kernel": 2 * T * d.D + 2 * d.n_a * d.D,
+        "mla_norm_rope_kernel": 2 * (d.q_lora_rank + d.kv_lora_rank) + 4 * T + 4 * T * R
+                                + 2 * T * R + 2 * T * H * R,
+        "mla_expand_kernel": 2 * d.w_b_elems + 2 * T * H * Dn + 2 * T * H * Dv,
+        "mla_quant_kernel": (T * d.n_q + 4 * T) if d.quant_q else 0,
+    }
+    f = {
+        "mla_compress_kernel": 2 * T * d.n_a * d.D,
+        "mla_norm_rope_kernel": 0,
+        "mla_expand_kernel": 2 * T * (d.n_q * d.q_lora_rank + d.n_kv * d.kv_lora_rank),
+        "mla_quant_kernel": 0,
+    }
+    assert sum(b.values()) == wl.algorithmic_bytes(d)
+    return b, f
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_attention_prolog_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as fh:
+            h.update(n.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for ln in open(p):
+        if ":" in ln and ln.strip().startswith("- "):
+            k, v = ln.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("csrc_digest") != csrc_digest():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    from mla_attention_prolog_gb300 import binding
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    d = w.dims
+    inp = wl.make_inputs(w)
+    H, Dn, Dv, R = d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
+
+    def bf(a, shape):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).reshape(shape).to(dev)
+
+    base = dict(x=bf(inp.x, (d.T, d.D)), gamma=bf(inp.gamma, (-1,)), W_a=bf(inp.W_a, (d.n_a, d.D)),
+                W_b=bf(inp.W_b, (-1,)), positions=torch.from_numpy(inp.positions).to(dev),
+                cos_sin=torch.from_numpy(inp.cos_sin).to(dev))
+
+    def new_outputs():
+        o = dict(out_k=torch.empty((d.T, H, Dn + R), dtype=torch.bfloat16, device=dev),
+                 out_v=torch.empty((d.T, H, Dv), dtype=torch.bfloat16, device=dev),
+                 out_kpe=torch.empty((d.T, R), dtype=torch.bfloat16, device=dev),
+                 out_q_int8=None, out_scale=None)
+        if d.q_lora_rank:
+            o["out_q_int8"] = torch.empty((d.T, H, Dn + R), dtype=torch.int8, device=dev)
+            o["out_scale"] = torch.empty((d.T,), dtype=torch.float32, device=dev)
+        return o
+
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values())
+    set_bytes += sum(t.numel() * t.element_size() for t in new_outputs().values() if t is not None)
+    n_sets = max(2, min(args.steps, -(-3 * L2_BYTES // set_bytes)))
+    n_sets = min(n_sets, max(2, int(8e9 // set_bytes)))
+    sets = []
+    for i in range(n_sets):
+        s = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        s.update(new_outputs())
+        sets.append(s)
+
+    p = binding.MlaProlog.from_dims(d)
+    names = p.kernel_names()
+    active = [n for n in names if n != "mla_quant_kernel" or d.q_lora_rank]
+    stream = torch.cuda.Stream(device=dev)
+
+    def one(s):
+        p.run(s["x"], s["gamma"], s["W_a"], s["W_b"], s["positions"], s["cos_sin"], s["out_k"], s["out_v"],
+              s["out_kpe"], s["out_q_int8"], s["out_scale"], stream=stream)
+
+    # eager warm-up (also builds the tensor maps of each set)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, n_sets)):
+            one(sets[i % n_sets])
+    stream.synchronize()
+    assert p.device_status(stream) == 0
+
+    K = args.steps
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(K):
+            one(sets[i % n_sets])
+    # instrumented graph: per-step events around every kernel
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    gi = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gi, stream=stream):
+        for i in range(K):
+            p.set_timing_events(ev[i])
+            one(sets[i % n_sets])
+        p.set_timing_events([])
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    stream.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            g.replay()
+            end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_total = start.elapsed_time(end)
+        with torch.cuda.stream(stream):
+            gi.replay()
+        stream.synchronize()
+    clocks = clk.summary()
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / K
+    per_kernel = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+                  for j, n in enumerate(names) if n in active}
+
+    # e2e: host buffers through the public call
+    pin = lambda t: t.cpu().pin_memory()
+    hx, hpos = pin(base["x"]), pin(base["positions"])
+    outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in sets[0].items()
+              if k.startswith("out_") and v is not None}
+    s0 = sets[0]
+    h2d = hx.numel() * hx.element_size() + hpos.numel() * hpos.element_size()
+    d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
+
+    def e2e_step():
+        s0["x"].copy_(hx, non_blocking=True)
+        s0["positions"].copy_(hpos, non_blocking=True)
+        one(s0)
+        for k, v in outs_h.items():
+            v.copy_(s0[k], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    assert p.device_status(stream) == 0
+
+    tokens = d.T * K * world
+    value = tokens / (ms_total / 1e3)
+    peaks, peak_src = load_peaks()
+    kb, kf = kernel_work(d)
+    dom = max(per_kernel, key=per_kernel.get)
+    dom_ms = per_kernel[dom]
+    if w.bound == "tensor":
+        ach = kf[dom] / (dom_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4)}
+    else:
+        ach = kb[dom] / (dom_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4)}
+    roof.update({"kernel": dom, "kernel_ms": round(dom_ms, 5), "peak_source": peak_src,
+                 "traffic": committed_traffic(dom, args.workload)})
+    whole = {"algorithmic_bytes": wl.algorithmic_bytes(d), "algorithmic_flops": wl.algorithmic_flops(d),
+             "hbm_frac": round(wl.algorithmic_bytes(d) / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+             "tc_frac": round(wl.algorithmic_flops(d) / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "T": d.T, "D": d.D, "q_lora_rank": d.q_lora_rank,
+                   "kv_lora_rank": d.kv_lora_rank, "rope_dim": d.rope_dim, "num_heads": d.num_heads,
+                   "nope_dim": d.nope_dim, "v_dim": d.v_dim, "quant_q": d.quant_q,
+                   "l2": f"{n_sets} rotating buffer sets of {set_bytes / 1e6:.1f} MB (> 3x L2)",
+                   "timing": "CUDA graph of K steps between CUDA events", "parallelism": f"replicas x{world}",
+                   "schedule": p.schedule(), "inputs_sha256": inp.sha256()[:16]},
+        "roofline": roof,
+        "whole_step": whole,
+        "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * len(active),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    p.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ CPU arm
+
+def oracle_sample(w: wl.Workload, max_tokens: int):
+    """Inputs and a token sample of the workload for the oracle (bounded)."""
+    inp = wl.make_inputs(w)
+    T = inp.dims.T
+    if T <= max_tokens:
+        return inp, None
+    rng = np.random.default_rng(3)
+    return inp, np.sort(rng.choice(T, max_tokens, replace=False)).astype(np.int32)
+
+
+def cpu_baseline(w: wl.Workload, seconds: float):
+    import oracle
+    oracle.build()
+    per_tok = wl.algorithmic_flops(w.dims) / w.dims.T
+    max_tokens = max(1, min(w.dims.T, int(4e10 / per_tok)))  # ~40 GFLOP of fp64 work per call at most
+    inp, tok = oracle_sample(w, max_tokens)
+    d = inp.dims
+    n = d.T if tok is None else len(tok)
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or el / calls * (calls + 1) > 3 * seconds:
+            break
+    return {"value": round(n * calls / el, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{calls} call(s) of {n} of the workload's {d.T} tokens ({el:.1f} s wall)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    per_tok = wl.algorithmic_flops(w.dims) / w.dims.T
+    max_tokens = max(1, min(w.dims.T, int(1e10 / per_tok)))
+    inp, tok = oracle_sample(w, max_tokens)
+    d = inp.dims
+    n = d.T if tok is None else len(tok)
+    call = lambda: oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    for _ in range(args.warmup):
+        call()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        call()
+    el = time.perf_counter() - t0
+    v = n * args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32",
+            "data": "synthetic", "config": {"workload": args.workload, "T": d.T},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": f"{n} of {d.T} tokens per step"},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="v2lite_decode", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+"""GPU parity of the fused prolog against the CPU oracle, through the C ABI.
+
+Small and ragged cases are compared on every element; the full-size
+workloads on a seeded sample of tokens that always includes the first and
+last token (and, for the long prefill, every token whose x row was scaled
+x20).  Tolerances are the parity bar: BF16 outputs |d| <= 1e-2 + 1e-2 |ref|,
+scales relative <= 1e-3, INT8 codes differ by <= 1 on <= 0.1% of elements,
+and the quant step bit-exact on the oracle's own FP32 q.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import alloc_outputs, bf16_within, device_inputs, quant_within, run_prolog
+from mla_attention_prolog_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    from mla_attention_prolog_gb300 import build
+    build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def _sample(w: wl.Workload, inp: wl.Inputs, n: int):
+    T = inp.dims.T
+    if T <= n:
+        return None
+    rng = np.random.default_rng(7)
+    must = {0, T - 1} | set(int(i) for i in inp.boosted_rows)
+    rest = rng.choice(np.setdiff1d(np.arange(T), np.array(sorted(must))), n - len(must), replace=False)
+    return np.array(sorted(must | set(int(i) for i in rest)), np.int32)
+
+
+def check_against_oracle(w: wl.Workload, dims=None, sample=512, positions=None):
+    inp = wl.make_inputs(w, dims)
+    if positions is not None:
+        inp.positions[:] = positions
+    d = inp.dims
+    dins = device_inputs(inp, DEV)
+    outs = alloc_outputs(d, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    run_prolog(p, dins, outs)
+    status = p.device_status()
+    tok = _sample(w, inp, sample)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = slice(None) if tok is None else torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    bf16_within(outs["out_k"].t[sel], ref["out_k"], "out_k")
+    bf16_within(outs["out_v"].t[sel], ref["out_v"], "out_v")
+    bf16_within(outs["out_kpe"].t[sel], ref["out_kpe"], "out_kpe")
+    if d.q_lora_rank:
+        quant_within(outs["out_q_int8"].t[sel], outs["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+    for k, g in outs.items():
+        assert g.guards_intact(), f"{k}: write outside the buffer"
+    p.close()
+    return status, ref, outs
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_q", "v2lite_decode", "v2lite_prefill", "v3_decode", "v3_prefill"])
+def test_workload_parity(name):
+    status, ref, _ = check_against_oracle(wl.WORKLOADS[name])
+    assert status == 0 and ref["bad_positions"] == 0
+
+
+RAGGED = wl.Dims(T=300, D=512, q_lora_rank=64, kv_lora_rank=128, rope_dim=32, num_heads=5,
+                 nope_dim=64, v_dim=48, max_pos=512, flags=wl.QUANT_Q)
+
+
+@pytest.mark.parametrize("dims", [
+    RAGGED,                                               # 3 token tiles, ragged tail, q path
+    dataclasses.replace(RAGGED, T=1),                     # one token (decode schedule)
+    dataclasses.replace(RAGGED, T=129),                   # decode, two tiles, 1-row tail
+    dataclasses.replace(RAGGED, T=257, q_lora_rank=0, flags=0),   # prefill, KV only
+    dataclasses.replace(RAGGED, T=200, D=1024, kv_lora_rank=512, rope_dim=64, num_heads=3,
+                        nope_dim=128, v_dim=128, q_lora_rank=0, flags=0),   # decode, narrow kv tiles
+    dataclasses.replace(RAGGED, T=96, D=2048, q_lora_rank=96, rope_dim=16, nope_dim=16, v_dim=16,
+                        num_heads=7),                     # narrow heads, Lq not a multiple of 64
+], ids=["ragged300q", "T1", "T129", "prefill257", "decode200", "narrow_heads"])
+def test_ragged_parity(dims):
+    w = wl.Workload("ragged", dims, positions="uniform")
+    status, ref, _ = check_against_oracle(w)
+    assert status == 0 and ref["bad_positions"] == 0
+
+
+def test_out_of_range_positions_zero_fill_and_status():
+    d = dataclasses.replace(RAGGED, T=40)
+    w = wl.Workload("badpos", d, positions="uniform")
+    inp = wl.make_inputs(w)
+    pos = inp.positions.copy()
+    pos[3] = d.max_pos
+    pos[17] = -5
+    status, ref, outs = check_against_oracle(w, positions=pos)
+    assert status & binding.STATUS_POSITION_RANGE
+    assert ref["bad_positions"] == 2
+    for t in (3, 17):
+        assert not outs["out_k"].t[t].float().abs().sum().item()
+        assert not outs["out_q_int8"].t[t].abs().sum().item()
+        assert outs["out_scale"].t[t].item() == 0
+
+
+def test_quant_step_bit_exact_on_oracle_q():
+    w = wl.WORKLOADS["v3_decode"]
+    inp = wl.make_inputs(w)
+    d = inp.dims
+    tok = np.arange(0, d.T, 4, dtype=np.int32)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin,
+                            tokens=tok, taps=True)
+    q = torch.from_numpy(ref["q"]).to(DEV)
+    q[1].zero_()  # an all-zero row: codes 0, scale 0
+    codes = torch.empty(q.shape, dtype=torch.int8, device=DEV)
+    scale = torch.empty(q.shape[0], dtype=torch.float32, device=DEV)
+    binding.quant_rows(q, codes, scale)
+    torch.cuda.synchronize()
+    qh = q.cpu().numpy()
+    for i in range(qh.shape[0]):
+        c, s = oracle.quant_row(qh[i])
+        assert np.array_equal(codes[i].cpu().numpy(), c), i
+        assert scale[i].item() == s, i
+    assert scale[1].item() == 0.0 and not codes[1].abs().sum().item()
+
+
+def test_runs_are_deterministic():
+    w = wl.WORKLOADS["v3_decode"]
+    inp = wl.make_inputs(w)
+    d = inp.dims
+    dins = device_inputs(inp, DEV)
+    a, b = alloc_outputs(d, DEV), alloc_outputs(d, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    run_prolog(p, dins, a)
+    run_prolog(p, dins, b)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k].t.view(torch.uint8) if a[k].t.dtype != torch.float32 else a[k].t,
+                           b[k].t.view(torch.uint8) if b[k].t.dtype != torch.float32 else b[k].t), k
+    p.close()
+
+
+def test_empty_batch_is_a_no_op():
+    d = dataclasses.replace(RAGGED, T=0)
+    p = binding.MlaProlog.from_dims(d)
+    dins = device_inputs(wl.make_inputs(wl.Workload("e", dataclasses.replace(d, T=1), positions="uniform")), DEV)
+    rc = binding.lib().mla_prolog_run(p.handle, *([None] * 12))
+    assert rc == 0
+    assert p.device_status() == 0
+    p.close()
+    del dins
+
+
+def test_bounded_wait_selftest_reports_timeout():
+    p = binding.MlaProlog.from_dims(wl.WORKLOADS["tiny"].dims)
+    p.selftest_wait_timeout(2_000_000)  # 2 ms
+    assert p.device_status() & binding.STATUS_WAIT_TIMEOUT
+    # the context stays usable
+    check_against_oracle(wl.WORKLOADS["tiny"])
+    p.close()
+
+
+def test_timing_events_hook():
+    w = wl.WORKLOADS["v2lite_decode"]
+    inp = wl.make_inputs(w)
+    d = inp.dims
+    dins = device_inputs(inp, DEV)
+    outs = alloc_outputs(d, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    names = p.kernel_names()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+    p.set_timing_events(ev)
+    run_prolog(p, dins, outs)
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(names))]
+    assert all(t >= 0 for t in times)
+    p.set_timing_events([])
+    p.close()
