@@ -255,6 +255,10 @@ def run_gpu(args):
             one(sets[i % n_sets])
     # instrumented graph: per-step events around every kernel
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    for row in ev:  # create the CUDA events before the capture
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
     gi = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gi, stream=stream):
         for i in range(K):

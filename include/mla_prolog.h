@@ -185,6 +185,34 @@ int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_
 int32_t mla_prolog_kernel_count(mla_prolog_t h);
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i);
 
+/*
+ * Copies an intermediate of the handle's most recent run out of its device
+ * workspace into `dst` (device memory, `bytes` long), enqueued on `stream`.
+ * For checking each step of the path on its own:
+ *   MLA_TAP_NORMED  BF16 [T, Lq + Lkv]  normed c_q | c_kv (after gamma and the
+ *                                       BF16 cast: input of the expansion)
+ *   MLA_TAP_Q       FP32 [T, H(Dn+R)]   q after its projection and RoPE (the
+ *                                       quantisation input; Lq > 0 only)
+ *   MLA_TAP_AMAX    FP32 [T]            max |q| per token (Lq > 0 only)
+ * Errors: INVALID_ARG (unknown tap, tap absent, size mismatch), CUDA.
+ */
+#define MLA_TAP_NORMED 1
+#define MLA_TAP_Q      2
+#define MLA_TAP_AMAX   3
+int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream);
+
+/*
+ * Tuning knobs; create() picks the defaults.
+ *   MLA_TUNE_COMPRESS_GROUP  K blocks of 64 summed by one tensor-core
+ *                            accumulation chain of the compression projection
+ *                            before the chain is drained into exactly
+ *                            compensated FP32 registers (1 .. 64).  Shorter
+ *                            chains round closer to the exact sum.
+ * Errors: INVALID_ARG (unknown key or value out of range).
+ */
+#define MLA_TUNE_COMPRESS_GROUP 1
+int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
+
 /* Bytes of device workspace the handle holds. */
 int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes);
 

@@ -27,8 +27,10 @@ EXPORTED = [
     "mla_prolog_strerror", "mla_prolog_last_cuda_error", "mla_prolog_quant_rows",
     "mla_prolog_set_wait_timeout", "mla_prolog_selftest_wait_timeout",
     "mla_prolog_set_timing_events", "mla_prolog_kernel_count", "mla_prolog_kernel_name",
-    "mla_prolog_workspace_bytes", "mla_prolog_schedule",
+    "mla_prolog_workspace_bytes", "mla_prolog_schedule", "mla_prolog_copy_tap", "mla_prolog_set_tuning",
 ]
+TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
+TUNE_COMPRESS_GROUP = 1
 
 
 class MlaPrologDims(ctypes.Structure):
@@ -75,6 +77,8 @@ def lib(path: Optional[str] = None):
     L.mla_prolog_kernel_name.restype = ctypes.c_char_p
     L.mla_prolog_workspace_bytes.argtypes = [V, P(ctypes.c_size_t)]
     L.mla_prolog_schedule.argtypes = [V, P(I32), P(I32), P(I32), P(I32)]
+    L.mla_prolog_copy_tap.argtypes = [V, I32, V, ctypes.c_size_t, V]
+    L.mla_prolog_set_tuning.argtypes = [V, I32, I32]
     for n in EXPORTED:
         if n not in ("mla_prolog_strerror", "mla_prolog_last_cuda_error", "mla_prolog_kernel_count",
                      "mla_prolog_kernel_name"):
@@ -185,12 +189,33 @@ class MlaProlog:
         if not events:
             _check(lib().mla_prolog_set_timing_events(self.handle, None, 0), "set_timing_events")
             return
+        for e in events:
+            if not e.cuda_event:  # torch creates the CUDA event on its first record
+                e.record(torch.cuda.current_stream(self.device))
         arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         _check(lib().mla_prolog_set_timing_events(self.handle, arr, len(events)), "set_timing_events")
 
     def kernel_names(self):
         n = lib().mla_prolog_kernel_count(self.handle)
         return [lib().mla_prolog_kernel_name(self.handle, i).decode() for i in range(n)]
+
+    def tap(self, which: int, stream=None) -> torch.Tensor:
+        """Device copy of an intermediate of the last run (normed rows, FP32 q, amax)."""
+        d = self.dims
+        if which == TAP_NORMED:
+            t = torch.empty((d.T, d.q_lora_rank + d.kv_lora_rank), dtype=torch.bfloat16, device=self.device)
+        elif which == TAP_Q:
+            t = torch.empty((d.T, d.num_heads * (d.nope_dim + d.rope_dim)), dtype=torch.float32, device=self.device)
+        elif which == TAP_AMAX:
+            t = torch.empty((d.T,), dtype=torch.float32, device=self.device)
+        else:
+            raise ValueError(which)
+        _check(lib().mla_prolog_copy_tap(self.handle, which, t.data_ptr(), t.numel() * t.element_size(),
+                                         _stream_ptr(stream)), "mla_prolog_copy_tap")
+        return t
+
+    def set_tuning(self, key: int, value: int) -> None:
+        _check(lib().mla_prolog_set_tuning(self.handle, key, value), "mla_prolog_set_tuning")
 
     def workspace_bytes(self) -> int:
         v = ctypes.c_size_t(0)

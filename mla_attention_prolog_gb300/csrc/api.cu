@@ -70,6 +70,7 @@ struct mla_prolog {
     bool decode = false;
     GemmShape shape_a = GemmShape::Wide, shape_b = GemmShape::Wide;
     int bn_a = 0, splits_a = 1, bn_kv = 0, m_tiles = 0;
+    int group_a = 1;  // K blocks per tensor-core accumulation chain (compression)
     // workspace
     void* ws = nullptr;
     size_t ws_bytes = 0;
@@ -105,13 +106,6 @@ int check_dims(const mla_prolog_dims& d) {
     const double big = static_cast<double>(d.T) * d.num_heads * (d.nope_dim + d.rope_dim + d.v_dim);
     if (big > 4.0e9 || static_cast<double>(d.T) * d.D > 4.0e9) return MLA_ERR_UNSUPPORTED_DIMS;
     return MLA_OK;
-}
-
-// Largest width in [lo, 256] (step 16) dividing n, else 256 with a ragged tail.
-int pick_wide_bn(int n, int lo) {
-    for (int bn = 256; bn >= lo; bn -= 16)
-        if (n % bn == 0) return bn;
-    return 256;
 }
 
 }  // namespace
@@ -172,9 +166,10 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->splits_a = s;
     } else {
         h->shape_a = GemmShape::Wide;
-        h->bn_a = pick_wide_bn(h->NA, 128);
+        h->bn_a = 128;
         h->splits_a = 1;
     }
+    h->group_a = h->decode ? 1 : 2;
     // Expansion: prefill uses 256-wide kv tiles (one head of V2/V3); decode
     // without a q path uses the narrow kernel with enough tiles to cover the
     // SMs; decode with a q path shares the wide kernel with the q heads.
@@ -285,7 +280,8 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     };
 
     mark(0);
-    CompressParams pa{h->partials, d.T, h->NA, h->bn_a, cdiv(d.D, kBK), h->splits_a, h->status, h->timeout_ns};
+    CompressParams pa{h->partials, d.T,        h->NA,     h->bn_a,     cdiv(d.D, kBK),
+                      h->splits_a, h->group_a, h->status, h->timeout_ns};
     dim3 ga(cdiv(h->NA, h->bn_a), h->m_tiles, h->splits_a);
     if ((e = launch_compress(h->shape_a, ga, h->tm_x, h->tm_wa, pa, st)) != cudaSuccess)
         return cuda_fail(e, "launch mla_compress_kernel");
@@ -406,6 +402,44 @@ int32_t mla_prolog_kernel_count(mla_prolog_t h) { return h ? kKernelCount : 0; }
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
     if (!h || i < 0 || i >= kKernelCount) return "";
     return kKernelNames[i];
+}
+
+int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream) {
+    if (!h || !dst) return MLA_ERR_INVALID_ARG;
+    const mla_prolog_dims& d = h->d;
+    const size_t T = static_cast<size_t>(d.T);
+    const void* src = nullptr;
+    size_t n = 0;
+    switch (which) {
+        case MLA_TAP_NORMED:
+            src = h->normed;
+            n = T * (d.q_lora_rank + d.kv_lora_rank) * 2;
+            break;
+        case MLA_TAP_Q:
+            src = h->qws;
+            n = T * h->NQ * 4;
+            break;
+        case MLA_TAP_AMAX:
+            src = d.q_lora_rank > 0 ? h->amax : nullptr;
+            n = T * 4;
+            break;
+        default: return MLA_ERR_INVALID_ARG;
+    }
+    if (!src || bytes != n) return MLA_ERR_INVALID_ARG;
+    if (n == 0) return MLA_OK;
+    cudaError_t e = cudaMemcpyAsync(dst, src, n, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "cudaMemcpyAsync(tap)");
+}
+
+int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
+    if (!h) return MLA_ERR_INVALID_ARG;
+    switch (key) {
+        case MLA_TUNE_COMPRESS_GROUP:
+            if (value < 1 || value > 64) return MLA_ERR_INVALID_ARG;
+            h->group_a = value;
+            return MLA_OK;
+        default: return MLA_ERR_INVALID_ARG;
+    }
 }
 
 int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes) {

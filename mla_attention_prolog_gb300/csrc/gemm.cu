@@ -139,33 +139,195 @@ __device__ __forceinline__ void gemm_tile(uint8_t* smem_raw, const TileJob& job,
 }
 
 // ------------------------------------------------------- compression (x W_a^T)
+//
+// The tensor core adds each K=16 product group into its FP32 accumulator with
+// a limited-precision aligned sum, and that error grows with the length of
+// the accumulation chain (measured on GB300: one 448-instruction chain flips
+// ~0.5% of the BF16-rounded outputs against the exact sum).  The compression
+// output is rounded to BF16 and then feeds the RMSNorm, the q projection and
+// the per-token INT8 codes, so this kernel keeps every tensor-core chain
+// short: the MMA warp restarts a fresh TMEM accumulator every `group` K
+// blocks (two TMEM buffers in turn), and the epilogue warps drain each chain
+// into registers with error-free TwoSum accumulation while the next chain is
+// being computed.
 
 template <int BN_MAX, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+struct DrainLayout {
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = BN_MAX * kBK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int BARS = STAGES * STAGE;
+    // full[S], empty[S], acc_full[2], acc_empty[2], mma_done
+    static constexpr int MISC = BARS + (2 * STAGES + 5) * 8;
+    static constexpr int BYTES = MISC + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 2 * BN_MAX <= 64 ? 64 : 2 * BN_MAX <= 128 ? 128 : 2 * BN_MAX <= 256 ? 256 : 512;
+    static_assert(STAGE % 1024 == 0, "stages must keep 1 KB alignment for the swizzle atoms");
+};
+
+constexpr int kDrainEpiWarps = 8;  // two warps per TMEM lane quarter, one per column half
+constexpr int kCompressThreads = 64 + 32 * kDrainEpiWarps;
+
+template <int BN_MAX, int STAGES>
+__global__ void __launch_bounds__(kCompressThreads, 1)
     mla_compress_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const __grid_constant__ CUtensorMap tm_wa, const CompressParams p) {
-    extern __shared__ uint8_t smem[];
+    using L = DrainLayout<BN_MAX, STAGES>;
+    constexpr int HALF = BN_MAX / 2;  // columns per epilogue thread
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    const uint32_t base = raw + pad;
+    uint8_t* base_ptr = smem_raw + pad;
+    const uint32_t full0 = base + L::BARS;
+    const uint32_t empty0 = full0 + 8 * STAGES;
+    const uint32_t accf0 = empty0 + 8 * STAGES;  // acc_full[2]
+    const uint32_t acce0 = accf0 + 16;           // acc_empty[2]
+    const uint32_t mma_done = acce0 + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::MISC + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
     const int n0 = blockIdx.x * p.bn;
     const int m0 = blockIdx.y * kBM;
     const int split = blockIdx.z;
     const int kb0 = split * p.kb_total / p.splits;
-    const int kb1 = (split + 1) * p.kb_total / p.splits;
-    const TileJob job{&tm_x, &tm_wa, m0, n0, kb0, kb1 - kb0, p.bn};
-    gemm_tile<BN_MAX, STAGES>(smem, job, p.timeout_ns, p.status,
-        [&](uint32_t tbase, int row) {
-            const int t = m0 + row;
-            float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0;
-            for (int c = 0; c < p.bn; c += 16) {
-                float v[16];
-                tmem_ld16(tbase + c, v);
-                if (t < p.T && n0 + c < p.NA) {
-                    float4* d4 = reinterpret_cast<float4*>(dst + c);
+    const int nkb = (split + 1) * p.kb_total / p.splits - kb0;
+    const int group = p.group;
+    const int ngroups = (nkb + group - 1) / group;
+    const uint64_t timeout_ns = p.timeout_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, kDrainEpiWarps);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_wa);
+            const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + p.bn * kBK * 2);
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % STAGES;
+                const uint32_t ph = (i / STAGES) & 1;
+                if (!mbar_wait(empty0 + 8 * s, ph ^ 1, timeout_ns, abort_flag)) { ok = false; break; }
+                const uint32_t sa = base + s * L::STAGE;
+                mbar_arrive_expect_tx(full0 + 8 * s, tx);
+                tma_load_2d(sa, &tm_x, full0 + 8 * s, (kb0 + i) * kBK, m0);
+                tma_load_2d(sa + L::A_BYTES, &tm_wa, full0 + 8 * s, (kb0 + i) * kBK, n0);
+                ++issued;
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, kStatusWaitTimeout);
+            }
+            for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+                mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, timeout_ns, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
+            bool ok = true;
+            int i = 0;
+            for (int g = 0; g < ngroups && ok; ++g) {
+                const int b = g & 1;
+                // wait until the epilogue drained this buffer's previous chain
+                if (!mbar_wait(acce0 + 8 * b, ((g >> 1) & 1) ^ 1, timeout_ns, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t dacc = tmem + static_cast<uint32_t>(b * BN_MAX);
+                const int iend = (g + 1) * group < nkb ? (g + 1) * group : nkb;
+                for (int first = 1; i < iend; ++i, first = 0) {
+                    const int s = i % STAGES;
+                    const uint32_t ph = (i / STAGES) & 1;
+                    if (!mbar_wait(full0 + 8 * s, ph, timeout_ns, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * L::STAGE;
+                    const uint64_t ad = smem_desc_sw128(sa);
+                    const uint64_t bd = smem_desc_sw128(sa + L::A_BYTES);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
+                    mma_commit(empty0 + 8 * s);
+                }
+                if (ok) mma_commit(accf0 + 8 * b);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                atomicOr(p.status, kStatusWaitTimeout);
+            }
+            // Every issued MMA must have finished before TMEM is released.
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, timeout_ns, nullptr);
+        }
+    } else {
+        const int ew = warp - 2;
+        const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+        const int half = ew >> 2;                 // column half
+        const int row = quarter * 32 + lane;
+        const int t = m0 + row;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        float acc[HALF], cmp[HALF];
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) acc[j] = cmp[j] = 0.0f;
+        bool ok = true;
+        for (int g = 0; g < ngroups; ++g) {
+            const int b = g & 1;
+            bool got = mbar_wait(accf0 + 8 * b, (g >> 1) & 1, timeout_ns, abort_flag);
+            got = __all_sync(0xffffffffu, got);
+            if (!got) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t src = tmem + lane_off + static_cast<uint32_t>(b * BN_MAX + half * HALF);
+#pragma unroll
+            for (int j = 0; j < HALF; j += 16) {
+                if (half * HALF + j < p.bn) {  // warp-uniform
+                    float v[16];
+                    tmem_ld16(src + j, v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) two_sum_add(acc[j + e], cmp[j + e], v[e]);
                 }
             }
-        });
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce0 + 8 * b);
+        }
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
+        } else if (t < p.T) {
+            float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
+#pragma unroll
+            for (int j = 0; j < HALF; j += 4) {
+                const int col = n0 + half * HALF + j;
+                if (half * HALF + j < p.bn && col < p.NA)
+                    *reinterpret_cast<float4*>(dst + j) =
+                        make_float4(__fadd_rn(acc[j], cmp[j]), __fadd_rn(acc[j + 1], cmp[j + 1]),
+                                    __fadd_rn(acc[j + 2], cmp[j + 2]), __fadd_rn(acc[j + 3], cmp[j + 3]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
 }
 
 // -------------------------------------------------- expansion (normed W_b^T)
@@ -297,13 +459,15 @@ __global__ void mla_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 using WideL = GemmLayout<256, 4>;
 using NarrowL = GemmLayout<64, 8>;
+using CWideL = DrainLayout<128, 6>;
+using CNarrowL = DrainLayout<64, 8>;
 
 int gemm_smem_bytes(GemmShape s) { return s == GemmShape::Wide ? WideL::BYTES : NarrowL::BYTES; }
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, WideL::BYTES))) return e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowL::BYTES))) return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, CWideL::BYTES))) return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, CNarrowL::BYTES))) return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, WideL::BYTES))) return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowL::BYTES))) return e;
     return cudaSuccess;
@@ -312,9 +476,9 @@ cudaError_t gemm_set_attributes() {
 cudaError_t launch_compress(GemmShape s, dim3 grid, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
                             const CompressParams& p, cudaStream_t st) {
     if (s == GemmShape::Wide)
-        mla_compress_kernel<256, 4><<<grid, kGemmThreads, WideL::BYTES, st>>>(tm_x, tm_wa, p);
+        mla_compress_kernel<128, 6><<<grid, kCompressThreads, CWideL::BYTES, st>>>(tm_x, tm_wa, p);
     else
-        mla_compress_kernel<64, 8><<<grid, kGemmThreads, NarrowL::BYTES, st>>>(tm_x, tm_wa, p);
+        mla_compress_kernel<64, 8><<<grid, kCompressThreads, CNarrowL::BYTES, st>>>(tm_x, tm_wa, p);
     return cudaGetLastError();
 }
 

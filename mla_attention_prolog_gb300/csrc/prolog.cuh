@@ -22,6 +22,7 @@ struct CompressParams {
     int bn;        // tile width over the NA weight rows
     int kb_total;  // K blocks of 64 over D
     int splits;    // split-K factor
+    int group;     // K blocks per tensor-core accumulation chain (>= 1)
     int* status;
     uint64_t timeout_ns;
 };
@@ -70,7 +71,9 @@ struct QuantParams {
 };
 
 // Shapes of the GEMM kernel instantiations.
-enum class GemmShape { Wide, Narrow };  // Wide: BN_MAX 256, 4 stages; Narrow: BN_MAX 64, 8 stages
+// Expansion kernel: Wide = BN_MAX 256, 4 stages; Narrow = BN_MAX 64, 8 stages.
+// Compression kernel: Wide = BN_MAX 128, 6 stages; Narrow = BN_MAX 64, 8 stages.
+enum class GemmShape { Wide, Narrow };
 int gemm_smem_bytes(GemmShape s);
 constexpr int kGemmThreads = 192;
 

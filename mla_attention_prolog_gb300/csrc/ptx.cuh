@@ -38,6 +38,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -204,6 +208,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Error-free accumulation: s + c tracks the exact sum of the added values
+// (TwoSum of Knuth/Moller: the rounding error of each addition is recovered
+// and carried in c).  Every operation is explicitly rounded so no compiler
+// contraction can change it.
+__device__ __forceinline__ void two_sum_add(float& s, float& c, float v) {
+    const float t = __fadd_rn(s, v);
+    const float bp = __fsub_rn(t, s);
+    const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(v, bp));
+    c = __fadd_rn(c, err);
+    s = t;
 }
 
 // --------------------------------------------------------------- conversions

@@ -60,10 +60,17 @@ __global__ void __launch_bounds__(kNormWarps * 32)
     const float* prow = p.partials + static_cast<size_t>(t) * NA;
     for (int i = lane * 4; i < NA; i += 128) {
         float4 a = *reinterpret_cast<const float4*>(prow + i);
-        for (int s = 1; s < p.splits; ++s) {
-            const float4 b = *reinterpret_cast<const float4*>(prow + s * split_stride + i);
-            a.x = __fadd_rn(a.x, b.x); a.y = __fadd_rn(a.y, b.y);
-            a.z = __fadd_rn(a.z, b.z); a.w = __fadd_rn(a.w, b.w);
+        if (p.splits > 1) {
+            // split order is fixed; TwoSum keeps the reduction exact to FP32 rounding
+            float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 1; s < p.splits; ++s) {
+                const float4 b = *reinterpret_cast<const float4*>(prow + s * split_stride + i);
+                two_sum_add(a.x, c.x, b.x);
+                two_sum_add(a.y, c.y, b.y);
+                two_sum_add(a.z, c.z, b.z);
+                two_sum_add(a.w, c.w, b.w);
+            }
+            a = make_float4(__fadd_rn(a.x, c.x), __fadd_rn(a.y, c.y), __fadd_rn(a.z, c.z), __fadd_rn(a.w, c.w));
         }
         const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
         *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
