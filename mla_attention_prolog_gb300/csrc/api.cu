@@ -275,8 +275,9 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     }
     const bool timed = h->n_events > 0;
     cudaError_t e;
+    // External records so that the events also time a run captured into a CUDA graph.
     auto mark = [&](int i) {
-        if (timed) cudaEventRecord(h->events[i], st);
+        if (timed) cudaEventRecordWithFlags(h->events[i], st, cudaEventRecordExternal);
     };
 
     mark(0);
