@@ -81,7 +81,7 @@ def barrier(world: int) -> None:
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -94,7 +94,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, ValueError):
@@ -105,6 +105,11 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    @staticmethod
+    def now():
+        import datetime
+        return datetime.datetime.now()
+
     def __exit__(self, *exc):
         if self.proc:
             self.proc.terminate()
@@ -113,25 +118,32 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen; samples inside
+        [t0, t1] (the timed region) when there are at least 3 of them, else
+        every sample of the run."""
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                rows.append((ts, float(parts[1]), float(parts[2]),
+                             [n for n, v in zip(names, parts[4:8]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        window = "timed region"
+        sel = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        if len(sel) < 3:
+            sel, window = rows, "whole run"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        reasons = sorted({n for r in sel for n in r[3]})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel), "window": window}
 
 
 # ------------------------------------------------------ per-kernel accounting
@@ -224,7 +236,7 @@ def run_gpu(args):
 
     set_bytes = sum(t.numel() * t.element_size() for t in base.values())
     set_bytes += sum(t.numel() * t.element_size() for t in new_outputs().values() if t is not None)
-    n_sets = max(2, min(args.steps, -(-3 * L2_BYTES // set_bytes)))
+    n_sets = max(2, -(-3 * L2_BYTES // set_bytes))
     n_sets = min(n_sets, max(2, int(8e9 // set_bytes)))
     sets = []
     for i in range(n_sets):
@@ -232,6 +244,7 @@ def run_gpu(args):
         s.update(new_outputs())
         sets.append(s)
 
+    clk = ClockSampler(local).__enter__()
     p = binding.MlaProlog.from_dims(d)
     names = p.kernel_names()
     active = [n for n in names if n != "mla_quant_kernel" or d.q_lora_rank]
@@ -248,48 +261,65 @@ def run_gpu(args):
     stream.synchronize()
     assert p.device_status(stream) == 0
 
-    K = args.steps
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(K):
+    # Step time estimate from eager runs, to size K when it is not given.
+    t_est0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_sets):
             one(sets[i % n_sets])
-    # instrumented graph: per-step events around every kernel
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    stream.synchronize()
+    t_step = (time.perf_counter() - t_est0) / n_sets
+    K = args.steps if args.steps else int(min(100000, max(50, 1.0 / t_step)))
+    G = K if K <= 200 else 100                     # steps per captured graph
+    reps, rem = divmod(K, G)
+
+    def capture(nsteps, hook=None):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(nsteps):
+                if hook is not None:
+                    p.set_timing_events(hook[i])
+                one(sets[i % n_sets])
+            if hook is not None:
+                p.set_timing_events([])
+        return gr
+
+    g = capture(G)
+    g_rem = capture(rem) if rem else None
+    # instrumented graph: per-step events around every kernel (G steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(G)]
     for row in ev:  # create the CUDA events before the capture
         for e in row:
             e.record(stream)
     stream.synchronize()
-    gi = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gi, stream=stream):
-        for i in range(K):
-            p.set_timing_events(ev[i])
-            one(sets[i % n_sets])
-        p.set_timing_events([])
+    gi = capture(G, ev)
 
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+        for _ in range(max(1, -(-args.warmup // G))):
             g.replay()
     stream.synchronize()
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            start.record(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = ClockSampler.now()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
             g.replay()
-            end.record(stream)
-        stream.synchronize()
-        torch.cuda.synchronize()
-        barrier(world)
-        ms_total = start.elapsed_time(end)
-        with torch.cuda.stream(stream):
-            gi.replay()
-        stream.synchronize()
-    clocks = clk.summary()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    stream.synchronize()
+    t_wall1 = ClockSampler.now()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    with torch.cuda.stream(stream):
+        gi.replay()
+    stream.synchronize()
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / K
-    per_kernel = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K))
+    per_kernel = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(G))
                   for j, n in enumerate(names) if n in active}
 
     # e2e: host buffers through the public call
@@ -312,16 +342,19 @@ def run_gpu(args):
         for _ in range(args.warmup):
             e2e_step()
     stream.synchronize()
+    K_e2e = min(K, 2000)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(K):
+        for _ in range(K_e2e):
             e2e_step()
         e1.record(stream)
     stream.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     assert p.device_status(stream) == 0
+    clk.__exit__(None, None, None)
+    clocks = clk.summary(t_wall0, t_wall1)
 
     tokens = d.T * K * world
     value = tokens / (ms_total / 1e3)
@@ -352,13 +385,14 @@ def run_gpu(args):
                    "kv_lora_rank": d.kv_lora_rank, "rope_dim": d.rope_dim, "num_heads": d.num_heads,
                    "nope_dim": d.nope_dim, "v_dim": d.v_dim, "quant_q": d.quant_q,
                    "l2": f"{n_sets} rotating buffer sets of {set_bytes / 1e6:.1f} MB (> 3x L2)",
-                   "timing": "CUDA graph of K steps between CUDA events", "parallelism": f"replicas x{world}",
+                   "timing": f"{reps} replay(s) of a {G}-step CUDA graph" + (f" + {rem}" if rem else "")
+                             + " between CUDA events", "parallelism": f"replicas x{world}",
                    "schedule": p.schedule(), "inputs_sha256": inp.sha256()[:16]},
         "roofline": roof,
         "whole_step": whole,
         "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
-        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(d.T * K_e2e * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K_e2e},
         "gpu_launches": K * len(active),
         "clocks": clocks,
     }
@@ -418,15 +452,16 @@ def run_reference(args):
     d = inp.dims
     n = d.T if tok is None else len(tok)
     call = lambda: oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    steps = args.steps or 10
     for _ in range(args.warmup):
         call()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         call()
     el = time.perf_counter() - t0
-    v = n * args.steps / el
+    v = n * steps / el
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32",
             "data": "synthetic", "config": {"workload": args.workload, "T": d.T},
             "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
@@ -438,7 +473,8 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: about one second of steps)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="v2lite_decode", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -275,18 +275,21 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     }
     const bool timed = h->n_events > 0;
     cudaError_t e;
-    // External records so that the events also time a run captured into a CUDA graph.
-    auto mark = [&](int i) {
-        if (timed) cudaEventRecordWithFlags(h->events[i], st, cudaEventRecordExternal);
+    // Inside a stream capture the records must be external event nodes to time graph replays.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (timed && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return cuda_fail(cudaGetLastError(), "cudaStreamIsCapturing");
+    const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    auto mark = [&](int i) -> cudaError_t {
+        return timed ? cudaEventRecordWithFlags(h->events[i], st, rec_flags) : cudaSuccess;
     };
 
-    mark(0);
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     CompressParams pa{h->partials, d.T,        h->NA,     h->bn_a,     cdiv(d.D, kBK),
                       h->splits_a, h->group_a, h->status, h->timeout_ns};
     dim3 ga(cdiv(h->NA, h->bn_a), h->m_tiles, h->splits_a);
     if ((e = launch_compress(h->shape_a, ga, h->tm_x, h->tm_wa, pa, st)) != cudaSuccess)
         return cuda_fail(e, "launch mla_compress_kernel");
-    mark(1);
+    if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
     NormRopeParams pn{};
     pn.partials = h->partials;
@@ -311,7 +314,7 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pn.amax = Lq > 0 ? h->amax : nullptr;
     pn.status = h->status;
     if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
-    mark(2);
+    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
     ExpandParams pb{};
     pb.T = d.T;
@@ -337,13 +340,13 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     dim3 gb(pb.nq_tiles + cdiv(h->NKV, h->bn_kv), h->m_tiles);
     if ((e = launch_expand(h->shape_b, gb, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb, st)) != cudaSuccess)
         return cuda_fail(e, "launch mla_expand_kernel");
-    mark(3);
+    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
     if (Lq > 0) {
         QuantParams pq{h->qws, h->amax, d.T, h->NQ, out_q_int8, out_scale};
-        if ((e = launch_quant(pq, st)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
+        if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
     }
-    mark(4);
+    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     return MLA_OK;
 }
 
@@ -367,7 +370,7 @@ int mla_prolog_quant_rows(const float* y, int32_t rows, int32_t row_len, int8_t*
     if (!y || !codes || !scale || !aligned(y, 16) || !aligned(codes, 4) || !aligned(scale, 4))
         return MLA_ERR_INVALID_ARG;
     QuantParams p{y, nullptr, rows, row_len, codes, scale};
-    cudaError_t e = launch_quant(p, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_quant(p, static_cast<cudaStream_t>(stream), false);
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "launch mla_quant_kernel");
 }
 

@@ -69,15 +69,28 @@ __device__ __forceinline__ void gemm_tile(uint8_t* smem_raw, const TileJob& job,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
+    if (warp != 0) pdl_wait();  // the producer waits after its early weight loads
 
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tensormap(job.tmA);
             prefetch_tensormap(job.tmB);
             const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + job.bn * kBK * 2);
-            int issued = 0;
+            // The weights (B) do not depend on the previous kernel: stream the
+            // first ring of them before waiting for it, then the activations.
+            const int pre = job.nkb < STAGES ? job.nkb : STAGES;
+            for (int i = 0; i < pre; ++i) {
+                const uint32_t sa = base + i * L::STAGE;
+                mbar_arrive_expect_tx(full0 + 8 * i, tx);
+                tma_load_2d(sa + L::A_BYTES, job.tmB, full0 + 8 * i, (job.kb0 + i) * kBK, job.b_row);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(base + i * L::STAGE, job.tmA, full0 + 8 * i, (job.kb0 + i) * kBK, job.a_row);
+            int issued = pre;
             bool ok = true;
-            for (int i = 0; i < job.nkb; ++i) {
+            for (int i = pre; i < job.nkb; ++i) {
                 const int s = i % STAGES;
                 const uint32_t ph = (i / STAGES) & 1;
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1, timeout_ns, abort_flag)) { ok = false; break; }
@@ -217,6 +230,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -458,18 +472,18 @@ __global__ void mla_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 // ------------------------------------------------------------ launchers
 
 using WideL = GemmLayout<256, 4>;
-using NarrowL = GemmLayout<64, 8>;
+using NarrowL = GemmLayout<64, 4>;
 using CWideL = DrainLayout<128, 6>;
-using CNarrowL = DrainLayout<64, 8>;
+using CNarrowL = DrainLayout<64, 4>;
 
 int gemm_smem_bytes(GemmShape s) { return s == GemmShape::Wide ? WideL::BYTES : NarrowL::BYTES; }
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, CWideL::BYTES))) return e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, CNarrowL::BYTES))) return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, CNarrowL::BYTES))) return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, WideL::BYTES))) return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowL::BYTES))) return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowL::BYTES))) return e;
     return cudaSuccess;
 }
 
@@ -478,7 +492,7 @@ cudaError_t launch_compress(GemmShape s, dim3 grid, const CUtensorMap& tm_x, con
     if (s == GemmShape::Wide)
         mla_compress_kernel<128, 6><<<grid, kCompressThreads, CWideL::BYTES, st>>>(tm_x, tm_wa, p);
     else
-        mla_compress_kernel<64, 8><<<grid, kCompressThreads, CNarrowL::BYTES, st>>>(tm_x, tm_wa, p);
+        mla_compress_kernel<64, 4><<<grid, kCompressThreads, CNarrowL::BYTES, st>>>(tm_x, tm_wa, p);
     return cudaGetLastError();
 }
 
@@ -486,10 +500,10 @@ cudaError_t launch_expand(GemmShape s, dim3 grid, const CUtensorMap& tm_aq, cons
                           const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
                           cudaStream_t st) {
     if (s == GemmShape::Wide)
-        mla_expand_kernel<256, 4><<<grid, kGemmThreads, WideL::BYTES, st>>>(tm_aq, tm_akv, tm_bq, tm_bkv, p);
-    else
-        mla_expand_kernel<64, 8><<<grid, kGemmThreads, NarrowL::BYTES, st>>>(tm_aq, tm_akv, tm_bq, tm_bkv, p);
-    return cudaGetLastError();
+        return launch_kernel(mla_expand_kernel<256, 4>, grid, dim3(kGemmThreads), WideL::BYTES, st, true,
+                             tm_aq, tm_akv, tm_bq, tm_bkv, p);
+    return launch_kernel(mla_expand_kernel<64, 4>, grid, dim3(kGemmThreads), NarrowL::BYTES, st, true,
+                         tm_aq, tm_akv, tm_bq, tm_bkv, p);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {

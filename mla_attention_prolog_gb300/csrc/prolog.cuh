@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace mlap {
 
 constexpr int kStatusPositionRange = 0x1;
@@ -71,11 +73,33 @@ struct QuantParams {
 };
 
 // Shapes of the GEMM kernel instantiations.
-// Expansion kernel: Wide = BN_MAX 256, 4 stages; Narrow = BN_MAX 64, 8 stages.
-// Compression kernel: Wide = BN_MAX 128, 6 stages; Narrow = BN_MAX 64, 8 stages.
+// Expansion kernel: Wide = BN_MAX 256, 4 stages; Narrow = BN_MAX 64, 4 stages.
+// Compression kernel: Wide = BN_MAX 128, 6 stages; Narrow = BN_MAX 64, 4 stages.
+// The narrow (decode) shapes use half the shared memory so that a compression
+// CTA and an expansion CTA fit on one SM and the expansion can start
+// streaming its weights while the compression is still running.
 enum class GemmShape { Wide, Narrow };
 int gemm_smem_bytes(GemmShape s);
 constexpr int kGemmThreads = 192;
+
+// Launches `kernel`; with `pdl` the launch may overlap the tail of the
+// previous kernel in the stream (programmatic dependent launch): the kernel
+// must call pdl_wait() before touching anything that kernel produced.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t gemm_set_attributes();
 cudaError_t launch_compress(GemmShape s, dim3 grid, const CUtensorMap& tm_x,
@@ -84,7 +108,7 @@ cudaError_t launch_expand(GemmShape s, dim3 grid, const CUtensorMap& tm_aq,
                           const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
                           const CUtensorMap& tm_bkv, const ExpandParams& p, cudaStream_t st);
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
-cudaError_t launch_quant(const QuantParams& p, cudaStream_t st);
+cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace mlap

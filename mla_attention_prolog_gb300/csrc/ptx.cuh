@@ -69,6 +69,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// ------------------------------------------------ programmatic dependent launch
+
+// Blocks the calling thread until the grids this grid depends on have
+// completed and their memory is visible (a no-op when the grid was launched
+// without a programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the dependent grid start launching (its CTAs then run their prologue
+// and block in pdl_wait() until this grid completes).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 // 2-D tiled bulk tensor load global -> shared, completion counted on `bar`.

@@ -17,35 +17,42 @@
 
 namespace mlap {
 
-constexpr int kNormWarps = 4;
+constexpr int kNormThreads = 256;
+constexpr int kNormWarps = kNormThreads / 32;
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sum of a per-thread value over the CTA in a fixed order (deterministic).
+__device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kNormWarps; ++w) s = __fadd_rn(s, red[w]);
+    return s;
 }
 
-__global__ void __launch_bounds__(kNormWarps * 32)
-    mla_norm_rope_kernel(const NormRopeParams p) {
-    extern __shared__ __align__(16) uint16_t norm_smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kNormWarps + warp;
-    if (t >= p.T) return;  // warp-uniform
+// One CTA per token.  Launched as a programmatic dependent of the compression
+// kernel: it waits for the partials, then lets the expansion kernel launch.
+__global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormRopeParams p) {
+    extern __shared__ __align__(16) uint16_t crow[];  // BF16 row of C [NA], then rotated k_pe [R]
+    __shared__ float red[2][kNormWarps];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int t = blockIdx.x, tid = threadIdx.x;
     const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, R = p.R, half = R / 2;
-    const int row_elems = NA + R;  // BF16 row of C, then the rotated k_pe
-    uint16_t* crow = norm_smem + static_cast<size_t>(warp) * row_elems;
     uint16_t* rot = crow + NA;
 
     const int pos = p.positions[t];
     const bool valid = pos >= 0 && pos < p.max_pos;
-    if (lane == 0 && p.amax) p.amax[t] = 0u;
-    if (!valid) {
-        if (lane == 0) atomicOr(p.status, kStatusPositionRange);
+    if (tid == 0 && p.amax) p.amax[t] = 0u;
+    uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
+    const int nchunk = R / 8;
+    if (!valid) {  // CTA-uniform
+        if (tid == 0) atomicOr(p.status, kStatusPositionRange);
         const uint4 z = make_uint4(0, 0, 0, 0);
-        uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
-        for (int i = lane * 8; i < Lq + Lkv; i += 256) *reinterpret_cast<uint4*>(nrow + i) = z;
-        const int nchunk = R / 8;
-        for (int k = lane; k < (p.H + 1) * nchunk; k += 32) {
+        for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) *reinterpret_cast<uint4*>(nrow + i) = z;
+        for (int k = tid; k < (p.H + 1) * nchunk; k += kNormThreads) {
             const int h = k / nchunk, c = k - h * nchunk;
             uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
                                     : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
@@ -54,17 +61,30 @@ __global__ void __launch_bounds__(kNormWarps * 32)
         return;
     }
 
-    // 1) Reduce the partials in split order, round to BF16, sum of squares / L.
+    // 1) Reduce the split-K partials in split order (TwoSum), round to BF16,
+    //    and accumulate x^2 / L of the c_q and c_kv blocks.
     float ssq_q = 0.0f, ssq_kv = 0.0f;
-    const size_t split_stride = static_cast<size_t>(p.T) * NA;
+    const size_t sstride = static_cast<size_t>(p.T) * NA;
     const float* prow = p.partials + static_cast<size_t>(t) * NA;
-    for (int i = lane * 4; i < NA; i += 128) {
+    for (int i = tid * 4; i < NA; i += kNormThreads * 4) {
         float4 a = *reinterpret_cast<const float4*>(prow + i);
         if (p.splits > 1) {
-            // split order is fixed; TwoSum keeps the reduction exact to FP32 rounding
             float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 1; s < p.splits; ++s) {
-                const float4 b = *reinterpret_cast<const float4*>(prow + s * split_stride + i);
+            int s = 1;
+            for (; s + 8 <= p.splits; s += 8) {  // eight loads in flight, then the ordered sums
+                float4 b[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) b[u] = *reinterpret_cast<const float4*>(prow + (s + u) * sstride + i);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    two_sum_add(a.x, c.x, b[u].x);
+                    two_sum_add(a.y, c.y, b[u].y);
+                    two_sum_add(a.z, c.z, b[u].z);
+                    two_sum_add(a.w, c.w, b[u].w);
+                }
+            }
+            for (; s < p.splits; ++s) {
+                const float4 b = *reinterpret_cast<const float4*>(prow + s * sstride + i);
                 two_sum_add(a.x, c.x, b.x);
                 two_sum_add(a.y, c.y, b.y);
                 two_sum_add(a.z, c.z, b.z);
@@ -83,17 +103,15 @@ __global__ void __launch_bounds__(kNormWarps * 32)
             for (int e = 0; e < 4; ++e) ssq_kv = __fadd_rn(ssq_kv, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lkv));
         }
     }
-    ssq_q = warp_sum(ssq_q);
-    ssq_kv = warp_sum(ssq_kv);
+    ssq_q = block_sum(ssq_q, red[0]);
+    ssq_kv = block_sum(ssq_kv, red[1]);  // its __syncthreads also publishes crow
     // Variant B of the pages' RMSNorm: std = sqrt(ms + eps), rstd = 1 / std,
     // both correctly rounded.
     const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
     const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
-    __syncwarp();
 
-    // 2) y = bf16((x * rstd) * gamma) for c_q and c_kv, 8 columns per lane.
-    uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
-    for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+    // 2) y = bf16((x * rstd) * gamma) for c_q and c_kv, 8 columns per thread.
+    for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) {
         const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
         const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma + i);
         const float rstd = i < Lq ? rstd_q : rstd_kv;
@@ -112,7 +130,7 @@ __global__ void __launch_bounds__(kNormWarps * 32)
     // 3) k_pe RoPE (rotate-half) in FP32 with this token's cos/sin row.
     const uint16_t* kp = crow + Lq + Lkv;
     const float* cs = p.cos_sin + static_cast<size_t>(pos) * R;
-    for (int i = lane; i < half; i += 32) {
+    for (int i = tid; i < half; i += kNormThreads) {
         const float x1 = __uint_as_float(static_cast<uint32_t>(kp[i]) << 16);
         const float x2 = __uint_as_float(static_cast<uint32_t>(kp[i + half]) << 16);
         const float c = cs[i], s = cs[half + i];
@@ -121,11 +139,10 @@ __global__ void __launch_bounds__(kNormWarps * 32)
         rot[i] = static_cast<uint16_t>(pack_bf16x2(o1, 0.0f) & 0xFFFFu);
         rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
     }
-    __syncwarp();
+    __syncthreads();
 
     // 4) out_kpe[t] and the shared rope slice of K for every head.
-    const int nchunk = R / 8;
-    for (int k = lane; k < (p.H + 1) * nchunk; k += 32) {
+    for (int k = tid; k < (p.H + 1) * nchunk; k += kNormThreads) {
         const int h = k / nchunk, c = k - h * nchunk;
         const uint4 v = *reinterpret_cast<const uint4*>(rot + c * 8);
         uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
@@ -139,6 +156,7 @@ __global__ void __launch_bounds__(kNormWarps * 32)
 constexpr int kQuantThreads = 256;
 
 __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantParams p) {
+    pdl_wait();
     const int row = blockIdx.x;
     const float* y = p.y + static_cast<size_t>(row) * p.row_len;
     const int n4 = p.row_len / 4;
@@ -168,6 +186,7 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
         return;
     }
     const float inv = __fdiv_rn(127.0f, amax);
+#pragma unroll 4
     for (int i = threadIdx.x; i < n4; i += kQuantThreads) {
         const float4 v = reinterpret_cast<const float4*>(y)[i];
         const float f[4] = {v.x, v.y, v.z, v.w};
@@ -187,16 +206,13 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
 
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
-    const int blocks = (p.T + kNormWarps - 1) / kNormWarps;
-    const size_t smem = static_cast<size_t>(kNormWarps) * (p.NA + p.R) * sizeof(uint16_t);
-    mla_norm_rope_kernel<<<blocks, kNormWarps * 32, smem, st>>>(p);
-    return cudaGetLastError();
+    const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
+    return launch_kernel(mla_norm_rope_kernel, dim3(p.T), dim3(kNormThreads), smem, st, true, p);
 }
 
-cudaError_t launch_quant(const QuantParams& p, cudaStream_t st) {
+cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
     if (p.rows == 0) return cudaSuccess;
-    mla_quant_kernel<<<p.rows, kQuantThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(mla_quant_kernel, dim3(p.rows), dim3(kQuantThreads), 0, st, pdl, p);
 }
 
 }  // namespace mlap
