@@ -213,6 +213,37 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
 #define MLA_TUNE_COMPRESS_GROUP 1
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
+/*
+ * mla_prolog_run() without a handle and without allocating device memory.
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that cannot call cudaMalloc, such as a plugin inside an inference runtime
+ * that reserves the whole device memory pool up front, or a latency-critical
+ * caller that cannot accept cudaMalloc's implicit synchronisation.
+ *
+ * Arguments and outputs are those of mla_prolog_run(), with the dims passed
+ * in directly.  The scratch that a handle keeps in its workspace is instead a
+ * static 32 MiB device array inside the library (each GPU that loads the
+ * library holds it until the process exits); dims whose workspace would not
+ * fit (split-K partials + normed rows + FP32 q rows + amax, i.e. decode-sized
+ * batches) are rejected with MLA_ERR_UNSUPPORTED_DIMS before anything runs.
+ * `status` (device int32, may be NULL) receives the run's device status word
+ * (MLA_STATUS_* bits).
+ *
+ * The first call on a device looks up the array's device address and sets
+ * the kernels' attributes; make that first call before any stream capture.
+ * All calls on one device share the array and it keeps the previous call's
+ * contents (this entry clears what must start at zero), so calls whose
+ * kernels overlap on one GPU -- e.g. on two streams -- race on it: order them
+ * on one stream.  No cudaMalloc, cudaFree or allocating library routine is
+ * called.  Errors: INVALID_ARG, UNSUPPORTED_DIMS, DEVICE, CUDA.
+ */
+int mla_prolog_run_noalloc(const mla_prolog_dims* dims,
+                           const void* x, const void* gamma, const void* W_a, const void* W_b,
+                           const int32_t* positions, const float* cos_sin,
+                           void* out_k, void* out_v, void* out_kpe,
+                           int8_t* out_q_int8, float* out_scale, int32_t* status,
+                           void* stream);
+
 /* Bytes of device workspace the handle holds. */
 int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes);
 

@@ -28,6 +28,7 @@ EXPORTED = [
     "mla_prolog_set_wait_timeout", "mla_prolog_selftest_wait_timeout",
     "mla_prolog_set_timing_events", "mla_prolog_kernel_count", "mla_prolog_kernel_name",
     "mla_prolog_workspace_bytes", "mla_prolog_schedule", "mla_prolog_copy_tap", "mla_prolog_set_tuning",
+    "mla_prolog_run_noalloc",
 ]
 TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
 TUNE_COMPRESS_GROUP = 1
@@ -79,6 +80,7 @@ def lib(path: Optional[str] = None):
     L.mla_prolog_schedule.argtypes = [V, P(I32), P(I32), P(I32), P(I32)]
     L.mla_prolog_copy_tap.argtypes = [V, I32, V, ctypes.c_size_t, V]
     L.mla_prolog_set_tuning.argtypes = [V, I32, I32]
+    L.mla_prolog_run_noalloc.argtypes = [P(MlaPrologDims)] + [V] * 13
     for n in EXPORTED:
         if n not in ("mla_prolog_strerror", "mla_prolog_last_cuda_error", "mla_prolog_kernel_count",
                      "mla_prolog_kernel_name"):
