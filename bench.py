@@ -213,8 +213,8 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
-    d = w.dims
-    inp = wl.make_inputs(w)
+    d = w.dims if not args.tokens else w.dims.with_T(args.tokens)
+    inp = wl.make_inputs(w, d)
     H, Dn, Dv, R = d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
 
     def bf(a, shape):
@@ -478,6 +478,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="v2lite_decode", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T of the workload (small profiling cases; not a bench line)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -211,6 +211,9 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  * Errors: INVALID_ARG (unknown key or value out of range).
  */
 #define MLA_TUNE_COMPRESS_GROUP 1
+/*   MLA_TUNE_COMPRESS_COMPENSATED  1: the drained chains are summed with
+ *                            error-free TwoSum; 0: with plain FP32 adds.   */
+#define MLA_TUNE_COMPRESS_COMPENSATED 2
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

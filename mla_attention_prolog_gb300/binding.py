@@ -32,6 +32,7 @@ EXPORTED = [
 ]
 TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
 TUNE_COMPRESS_GROUP = 1
+TUNE_COMPRESS_COMPENSATED = 2
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -70,7 +70,9 @@ struct mla_prolog {
     bool decode = false;
     GemmShape shape_a = GemmShape::Wide, shape_b = GemmShape::Wide;
     int bn_a = 0, splits_a = 1, bn_kv = 0, m_tiles = 0;
-    int group_a = 1;  // K blocks per tensor-core accumulation chain (compression)
+    int group_a = 1;      // K blocks per tensor-core accumulation chain (compression)
+    int compensated = 1;  // TwoSum accumulation of the drained chains
+    int sms = 0;
     // workspace
     void* ws = nullptr;
     size_t ws_bytes = 0;
@@ -151,6 +153,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->NKV = d.num_heads * (d.nope_dim + d.v_dim);
     h->m_tiles = cdiv(d.T, kBM);
     const int sms = prop.multiProcessorCount;
+    h->sms = sms;
 
     // Schedule: few token tiles -> decode (weights streamed by many narrow or
     // split-K tiles); otherwise prefill (wide tiles, tensor-core bound).
@@ -169,7 +172,11 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->bn_a = 128;
         h->splits_a = 1;
     }
-    h->group_a = h->decode ? 1 : 2;
+    // Accumulation chain length (K blocks) of the compression projection and
+    // TwoSum draining: measured on GB300 to keep INT8 code flips of the
+    // V3-shaped q path at 3-4.5e-4 (bar: 1e-3) at the lowest cost.
+    h->group_a = h->decode ? 2 : 4;
+    h->compensated = 1;
     // Expansion: prefill uses 256-wide kv tiles (one head of V2/V3); decode
     // without a q path uses the narrow kernel with enough tiles to cover the
     // SMs; decode with a q path shares the wide kernel with the q heads.
@@ -284,10 +291,22 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     };
 
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
-    CompressParams pa{h->partials, d.T,        h->NA,     h->bn_a,     cdiv(d.D, kBK),
-                      h->splits_a, h->group_a, h->status, h->timeout_ns};
-    dim3 ga(cdiv(h->NA, h->bn_a), h->m_tiles, h->splits_a);
-    if ((e = launch_compress(h->shape_a, ga, h->tm_x, h->tm_wa, pa, st)) != cudaSuccess)
+    CompressParams pa{};
+    pa.partials = h->partials;
+    pa.T = d.T;
+    pa.NA = h->NA;
+    pa.bn = h->bn_a;
+    pa.kb_total = cdiv(d.D, kBK);
+    pa.splits = h->splits_a;
+    pa.group = h->group_a;
+    pa.n_tiles = cdiv(h->NA, h->bn_a);
+    pa.m_tiles = h->m_tiles;
+    pa.compensated = h->compensated;
+    pa.status = h->status;
+    pa.timeout_ns = h->timeout_ns;
+    const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
+    if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
+        cudaSuccess)
         return cuda_fail(e, "launch mla_compress_kernel");
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
@@ -325,7 +344,10 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.NQ = h->NQ;
     pb.NKV = h->NKV;
     pb.nq_tiles = Lq > 0 ? d.num_heads : 0;
+    pb.nkv_tiles = cdiv(h->NKV, h->bn_kv);
     pb.bn_kv = h->bn_kv;
+    pb.m_tiles = h->m_tiles;
+    pb.group_n = 16;
     pb.kb_q = cdiv(Lq, kBK);
     pb.kb_kv = cdiv(Lkv, kBK);
     pb.positions = positions;
@@ -337,8 +359,9 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.amax = h->amax;
     pb.status = h->status;
     pb.timeout_ns = h->timeout_ns;
-    dim3 gb(pb.nq_tiles + cdiv(h->NKV, h->bn_kv), h->m_tiles);
-    if ((e = launch_expand(h->shape_b, gb, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb, st)) != cudaSuccess)
+    const int jobs_b = (pb.nq_tiles + pb.nkv_tiles) * pb.m_tiles;
+    if ((e = launch_expand(h->shape_b, jobs_b < h->sms ? jobs_b : h->sms, h->tm_nq, h->tm_nkv, h->tm_wqb,
+                           h->tm_wkvb, pb, st)) != cudaSuccess)
         return cuda_fail(e, "launch mla_expand_kernel");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
@@ -441,6 +464,10 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
         case MLA_TUNE_COMPRESS_GROUP:
             if (value < 1 || value > 64) return MLA_ERR_INVALID_ARG;
             h->group_a = value;
+            return MLA_OK;
+        case MLA_TUNE_COMPRESS_COMPENSATED:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            h->compensated = value;
             return MLA_OK;
         default: return MLA_ERR_INVALID_ARG;
     }

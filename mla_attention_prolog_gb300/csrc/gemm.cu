@@ -2,153 +2,195 @@
 // split-K partials) and the expansion projections (normed . W_b^T) with the
 // split / RoPE / assemble epilogue.
 //
-// One CTA computes one 128 x BN tile with six warps:
-//   warp 0     TMA producer: streams 128x64 A and BNx64 B tiles (128-byte
-//              swizzle) into a STAGES-deep shared-memory ring;
-//   warp 1     allocates the TMEM accumulator and issues tcgen05.mma
-//              (M = 128, N = BN, K = 16 per instruction) from one thread;
-//              each stage is released by tcgen05.commit on its "empty" barrier;
-//   warps 2-5  epilogue: after the final commit, each warp reads its 32 TMEM
-//              lanes (one token row per thread) with tcgen05.ld and stores.
+// Both kernels are persistent: a grid of at most one CTA per SM walks a
+// static list of jobs (128-row x BN-column output tiles, or K-slices of them)
+// with blockIdx.x, blockIdx.x + gridDim.x, ...  Roles inside a CTA:
+//   warp 0       TMA producer: streams 128x64 A and BNx64 B tiles (128-byte
+//                swizzle) into a STAGES-deep shared-memory ring;
+//   warp 1       allocates TMEM and issues tcgen05.mma (M = 128, N = BN,
+//                K = 16 per instruction) from one thread, committing each
+//                ring stage back to the producer;
+//   other warps  epilogue: read their 32 TMEM lanes (one token row per
+//                thread) with tcgen05.ld and finish the tile.
+// TMEM holds two accumulator buffers: the MMA warp fills one while the
+// epilogue drains the other, so a tile's epilogue overlaps the next tile's
+// main loop.  All three roles count ring slots and accumulator "chains" with
+// CTA-global counters, so the barrier phases follow from the counters alone.
+//
 // All waits are bounded (see ptx.cuh); a wait that gives up sets the status
-// word and the CTA still drains its copies and frees TMEM before leaving.
+// word, raises the CTA's abort flag, and the CTA still waits (bounded) for
+// its own copies and MMAs before freeing TMEM.
 #include "prolog.cuh"
 #include "ptx.cuh"
 
 namespace mlap {
 
 template <int BN_MAX, int STAGES>
-struct GemmLayout {
+struct Layout {
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN_MAX * kBK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int BARS = STAGES * STAGE;
-    static constexpr int MISC = BARS + (2 * STAGES + 1) * 8;
+    static constexpr int RING = STAGES * STAGE;
+    // full[S], empty[S], acc_full[2], acc_empty[2], mma_done
+    static constexpr int MISC = RING + (2 * STAGES + 5) * 8;
     static constexpr int BYTES = MISC + 16 + 1024;  // + slack to align the ring to 1 KB
-    static constexpr uint32_t TMEM_COLS = BN_MAX <= 32 ? 32 : BN_MAX <= 64 ? 64 : BN_MAX <= 128 ? 128 : 256;
+    static constexpr uint32_t TMEM_COLS =
+        2 * BN_MAX <= 32 ? 32 : 2 * BN_MAX <= 64 ? 64 : 2 * BN_MAX <= 128 ? 128 : 2 * BN_MAX <= 256 ? 256 : 512;
     static_assert(STAGE % 1024 == 0, "stages must keep 1 KB alignment for the swizzle atoms");
+    static_assert(2 * BN_MAX <= 512, "two accumulators must fit in TMEM");
 };
 
-struct TileJob {
-    const CUtensorMap* tmA;  // activations, K-major [rows, K]
-    const CUtensorMap* tmB;  // weights, K-major [N, K]
-    int a_row, b_row;        // first row of the A and B tiles
-    int kb0, nkb;            // first K block and number of K blocks (>= 1)
-    int bn;                  // tile width, multiple of 16, <= BN_MAX
+struct Smem {
+    uint32_t base;  // 1 KB aligned start of the ring
+    uint32_t full0, empty0, accf0, acce0, done;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
 };
 
-template <int BN_MAX, int STAGES, class Epilogue>
-__device__ __forceinline__ void gemm_tile(uint8_t* smem_raw, const TileJob& job,
-                                          uint64_t timeout_ns, int* status, const Epilogue& epi) {
-    using L = GemmLayout<BN_MAX, STAGES>;
-    const uint32_t raw = smem_u32(smem_raw);
+template <int BN_MAX, int STAGES>
+__device__ __forceinline__ Smem carve(uint8_t* raw_ptr) {
+    using L = Layout<BN_MAX, STAGES>;
+    const uint32_t raw = smem_u32(raw_ptr);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    const uint32_t base = raw + pad;
-    uint8_t* base_ptr = smem_raw + pad;
-    const uint32_t full0 = base + L::BARS;
-    const uint32_t empty0 = full0 + 8 * STAGES;
-    const uint32_t acc_full = empty0 + 8 * STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::MISC + 4);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Smem s;
+    s.base = raw + pad;
+    s.full0 = s.base + L::RING;
+    s.empty0 = s.full0 + 8 * STAGES;
+    s.accf0 = s.empty0 + 8 * STAGES;
+    s.acce0 = s.accf0 + 16;
+    s.done = s.acce0 + 16;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(raw_ptr + pad + L::MISC);
+    s.abort_flag = reinterpret_cast<volatile int*>(raw_ptr + pad + L::MISC + 4);
+    return s;
+}
 
+// Barrier init, TMEM allocation; returns the TMEM base address.
+template <int BN_MAX, int STAGES>
+__device__ __forceinline__ uint32_t gemm_setup(const Smem& sm, int epi_warps) {
+    using L = Layout<BN_MAX, STAGES>;
+    const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(sm.full0 + 8 * s, 1);
+            mbar_init(sm.empty0 + 8 * s, 1);
         }
-        mbar_init(acc_full, 1);
-        *abort_flag = 0;
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(sm.accf0 + 8 * b, 1);
+            mbar_init(sm.acce0 + 8 * b, epi_warps);
+        }
+        mbar_init(sm.done, 1);
+        *sm.abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_alloc(smem_u32(sm.tmem_slot), L::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    pdl_launch_dependents();
-    if (warp != 0) pdl_wait();  // the producer waits after its early weight loads
+    return *sm.tmem_slot;
+}
 
-    if (warp == 0) {
-        if (lane == 0) {
-            prefetch_tensormap(job.tmA);
-            prefetch_tensormap(job.tmB);
-            const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + job.bn * kBK * 2);
-            // The weights (B) do not depend on the previous kernel: stream the
-            // first ring of them before waiting for it, then the activations.
-            const int pre = job.nkb < STAGES ? job.nkb : STAGES;
-            for (int i = 0; i < pre; ++i) {
-                const uint32_t sa = base + i * L::STAGE;
-                mbar_arrive_expect_tx(full0 + 8 * i, tx);
-                tma_load_2d(sa + L::A_BYTES, job.tmB, full0 + 8 * i, (job.kb0 + i) * kBK, job.b_row);
-            }
-            pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(base + i * L::STAGE, job.tmA, full0 + 8 * i, (job.kb0 + i) * kBK, job.a_row);
-            int issued = pre;
-            bool ok = true;
-            for (int i = pre; i < job.nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                if (!mbar_wait(empty0 + 8 * s, ph ^ 1, timeout_ns, abort_flag)) { ok = false; break; }
-                const uint32_t sa = base + s * L::STAGE;
-                mbar_arrive_expect_tx(full0 + 8 * s, tx);
-                tma_load_2d(sa, job.tmA, full0 + 8 * s, (job.kb0 + i) * kBK, job.a_row);
-                tma_load_2d(sa + L::A_BYTES, job.tmB, full0 + 8 * s, (job.kb0 + i) * kBK, job.b_row);
-                ++issued;
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                atomicOr(status, kStatusWaitTimeout);
-            }
-            // No copy may still be landing in shared memory when the CTA leaves.
-            for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
-                mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, timeout_ns, nullptr);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kBM, job.bn);
-            bool ok = true;
-            for (int i = 0; i < job.nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                if (!mbar_wait(full0 + 8 * s, ph, timeout_ns, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t sa = base + s * L::STAGE;
-                const uint64_t ad = smem_desc_sw128(sa);
-                const uint64_t bd = smem_desc_sw128(sa + L::A_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes of K per instruction
-                    mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i | kk) != 0);
-                mma_commit(empty0 + 8 * s);
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                atomicOr(status, kStatusWaitTimeout);
-            }
-            mma_commit(acc_full);
-            // The accumulator must be complete before TMEM is released.
-            mbar_wait(acc_full, 0, timeout_ns, nullptr);
-        }
-    } else {
-        bool ok = mbar_wait(acc_full, 0, timeout_ns, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
-        if (ok) {
-            epi(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16), (warp & 3) * 32 + lane);
-        } else if (lane == 0) {
-            atomicOr(status, kStatusWaitTimeout);
-        }
-    }
+template <int BN_MAX, int STAGES>
+__device__ __forceinline__ void gemm_teardown(const Smem& sm, uint32_t tmem) {
+    using L = Layout<BN_MAX, STAGES>;
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if ((threadIdx.x >> 5) == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
     }
+}
+
+__device__ __forceinline__ void raise_abort(const Smem& sm, int* status) {
+    *sm.abort_flag = 1;
+    atomicOr(status, kStatusWaitTimeout);
+}
+
+// Producer: streams the nkb K blocks of one job.  `loads` counts ring slots
+// filled so far by this CTA (slot = loads % STAGES, pass = loads / STAGES).
+// With `weights_first` (the first job of a programmatic dependent launch,
+// ring still empty) the weight tiles of the first ring pass are issued before
+// waiting for the previous kernel, and the activation tiles after it.
+template <int BN_MAX, int STAGES>
+__device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, const CUtensorMap* tmA,
+                                            const CUtensorMap* tmB, int a_row, int b_row, int kb0, int nkb,
+                                            int bn, bool weights_first, uint64_t timeout_ns) {
+    using L = Layout<BN_MAX, STAGES>;
+    const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + bn * kBK * 2);
+    int i = 0;
+    if (weights_first) {
+        const int pre = nkb < STAGES ? nkb : STAGES;
+        for (int k = 0; k < pre; ++k) {
+            mbar_arrive_expect_tx(sm.full0 + 8 * k, tx);
+            tma_load_2d(sm.base + k * L::STAGE + L::A_BYTES, tmB, sm.full0 + 8 * k, (kb0 + k) * kBK, b_row);
+        }
+        pdl_wait();
+        for (int k = 0; k < pre; ++k)
+            tma_load_2d(sm.base + k * L::STAGE, tmA, sm.full0 + 8 * k, (kb0 + k) * kBK, a_row);
+        i = pre;
+        loads += pre;
+    }
+    for (; i < nkb; ++i, ++loads) {
+        const int s = loads % STAGES;
+        const uint32_t ph = (loads / STAGES) & 1;
+        if (!mbar_wait(sm.empty0 + 8 * s, ph ^ 1, timeout_ns, sm.abort_flag)) return false;
+        const uint32_t sa = sm.base + s * L::STAGE;
+        mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
+        tma_load_2d(sa, tmA, sm.full0 + 8 * s, (kb0 + i) * kBK, a_row);
+        tma_load_2d(sa + L::A_BYTES, tmB, sm.full0 + 8 * s, (kb0 + i) * kBK, b_row);
+    }
+    return true;
+}
+
+// No copy may still be landing in shared memory when the CTA leaves.
+template <int STAGES>
+__device__ __forceinline__ void drain_loads(const Smem& sm, uint32_t loads, uint64_t timeout_ns) {
+    for (uint32_t l = loads > STAGES ? loads - STAGES : 0; l < loads; ++l)
+        mbar_wait(sm.full0 + 8 * (l % STAGES), (l / STAGES) & 1, timeout_ns, nullptr);
+}
+
+// MMA issuer: one accumulation chain of nkb K blocks into TMEM buffer
+// (chain & 1), after the epilogue released that buffer's previous chain.
+template <int BN_MAX, int STAGES>
+__device__ __forceinline__ bool mma_chain(const Smem& sm, uint32_t& consumed, uint32_t chain, int nkb,
+                                          uint32_t tmem, uint32_t idesc, uint64_t timeout_ns) {
+    using L = Layout<BN_MAX, STAGES>;
+    const uint32_t b = chain & 1;
+    if (!mbar_wait(sm.acce0 + 8 * b, ((chain >> 1) & 1) ^ 1, timeout_ns, sm.abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t dacc = tmem + b * BN_MAX;
+    for (int i = 0; i < nkb; ++i, ++consumed) {
+        const int s = consumed % STAGES;
+        const uint32_t ph = (consumed / STAGES) & 1;
+        if (!mbar_wait(sm.full0 + 8 * s, ph, timeout_ns, sm.abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sa = sm.base + s * L::STAGE;
+        const uint64_t ad = smem_desc_sw128(sa);
+        const uint64_t bd = smem_desc_sw128(sa + L::A_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes of K per instruction
+            mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (i == 0 && kk == 0) ? 0u : 1u);
+        mma_commit(sm.empty0 + 8 * s);
+    }
+    mma_commit(sm.accf0 + 8 * b);
+    return true;
+}
+
+// Epilogue side of a chain: wait for it (warp-uniform result) ...
+__device__ __forceinline__ bool epi_acquire(const Smem& sm, uint32_t chain, uint64_t timeout_ns) {
+    bool got = mbar_wait(sm.accf0 + 8 * (chain & 1), (chain >> 1) & 1, timeout_ns, sm.abort_flag);
+    got = __all_sync(0xffffffffu, got);
+    tc_fence_after();
+    return got;
+}
+
+// ... and hand the buffer back to the MMA warp (one arrival per warp).
+__device__ __forceinline__ void epi_release(const Smem& sm, uint32_t chain) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(sm.acce0 + 8 * (chain & 1));
 }
 
 // ------------------------------------------------------- compression (x W_a^T)
@@ -160,22 +202,8 @@ __device__ __forceinline__ void gemm_tile(uint8_t* smem_raw, const TileJob& job,
 // output is rounded to BF16 and then feeds the RMSNorm, the q projection and
 // the per-token INT8 codes, so this kernel keeps every tensor-core chain
 // short: the MMA warp restarts a fresh TMEM accumulator every `group` K
-// blocks (two TMEM buffers in turn), and the epilogue warps drain each chain
-// into registers with error-free TwoSum accumulation while the next chain is
-// being computed.
-
-template <int BN_MAX, int STAGES>
-struct DrainLayout {
-    static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BN_MAX * kBK * 2;
-    static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int BARS = STAGES * STAGE;
-    // full[S], empty[S], acc_full[2], acc_empty[2], mma_done
-    static constexpr int MISC = BARS + (2 * STAGES + 5) * 8;
-    static constexpr int BYTES = MISC + 16 + 1024;
-    static constexpr uint32_t TMEM_COLS = 2 * BN_MAX <= 64 ? 64 : 2 * BN_MAX <= 128 ? 128 : 2 * BN_MAX <= 256 ? 256 : 512;
-    static_assert(STAGE % 1024 == 0, "stages must keep 1 KB alignment for the swizzle atoms");
-};
+// blocks, and the epilogue warps drain each chain into registers (TwoSum
+// error-free accumulation, or plain FP32 adds) while the next chain runs.
 
 constexpr int kDrainEpiWarps = 8;  // two warps per TMEM lane quarter, one per column half
 constexpr int kCompressThreads = 64 + 32 * kDrainEpiWarps;
@@ -184,167 +212,214 @@ template <int BN_MAX, int STAGES>
 __global__ void __launch_bounds__(kCompressThreads, 1)
     mla_compress_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const __grid_constant__ CUtensorMap tm_wa, const CompressParams p) {
-    using L = DrainLayout<BN_MAX, STAGES>;
     constexpr int HALF = BN_MAX / 2;  // columns per epilogue thread
     extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    const uint32_t base = raw + pad;
-    uint8_t* base_ptr = smem_raw + pad;
-    const uint32_t full0 = base + L::BARS;
-    const uint32_t empty0 = full0 + 8 * STAGES;
-    const uint32_t accf0 = empty0 + 8 * STAGES;  // acc_full[2]
-    const uint32_t acce0 = accf0 + 16;           // acc_empty[2]
-    const uint32_t mma_done = acce0 + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + L::MISC);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + L::MISC + 4);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    const int n0 = blockIdx.x * p.bn;
-    const int m0 = blockIdx.y * kBM;
-    const int split = blockIdx.z;
-    const int kb0 = split * p.kb_total / p.splits;
-    const int nkb = (split + 1) * p.kb_total / p.splits - kb0;
-    const int group = p.group;
-    const int ngroups = (nkb + group - 1) / group;
-    const uint64_t timeout_ns = p.timeout_ns;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(accf0 + 8 * b, 1);
-            mbar_init(acce0 + 8 * b, kDrainEpiWarps);
-        }
-        mbar_init(mma_done, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const Smem sm = carve<BN_MAX, STAGES>(smem_raw);
+    const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kDrainEpiWarps);
     pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_m = p.n_tiles * p.splits;
+    const int njobs = p.m_tiles * per_m;
+    const int group = p.group;
+    auto job_of = [&](int j, int& m0, int& n0, int& split, int& kb0, int& nkb) {
+        const int m = j / per_m, r = j - m * per_m;
+        const int n = r / p.splits;
+        split = r - n * p.splits;
+        m0 = m * kBM;
+        n0 = n * p.bn;
+        kb0 = split * p.kb_total / p.splits;
+        nkb = (split + 1) * p.kb_total / p.splits - kb0;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tensormap(&tm_x);
             prefetch_tensormap(&tm_wa);
-            const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + p.bn * kBK * 2);
-            int issued = 0;
-            bool ok = true;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % STAGES;
-                const uint32_t ph = (i / STAGES) & 1;
-                if (!mbar_wait(empty0 + 8 * s, ph ^ 1, timeout_ns, abort_flag)) { ok = false; break; }
-                const uint32_t sa = base + s * L::STAGE;
-                mbar_arrive_expect_tx(full0 + 8 * s, tx);
-                tma_load_2d(sa, &tm_x, full0 + 8 * s, (kb0 + i) * kBK, m0);
-                tma_load_2d(sa + L::A_BYTES, &tm_wa, full0 + 8 * s, (kb0 + i) * kBK, n0);
-                ++issued;
+            uint32_t loads = 0;
+            for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
+                int m0, n0, split, kb0, nkb;
+                job_of(j, m0, n0, split, kb0, nkb);
+                if (!produce_job<BN_MAX, STAGES>(sm, loads, &tm_x, &tm_wa, m0, n0, kb0, nkb, p.bn, false,
+                                                 p.timeout_ns)) {
+                    raise_abort(sm, p.status);
+                    break;
+                }
             }
-            if (!ok) {
-                *abort_flag = 1;
-                atomicOr(p.status, kStatusWaitTimeout);
-            }
-            for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
-                mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, timeout_ns, nullptr);
+            drain_loads<STAGES>(sm, loads, p.timeout_ns);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
+            uint32_t consumed = 0, chain = 0;
             bool ok = true;
-            int i = 0;
-            for (int g = 0; g < ngroups && ok; ++g) {
-                const int b = g & 1;
-                // wait until the epilogue drained this buffer's previous chain
-                if (!mbar_wait(acce0 + 8 * b, ((g >> 1) & 1) ^ 1, timeout_ns, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t dacc = tmem + static_cast<uint32_t>(b * BN_MAX);
-                const int iend = (g + 1) * group < nkb ? (g + 1) * group : nkb;
-                for (int first = 1; i < iend; ++i, first = 0) {
-                    const int s = i % STAGES;
-                    const uint32_t ph = (i / STAGES) & 1;
-                    if (!mbar_wait(full0 + 8 * s, ph, timeout_ns, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t sa = base + s * L::STAGE;
-                    const uint64_t ad = smem_desc_sw128(sa);
-                    const uint64_t bd = smem_desc_sw128(sa + L::A_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (first && kk == 0) ? 0u : 1u);
-                    mma_commit(empty0 + 8 * s);
-                }
-                if (ok) mma_commit(accf0 + 8 * b);
+            for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x) {
+                int m0, n0, split, kb0, nkb;
+                job_of(j, m0, n0, split, kb0, nkb);
+                for (int k = 0; k < nkb && ok; k += group, ++chain)
+                    ok = mma_chain<BN_MAX, STAGES>(sm, consumed, chain, nkb - k < group ? nkb - k : group, tmem,
+                                                   idesc, p.timeout_ns);
             }
-            if (!ok) {
-                *abort_flag = 1;
-                atomicOr(p.status, kStatusWaitTimeout);
-            }
+            if (!ok) raise_abort(sm, p.status);
             // Every issued MMA must have finished before TMEM is released.
-            mma_commit(mma_done);
-            mbar_wait(mma_done, 0, timeout_ns, nullptr);
+            mma_commit(sm.done);
+            mbar_wait(sm.done, 0, p.timeout_ns, nullptr);
         }
     } else {
         const int ew = warp - 2;
-        const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-        const int half = ew >> 2;                 // column half
+        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int half = ew >> 2;      // column half
         const int row = quarter * 32 + lane;
-        const int t = m0 + row;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        float acc[HALF], cmp[HALF];
-#pragma unroll
-        for (int j = 0; j < HALF; ++j) acc[j] = cmp[j] = 0.0f;
+        uint32_t chain = 0;
         bool ok = true;
-        for (int g = 0; g < ngroups; ++g) {
-            const int b = g & 1;
-            bool got = mbar_wait(accf0 + 8 * b, (g >> 1) & 1, timeout_ns, abort_flag);
-            got = __all_sync(0xffffffffu, got);
-            if (!got) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t src = tmem + lane_off + static_cast<uint32_t>(b * BN_MAX + half * HALF);
+        for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x) {
+            int m0, n0, split, kb0, nkb;
+            job_of(j, m0, n0, split, kb0, nkb);
+            float acc[HALF], cmp[HALF];
 #pragma unroll
-            for (int j = 0; j < HALF; j += 16) {
-                if (half * HALF + j < p.bn) {  // warp-uniform
-                    float v[16];
-                    tmem_ld16(src + j, v);
+            for (int c = 0; c < HALF; ++c) acc[c] = cmp[c] = 0.0f;
+            for (int k = 0; k < nkb; k += group, ++chain) {
+                if (!epi_acquire(sm, chain, p.timeout_ns)) { ok = false; break; }
+                const uint32_t src = tmem + lane_off + (chain & 1) * BN_MAX + half * HALF;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) two_sum_add(acc[j + e], cmp[j + e], v[e]);
+                for (int c = 0; c < HALF; c += 16) {
+                    if (half * HALF + c < p.bn) {  // warp-uniform
+                        float v[16];
+                        tmem_ld16(src + c, v);
+                        if (p.compensated) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) two_sum_add(acc[c + e], cmp[c + e], v[e]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) acc[c + e] = __fadd_rn(acc[c + e], v[e]);
+                        }
+                    }
+                }
+                epi_release(sm, chain);
+            }
+            if (!ok) break;
+            const int t = m0 + row;
+            if (t < p.T) {
+                float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
+#pragma unroll
+                for (int c = 0; c < HALF; c += 4) {
+                    if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA)
+                        *reinterpret_cast<float4*>(dst + c) =
+                            make_float4(__fadd_rn(acc[c], cmp[c]), __fadd_rn(acc[c + 1], cmp[c + 1]),
+                                        __fadd_rn(acc[c + 2], cmp[c + 2]), __fadd_rn(acc[c + 3], cmp[c + 3]));
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce0 + 8 * b);
         }
-        if (!ok) {
-            if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
-        } else if (t < p.T) {
-            float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
-#pragma unroll
-            for (int j = 0; j < HALF; j += 4) {
-                const int col = n0 + half * HALF + j;
-                if (half * HALF + j < p.bn && col < p.NA)
-                    *reinterpret_cast<float4*>(dst + j) =
-                        make_float4(__fadd_rn(acc[j], cmp[j]), __fadd_rn(acc[j + 1], cmp[j + 1]),
-                                    __fadd_rn(acc[j + 2], cmp[j + 2]), __fadd_rn(acc[j + 3], cmp[j + 3]));
-            }
-        }
+        if (!ok && lane == 0) atomicOr(p.status, kStatusWaitTimeout);
     }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, L::TMEM_COLS);
-    }
+    gemm_teardown<BN_MAX, STAGES>(sm, tmem);
 }
 
 // -------------------------------------------------- expansion (normed W_b^T)
+
+constexpr int kExpandEpiWarps = 4;
+
+// Job j -> (tile, token tile).  Tiles [0, nq_tiles) are q heads, the rest kv
+// tiles.  Jobs go through the tiles in groups of group_n: all token tiles of
+// a group before the next group, so the weights of a group stay in L2 while
+// every token tile passes through them.
+__device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& tile, int& m_tile) {
+    const int ntiles = p.nq_tiles + p.nkv_tiles;
+    const int per_group = p.group_n * p.m_tiles;
+    const int g = j / per_group, r = j - g * per_group;
+    const int gw = ntiles - g * p.group_n < p.group_n ? ntiles - g * p.group_n : p.group_n;
+    m_tile = r / gw;
+    tile = g * p.group_n + (r - m_tile * gw);
+}
+
+// q head h of token rows [m0, m0+128): FP32 q, RoPE of its rope slice, per-token max |q|.
+__device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, int row, int m0, int h) {
+    const int Dn = p.Dn, R = p.R;
+    const int t = m0 + row;
+    const bool in = t < p.T;
+    const int pos = in ? p.positions[t] : 0;
+    const bool valid = in && pos >= 0 && pos < p.max_pos;
+    float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * (Dn + R);
+    float amax = 0.0f;
+    for (int c = 0; c < Dn; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        if (in) {
+            float4* d4 = reinterpret_cast<float4*>(qrow + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 o = valid ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3])
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
+                d4[q] = o;
+            }
+        }
+    }
+    const int half = R / 2;
+    const float* cs = p.cos_sin + static_cast<size_t>(valid ? pos : 0) * R;
+    for (int i = 0; i < half; i += 8) {
+        float a[8], b[8];
+        tmem_ld8(tbase + Dn + i, a);
+        tmem_ld8(tbase + Dn + half + i, b);
+        if (in) {
+            float o1[8], o2[8];
+            if (valid) {
+                const float4 c0 = *reinterpret_cast<const float4*>(cs + i);
+                const float4 c1 = *reinterpret_cast<const float4*>(cs + i + 4);
+                const float4 s0 = *reinterpret_cast<const float4*>(cs + half + i);
+                const float4 s1 = *reinterpret_cast<const float4*>(cs + half + i + 4);
+                const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    // x*cos + rotate_half(x)*sin, rotate_half(x1, x2) = (-x2, x1)
+                    o1[e] = __fadd_rn(__fmul_rn(a[e], cc[e]), __fmul_rn(-b[e], ss[e]));
+                    o2[e] = __fadd_rn(__fmul_rn(b[e], cc[e]), __fmul_rn(a[e], ss[e]));
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
+            float4* d1 = reinterpret_cast<float4*>(qrow + Dn + i);
+            float4* d2 = reinterpret_cast<float4*>(qrow + Dn + half + i);
+            d1[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
+            d1[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
+            d2[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
+            d2[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
+        }
+    }
+    // |q| >= 0, so the order of the float bit patterns is the order of the values.
+    if (valid) atomicMax(p.amax + t, __float_as_uint(amax));
+}
+
+// kv columns [n0, n0 + bn) of [T, H, Dn + Dv]: k_nope into K's first Dn
+// columns, value into out_v, both BF16.
+__device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32_t tbase, int row, int m0, int n0) {
+    const int Dn = p.Dn, R = p.R, HD = p.Dn + p.Dv;
+    const int t = m0 + row;
+    const bool in = t < p.T;
+    const int pos = in ? p.positions[t] : 0;
+    const bool valid = in && pos >= 0 && pos < p.max_pos;
+    for (int c = 0; c < p.bn_kv; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        const int n = n0 + c;
+        if (in && n < p.NKV) {
+            const int h = n / HD;
+            const int j = n - h * HD;
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
+            uint16_t* dst = j < Dn ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (Dn + R) + j
+                                   : p.out_v + (static_cast<size_t>(t) * p.H + h) * p.Dv + (j - Dn);
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+}
 
 template <int BN_MAX, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -352,107 +427,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                       const __grid_constant__ CUtensorMap tm_akv,
                       const __grid_constant__ CUtensorMap tm_bq,
                       const __grid_constant__ CUtensorMap tm_bkv, const ExpandParams p) {
-    extern __shared__ uint8_t smem[];
-    const int m0 = blockIdx.y * kBM;
-    const int tile = blockIdx.x;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve<BN_MAX, STAGES>(smem_raw);
+    const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kExpandEpiWarps);
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp != 0) pdl_wait();  // the producer waits after its first weight tiles
+    const int njobs = (p.nq_tiles + p.nkv_tiles) * p.m_tiles;
     const int Dn = p.Dn, R = p.R;
 
-    if (tile < p.nq_tiles) {
-        // q head h: FP32 q, RoPE on its rope slice, per-token running max |q|.
-        const int h = tile;
-        const TileJob job{&tm_aq, &tm_bq, m0, h * (Dn + R), 0, p.kb_q, Dn + R};
-        gemm_tile<BN_MAX, STAGES>(smem, job, p.timeout_ns, p.status,
-            [&](uint32_t tbase, int row) {
-                const int t = m0 + row;
-                const bool in = t < p.T;
-                const int pos = in ? p.positions[t] : 0;
-                const bool valid = in && pos >= 0 && pos < p.max_pos;
-                float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * (Dn + R);
-                float amax = 0.0f;
-                for (int c = 0; c < Dn; c += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + c, v);
-                    if (in) {
-                        float4* d4 = reinterpret_cast<float4*>(qrow + c);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            float4 o = valid ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3])
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
-                            d4[q] = o;
-                        }
-                    }
-                }
-                const int half = R / 2;
-                const float* cs = p.cos_sin + static_cast<size_t>(valid ? pos : 0) * R;
-                for (int i = 0; i < half; i += 8) {
-                    float a[8], b[8];
-                    tmem_ld8(tbase + Dn + i, a);
-                    tmem_ld8(tbase + Dn + half + i, b);
-                    if (in) {
-                        float o1[8], o2[8];
-                        if (valid) {
-                            const float4 c0 = *reinterpret_cast<const float4*>(cs + i);
-                            const float4 c1 = *reinterpret_cast<const float4*>(cs + i + 4);
-                            const float4 s0 = *reinterpret_cast<const float4*>(cs + half + i);
-                            const float4 s1 = *reinterpret_cast<const float4*>(cs + half + i + 4);
-                            const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                            const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                // x*cos + rotate_half(x)*sin, rotate_half(x1, x2) = (-x2, x1)
-                                o1[e] = __fadd_rn(__fmul_rn(a[e], cc[e]), __fmul_rn(-b[e], ss[e]));
-                                o2[e] = __fadd_rn(__fmul_rn(b[e], cc[e]), __fmul_rn(a[e], ss[e]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
-                        float4* d1 = reinterpret_cast<float4*>(qrow + Dn + i);
-                        float4* d2 = reinterpret_cast<float4*>(qrow + Dn + half + i);
-                        d1[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
-                        d1[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
-                        d2[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
-                        d2[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
-                    }
-                }
-                // |q| >= 0, so the order of the float bit patterns is the order of the values.
-                if (valid) atomicMax(p.amax + t, __float_as_uint(amax));
-            });
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tensormap(&tm_aq);
+            prefetch_tensormap(&tm_akv);
+            prefetch_tensormap(&tm_bq);
+            prefetch_tensormap(&tm_bkv);
+            uint32_t loads = 0;
+            bool ok = true;
+            for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
+                int tile, m;
+                expand_job(p, j, tile, m);
+                const bool first = j == static_cast<int>(blockIdx.x);
+                ok = tile < p.nq_tiles
+                         ? produce_job<BN_MAX, STAGES>(sm, loads, &tm_aq, &tm_bq, m * kBM, tile * (Dn + R), 0,
+                                                       p.kb_q, Dn + R, first, p.timeout_ns)
+                         : produce_job<BN_MAX, STAGES>(sm, loads, &tm_akv, &tm_bkv, m * kBM,
+                                                       (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
+                                                       p.timeout_ns);
+                if (!ok) break;
+            }
+            if (loads == 0) pdl_wait();
+            if (!ok) raise_abort(sm, p.status);
+            drain_loads<STAGES>(sm, loads, p.timeout_ns);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc_q = idesc_bf16_f32(kBM, Dn + R);
+            const uint32_t idesc_kv = idesc_bf16_f32(kBM, p.bn_kv);
+            uint32_t consumed = 0, chain = 0;
+            bool ok = true;
+            for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x, ++chain) {
+                int tile, m;
+                expand_job(p, j, tile, m);
+                const bool q = tile < p.nq_tiles;
+                ok = mma_chain<BN_MAX, STAGES>(sm, consumed, chain, q ? p.kb_q : p.kb_kv, tmem,
+                                               q ? idesc_q : idesc_kv, p.timeout_ns);
+            }
+            if (!ok) raise_abort(sm, p.status);
+            mma_commit(sm.done);
+            mbar_wait(sm.done, 0, p.timeout_ns, nullptr);
+        }
     } else {
-        // kv tile: columns [n0, n0 + bn_kv) of [T, H, Dn + Dv]; split into
-        // k_nope (into K's first Dn columns) and value.
-        const int n0 = (tile - p.nq_tiles) * p.bn_kv;
-        const TileJob job{&tm_akv, &tm_bkv, m0, n0, 0, p.kb_kv, p.bn_kv};
-        const int HD = Dn + p.Dv;
-        gemm_tile<BN_MAX, STAGES>(smem, job, p.timeout_ns, p.status,
-            [&](uint32_t tbase, int row) {
-                const int t = m0 + row;
-                const bool in = t < p.T;
-                const int pos = in ? p.positions[t] : 0;
-                const bool valid = in && pos >= 0 && pos < p.max_pos;
-                for (int c = 0; c < p.bn_kv; c += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + c, v);
-                    const int n = n0 + c;
-                    if (in && n < p.NKV) {
-                        const int h = n / HD;
-                        const int j = n - h * HD;
-                        uint32_t w[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w[e] = valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
-                        uint16_t* dst = j < Dn
-                            ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (Dn + R) + j
-                            : p.out_v + (static_cast<size_t>(t) * p.H + h) * p.Dv + (j - Dn);
-                        uint4* d4 = reinterpret_cast<uint4*>(dst);
-                        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
-                }
-            });
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t chain = 0;
+        for (int j = blockIdx.x; j < njobs; j += gridDim.x, ++chain) {
+            int tile, m;
+            expand_job(p, j, tile, m);
+            if (!epi_acquire(sm, chain, p.timeout_ns)) {
+                if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
+                break;
+            }
+            const uint32_t tbase = tmem + lane_off + (chain & 1) * BN_MAX;
+            if (tile < p.nq_tiles)
+                expand_q_epilogue(p, tbase, row, m * kBM, tile);
+            else
+                expand_kv_epilogue(p, tbase, row, m * kBM, (tile - p.nq_tiles) * p.bn_kv);
+            epi_release(sm, chain);
+        }
     }
+    gemm_teardown<BN_MAX, STAGES>(sm, tmem);
 }
 
 // ------------------------------------------------------------ self-test
@@ -471,39 +516,47 @@ __global__ void mla_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 // ------------------------------------------------------------ launchers
 
-using WideL = GemmLayout<256, 4>;
-using NarrowL = GemmLayout<64, 4>;
-using CWideL = DrainLayout<128, 6>;
-using CNarrowL = DrainLayout<64, 4>;
+using EWide = Layout<256, 4>;
+using ENarrow = Layout<64, 4>;
+using CWide = Layout<128, 6>;
+using CNarrow = Layout<64, 4>;
 
-int gemm_smem_bytes(GemmShape s) { return s == GemmShape::Wide ? WideL::BYTES : NarrowL::BYTES; }
+int gemm_smem_bytes(GemmShape s) { return s == GemmShape::Wide ? EWide::BYTES : ENarrow::BYTES; }
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, CWideL::BYTES))) return e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, CNarrowL::BYTES))) return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, WideL::BYTES))) return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, NarrowL::BYTES))) return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  CWide::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  CNarrow::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  EWide::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  ENarrow::BYTES)))
+        return e;
     return cudaSuccess;
 }
 
-cudaError_t launch_compress(GemmShape s, dim3 grid, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
+cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
                             const CompressParams& p, cudaStream_t st) {
     if (s == GemmShape::Wide)
-        mla_compress_kernel<128, 6><<<grid, kCompressThreads, CWideL::BYTES, st>>>(tm_x, tm_wa, p);
-    else
-        mla_compress_kernel<64, 4><<<grid, kCompressThreads, CNarrowL::BYTES, st>>>(tm_x, tm_wa, p);
-    return cudaGetLastError();
+        return launch_kernel(mla_compress_kernel<128, 6>, dim3(grid), dim3(kCompressThreads), CWide::BYTES, st,
+                             false, tm_x, tm_wa, p);
+    return launch_kernel(mla_compress_kernel<64, 4>, dim3(grid), dim3(kCompressThreads), CNarrow::BYTES, st, false,
+                         tm_x, tm_wa, p);
 }
 
-cudaError_t launch_expand(GemmShape s, dim3 grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
+cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
                           const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
                           cudaStream_t st) {
     if (s == GemmShape::Wide)
-        return launch_kernel(mla_expand_kernel<256, 4>, grid, dim3(kGemmThreads), WideL::BYTES, st, true,
+        return launch_kernel(mla_expand_kernel<256, 4>, dim3(grid), dim3(kGemmThreads), EWide::BYTES, st, true,
                              tm_aq, tm_akv, tm_bq, tm_bkv, p);
-    return launch_kernel(mla_expand_kernel<64, 4>, grid, dim3(kGemmThreads), NarrowL::BYTES, st, true,
-                         tm_aq, tm_akv, tm_bq, tm_bkv, p);
+    return launch_kernel(mla_expand_kernel<64, 4>, dim3(grid), dim3(kGemmThreads), ENarrow::BYTES, st, true, tm_aq,
+                         tm_akv, tm_bq, tm_bkv, p);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {

@@ -125,7 +125,7 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
         shape_a = GemmShape::Wide;
         bn_a = 128;
     }
-    group_a = decode ? 1 : 2;
+    group_a = decode ? 2 : 4;
     if (!decode) {
         shape_b = GemmShape::Wide;
         bn_kv = 256;
@@ -193,8 +193,21 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     // overwritten in full and amax is cleared by the norm kernel.
     if (cudaMemsetAsync(dstatus, 0, sizeof(int), st) != cudaSuccess) return set_error("cudaMemsetAsync");
 
-    CompressParams pa{partials, d.T, NA, bn_a, kb_a, splits_a, group_a, dstatus, timeout_ns};
-    if (launch_compress(shape_a, dim3(cdiv(NA, bn_a), m_tiles, splits_a), tm_x, tm_wa, pa, st) != cudaSuccess)
+    CompressParams pa{};
+    pa.partials = partials;
+    pa.T = d.T;
+    pa.NA = NA;
+    pa.bn = bn_a;
+    pa.kb_total = kb_a;
+    pa.splits = splits_a;
+    pa.group = group_a;
+    pa.n_tiles = cdiv(NA, bn_a);
+    pa.m_tiles = m_tiles;
+    pa.compensated = 1;
+    pa.status = dstatus;
+    pa.timeout_ns = timeout_ns;
+    const int jobs_a = pa.n_tiles * m_tiles * splits_a;
+    if (launch_compress(shape_a, jobs_a < sms ? jobs_a : sms, tm_x, tm_wa, pa, st) != cudaSuccess)
         return set_error("launch mla_compress_kernel");
 
     NormRopeParams pn{};
@@ -230,7 +243,10 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.NQ = NQ;
     pb.NKV = NKV;
     pb.nq_tiles = Lq > 0 ? H : 0;
+    pb.nkv_tiles = cdiv(NKV, bn_kv);
     pb.bn_kv = bn_kv;
+    pb.m_tiles = m_tiles;
+    pb.group_n = 16;
     pb.kb_q = cdiv(Lq, kBK);
     pb.kb_kv = cdiv(Lkv, kBK);
     pb.positions = positions;
@@ -242,8 +258,8 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.amax = amax;
     pb.status = dstatus;
     pb.timeout_ns = timeout_ns;
-    if (launch_expand(shape_b, dim3(pb.nq_tiles + cdiv(NKV, bn_kv), m_tiles), tm_nq, tm_nkv, tm_wqb, tm_wkvb, pb,
-                      st) != cudaSuccess)
+    const int jobs_b = (pb.nq_tiles + pb.nkv_tiles) * m_tiles;
+    if (launch_expand(shape_b, jobs_b < sms ? jobs_b : sms, tm_nq, tm_nkv, tm_wqb, tm_wkvb, pb, st) != cudaSuccess)
         return set_error("launch mla_expand_kernel");
     if (Lq > 0) {
         QuantParams pq{qws, amax, d.T, NQ, out_q_int8, out_scale};

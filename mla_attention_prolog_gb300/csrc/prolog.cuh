@@ -17,14 +17,16 @@ constexpr int kBM = 128;  // MMA M: token rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;   // K per pipeline stage: one 128-byte swizzle atom of BF16
 
 // Compression projection: partial[split][t][n] = sum over the split's K range
-// of x[t, k] * W_a[n, k]  (FP32, one split per blockIdx.z).
+// of x[t, k] * W_a[n, k] (FP32).  Jobs: m_tiles x n_tiles x splits.
 struct CompressParams {
     float* partials;  // [splits][T][NA]
     int T, NA;
-    int bn;        // tile width over the NA weight rows
-    int kb_total;  // K blocks of 64 over D
-    int splits;    // split-K factor
-    int group;     // K blocks per tensor-core accumulation chain (>= 1)
+    int bn;           // tile width over the NA weight rows
+    int kb_total;     // K blocks of 64 over D
+    int splits;       // split-K factor
+    int group;        // K blocks per tensor-core accumulation chain (>= 1)
+    int n_tiles, m_tiles;
+    int compensated;  // drained chains summed with TwoSum (1) or plain FP32 adds (0)
     int* status;
     uint64_t timeout_ns;
 };
@@ -51,7 +53,8 @@ struct NormRopeParams {
 struct ExpandParams {
     int T, H, Dn, Dv, R;
     int NQ, NKV;
-    int nq_tiles, bn_kv;
+    int nq_tiles, nkv_tiles, bn_kv;
+    int m_tiles, group_n;  // token tiles; weight tiles per L2 group of the job order
     int kb_q, kb_kv;
     const int32_t* positions;
     const float* cos_sin;
@@ -102,9 +105,9 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 }
 
 cudaError_t gemm_set_attributes();
-cudaError_t launch_compress(GemmShape s, dim3 grid, const CUtensorMap& tm_x,
+cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x,
                             const CUtensorMap& tm_wa, const CompressParams& p, cudaStream_t st);
-cudaError_t launch_expand(GemmShape s, dim3 grid, const CUtensorMap& tm_aq,
+cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq,
                           const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
                           const CUtensorMap& tm_bkv, const ExpandParams& p, cudaStream_t st);
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
