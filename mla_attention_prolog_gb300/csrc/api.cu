@@ -4,7 +4,10 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <new>
+#include <utility>
+#include <vector>
 
 #include "../../include/mla_prolog.h"
 #include "prolog.cuh"
@@ -81,6 +84,8 @@ struct mla_prolog {
     float* qws = nullptr;
     uint32_t* amax = nullptr;
     int* status = nullptr;
+    int* job_table = nullptr;  // balanced expansion job lists (decode)
+    int expand_grid = 0;
     uint64_t timeout_ns = 1000000000ull;
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wqb{}, tm_wkvb{};
@@ -160,8 +165,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->decode = h->m_tiles <= 2;
     const int kb_a = cdiv(d.D, kBK);
     if (h->decode) {
-        h->shape_a = GemmShape::Narrow;
-        h->bn_a = 64;
+        h->shape_a = GemmShape::Wide;  // 128-wide weight tiles: more weight bytes in flight per stage
+        h->bn_a = 128;
         const int tiles = cdiv(h->NA, h->bn_a) * h->m_tiles;
         int s = sms / (tiles > 0 ? tiles : 1);
         if (s < 1) s = 1;
@@ -187,11 +192,46 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->shape_b = GemmShape::Narrow;
         h->bn_kv = cdiv(h->NKV, 64) * h->m_tiles >= sms ? 64 : 32;
     } else {
-        h->shape_b = GemmShape::Wide;
+        // one q head per tile: the 192-wide, 5-stage shape when the head fits
+        h->shape_b = d.nope_dim + R <= 192 ? GemmShape::Mid : GemmShape::Wide;
         h->bn_kv = 128;
     }
 
-    // Workspace: partials | normed | q | amax | status, each 256-byte aligned.
+    // Decode expansion: jobs of unequal size (a q head streams (Dn+R)*Lq
+    // weights, a kv tile bn_kv*Lkv); assign them to the CTAs longest first,
+    // each to the least loaded CTA, so every SM streams about the same bytes.
+    const int njobs_b = ((Lq > 0 ? d.num_heads : 0) + cdiv(h->NKV, h->bn_kv)) * h->m_tiles;
+    h->expand_grid = njobs_b < sms ? njobs_b : sms;
+    std::vector<int> table;
+    if (h->decode && njobs_b > h->expand_grid) {
+        const int nq = Lq > 0 ? d.num_heads : 0;
+        std::vector<std::pair<long long, int>> w;  // (-bytes, job) sorted: heaviest first
+        const int ntiles = nq + cdiv(h->NKV, h->bn_kv), gn = 16;
+        for (int j = 0; j < njobs_b; ++j) {
+            // the job -> tile order of the kernel (groups of gn tiles, token tiles inside)
+            const int g = j / (gn * h->m_tiles), r = j - g * gn * h->m_tiles;
+            const int gw = ntiles - g * gn < gn ? ntiles - g * gn : gn;
+            const int tile = g * gn + (r - (r / gw) * gw);
+            const long long bytes = tile < nq ? 2LL * (d.nope_dim + R) * Lq : 2LL * h->bn_kv * Lkv;
+            w.push_back({-bytes, j});
+        }
+        std::sort(w.begin(), w.end());
+        const int G = h->expand_grid;
+        std::vector<long long> load(G, 0);
+        std::vector<std::vector<int>> lists(G);
+        for (const auto& e : w) {
+            int best = 0;
+            for (int c = 1; c < G; ++c)
+                if (load[c] < load[best]) best = c;
+            load[best] -= e.first;
+            lists[best].push_back(e.second);
+        }
+        table.push_back(0);
+        for (int c = 0; c < G; ++c) table.push_back(table.back() + static_cast<int>(lists[c].size()));
+        for (int c = 0; c < G; ++c) table.insert(table.end(), lists[c].begin(), lists[c].end());
+    }
+
+    // Workspace: partials | normed | q | amax | status | job table, each 256-byte aligned.
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t T = static_cast<size_t>(d.T);
     const size_t b_part = al(static_cast<size_t>(h->splits_a) * T * h->NA * 4);
@@ -199,7 +239,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t b_q = Lq > 0 ? al(T * h->NQ * 4) : 0;
     const size_t b_amax = al(T * 4);
     const size_t b_stat = 256;
-    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat;
+    const size_t b_tab = al(table.size() * sizeof(int));
+    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab;
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
         delete h;
         return cuda_fail(e, "cudaMalloc(workspace)");
@@ -210,10 +251,20 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->qws = Lq > 0 ? reinterpret_cast<float*>(w + b_part + b_norm) : nullptr;
     h->amax = reinterpret_cast<uint32_t*>(w + b_part + b_norm + b_q);
     h->status = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax);
+
     if ((e = cudaMemset(h->ws, 0, h->ws_bytes)) != cudaSuccess) {
         cudaFree(h->ws);
         delete h;
         return cuda_fail(e, "cudaMemset(workspace)");
+    }
+    if (!table.empty()) {
+        h->job_table = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax + b_stat);
+        if ((e = cudaMemcpy(h->job_table, table.data(), table.size() * sizeof(int), cudaMemcpyHostToDevice)) !=
+            cudaSuccess) {
+            cudaFree(h->ws);
+            delete h;
+            return cuda_fail(e, "cudaMemcpy(job table)");
+        }
     }
     const uint64_t Tm = d.T > 0 ? static_cast<uint64_t>(d.T) : 1;
     bool ok = encode_bf16(&h->tm_nkv, h->normed + Lq, Lkv, Tm, Lq + Lkv, kBM);
@@ -302,6 +353,13 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pa.n_tiles = cdiv(h->NA, h->bn_a);
     pa.m_tiles = h->m_tiles;
     pa.compensated = h->compensated;
+    pa.prefetch_l2 = h->decode ? 1 : 0;
+    pa.positions = positions;
+    pa.cos_sin = cos_sin;
+    pa.R = R;
+    pa.max_pos = d.max_pos;
+    pa.gamma = static_cast<const uint16_t*>(gamma);
+    pa.n_gamma = Lq + Lkv;
     pa.status = h->status;
     pa.timeout_ns = h->timeout_ns;
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
@@ -348,6 +406,12 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.bn_kv = h->bn_kv;
     pb.m_tiles = h->m_tiles;
     pb.group_n = 16;
+    pb.job_table = h->job_table;
+    pb.prefetch_l2 = h->decode ? 1 : 0;
+    pb.w_qb = wb;
+    pb.w_kvb = wb + static_cast<size_t>(h->NQ) * Lq;
+    pb.Lq = Lq;
+    pb.Lkv = Lkv;
     pb.kb_q = cdiv(Lq, kBK);
     pb.kb_kv = cdiv(Lkv, kBK);
     pb.positions = positions;
@@ -355,18 +419,18 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.max_pos = d.max_pos;
     pb.out_k = static_cast<uint16_t*>(out_k);
     pb.out_v = static_cast<uint16_t*>(out_v);
+    pb.out_aligned32 = (reinterpret_cast<uintptr_t>(out_k) % 32 == 0) && (reinterpret_cast<uintptr_t>(out_v) % 32 == 0);
     pb.qws = h->qws;
     pb.amax = h->amax;
     pb.status = h->status;
     pb.timeout_ns = h->timeout_ns;
-    const int jobs_b = (pb.nq_tiles + pb.nkv_tiles) * pb.m_tiles;
-    if ((e = launch_expand(h->shape_b, jobs_b < h->sms ? jobs_b : h->sms, h->tm_nq, h->tm_nkv, h->tm_wqb,
-                           h->tm_wkvb, pb, st)) != cudaSuccess)
+    if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb, st)) !=
+        cudaSuccess)
         return cuda_fail(e, "launch mla_expand_kernel");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
     if (Lq > 0) {
-        QuantParams pq{h->qws, h->amax, d.T, h->NQ, out_q_int8, out_scale};
+        QuantParams pq{h->qws, h->amax, d.T, h->NQ, h->NQ, out_q_int8, out_scale};
         if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
     }
     if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
@@ -392,7 +456,7 @@ int mla_prolog_quant_rows(const float* y, int32_t rows, int32_t row_len, int8_t*
     if (rows == 0) return MLA_OK;
     if (!y || !codes || !scale || !aligned(y, 16) || !aligned(codes, 4) || !aligned(scale, 4))
         return MLA_ERR_INVALID_ARG;
-    QuantParams p{y, nullptr, rows, row_len, codes, scale};
+    QuantParams p{y, nullptr, rows, row_len, row_len, codes, scale};
     cudaError_t e = launch_quant(p, static_cast<cudaStream_t>(stream), false);
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "launch mla_quant_kernel");
 }

@@ -144,6 +144,21 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
     return true;
 }
 
+// Decode schedules stream weights that are read once.  A job's weight rows
+// form one contiguous slab of memory, but the ring reads it as 64-column
+// boxes, i.e. one 128-byte piece per row at the row stride.  Prefetching the
+// slab into L2 as contiguous ranges when the job starts turns that into
+// sequential DRAM bursts and keeps far more bytes in flight than the
+// shared-memory ring can hold.
+__device__ __forceinline__ void prefetch_slab(const void* base, size_t bytes) {
+    const char* p = static_cast<const char*>(base);
+    constexpr size_t kChunk = 32768;
+    for (size_t o = 0; o < bytes; o += kChunk) {
+        const size_t n = bytes - o < kChunk ? bytes - o : kChunk;
+        bulk_prefetch_l2(p + o, static_cast<uint32_t>(n));
+    }
+}
+
 // No copy may still be landing in shared memory when the CTA leaves.
 template <int STAGES>
 __device__ __forceinline__ void drain_loads(const Smem& sm, uint32_t loads, uint64_t timeout_ns) {
@@ -231,6 +246,19 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
         nkb = (split + 1) * p.kb_total / p.splits - kb0;
     };
 
+    if (warp == 0 && lane != 0 && p.prefetch_l2) {
+        // Warm L2 with the small inputs the norm and expansion kernels read
+        // (cos/sin rows of this batch's positions, gamma): when they run, HBM
+        // queues are full of weight traffic and a miss there waits behind it.
+        const int nthr = 31 * static_cast<int>(gridDim.x);
+        for (int t = static_cast<int>(blockIdx.x) * 31 + lane - 1; t < p.T; t += nthr) {
+            const int pos = p.positions[t];
+            if (pos >= 0 && pos < p.max_pos)
+                bulk_prefetch_l2(p.cos_sin + static_cast<size_t>(pos) * p.R, static_cast<uint32_t>(p.R * 4));
+        }
+        if (blockIdx.x == 0 && lane == 1 && p.n_gamma > 0)
+            bulk_prefetch_l2(p.gamma, static_cast<uint32_t>(p.n_gamma * 2));
+    }
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tensormap(&tm_x);
@@ -302,11 +330,12 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
             if (t < p.T) {
                 float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
 #pragma unroll
-                for (int c = 0; c < HALF; c += 4) {
+                for (int c = 0; c < HALF; c += 8) {
                     if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA)
-                        *reinterpret_cast<float4*>(dst + c) =
-                            make_float4(__fadd_rn(acc[c], cmp[c]), __fadd_rn(acc[c + 1], cmp[c + 1]),
-                                        __fadd_rn(acc[c + 2], cmp[c + 2]), __fadd_rn(acc[c + 3], cmp[c + 3]));
+                        st_v8(dst + c, __fadd_rn(acc[c], cmp[c]), __fadd_rn(acc[c + 1], cmp[c + 1]),
+                              __fadd_rn(acc[c + 2], cmp[c + 2]), __fadd_rn(acc[c + 3], cmp[c + 3]),
+                              __fadd_rn(acc[c + 4], cmp[c + 4]), __fadd_rn(acc[c + 5], cmp[c + 5]),
+                              __fadd_rn(acc[c + 6], cmp[c + 6]), __fadd_rn(acc[c + 7], cmp[c + 7]));
                 }
             }
         }
@@ -317,7 +346,8 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
 
 // -------------------------------------------------- expansion (normed W_b^T)
 
-constexpr int kExpandEpiWarps = 4;
+constexpr int kExpandEpiWarps = 8;  // two warps per TMEM lane quarter, one per column half
+constexpr int kExpandThreads = 64 + 32 * kExpandEpiWarps;
 
 // Job j -> (tile, token tile).  Tiles [0, nq_tiles) are q heads, the rest kv
 // tiles.  Jobs go through the tiles in groups of group_n: all token tiles of
@@ -332,97 +362,175 @@ __device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& ti
     tile = g * p.group_n + (r - m_tile * gw);
 }
 
-// q head h of token rows [m0, m0+128): FP32 q, RoPE of its rope slice, per-token max |q|.
-__device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, int row, int m0, int h) {
-    const int Dn = p.Dn, R = p.R;
-    const int t = m0 + row;
-    const bool in = t < p.T;
-    const int pos = in ? p.positions[t] : 0;
-    const bool valid = in && pos >= 0 && pos < p.max_pos;
-    float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * (Dn + R);
-    float amax = 0.0f;
-    for (int c = 0; c < Dn; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
-        if (in) {
-            float4* d4 = reinterpret_cast<float4*>(qrow + c);
+// Per-row state of the expansion epilogue: the row's token, whether its
+// position is valid, and (for the q path, R <= 64) its cos/sin row.  Loaded
+// once per token tile, while the epilogue warps wait for the accumulator, so
+// the RoPE does not wait on global loads between TMEM loads.
+struct RowCtx {
+    int t;
+    bool in, valid;
+    float c[32], s[32];
+};
+
+__device__ __forceinline__ void load_row_ctx(const ExpandParams& p, int t, RowCtx& rc) {
+    rc.t = t;
+    rc.in = t < p.T;
+    const int pos = rc.in ? p.positions[t] : 0;
+    rc.valid = rc.in && pos >= 0 && pos < p.max_pos;
+    if (p.nq_tiles > 0 && p.R <= 64) {
+        const int half = p.R / 2;
+        const float* cs = p.cos_sin + static_cast<size_t>(rc.valid ? pos : 0) * p.R;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 o = valid ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3])
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(o.x), fabsf(o.y)), fmaxf(fabsf(o.z), fabsf(o.w))));
-                d4[q] = o;
+        for (int i = 0; i < 32; i += 4) {
+            if (i < half) {
+                const float4 c4 = *reinterpret_cast<const float4*>(cs + i);
+                const float4 s4 = *reinterpret_cast<const float4*>(cs + half + i);
+                rc.c[i] = c4.x, rc.c[i + 1] = c4.y, rc.c[i + 2] = c4.z, rc.c[i + 3] = c4.w;
+                rc.s[i] = s4.x, rc.s[i + 1] = s4.y, rc.s[i + 2] = s4.z, rc.s[i + 3] = s4.w;
             }
         }
     }
-    const int half = R / 2;
-    const float* cs = p.cos_sin + static_cast<size_t>(valid ? pos : 0) * R;
-    for (int i = 0; i < half; i += 8) {
-        float a[8], b[8];
-        tmem_ld8(tbase + Dn + i, a);
-        tmem_ld8(tbase + Dn + half + i, b);
+}
+
+// x*cos + rotate_half(x)*sin on 8 pairs, rotate_half(x1, x2) = (-x2, x1)
+__device__ __forceinline__ void rope8(const float (&a)[8], const float (&b)[8], const float* cc, const float* ss,
+                                      float (&o1)[8], float (&o2)[8]) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        o1[e] = __fadd_rn(__fmul_rn(a[e], cc[e]), __fmul_rn(-b[e], ss[e]));
+        o2[e] = __fadd_rn(__fmul_rn(b[e], cc[e]), __fmul_rn(a[e], ss[e]));
+    }
+}
+
+// q head h of one token row: FP32 q, RoPE of its rope slice, per-token max
+// |q|.  Column half 0 takes the nope columns, half 1 the rope slice.
+__device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int h,
+                                                  int half_idx) {
+    const int Dn = p.Dn, R = p.R;
+    const int t = rc.t;
+    const bool in = rc.in, valid = rc.valid;
+    float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * (Dn + R);
+    float amax = 0.0f;
+    for (int c = 0; c < (half_idx == 0 ? Dn : 0); c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
         if (in) {
-            float o1[8], o2[8];
-            if (valid) {
-                const float4 c0 = *reinterpret_cast<const float4*>(cs + i);
-                const float4 c1 = *reinterpret_cast<const float4*>(cs + i + 4);
-                const float4 s0 = *reinterpret_cast<const float4*>(cs + half + i);
-                const float4 s1 = *reinterpret_cast<const float4*>(cs + half + i + 4);
-                const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            if (!valid) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    // x*cos + rotate_half(x)*sin, rotate_half(x1, x2) = (-x2, x1)
-                    o1[e] = __fadd_rn(__fmul_rn(a[e], cc[e]), __fmul_rn(-b[e], ss[e]));
-                    o2[e] = __fadd_rn(__fmul_rn(b[e], cc[e]), __fmul_rn(a[e], ss[e]));
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
+                for (int e = 0; e < 16; ++e) v[e] = 0.0f;
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
-            float4* d1 = reinterpret_cast<float4*>(qrow + Dn + i);
-            float4* d2 = reinterpret_cast<float4*>(qrow + Dn + half + i);
-            d1[0] = make_float4(o1[0], o1[1], o1[2], o1[3]);
-            d1[1] = make_float4(o1[4], o1[5], o1[6], o1[7]);
-            d2[0] = make_float4(o2[0], o2[1], o2[2], o2[3]);
-            d2[1] = make_float4(o2[4], o2[5], o2[6], o2[7]);
+            for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+            st_v8(qrow + c, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+            st_v8(qrow + c + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+        }
+    }
+    const int half = R / 2;
+    auto finish = [&](int i, const float (&o1)[8], const float (&o2)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
+        st_v8(qrow + Dn + i, o1[0], o1[1], o1[2], o1[3], o1[4], o1[5], o1[6], o1[7]);
+        st_v8(qrow + Dn + half + i, o2[0], o2[1], o2[2], o2[3], o2[4], o2[5], o2[6], o2[7]);
+    };
+    if (half_idx == 0) {
+        // nope columns only
+    } else if (R <= 64) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+            if (i < half) {  // warp-uniform
+                float a[8], b[8], o1[8], o2[8];
+                tmem_ld8(tbase + Dn + i, a);
+                tmem_ld8(tbase + Dn + half + i, b);
+                if (in) {
+                    if (valid) {
+                        rope8(a, b, rc.c + i, rc.s + i, o1, o2);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
+                    }
+                    finish(i, o1, o2);
+                }
+            }
+        }
+    } else {
+        // wide rope slices: cos/sin straight from the table
+        const int pos = in ? p.positions[t] : 0;
+        const float* cs = p.cos_sin + static_cast<size_t>(valid ? pos : 0) * R;
+        for (int i = 0; i < half; i += 8) {
+            float a[8], b[8], o1[8], o2[8];
+            tmem_ld8(tbase + Dn + i, a);
+            tmem_ld8(tbase + Dn + half + i, b);
+            if (in) {
+                if (valid) {
+                    float cc[8], ss[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cc[e] = cs[i + e], ss[e] = cs[half + i + e];
+                    rope8(a, b, cc, ss, o1, o2);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
+                }
+                finish(i, o1, o2);
+            }
         }
     }
     // |q| >= 0, so the order of the float bit patterns is the order of the values.
     if (valid) atomicMax(p.amax + t, __float_as_uint(amax));
 }
 
-// kv columns [n0, n0 + bn) of [T, H, Dn + Dv]: k_nope into K's first Dn
-// columns, value into out_v, both BF16.
-__device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32_t tbase, int row, int m0, int n0) {
+// kv columns [n0, n0 + bn) of [T, H, Dn + Dv] for one token row: k_nope
+// into K's first Dn columns, value into out_v, both BF16.  Column half h
+// takes columns [h * bn / 2, (h + 1) * bn / 2).
+__device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int n0,
+                                                   int half_idx) {
     const int Dn = p.Dn, R = p.R, HD = p.Dn + p.Dv;
-    const int t = m0 + row;
-    const bool in = t < p.T;
-    const int pos = in ? p.positions[t] : 0;
-    const bool valid = in && pos >= 0 && pos < p.max_pos;
-    for (int c = 0; c < p.bn_kv; c += 16) {
+    const int t = rc.t;
+    const int hw = p.bn_kv / 2;
+    for (int c = half_idx * hw; c < (half_idx + 1) * hw; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
         const int n = n0 + c;
-        if (in && n < p.NKV) {
+        if (rc.in && n < p.NKV) {
             const int h = n / HD;
             const int j = n - h * HD;
             uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
+            for (int e = 0; e < 8; ++e) w[e] = rc.valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
             uint16_t* dst = j < Dn ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (Dn + R) + j
                                    : p.out_v + (static_cast<size_t>(t) * p.H + h) * p.Dv + (j - Dn);
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            if (p.out_aligned32) {
+                st_v8(dst, w);
+            } else {
+                uint4* d4 = reinterpret_cast<uint4*>(dst);
+                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
         }
     }
 }
 
+// The jobs of this CTA: round robin over [0, njobs), or, when a balanced
+// table is given, entries [table[c], table[c + 1]) of the id list that
+// follows the gridDim.x + 1 start offsets.
+struct CtaJobs {
+    const int* table;
+    int begin, end;
+    __device__ __forceinline__ CtaJobs(const int* t, int njobs) : table(t) {
+        if (t) {
+            begin = t[blockIdx.x];
+            end = t[blockIdx.x + 1];
+        } else {
+            begin = 0;
+            end = (njobs - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+        }
+    }
+    __device__ __forceinline__ int operator[](int i) const {
+        return table ? table[gridDim.x + 1 + i] : static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    }
+};
+
 template <int BN_MAX, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kExpandThreads, 1)
     mla_expand_kernel(const __grid_constant__ CUtensorMap tm_aq,
                       const __grid_constant__ CUtensorMap tm_akv,
                       const __grid_constant__ CUtensorMap tm_bq,
@@ -433,7 +541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp != 0) pdl_wait();  // the producer waits after its first weight tiles
-    const int njobs = (p.nq_tiles + p.nkv_tiles) * p.m_tiles;
+    const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles);
     const int Dn = p.Dn, R = p.R;
 
     if (warp == 0) {
@@ -444,10 +552,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             prefetch_tensormap(&tm_bkv);
             uint32_t loads = 0;
             bool ok = true;
-            for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
+            auto prefetch = [&](int i) {
                 int tile, m;
-                expand_job(p, j, tile, m);
-                const bool first = j == static_cast<int>(blockIdx.x);
+                expand_job(p, jobs[i], tile, m);
+                if (tile < p.nq_tiles) {
+                    const size_t head = static_cast<size_t>(Dn + R) * p.Lq * 2;
+                    prefetch_slab(static_cast<const char*>(p.w_qb) + head * tile, head);
+                } else {
+                    const int n0 = (tile - p.nq_tiles) * p.bn_kv;
+                    const int rows = p.NKV - n0 < p.bn_kv ? p.NKV - n0 : p.bn_kv;
+                    prefetch_slab(static_cast<const char*>(p.w_kvb) + static_cast<size_t>(n0) * p.Lkv * 2,
+                                  static_cast<size_t>(rows) * p.Lkv * 2);
+                }
+            };
+            for (int i = jobs.begin; i < jobs.end; ++i) {
+                int tile, m;
+                expand_job(p, jobs[i], tile, m);
+                const bool first = i == jobs.begin;
+                if (p.prefetch_l2) {
+                    if (first) prefetch(i);
+                    if (i + 1 < jobs.end) prefetch(i + 1);
+                }
                 ok = tile < p.nq_tiles
                          ? produce_job<BN_MAX, STAGES>(sm, loads, &tm_aq, &tm_bq, m * kBM, tile * (Dn + R), 0,
                                                        p.kb_q, Dn + R, first, p.timeout_ns)
@@ -466,9 +591,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t idesc_kv = idesc_bf16_f32(kBM, p.bn_kv);
             uint32_t consumed = 0, chain = 0;
             bool ok = true;
-            for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x, ++chain) {
+            for (int i = jobs.begin; i < jobs.end && ok; ++i, ++chain) {
                 int tile, m;
-                expand_job(p, j, tile, m);
+                expand_job(p, jobs[i], tile, m);
                 const bool q = tile < p.nq_tiles;
                 ok = mma_chain<BN_MAX, STAGES>(sm, consumed, chain, q ? p.kb_q : p.kb_kv, tmem,
                                                q ? idesc_q : idesc_kv, p.timeout_ns);
@@ -478,22 +603,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(sm.done, 0, p.timeout_ns, nullptr);
         }
     } else {
-        const int quarter = warp & 3;
+        const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+        const int half_idx = (warp - 2) >> 2;  // column half
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         uint32_t chain = 0;
-        for (int j = blockIdx.x; j < njobs; j += gridDim.x, ++chain) {
+        int cur_m = -1;
+        RowCtx rc;
+        for (int i = jobs.begin; i < jobs.end; ++i, ++chain) {
             int tile, m;
-            expand_job(p, j, tile, m);
+            expand_job(p, jobs[i], tile, m);
+            if (m != cur_m) {  // before waiting for the accumulator
+                load_row_ctx(p, m * kBM + row, rc);
+                cur_m = m;
+            }
             if (!epi_acquire(sm, chain, p.timeout_ns)) {
                 if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
                 break;
             }
             const uint32_t tbase = tmem + lane_off + (chain & 1) * BN_MAX;
             if (tile < p.nq_tiles)
-                expand_q_epilogue(p, tbase, row, m * kBM, tile);
+                expand_q_epilogue(p, tbase, rc, tile, half_idx);
             else
-                expand_kv_epilogue(p, tbase, row, m * kBM, (tile - p.nq_tiles) * p.bn_kv);
+                expand_kv_epilogue(p, tbase, rc, (tile - p.nq_tiles) * p.bn_kv, half_idx);
             epi_release(sm, chain);
         }
     }
@@ -517,11 +649,14 @@ __global__ void mla_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 // ------------------------------------------------------------ launchers
 
 using EWide = Layout<256, 4>;
+using EMid = Layout<192, 5>;
 using ENarrow = Layout<64, 4>;
 using CWide = Layout<128, 6>;
 using CNarrow = Layout<64, 4>;
 
-int gemm_smem_bytes(GemmShape s) { return s == GemmShape::Wide ? EWide::BYTES : ENarrow::BYTES; }
+int gemm_smem_bytes(GemmShape s) {
+    return s == GemmShape::Wide ? EWide::BYTES : s == GemmShape::Mid ? EMid::BYTES : ENarrow::BYTES;
+}
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
@@ -533,6 +668,9 @@ cudaError_t gemm_set_attributes() {
         return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EWide::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<192, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  EMid::BYTES)))
         return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   ENarrow::BYTES)))
@@ -553,10 +691,13 @@ cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq, const
                           const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
                           cudaStream_t st) {
     if (s == GemmShape::Wide)
-        return launch_kernel(mla_expand_kernel<256, 4>, dim3(grid), dim3(kGemmThreads), EWide::BYTES, st, true,
+        return launch_kernel(mla_expand_kernel<256, 4>, dim3(grid), dim3(kExpandThreads), EWide::BYTES, st, true,
                              tm_aq, tm_akv, tm_bq, tm_bkv, p);
-    return launch_kernel(mla_expand_kernel<64, 4>, dim3(grid), dim3(kGemmThreads), ENarrow::BYTES, st, true, tm_aq,
-                         tm_akv, tm_bq, tm_bkv, p);
+    if (s == GemmShape::Mid)
+        return launch_kernel(mla_expand_kernel<192, 5>, dim3(grid), dim3(kExpandThreads), EMid::BYTES, st, true,
+                             tm_aq, tm_akv, tm_bq, tm_bkv, p);
+    return launch_kernel(mla_expand_kernel<64, 4>, dim3(grid), dim3(kExpandThreads), ENarrow::BYTES, st, true,
+                         tm_aq, tm_akv, tm_bq, tm_bkv, p);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {

@@ -114,8 +114,8 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     GemmShape shape_a, shape_b;
     int bn_a, splits_a = 1, bn_kv, group_a;
     if (decode) {
-        shape_a = GemmShape::Narrow;
-        bn_a = 64;
+        shape_a = GemmShape::Wide;
+        bn_a = 128;
         const int tiles = cdiv(NA, bn_a) * m_tiles;
         int s = sms / (tiles > 0 ? tiles : 1);
         if (s < 1) s = 1;
@@ -133,7 +133,7 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
         shape_b = GemmShape::Narrow;
         bn_kv = cdiv(NKV, 64) * m_tiles >= sms ? 64 : 32;
     } else {
-        shape_b = GemmShape::Wide;
+        shape_b = d.nope_dim + R <= 192 ? GemmShape::Mid : GemmShape::Wide;
         bn_kv = 128;
     }
 
@@ -204,6 +204,13 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pa.n_tiles = cdiv(NA, bn_a);
     pa.m_tiles = m_tiles;
     pa.compensated = 1;
+    pa.prefetch_l2 = decode ? 1 : 0;
+    pa.positions = positions;
+    pa.cos_sin = cos_sin;
+    pa.R = R;
+    pa.max_pos = d.max_pos;
+    pa.gamma = static_cast<const uint16_t*>(gamma);
+    pa.n_gamma = Lq + Lkv;
     pa.status = dstatus;
     pa.timeout_ns = timeout_ns;
     const int jobs_a = pa.n_tiles * m_tiles * splits_a;
@@ -247,6 +254,12 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.bn_kv = bn_kv;
     pb.m_tiles = m_tiles;
     pb.group_n = 16;
+    pb.job_table = nullptr;  // round robin: same per-job results as the balanced order
+    pb.prefetch_l2 = decode ? 1 : 0;
+    pb.w_qb = wb;
+    pb.w_kvb = wb + static_cast<size_t>(NQ) * Lq;
+    pb.Lq = Lq;
+    pb.Lkv = Lkv;
     pb.kb_q = cdiv(Lq, kBK);
     pb.kb_kv = cdiv(Lkv, kBK);
     pb.positions = positions;
@@ -254,6 +267,7 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.max_pos = d.max_pos;
     pb.out_k = static_cast<uint16_t*>(out_k);
     pb.out_v = static_cast<uint16_t*>(out_v);
+    pb.out_aligned32 = (reinterpret_cast<uintptr_t>(out_k) % 32 == 0) && (reinterpret_cast<uintptr_t>(out_v) % 32 == 0);
     pb.qws = qws;
     pb.amax = amax;
     pb.status = dstatus;
@@ -262,7 +276,7 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     if (launch_expand(shape_b, jobs_b < sms ? jobs_b : sms, tm_nq, tm_nkv, tm_wqb, tm_wkvb, pb, st) != cudaSuccess)
         return set_error("launch mla_expand_kernel");
     if (Lq > 0) {
-        QuantParams pq{qws, amax, d.T, NQ, out_q_int8, out_scale};
+        QuantParams pq{qws, amax, d.T, NQ, NQ, out_q_int8, out_scale};
         if (launch_quant(pq, st, true) != cudaSuccess) return set_error("launch mla_quant_kernel");
     }
     if (status && cudaMemcpyAsync(status, dstatus, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

@@ -27,6 +27,12 @@ struct CompressParams {
     int group;        // K blocks per tensor-core accumulation chain (>= 1)
     int n_tiles, m_tiles;
     int compensated;  // drained chains summed with TwoSum (1) or plain FP32 adds (0)
+    int prefetch_l2;  // warm L2 with the later kernels' small inputs (decode)
+    const int32_t* positions;
+    const float* cos_sin;
+    int R, max_pos;
+    const uint16_t* gamma;
+    int n_gamma;
     int* status;
     uint64_t timeout_ns;
 };
@@ -55,12 +61,18 @@ struct ExpandParams {
     int NQ, NKV;
     int nq_tiles, nkv_tiles, bn_kv;
     int m_tiles, group_n;  // token tiles; weight tiles per L2 group of the job order
+    const int* job_table;  // balanced per-CTA job lists (null: round robin)
+    int prefetch_l2;       // prefetch each job's weight rows into L2 (decode)
+    const void* w_qb;      // W_q_b [NQ][Lq] and W_kv_b [NKV][Lkv], for the L2 prefetch
+    const void* w_kvb;
+    int Lq, Lkv;
     int kb_q, kb_kv;
     const int32_t* positions;
     const float* cos_sin;
     int max_pos;
     uint16_t* out_k;  // [T][H][Dn + R]
     uint16_t* out_v;  // [T][H][Dv]
+    int out_aligned32;  // out_k and out_v 32-byte aligned: 256-bit stores
     float* qws;       // [T][NQ] FP32 q after RoPE
     uint32_t* amax;   // [T] bits of max |q| per token
     int* status;
@@ -71,19 +83,21 @@ struct QuantParams {
     const float* y;          // [rows][row_len]
     const uint32_t* amax;    // [rows] bits of max|y| (null: the kernel finds it)
     int rows, row_len;
+    int chunk;               // elements per CTA (row_len when amax is null)
     int8_t* codes;
     float* scale;
 };
 
 // Shapes of the GEMM kernel instantiations.
-// Expansion kernel: Wide = BN_MAX 256, 4 stages; Narrow = BN_MAX 64, 4 stages.
+// Expansion kernel: Wide = BN_MAX 256, 4 stages; Mid = BN_MAX 192, 5 stages
+// (decode with a q path: one head of Dn + R <= 192 columns per tile);
+// Narrow = BN_MAX 64, 4 stages.
 // Compression kernel: Wide = BN_MAX 128, 6 stages; Narrow = BN_MAX 64, 4 stages.
 // The narrow (decode) shapes use half the shared memory so that a compression
 // CTA and an expansion CTA fit on one SM and the expansion can start
 // streaming its weights while the compression is still running.
-enum class GemmShape { Wide, Narrow };
+enum class GemmShape { Wide, Mid, Narrow };
 int gemm_smem_bytes(GemmShape s);
-constexpr int kGemmThreads = 192;
 
 // Launches `kernel`; with `pdl` the launch may overlap the tail of the
 // previous kernel in the stream (programmatic dependent launch): the kernel

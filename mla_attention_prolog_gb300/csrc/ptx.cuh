@@ -106,6 +106,23 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Starts bringing a 2-D tile of a tensor into L2 (no shared memory, no
+// completion): lets HBM work on tiles long before the shared-memory ring has
+// room for them.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// Starts bringing a contiguous byte range into L2 (16-byte aligned address
+// and size): sequential DRAM bursts instead of one 128-byte piece per row.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -233,6 +250,21 @@ __device__ __forceinline__ void two_sum_add(float& s, float& c, float v) {
     const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(v, bp));
     c = __fadd_rn(c, err);
     s = t;
+}
+
+// 256-bit stores: one whole 32-byte sector per thread, so L2 never has to
+// merge a partially written sector (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_v8(float* p, float a0, float a1, float a2, float a3, float a4, float a5, float a6,
+                                      float a7) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2), "f"(a3),
+                 "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 // --------------------------------------------------------------- conversions

@@ -34,6 +34,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // One CTA per token.  Launched as a programmatic dependent of the compression
 // kernel: it waits for the partials, then lets the expansion kernel launch.
+template <bool SPLIT>
 __global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormRopeParams p) {
     extern __shared__ __align__(16) uint16_t crow[];  // BF16 row of C [NA], then rotated k_pe [R]
     __shared__ float red[2][kNormWarps];
@@ -68,27 +69,24 @@ __global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormR
     const float* prow = p.partials + static_cast<size_t>(t) * NA;
     for (int i = tid * 4; i < NA; i += kNormThreads * 4) {
         float4 a = *reinterpret_cast<const float4*>(prow + i);
-        if (p.splits > 1) {
+        if (SPLIT) {
+            // every split's load in flight first (up to 8 at a time), then the
+            // sums in split order with TwoSum
             float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-            int s = 1;
-            for (; s + 8 <= p.splits; s += 8) {  // eight loads in flight, then the ordered sums
+            for (int s0 = 1; s0 < p.splits; s0 += 8) {
                 float4 b[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) b[u] = *reinterpret_cast<const float4*>(prow + (s + u) * sstride + i);
+                for (int u = 0; u < 8; ++u)
+                    if (s0 + u < p.splits) b[u] = *reinterpret_cast<const float4*>(prow + (s0 + u) * sstride + i);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    two_sum_add(a.x, c.x, b[u].x);
-                    two_sum_add(a.y, c.y, b[u].y);
-                    two_sum_add(a.z, c.z, b[u].z);
-                    two_sum_add(a.w, c.w, b[u].w);
+                    if (s0 + u < p.splits) {
+                        two_sum_add(a.x, c.x, b[u].x);
+                        two_sum_add(a.y, c.y, b[u].y);
+                        two_sum_add(a.z, c.z, b[u].z);
+                        two_sum_add(a.w, c.w, b[u].w);
+                    }
                 }
-            }
-            for (; s < p.splits; ++s) {
-                const float4 b = *reinterpret_cast<const float4*>(prow + s * sstride + i);
-                two_sum_add(a.x, c.x, b.x);
-                two_sum_add(a.y, c.y, b.y);
-                two_sum_add(a.z, c.z, b.z);
-                two_sum_add(a.w, c.w, b.w);
             }
             a = make_float4(__fadd_rn(a.x, c.x), __fadd_rn(a.y, c.y), __fadd_rn(a.z, c.z), __fadd_rn(a.w, c.w));
         }
@@ -154,20 +152,25 @@ __global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormR
 // ---------------------------------------------------------------- quant
 
 constexpr int kQuantThreads = 256;
+constexpr int kQuantChunk = 4096;  // elements per CTA when amax is known
 
+// blockIdx.x = row, blockIdx.y = chunk of the row.  With a known amax the
+// chunks of a row are independent; without one, one CTA takes the whole row
+// and first reduces max |y|.
 __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantParams p) {
     pdl_wait();
     const int row = blockIdx.x;
     const float* y = p.y + static_cast<size_t>(row) * p.row_len;
-    const int n4 = p.row_len / 4;
+    const int c0 = blockIdx.y * p.chunk;
+    const int c1 = c0 + p.chunk < p.row_len ? c0 + p.chunk : p.row_len;
     float amax;
     if (p.amax) {
         amax = __uint_as_float(p.amax[row]);
     } else {
         __shared__ float red[kQuantThreads / 32];
         float m = 0.0f;
-        for (int i = threadIdx.x; i < n4; i += kQuantThreads) {
-            const float4 v = reinterpret_cast<const float4*>(y)[i];
+        for (int i = threadIdx.x * 4; i < p.row_len; i += kQuantThreads * 4) {
+            const float4 v = *reinterpret_cast<const float4*>(y + i);
             m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
         }
 #pragma unroll
@@ -179,16 +182,17 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
         for (int w = 0; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
         amax = m;
     }
-    char4* out = reinterpret_cast<char4*>(p.codes + static_cast<size_t>(row) * p.row_len);
+    int8_t* out = p.codes + static_cast<size_t>(row) * p.row_len;
     if (amax == 0.0f) {
-        for (int i = threadIdx.x; i < n4; i += kQuantThreads) out[i] = make_char4(0, 0, 0, 0);
-        if (threadIdx.x == 0) p.scale[row] = 0.0f;
+        for (int i = c0 + threadIdx.x * 4; i < c1; i += kQuantThreads * 4)
+            *reinterpret_cast<char4*>(out + i) = make_char4(0, 0, 0, 0);
+        if (threadIdx.x == 0 && blockIdx.y == 0) p.scale[row] = 0.0f;
         return;
     }
     const float inv = __fdiv_rn(127.0f, amax);
 #pragma unroll 4
-    for (int i = threadIdx.x; i < n4; i += kQuantThreads) {
-        const float4 v = reinterpret_cast<const float4*>(y)[i];
+    for (int i = c0 + threadIdx.x * 4; i < c1; i += kQuantThreads * 4) {
+        const float4 v = *reinterpret_cast<const float4*>(y + i);
         const float f[4] = {v.x, v.y, v.z, v.w};
         signed char c[4];
 #pragma unroll
@@ -197,9 +201,9 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
             q = q > 127 ? 127 : (q < -127 ? -127 : q);
             c[e] = static_cast<signed char>(q);
         }
-        out[i] = make_char4(c[0], c[1], c[2], c[3]);
+        *reinterpret_cast<char4*>(out + i) = make_char4(c[0], c[1], c[2], c[3]);
     }
-    if (threadIdx.x == 0) p.scale[row] = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0 && blockIdx.y == 0) p.scale[row] = __fdiv_rn(amax, 127.0f);
 }
 
 // ------------------------------------------------------------ launchers
@@ -207,12 +211,17 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
-    return launch_kernel(mla_norm_rope_kernel, dim3(p.T), dim3(kNormThreads), smem, st, true, p);
+    if (p.splits > 1)
+        return launch_kernel(mla_norm_rope_kernel<true>, dim3(p.T), dim3(kNormThreads), smem, st, true, p);
+    return launch_kernel(mla_norm_rope_kernel<false>, dim3(p.T), dim3(kNormThreads), smem, st, true, p);
 }
 
-cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
-    if (p.rows == 0) return cudaSuccess;
-    return launch_kernel(mla_quant_kernel, dim3(p.rows), dim3(kQuantThreads), 0, st, pdl, p);
+cudaError_t launch_quant(const QuantParams& p_in, cudaStream_t st, bool pdl) {
+    if (p_in.rows == 0) return cudaSuccess;
+    QuantParams p = p_in;
+    p.chunk = p.amax ? kQuantChunk : p.row_len;
+    const int chunks = (p.row_len + p.chunk - 1) / p.chunk;
+    return launch_kernel(mla_quant_kernel, dim3(p.rows, chunks), dim3(kQuantThreads), 0, st, pdl, p);
 }
 
 }  // namespace mlap
