@@ -17,10 +17,8 @@
 
 namespace mlap {
 
-constexpr int kNormThreads = 256;
-constexpr int kNormWarps = kNormThreads / 32;
-
 // Sum of a per-thread value over the CTA in a fixed order (deterministic).
+template <int NW>
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -28,14 +26,19 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     __syncthreads();
     float s = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kNormWarps; ++w) s = __fadd_rn(s, red[w]);
+    for (int w = 0; w < NW; ++w) s = __fadd_rn(s, red[w]);
     return s;
 }
 
 // One CTA per token.  Launched as a programmatic dependent of the compression
 // kernel: it waits for the partials, then lets the expansion kernel launch.
-template <bool SPLIT>
-__global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormRopeParams p) {
+// With split-K partials (decode) the CTA is wider and keeps every split's
+// load of its columns in flight at once: the step is latency bound.
+template <bool SPLIT, int NT>
+__global__ void __launch_bounds__(NT) mla_norm_rope_kernel(const NormRopeParams p) {
+    constexpr int kNormThreads = NT;
+    constexpr int kNormWarps = NT / 32;
+    constexpr int kBatch = SPLIT ? 16 : 1;
     extern __shared__ __align__(16) uint16_t crow[];  // BF16 row of C [NA], then rotated k_pe [R]
     __shared__ float red[2][kNormWarps];
     pdl_wait();
@@ -70,16 +73,16 @@ __global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormR
     for (int i = tid * 4; i < NA; i += kNormThreads * 4) {
         float4 a = *reinterpret_cast<const float4*>(prow + i);
         if (SPLIT) {
-            // every split's load in flight first (up to 8 at a time), then the
-            // sums in split order with TwoSum
+            // every split's load in flight first (up to kBatch at a time),
+            // then the sums in split order with TwoSum
             float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 1; s0 < p.splits; s0 += 8) {
-                float4 b[8];
+            for (int s0 = 1; s0 < p.splits; s0 += kBatch) {
+                float4 b[kBatch];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < kBatch; ++u)
                     if (s0 + u < p.splits) b[u] = *reinterpret_cast<const float4*>(prow + (s0 + u) * sstride + i);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kBatch; ++u) {
                     if (s0 + u < p.splits) {
                         two_sum_add(a.x, c.x, b[u].x);
                         two_sum_add(a.y, c.y, b[u].y);
@@ -101,8 +104,8 @@ __global__ void __launch_bounds__(kNormThreads) mla_norm_rope_kernel(const NormR
             for (int e = 0; e < 4; ++e) ssq_kv = __fadd_rn(ssq_kv, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lkv));
         }
     }
-    ssq_q = block_sum(ssq_q, red[0]);
-    ssq_kv = block_sum(ssq_kv, red[1]);  // its __syncthreads also publishes crow
+    ssq_q = block_sum<kNormWarps>(ssq_q, red[0]);
+    ssq_kv = block_sum<kNormWarps>(ssq_kv, red[1]);  // its __syncthreads also publishes crow
     // Variant B of the pages' RMSNorm: std = sqrt(ms + eps), rstd = 1 / std,
     // both correctly rounded.
     const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
@@ -212,8 +215,8 @@ cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
     if (p.splits > 1)
-        return launch_kernel(mla_norm_rope_kernel<true>, dim3(p.T), dim3(kNormThreads), smem, st, true, p);
-    return launch_kernel(mla_norm_rope_kernel<false>, dim3(p.T), dim3(kNormThreads), smem, st, true, p);
+        return launch_kernel(mla_norm_rope_kernel<true, 512>, dim3(p.T), dim3(512), smem, st, true, p);
+    return launch_kernel(mla_norm_rope_kernel<false, 256>, dim3(p.T), dim3(256), smem, st, true, p);
 }
 
 cudaError_t launch_quant(const QuantParams& p_in, cudaStream_t st, bool pdl) {
