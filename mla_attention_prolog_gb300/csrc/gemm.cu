@@ -303,9 +303,10 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
         for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x) {
             int m0, n0, split, kb0, nkb;
             job_of(j, m0, n0, split, kb0, nkb);
-            float acc[HALF], cmp[HALF];
+            // column pairs in packed f32x2 registers: half the drain instructions
+            uint64_t acc[HALF / 2], cmp[HALF / 2];
 #pragma unroll
-            for (int c = 0; c < HALF; ++c) acc[c] = cmp[c] = 0.0f;
+            for (int c = 0; c < HALF / 2; ++c) acc[c] = cmp[c] = 0ull;
             for (int k = 0; k < nkb; k += group, ++chain) {
                 if (!epi_acquire(sm, chain, p.timeout_ns)) { ok = false; break; }
                 const uint32_t src = tmem + lane_off + (chain & 1) * BN_MAX + half * HALF;
@@ -316,10 +317,12 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
                         tmem_ld16(src + c, v);
                         if (p.compensated) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) two_sum_add(acc[c + e], cmp[c + e], v[e]);
+                            for (int e = 0; e < 16; e += 2)
+                                two_sum_add2(acc[(c + e) / 2], cmp[(c + e) / 2], pk2(v[e], v[e + 1]));
                         } else {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) acc[c + e] = __fadd_rn(acc[c + e], v[e]);
+                            for (int e = 0; e < 16; e += 2)
+                                acc[(c + e) / 2] = add2(acc[(c + e) / 2], pk2(v[e], v[e + 1]));
                         }
                     }
                 }
@@ -331,11 +334,12 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
                 float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
 #pragma unroll
                 for (int c = 0; c < HALF; c += 8) {
-                    if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA)
-                        st_v8(dst + c, __fadd_rn(acc[c], cmp[c]), __fadd_rn(acc[c + 1], cmp[c + 1]),
-                              __fadd_rn(acc[c + 2], cmp[c + 2]), __fadd_rn(acc[c + 3], cmp[c + 3]),
-                              __fadd_rn(acc[c + 4], cmp[c + 4]), __fadd_rn(acc[c + 5], cmp[c + 5]),
-                              __fadd_rn(acc[c + 6], cmp[c + 6]), __fadd_rn(acc[c + 7], cmp[c + 7]));
+                    if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA) {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) upk2(add2(acc[(c + e) / 2], cmp[(c + e) / 2]), o[e], o[e + 1]);
+                        st_v8(dst + c, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+                    }
                 }
             }
         }

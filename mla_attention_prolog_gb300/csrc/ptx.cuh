@@ -267,6 +267,36 @@ __device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
                  : "memory");
 }
 
+// Two lanes of FP32 per instruction (packed f32x2; each lane rounded as its
+// scalar add would be).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// two_sum_add on a pair of accumulators at once.
+__device__ __forceinline__ void two_sum_add2(uint64_t& s, uint64_t& c, uint64_t v) {
+    const uint64_t t = add2(s, v);
+    const uint64_t bp = sub2(t, s);
+    const uint64_t err = add2(sub2(s, sub2(t, bp)), sub2(v, bp));
+    c = add2(c, err);
+    s = t;
+}
+
 // --------------------------------------------------------------- conversions
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

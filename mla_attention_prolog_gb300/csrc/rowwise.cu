@@ -152,6 +152,97 @@ __global__ void __launch_bounds__(NT) mla_norm_rope_kernel(const NormRopeParams 
     }
 }
 
+// Prefill variant (no split-K partials): one warp per token, eight tokens
+// per CTA, so many tokens' loads are in flight per SM and no CTA-wide
+// barrier sits between the steps.  Same arithmetic as mla_norm_rope_kernel.
+constexpr int kNormWarpTokens = 8;
+
+__global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kernel(const NormRopeParams p) {
+    extern __shared__ __align__(16) uint16_t wsm[];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kNormWarpTokens + warp;
+    if (t >= p.T) return;  // warp-uniform
+    const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, R = p.R, half = R / 2;
+    uint16_t* crow = wsm + static_cast<size_t>(warp) * (NA + R);
+    uint16_t* rot = crow + NA;
+    const int pos = p.positions[t];
+    const bool valid = pos >= 0 && pos < p.max_pos;
+    if (lane == 0 && p.amax) p.amax[t] = 0u;
+    uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
+    const int nchunk = R / 8;
+    if (!valid) {
+        if (lane == 0) atomicOr(p.status, kStatusPositionRange);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int i = lane * 8; i < Lq + Lkv; i += 256) *reinterpret_cast<uint4*>(nrow + i) = z;
+        for (int k = lane; k < (p.H + 1) * nchunk; k += 32) {
+            const int h = k / nchunk, c = k - h * nchunk;
+            uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
+                                    : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
+            *reinterpret_cast<uint4*>(dst) = z;
+        }
+        return;
+    }
+    float ssq_q = 0.0f, ssq_kv = 0.0f;
+    const float* prow = p.partials + static_cast<size_t>(t) * NA;
+    for (int i = lane * 4; i < NA; i += 128) {
+        const float4 a = *reinterpret_cast<const float4*>(prow + i);
+        const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
+        *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
+        const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+        if (i < Lq) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ssq_q = __fadd_rn(ssq_q, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lq));
+        } else if (i < Lq + Lkv) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ssq_kv = __fadd_rn(ssq_kv, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lkv));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ssq_q = __fadd_rn(ssq_q, __shfl_xor_sync(0xffffffffu, ssq_q, o));
+        ssq_kv = __fadd_rn(ssq_kv, __shfl_xor_sync(0xffffffffu, ssq_kv, o));
+    }
+    const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
+    const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
+    __syncwarp();
+    for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
+        const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma + i);
+        const float rstd = i < Lq ? rstd_q : rstd_kv;
+        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xs[e]), rstd), bf16_lo(gs[e]));
+            const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[e]), rstd), bf16_hi(gs[e]));
+            o[e] = pack_bf16x2(y0, y1);
+        }
+        *reinterpret_cast<uint4*>(nrow + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    const uint16_t* kp = crow + Lq + Lkv;
+    const float* cs = p.cos_sin + static_cast<size_t>(pos) * R;
+    for (int i = lane; i < half; i += 32) {
+        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[i]) << 16);
+        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[i + half]) << 16);
+        const float c = cs[i], s = cs[half + i];
+        const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
+        const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
+        rot[i] = static_cast<uint16_t>(pack_bf16x2(o1, 0.0f) & 0xFFFFu);
+        rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
+    }
+    __syncwarp();
+    for (int k = lane; k < (p.H + 1) * nchunk; k += 32) {
+        const int h = k / nchunk, c = k - h * nchunk;
+        const uint4 v = *reinterpret_cast<const uint4*>(rot + c * 8);
+        uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
+                                : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
+        *reinterpret_cast<uint4*>(dst) = v;
+    }
+}
+
 // ---------------------------------------------------------------- quant
 
 constexpr int kQuantThreads = 256;
@@ -216,7 +307,8 @@ cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
     if (p.splits > 1)
         return launch_kernel(mla_norm_rope_kernel<true, 512>, dim3(p.T), dim3(512), smem, st, true, p);
-    return launch_kernel(mla_norm_rope_kernel<false, 256>, dim3(p.T), dim3(256), smem, st, true, p);
+    return launch_kernel(mla_norm_rope_warp_kernel, dim3((p.T + kNormWarpTokens - 1) / kNormWarpTokens),
+                         dim3(32 * kNormWarpTokens), smem * kNormWarpTokens, st, true, p);
 }
 
 cudaError_t launch_quant(const QuantParams& p_in, cudaStream_t st, bool pdl) {
