@@ -134,7 +134,8 @@ int mla_prolog_destroy(mla_prolog_t h);
 /*
  * Synchronises `stream`, copies the handle's device status word (an OR of
  * MLA_STATUS_* bits accumulated since the last call) into *status, and clears
- * it.  Errors: INVALID_ARG, CUDA.
+ * it (after a wait timeout it also resets the decode kernel's grid barrier).
+ * Errors: INVALID_ARG, CUDA.
  */
 int mla_prolog_device_status(mla_prolog_t h, void* stream, int32_t* status);
 
@@ -214,6 +215,11 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
 /*   MLA_TUNE_COMPRESS_COMPENSATED  1: the drained chains are summed with
  *                            error-free TwoSum; 0: with plain FP32 adds.   */
 #define MLA_TUNE_COMPRESS_COMPENSATED 2
+/*   MLA_TUNE_DECODE_FUSED    1: batches of at most 128 tokens run as one
+ *                            cooperative kernel (the default where the dims
+ *                            and the device allow it); 0: as four kernels.
+ *                            INVALID_ARG when 1 is not available.          */
+#define MLA_TUNE_DECODE_FUSED 3
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

@@ -33,6 +33,7 @@ EXPORTED = [
 TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
 TUNE_COMPRESS_GROUP = 1
 TUNE_COMPRESS_COMPENSATED = 2
+TUNE_DECODE_FUSED = 3
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -59,9 +59,10 @@ bool encode_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-constexpr int kKernelCount = 4;
+constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
+const char* const kFusedKernelName = "mla_decode_kernel";
 
 }  // namespace
 
@@ -86,6 +87,11 @@ struct mla_prolog {
     int* status = nullptr;
     int* job_table = nullptr;  // balanced expansion job lists (decode)
     int expand_grid = 0;
+    // cooperative decode kernel (one launch for the whole pass)
+    bool fused_ok = false;     // the dims and the device allow it
+    bool fused = false;        // in use (tunable)
+    size_t decode_smem = 0;
+    unsigned* bar = nullptr;   // its grid barrier [arrivals, generation]
     uint64_t timeout_ns = 1000000000ull;
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wqb{}, tm_wkvb{};
@@ -202,8 +208,21 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // each to the least loaded CTA, so every SM streams about the same bytes.
     const int njobs_b = ((Lq > 0 ? d.num_heads : 0) + cdiv(h->NKV, h->bn_kv)) * h->m_tiles;
     h->expand_grid = njobs_b < sms ? njobs_b : sms;
+    // The cooperative decode kernel takes one token tile, heads of at most
+    // kDecodeMaxBN columns and needs one resident CTA per SM.
+    if (h->m_tiles == 1 && h->bn_kv <= kDecodeMaxBN && (Lq == 0 || d.nope_dim + R <= kDecodeMaxBN)) {
+        int coop = 0, blocks = 0;
+        h->decode_smem = decode_smem_bytes(h->NA + R);
+        if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
+            decode_set_attributes(h->decode_smem) == cudaSuccess &&
+            decode_occupancy(h->decode_smem, &blocks) == cudaSuccess && blocks >= 1)
+            h->fused_ok = true;
+        cudaGetLastError();
+    }
+    h->fused = h->fused_ok;
+    const int table_grid = h->fused ? sms : h->expand_grid;
     std::vector<int> table;
-    if (h->decode && njobs_b > h->expand_grid) {
+    if (h->decode && njobs_b > table_grid) {
         const int nq = Lq > 0 ? d.num_heads : 0;
         std::vector<std::pair<long long, int>> w;  // (-bytes, job) sorted: heaviest first
         const int ntiles = nq + cdiv(h->NKV, h->bn_kv), gn = 16;
@@ -216,7 +235,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             w.push_back({-bytes, j});
         }
         std::sort(w.begin(), w.end());
-        const int G = h->expand_grid;
+        const int G = table_grid;
         std::vector<long long> load(G, 0);
         std::vector<std::vector<int>> lists(G);
         for (const auto& e : w) {
@@ -251,6 +270,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->qws = Lq > 0 ? reinterpret_cast<float*>(w + b_part + b_norm) : nullptr;
     h->amax = reinterpret_cast<uint32_t*>(w + b_part + b_norm + b_q);
     h->status = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax);
+    h->bar = reinterpret_cast<unsigned*>(w + b_part + b_norm + b_q + b_amax + 64);
 
     if ((e = cudaMemset(h->ws, 0, h->ws_bytes)) != cudaSuccess) {
         cudaFree(h->ws);
@@ -341,7 +361,6 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
         return timed ? cudaEventRecordWithFlags(h->events[i], st, rec_flags) : cudaSuccess;
     };
 
-    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     CompressParams pa{};
     pa.partials = h->partials;
     pa.T = d.T;
@@ -362,11 +381,6 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pa.n_gamma = Lq + Lkv;
     pa.status = h->status;
     pa.timeout_ns = h->timeout_ns;
-    const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
-    if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
-        cudaSuccess)
-        return cuda_fail(e, "launch mla_compress_kernel");
-    if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
     NormRopeParams pn{};
     pn.partials = h->partials;
@@ -390,8 +404,6 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pn.out_kpe = static_cast<uint16_t*>(out_kpe);
     pn.amax = Lq > 0 ? h->amax : nullptr;
     pn.status = h->status;
-    if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
-    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
 
     ExpandParams pb{};
     pb.T = d.T;
@@ -424,13 +436,39 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.amax = h->amax;
     pb.status = h->status;
     pb.timeout_ns = h->timeout_ns;
+
+    QuantParams pq{h->qws, h->amax, Lq > 0 ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
+
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+    if (h->fused) {
+        DecodeParams pd{};
+        pd.a = pa;
+        pd.n = pn;
+        pd.b = pb;
+        pd.q = pq;
+        pd.q.chunk = 4096;
+        pd.bar = h->bar;
+        pd.early_prefetch_bytes = 256 * 1024;
+        pd.status = h->status;
+        pd.timeout_ns = h->timeout_ns;
+        if ((e = launch_decode(h->sms, h->decode_smem, h->tm_x, h->tm_wa, h->tm_nq, h->tm_nkv, h->tm_wqb,
+                               h->tm_wkvb, pd, st)) != cudaSuccess)
+            return cuda_fail(e, "launch mla_decode_kernel");
+        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        return MLA_OK;
+    }
+    const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
+    if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
+        cudaSuccess)
+        return cuda_fail(e, "launch mla_compress_kernel");
+    if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+    if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
+    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb, st)) !=
         cudaSuccess)
         return cuda_fail(e, "launch mla_expand_kernel");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
-
     if (Lq > 0) {
-        QuantParams pq{h->qws, h->amax, d.T, h->NQ, h->NQ, out_q_int8, out_scale};
         if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
     }
     if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
@@ -446,6 +484,9 @@ int mla_prolog_device_status(mla_prolog_t h, void* stream, int32_t* status) {
     if ((e = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpy(status)");
     if ((e = cudaMemset(h->status, 0, sizeof v)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    // A barrier wait that gave up leaves its arrival count behind: reset it.
+    if ((v & MLA_STATUS_WAIT_TIMEOUT) && (e = cudaMemset(h->bar, 0, sizeof(unsigned))) != cudaSuccess)
+        return cuda_fail(e, "cudaMemset(barrier)");
     *status = v;
     return MLA_OK;
 }
@@ -479,20 +520,21 @@ int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_
         h->n_events = 0;
         return MLA_OK;
     }
-    if (!events || n_events < kKernelCount + 1) return MLA_ERR_INVALID_ARG;
-    for (int i = 0; i <= kKernelCount; ++i) {
+    const int need = mla_prolog_kernel_count(h) + 1;
+    if (!events || n_events < need) return MLA_ERR_INVALID_ARG;
+    for (int i = 0; i < need; ++i) {
         if (!events[i]) return MLA_ERR_INVALID_ARG;
         h->events[i] = static_cast<cudaEvent_t>(events[i]);
     }
-    h->n_events = kKernelCount + 1;
+    h->n_events = need;
     return MLA_OK;
 }
 
-int32_t mla_prolog_kernel_count(mla_prolog_t h) { return h ? kKernelCount : 0; }
+int32_t mla_prolog_kernel_count(mla_prolog_t h) { return h ? (h->fused ? 1 : kKernelCount) : 0; }
 
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
-    if (!h || i < 0 || i >= kKernelCount) return "";
-    return kKernelNames[i];
+    if (!h || i < 0 || i >= mla_prolog_kernel_count(h)) return "";
+    return h->fused ? kFusedKernelName : kKernelNames[i];
 }
 
 int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream) {
@@ -532,6 +574,12 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
         case MLA_TUNE_COMPRESS_COMPENSATED:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             h->compensated = value;
+            return MLA_OK;
+        case MLA_TUNE_DECODE_FUSED:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->fused_ok) return MLA_ERR_INVALID_ARG;
+            h->fused = value == 1;
+            h->n_events = 0;  // the kernel count changed: re-arm the timing hook
             return MLA_OK;
         default: return MLA_ERR_INVALID_ARG;
     }

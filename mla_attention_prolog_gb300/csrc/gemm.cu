@@ -1,537 +1,24 @@
-// tcgen05 GEMM kernels of the prolog: the compression projection (x . W_a^T,
-// split-K partials) and the expansion projections (normed . W_b^T) with the
-// split / RoPE / assemble epilogue.
-//
-// Both kernels are persistent: a grid of at most one CTA per SM walks a
-// static list of jobs (128-row x BN-column output tiles, or K-slices of them)
-// with blockIdx.x, blockIdx.x + gridDim.x, ...  Roles inside a CTA:
-//   warp 0       TMA producer: streams 128x64 A and BNx64 B tiles (128-byte
-//                swizzle) into a STAGES-deep shared-memory ring;
-//   warp 1       allocates TMEM and issues tcgen05.mma (M = 128, N = BN,
-//                K = 16 per instruction) from one thread, committing each
-//                ring stage back to the producer;
-//   other warps  epilogue: read their 32 TMEM lanes (one token row per
-//                thread) with tcgen05.ld and finish the tile.
-// TMEM holds two accumulator buffers: the MMA warp fills one while the
-// epilogue drains the other, so a tile's epilogue overlaps the next tile's
-// main loop.  All three roles count ring slots and accumulator "chains" with
-// CTA-global counters, so the barrier phases follow from the counters alone.
-//
-// All waits are bounded (see ptx.cuh); a wait that gives up sets the status
-// word, raises the CTA's abort flag, and the CTA still waits (bounded) for
-// its own copies and MMAs before freeing TMEM.
-#include "prolog.cuh"
-#include "ptx.cuh"
+// Standalone tcgen05 GEMM kernels of the prolog (prefill, and decode
+// shapes the cooperative kernel does not take): the compression projection
+// (x . W_a^T, split-K partials) and the expansion projections (normed .
+// W_b^T) with the split / RoPE / assemble epilogue.  Both are persistent: a
+// grid of at most one CTA per SM walks a static job list (see engine.cuh).
+#include "engine.cuh"
 
 namespace mlap {
-
-template <int BN_MAX, int STAGES>
-struct Layout {
-    static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BN_MAX * kBK * 2;
-    static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int RING = STAGES * STAGE;
-    // full[S], empty[S], acc_full[2], acc_empty[2], mma_done
-    static constexpr int MISC = RING + (2 * STAGES + 5) * 8;
-    static constexpr int BYTES = MISC + 16 + 1024;  // + slack to align the ring to 1 KB
-    static constexpr uint32_t TMEM_COLS =
-        2 * BN_MAX <= 32 ? 32 : 2 * BN_MAX <= 64 ? 64 : 2 * BN_MAX <= 128 ? 128 : 2 * BN_MAX <= 256 ? 256 : 512;
-    static_assert(STAGE % 1024 == 0, "stages must keep 1 KB alignment for the swizzle atoms");
-    static_assert(2 * BN_MAX <= 512, "two accumulators must fit in TMEM");
-};
-
-struct Smem {
-    uint32_t base;  // 1 KB aligned start of the ring
-    uint32_t full0, empty0, accf0, acce0, done;
-    uint32_t* tmem_slot;
-    volatile int* abort_flag;
-};
-
-template <int BN_MAX, int STAGES>
-__device__ __forceinline__ Smem carve(uint8_t* raw_ptr) {
-    using L = Layout<BN_MAX, STAGES>;
-    const uint32_t raw = smem_u32(raw_ptr);
-    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    Smem s;
-    s.base = raw + pad;
-    s.full0 = s.base + L::RING;
-    s.empty0 = s.full0 + 8 * STAGES;
-    s.accf0 = s.empty0 + 8 * STAGES;
-    s.acce0 = s.accf0 + 16;
-    s.done = s.acce0 + 16;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(raw_ptr + pad + L::MISC);
-    s.abort_flag = reinterpret_cast<volatile int*>(raw_ptr + pad + L::MISC + 4);
-    return s;
-}
-
-// Barrier init, TMEM allocation; returns the TMEM base address.
-template <int BN_MAX, int STAGES>
-__device__ __forceinline__ uint32_t gemm_setup(const Smem& sm, int epi_warps) {
-    using L = Layout<BN_MAX, STAGES>;
-    const int warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(sm.full0 + 8 * s, 1);
-            mbar_init(sm.empty0 + 8 * s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(sm.accf0 + 8 * b, 1);
-            mbar_init(sm.acce0 + 8 * b, epi_warps);
-        }
-        mbar_init(sm.done, 1);
-        *sm.abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(smem_u32(sm.tmem_slot), L::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    return *sm.tmem_slot;
-}
-
-template <int BN_MAX, int STAGES>
-__device__ __forceinline__ void gemm_teardown(const Smem& sm, uint32_t tmem) {
-    using L = Layout<BN_MAX, STAGES>;
-    tc_fence_before();
-    __syncthreads();
-    if ((threadIdx.x >> 5) == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, L::TMEM_COLS);
-    }
-}
-
-__device__ __forceinline__ void raise_abort(const Smem& sm, int* status) {
-    *sm.abort_flag = 1;
-    atomicOr(status, kStatusWaitTimeout);
-}
-
-// Producer: streams the nkb K blocks of one job.  `loads` counts ring slots
-// filled so far by this CTA (slot = loads % STAGES, pass = loads / STAGES).
-// With `weights_first` (the first job of a programmatic dependent launch,
-// ring still empty) the weight tiles of the first ring pass are issued before
-// waiting for the previous kernel, and the activation tiles after it.
-template <int BN_MAX, int STAGES>
-__device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, const CUtensorMap* tmA,
-                                            const CUtensorMap* tmB, int a_row, int b_row, int kb0, int nkb,
-                                            int bn, bool weights_first, uint64_t timeout_ns) {
-    using L = Layout<BN_MAX, STAGES>;
-    const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + bn * kBK * 2);
-    int i = 0;
-    if (weights_first) {
-        const int pre = nkb < STAGES ? nkb : STAGES;
-        for (int k = 0; k < pre; ++k) {
-            mbar_arrive_expect_tx(sm.full0 + 8 * k, tx);
-            tma_load_2d(sm.base + k * L::STAGE + L::A_BYTES, tmB, sm.full0 + 8 * k, (kb0 + k) * kBK, b_row);
-        }
-        pdl_wait();
-        for (int k = 0; k < pre; ++k)
-            tma_load_2d(sm.base + k * L::STAGE, tmA, sm.full0 + 8 * k, (kb0 + k) * kBK, a_row);
-        i = pre;
-        loads += pre;
-    }
-    for (; i < nkb; ++i, ++loads) {
-        const int s = loads % STAGES;
-        const uint32_t ph = (loads / STAGES) & 1;
-        if (!mbar_wait(sm.empty0 + 8 * s, ph ^ 1, timeout_ns, sm.abort_flag)) return false;
-        const uint32_t sa = sm.base + s * L::STAGE;
-        mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
-        tma_load_2d(sa, tmA, sm.full0 + 8 * s, (kb0 + i) * kBK, a_row);
-        tma_load_2d(sa + L::A_BYTES, tmB, sm.full0 + 8 * s, (kb0 + i) * kBK, b_row);
-    }
-    return true;
-}
-
-// Decode schedules stream weights that are read once.  A job's weight rows
-// form one contiguous slab of memory, but the ring reads it as 64-column
-// boxes, i.e. one 128-byte piece per row at the row stride.  Prefetching the
-// slab into L2 as contiguous ranges when the job starts turns that into
-// sequential DRAM bursts and keeps far more bytes in flight than the
-// shared-memory ring can hold.
-__device__ __forceinline__ void prefetch_slab(const void* base, size_t bytes) {
-    const char* p = static_cast<const char*>(base);
-    constexpr size_t kChunk = 32768;
-    for (size_t o = 0; o < bytes; o += kChunk) {
-        const size_t n = bytes - o < kChunk ? bytes - o : kChunk;
-        bulk_prefetch_l2(p + o, static_cast<uint32_t>(n));
-    }
-}
-
-// No copy may still be landing in shared memory when the CTA leaves.
-template <int STAGES>
-__device__ __forceinline__ void drain_loads(const Smem& sm, uint32_t loads, uint64_t timeout_ns) {
-    for (uint32_t l = loads > STAGES ? loads - STAGES : 0; l < loads; ++l)
-        mbar_wait(sm.full0 + 8 * (l % STAGES), (l / STAGES) & 1, timeout_ns, nullptr);
-}
-
-// MMA issuer: one accumulation chain of nkb K blocks into TMEM buffer
-// (chain & 1), after the epilogue released that buffer's previous chain.
-template <int BN_MAX, int STAGES>
-__device__ __forceinline__ bool mma_chain(const Smem& sm, uint32_t& consumed, uint32_t chain, int nkb,
-                                          uint32_t tmem, uint32_t idesc, uint64_t timeout_ns) {
-    using L = Layout<BN_MAX, STAGES>;
-    const uint32_t b = chain & 1;
-    if (!mbar_wait(sm.acce0 + 8 * b, ((chain >> 1) & 1) ^ 1, timeout_ns, sm.abort_flag)) return false;
-    tc_fence_after();
-    const uint32_t dacc = tmem + b * BN_MAX;
-    for (int i = 0; i < nkb; ++i, ++consumed) {
-        const int s = consumed % STAGES;
-        const uint32_t ph = (consumed / STAGES) & 1;
-        if (!mbar_wait(sm.full0 + 8 * s, ph, timeout_ns, sm.abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sa = sm.base + s * L::STAGE;
-        const uint64_t ad = smem_desc_sw128(sa);
-        const uint64_t bd = smem_desc_sw128(sa + L::A_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes of K per instruction
-            mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (i == 0 && kk == 0) ? 0u : 1u);
-        mma_commit(sm.empty0 + 8 * s);
-    }
-    mma_commit(sm.accf0 + 8 * b);
-    return true;
-}
-
-// Epilogue side of a chain: wait for it (warp-uniform result) ...
-__device__ __forceinline__ bool epi_acquire(const Smem& sm, uint32_t chain, uint64_t timeout_ns) {
-    bool got = mbar_wait(sm.accf0 + 8 * (chain & 1), (chain >> 1) & 1, timeout_ns, sm.abort_flag);
-    got = __all_sync(0xffffffffu, got);
-    tc_fence_after();
-    return got;
-}
-
-// ... and hand the buffer back to the MMA warp (one arrival per warp).
-__device__ __forceinline__ void epi_release(const Smem& sm, uint32_t chain) {
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(sm.acce0 + 8 * (chain & 1));
-}
-
-// ------------------------------------------------------- compression (x W_a^T)
-//
-// The tensor core adds each K=16 product group into its FP32 accumulator with
-// a limited-precision aligned sum, and that error grows with the length of
-// the accumulation chain (measured on GB300: one 448-instruction chain flips
-// ~0.5% of the BF16-rounded outputs against the exact sum).  The compression
-// output is rounded to BF16 and then feeds the RMSNorm, the q projection and
-// the per-token INT8 codes, so this kernel keeps every tensor-core chain
-// short: the MMA warp restarts a fresh TMEM accumulator every `group` K
-// blocks, and the epilogue warps drain each chain into registers (TwoSum
-// error-free accumulation, or plain FP32 adds) while the next chain runs.
-
-constexpr int kDrainEpiWarps = 8;  // two warps per TMEM lane quarter, one per column half
-constexpr int kCompressThreads = 64 + 32 * kDrainEpiWarps;
 
 template <int BN_MAX, int STAGES>
 __global__ void __launch_bounds__(kCompressThreads, 1)
     mla_compress_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const __grid_constant__ CUtensorMap tm_wa, const CompressParams p) {
-    constexpr int HALF = BN_MAX / 2;  // columns per epilogue thread
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve<BN_MAX, STAGES>(smem_raw);
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kDrainEpiWarps);
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int per_m = p.n_tiles * p.splits;
-    const int njobs = p.m_tiles * per_m;
-    const int group = p.group;
-    auto job_of = [&](int j, int& m0, int& n0, int& split, int& kb0, int& nkb) {
-        const int m = j / per_m, r = j - m * per_m;
-        const int n = r / p.splits;
-        split = r - n * p.splits;
-        m0 = m * kBM;
-        n0 = n * p.bn;
-        kb0 = split * p.kb_total / p.splits;
-        nkb = (split + 1) * p.kb_total / p.splits - kb0;
-    };
-
-    if (warp == 0 && lane != 0 && p.prefetch_l2) {
-        // Warm L2 with the small inputs the norm and expansion kernels read
-        // (cos/sin rows of this batch's positions, gamma): when they run, HBM
-        // queues are full of weight traffic and a miss there waits behind it.
-        const int nthr = 31 * static_cast<int>(gridDim.x);
-        for (int t = static_cast<int>(blockIdx.x) * 31 + lane - 1; t < p.T; t += nthr) {
-            const int pos = p.positions[t];
-            if (pos >= 0 && pos < p.max_pos)
-                bulk_prefetch_l2(p.cos_sin + static_cast<size_t>(pos) * p.R, static_cast<uint32_t>(p.R * 4));
-        }
-        if (blockIdx.x == 0 && lane == 1 && p.n_gamma > 0)
-            bulk_prefetch_l2(p.gamma, static_cast<uint32_t>(p.n_gamma * 2));
-    }
-    if (warp == 0) {
-        if (lane == 0) {
-            prefetch_tensormap(&tm_x);
-            prefetch_tensormap(&tm_wa);
-            uint32_t loads = 0;
-            for (int j = blockIdx.x; j < njobs; j += gridDim.x) {
-                int m0, n0, split, kb0, nkb;
-                job_of(j, m0, n0, split, kb0, nkb);
-                if (!produce_job<BN_MAX, STAGES>(sm, loads, &tm_x, &tm_wa, m0, n0, kb0, nkb, p.bn, false,
-                                                 p.timeout_ns)) {
-                    raise_abort(sm, p.status);
-                    break;
-                }
-            }
-            drain_loads<STAGES>(sm, loads, p.timeout_ns);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
-            uint32_t consumed = 0, chain = 0;
-            bool ok = true;
-            for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x) {
-                int m0, n0, split, kb0, nkb;
-                job_of(j, m0, n0, split, kb0, nkb);
-                for (int k = 0; k < nkb && ok; k += group, ++chain)
-                    ok = mma_chain<BN_MAX, STAGES>(sm, consumed, chain, nkb - k < group ? nkb - k : group, tmem,
-                                                   idesc, p.timeout_ns);
-            }
-            if (!ok) raise_abort(sm, p.status);
-            // Every issued MMA must have finished before TMEM is released.
-            mma_commit(sm.done);
-            mbar_wait(sm.done, 0, p.timeout_ns, nullptr);
-        }
-    } else {
-        const int ew = warp - 2;
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-        const int half = ew >> 2;      // column half
-        const int row = quarter * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t chain = 0;
-        bool ok = true;
-        for (int j = blockIdx.x; j < njobs && ok; j += gridDim.x) {
-            int m0, n0, split, kb0, nkb;
-            job_of(j, m0, n0, split, kb0, nkb);
-            // column pairs in packed f32x2 registers: half the drain instructions
-            uint64_t acc[HALF / 2], cmp[HALF / 2];
-#pragma unroll
-            for (int c = 0; c < HALF / 2; ++c) acc[c] = cmp[c] = 0ull;
-            for (int k = 0; k < nkb; k += group, ++chain) {
-                if (!epi_acquire(sm, chain, p.timeout_ns)) { ok = false; break; }
-                const uint32_t src = tmem + lane_off + (chain & 1) * BN_MAX + half * HALF;
-#pragma unroll
-                for (int c = 0; c < HALF; c += 16) {
-                    if (half * HALF + c < p.bn) {  // warp-uniform
-                        float v[16];
-                        tmem_ld16(src + c, v);
-                        if (p.compensated) {
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2)
-                                two_sum_add2(acc[(c + e) / 2], cmp[(c + e) / 2], pk2(v[e], v[e + 1]));
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2)
-                                acc[(c + e) / 2] = add2(acc[(c + e) / 2], pk2(v[e], v[e + 1]));
-                        }
-                    }
-                }
-                epi_release(sm, chain);
-            }
-            if (!ok) break;
-            const int t = m0 + row;
-            if (t < p.T) {
-                float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
-#pragma unroll
-                for (int c = 0; c < HALF; c += 8) {
-                    if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA) {
-                        float o[8];
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) upk2(add2(acc[(c + e) / 2], cmp[(c + e) / 2]), o[e], o[e + 1]);
-                        st_v8(dst + c, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
-                    }
-                }
-            }
-        }
-        if (!ok && lane == 0) atomicOr(p.status, kStatusWaitTimeout);
-    }
-    gemm_teardown<BN_MAX, STAGES>(sm, tmem);
+    RoleCounters rc;
+    compress_phase<BN_MAX, STAGES, BN_MAX>(sm, tmem, &tm_x, &tm_wa, p, rc, blockIdx.x, gridDim.x);
+    gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
-
-// -------------------------------------------------- expansion (normed W_b^T)
-
-constexpr int kExpandEpiWarps = 8;  // two warps per TMEM lane quarter, one per column half
-constexpr int kExpandThreads = 64 + 32 * kExpandEpiWarps;
-
-// Job j -> (tile, token tile).  Tiles [0, nq_tiles) are q heads, the rest kv
-// tiles.  Jobs go through the tiles in groups of group_n: all token tiles of
-// a group before the next group, so the weights of a group stay in L2 while
-// every token tile passes through them.
-__device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& tile, int& m_tile) {
-    const int ntiles = p.nq_tiles + p.nkv_tiles;
-    const int per_group = p.group_n * p.m_tiles;
-    const int g = j / per_group, r = j - g * per_group;
-    const int gw = ntiles - g * p.group_n < p.group_n ? ntiles - g * p.group_n : p.group_n;
-    m_tile = r / gw;
-    tile = g * p.group_n + (r - m_tile * gw);
-}
-
-// Per-row state of the expansion epilogue: the row's token, whether its
-// position is valid, and (for the q path, R <= 64) its cos/sin row.  Loaded
-// once per token tile, while the epilogue warps wait for the accumulator, so
-// the RoPE does not wait on global loads between TMEM loads.
-struct RowCtx {
-    int t;
-    bool in, valid;
-    float c[32], s[32];
-};
-
-__device__ __forceinline__ void load_row_ctx(const ExpandParams& p, int t, RowCtx& rc) {
-    rc.t = t;
-    rc.in = t < p.T;
-    const int pos = rc.in ? p.positions[t] : 0;
-    rc.valid = rc.in && pos >= 0 && pos < p.max_pos;
-    if (p.nq_tiles > 0 && p.R <= 64) {
-        const int half = p.R / 2;
-        const float* cs = p.cos_sin + static_cast<size_t>(rc.valid ? pos : 0) * p.R;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            if (i < half) {
-                const float4 c4 = *reinterpret_cast<const float4*>(cs + i);
-                const float4 s4 = *reinterpret_cast<const float4*>(cs + half + i);
-                rc.c[i] = c4.x, rc.c[i + 1] = c4.y, rc.c[i + 2] = c4.z, rc.c[i + 3] = c4.w;
-                rc.s[i] = s4.x, rc.s[i + 1] = s4.y, rc.s[i + 2] = s4.z, rc.s[i + 3] = s4.w;
-            }
-        }
-    }
-}
-
-// x*cos + rotate_half(x)*sin on 8 pairs, rotate_half(x1, x2) = (-x2, x1)
-__device__ __forceinline__ void rope8(const float (&a)[8], const float (&b)[8], const float* cc, const float* ss,
-                                      float (&o1)[8], float (&o2)[8]) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        o1[e] = __fadd_rn(__fmul_rn(a[e], cc[e]), __fmul_rn(-b[e], ss[e]));
-        o2[e] = __fadd_rn(__fmul_rn(b[e], cc[e]), __fmul_rn(a[e], ss[e]));
-    }
-}
-
-// q head h of one token row: FP32 q, RoPE of its rope slice, per-token max
-// |q|.  Column half 0 takes the nope columns, half 1 the rope slice.
-__device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int h,
-                                                  int half_idx) {
-    const int Dn = p.Dn, R = p.R;
-    const int t = rc.t;
-    const bool in = rc.in, valid = rc.valid;
-    float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * (Dn + R);
-    float amax = 0.0f;
-    for (int c = 0; c < (half_idx == 0 ? Dn : 0); c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
-        if (in) {
-            if (!valid) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = 0.0f;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
-            st_v8(qrow + c, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
-            st_v8(qrow + c + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
-        }
-    }
-    const int half = R / 2;
-    auto finish = [&](int i, const float (&o1)[8], const float (&o2)[8]) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
-        st_v8(qrow + Dn + i, o1[0], o1[1], o1[2], o1[3], o1[4], o1[5], o1[6], o1[7]);
-        st_v8(qrow + Dn + half + i, o2[0], o2[1], o2[2], o2[3], o2[4], o2[5], o2[6], o2[7]);
-    };
-    if (half_idx == 0) {
-        // nope columns only
-    } else if (R <= 64) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-            if (i < half) {  // warp-uniform
-                float a[8], b[8], o1[8], o2[8];
-                tmem_ld8(tbase + Dn + i, a);
-                tmem_ld8(tbase + Dn + half + i, b);
-                if (in) {
-                    if (valid) {
-                        rope8(a, b, rc.c + i, rc.s + i, o1, o2);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
-                    }
-                    finish(i, o1, o2);
-                }
-            }
-        }
-    } else {
-        // wide rope slices: cos/sin straight from the table
-        const int pos = in ? p.positions[t] : 0;
-        const float* cs = p.cos_sin + static_cast<size_t>(valid ? pos : 0) * R;
-        for (int i = 0; i < half; i += 8) {
-            float a[8], b[8], o1[8], o2[8];
-            tmem_ld8(tbase + Dn + i, a);
-            tmem_ld8(tbase + Dn + half + i, b);
-            if (in) {
-                if (valid) {
-                    float cc[8], ss[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) cc[e] = cs[i + e], ss[e] = cs[half + i + e];
-                    rope8(a, b, cc, ss, o1, o2);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
-                }
-                finish(i, o1, o2);
-            }
-        }
-    }
-    // |q| >= 0, so the order of the float bit patterns is the order of the values.
-    if (valid) atomicMax(p.amax + t, __float_as_uint(amax));
-}
-
-// kv columns [n0, n0 + bn) of [T, H, Dn + Dv] for one token row: k_nope
-// into K's first Dn columns, value into out_v, both BF16.  Column half h
-// takes columns [h * bn / 2, (h + 1) * bn / 2).
-__device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int n0,
-                                                   int half_idx) {
-    const int Dn = p.Dn, R = p.R, HD = p.Dn + p.Dv;
-    const int t = rc.t;
-    const int hw = p.bn_kv / 2;
-    for (int c = half_idx * hw; c < (half_idx + 1) * hw; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
-        const int n = n0 + c;
-        if (rc.in && n < p.NKV) {
-            const int h = n / HD;
-            const int j = n - h * HD;
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = rc.valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
-            uint16_t* dst = j < Dn ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (Dn + R) + j
-                                   : p.out_v + (static_cast<size_t>(t) * p.H + h) * p.Dv + (j - Dn);
-            if (p.out_aligned32) {
-                st_v8(dst, w);
-            } else {
-                uint4* d4 = reinterpret_cast<uint4*>(dst);
-                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-        }
-    }
-}
-
-// The jobs of this CTA: round robin over [0, njobs), or, when a balanced
-// table is given, entries [table[c], table[c + 1]) of the id list that
-// follows the gridDim.x + 1 start offsets.
-struct CtaJobs {
-    const int* table;
-    int begin, end;
-    __device__ __forceinline__ CtaJobs(const int* t, int njobs) : table(t) {
-        if (t) {
-            begin = t[blockIdx.x];
-            end = t[blockIdx.x + 1];
-        } else {
-            begin = 0;
-            end = (njobs - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-        }
-    }
-    __device__ __forceinline__ int operator[](int i) const {
-        return table ? table[gridDim.x + 1 + i] : static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
-    }
-};
 
 template <int BN_MAX, int STAGES>
 __global__ void __launch_bounds__(kExpandThreads, 1)
@@ -543,97 +30,10 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const Smem sm = carve<BN_MAX, STAGES>(smem_raw);
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kExpandEpiWarps);
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp != 0) pdl_wait();  // the producer waits after its first weight tiles
+    RoleCounters rc;
     const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles);
-    const int Dn = p.Dn, R = p.R;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            prefetch_tensormap(&tm_aq);
-            prefetch_tensormap(&tm_akv);
-            prefetch_tensormap(&tm_bq);
-            prefetch_tensormap(&tm_bkv);
-            uint32_t loads = 0;
-            bool ok = true;
-            auto prefetch = [&](int i) {
-                int tile, m;
-                expand_job(p, jobs[i], tile, m);
-                if (tile < p.nq_tiles) {
-                    const size_t head = static_cast<size_t>(Dn + R) * p.Lq * 2;
-                    prefetch_slab(static_cast<const char*>(p.w_qb) + head * tile, head);
-                } else {
-                    const int n0 = (tile - p.nq_tiles) * p.bn_kv;
-                    const int rows = p.NKV - n0 < p.bn_kv ? p.NKV - n0 : p.bn_kv;
-                    prefetch_slab(static_cast<const char*>(p.w_kvb) + static_cast<size_t>(n0) * p.Lkv * 2,
-                                  static_cast<size_t>(rows) * p.Lkv * 2);
-                }
-            };
-            for (int i = jobs.begin; i < jobs.end; ++i) {
-                int tile, m;
-                expand_job(p, jobs[i], tile, m);
-                const bool first = i == jobs.begin;
-                if (p.prefetch_l2) {
-                    if (first) prefetch(i);
-                    if (i + 1 < jobs.end) prefetch(i + 1);
-                }
-                ok = tile < p.nq_tiles
-                         ? produce_job<BN_MAX, STAGES>(sm, loads, &tm_aq, &tm_bq, m * kBM, tile * (Dn + R), 0,
-                                                       p.kb_q, Dn + R, first, p.timeout_ns)
-                         : produce_job<BN_MAX, STAGES>(sm, loads, &tm_akv, &tm_bkv, m * kBM,
-                                                       (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
-                                                       p.timeout_ns);
-                if (!ok) break;
-            }
-            if (loads == 0) pdl_wait();
-            if (!ok) raise_abort(sm, p.status);
-            drain_loads<STAGES>(sm, loads, p.timeout_ns);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc_q = idesc_bf16_f32(kBM, Dn + R);
-            const uint32_t idesc_kv = idesc_bf16_f32(kBM, p.bn_kv);
-            uint32_t consumed = 0, chain = 0;
-            bool ok = true;
-            for (int i = jobs.begin; i < jobs.end && ok; ++i, ++chain) {
-                int tile, m;
-                expand_job(p, jobs[i], tile, m);
-                const bool q = tile < p.nq_tiles;
-                ok = mma_chain<BN_MAX, STAGES>(sm, consumed, chain, q ? p.kb_q : p.kb_kv, tmem,
-                                               q ? idesc_q : idesc_kv, p.timeout_ns);
-            }
-            if (!ok) raise_abort(sm, p.status);
-            mma_commit(sm.done);
-            mbar_wait(sm.done, 0, p.timeout_ns, nullptr);
-        }
-    } else {
-        const int quarter = warp & 3;        // TMEM lane quarter this warp may access
-        const int half_idx = (warp - 2) >> 2;  // column half
-        const int row = quarter * 32 + lane;
-        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t chain = 0;
-        int cur_m = -1;
-        RowCtx rc;
-        for (int i = jobs.begin; i < jobs.end; ++i, ++chain) {
-            int tile, m;
-            expand_job(p, jobs[i], tile, m);
-            if (m != cur_m) {  // before waiting for the accumulator
-                load_row_ctx(p, m * kBM + row, rc);
-                cur_m = m;
-            }
-            if (!epi_acquire(sm, chain, p.timeout_ns)) {
-                if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
-                break;
-            }
-            const uint32_t tbase = tmem + lane_off + (chain & 1) * BN_MAX;
-            if (tile < p.nq_tiles)
-                expand_q_epilogue(p, tbase, rc, tile, half_idx);
-            else
-                expand_kv_epilogue(p, tbase, rc, (tile - p.nq_tiles) * p.bn_kv, half_idx);
-            epi_release(sm, chain);
-        }
-    }
-    gemm_teardown<BN_MAX, STAGES>(sm, tmem);
+    expand_phase<BN_MAX, STAGES>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true);
+    gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
 
 // ------------------------------------------------------------ self-test

@@ -88,6 +88,26 @@ struct QuantParams {
     float* scale;
 };
 
+// The cooperative decode kernel: the four steps as phases of one launch.
+struct DecodeParams {
+    CompressParams a;
+    NormRopeParams n;
+    ExpandParams b;
+    QuantParams q;               // q.rows == 0 without a q path
+    unsigned* bar;               // grid barrier: [arrivals, generation]
+    size_t early_prefetch_bytes; // L2 prefetch of each CTA's first expansion weights during phase A
+    int* status;
+    uint64_t timeout_ns;
+};
+
+size_t decode_smem_bytes(int norm_row_elems);
+cudaError_t decode_set_attributes(size_t smem);
+cudaError_t decode_occupancy(size_t smem, int* blocks_per_sm);
+cudaError_t launch_decode(int grid, size_t smem, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
+                          const CUtensorMap& tm_aq, const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
+                          const CUtensorMap& tm_bkv, const DecodeParams& p, cudaStream_t st);
+constexpr int kDecodeMaxBN = 192;  // widest expansion tile the decode kernel takes
+
 // Shapes of the GEMM kernel instantiations.
 // Expansion kernel: Wide = BN_MAX 256, 4 stages; Mid = BN_MAX 192, 5 stages
 // (decode with a q path: one head of Dn + R <= 192 columns per tile);

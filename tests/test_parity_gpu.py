@@ -181,3 +181,30 @@ def test_timing_events_hook():
     assert all(t >= 0 for t in times)
     p.set_timing_events([])
     p.close()
+
+
+@pytest.mark.parametrize("name", ["tiny_q", "v2lite_decode", "v3_decode"])
+def test_fused_decode_kernel_matches_four_kernels(name):
+    """The cooperative decode kernel runs the same arithmetic as the four
+    standalone kernels, so their outputs must be bit-identical."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    d = inp.dims
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    fused = p.kernel_names() == ["mla_decode_kernel"]
+    assert fused, "decode-sized batches should default to the cooperative kernel"
+    a = alloc_outputs(d, DEV)
+    run_prolog(p, dins, a)
+    assert p.device_status() == 0
+    p.set_tuning(binding.TUNE_DECODE_FUSED, 0)
+    assert p.kernel_names()[0] == "mla_compress_kernel"
+    b = alloc_outputs(d, DEV)
+    run_prolog(p, dins, b)
+    assert p.device_status() == 0
+    for k in a:
+        x, y = a[k].t, b[k].t
+        if x.dtype != torch.float32:
+            x, y = x.view(torch.uint8), y.view(torch.uint8)
+        assert torch.equal(x, y), k
+    p.close()
