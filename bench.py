@@ -170,6 +170,9 @@ def kernel_work(d: wl.Dims):
         "mla_quant_kernel": 0,
     }
     assert sum(b.values()) == wl.algorithmic_bytes(d)
+    # the cooperative decode kernel runs every step in one launch
+    b["mla_decode_kernel"] = wl.algorithmic_bytes(d)
+    f["mla_decode_kernel"] = wl.algorithmic_flops(d)
     return b, f
 
 

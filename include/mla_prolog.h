@@ -216,9 +216,9 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            error-free TwoSum; 0: with plain FP32 adds.   */
 #define MLA_TUNE_COMPRESS_COMPENSATED 2
 /*   MLA_TUNE_DECODE_FUSED    1: batches of at most 128 tokens run as one
- *                            cooperative kernel (the default where the dims
- *                            and the device allow it); 0: as four kernels.
- *                            INVALID_ARG when 1 is not available.          */
+ *                            cooperative kernel (where the dims and the
+ *                            device allow it); 0 (the default): as four
+ *                            kernels.  INVALID_ARG when 1 is not available. */
 #define MLA_TUNE_DECODE_FUSED 3
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 

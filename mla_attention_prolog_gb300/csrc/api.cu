@@ -219,10 +219,15 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             h->fused_ok = true;
         cudaGetLastError();
     }
-    h->fused = h->fused_ok;
-    const int table_grid = h->fused ? sms : h->expand_grid;
+    // Off by default: a grid-wide barrier across 152 CTAs costs about 2 us on
+    // GB300 (both dies' L2s take part), so the kernel's three barriers cost
+    // more than the overlapped (PDL) hand-offs of the four-kernel path.
+    h->fused = false;
+    // A table is needed only when there are more jobs than SMs; the expansion
+    // grid and the cooperative grid are then both one CTA per SM, so one
+    // table serves either path.
     std::vector<int> table;
-    if (h->decode && njobs_b > table_grid) {
+    if (h->decode && njobs_b > sms) {
         const int nq = Lq > 0 ? d.num_heads : 0;
         std::vector<std::pair<long long, int>> w;  // (-bytes, job) sorted: heaviest first
         const int ntiles = nq + cdiv(h->NKV, h->bn_kv), gn = 16;
@@ -235,7 +240,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             w.push_back({-bytes, j});
         }
         std::sort(w.begin(), w.end());
-        const int G = table_grid;
+        const int G = sms;
         std::vector<long long> load(G, 0);
         std::vector<std::vector<int>> lists(G);
         for (const auto& e : w) {

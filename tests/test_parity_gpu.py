@@ -192,8 +192,9 @@ def test_fused_decode_kernel_matches_four_kernels(name):
     d = inp.dims
     dins = device_inputs(inp, DEV)
     p = binding.MlaProlog.from_dims(d)
-    fused = p.kernel_names() == ["mla_decode_kernel"]
-    assert fused, "decode-sized batches should default to the cooperative kernel"
+    assert p.kernel_names()[0] == "mla_compress_kernel", "four kernels are the default"
+    p.set_tuning(binding.TUNE_DECODE_FUSED, 1)
+    assert p.kernel_names() == ["mla_decode_kernel"]
     a = alloc_outputs(d, DEV)
     run_prolog(p, dins, a)
     assert p.device_status() == 0
