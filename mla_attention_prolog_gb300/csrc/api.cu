@@ -166,42 +166,15 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const int sms = prop.multiProcessorCount;
     h->sms = sms;
 
-    // Schedule: few token tiles -> decode (weights streamed by many narrow or
-    // split-K tiles); otherwise prefill (wide tiles, tensor-core bound).
-    h->decode = h->m_tiles <= 2;
-    const int kb_a = cdiv(d.D, kBK);
-    if (h->decode) {
-        h->shape_a = GemmShape::Wide;  // 128-wide weight tiles: more weight bytes in flight per stage
-        h->bn_a = 128;
-        const int tiles = cdiv(h->NA, h->bn_a) * h->m_tiles;
-        int s = sms / (tiles > 0 ? tiles : 1);
-        if (s < 1) s = 1;
-        if (s > kb_a / 2) s = kb_a / 2 > 0 ? kb_a / 2 : 1;
-        h->splits_a = s;
-    } else {
-        h->shape_a = GemmShape::Wide;
-        h->bn_a = 128;
-        h->splits_a = 1;
-    }
-    // Accumulation chain length (K blocks) of the compression projection and
-    // TwoSum draining: measured on GB300 to keep INT8 code flips of the
-    // V3-shaped q path at 3-4.5e-4 (bar: 1e-3) at the lowest cost.
-    h->group_a = h->decode ? 2 : 4;
+    const Schedule sc = plan_schedule(d.T, d.D, Lq, Lkv, R, d.num_heads, d.nope_dim, d.v_dim, sms);
+    h->decode = sc.decode;
+    h->shape_a = sc.shape_a;
+    h->bn_a = sc.bn_a;
+    h->splits_a = sc.splits_a;
+    h->group_a = sc.group_a;
     h->compensated = 1;
-    // Expansion: prefill uses 256-wide kv tiles (one head of V2/V3); decode
-    // without a q path uses the narrow kernel with enough tiles to cover the
-    // SMs; decode with a q path shares the wide kernel with the q heads.
-    if (!h->decode) {
-        h->shape_b = GemmShape::Wide;
-        h->bn_kv = 256;
-    } else if (Lq == 0) {
-        h->shape_b = GemmShape::Narrow;
-        h->bn_kv = cdiv(h->NKV, 64) * h->m_tiles >= sms ? 64 : 32;
-    } else {
-        // one q head per tile: the 192-wide, 5-stage shape when the head fits
-        h->shape_b = d.nope_dim + R <= 192 ? GemmShape::Mid : GemmShape::Wide;
-        h->bn_kv = 128;
-    }
+    h->shape_b = sc.shape_b;
+    h->bn_kv = sc.bn_kv;
 
     // Decode expansion: jobs of unequal size (a q head streams (Dn+R)*Lq
     // weights, a kv tile bn_kv*Lkv); assign them to the CTAs longest first,
@@ -424,7 +397,6 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.m_tiles = h->m_tiles;
     pb.group_n = 16;
     pb.job_table = h->job_table;
-    pb.prefetch_l2 = h->decode ? 1 : 0;
     pb.w_qb = wb;
     pb.w_kvb = wb + static_cast<size_t>(h->NQ) * Lq;
     pb.Lq = Lq;

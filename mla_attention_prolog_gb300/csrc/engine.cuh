@@ -146,12 +146,8 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
     return true;
 }
 
-// Decode schedules stream weights that are read once.  A job's weight rows
-// form one contiguous slab of memory, but the ring reads it as 64-column
-// boxes, i.e. one 128-byte piece per row at the row stride.  Prefetching the
-// slab into L2 as contiguous ranges when the job starts turns that into
-// sequential DRAM bursts and keeps far more bytes in flight than the
-// shared-memory ring can hold.
+// Contiguous L2 prefetch of a weight slab (the cooperative kernel's early
+// prefetch of its first expansion job).
 __device__ __forceinline__ void prefetch_slab(const void* base, size_t bytes) {
     const char* p = static_cast<const char*>(base);
     constexpr size_t kChunk = 32768;
@@ -412,21 +408,6 @@ struct CtaJobs {
 };
 
 
-// L2 prefetch of one expansion job's weight slab (decode: weights read once).
-__device__ __forceinline__ void expand_prefetch(const ExpandParams& p, const CtaJobs& jobs, int i) {
-    int tile, m;
-    expand_job(p, jobs[i], tile, m);
-    if (tile < p.nq_tiles) {
-        const size_t head = static_cast<size_t>(p.Dn + p.R) * p.Lq * 2;
-        prefetch_slab(static_cast<const char*>(p.w_qb) + head * tile, head);
-    } else {
-        const int n0 = (tile - p.nq_tiles) * p.bn_kv;
-        const int rows = p.NKV - n0 < p.bn_kv ? p.NKV - n0 : p.bn_kv;
-        prefetch_slab(static_cast<const char*>(p.w_kvb) + static_cast<size_t>(n0) * p.Lkv * 2,
-                      static_cast<size_t>(rows) * p.Lkv * 2);
-    }
-}
-
 // Counters each role carries from one job (and one phase) to the next: ring
 // slots filled (producer), ring slots consumed and accumulator chains issued
 // (MMA), accumulator chains drained (epilogue).
@@ -575,10 +556,6 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 int tile, m;
                 expand_job(p, jobs[i], tile, m);
                 const bool first = pdl_first && i == jobs.begin;
-                if (p.prefetch_l2) {
-                    if (i == jobs.begin) expand_prefetch(p, jobs, i);
-                    if (i + 1 < jobs.end) expand_prefetch(p, jobs, i + 1);
-                }
                 ok = tile < p.nq_tiles
                          ? produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_aq, tm_bq, m * kBM, tile * (Dn + R), 0, p.kb_q,
                                                        Dn + R, first, p.timeout_ns)

@@ -109,33 +109,11 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     int sms = 0;
     int rc = setup_device(dev, &scratch, &sms);
     if (rc != MLA_OK) return rc;
-    const bool decode = m_tiles <= 2;
+    const Schedule sc = plan_schedule(d.T, d.D, Lq, Lkv, R, H, d.nope_dim, d.v_dim, sms);
+    const bool decode = sc.decode;
+    const GemmShape shape_a = sc.shape_a, shape_b = sc.shape_b;
+    const int bn_a = sc.bn_a, splits_a = sc.splits_a, bn_kv = sc.bn_kv, group_a = sc.group_a;
     const int kb_a = cdiv(d.D, kBK);
-    GemmShape shape_a, shape_b;
-    int bn_a, splits_a = 1, bn_kv, group_a;
-    if (decode) {
-        shape_a = GemmShape::Wide;
-        bn_a = 128;
-        const int tiles = cdiv(NA, bn_a) * m_tiles;
-        int s = sms / (tiles > 0 ? tiles : 1);
-        if (s < 1) s = 1;
-        if (s > kb_a / 2) s = kb_a / 2 > 0 ? kb_a / 2 : 1;
-        splits_a = s;
-    } else {
-        shape_a = GemmShape::Wide;
-        bn_a = 128;
-    }
-    group_a = decode ? 2 : 4;
-    if (!decode) {
-        shape_b = GemmShape::Wide;
-        bn_kv = 256;
-    } else if (Lq == 0) {
-        shape_b = GemmShape::Narrow;
-        bn_kv = cdiv(NKV, 64) * m_tiles >= sms ? 64 : 32;
-    } else {
-        shape_b = d.nope_dim + R <= 192 ? GemmShape::Mid : GemmShape::Wide;
-        bn_kv = 128;
-    }
 
     // Scratch layout (same order as the handle's workspace) and its limit.
     const size_t T = static_cast<size_t>(d.T);
@@ -255,7 +233,6 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.m_tiles = m_tiles;
     pb.group_n = 16;
     pb.job_table = nullptr;  // round robin: same per-job results as the balanced order
-    pb.prefetch_l2 = decode ? 1 : 0;
     pb.w_qb = wb;
     pb.w_kvb = wb + static_cast<size_t>(NQ) * Lq;
     pb.Lq = Lq;

@@ -62,8 +62,7 @@ struct ExpandParams {
     int nq_tiles, nkv_tiles, bn_kv;
     int m_tiles, group_n;  // token tiles; weight tiles per L2 group of the job order
     const int* job_table;  // balanced per-CTA job lists (null: round robin)
-    int prefetch_l2;       // prefetch each job's weight rows into L2 (decode)
-    const void* w_qb;      // W_q_b [NQ][Lq] and W_kv_b [NKV][Lkv], for the L2 prefetch
+    const void* w_qb;      // W_q_b [NQ][Lq] and W_kv_b [NKV][Lkv] (the cooperative kernel's early prefetch)
     const void* w_kvb;
     int Lq, Lkv;
     int kb_q, kb_kv;
@@ -117,6 +116,68 @@ constexpr int kDecodeMaxBN = 192;  // widest expansion tile the decode kernel ta
 // CTA and an expansion CTA fit on one SM and the expansion can start
 // streaming its weights while the compression is still running.
 enum class GemmShape { Wide, Mid, Narrow };
+
+// Tile shapes and work split of one problem size, chosen on the host.
+struct Schedule {
+    bool decode;          // few token tiles: weights streamed once by split-K / narrow tiles
+    int m_tiles;          // 128-token tiles
+    GemmShape shape_a;    // compression kernel shape
+    int bn_a, splits_a;   // compression weight-tile width, split-K factor
+    int group_a;          // K blocks per tensor-core accumulation chain (compression)
+    GemmShape shape_b;    // expansion kernel shape
+    int bn_kv;            // expansion kv tile width
+};
+
+inline int cdiv_host(int a, int b) { return (a + b - 1) / b; }
+
+// T tokens, D model width, Lq / Lkv / R ranks, H heads of Dn + R (q) and
+// Dn + Dv (kv) columns, on a device with `sms` SMs.
+inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int Dn, int Dv, int sms) {
+    Schedule s{};
+    const int NA = Lq + Lkv + R, NKV = H * (Dn + Dv);
+    const int kb_a = cdiv_host(D, kBK);
+    s.m_tiles = cdiv_host(T, kBM);
+    s.decode = s.m_tiles <= 2;
+    s.shape_a = GemmShape::Wide;
+    s.bn_a = 128;
+    s.splits_a = 1;
+    if (s.decode) {
+        // Split-K over weight tiles of 128 columns or a little less: the
+        // width (multiple of 16) that puts the most CTAs to work, the widest
+        // on a tie (more weight bytes in flight per ring stage).
+        int best = 0;
+        for (int bn = 128; bn >= 96; bn -= 16) {
+            const int tiles = cdiv_host(NA, bn) * s.m_tiles;
+            int k = tiles > 0 ? sms / tiles : 1;
+            if (k > kb_a / 2) k = kb_a / 2;
+            if (k < 1) k = 1;
+            const int ctas = tiles * k <= sms ? tiles * k : 0;
+            if (ctas > best) best = ctas, s.bn_a = bn, s.splits_a = k;
+        }
+    }
+    // Accumulation chain length (K blocks) of the compression projection with
+    // TwoSum draining: measured on GB300 to keep INT8 code flips of the
+    // V3-shaped q path at 3-4.5e-4 (bar: 1e-3) at the lowest cost.
+    s.group_a = s.decode ? 2 : 4;
+    // Expansion: prefill uses 256-wide kv tiles (one head of V2/V3); decode
+    // without a q path uses the narrow kernel with enough tiles to cover the
+    // SMs; decode with a q path puts one q head per tile (the 192-wide,
+    // 5-stage shape when the head fits) and kv tiles as wide as the ring, so
+    // a kv K block moves as many weight bytes as a q one and the per-CTA job
+    // lists balance by bytes and by K blocks alike.
+    if (!s.decode) {
+        s.shape_b = GemmShape::Wide;
+        s.bn_kv = 256;
+    } else if (Lq == 0) {
+        s.shape_b = GemmShape::Narrow;
+        s.bn_kv = cdiv_host(NKV, 64) * s.m_tiles >= sms ? 64 : 32;
+    } else {
+        s.shape_b = Dn + R <= 192 ? GemmShape::Mid : GemmShape::Wide;
+        s.bn_kv = s.shape_b == GemmShape::Mid ? 192 : 256;
+    }
+    return s;
+}
+
 int gemm_smem_bytes(GemmShape s);
 
 // Launches `kernel`; with `pdl` the launch may overlap the tail of the

@@ -106,16 +106,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Starts bringing a 2-D tile of a tensor into L2 (no shared memory, no
-// completion): lets HBM work on tiles long before the shared-memory ring has
-// room for them.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 // Starts bringing a contiguous byte range into L2 (16-byte aligned address
 // and size): sequential DRAM bursts instead of one 128-byte piece per row.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
