@@ -91,7 +91,7 @@ struct mla_prolog {
     bool fused_ok = false;     // the dims and the device allow it
     bool fused = false;        // in use (tunable)
     size_t decode_smem = 0;
-    unsigned* bar = nullptr;   // its grid barrier [arrivals, generation]
+    unsigned* sync = nullptr;  // its hand-over counters (kSyncWords words)
     uint64_t timeout_ns = 1000000000ull;
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wqb{}, tm_wkvb{};
@@ -185,7 +185,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // kDecodeMaxBN columns and needs one resident CTA per SM.
     if (h->m_tiles == 1 && h->bn_kv <= kDecodeMaxBN && (Lq == 0 || d.nope_dim + R <= kDecodeMaxBN)) {
         int coop = 0, blocks = 0;
-        h->decode_smem = decode_smem_bytes(h->NA + R);
+        h->decode_smem = decode_smem_bytes(h->NA, R, Lq, Lkv);
         if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop &&
             decode_set_attributes(h->decode_smem) == cudaSuccess &&
             decode_occupancy(h->decode_smem, &blocks) == cudaSuccess && blocks >= 1)
@@ -235,7 +235,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t b_norm = al(T * (Lq + Lkv) * 2);
     const size_t b_q = Lq > 0 ? al(T * h->NQ * 4) : 0;
     const size_t b_amax = al(T * 4);
-    const size_t b_stat = 256;
+    const size_t b_stat = 1024;  // status word, then the cooperative kernel's counters
     const size_t b_tab = al(table.size() * sizeof(int));
     h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab;
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
@@ -248,7 +248,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->qws = Lq > 0 ? reinterpret_cast<float*>(w + b_part + b_norm) : nullptr;
     h->amax = reinterpret_cast<uint32_t*>(w + b_part + b_norm + b_q);
     h->status = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax);
-    h->bar = reinterpret_cast<unsigned*>(w + b_part + b_norm + b_q + b_amax + 64);
+    h->sync = reinterpret_cast<unsigned*>(w + b_part + b_norm + b_q + b_amax + 128);
 
     if ((e = cudaMemset(h->ws, 0, h->ws_bytes)) != cudaSuccess) {
         cudaFree(h->ws);
@@ -397,8 +397,6 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.m_tiles = h->m_tiles;
     pb.group_n = 16;
     pb.job_table = h->job_table;
-    pb.w_qb = wb;
-    pb.w_kvb = wb + static_cast<size_t>(h->NQ) * Lq;
     pb.Lq = Lq;
     pb.Lkv = Lkv;
     pb.kb_q = cdiv(Lq, kBK);
@@ -423,9 +421,8 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
         pd.n = pn;
         pd.b = pb;
         pd.q = pq;
-        pd.q.chunk = 4096;
-        pd.bar = h->bar;
-        pd.early_prefetch_bytes = 256 * 1024;
+        pd.q.chunk = 8192;  // one batch of eight loads per epilogue thread
+        pd.sync = h->sync;
         pd.status = h->status;
         pd.timeout_ns = h->timeout_ns;
         if ((e = launch_decode(h->sms, h->decode_smem, h->tm_x, h->tm_wa, h->tm_nq, h->tm_nkv, h->tm_wqb,
@@ -461,9 +458,9 @@ int mla_prolog_device_status(mla_prolog_t h, void* stream, int32_t* status) {
     if ((e = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpy(status)");
     if ((e = cudaMemset(h->status, 0, sizeof v)) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
-    // A barrier wait that gave up leaves its arrival count behind: reset it.
-    if ((v & MLA_STATUS_WAIT_TIMEOUT) && (e = cudaMemset(h->bar, 0, sizeof(unsigned))) != cudaSuccess)
-        return cuda_fail(e, "cudaMemset(barrier)");
+    // After a wait that gave up, start the cooperative kernel's counters over.
+    if ((v & MLA_STATUS_WAIT_TIMEOUT) && (e = cudaMemset(h->sync, 0, kSyncWords * sizeof(unsigned))) != cudaSuccess)
+        return cuda_fail(e, "cudaMemset(sync)");
     *status = v;
     return MLA_OK;
 }

@@ -1,79 +1,69 @@
 // Cooperative decode kernel: the whole prolog pass in one launch for batches
 // of at most one 128-token tile.
 //
-// With so few tokens every step of the multi-kernel pipeline is latency
-// bound, and the hand-offs between kernels (grid completion, the next
-// kernel's CTAs waiting for shared memory and registers on each SM) cost as
-// much as the work.  Here one CTA per SM runs the four steps as phases
-// separated by grid-wide barriers, keeping its shared-memory ring, TMEM
-// accumulators and barrier phase counters from one phase to the next:
+// With so few tokens every step is latency bound, and the hand-offs between
+// the four kernels (grid completion, the next kernel's CTAs waiting for an
+// SM) cost as much as the work.  Here one CTA per SM runs the steps as
+// phases and keeps its shared-memory ring, TMEM accumulators and barrier
+// counters from one phase to the next:
 //   A  compression projection (split-K partials, drained chains)
-//   B  split-K reduction + BF16 cast + RMSNorm + k_pe RoPE, one token per CTA
+//   B  split-K reduction + BF16 cast + RMSNorm + k_pe RoPE, one token per CTA,
+//      by the epilogue warps alone
 //   C  expansion projections with the split / RoPE / assemble epilogues
 //   D  per-token INT8 quantisation of q (q path only)
-// During A, each CTA already prefetches (into L2) the first weights it will
-// stream in C.  The launch is cooperative, so all CTAs are resident and the
-// barriers cannot wait on a CTA that has not started; every barrier wait is
-// bounded and reports MLA_STATUS_WAIT_TIMEOUT when it gives up.
+// The phases hand over through counters in global memory, not grid-wide
+// barriers, so only the warps that need a result wait for it: the producer
+// goes straight from the compression's loads to the expansion's weight tiles
+// and waits for the norm only before its first activation tiles; the MMA
+// warp waits on its ring as always; the epilogue warps wait for the
+// compression before the norm and for every q tile before the quantisation.
+// A grid-wide barrier costs about 2 us on GB300 (152 CTAs, two dies), so
+// the weight stream must not stop at one.
 //
-// Measured on GB300 the kernel loses to the four-kernel path: one grid-wide
-// barrier over 152 CTAs costs about 2 us even when every CTA arrives at once
-// (atomic counter, acquire/release atomics, a two-level tree and a per-CTA
-// flag array all land at 1.9-2.9 us), and each barrier here also drains the
-// phase's outstanding stores, while the four kernels hand off with
-// programmatic dependent launch and overlap each prologue with the previous
-// kernel's tail.  It stays selectable (MLA_TUNE_DECODE_FUSED) and is held to
-// bit-identical output with the four kernels.
+// Counters (`DecodeParams::sync`): an epoch (runs completed) and four arrival
+// counts that grow by a fixed amount per run, compared modulo 2^32 against
+// (epoch + 1) x that amount.  Every CTA arrives on every counter in every run,
+// also after a wait gave up, so the counts stay consistent; the last CTA to
+// finish advances the epoch.  The launch is cooperative: all CTAs are
+// resident, so no wait is on a CTA that has not started; every wait is
+// bounded and reports MLA_STATUS_WAIT_TIMEOUT when it gives up.
 #include "engine.cuh"
 #include "rows.cuh"
 
 namespace mlap {
 
 constexpr int kDecodeThreads = kExpandThreads;  // 2 + 8 warps, as the standalone GEMM kernels
-constexpr int kDecodeWarps = kDecodeThreads / 32;
+constexpr int kDecodeEpiFirst = 64;             // the epilogue warps: threads [64, 320)
+constexpr int kDecodeEpiThreads = kDecodeThreads - kDecodeEpiFirst;
 constexpr int kDecodeBN = 192;                  // smem ring / TMEM sized for a 192-wide q head
 constexpr int kDecodeStages = 5;
 constexpr int kDecodeCompressBN = 128;          // compression tile width (drain registers)
 using DLayout = Layout<kDecodeBN, kDecodeStages>;
 constexpr size_t kDecodeNormOff = (DLayout::BYTES + 127) & ~static_cast<size_t>(127);  // 16-byte aligned row
 static_assert(kCompressThreads == kDecodeThreads, "compression and expansion roles share the CTA shape");
+static_assert(kDecodeEpiThreads == 32 * kExpandEpiWarps, "the norm runs on the epilogue warps");
 
-// All-CTA barrier on a generation counter: bar[0] counts arrivals, bar[1] is
-// the generation.  The last CTA to arrive resets the count and bumps the
-// generation; the others wait (bounded) for the bump.  Writes before the
-// barrier are visible to every CTA after it.  Returns, uniformly over the
-// CTA, whether every thread of this CTA came in with `ok` and the wait did
-// not give up.
-__device__ __forceinline__ bool grid_barrier(bool ok_in, unsigned* bar, uint64_t timeout_ns, int* status,
-                                             int* ok_slot) {
-    const int all_ok = __syncthreads_and(ok_in ? 1 : 0);
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        volatile unsigned* vgen = bar + 1;
-        const unsigned gen = *vgen;
-        __threadfence();
-        const unsigned arrived = atomicAdd(bar, 1u) + 1u;
-        if (arrived == gridDim.x) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
-            const uint64_t t0 = global_timer_ns();
-            while (*vgen == gen) {
-                __nanosleep(64);
-                if (global_timer_ns() - t0 > timeout_ns) {
-                    ok = 0;
-                    atomicOr(status, kStatusWaitTimeout);
-                    break;
-                }
-            }
-        }
-        __threadfence();
-        *ok_slot = ok && all_ok;
+// Epilogue-group arrival: every thread's earlier writes are made visible at
+// GPU scope, then one thread adds `n` with release semantics.  Returns the
+// AND of `ok` over the group, so that the group's next steps (and their
+// named barriers) stay uniform even when one warp's wait gave up.
+__device__ __forceinline__ bool epi_arrive(unsigned* counter, unsigned n, bool ok) {
+    __threadfence();
+    const bool all = named_bar_and(1, kDecodeEpiThreads, ok);
+    if (threadIdx.x == kDecodeEpiFirst) red_release_gpu_add(counter, n);
+    return all;
+}
+
+// Epilogue-group wait: one thread waits (bounded), the group follows.
+// Returns, uniformly over the group, whether the count was reached.
+__device__ __forceinline__ bool epi_wait(const unsigned* counter, unsigned target, const DecodeParams& p,
+                                         const Smem& sm, int* ok_slot) {
+    if (threadIdx.x == kDecodeEpiFirst) {
+        const bool got = wait_counter(counter, target, p.timeout_ns, sm.abort_flag);
+        if (!got) atomicOr(p.status, kStatusWaitTimeout);
+        *ok_slot = got;
     }
-    __syncthreads();
-    // global data written by generic stores is read next by TMA (async proxy)
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+    named_bar_sync(1, kDecodeEpiThreads);
     return *ok_slot != 0;
 }
 
@@ -83,65 +73,75 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                       const __grid_constant__ CUtensorMap tm_bq, const __grid_constant__ CUtensorMap tm_bkv,
                       const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ float red[2 * kDecodeWarps];
-    __shared__ int bar_ok;
+    __shared__ float red[2];
+    __shared__ unsigned epoch_s;
+    __shared__ int epi_ok;
     const Smem sm = carve<kDecodeBN, kDecodeStages>(smem_raw);
     // the norm phase's BF16 row lives after the ring (and its alignment slack)
     uint16_t* crow = reinterpret_cast<uint16_t*>(smem_raw + kDecodeNormOff);
-    const uint32_t tmem = gemm_setup<kDecodeBN, kDecodeStages>(sm, kExpandEpiWarps);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) epoch_s = *reinterpret_cast<volatile unsigned*>(p.sync + kSyncEpoch);
+    const uint32_t tmem = gemm_setup<kDecodeBN, kDecodeStages>(sm, kExpandEpiWarps);  // includes __syncthreads
+    const unsigned run = epoch_s + 1u;
+    const unsigned grid = gridDim.x;
+    const int warp = threadIdx.x >> 5;
+    const bool epi = warp >= 2;
     RoleCounters rc;
     const CtaJobs jobs(p.b.job_table, (p.b.nq_tiles + p.b.nkv_tiles) * p.b.m_tiles);
 
-    // Phase C's first weights, into L2 while A streams W_a (an idle lane of
-    // the MMA warp; capped so that the partials of A stay resident).
-    if (warp == 1 && lane == 1 && jobs.begin < jobs.end) {
-        int tile, m;
-        expand_job(p.b, jobs[jobs.begin], tile, m);
-        const size_t cap = p.early_prefetch_bytes;
-        if (tile < p.b.nq_tiles) {
-            const size_t head = static_cast<size_t>(p.b.Dn + p.b.R) * p.b.Lq * 2;
-            prefetch_slab(static_cast<const char*>(p.b.w_qb) + head * tile, head < cap ? head : cap);
-        } else {
-            const int n0 = (tile - p.b.nq_tiles) * p.b.bn_kv;
-            const size_t bytes = static_cast<size_t>(p.b.bn_kv) * p.b.Lkv * 2;
-            prefetch_slab(static_cast<const char*>(p.b.w_kvb) + static_cast<size_t>(n0) * p.b.Lkv * 2,
-                          bytes < cap ? bytes : cap);
-        }
-    }
-
-    // A: compression projection
+    // A: compression projection (all roles)
     bool ok = compress_phase<kDecodeBN, kDecodeStages, kDecodeCompressBN>(sm, tmem, &tm_x, &tm_wa, p.a, rc,
                                                                           blockIdx.x, gridDim.x);
-    ok = grid_barrier(ok, p.bar, p.timeout_ns, p.status, &bar_ok);
+    if (epi) {
+        // B: once every CTA's partials are out, the norm of this CTA's tokens
+        // (`ok` is uniform over the epilogue group from here on)
+        ok = epi_arrive(p.sync + kSyncCompressed, 1u, ok);
+        ok = epi_wait(p.sync + kSyncCompressed, run * grid, p, sm, &epi_ok) && ok;
+        for (int t = blockIdx.x; t < p.n.T; t += gridDim.x) {
+            if (ok) norm_token<kDecodeEpiThreads, 8, kDecodeEpiFirst>(p.n, t, crow, red);
+            epi_arrive(p.sync + kSyncNormed, 1u, true);
+        }
+        // The expansion epilogue's amax updates must follow every token's
+        // amax clearing in the norm: acquire the norm count before them.
+        ok = epi_wait(p.sync + kSyncNormed, run * static_cast<unsigned>(p.n.T), p, sm, &epi_ok) && ok;
+    }
 
-    // B: norm + k_pe RoPE, one token per CTA
-    if (ok)
-        for (int t = blockIdx.x; t < p.n.T; t += gridDim.x) norm_token<kDecodeThreads, 16>(p.n, t, crow, red);
-    ok = grid_barrier(ok, p.bar, p.timeout_ns, p.status, &bar_ok);
+    // C: expansion projections; the producer's first activation tiles wait
+    // for every token's normed row (its weight tiles do not)
+    const unsigned normed_target = run * static_cast<unsigned>(p.n.T);
+    const bool c_ok = expand_phase<kDecodeBN, kDecodeStages>(
+        sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p.b, rc, jobs, false, [&] {
+            const bool got = wait_counter(p.sync + kSyncNormed, normed_target, p.timeout_ns, sm.abort_flag);
+            if (!got) atomicOr(p.status, kStatusWaitTimeout);
+            return got;
+        });
+    ok = ok && c_ok;
 
-    // C: expansion projections
-    if (ok) ok = expand_phase<kDecodeBN, kDecodeStages>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p.b, rc, jobs,
-                                                        false);
-
-    // D: per-token INT8 quantisation of q
-    if (p.q.rows > 0) {
-        ok = grid_barrier(ok, p.bar, p.timeout_ns, p.status, &bar_ok);
-        if (ok) {
+    // D: per-token INT8 quantisation of q, once every q tile is out
+    if (epi && p.q.rows > 0) {
+        ok = epi_arrive(p.sync + kSyncExpanded, 1u, ok);
+        ok = epi_wait(p.sync + kSyncExpanded, run * grid, p, sm, &epi_ok) && ok;
+        if (ok) {  // no barrier inside: a per-thread loop
             const int chunks = (p.q.row_len + p.q.chunk - 1) / p.q.chunk;
             for (int k = blockIdx.x; k < p.q.rows * chunks; k += gridDim.x) {
                 const int row = k / chunks, c = k - row * chunks;
                 const int c0 = c * p.q.chunk;
                 const int c1 = c0 + p.q.chunk < p.q.row_len ? c0 + p.q.chunk : p.q.row_len;
-                quant_span(p.q, row, c0, c1, __uint_as_float(p.q.amax[row]), threadIdx.x, kDecodeThreads);
+                quant_span(p.q, row, c0, c1, __uint_as_float(p.q.amax[row]), threadIdx.x - kDecodeEpiFirst,
+                           kDecodeEpiThreads);
             }
         }
     }
-    gemm_finish<kDecodeBN, kDecodeStages>(sm, tmem, rc, p.timeout_ns);
+    gemm_finish<kDecodeBN, kDecodeStages>(sm, tmem, rc, p.timeout_ns);  // includes __syncthreads
+    // the last CTA out advances the epoch for the next run
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned ticket = atomicAdd(p.sync + kSyncFinished, 1u);
+        if (ticket + 1u == run * grid) atomicAdd(p.sync + kSyncEpoch, 1u);
+    }
 }
 
-size_t decode_smem_bytes(int norm_row_elems) {
-    return kDecodeNormOff + ((static_cast<size_t>(norm_row_elems) * 2 + 15) & ~static_cast<size_t>(15));
+size_t decode_smem_bytes(int NA, int R, int Lq, int Lkv) {
+    return kDecodeNormOff + norm_token_smem_bytes(NA, R, Lq, Lkv);
 }
 
 cudaError_t decode_set_attributes(size_t smem) {

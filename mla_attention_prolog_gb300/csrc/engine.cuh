@@ -112,27 +112,37 @@ __device__ __forceinline__ void raise_abort(const Smem& sm, int* status) {
 
 // Producer: streams the nkb K blocks of one job.  `loads` counts ring slots
 // filled so far by this CTA (slot = loads % STAGES, pass = loads / STAGES).
-// With `weights_first` (the first job of a programmatic dependent launch,
-// ring still empty) the weight tiles of the first ring pass are issued before
-// waiting for the previous kernel, and the activation tiles after it.
-template <int BN_MAX, int STAGES>
+// With `weights_first` (the first job after a dependency: the previous
+// kernel of a programmatic dependent launch, or an earlier phase of the
+// same grid) the weight tiles of up to one ring pass are issued as their
+// slots free up, then `dep()` waits for the activations to exist, then the
+// activation tiles of those slots follow.
+template <int BN_MAX, int STAGES, class Dep>
 __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, const CUtensorMap* tmA,
                                             const CUtensorMap* tmB, int a_row, int b_row, int kb0, int nkb,
-                                            int bn, bool weights_first, uint64_t timeout_ns) {
+                                            int bn, bool weights_first, uint64_t timeout_ns, Dep&& dep) {
     using L = Layout<BN_MAX, STAGES>;
     const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + bn * kBK * 2);
     int i = 0;
     if (weights_first) {
         const int pre = nkb < STAGES ? nkb : STAGES;
         for (int k = 0; k < pre; ++k) {
-            mbar_arrive_expect_tx(sm.full0 + 8 * k, tx);
-            tma_load_2d(sm.base + k * L::STAGE + L::A_BYTES, tmB, sm.full0 + 8 * k, (kb0 + k) * kBK, b_row);
+            const uint32_t l = loads + k;
+            const int s = l % STAGES;
+            if (!mbar_wait(sm.empty0 + 8 * s, ((l / STAGES) & 1) ^ 1, timeout_ns, sm.abort_flag)) return false;
+            mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
+            tma_load_2d(sm.base + s * L::STAGE + L::A_BYTES, tmB, sm.full0 + 8 * s, (kb0 + k) * kBK, b_row);
         }
-        pdl_wait();
-        for (int k = 0; k < pre; ++k)
-            tma_load_2d(sm.base + k * L::STAGE, tmA, sm.full0 + 8 * k, (kb0 + k) * kBK, a_row);
+        // The weight tiles above are in flight: their slots must still be
+        // completed (the activation tiles) even when the wait gives up.
+        const bool dep_ok = dep();
+        for (int k = 0; k < pre; ++k) {
+            const int s = (loads + k) % STAGES;
+            tma_load_2d(sm.base + s * L::STAGE, tmA, sm.full0 + 8 * s, (kb0 + k) * kBK, a_row);
+        }
         i = pre;
         loads += pre;
+        if (!dep_ok) return false;
     }
     for (; i < nkb; ++i, ++loads) {
         const int s = loads % STAGES;
@@ -144,17 +154,6 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
         tma_load_2d(sa + L::A_BYTES, tmB, sm.full0 + 8 * s, (kb0 + i) * kBK, b_row);
     }
     return true;
-}
-
-// Contiguous L2 prefetch of a weight slab (the cooperative kernel's early
-// prefetch of its first expansion job).
-__device__ __forceinline__ void prefetch_slab(const void* base, size_t bytes) {
-    const char* p = static_cast<const char*>(base);
-    constexpr size_t kChunk = 32768;
-    for (size_t o = 0; o < bytes; o += kChunk) {
-        const size_t n = bytes - o < kChunk ? bytes - o : kChunk;
-        bulk_prefetch_l2(p + o, static_cast<uint32_t>(n));
-    }
 }
 
 // No copy may still be landing in shared memory when the CTA leaves.
@@ -459,7 +458,7 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
                 int m0, n0, split, kb0, nkb;
                 job_of(j, m0, n0, split, kb0, nkb);
                 if (!produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_x, tm_wa, m0, n0, kb0, nkb, p.bn, false,
-                                                 p.timeout_ns)) {
+                                                 p.timeout_ns, [] { return true; })) {
                     raise_abort(sm, p.status);
                     ok = false;
                     break;
@@ -534,18 +533,20 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
 
 // ---- expansion phase: this CTA's jobs (round robin or balanced table) ----
 //
-// `pdl_first`: the phase opens a programmatic dependent launch, so the
-// producer streams its first ring of weights before waiting for the
-// previous kernel (and the other roles wait right away).
-template <int BN_MAX, int STAGES>
+// The normed activations come from an earlier step: `dep()` (called by the
+// producer, after it has issued its first ring pass of weight tiles) waits
+// for them.  With `pdl` the phase opens a programmatic dependent launch and
+// the other roles also wait for the previous kernel right away (the
+// epilogue's amax updates must follow the norm kernel's clearing).
+template <int BN_MAX, int STAGES, class Dep>
 __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_aq,
                                              const CUtensorMap* tm_akv, const CUtensorMap* tm_bq,
                                              const CUtensorMap* tm_bkv, const ExpandParams& p, RoleCounters& rc,
-                                             const CtaJobs& jobs, bool pdl_first) {
+                                             const CtaJobs& jobs, bool pdl, Dep&& dep) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Dn = p.Dn, R = p.R;
     bool ok = true;
-    if (pdl_first && warp != 0) pdl_wait();
+    if (pdl && warp != 0) pdl_wait();
     if (warp == 0) {
         if (lane == 0) {
             prefetch_tensormap(tm_aq);
@@ -555,15 +556,15 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             for (int i = jobs.begin; i < jobs.end && ok; ++i) {
                 int tile, m;
                 expand_job(p, jobs[i], tile, m);
-                const bool first = pdl_first && i == jobs.begin;
+                const bool first = i == jobs.begin;
                 ok = tile < p.nq_tiles
                          ? produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_aq, tm_bq, m * kBM, tile * (Dn + R), 0, p.kb_q,
-                                                       Dn + R, first, p.timeout_ns)
+                                                       Dn + R, first, p.timeout_ns, dep)
                          : produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_akv, tm_bkv, m * kBM,
                                                        (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
-                                                       p.timeout_ns);
+                                                       p.timeout_ns, dep);
             }
-            if (pdl_first && jobs.begin == jobs.end) pdl_wait();
+            if (pdl && jobs.begin == jobs.end) pdl_wait();
             if (!ok) raise_abort(sm, p.status);
         }
     } else if (warp == 1) {

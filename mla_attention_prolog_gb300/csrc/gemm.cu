@@ -32,7 +32,10 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     pdl_launch_dependents();
     RoleCounters rc;
     const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles);
-    expand_phase<BN_MAX, STAGES>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true);
+    expand_phase<BN_MAX, STAGES>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true, [] {
+        pdl_wait();
+        return true;
+    });
     gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
 

@@ -233,8 +233,6 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.m_tiles = m_tiles;
     pb.group_n = 16;
     pb.job_table = nullptr;  // round robin: same per-job results as the balanced order
-    pb.w_qb = wb;
-    pb.w_kvb = wb + static_cast<size_t>(NQ) * Lq;
     pb.Lq = Lq;
     pb.Lkv = Lkv;
     pb.kb_q = cdiv(Lq, kBK);

@@ -62,8 +62,6 @@ struct ExpandParams {
     int nq_tiles, nkv_tiles, bn_kv;
     int m_tiles, group_n;  // token tiles; weight tiles per L2 group of the job order
     const int* job_table;  // balanced per-CTA job lists (null: round robin)
-    const void* w_qb;      // W_q_b [NQ][Lq] and W_kv_b [NKV][Lkv] (the cooperative kernel's early prefetch)
-    const void* w_kvb;
     int Lq, Lkv;
     int kb_q, kb_kv;
     const int32_t* positions;
@@ -87,19 +85,29 @@ struct QuantParams {
     float* scale;
 };
 
-// The cooperative decode kernel: the four steps as phases of one launch.
+// The cooperative decode kernel: the four steps as phases of one launch,
+// handing over through counters (word offsets into `sync`, one 128-byte line
+// each): runs completed, and per run one arrival per CTA after the
+// compression, one per token after the norm, one per CTA after the
+// expansion and one per CTA at exit.
+constexpr int kSyncEpoch = 0;
+constexpr int kSyncCompressed = 32;
+constexpr int kSyncNormed = 64;
+constexpr int kSyncExpanded = 96;
+constexpr int kSyncFinished = 128;
+constexpr int kSyncWords = 160;
+
 struct DecodeParams {
     CompressParams a;
     NormRopeParams n;
     ExpandParams b;
-    QuantParams q;               // q.rows == 0 without a q path
-    unsigned* bar;               // grid barrier: [arrivals, generation]
-    size_t early_prefetch_bytes; // L2 prefetch of each CTA's first expansion weights during phase A
+    QuantParams q;   // q.rows == 0 without a q path
+    unsigned* sync;  // kSyncWords words, zero at creation
     int* status;
     uint64_t timeout_ns;
 };
 
-size_t decode_smem_bytes(int norm_row_elems);
+size_t decode_smem_bytes(int NA, int R, int Lq, int Lkv);
 cudaError_t decode_set_attributes(size_t smem);
 cudaError_t decode_occupancy(size_t smem, int* blocks_per_sm);
 cudaError_t launch_decode(int grid, size_t smem, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,

@@ -69,6 +69,59 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// ------------------------------------------------------- CTA-group barriers
+
+// Barrier over `count` threads (whole warps) of the CTA, on barrier `id`
+// (0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Barrier as above that also returns, to every thread, the AND of `v` over
+// the participating threads.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------- cross-CTA counters (one grid)
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Adds v with release semantics at GPU scope: the writes this thread made or
+// observed before it are visible to whoever acquires the new value.
+__device__ __forceinline__ void red_release_gpu_add(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits (one thread) until *p has reached `target`, comparing modulo 2^32 so
+// that counters may wrap.  Returns false after `timeout_ns` or as soon as
+// *abort_flag is set (may be null).
+__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, uint64_t timeout_ns,
+                                             const volatile int* abort_flag) {
+    if (static_cast<int>(ld_acquire_gpu(p) - target) >= 0) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i)
+            if (static_cast<int>(ld_acquire_gpu(p) - target) >= 0) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Blocks the calling thread until the grids this grid depends on have

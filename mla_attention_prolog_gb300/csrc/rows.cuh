@@ -7,32 +7,106 @@
 
 namespace mlap {
 
-// Sum of a per-thread value over the CTA in a fixed order (deterministic).
-template <int NW>
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float s = 0.0f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) s = __fadd_rn(s, red[w]);
-    return s;
+// The thread group that runs a row step: FIRST == 0 is the whole CTA (NT
+// threads, __syncthreads); otherwise threads [FIRST, FIRST + NT), whole
+// warps, synchronised on named barrier 1 while the other warps work on.
+template <int NT, int FIRST>
+__device__ __forceinline__ void group_sync() {
+    if constexpr (FIRST == 0)
+        __syncthreads();
+    else
+        named_bar_sync(1, NT);
 }
 
-// One token of the norm step, by a CTA of NT threads (threadIdx.x < NT):
+// Sum of squares of a normed block in the one order every norm kernel uses,
+// whatever its thread count: 4-column chunk j contributes
+// ((t0 + t1) + t2) + t3 (t = x^2 / L of its BF16 values), lane j % 32 of a
+// warp adds its chunks in increasing j, and a butterfly over the 32 lanes
+// (every lane ends with the same sum) finishes.  So a token's normed row is
+// the same bits in the decode, prefill and cooperative kernels.
+__device__ __forceinline__ float chunk_ssq(const float (&v)[4], float inv_l) {
+    float c = __fmul_rn(__fmul_rn(v[0], v[0]), inv_l);
+#pragma unroll
+    for (int e = 1; e < 4; ++e) c = __fadd_rn(c, __fmul_rn(__fmul_rn(v[e], v[e]), inv_l));
+    return c;
+}
+
+__device__ __forceinline__ float lane_butterfly_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Shared memory a norm group needs per token: the BF16 row (NA + R) and the
+// FP32 chunk sums ((Lq + Lkv) / 4), 16-byte aligned.
+__host__ __device__ inline size_t norm_token_smem_bytes(int NA, int R, int Lq, int Lkv) {
+    return ((static_cast<size_t>(NA + R) * 2 + 15) & ~static_cast<size_t>(15)) +
+           static_cast<size_t>((Lq + Lkv) / 4) * 4;
+}
+
+// Step 1 of the norm for one group of a thread's 4-column chunks (CPG of
+// them, NT * 4 columns apart, the first at column i0): every split's partial
+// of every chunk, BATCH loads in flight at a time, summed in split order
+// with TwoSum, rounded to BF16 into `crow`, chunk sums of x^2 / L into
+// `csum` (see chunk_ssq).
+template <int CPG, int BATCH, int NT>
+__device__ __forceinline__ void norm_chunk_group(const NormRopeParams& p, const float* prow, int i0,
+                                                 uint16_t* crow, float* csum) {
+    constexpr int SPB = BATCH / CPG;  // splits per chunk and batch
+    const size_t sstride = static_cast<size_t>(p.T) * p.NA;
+    const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, splits = p.splits;
+    float4 acc[CPG], cmp[CPG];
+    for (int s0 = 0; s0 < splits; s0 += SPB) {
+        float4 r[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int sp = s0 + u % SPB, i = i0 + (u / SPB) * NT * 4;
+            if (sp < splits && i < NA) r[u] = *reinterpret_cast<const float4*>(prow + sp * sstride + i);
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int c = u / SPB, sp = s0 + u % SPB, i = i0 + c * NT * 4;
+            if (sp < splits && i < NA) {
+                if (sp == 0) {
+                    acc[c] = r[u];
+                    cmp[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    two_sum_add(acc[c].x, cmp[c].x, r[u].x);
+                    two_sum_add(acc[c].y, cmp[c].y, r[u].y);
+                    two_sum_add(acc[c].z, cmp[c].z, r[u].z);
+                    two_sum_add(acc[c].w, cmp[c].w, r[u].w);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < CPG; ++c) {
+        const int i = i0 + c * NT * 4;
+        if (i < NA) {
+            const float4 a = make_float4(__fadd_rn(acc[c].x, cmp[c].x), __fadd_rn(acc[c].y, cmp[c].y),
+                                         __fadd_rn(acc[c].z, cmp[c].z), __fadd_rn(acc[c].w, cmp[c].w));
+            const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
+            *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
+            const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+            if (i < Lq + Lkv) csum[i / 4] = chunk_ssq(v, i < Lq ? p.inv_lq : p.inv_lkv);
+        }
+    }
+}
+
+// One token of the norm step, by a group of NT threads (see group_sync):
 // reduce the token's split-K partials in split order (TwoSum), round to
-// BF16, RMSNorm of c_q and c_kv (x^2/L summed, + eps, sqrt, reciprocal,
-// x * rstd, * gamma, BF16), rotate-half RoPE of k_pe, and write the normed
-// row, out_kpe and K's rope slice of every head.  `crow` is NA + R BF16
-// values of shared memory, `red` 2 * NT / 32 floats.
-template <int NT, int BATCH>
+// BF16, RMSNorm of c_q and c_kv (x^2/L summed as chunk_ssq describes,
+// + eps, sqrt, reciprocal, x * rstd, * gamma, BF16), rotate-half RoPE of
+// k_pe, and write the normed row, out_kpe and K's rope slice of every head.
+// `crow` is norm_token_smem_bytes of shared memory, `red` 2 floats.
+template <int NT, int BATCH, int FIRST = 0>
 __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint16_t* crow, float* red) {
     constexpr int kNormThreads = NT;
-    constexpr int kNormWarps = NT / 32;
-    const int tid = threadIdx.x;
+    const int tid = static_cast<int>(threadIdx.x) - FIRST;
     const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, R = p.R, half = R / 2;
     uint16_t* rot = crow + NA;
+    float* csum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(crow) +
+                                           ((static_cast<size_t>(NA + R) * 2 + 15) & ~static_cast<size_t>(15)));
 
     const int pos = p.positions[t];
     const bool valid = pos >= 0 && pos < p.max_pos;
@@ -52,56 +126,54 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
         return;
     }
 
-    // 1) Reduce the split-K partials in split order (TwoSum), round to BF16,
-    //    and accumulate x^2 / L of the c_q and c_kv blocks.
-    float ssq_q = 0.0f, ssq_kv = 0.0f;
-    const size_t sstride = static_cast<size_t>(p.T) * NA;
-    const float* prow = p.partials + static_cast<size_t>(t) * NA;
-    for (int i = tid * 4; i < NA; i += kNormThreads * 4) {
-        float4 a = *reinterpret_cast<const float4*>(prow + i);
-        if (BATCH > 1 && p.splits > 1) {
-            // every split's load in flight first (up to BATCH at a time),
-            // then the sums in split order with TwoSum
-            float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 1; s0 < p.splits; s0 += BATCH) {
-                float4 b[BATCH];
+    // 0) Loads that do not wait for the partials: gamma for step 2 and this
+    //    token's cos/sin row for step 3, in flight with step 1's loads.
+    constexpr int kGammaPre = 2;
+    uint4 gpre[kGammaPre];
 #pragma unroll
-                for (int u = 0; u < BATCH; ++u)
-                    if (s0 + u < p.splits) b[u] = *reinterpret_cast<const float4*>(prow + (s0 + u) * sstride + i);
-#pragma unroll
-                for (int u = 0; u < BATCH; ++u) {
-                    if (s0 + u < p.splits) {
-                        two_sum_add(a.x, c.x, b[u].x);
-                        two_sum_add(a.y, c.y, b[u].y);
-                        two_sum_add(a.z, c.z, b[u].z);
-                        two_sum_add(a.w, c.w, b[u].w);
-                    }
-                }
-            }
-            a = make_float4(__fadd_rn(a.x, c.x), __fadd_rn(a.y, c.y), __fadd_rn(a.z, c.z), __fadd_rn(a.w, c.w));
-        }
-        const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
-        *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
-        const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-        if (i < Lq) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ssq_q = __fadd_rn(ssq_q, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lq));
-        } else if (i < Lq + Lkv) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ssq_kv = __fadd_rn(ssq_kv, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lkv));
-        }
+    for (int u = 0; u < kGammaPre; ++u) {
+        const int i = (tid + u * kNormThreads) * 8;
+        if (i < Lq + Lkv) gpre[u] = *reinterpret_cast<const uint4*>(p.gamma + i);
     }
-    ssq_q = block_sum<kNormWarps>(ssq_q, red);
-    ssq_kv = block_sum<kNormWarps>(ssq_kv, red + kNormWarps);  // its __syncthreads also publishes crow
+    const float* cs = p.cos_sin + static_cast<size_t>(pos) * R;
+    float c_pre = 0.0f, s_pre = 0.0f;
+    if (tid < half) c_pre = cs[tid], s_pre = cs[half + tid];
+
+    // 1) Reduce the split-K partials in split order (TwoSum), round to BF16,
+    //    and the chunk sums of x^2 / L of the c_q and c_kv blocks.  A thread's
+    //    chunks go in groups whose loads (every split of up to two chunks,
+    //    BATCH at most) are all in flight before the first sum.
+    const float* prow = p.partials + static_cast<size_t>(t) * NA;
+    if (2 * p.splits <= BATCH) {
+        for (int i0 = tid * 4; i0 < NA; i0 += 2 * kNormThreads * 4)
+            norm_chunk_group<2, BATCH, NT>(p, prow, i0, crow, csum);
+    } else {
+        for (int i0 = tid * 4; i0 < NA; i0 += kNormThreads * 4)
+            norm_chunk_group<1, BATCH, NT>(p, prow, i0, crow, csum);
+    }
+    group_sync<NT, FIRST>();  // also publishes crow
+    if (tid < 32) {
+        float sq = 0.0f, skv = 0.0f;
+        for (int j = tid; j < (Lq + Lkv) / 4; j += 32) {
+            if (j < Lq / 4)
+                sq = __fadd_rn(sq, csum[j]);
+            else
+                skv = __fadd_rn(skv, csum[j]);
+        }
+        sq = lane_butterfly_sum(sq);
+        skv = lane_butterfly_sum(skv);
+        if (tid == 0) red[0] = sq, red[1] = skv;
+    }
+    group_sync<NT, FIRST>();
+    const float ssq_q = red[0], ssq_kv = red[1];
     // Variant B of the pages' RMSNorm: std = sqrt(ms + eps), rstd = 1 / std,
     // both correctly rounded.
     const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
     const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
 
     // 2) y = bf16((x * rstd) * gamma) for c_q and c_kv, 8 columns per thread.
-    for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) {
+    auto norm8 = [&](int i, const uint4 gv) {
         const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
-        const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma + i);
         const float rstd = i < Lq ? rstd_q : rstd_kv;
         const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
         const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -113,21 +185,27 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
             o[e] = pack_bf16x2(y0, y1);
         }
         *reinterpret_cast<uint4*>(nrow + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+#pragma unroll
+    for (int u = 0; u < kGammaPre; ++u) {
+        const int i = (tid + u * kNormThreads) * 8;
+        if (i < Lq + Lkv) norm8(i, gpre[u]);
     }
+    for (int i = (tid + kGammaPre * kNormThreads) * 8; i < Lq + Lkv; i += kNormThreads * 8)
+        norm8(i, *reinterpret_cast<const uint4*>(p.gamma + i));
 
     // 3) k_pe RoPE (rotate-half) in FP32 with this token's cos/sin row.
     const uint16_t* kp = crow + Lq + Lkv;
-    const float* cs = p.cos_sin + static_cast<size_t>(pos) * R;
     for (int i = tid; i < half; i += kNormThreads) {
         const float x1 = __uint_as_float(static_cast<uint32_t>(kp[i]) << 16);
         const float x2 = __uint_as_float(static_cast<uint32_t>(kp[i + half]) << 16);
-        const float c = cs[i], s = cs[half + i];
+        const float c = i == tid ? c_pre : cs[i], s = i == tid ? s_pre : cs[half + i];
         const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
         const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
         rot[i] = static_cast<uint16_t>(pack_bf16x2(o1, 0.0f) & 0xFFFFu);
         rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
     }
-    __syncthreads();
+    group_sync<NT, FIRST>();
 
     // 4) out_kpe[t] and the shared rope slice of K for every head.
     for (int k = tid; k < (p.H + 1) * nchunk; k += kNormThreads) {
@@ -153,18 +231,30 @@ __device__ __forceinline__ void quant_span(const QuantParams& p, int row, int c0
         return;
     }
     const float inv = __fdiv_rn(127.0f, amax);
-#pragma unroll 4
-    for (int i = c0 + tid * 4; i < c1; i += nthr * 4) {
-        const float4 v = *reinterpret_cast<const float4*>(y + i);
-        const float f[4] = {v.x, v.y, v.z, v.w};
-        signed char c[4];
+    // eight loads in flight per thread before any store
+    constexpr int kB = 8;
+    for (int i0 = c0 + tid * 4; i0 < c1; i0 += kB * nthr * 4) {
+        float4 v[kB];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            int q = __float2int_rn(__fmul_rn(f[e], inv));  // round to nearest, ties to even
-            q = q > 127 ? 127 : (q < -127 ? -127 : q);
-            c[e] = static_cast<signed char>(q);
+        for (int u = 0; u < kB; ++u) {
+            const int i = i0 + u * nthr * 4;
+            if (i < c1) v[u] = *reinterpret_cast<const float4*>(y + i);
         }
-        *reinterpret_cast<char4*>(out + i) = make_char4(c[0], c[1], c[2], c[3]);
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int i = i0 + u * nthr * 4;
+            if (i < c1) {
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                signed char c[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int q = __float2int_rn(__fmul_rn(f[e], inv));  // round to nearest, ties to even
+                    q = q > 127 ? 127 : (q < -127 ? -127 : q);
+                    c[e] = static_cast<signed char>(q);
+                }
+                *reinterpret_cast<char4*>(out + i) = make_char4(c[0], c[1], c[2], c[3]);
+            }
+        }
     }
     if (tid == 0 && c0 == 0) p.scale[row] = __fdiv_rn(amax, 127.0f);
 }

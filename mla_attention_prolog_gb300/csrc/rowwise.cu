@@ -23,7 +23,7 @@ namespace mlap {
 template <int NT, int BATCH>
 __global__ void __launch_bounds__(NT) mla_norm_rope_kernel(const NormRopeParams p) {
     extern __shared__ __align__(16) uint16_t crow[];  // BF16 row of C [NA], then rotated k_pe [R]
-    __shared__ float red[2 * (NT / 32)];
+    __shared__ float red[2];
     pdl_wait();
     pdl_launch_dependents();
     norm_token<NT, BATCH>(p, blockIdx.x, crow, red);
@@ -68,19 +68,14 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
         const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
         *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
         const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-        if (i < Lq) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ssq_q = __fadd_rn(ssq_q, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lq));
-        } else if (i < Lq + Lkv) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ssq_kv = __fadd_rn(ssq_kv, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_lkv));
-        }
+        // chunk i / 4 on lane (i / 4) % 32, in increasing order (chunk_ssq)
+        if (i < Lq)
+            ssq_q = __fadd_rn(ssq_q, chunk_ssq(v, p.inv_lq));
+        else if (i < Lq + Lkv)
+            ssq_kv = __fadd_rn(ssq_kv, chunk_ssq(v, p.inv_lkv));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        ssq_q = __fadd_rn(ssq_q, __shfl_xor_sync(0xffffffffu, ssq_q, o));
-        ssq_kv = __fadd_rn(ssq_kv, __shfl_xor_sync(0xffffffffu, ssq_kv, o));
-    }
+    ssq_q = lane_butterfly_sum(ssq_q);
+    ssq_kv = lane_butterfly_sum(ssq_kv);
     const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
     const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
     __syncwarp();
@@ -160,9 +155,10 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
 
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
     if (p.splits > 1)
-        return launch_kernel(mla_norm_rope_kernel<512, 16>, dim3(p.T), dim3(512), smem, st, true, p);
+        return launch_kernel(mla_norm_rope_kernel<512, 16>, dim3(p.T), dim3(512),
+                             norm_token_smem_bytes(p.NA, p.R, p.Lq, p.Lkv), st, true, p);
+    const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
     return launch_kernel(mla_norm_rope_warp_kernel, dim3((p.T + kNormWarpTokens - 1) / kNormWarpTokens),
                          dim3(32 * kNormWarpTokens), smem * kNormWarpTokens, st, true, p);
 }
