@@ -29,7 +29,10 @@ from typing import Dict, Optional
 import numpy as np
 import torch
 
-QUANT_Q = 1  # flag bit: per-token INT8 quantisation of the q path
+QUANT_Q = 1           # flag bits (the C header's MLA_PROLOG_*): INT8 quantisation of the q path
+ROPE_INTERLEAVED = 2  # rope slices de-interleaved before the rotate-half RoPE
+Q_HEAD_NORM = 4       # per-head RMSNorm (no gamma) of q before its RoPE
+QUANT_PER_HEAD = 8    # one q scale per (token, head) instead of per token
 
 
 @dataclasses.dataclass(frozen=True)
@@ -69,6 +72,15 @@ class Dims:
     @property
     def quant_q(self) -> bool:
         return bool(self.flags & QUANT_Q)
+
+    @property
+    def quant_per_head(self) -> bool:
+        return bool(self.flags & QUANT_PER_HEAD)
+
+    @property
+    def n_scales(self) -> int:
+        """q scales per token."""
+        return self.num_heads if self.quant_per_head else 1
 
     def with_T(self, T: int) -> "Dims":
         return dataclasses.replace(self, T=T)
@@ -206,7 +218,7 @@ def algorithmic_bytes(d: Dims) -> int:
     b += 2 * T * d.num_heads * d.v_dim                    # out_v
     b += 2 * T * d.rope_dim                               # out_kpe
     if d.quant_q:
-        b += T * d.n_q + 4 * T                            # int8 codes + scales
+        b += T * d.n_q + 4 * T * d.n_scales               # int8 codes + scales
     return b
 
 
@@ -222,7 +234,7 @@ def output_shapes(d: Dims) -> Dict[str, tuple]:
     }
     if d.quant_q:
         s["out_q_int8"] = (d.T, d.num_heads, d.nope_dim + d.rope_dim)
-        s["out_scale"] = (d.T,)
+        s["out_scale"] = (d.T, d.num_heads) if d.quant_per_head else (d.T,)
     return s
 
 

@@ -25,6 +25,12 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
 
+QUANT_Q = 1            # dims flags, the same bits as the C oracle's
+ROPE_INTERLEAVED = 2
+Q_HEAD_NORM = 4
+QUANT_PER_HEAD = 8
+
+
 class OracleDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "T", "D", "q_lora_rank", "kv_lora_rank", "rope_dim", "num_heads",
@@ -59,6 +65,8 @@ def lib():
         L.oracle_rmsnorm_row.argtypes = [P, P, ctypes.c_int, ctypes.c_float, P, P]
         L.oracle_rope_f32.argtypes = [P, P, ctypes.c_int, P]
         L.oracle_quant_row.argtypes = [P, ctypes.c_int, P, P]
+        L.oracle_deinterleave.argtypes = [P, ctypes.c_int, P]
+        L.oracle_rmsnorm_f32_row.argtypes = [P, ctypes.c_int, ctypes.c_float, P]
         L.oracle_max_threads.restype = ctypes.c_int
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -104,7 +112,7 @@ def mla_prolog(d, x, gamma, W_a, W_b, positions, cos_sin,
     q8 = sc = None
     if d.q_lora_rank > 0:
         q8 = out["out_q_int8"] = np.zeros((n, H, Dn + R), np.int8)
-        sc = out["out_scale"] = np.zeros((n,), np.float32)
+        sc = out["out_scale"] = np.zeros((n, H) if d.flags & QUANT_PER_HEAD else (n,), np.float32)
     c = nrm = q = None
     if taps:
         c = out["c"] = np.zeros((n, d.q_lora_rank + d.kv_lora_rank + R), np.uint16)
@@ -121,6 +129,29 @@ def mla_prolog(d, x, gamma, W_a, W_b, positions, cos_sin,
         raise ValueError("oracle rejected its arguments")
     out["bad_positions"] = rc
     return out
+
+
+def scatter_kv_cache(cache: np.ndarray, slot_mapping: np.ndarray, normed: np.ndarray, out_kpe: np.ndarray,
+                     q_lora_rank: int) -> int:
+    """Writes the latent KV cache rows of the listed tokens in place.
+
+    The cache write of the pages (the DeepSeek-V3.2-Exp PyPTO article: results
+    cached into the KV cache, written with ScatterUpdate into the KCache): row
+    ``slot_mapping[j]`` of ``cache`` [num_slots, Lkv + R] receives token j's
+    normed c_kv (BF16 bits) followed by its rotated k_pe.  A negative slot is
+    skipped (a padding token); a slot >= num_slots is skipped and counted.
+    Returns the number of out-of-range slots.
+    """
+    num_slots = cache.shape[0]
+    bad = 0
+    for j, slot in enumerate(np.asarray(slot_mapping, np.int64)):
+        if slot < 0:
+            continue
+        if slot >= num_slots:
+            bad += 1
+            continue
+        cache[slot] = np.concatenate([normed[j, q_lora_rank:], out_kpe[j]])
+    return bad
 
 
 # -- single steps, for the pins ------------------------------------------------
@@ -166,6 +197,20 @@ def rope(x: np.ndarray, cs_row: np.ndarray) -> np.ndarray:
     cs_row = np.ascontiguousarray(cs_row, np.float32)
     out = np.zeros_like(x)
     lib().oracle_rope_f32(_p(x), _p(cs_row), len(x), _p(out))
+    return out
+
+
+def deinterleave(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.zeros_like(x)
+    lib().oracle_deinterleave(_p(x), len(x), _p(out))
+    return out
+
+
+def rmsnorm_f32_row(x: np.ndarray, eps: float) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.zeros_like(x)
+    lib().oracle_rmsnorm_f32_row(_p(x), len(x), ctypes.c_float(eps), _p(out))
     return out
 
 

@@ -27,6 +27,14 @@
  *     PrologQuant; grouped_matmul_swiglu_quant article, sections "数学公式" and
  *     "5. 量化流水线的数值细节").
  *
+ *   - Variants (flags): ORACLE_ROPE_INTERLEAVED de-interleaves each rope
+ *     slice before the rotate-half RoPE (QuantRope3D, DeepSeek-V3.2-Exp
+ *     PyPTO article, section 3.3); ORACLE_Q_HEAD_NORM applies a per-head FP32
+ *     RMSNorm without gamma to every q head before its RoPE (AT-10 article,
+ *     section 九, the DeepSeek-V4 q path); ORACLE_QUANT_PER_HEAD quantises
+ *     each (token, head) row of Dn + R values with its own scale (the quant
+ *     formula of section 3.1 applied per head row).
+ *
  * Readings where the pages are silent (also listed in the design notes):
  *   - a zero row (amax == 0) yields codes 0 and scale 0;
  *   - a position outside [0, max_pos) zero-fills every output of that token
@@ -46,6 +54,9 @@
 #endif
 
 #define ORACLE_QUANT_Q 1u
+#define ORACLE_ROPE_INTERLEAVED 2u
+#define ORACLE_Q_HEAD_NORM 4u
+#define ORACLE_QUANT_PER_HEAD 8u
 
 typedef struct {
     int32_t T, D, q_lora_rank, kv_lora_rank, rope_dim, num_heads, nope_dim, v_dim, max_pos;
@@ -156,6 +167,37 @@ void oracle_rope_f32(const float* x, const float* cs_row, int R, float* out) {
     }
 }
 
+/* The de-interleave of QuantRope3D (DeepSeek-V3.2-Exp PyPTO article,
+ * section 3.3 and section 2.3): the R rope values are viewed as [R/2, 2]
+ * (chunks of 2) and transposed to [2, R/2], so out[i] = x[2i] and
+ * out[R/2 + i] = x[2i + 1]; the rotate-half RoPE then pairs the values that
+ * sat next to each other.  The result stays in the transposed order. */
+void oracle_deinterleave(const float* x, int R, float* out) {
+    const int h = R / 2;
+    for (int i = 0; i < h; ++i) {
+        out[i] = x[2 * i];
+        out[h + i] = x[2 * i + 1];
+    }
+}
+
+/* RMSNorm of one FP32 row without gamma, FP32 in and out: the second,
+ * per-head RMSNorm of the DeepSeek-V4 q path (PyPTO-Gym AT-10 article,
+ * section 九: q_b_proj, reshape to (heads, head_dim), RMSNorm again; the
+ * no-gamma variant rms_norm_new of the same section), with the variant-B
+ * steps of section 三: x^2, times 1/L, sum, + eps, sqrt, 1/std, x * rstd. */
+void oracle_rmsnorm_f32_row(const float* x, int L, float eps, float* out) {
+    const float inv_l = 1.0f / (float)L;
+    float ms = 0.0f;
+    for (int i = 0; i < L; ++i) {
+        float sq = x[i] * x[i];
+        ms += sq * inv_l;
+    }
+    float var = ms + eps;
+    float sd = sqrtf(var);
+    float rstd = 1.0f / sd;
+    for (int i = 0; i < L; ++i) out[i] = x[i] * rstd;
+}
+
 /* Per-token symmetric INT8 quantisation of one FP32 row. */
 void oracle_quant_row(const float* y, int n, int8_t* codes, float* scale) {
     float amax = 0.0f;
@@ -207,6 +249,9 @@ int oracle_mla_prolog(const oracle_dims* d,
     const int H = d->num_heads, Dn = d->nope_dim, Dv = d->v_dim;
     const int NA = Lq + Lkv + R, NQ = H * (Dn + R);
     const int quant = (d->flags & ORACLE_QUANT_Q) != 0;
+    const int interleaved = (d->flags & ORACLE_ROPE_INTERLEAVED) != 0;
+    const int head_norm = (d->flags & ORACLE_Q_HEAD_NORM) != 0;
+    const int per_head = (d->flags & ORACLE_QUANT_PER_HEAD) != 0;
     if (T < 0 || D <= 0 || Lq < 0 || Lkv <= 0 || R <= 0 || (R & 1) || H <= 0 || Dn < 0 || Dv < 0)
         return -1;
     if ((Lq + Lkv) > 0 && !gamma) return -1;
@@ -232,7 +277,10 @@ int oracle_mla_prolog(const oracle_dims* d,
             memset(okpe, 0, sizeof(uint16_t) * (size_t)R);
             if (Lq > 0) {
                 memset(out_q_int8 + (size_t)j * NQ, 0, (size_t)NQ);
-                out_scale[j] = 0.0f;
+                if (per_head)
+                    memset(out_scale + (size_t)j * H, 0, sizeof(float) * (size_t)H);
+                else
+                    out_scale[j] = 0.0f;
             }
             if (c_out) memset(c_out + (size_t)j * NA, 0, sizeof(uint16_t) * (size_t)NA);
             if (normed_out) memset(normed_out + (size_t)j * (Lq + Lkv), 0, sizeof(uint16_t) * (size_t)(Lq + Lkv));
@@ -252,8 +300,13 @@ int oracle_mla_prolog(const oracle_dims* d,
         /* Step 3: RMSNorm of c_q and c_kv with their gammas, then BF16. */
         if (Lq > 0) oracle_rmsnorm_row(c, gamma, Lq, d->eps, NULL, nrm);
         oracle_rmsnorm_row(c + Lq, gamma + Lq, Lkv, d->eps, NULL, nrm + Lq);
-        /* Step 4 (k_pe RoPE): rotate-half in FP32 with this token's table row. */
+        /* Step 4 (k_pe RoPE): rotate-half in FP32 with this token's table row
+         * (after the de-interleave in the interleaved variant). */
         for (int i = 0; i < R; ++i) kpe_f[i] = bf16_to_f32(c[Lq + Lkv + i]);
+        if (interleaved) {
+            oracle_deinterleave(kpe_f, R, kpe_r);
+            memcpy(kpe_f, kpe_r, sizeof(float) * (size_t)R);
+        }
         oracle_rope_f32(kpe_f, cs, R, kpe_r);
         for (int i = 0; i < R; ++i) okpe[i] = oracle_f32_to_bf16(kpe_r[i]);
         /* Steps 5-7: KV expansion, split per head into k_nope | value, assemble
@@ -266,17 +319,34 @@ int oracle_mla_prolog(const oracle_dims* d,
                 ov[(size_t)h * Dv + i] = oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)(Dn + i) * Lkv, Lkv));
             for (int i = 0; i < R; ++i) ok[(size_t)h * (Dn + R) + Dn + i] = okpe[i];
         }
-        /* q path: expansion, RoPE on each head's rope slice, per-token quant. */
+        /* q path: expansion, (per-head RMSNorm,) RoPE on each head's rope
+         * slice, INT8 quant per token (or per head row). */
         if (Lq > 0) {
             float* q = (float*)malloc(sizeof(float) * (size_t)NQ);
+            float* hb = (float*)malloc(sizeof(float) * (size_t)(Dn + R));
             oracle_project_f32(nrm, W_qb, NQ, Lq, q);
             for (int h = 0; h < H; ++h) {
-                float* qr = q + (size_t)h * (Dn + R) + Dn;
-                memcpy(kpe_f, qr, sizeof(float) * (size_t)R);
+                float* qh = q + (size_t)h * (Dn + R);
+                if (head_norm) {
+                    oracle_rmsnorm_f32_row(qh, Dn + R, d->eps, hb);
+                    memcpy(qh, hb, sizeof(float) * (size_t)(Dn + R));
+                }
+                float* qr = qh + Dn;
+                if (interleaved)
+                    oracle_deinterleave(qr, R, kpe_f);
+                else
+                    memcpy(kpe_f, qr, sizeof(float) * (size_t)R);
                 oracle_rope_f32(kpe_f, cs, R, qr);
             }
             if (q_out) memcpy(q_out + (size_t)j * NQ, q, sizeof(float) * (size_t)NQ);
-            oracle_quant_row(q, NQ, out_q_int8 + (size_t)j * NQ, out_scale + j);
+            if (per_head) {
+                for (int h = 0; h < H; ++h)
+                    oracle_quant_row(q + (size_t)h * (Dn + R), Dn + R, out_q_int8 + (size_t)j * NQ + (size_t)h * (Dn + R),
+                                     out_scale + (size_t)j * H + h);
+            } else {
+                oracle_quant_row(q, NQ, out_q_int8 + (size_t)j * NQ, out_scale + j);
+            }
+            free(hb);
             free(q);
         }
         if (c_out) memcpy(c_out + (size_t)j * NA, c, sizeof(uint16_t) * (size_t)NA);
