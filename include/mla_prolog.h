@@ -61,10 +61,38 @@ extern "C" {
                                          token's outputs were zero-filled                  */
 #define MLA_STATUS_WAIT_TIMEOUT   0x2 /* a bounded in-kernel wait gave up; outputs of the
                                          affected tile are undefined                       */
+#define MLA_STATUS_SLOT_RANGE     0x4 /* mla_prolog_run_cached: some slot_mapping[t] was
+                                         >= num_slots; that token's cache row was skipped  */
 
 /* ---- dims flags --------------------------------------------------------- */
 #define MLA_PROLOG_QUANT_Q 0x1u /* q path emits INT8 codes + FP32 per-token scales.
                                    Required exactly when q_lora_rank > 0.               */
+/*
+ * Interleaved RoPE (QuantRope3D, DeepSeek-V3.2-Exp PyPTO article, sections
+ * 2.3 and 3.3: the rope slice viewed as [R/2, 2] chunks and transposed before
+ * the rotation).  Every rope slice -- k_pe and each q head's -- is first
+ * de-interleaved, x'[i] = x[2i], x'[R/2 + i] = x[2i + 1], then rotated as
+ * above; the rotated values stay in the de-interleaved order (out_kpe, K's
+ * rope slice, the q codes).  The pages do not print the chunk size: 2 is the
+ * reading taken, the one that turns adjacent pairs into rotate-half pairs.
+ */
+#define MLA_PROLOG_ROPE_INTERLEAVED 0x2u
+/*
+ * Per-head q RMSNorm (the DeepSeek-V4 q path, PyPTO-Gym AT-10 article,
+ * section 九: q_b_proj, reshape to (heads, head_dim), RMSNorm again).  Each
+ * head's Dn + R FP32 values of q are normalised before the RoPE, without a
+ * gamma: ms = sum(x^2 / (Dn + R)), rstd = 1/sqrt(ms + eps), x * rstd, all
+ * FP32.  Requires q_lora_rank > 0.
+ */
+#define MLA_PROLOG_Q_HEAD_NORM 0x4u
+/*
+ * Per-(token, head) INT8 quantisation of q: the quantisation formula of the
+ * q path applied to each head row of Dn + R values, so out_scale is FP32
+ * [T, H].  Runs inside the expansion kernel (no FP32 q round trip through
+ * memory); the MLA_TAP_Q and MLA_TAP_AMAX taps are then absent.  Requires
+ * q_lora_rank > 0.
+ */
+#define MLA_PROLOG_QUANT_PER_HEAD 0x8u
 
 /*
  * Problem sizes, fixed for the life of a handle.
@@ -84,7 +112,7 @@ typedef struct mla_prolog_dims {
     int32_t  v_dim;        /* Dv                                                 */
     int32_t  max_pos;      /* rows of the cos/sin table                          */
     float    eps;          /* RMSNorm epsilon (1e-6 in the DeepSeek shapes)      */
-    uint32_t flags;        /* MLA_PROLOG_QUANT_Q                                 */
+    uint32_t flags;        /* OR of MLA_PROLOG_* flags                           */
 } mla_prolog_dims;
 
 typedef struct mla_prolog* mla_prolog_t;
@@ -116,7 +144,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out);
  *   out_v      BF16 [T, H, Dv]
  *   out_kpe    BF16 [T, R]          rotated k_pe (shared by every head)
  *   out_q_int8 int8 [T, H, Dn + R]  q codes (NULL iff Lq == 0)
- *   out_scale  FP32 [T]             per-token q scale (NULL iff Lq == 0)
+ *   out_scale  FP32 [T]             per-token q scale (NULL iff Lq == 0);
+ *              FP32 [T, H] with MLA_PROLOG_QUANT_PER_HEAD
  * One run at a time per handle (the workspace is shared): use one handle per
  * concurrent stream.  Inputs and outputs must not overlap.
  * Errors: INVALID_ARG, CUDA.
@@ -127,6 +156,30 @@ int mla_prolog_run(mla_prolog_t h,
                    void* out_k, void* out_v, void* out_kpe,
                    int8_t* out_q_int8, float* out_scale,
                    void* stream);
+
+/*
+ * mla_prolog_run() plus the write of the MLA latent KV cache.  The
+ * DeepSeek-V3.2-Exp PyPTO article (section 2.3 and its step 2) caches the
+ * prolog's results in the KV cache with a ScatterUpdate; the cache layout is
+ * not printed, and this library reads it as one BF16 row per slot:
+ *   kv_cache      BF16 [num_slots, Lkv + R], 16-byte aligned (device)
+ *   slot_mapping  int32 [T] (device): token t writes row slot_mapping[t] =
+ *                 [normed c_kv (Lkv, the expansion's input) | k_pe_rot (R)]
+ * A negative slot marks a padding token: nothing is written.  A slot
+ * >= num_slots is skipped and sets MLA_STATUS_SLOT_RANGE.  A token whose
+ * position is out of range writes a zero row (as for its other outputs).
+ * Two tokens with the same slot leave one of their rows (which one is not
+ * specified).  Every other output and argument is that of mla_prolog_run().
+ * Errors: INVALID_ARG (null cache or slot_mapping, misalignment,
+ * num_slots < 0), CUDA.
+ */
+int mla_prolog_run_cached(mla_prolog_t h,
+                          const void* x, const void* gamma, const void* W_a, const void* W_b,
+                          const int32_t* positions, const float* cos_sin,
+                          void* out_k, void* out_v, void* out_kpe,
+                          int8_t* out_q_int8, float* out_scale,
+                          const int32_t* slot_mapping, void* kv_cache, int64_t num_slots,
+                          void* stream);
 
 /* Frees the workspace and the handle.  NULL-safe.  Synchronises the device. */
 int mla_prolog_destroy(mla_prolog_t h);
@@ -193,8 +246,9 @@ const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i);
  *   MLA_TAP_NORMED  BF16 [T, Lq + Lkv]  normed c_q | c_kv (after gamma and the
  *                                       BF16 cast: input of the expansion)
  *   MLA_TAP_Q       FP32 [T, H(Dn+R)]   q after its projection and RoPE (the
- *                                       quantisation input; Lq > 0 only)
- *   MLA_TAP_AMAX    FP32 [T]            max |q| per token (Lq > 0 only)
+ *                                       quantisation input; Lq > 0 and no
+ *                                       MLA_PROLOG_QUANT_PER_HEAD)
+ *   MLA_TAP_AMAX    FP32 [T]            max |q| per token (as MLA_TAP_Q)
  * Errors: INVALID_ARG (unknown tap, tap absent, size mismatch), CUDA.
  */
 #define MLA_TAP_NORMED 1
@@ -236,7 +290,8 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
  * fit (split-K partials + normed rows + FP32 q rows + amax, i.e. decode-sized
  * batches) are rejected with MLA_ERR_UNSUPPORTED_DIMS before anything runs.
  * `status` (device int32, may be NULL) receives the run's device status word
- * (MLA_STATUS_* bits).
+ * (MLA_STATUS_* bits).  Of the dims flags only MLA_PROLOG_QUANT_Q is taken
+ * (the variant flags give MLA_ERR_INVALID_ARG).
  *
  * The first call on a device looks up the array's device address and sets
  * the kernels' attributes; make that first call before any stream capture.

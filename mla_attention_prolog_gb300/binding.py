@@ -19,8 +19,12 @@ LIB_PATH = os.path.join(_HERE, "libmla_prolog.so")
 
 MLA_OK = 0
 MLA_PROLOG_QUANT_Q = 1
+MLA_PROLOG_ROPE_INTERLEAVED = 2
+MLA_PROLOG_Q_HEAD_NORM = 4
+MLA_PROLOG_QUANT_PER_HEAD = 8
 STATUS_POSITION_RANGE = 0x1
 STATUS_WAIT_TIMEOUT = 0x2
+STATUS_SLOT_RANGE = 0x4
 
 EXPORTED = [
     "mla_prolog_create", "mla_prolog_run", "mla_prolog_destroy", "mla_prolog_device_status",
@@ -28,7 +32,7 @@ EXPORTED = [
     "mla_prolog_set_wait_timeout", "mla_prolog_selftest_wait_timeout",
     "mla_prolog_set_timing_events", "mla_prolog_kernel_count", "mla_prolog_kernel_name",
     "mla_prolog_workspace_bytes", "mla_prolog_schedule", "mla_prolog_copy_tap", "mla_prolog_set_tuning",
-    "mla_prolog_run_noalloc",
+    "mla_prolog_run_noalloc", "mla_prolog_run_cached",
 ]
 TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
 TUNE_COMPRESS_GROUP = 1
@@ -83,6 +87,7 @@ def lib(path: Optional[str] = None):
     L.mla_prolog_copy_tap.argtypes = [V, I32, V, ctypes.c_size_t, V]
     L.mla_prolog_set_tuning.argtypes = [V, I32, I32]
     L.mla_prolog_run_noalloc.argtypes = [P(MlaPrologDims)] + [V] * 13
+    L.mla_prolog_run_cached.argtypes = [V] * 14 + [ctypes.c_int64, V]
     for n in EXPORTED:
         if n not in ("mla_prolog_strerror", "mla_prolog_last_cuda_error", "mla_prolog_kernel_count",
                      "mla_prolog_kernel_name"):
@@ -153,14 +158,14 @@ class MlaProlog:
         except Exception:
             pass
 
-    def run(self, x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe,
-            out_q_int8=None, out_scale=None, stream=None) -> None:
+    def _args(self, x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe, out_q_int8, out_scale):
         d = self.dims
         dev = self.device
         Lq, Lkv, R, H, Dn, Dv = d.q_lora_rank, d.kv_lora_rank, d.rope_dim, d.num_heads, d.nope_dim, d.v_dim
         bf = torch.bfloat16
         wb = H * (Dn + R) * Lq + H * (Dn + Dv) * Lkv
-        args = [
+        scale_shape = (d.T, H) if d.flags & MLA_PROLOG_QUANT_PER_HEAD else (d.T,)
+        return [
             _ptr(x, "x", bf, (d.T, d.D), dev),
             _ptr(gamma, "gamma", bf, (Lq + Lkv,), dev),
             _ptr(W_a, "W_a", bf, (Lq + Lkv + R, d.D), dev),
@@ -171,10 +176,27 @@ class MlaProlog:
             _ptr(out_v, "out_v", bf, (d.T, H, Dv), dev),
             _ptr(out_kpe, "out_kpe", bf, (d.T, R), dev),
             _ptr(out_q_int8, "out_q_int8", torch.int8, (d.T, H, Dn + R), dev),
-            _ptr(out_scale, "out_scale", torch.float32, (d.T,), dev),
-            _stream_ptr(stream),
+            _ptr(out_scale, "out_scale", torch.float32, scale_shape, dev),
         ]
-        _check(lib().mla_prolog_run(self.handle, *args), "mla_prolog_run")
+
+    def run(self, x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe,
+            out_q_int8=None, out_scale=None, stream=None) -> None:
+        args = self._args(x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe, out_q_int8, out_scale)
+        _check(lib().mla_prolog_run(self.handle, *args, _stream_ptr(stream)), "mla_prolog_run")
+
+    def run_cached(self, x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe,
+                   out_q_int8, out_scale, slot_mapping, kv_cache, stream=None) -> None:
+        """``run`` plus the latent KV-cache write: row ``slot_mapping[t]`` of
+        ``kv_cache`` (BF16 ``[num_slots, Lkv + R]``) gets ``[normed c_kv | k_pe_rot]``."""
+        d = self.dims
+        args = self._args(x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe, out_q_int8, out_scale)
+        if kv_cache.dim() != 2:
+            raise ValueError("kv_cache must be [num_slots, kv_lora_rank + rope_dim]")
+        n = kv_cache.shape[0]
+        cache = _ptr(kv_cache, "kv_cache", torch.bfloat16, (n, d.kv_lora_rank + d.rope_dim), self.device)
+        slots = _ptr(slot_mapping, "slot_mapping", torch.int32, (d.T,), self.device)
+        _check(lib().mla_prolog_run_cached(self.handle, *args, slots, cache, n, _stream_ptr(stream)),
+               "mla_prolog_run_cached")
 
     def device_status(self, stream=None) -> int:
         v = ctypes.c_int32(0)

@@ -112,8 +112,13 @@ int check_dims(const mla_prolog_dims& d) {
     if (d.rope_dim > 128 || d.T < 0 || d.num_heads < 1 || d.max_pos < 1) return MLA_ERR_UNSUPPORTED_DIMS;
     if (!std::isfinite(d.eps) || d.eps < 0.0f) return MLA_ERR_UNSUPPORTED_DIMS;
     const bool quant = (d.flags & MLA_PROLOG_QUANT_Q) != 0;
-    if ((d.flags & ~MLA_PROLOG_QUANT_Q) != 0) return MLA_ERR_INVALID_ARG;
+    const uint32_t known = MLA_PROLOG_QUANT_Q | MLA_PROLOG_ROPE_INTERLEAVED | MLA_PROLOG_Q_HEAD_NORM |
+                           MLA_PROLOG_QUANT_PER_HEAD;
+    if ((d.flags & ~known) != 0) return MLA_ERR_INVALID_ARG;
     if (quant != (d.q_lora_rank > 0)) return MLA_ERR_INVALID_ARG;
+    // the per-head norm and the per-head quant act on the q path
+    if ((d.flags & (MLA_PROLOG_Q_HEAD_NORM | MLA_PROLOG_QUANT_PER_HEAD)) && d.q_lora_rank == 0)
+        return MLA_ERR_INVALID_ARG;
     if (d.q_lora_rank > 0 && d.nope_dim + d.rope_dim > 256) return MLA_ERR_UNSUPPORTED_DIMS;
     // 32-bit index headroom of the kernels' row arithmetic
     const double big = static_cast<double>(d.T) * d.num_heads * (d.nope_dim + d.rope_dim + d.v_dim);
@@ -233,7 +238,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t T = static_cast<size_t>(d.T);
     const size_t b_part = al(static_cast<size_t>(h->splits_a) * T * h->NA * 4);
     const size_t b_norm = al(T * (Lq + Lkv) * 2);
-    const size_t b_q = Lq > 0 ? al(T * h->NQ * 4) : 0;
+    const bool per_head = (d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;  // no FP32 q round trip
+    const size_t b_q = Lq > 0 && !per_head ? al(T * h->NQ * 4) : 0;
     const size_t b_amax = al(T * 4);
     const size_t b_stat = 1024;  // status word, then the cooperative kernel's counters
     const size_t b_tab = al(table.size() * sizeof(int));
@@ -245,7 +251,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     char* w = static_cast<char*>(h->ws);
     h->partials = reinterpret_cast<float*>(w);
     h->normed = reinterpret_cast<uint16_t*>(w + b_part);
-    h->qws = Lq > 0 ? reinterpret_cast<float*>(w + b_part + b_norm) : nullptr;
+    h->qws = b_q > 0 ? reinterpret_cast<float*>(w + b_part + b_norm) : nullptr;
     h->amax = reinterpret_cast<uint32_t*>(w + b_part + b_norm + b_q);
     h->status = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax);
     h->sync = reinterpret_cast<unsigned*>(w + b_part + b_norm + b_q + b_amax + 128);
@@ -289,12 +295,24 @@ int mla_prolog_destroy(mla_prolog_t h) {
     return MLA_OK;
 }
 
-int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, const void* W_b,
-                   const int32_t* positions, const float* cos_sin, void* out_k, void* out_v, void* out_kpe,
-                   int8_t* out_q_int8, float* out_scale, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One pass of the prolog (mla_prolog_run, and mla_prolog_run_cached when
+// `cache` is not null).
+int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, const void* W_b,
+             const int32_t* positions, const float* cos_sin, void* out_k, void* out_v, void* out_kpe,
+             int8_t* out_q_int8, float* out_scale, const int32_t* slot_mapping, void* cache, int64_t num_slots,
+             void* stream) {
     if (!h) return MLA_ERR_INVALID_ARG;
     const mla_prolog_dims& d = h->d;
     const int Lq = d.q_lora_rank, Lkv = d.kv_lora_rank, R = d.rope_dim;
+    const bool interleaved = (d.flags & MLA_PROLOG_ROPE_INTERLEAVED) != 0;
+    const bool head_norm = (d.flags & MLA_PROLOG_Q_HEAD_NORM) != 0;
+    const bool per_head = (d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;
+    if (cache && (!slot_mapping || !aligned(slot_mapping, 4) || !aligned(cache, 16) || num_slots < 0))
+        return MLA_ERR_INVALID_ARG;
     if (d.T == 0) return MLA_OK;
     const void* p16[] = {x, gamma, W_a, W_b, cos_sin, out_k, out_v, out_kpe};
     for (const void* p : p16)
@@ -380,8 +398,12 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pn.normed = h->normed;
     pn.out_k = static_cast<uint16_t*>(out_k);
     pn.out_kpe = static_cast<uint16_t*>(out_kpe);
-    pn.amax = Lq > 0 ? h->amax : nullptr;
+    pn.amax = Lq > 0 && !per_head ? h->amax : nullptr;
     pn.status = h->status;
+    pn.interleaved = interleaved;
+    pn.cache = static_cast<uint16_t*>(cache);
+    pn.slots = slot_mapping;
+    pn.num_slots = num_slots;
 
     ExpandParams pb{};
     pb.T = d.T;
@@ -411,8 +433,16 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
     pb.amax = h->amax;
     pb.status = h->status;
     pb.timeout_ns = h->timeout_ns;
+    pb.interleaved = interleaved;
+    pb.head_norm = head_norm;
+    pb.inv_hd = 1.0f / static_cast<float>(d.nope_dim + R);
+    pb.eps = d.eps;
+    pb.per_head = per_head;
+    pb.q_codes = out_q_int8;
+    pb.q_scale = out_scale;
 
-    QuantParams pq{h->qws, h->amax, Lq > 0 ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
+    // the per-token quant kernel (the per-head quant runs in the q epilogue)
+    QuantParams pq{h->qws, h->amax, Lq > 0 && !per_head ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
 
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if (h->fused) {
@@ -442,11 +472,31 @@ int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void*
         cudaSuccess)
         return cuda_fail(e, "launch mla_expand_kernel");
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
-    if (Lq > 0) {
+    if (pq.rows > 0) {
         if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
     }
     if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_prolog_run(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, const void* W_b,
+                   const int32_t* positions, const float* cos_sin, void* out_k, void* out_v, void* out_kpe,
+                   int8_t* out_q_int8, float* out_scale, void* stream) {
+    return run_pass(h, x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe, out_q_int8, out_scale,
+                    nullptr, nullptr, 0, stream);
+}
+
+int mla_prolog_run_cached(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, const void* W_b,
+                          const int32_t* positions, const float* cos_sin, void* out_k, void* out_v, void* out_kpe,
+                          int8_t* out_q_int8, float* out_scale, const int32_t* slot_mapping, void* kv_cache,
+                          int64_t num_slots, void* stream) {
+    if (!kv_cache) return MLA_ERR_INVALID_ARG;
+    return run_pass(h, x, gamma, W_a, W_b, positions, cos_sin, out_k, out_v, out_kpe, out_q_int8, out_scale,
+                    slot_mapping, kv_cache, num_slots, stream);
 }
 
 int mla_prolog_device_status(mla_prolog_t h, void* stream, int32_t* status) {
@@ -522,12 +572,12 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
             src = h->normed;
             n = T * (d.q_lora_rank + d.kv_lora_rank) * 2;
             break;
-        case MLA_TAP_Q:
+        case MLA_TAP_Q:  // absent with the per-head quant (q never leaves the epilogue)
             src = h->qws;
             n = T * h->NQ * 4;
             break;
         case MLA_TAP_AMAX:
-            src = d.q_lora_rank > 0 ? h->amax : nullptr;
+            src = h->qws ? h->amax : nullptr;
             n = T * 4;
             break;
         default: return MLA_ERR_INVALID_ARG;

@@ -244,7 +244,7 @@ __device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& ti
 // once per token tile, while the epilogue warps wait for the accumulator, so
 // the RoPE does not wait on global loads between TMEM loads.
 struct RowCtx {
-    int t;
+    int t, pos;
     bool in, valid;
     float c[32], s[32];
 };
@@ -254,9 +254,10 @@ __device__ __forceinline__ void load_row_ctx(const ExpandParams& p, int t, RowCt
     rc.in = t < p.T;
     const int pos = rc.in ? p.positions[t] : 0;
     rc.valid = rc.in && pos >= 0 && pos < p.max_pos;
+    rc.pos = rc.valid ? pos : 0;
     if (p.nq_tiles > 0 && p.R <= 64) {
         const int half = p.R / 2;
-        const float* cs = p.cos_sin + static_cast<size_t>(rc.valid ? pos : 0) * p.R;
+        const float* cs = p.cos_sin + static_cast<size_t>(rc.pos) * p.R;
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
             if (i < half) {
@@ -279,77 +280,170 @@ __device__ __forceinline__ void rope8(const float (&a)[8], const float (&b)[8], 
     }
 }
 
-// q head h of one token row: FP32 q, RoPE of its rope slice, per-token max
-// |q|.  Column half 0 takes the nope columns, half 1 the rope slice.
-__device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int h,
-                                                  int half_idx) {
-    const int Dn = p.Dn, R = p.R;
-    const int t = rc.t;
-    const bool in = rc.in, valid = rc.valid;
-    float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * (Dn + R);
-    float amax = 0.0f;
-    for (int c = 0; c < (half_idx == 0 ? Dn : 0); c += 16) {
+// Rope pairs [i, i + 8) of q head's rope slice (TMEM columns Dn .. Dn + R of
+// this row): pair j is (Dn + j, Dn + R/2 + j), or, de-interleaved,
+// (Dn + 2j, Dn + 2j + 1); each value times rstd (the per-head norm) when
+// `scaled`, then rotated with (cc, ss).  Zero for a row whose position is
+// invalid.  Whole warp (TMEM loads).
+__device__ __forceinline__ void q_rope8(const ExpandParams& p, uint32_t tbase, bool valid, int i, bool scaled,
+                                        float rstd, const float* cc, const float* ss, float (&o1)[8],
+                                        float (&o2)[8]) {
+    const int Dn = p.Dn, half = p.R / 2;
+    float a[8], b[8];
+    if (p.interleaved) {
         float v[16];
-        tmem_ld16(tbase + c, v);
-        if (in) {
-            if (!valid) {
+        tmem_ld16(tbase + Dn + 2 * i, v);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = 0.0f;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
-            st_v8(qrow + c, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
-            st_v8(qrow + c + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
-        }
+        for (int e = 0; e < 8; ++e) a[e] = v[2 * e], b[e] = v[2 * e + 1];
+    } else {
+        tmem_ld8(tbase + Dn + i, a);
+        tmem_ld8(tbase + Dn + half + i, b);
     }
-    const int half = R / 2;
-    auto finish = [&](int i, const float (&o1)[8], const float (&o2)[8]) {
+    if (scaled) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
-        st_v8(qrow + Dn + i, o1[0], o1[1], o1[2], o1[3], o1[4], o1[5], o1[6], o1[7]);
-        st_v8(qrow + Dn + half + i, o2[0], o2[1], o2[2], o2[3], o2[4], o2[5], o2[6], o2[7]);
-    };
-    if (half_idx == 0) {
-        // nope columns only
-    } else if (R <= 64) {
+        for (int e = 0; e < 8; ++e) a[e] = __fmul_rn(a[e], rstd), b[e] = __fmul_rn(b[e], rstd);
+    }
+    if (valid) {
+        rope8(a, b, cc, ss, o1, o2);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
+    }
+}
+
+// Calls f(i, o1, o2) for every 8-pair chunk i of the row's rotated rope slice
+// (see q_rope8); cos/sin from the row context (R <= 64) or the table.
+template <class F>
+__device__ __forceinline__ void q_rope_chunks(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, bool scaled,
+                                              float rstd, F&& f) {
+    const int half = p.R / 2;
+    if (p.R <= 64) {
 #pragma unroll
         for (int i = 0; i < 32; i += 8) {
             if (i < half) {  // warp-uniform
-                float a[8], b[8], o1[8], o2[8];
-                tmem_ld8(tbase + Dn + i, a);
-                tmem_ld8(tbase + Dn + half + i, b);
-                if (in) {
-                    if (valid) {
-                        rope8(a, b, rc.c + i, rc.s + i, o1, o2);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
-                    }
-                    finish(i, o1, o2);
-                }
+                float o1[8], o2[8];
+                q_rope8(p, tbase, rc.valid, i, scaled, rstd, rc.c + i, rc.s + i, o1, o2);
+                f(i, o1, o2);
             }
         }
     } else {
-        // wide rope slices: cos/sin straight from the table
-        const int pos = in ? p.positions[t] : 0;
-        const float* cs = p.cos_sin + static_cast<size_t>(valid ? pos : 0) * R;
+        const float* cs = p.cos_sin + static_cast<size_t>(rc.pos) * p.R;
         for (int i = 0; i < half; i += 8) {
-            float a[8], b[8], o1[8], o2[8];
-            tmem_ld8(tbase + Dn + i, a);
-            tmem_ld8(tbase + Dn + half + i, b);
-            if (in) {
-                if (valid) {
-                    float cc[8], ss[8];
+            float cc[8], ss[8], o1[8], o2[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) cc[e] = cs[i + e], ss[e] = cs[half + i + e];
-                    rope8(a, b, cc, ss, o1, o2);
-                } else {
+            for (int e = 0; e < 8; ++e) cc[e] = cs[i + e], ss[e] = cs[half + i + e];
+            q_rope8(p, tbase, rc.valid, i, scaled, rstd, cc, ss, o1, o2);
+            f(i, o1, o2);
+        }
+    }
+}
+
+// Nope columns [c, c + 16) of the q head (times rstd when `scaled`; zero for
+// an invalid position).  Whole warp.
+__device__ __forceinline__ void q_nope16(uint32_t tbase, bool valid, int c, bool scaled, float rstd,
+                                         float (&v)[16]) {
+    tmem_ld16(tbase + c, v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o1[e] = o2[e] = 0.0f;
+    for (int e = 0; e < 16; ++e) v[e] = !valid ? 0.0f : scaled ? __fmul_rn(v[e], rstd) : v[e];
+}
+
+// Symmetric INT8 code of one value: rint(v * inv) (ties to even), clamped to
+// +-127, as one byte of a packed word.
+__device__ __forceinline__ uint32_t q_code(float v, float inv) {
+    int q = __float2int_rn(__fmul_rn(v, inv));
+    q = q > 127 ? 127 : (q < -127 ? -127 : q);
+    return static_cast<uint32_t>(q) & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t q_code4(const float* v, float inv) {
+    return q_code(v[0], inv) | (q_code(v[1], inv) << 8) | (q_code(v[2], inv) << 16) | (q_code(v[3], inv) << 24);
+}
+
+// q head h of one token row.  Column half 0 writes the nope columns, half 1
+// the rope slice.  Steps, as the q path defines them: the optional per-head
+// RMSNorm (no gamma; x^2 times 1/(Dn + R), summed in column order, + eps,
+// sqrt, reciprocal, x * rstd: both warps of the row compute the same rstd
+// from the whole head), the RoPE of the rope slice, then either
+//   per-token quant: FP32 q rows into the workspace and an atomic max of |q|
+//     per token (the quant kernel finishes), or
+//   per-(token, head) quant: amax of the head row (both warps, whole row),
+//     inv = 127/amax, codes rint(q * inv) clamped to +-127, scale amax/127,
+//     written straight from the epilogue (a zero row gives codes 0, scale 0).
+__device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int h,
+                                                  int half_idx) {
+    const int Dn = p.Dn, R = p.R, HD = Dn + R, half = R / 2;
+    const int t = rc.t;
+    const bool in = rc.in, valid = rc.valid;
+    const bool scaled = p.head_norm != 0;
+    float rstd = 1.0f;
+    if (scaled) {
+        float ms = 0.0f;
+        for (int c = 0; c < HD; c += 16) {
+            float v[16];
+            tmem_ld16(tbase + c, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ms = __fadd_rn(ms, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_hd));
+        }
+        rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+    }
+
+    if (p.per_head) {
+        float amax = 0.0f;
+        for (int c = 0; c < Dn; c += 16) {
+            float v[16];
+            q_nope16(tbase, valid, c, scaled, rstd, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        }
+        q_rope_chunks(p, tbase, rc, scaled, rstd, [&](int, const float (&o1)[8], const float (&o2)[8]) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
+        });
+        const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+        int8_t* crow = p.q_codes + (static_cast<size_t>(t) * p.H + h) * HD;
+        if (half_idx == 0) {
+            for (int c = 0; c < Dn; c += 16) {
+                float v[16];
+                q_nope16(tbase, valid, c, scaled, rstd, v);
+                if (in)
+                    *reinterpret_cast<uint4*>(crow + c) =
+                        make_uint4(q_code4(v, inv), q_code4(v + 4, inv), q_code4(v + 8, inv), q_code4(v + 12, inv));
+            }
+            if (in) p.q_scale[static_cast<size_t>(t) * p.H + h] = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f;
+        } else {
+            q_rope_chunks(p, tbase, rc, scaled, rstd, [&](int i, const float (&o1)[8], const float (&o2)[8]) {
+                if (in) {
+                    *reinterpret_cast<uint2*>(crow + Dn + i) = make_uint2(q_code4(o1, inv), q_code4(o1 + 4, inv));
+                    *reinterpret_cast<uint2*>(crow + Dn + half + i) =
+                        make_uint2(q_code4(o2, inv), q_code4(o2 + 4, inv));
                 }
-                finish(i, o1, o2);
+            });
+        }
+        return;
+    }
+
+    float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * HD;
+    float amax = 0.0f;
+    if (half_idx == 0) {
+        for (int c = 0; c < Dn; c += 16) {
+            float v[16];
+            q_nope16(tbase, valid, c, scaled, rstd, v);
+            if (in) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+                st_v8(qrow + c, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+                st_v8(qrow + c + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
             }
         }
+    } else {
+        q_rope_chunks(p, tbase, rc, scaled, rstd, [&](int i, const float (&o1)[8], const float (&o2)[8]) {
+            if (in) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
+                st_v8(qrow + Dn + i, o1[0], o1[1], o1[2], o1[3], o1[4], o1[5], o1[6], o1[7]);
+                st_v8(qrow + Dn + half + i, o2[0], o2[1], o2[2], o2[3], o2[4], o2[5], o2[6], o2[7]);
+            }
+        });
     }
     // |q| >= 0, so the order of the float bit patterns is the order of the values.
     if (valid) atomicMax(p.amax + t, __float_as_uint(amax));

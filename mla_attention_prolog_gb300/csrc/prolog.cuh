@@ -12,6 +12,7 @@ namespace mlap {
 
 constexpr int kStatusPositionRange = 0x1;
 constexpr int kStatusWaitTimeout = 0x2;
+constexpr int kStatusSlotRange = 0x4;
 
 constexpr int kBM = 128;  // MMA M: token rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;   // K per pipeline stage: one 128-byte swizzle atom of BF16
@@ -50,8 +51,14 @@ struct NormRopeParams {
     uint16_t* normed;   // [T][Lq + Lkv]
     uint16_t* out_k;    // [T][H][Dn + R]
     uint16_t* out_kpe;  // [T][R]
-    uint32_t* amax;     // [T] (cleared here when the q path is on)
+    uint32_t* amax;     // [T] (cleared here when the per-token q quant is on)
     int* status;
+    int interleaved;    // k_pe de-interleaved (pairs (2i, 2i+1)) before the RoPE
+    // latent KV cache (null: none): row slots[t] of [num_slots][Lkv + R]
+    // receives [normed c_kv | k_pe_rot]; a negative slot is skipped
+    uint16_t* cache;
+    const int32_t* slots;
+    long long num_slots;
 };
 
 // Expansion projections.  Tiles [0, nq_tiles) are q heads (one head of
@@ -70,10 +77,16 @@ struct ExpandParams {
     uint16_t* out_k;  // [T][H][Dn + R]
     uint16_t* out_v;  // [T][H][Dv]
     int out_aligned32;  // out_k and out_v 32-byte aligned: 256-bit stores
-    float* qws;       // [T][NQ] FP32 q after RoPE
-    uint32_t* amax;   // [T] bits of max |q| per token
+    float* qws;       // [T][NQ] FP32 q after RoPE (per-token quant)
+    uint32_t* amax;   // [T] bits of max |q| per token (per-token quant)
     int* status;
     uint64_t timeout_ns;
+    int interleaved;  // rope slices de-interleaved before the RoPE
+    int head_norm;    // per-head RMSNorm (no gamma) of q before its RoPE
+    float inv_hd, eps;  // 1 / (Dn + R) and the norm's epsilon
+    int per_head;     // INT8 codes and one scale per (token, head) in the epilogue
+    int8_t* q_codes;  // [T][H][Dn + R] (per_head)
+    float* q_scale;   // [T][H] (per_head)
 };
 
 struct QuantParams {

@@ -37,6 +37,34 @@ __device__ __forceinline__ float lane_butterfly_sum(float v) {
     return v;
 }
 
+// The latent KV-cache row of token t: null without a cache, for a negative
+// (padding) slot, and for a slot past the cache, which also sets
+// kStatusSlotRange (when `report`, i.e. from one thread of the token).
+__device__ __forceinline__ uint16_t* kv_cache_row(const NormRopeParams& p, int t, bool report) {
+    if (!p.cache) return nullptr;
+    const long long slot = p.slots[t];
+    if (slot < 0) return nullptr;
+    if (slot >= p.num_slots) {
+        if (report) atomicOr(p.status, kStatusSlotRange);
+        return nullptr;
+    }
+    return p.cache + slot * static_cast<long long>(p.Lkv + p.R);
+}
+
+// Destination of 8-column chunk c of the rotated k_pe: the rope slice of K's
+// head h (h < H), out_kpe (h == H), or the latent cache row (h == H + 1).
+__device__ __forceinline__ uint16_t* kpe_dst(const NormRopeParams& p, int t, int h, int c, uint16_t* cache_row) {
+    if (h < p.H) return p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + p.R) + p.Dn + c * 8;
+    if (h == p.H) return p.out_kpe + static_cast<size_t>(t) * p.R + c * 8;
+    return cache_row + p.Lkv + c * 8;
+}
+
+// Rope pair i of a k_pe row: (i, i + R/2), or, de-interleaved, (2i, 2i + 1).
+__device__ __forceinline__ void kpe_pair(int interleaved, int i, int half, int& j1, int& j2) {
+    j1 = interleaved ? 2 * i : i;
+    j2 = interleaved ? 2 * i + 1 : i + half;
+}
+
 // Shared memory a norm group needs per token: the BF16 row (NA + R) and the
 // FP32 chunk sums ((Lq + Lkv) / 4), 16-byte aligned.
 __host__ __device__ inline size_t norm_token_smem_bytes(int NA, int R, int Lq, int Lkv) {
@@ -97,7 +125,8 @@ __device__ __forceinline__ void norm_chunk_group(const NormRopeParams& p, const 
 // reduce the token's split-K partials in split order (TwoSum), round to
 // BF16, RMSNorm of c_q and c_kv (x^2/L summed as chunk_ssq describes,
 // + eps, sqrt, reciprocal, x * rstd, * gamma, BF16), rotate-half RoPE of
-// k_pe, and write the normed row, out_kpe and K's rope slice of every head.
+// k_pe, and write the normed row, out_kpe, K's rope slice of every head and
+// (with a cache) the token's latent cache row [normed c_kv | k_pe_rot].
 // `crow` is norm_token_smem_bytes of shared memory, `red` 2 floats.
 template <int NT, int BATCH, int FIRST = 0>
 __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint16_t* crow, float* red) {
@@ -112,16 +141,19 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     const bool valid = pos >= 0 && pos < p.max_pos;
     if (tid == 0 && p.amax) p.amax[t] = 0u;
     uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
+    uint16_t* cache_row = kv_cache_row(p, t, tid == 0);
     const int nchunk = R / 8;
+    const int ndst = p.H + (cache_row ? 2 : 1);  // rope-slice destinations (kpe_dst)
     if (!valid) {  // CTA-uniform
         if (tid == 0) atomicOr(p.status, kStatusPositionRange);
         const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) *reinterpret_cast<uint4*>(nrow + i) = z;
-        for (int k = tid; k < (p.H + 1) * nchunk; k += kNormThreads) {
+        for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) {
+            *reinterpret_cast<uint4*>(nrow + i) = z;
+            if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = z;
+        }
+        for (int k = tid; k < ndst * nchunk; k += kNormThreads) {
             const int h = k / nchunk, c = k - h * nchunk;
-            uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
-                                    : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
-            *reinterpret_cast<uint4*>(dst) = z;
+            *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = z;
         }
         return;
     }
@@ -184,7 +216,9 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
             const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[e]), rstd), bf16_hi(gs[e]));
             o[e] = pack_bf16x2(y0, y1);
         }
-        *reinterpret_cast<uint4*>(nrow + i) = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(nrow + i) = ov;
+        if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
     };
 #pragma unroll
     for (int u = 0; u < kGammaPre; ++u) {
@@ -194,11 +228,15 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     for (int i = (tid + kGammaPre * kNormThreads) * 8; i < Lq + Lkv; i += kNormThreads * 8)
         norm8(i, *reinterpret_cast<const uint4*>(p.gamma + i));
 
-    // 3) k_pe RoPE (rotate-half) in FP32 with this token's cos/sin row.
+    // 3) k_pe RoPE (rotate-half) in FP32 with this token's cos/sin row; the
+    //    interleaved variant pairs (2i, 2i + 1) and stores the pair at
+    //    (i, i + R/2) (de-interleaved order).
     const uint16_t* kp = crow + Lq + Lkv;
     for (int i = tid; i < half; i += kNormThreads) {
-        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[i]) << 16);
-        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[i + half]) << 16);
+        int j1, j2;
+        kpe_pair(p.interleaved, i, half, j1, j2);
+        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[j1]) << 16);
+        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[j2]) << 16);
         const float c = i == tid ? c_pre : cs[i], s = i == tid ? s_pre : cs[half + i];
         const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
         const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
@@ -207,13 +245,11 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     }
     group_sync<NT, FIRST>();
 
-    // 4) out_kpe[t] and the shared rope slice of K for every head.
-    for (int k = tid; k < (p.H + 1) * nchunk; k += kNormThreads) {
+    // 4) out_kpe[t], the shared rope slice of K for every head and the
+    //    cache row's k_pe.
+    for (int k = tid; k < ndst * nchunk; k += kNormThreads) {
         const int h = k / nchunk, c = k - h * nchunk;
-        const uint4 v = *reinterpret_cast<const uint4*>(rot + c * 8);
-        uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
-                                : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
-        *reinterpret_cast<uint4*>(dst) = v;
+        *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = *reinterpret_cast<const uint4*>(rot + c * 8);
     }
 }
 

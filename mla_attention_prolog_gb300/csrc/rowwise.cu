@@ -6,7 +6,10 @@
 //   (sum of x^2/L, + eps, sqrt, reciprocal, x * rstd, * gamma, cast to BF16:
 //   PyPTO-Gym AT-10 article, section 三 variant B and section 五) and
 //   rotate-half RoPE to k_pe, and writes out_kpe plus the rope slice of every
-//   head of out_k (the "assemble" step of the V2-Lite migration guide).
+//   head of out_k (the "assemble" step of the V2-Lite migration guide) and,
+//   when a latent KV cache is given, the token's cache row [normed c_kv |
+//   k_pe_rot] (the ScatterUpdate into the KV cache of the DeepSeek-V3.2-Exp
+//   PyPTO article).
 //
 // mla_quant_kernel  one CTA per token row: per-token symmetric INT8 with
 //   correctly rounded FP32 operations (inv = 127/amax, rint(y*inv) ties to
@@ -48,16 +51,19 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
     const bool valid = pos >= 0 && pos < p.max_pos;
     if (lane == 0 && p.amax) p.amax[t] = 0u;
     uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
+    uint16_t* cache_row = kv_cache_row(p, t, lane == 0);
     const int nchunk = R / 8;
+    const int ndst = p.H + (cache_row ? 2 : 1);  // rope-slice destinations (kpe_dst)
     if (!valid) {
         if (lane == 0) atomicOr(p.status, kStatusPositionRange);
         const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = lane * 8; i < Lq + Lkv; i += 256) *reinterpret_cast<uint4*>(nrow + i) = z;
-        for (int k = lane; k < (p.H + 1) * nchunk; k += 32) {
+        for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+            *reinterpret_cast<uint4*>(nrow + i) = z;
+            if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = z;
+        }
+        for (int k = lane; k < ndst * nchunk; k += 32) {
             const int h = k / nchunk, c = k - h * nchunk;
-            uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
-                                    : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
-            *reinterpret_cast<uint4*>(dst) = z;
+            *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = z;
         }
         return;
     }
@@ -92,13 +98,17 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
             const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[e]), rstd), bf16_hi(gs[e]));
             o[e] = pack_bf16x2(y0, y1);
         }
-        *reinterpret_cast<uint4*>(nrow + i) = make_uint4(o[0], o[1], o[2], o[3]);
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(nrow + i) = ov;
+        if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
     }
     const uint16_t* kp = crow + Lq + Lkv;
     const float* cs = p.cos_sin + static_cast<size_t>(pos) * R;
     for (int i = lane; i < half; i += 32) {
-        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[i]) << 16);
-        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[i + half]) << 16);
+        int j1, j2;
+        kpe_pair(p.interleaved, i, half, j1, j2);
+        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[j1]) << 16);
+        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[j2]) << 16);
         const float c = cs[i], s = cs[half + i];
         const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
         const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
@@ -106,12 +116,9 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
         rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
     }
     __syncwarp();
-    for (int k = lane; k < (p.H + 1) * nchunk; k += 32) {
+    for (int k = lane; k < ndst * nchunk; k += 32) {
         const int h = k / nchunk, c = k - h * nchunk;
-        const uint4 v = *reinterpret_cast<const uint4*>(rot + c * 8);
-        uint16_t* dst = h < p.H ? p.out_k + (static_cast<size_t>(t) * p.H + h) * (p.Dn + R) + p.Dn + c * 8
-                                : p.out_kpe + static_cast<size_t>(t) * R + c * 8;
-        *reinterpret_cast<uint4*>(dst) = v;
+        *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = *reinterpret_cast<const uint4*>(rot + c * 8);
     }
 }
 

@@ -64,7 +64,7 @@ def alloc_outputs(d: wl.Dims, dev):
     )
     if d.q_lora_rank > 0:
         outs["out_q_int8"] = Guarded((d.T, H, Dn + R), torch.int8, dev)
-        outs["out_scale"] = Guarded((d.T,), torch.float32, dev)
+        outs["out_scale"] = Guarded((d.T, d.num_heads) if d.quant_per_head else (d.T,), torch.float32, dev)
     return outs
 
 

@@ -57,6 +57,8 @@ def _dims(**kw):
     (dict(eps=float("nan")), -2), (dict(eps=-1.0), -2), (dict(q_lora_rank=24, flags=1), -2),
     (dict(q_lora_rank=64, flags=0), -1), (dict(flags=1), -1), (dict(flags=4), -1),
     (dict(q_lora_rank=64, flags=1, nope_dim=256, rope_dim=64), -2),
+    (dict(flags=8), -1), (dict(flags=2 | 4), -1), (dict(flags=16), -1),   # q variants without a q path
+    (dict(q_lora_rank=64, flags=1 | 32), -1), (dict(q_lora_rank=64, flags=8), -1),
 ])
 def test_create_rejects_bad_dims_without_touching_cuda(L, kw, code):
     h = ctypes.c_void_p()
@@ -69,6 +71,7 @@ def test_null_arguments(L):
     h = ctypes.c_void_p()
     assert L.mla_prolog_create(None, ctypes.byref(h)) == -1
     assert L.mla_prolog_run(None, *([None] * 12)) == -1
+    assert L.mla_prolog_run_cached(None, *([None] * 13), 0, None) == -1
     assert L.mla_prolog_destroy(None) == 0
     st = ctypes.c_int32()
     assert L.mla_prolog_device_status(None, None, ctypes.byref(st)) == -1
@@ -84,3 +87,17 @@ def test_quant_rows_validates_before_launch(L):
     assert L.mla_prolog_quant_rows(ctypes.c_void_p(8), 2, 8, None, None, None) == -1
     assert L.mla_prolog_quant_rows(ctypes.c_void_p(20), 2, 8, ctypes.c_void_p(16),
                                    ctypes.c_void_p(16), None) == -1       # y not 16-B aligned
+
+
+def test_flag_bits_agree_across_header_binding_and_inputs():
+    """One set of flag bits: the header's, the binding's and the input module's."""
+    src = open(HEADER).read()
+    from mla_attention_prolog_gb300 import workloads as wl
+    for name, py, w in (("QUANT_Q", binding.MLA_PROLOG_QUANT_Q, wl.QUANT_Q),
+                        ("ROPE_INTERLEAVED", binding.MLA_PROLOG_ROPE_INTERLEAVED, wl.ROPE_INTERLEAVED),
+                        ("Q_HEAD_NORM", binding.MLA_PROLOG_Q_HEAD_NORM, wl.Q_HEAD_NORM),
+                        ("QUANT_PER_HEAD", binding.MLA_PROLOG_QUANT_PER_HEAD, wl.QUANT_PER_HEAD)):
+        m = re.search(r"#define MLA_PROLOG_%s\s+(0x[0-9a-fA-F]+)u" % name, src)
+        assert m and int(m.group(1), 16) == py == w, name
+    m = re.search(r"#define MLA_STATUS_SLOT_RANGE\s+(0x[0-9a-fA-F]+)", src)
+    assert m and int(m.group(1), 16) == binding.STATUS_SLOT_RANGE
