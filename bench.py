@@ -22,6 +22,7 @@ on the data path); value = tokens of all ranks / max time over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -148,20 +149,25 @@ class ClockSampler:
 
 # ------------------------------------------------------ per-kernel accounting
 
-def kernel_work(d: wl.Dims):
+def kernel_work(d: wl.Dims, cache: bool = False):
     """Algorithmic bytes and flops attributed to each kernel of one run.
 
     Bytes: every input a kernel must read once plus every output it must write
     once (workspace traffic excluded); they add up to the whole op's count.
+    The per-head quant writes its codes and scales from the expansion kernel;
+    the latent cache rows are written by the norm kernel.
     Flops: 2 * T * N * K of the projection the kernel computes.
     """
     T, H, Dn, Dv, R = d.T, d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
+    q_out = (T * d.n_q + 4 * T * d.n_scales) if d.quant_q else 0
     b = {
         "mla_compress_kernel": 2 * T * d.D + 2 * d.n_a * d.D,
         "mla_norm_rope_kernel": 2 * (d.q_lora_rank + d.kv_lora_rank) + 4 * T + 4 * T * R
-                                + 2 * T * R + 2 * T * H * R,
-        "mla_expand_kernel": 2 * d.w_b_elems + 2 * T * H * Dn + 2 * T * H * Dv,
-        "mla_quant_kernel": (T * d.n_q + 4 * T) if d.quant_q else 0,
+                                + 2 * T * R + 2 * T * H * R
+                                + ((4 * T + 2 * T * (d.kv_lora_rank + R)) if cache else 0),
+        "mla_expand_kernel": 2 * d.w_b_elems + 2 * T * H * Dn + 2 * T * H * Dv
+                             + (q_out if d.quant_per_head else 0),
+        "mla_quant_kernel": 0 if d.quant_per_head else q_out,
     }
     f = {
         "mla_compress_kernel": 2 * T * d.n_a * d.D,
@@ -169,9 +175,12 @@ def kernel_work(d: wl.Dims):
         "mla_expand_kernel": 2 * T * (d.n_q * d.q_lora_rank + d.n_kv * d.kv_lora_rank),
         "mla_quant_kernel": 0,
     }
-    assert sum(b.values()) == wl.algorithmic_bytes(d)
+    assert sum(b.values()) == wl.algorithmic_bytes(d, cache)
+    # the cluster kernel runs the compression and the norm step
+    b["mla_compress_norm_kernel"] = b["mla_compress_kernel"] + b["mla_norm_rope_kernel"]
+    f["mla_compress_norm_kernel"] = f["mla_compress_kernel"]
     # the cooperative decode kernel runs every step in one launch
-    b["mla_decode_kernel"] = wl.algorithmic_bytes(d)
+    b["mla_decode_kernel"] = wl.algorithmic_bytes(d, cache)
     f["mla_decode_kernel"] = wl.algorithmic_flops(d)
     return b, f
 
@@ -216,7 +225,10 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
+    variants = parse_variants(args.variant)
     d = w.dims if not args.tokens else w.dims.with_T(args.tokens)
+    d = dataclasses.replace(d, flags=d.flags | sum(wl.VARIANTS[v] for v in variants))
+    cached = "cache" in variants
     inp = wl.make_inputs(w, d)
     H, Dn, Dv, R = d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
 
@@ -234,9 +246,15 @@ def run_gpu(args):
                  out_q_int8=None, out_scale=None)
         if d.q_lora_rank:
             o["out_q_int8"] = torch.empty((d.T, H, Dn + R), dtype=torch.int8, device=dev)
-            o["out_scale"] = torch.empty((d.T,), dtype=torch.float32, device=dev)
+            o["out_scale"] = torch.empty((d.T, H) if d.quant_per_head else (d.T,), dtype=torch.float32,
+                                         device=dev)
+        if cached:  # a latent cache of 2T slots, token t -> a seeded slot
+            o["kv_cache"] = torch.empty((2 * d.T, d.kv_lora_rank + R), dtype=torch.bfloat16, device=dev)
         return o
 
+    if cached:
+        base["slot_mapping"] = torch.from_numpy(
+            np.random.default_rng(1).permutation(2 * d.T)[:d.T].astype(np.int32)).to(dev)
     set_bytes = sum(t.numel() * t.element_size() for t in base.values())
     set_bytes += sum(t.numel() * t.element_size() for t in new_outputs().values() if t is not None)
     n_sets = max(2, -(-3 * L2_BYTES // set_bytes))
@@ -250,12 +268,17 @@ def run_gpu(args):
     clk = ClockSampler(local).__enter__()
     p = binding.MlaProlog.from_dims(d)
     names = p.kernel_names()
-    active = [n for n in names if n != "mla_quant_kernel" or d.q_lora_rank]
+    active = [n for n in names if n != "mla_quant_kernel" or (d.q_lora_rank and not d.quant_per_head)]
     stream = torch.cuda.Stream(device=dev)
 
     def one(s):
-        p.run(s["x"], s["gamma"], s["W_a"], s["W_b"], s["positions"], s["cos_sin"], s["out_k"], s["out_v"],
-              s["out_kpe"], s["out_q_int8"], s["out_scale"], stream=stream)
+        if cached:
+            p.run_cached(s["x"], s["gamma"], s["W_a"], s["W_b"], s["positions"], s["cos_sin"], s["out_k"],
+                         s["out_v"], s["out_kpe"], s["out_q_int8"], s["out_scale"], s["slot_mapping"],
+                         s["kv_cache"], stream=stream)
+        else:
+            p.run(s["x"], s["gamma"], s["W_a"], s["W_b"], s["positions"], s["cos_sin"], s["out_k"], s["out_v"],
+                  s["out_kpe"], s["out_q_int8"], s["out_scale"], stream=stream)
 
     # eager warm-up (also builds the tensor maps of each set)
     with torch.cuda.stream(stream):
@@ -329,7 +352,7 @@ def run_gpu(args):
     pin = lambda t: t.cpu().pin_memory()
     hx, hpos = pin(base["x"]), pin(base["positions"])
     outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in sets[0].items()
-              if k.startswith("out_") and v is not None}
+              if (k.startswith("out_") or k == "kv_cache") and v is not None}
     s0 = sets[0]
     h2d = hx.numel() * hx.element_size() + hpos.numel() * hpos.element_size()
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
@@ -362,7 +385,7 @@ def run_gpu(args):
     tokens = d.T * K * world
     value = tokens / (ms_total / 1e3)
     peaks, peak_src = load_peaks()
-    kb, kf = kernel_work(d)
+    kb, kf = kernel_work(d, cached)
     dom = max(per_kernel, key=per_kernel.get)
     dom_ms = per_kernel[dom]
     if w.bound == "tensor":
@@ -375,18 +398,21 @@ def run_gpu(args):
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4)}
+    wname = "+".join([args.workload] + variants)
     roof.update({"kernel": dom, "kernel_ms": round(dom_ms, 5), "peak_source": peak_src,
-                 "traffic": committed_traffic(dom, args.workload)})
-    whole = {"algorithmic_bytes": wl.algorithmic_bytes(d), "algorithmic_flops": wl.algorithmic_flops(d),
-             "hbm_frac": round(wl.algorithmic_bytes(d) / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                 "traffic": committed_traffic(dom, wname)})
+    abytes = wl.algorithmic_bytes(d, cached)
+    whole = {"algorithmic_bytes": abytes, "algorithmic_flops": wl.algorithmic_flops(d),
+             "hbm_frac": round(abytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
              "tc_frac": round(wl.algorithmic_flops(d) / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "T": d.T, "D": d.D, "q_lora_rank": d.q_lora_rank,
+        "config": {"workload": wname, "T": d.T, "D": d.D, "q_lora_rank": d.q_lora_rank,
                    "kv_lora_rank": d.kv_lora_rank, "rope_dim": d.rope_dim, "num_heads": d.num_heads,
-                   "nope_dim": d.nope_dim, "v_dim": d.v_dim, "quant_q": d.quant_q,
+                   "nope_dim": d.nope_dim, "v_dim": d.v_dim, "quant_q": d.quant_q, "flags": d.flags,
+                   "kv_cache_write": cached,
                    "l2": f"{n_sets} rotating buffer sets of {set_bytes / 1e6:.1f} MB (> 3x L2)",
                    "timing": f"{reps} replay(s) of a {G}-step CUDA graph" + (f" + {rem}" if rem else "")
                              + " between CUDA events", "parallelism": f"replicas x{world}",
@@ -400,7 +426,7 @@ def run_gpu(args):
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, d)
     p.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -409,11 +435,20 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def parse_variants(spec: str):
+    """'' or a comma list of interleaved, head_norm, per_head, cache."""
+    out = [v for v in (x.strip() for x in spec.split(",")) if v]
+    for v in out:
+        if v not in wl.VARIANTS:
+            raise SystemExit(f"unknown variant {v!r}; choose from {sorted(wl.VARIANTS)}")
+    return sorted(set(out), key=list(wl.VARIANTS).index)
+
+
 # ------------------------------------------------------------------ CPU arm
 
-def oracle_sample(w: wl.Workload, max_tokens: int):
+def oracle_sample(w: wl.Workload, max_tokens: int, dims=None):
     """Inputs and a token sample of the workload for the oracle (bounded)."""
-    inp = wl.make_inputs(w)
+    inp = wl.make_inputs(w, dims)
     T = inp.dims.T
     if T <= max_tokens:
         return inp, None
@@ -421,12 +456,13 @@ def oracle_sample(w: wl.Workload, max_tokens: int):
     return inp, np.sort(rng.choice(T, max_tokens, replace=False)).astype(np.int32)
 
 
-def cpu_baseline(w: wl.Workload, seconds: float):
+def cpu_baseline(w: wl.Workload, seconds: float, dims=None):
     import oracle
     oracle.build()
-    per_tok = wl.algorithmic_flops(w.dims) / w.dims.T
-    max_tokens = max(1, min(w.dims.T, int(4e10 / per_tok)))  # ~40 GFLOP of fp64 work per call at most
-    inp, tok = oracle_sample(w, max_tokens)
+    dims = dims or w.dims
+    per_tok = wl.algorithmic_flops(dims) / max(1, dims.T)
+    max_tokens = max(1, min(dims.T, int(4e10 / per_tok)))  # ~40 GFLOP of fp64 work per call at most
+    inp, tok = oracle_sample(w, max_tokens, dims)
     d = inp.dims
     n = d.T if tok is None else len(tok)
     t0 = time.perf_counter()
@@ -483,6 +519,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T of the workload (small profiling cases; not a bench line)")
+    ap.add_argument("--variant", default="",
+                    help="comma list of interleaved, head_norm, per_head (dims flags) and cache "
+                         "(the latent KV-cache write); default: the base path")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

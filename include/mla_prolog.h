@@ -274,6 +274,19 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            device allow it); 0 (the default): as four
  *                            kernels.  INVALID_ARG when 1 is not available. */
 #define MLA_TUNE_DECODE_FUSED 3
+/*   MLA_TUNE_CLUSTER_NORM    1: the compression projection and the norm run
+ *                            in one thread-block cluster of up to 16 CTAs
+ *                            that sum the split-K partials in distributed
+ *                            shared memory, then the expansion kernel
+ *                            (available for batches of at most 128 tokens
+ *                            with small compression weights, e.g. the
+ *                            DeepSeek-V2-Lite KV prolog; the default only for
+ *                            tiny problems, where it measured faster); 0:
+ *                            split-K compression over every SM, norm kernel,
+ *                            expansion.  INVALID_ARG when 1 is not available.
+ *                            Setting 1 turns MLA_TUNE_DECODE_FUSED off, and
+ *                            the reverse. */
+#define MLA_TUNE_CLUSTER_NORM 4
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*
@@ -313,7 +326,8 @@ int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes);
 
 /*
  * Schedule chosen at create time, for reports: tile widths and split-K of the
- * two projections.  Any pointer may be NULL.
+ * two projections (with the cluster compression: the column-group width and
+ * the K splits of the cluster).  Any pointer may be NULL.
  */
 int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a,
                         int32_t* bn_kv, int32_t* bn_q);

@@ -38,6 +38,7 @@ TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
 TUNE_COMPRESS_GROUP = 1
 TUNE_COMPRESS_COMPENSATED = 2
 TUNE_DECODE_FUSED = 3
+TUNE_CLUSTER_NORM = 4
 
 
 class MlaPrologDims(ctypes.Structure):

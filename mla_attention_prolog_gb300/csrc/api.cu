@@ -62,6 +62,7 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
+const char* const kClusterKernelNames[3] = {"mla_compress_norm_kernel", "mla_expand_kernel", "mla_quant_kernel"};
 const char* const kFusedKernelName = "mla_decode_kernel";
 
 }  // namespace
@@ -93,8 +94,14 @@ struct mla_prolog {
     size_t decode_smem = 0;
     unsigned* sync = nullptr;  // its hand-over counters (kSyncWords words)
     uint64_t timeout_ns = 1000000000ull;
+    // compression + norm in one thread-block cluster (small decode batches)
+    bool cluster_ok = false;   // the dims and the device allow it
+    bool cluster = false;      // in use (tunable; on by default where allowed)
+    ClusterPlan cplan;
+    int cluster_ctas = 0, cluster_expand_grid = 0;
+    GemmShape cluster_shape_b = GemmShape::Narrow;
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
-    CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wqb{}, tm_wkvb{};
+    CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wa_c{}, tm_wqb{}, tm_wkvb{};
     const void* last_x = nullptr;
     const void* last_wa = nullptr;
     const void* last_wb = nullptr;
@@ -201,6 +208,31 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // GB300 (both dies' L2s take part), so the kernel's three barriers cost
     // more than the overlapped (PDL) hand-offs of the four-kernel path.
     h->fused = false;
+    // Small decode batches: compression + norm in one cluster of up to 16
+    // CTAs (8 where 16 cannot be co-scheduled), the expansion on the other
+    // SMs with every K block of its weights in flight before the hand-off.
+    if (h->m_tiles == 1) {
+        for (int ctas_max : {kClusterMaxCtas, 8}) {
+            const ClusterPlan cp = plan_cluster(d.T, d.D, Lq, Lkv, R, ctas_max);
+            if (!cp.ok) break;
+            const int ctas = cp.nc * cp.ks;
+            int active = 0;
+            if (cluster_set_attributes(cp.smem, ctas) == cudaSuccess &&
+                cluster_max_active(cp.smem, ctas, &active) == cudaSuccess && active >= 1 && ctas < sms) {
+                h->cluster_ok = true;
+                h->cplan = cp;
+                h->cluster_ctas = ctas;
+                break;
+            }
+            cudaGetLastError();
+        }
+        cudaGetLastError();
+    }
+    if (h->cluster_ok) {
+        h->cluster = h->cplan.est_us <= kClusterDefaultUs;
+        h->cluster_expand_grid = njobs_b < sms - h->cluster_ctas ? njobs_b : sms - h->cluster_ctas;
+        h->cluster_shape_b = h->shape_b == GemmShape::Narrow ? GemmShape::Deep : h->shape_b;
+    }
     // A table is needed only when there are more jobs than SMs; the expansion
     // grid and the cooperative grid are then both one CTA per SM, so one
     // table serves either path.
@@ -333,6 +365,11 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     if (W_a != h->last_wa) {
         if (!encode_bf16(&h->tm_wa, W_a, d.D, h->NA, d.D, h->bn_a))
             return cuda_fail(cudaErrorInvalidValue, "tensor map W_a");
+        if (h->cluster_ok) {
+            const int cgw = h->cplan.cgw;
+            if (!encode_bf16(&h->tm_wa_c, W_a, d.D, h->NA, d.D, cgw <= 256 ? cgw : cgw / 2))
+                return cuda_fail(cudaErrorInvalidValue, "tensor map W_a (cluster)");
+        }
         h->last_wa = W_a;
     }
     if (W_b != h->last_wb) {
@@ -461,6 +498,39 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
         return MLA_OK;
     }
+    if (h->cluster) {
+        ClusterNormParams pc{};
+        const ClusterPlan& cp = h->cplan;
+        pc.T = d.T;
+        pc.NA = h->NA;
+        pc.kb_total = cdiv(d.D, kBK);
+        pc.nc = cp.nc;
+        pc.ks = cp.ks;
+        pc.cgw = cp.cgw;
+        pc.tpo = cp.tpo;
+        pc.stages = cp.stages;
+        pc.b_boxes = cp.cgw <= 256 ? 1 : 2;
+        pc.tmem_cols = cp.cgw <= 32 ? 32 : cp.cgw <= 64 ? 64 : cp.cgw <= 128 ? 128 : cp.cgw <= 256 ? 256 : 512;
+        pc.area_bytes = cp.area;
+        pc.recv_bytes = cp.recv;
+        pc.stg_off = cp.stg_off;
+        pc.const_off = cp.const_off;
+        pc.n = pn;
+        pc.status = h->status;
+        pc.timeout_ns = h->timeout_ns;
+        pb.job_table = nullptr;  // one job per CTA, or round robin
+        if ((e = launch_compress_norm_cluster(h->cluster_ctas, cp.smem, h->tm_x, h->tm_wa_c, pc, st)) != cudaSuccess)
+            return cuda_fail(e, "launch mla_compress_norm_kernel");
+        if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        if ((e = launch_expand(h->cluster_shape_b, h->cluster_expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb,
+                               h->tm_wkvb, pb, st)) != cudaSuccess)
+            return cuda_fail(e, "launch mla_expand_kernel");
+        if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        if (pq.rows > 0 && (e = launch_quant(pq, st, true)) != cudaSuccess)
+            return cuda_fail(e, "launch mla_quant_kernel");
+        if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        return MLA_OK;
+    }
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
     if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
         cudaSuccess)
@@ -554,11 +624,13 @@ int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_
     return MLA_OK;
 }
 
-int32_t mla_prolog_kernel_count(mla_prolog_t h) { return h ? (h->fused ? 1 : kKernelCount) : 0; }
+int32_t mla_prolog_kernel_count(mla_prolog_t h) {
+    return h ? (h->fused ? 1 : h->cluster ? 3 : kKernelCount) : 0;
+}
 
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
     if (!h || i < 0 || i >= mla_prolog_kernel_count(h)) return "";
-    return h->fused ? kFusedKernelName : kKernelNames[i];
+    return h->fused ? kFusedKernelName : h->cluster ? kClusterKernelNames[i] : kKernelNames[i];
 }
 
 int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream) {
@@ -603,7 +675,15 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->fused_ok) return MLA_ERR_INVALID_ARG;
             h->fused = value == 1;
+            if (h->fused) h->cluster = false;
             h->n_events = 0;  // the kernel count changed: re-arm the timing hook
+            return MLA_OK;
+        case MLA_TUNE_CLUSTER_NORM:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->cluster_ok) return MLA_ERR_INVALID_ARG;
+            h->cluster = value == 1;
+            if (h->cluster) h->fused = false;
+            h->n_events = 0;
             return MLA_OK;
         default: return MLA_ERR_INVALID_ARG;
     }
@@ -617,8 +697,8 @@ int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes) {
 
 int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a, int32_t* bn_kv, int32_t* bn_q) {
     if (!h) return MLA_ERR_INVALID_ARG;
-    if (bn_a) *bn_a = h->bn_a;
-    if (splits_a) *splits_a = h->splits_a;
+    if (bn_a) *bn_a = h->cluster ? h->cplan.cgw : h->bn_a;
+    if (splits_a) *splits_a = h->cluster ? h->cplan.ks : h->splits_a;
     if (bn_kv) *bn_kv = h->bn_kv;
     if (bn_q) *bn_q = h->d.q_lora_rank > 0 ? h->d.nope_dim + h->d.rope_dim : 0;
     return MLA_OK;

@@ -58,11 +58,13 @@ __global__ void mla_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 using EWide = Layout<256, 4>;
 using EMid = Layout<192, 5>;
 using ENarrow = Layout<64, 4>;
+using EDeep = Layout<64, 8>;
 using CWide = Layout<128, 6>;
 using CNarrow = Layout<64, 4>;
 
 int gemm_smem_bytes(GemmShape s) {
-    return s == GemmShape::Wide ? EWide::BYTES : s == GemmShape::Mid ? EMid::BYTES : ENarrow::BYTES;
+    return s == GemmShape::Wide ? EWide::BYTES : s == GemmShape::Mid ? EMid::BYTES
+                                : s == GemmShape::Deep ? EDeep::BYTES : ENarrow::BYTES;
 }
 
 cudaError_t gemm_set_attributes() {
@@ -81,6 +83,9 @@ cudaError_t gemm_set_attributes() {
         return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   ENarrow::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  EDeep::BYTES)))
         return e;
     return cudaSuccess;
 }
@@ -102,6 +107,9 @@ cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq, const
                              tm_aq, tm_akv, tm_bq, tm_bkv, p);
     if (s == GemmShape::Mid)
         return launch_kernel(mla_expand_kernel<192, 5>, dim3(grid), dim3(kExpandThreads), EMid::BYTES, st, true,
+                             tm_aq, tm_akv, tm_bq, tm_bkv, p);
+    if (s == GemmShape::Deep)
+        return launch_kernel(mla_expand_kernel<64, 8>, dim3(grid), dim3(kExpandThreads), EDeep::BYTES, st, true,
                              tm_aq, tm_akv, tm_bq, tm_bkv, p);
     return launch_kernel(mla_expand_kernel<64, 4>, dim3(grid), dim3(kExpandThreads), ENarrow::BYTES, st, true,
                          tm_aq, tm_akv, tm_bq, tm_bkv, p);

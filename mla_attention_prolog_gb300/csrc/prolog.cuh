@@ -17,6 +17,8 @@ constexpr int kStatusSlotRange = 0x4;
 constexpr int kBM = 128;  // MMA M: token rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;   // K per pipeline stage: one 128-byte swizzle atom of BF16
 
+inline int cdiv_host(int a, int b) { return (a + b - 1) / b; }
+
 // Compression projection: partial[split][t][n] = sum over the split's K range
 // of x[t, k] * W_a[n, k] (FP32).  Jobs: m_tiles x n_tiles x splits.
 struct CompressParams {
@@ -120,6 +122,117 @@ struct DecodeParams {
     uint64_t timeout_ns;
 };
 
+// Compression + split + RMSNorm + k_pe RoPE of one token tile in one
+// thread-block cluster (small decode batches): CTA rank r computes the
+// split-K partial of column group r / ks over K-split r % ks, stages it in
+// its own shared memory and copies each token's row (bulk copies, completed
+// on the owner's mbarrier) into the shared memory of the CTA that owns the
+// token (tokens [o * tpo, (o + 1) * tpo) belong to rank o), which then runs
+// the norm step for its tokens.
+//
+// Shared memory (from a 1 KB aligned base): the ring [0, area); once the
+// ring is free, the receive buffer [0, recv) ([split][group][token][cgw]
+// FP32), the norm groups' rows [recv, stg_off) and the staging rows
+// [stg_off, ...) (T rows of cgw FP32, 16-byte chunks XOR-swizzled by the
+// token's row); then the barriers, and from const_off the norm constants of
+// the owned tokens (gamma, positions, cos/sin rows) and the groups' partial
+// sums.
+struct ClusterNormParams {
+    int T, NA, kb_total;
+    int nc, ks, cgw, tpo;  // column groups, K splits, group width, tokens per owner
+    int stages;            // ring stages
+    int b_boxes;           // TMA boxes per weight tile (cgw > 256: two of cgw / 2 rows)
+    uint32_t tmem_cols;
+    uint32_t area_bytes;   // ring / receive area (1 KB aligned) before the barriers
+    uint32_t recv_bytes;   // receive buffer at the start of the area
+    uint32_t stg_off;      // staging rows (cgw floats each)
+    uint32_t const_off;    // norm constants
+    NormRopeParams n;      // outputs and norm constants (partials unused)
+    int* status;
+    uint64_t timeout_ns;
+};
+
+// The cluster layout for a problem, or ok = false when it does not pay
+// (more than one token tile, or too many weight bytes for a dozen SMs).
+// Measured on GB300, the cluster path beats the split-K path only when its
+// estimated loads + exchange stay near a microsecond (tiny batches): each of
+// its phases (cluster barriers, the exchange, the norm) costs 0.3-0.8 us of
+// latency whatever its size, and the 16 SMs receive weights at ~100 GB/s
+// each.  It is the default below kClusterDefaultUs and opt-in above.
+struct ClusterPlan {
+    bool ok = false;
+    int nc = 0, ks = 0, cgw = 0, tpo = 0, stages = 0;
+    double est_us = 0.0;  // estimated loads + exchange time
+    size_t smem = 0;
+    uint32_t area = 0, recv = 0, stg_off = 0, const_off = 0;
+};
+
+constexpr int kClusterThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 drain; all ten warps norm
+constexpr int kClusterNormGroups = 5;  // norm groups of two warps, one token each at a time
+constexpr int kClusterMaxCtas = 16;
+constexpr size_t kClusterSmemBudget = 216 * 1024;  // ring or receive area (+ barriers < 227 KB)
+constexpr size_t kClusterSmemMax = 227 * 1024;
+constexpr double kClusterDefaultUs = 1.5;
+
+__host__ __device__ inline size_t align16(size_t b) { return (b + 15) & ~static_cast<size_t>(15); }
+
+inline ClusterPlan plan_cluster(int T, int D, int Lq, int Lkv, int R, int max_ctas) {
+    ClusterPlan best;
+    const int NA = Lq + Lkv + R, kb = cdiv_host(D, kBK);
+    if (T < 1 || T > kBM) return best;
+    long long best_bytes = 0;
+    for (int nc = 1; nc <= max_ctas; ++nc) {
+        const int cgw = cdiv_host(cdiv_host(NA, nc), 32) * 32;
+        if (cgw > 512) continue;
+        const int ks = max_ctas / nc < kb ? max_ctas / nc : kb;
+        if (ks < 1) break;
+        const int kbps = cdiv_host(kb, ks);
+        const size_t stage = static_cast<size_t>(kBM) * kBK * 2 + static_cast<size_t>(cgw) * kBK * 2;
+        int stages = static_cast<int>(kClusterSmemBudget / stage);
+        if (stages > kbps) stages = kbps;
+        if (stages < 1 || (stages < 2 && kbps > 1)) continue;
+        const int ctas = nc * ks, tpo = cdiv_host(T, ctas);
+        const size_t recv = static_cast<size_t>(ks) * nc * tpo * cgw * 4;
+        const size_t rows = kClusterNormGroups * align16(static_cast<size_t>(NA + R) * 2);
+        const size_t stg_off = (recv + rows + 127) & ~static_cast<size_t>(127);
+        const size_t need = stg_off + static_cast<size_t>(T) * cgw * 4;
+        if (need > kClusterSmemBudget) continue;
+        const size_t ring = static_cast<size_t>(stages) * stage;
+        const size_t area = ((ring > need ? ring : need) + 1023) & ~static_cast<size_t>(1023);
+        const size_t const_off = area + 8 * (2 * stages + 2) + 16;
+        const size_t smem = const_off + align16(static_cast<size_t>(Lq + Lkv) * 2) + align16(tpo * 4) +
+                            static_cast<size_t>(tpo) * R * 4 + kClusterNormGroups * 4 * 4 + 1024;
+        if (smem > kClusterSmemMax) continue;
+        // Estimated time: the bytes one CTA must receive (its weight rows and
+        // the token rows of x) at ~100 GB/s per SM, plus the split partials
+        // exchanged inside the cluster at ~450 GB/s for the whole cluster
+        // (both rates measured on GB300).
+        const double t_load = static_cast<double>(kbps) * kBK * 2 * (cgw + T) / 100e3;
+        const double t_swap = static_cast<double>(ks - 1) * T * NA * 4 / 450e3;
+        const long long bytes = static_cast<long long>((t_load + t_swap) * 1e3);  // ns
+        if (!best.ok || bytes < best_bytes) {
+            best.ok = true;
+            best_bytes = bytes;
+            best.nc = nc, best.ks = ks, best.cgw = cgw, best.tpo = tpo, best.stages = stages;
+            best.area = static_cast<uint32_t>(area);
+            best.recv = static_cast<uint32_t>(recv);
+            best.stg_off = static_cast<uint32_t>(stg_off);
+            best.const_off = static_cast<uint32_t>(const_off);
+            best.smem = smem;
+            best.est_us = t_load + t_swap;
+        }
+    }
+    // Worth it while the loads and the exchange take a few microseconds;
+    // beyond that the split-K path over every SM wins.
+    if (best.ok && best_bytes > 5000) best.ok = false;
+    return best;
+}
+
+cudaError_t cluster_set_attributes(size_t smem, int ctas);
+cudaError_t cluster_max_active(size_t smem, int ctas, int* clusters);
+cudaError_t launch_compress_norm_cluster(int ctas, size_t smem, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
+                                         const ClusterNormParams& p, cudaStream_t st);
+
 size_t decode_smem_bytes(int NA, int R, int Lq, int Lkv);
 cudaError_t decode_set_attributes(size_t smem);
 cudaError_t decode_occupancy(size_t smem, int* blocks_per_sm);
@@ -131,12 +244,14 @@ constexpr int kDecodeMaxBN = 192;  // widest expansion tile the decode kernel ta
 // Shapes of the GEMM kernel instantiations.
 // Expansion kernel: Wide = BN_MAX 256, 4 stages; Mid = BN_MAX 192, 5 stages
 // (decode with a q path: one head of Dn + R <= 192 columns per tile);
-// Narrow = BN_MAX 64, 4 stages.
+// Narrow = BN_MAX 64, 4 stages; Deep = BN_MAX 64, 8 stages (after the
+// cluster compression: every K block of a narrow kv tile's weights is in
+// flight before the normed rows exist).
 // Compression kernel: Wide = BN_MAX 128, 6 stages; Narrow = BN_MAX 64, 4 stages.
 // The narrow (decode) shapes use half the shared memory so that a compression
 // CTA and an expansion CTA fit on one SM and the expansion can start
 // streaming its weights while the compression is still running.
-enum class GemmShape { Wide, Mid, Narrow };
+enum class GemmShape { Wide, Mid, Narrow, Deep };
 
 // Tile shapes and work split of one problem size, chosen on the host.
 struct Schedule {
@@ -148,8 +263,6 @@ struct Schedule {
     GemmShape shape_b;    // expansion kernel shape
     int bn_kv;            // expansion kv tile width
 };
-
-inline int cdiv_host(int a, int b) { return (a + b - 1) / b; }
 
 // T tokens, D model width, Lq / Lkv / R ranks, H heads of Dn + R (q) and
 // Dn + Dv (kv) columns, on a device with `sms` SMs.

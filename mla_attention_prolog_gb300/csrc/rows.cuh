@@ -253,6 +253,103 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     }
 }
 
+// One token of the norm step by one warp: reduce the token's `splits`
+// partial rows (prow + sp * sstride, FP32, global or shared memory) in split
+// order with TwoSum, round to BF16, RMSNorm of c_q and c_kv, RoPE of k_pe,
+// and write the normed row, out_kpe, K's rope slice of every head and the
+// cache row -- the arithmetic of norm_token, with the chunk sums of x^2 / L
+// on lane (i / 4) % 32 in increasing chunk order, so the bits agree with it
+// for equal partials.  `pos` is the token's position, `cs_row` its cos/sin
+// row (read only when pos is valid) and `gamma` the Lq + Lkv weights, from
+// global or shared memory.  `crow` is (NA + R) BF16 of this warp's shared
+// memory.
+__device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, int pos, const float* cs_row,
+                                                const uint16_t* gamma, const float* prow, size_t sstride,
+                                                int splits, uint16_t* crow) {
+    const int lane = threadIdx.x & 31;
+    const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, R = p.R, half = R / 2;
+    uint16_t* rot = crow + NA;
+    const bool valid = pos >= 0 && pos < p.max_pos;
+    if (lane == 0 && p.amax) p.amax[t] = 0u;
+    uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
+    uint16_t* cache_row = kv_cache_row(p, t, lane == 0);
+    const int nchunk = R / 8;
+    const int ndst = p.H + (cache_row ? 2 : 1);  // rope-slice destinations (kpe_dst)
+    if (!valid) {
+        if (lane == 0) atomicOr(p.status, kStatusPositionRange);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+            *reinterpret_cast<uint4*>(nrow + i) = z;
+            if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = z;
+        }
+        for (int k = lane; k < ndst * nchunk; k += 32) {
+            const int h = k / nchunk, c = k - h * nchunk;
+            *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = z;
+        }
+        return;
+    }
+    float ssq_q = 0.0f, ssq_kv = 0.0f;
+    for (int i = lane * 4; i < NA; i += 128) {
+        float4 a = *reinterpret_cast<const float4*>(prow + i), cmp = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4 r = *reinterpret_cast<const float4*>(prow + sp * sstride + i);
+            two_sum_add(a.x, cmp.x, r.x);
+            two_sum_add(a.y, cmp.y, r.y);
+            two_sum_add(a.z, cmp.z, r.z);
+            two_sum_add(a.w, cmp.w, r.w);
+        }
+        if (splits > 1)
+            a = make_float4(__fadd_rn(a.x, cmp.x), __fadd_rn(a.y, cmp.y), __fadd_rn(a.z, cmp.z), __fadd_rn(a.w, cmp.w));
+        const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
+        *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
+        const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+        // chunk i / 4 on lane (i / 4) % 32, in increasing order (chunk_ssq)
+        if (i < Lq)
+            ssq_q = __fadd_rn(ssq_q, chunk_ssq(v, p.inv_lq));
+        else if (i < Lq + Lkv)
+            ssq_kv = __fadd_rn(ssq_kv, chunk_ssq(v, p.inv_lkv));
+    }
+    ssq_q = lane_butterfly_sum(ssq_q);
+    ssq_kv = lane_butterfly_sum(ssq_kv);
+    const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
+    const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
+    __syncwarp();
+    for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
+        const uint4 gv = *reinterpret_cast<const uint4*>(gamma + i);
+        const float rstd = i < Lq ? rstd_q : rstd_kv;
+        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+        const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xs[e]), rstd), bf16_lo(gs[e]));
+            const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[e]), rstd), bf16_hi(gs[e]));
+            o[e] = pack_bf16x2(y0, y1);
+        }
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(nrow + i) = ov;
+        if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
+    }
+    const uint16_t* kp = crow + Lq + Lkv;
+    for (int i = lane; i < half; i += 32) {
+        int j1, j2;
+        kpe_pair(p.interleaved, i, half, j1, j2);
+        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[j1]) << 16);
+        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[j2]) << 16);
+        const float c = cs_row[i], s = cs_row[half + i];
+        const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
+        const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
+        rot[i] = static_cast<uint16_t>(pack_bf16x2(o1, 0.0f) & 0xFFFFu);
+        rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
+    }
+    __syncwarp();
+    for (int k = lane; k < ndst * nchunk; k += 32) {
+        const int h = k / nchunk, c = k - h * nchunk;
+        *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = *reinterpret_cast<const uint4*>(rot + c * 8);
+    }
+}
+
 // Quantises columns [c0, c1) of one row with the row's amax, by `nthr`
 // threads (this one is `tid`): inv = 127/amax, rint(y*inv) ties to even,
 // clamp +-127, all correctly rounded; the chunk holding column 0 writes the

@@ -1,6 +1,7 @@
 // Row-wise kernels of the prolog.
 //
-// mla_norm_rope_kernel  one warp per token: sums the split-K partials of the
+// mla_norm_rope_kernel  one CTA per token (split-K partials) or one warp per
+//   token (mla_norm_rope_warp_kernel, prefill): sums the split-K partials of the
 //   compression projection in split order (deterministic), rounds each value
 //   to BF16, splits the row into c_q | c_kv | k_pe, applies RMSNorm in FP32
 //   (sum of x^2/L, + eps, sqrt, reciprocal, x * rstd, * gamma, cast to BF16:
@@ -41,85 +42,13 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
     extern __shared__ __align__(16) uint16_t wsm[];
     pdl_wait();
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int t = blockIdx.x * kNormWarpTokens + warp;
     if (t >= p.T) return;  // warp-uniform
-    const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, R = p.R, half = R / 2;
-    uint16_t* crow = wsm + static_cast<size_t>(warp) * (NA + R);
-    uint16_t* rot = crow + NA;
     const int pos = p.positions[t];
-    const bool valid = pos >= 0 && pos < p.max_pos;
-    if (lane == 0 && p.amax) p.amax[t] = 0u;
-    uint16_t* nrow = p.normed + static_cast<size_t>(t) * (Lq + Lkv);
-    uint16_t* cache_row = kv_cache_row(p, t, lane == 0);
-    const int nchunk = R / 8;
-    const int ndst = p.H + (cache_row ? 2 : 1);  // rope-slice destinations (kpe_dst)
-    if (!valid) {
-        if (lane == 0) atomicOr(p.status, kStatusPositionRange);
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int i = lane * 8; i < Lq + Lkv; i += 256) {
-            *reinterpret_cast<uint4*>(nrow + i) = z;
-            if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = z;
-        }
-        for (int k = lane; k < ndst * nchunk; k += 32) {
-            const int h = k / nchunk, c = k - h * nchunk;
-            *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = z;
-        }
-        return;
-    }
-    float ssq_q = 0.0f, ssq_kv = 0.0f;
-    const float* prow = p.partials + static_cast<size_t>(t) * NA;
-    for (int i = lane * 4; i < NA; i += 128) {
-        const float4 a = *reinterpret_cast<const float4*>(prow + i);
-        const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
-        *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
-        const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-        // chunk i / 4 on lane (i / 4) % 32, in increasing order (chunk_ssq)
-        if (i < Lq)
-            ssq_q = __fadd_rn(ssq_q, chunk_ssq(v, p.inv_lq));
-        else if (i < Lq + Lkv)
-            ssq_kv = __fadd_rn(ssq_kv, chunk_ssq(v, p.inv_lkv));
-    }
-    ssq_q = lane_butterfly_sum(ssq_q);
-    ssq_kv = lane_butterfly_sum(ssq_kv);
-    const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
-    const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
-    __syncwarp();
-    for (int i = lane * 8; i < Lq + Lkv; i += 256) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
-        const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma + i);
-        const float rstd = i < Lq ? rstd_q : rstd_kv;
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-        const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xs[e]), rstd), bf16_lo(gs[e]));
-            const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[e]), rstd), bf16_hi(gs[e]));
-            o[e] = pack_bf16x2(y0, y1);
-        }
-        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(nrow + i) = ov;
-        if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
-    }
-    const uint16_t* kp = crow + Lq + Lkv;
-    const float* cs = p.cos_sin + static_cast<size_t>(pos) * R;
-    for (int i = lane; i < half; i += 32) {
-        int j1, j2;
-        kpe_pair(p.interleaved, i, half, j1, j2);
-        const float x1 = __uint_as_float(static_cast<uint32_t>(kp[j1]) << 16);
-        const float x2 = __uint_as_float(static_cast<uint32_t>(kp[j2]) << 16);
-        const float c = cs[i], s = cs[half + i];
-        const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
-        const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
-        rot[i] = static_cast<uint16_t>(pack_bf16x2(o1, 0.0f) & 0xFFFFu);
-        rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
-    }
-    __syncwarp();
-    for (int k = lane; k < ndst * nchunk; k += 32) {
-        const int h = k / nchunk, c = k - h * nchunk;
-        *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = *reinterpret_cast<const uint4*>(rot + c * 8);
-    }
+    norm_token_warp(p, t, pos, p.cos_sin + static_cast<size_t>(pos >= 0 && pos < p.max_pos ? pos : 0) * p.R,
+                    p.gamma, p.partials + static_cast<size_t>(t) * p.NA, 0, 1,
+                    wsm + static_cast<size_t>(warp) * (p.NA + p.R));
 }
 
 // ---------------------------------------------------------------- quant

@@ -34,6 +34,10 @@ ROPE_INTERLEAVED = 2  # rope slices de-interleaved before the rotate-half RoPE
 Q_HEAD_NORM = 4       # per-head RMSNorm (no gamma) of q before its RoPE
 QUANT_PER_HEAD = 8    # one q scale per (token, head) instead of per token
 
+# Variant names (benchmark and tests) -> flag bits; "cache" is the latent
+# KV-cache write of mla_prolog_run_cached, not a flag.
+VARIANTS = {"interleaved": ROPE_INTERLEAVED, "head_norm": Q_HEAD_NORM, "per_head": QUANT_PER_HEAD, "cache": 0}
+
 
 @dataclasses.dataclass(frozen=True)
 class Dims:
@@ -210,7 +214,9 @@ def make_inputs(wl: Workload, dims: Optional[Dims] = None, seed: Optional[int] =
 # ---------------------------------------------------------------------------
 # Algorithmic work counts (inputs read once, outputs written once; GEMM flops).
 
-def algorithmic_bytes(d: Dims) -> int:
+def algorithmic_bytes(d: Dims, cache: bool = False) -> int:
+    """Every input read once + every output written once; with ``cache`` also
+    the slot indices read and the latent cache rows (Lkv + R BF16) written."""
     T = d.T
     b = 2 * T * d.D + 2 * d.n_a * d.D + 2 * (d.q_lora_rank + d.kv_lora_rank)
     b += 2 * d.w_b_elems + 4 * T + 4 * T * d.rope_dim  # positions + gathered cos/sin rows
@@ -219,6 +225,8 @@ def algorithmic_bytes(d: Dims) -> int:
     b += 2 * T * d.rope_dim                               # out_kpe
     if d.quant_q:
         b += T * d.n_q + 4 * T * d.n_scales               # int8 codes + scales
+    if cache:
+        b += 4 * T + 2 * T * (d.kv_lora_rank + d.rope_dim)  # slot_mapping + cache rows
     return b
 
 

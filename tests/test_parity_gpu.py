@@ -192,7 +192,9 @@ def test_fused_decode_kernel_matches_four_kernels(name):
     d = inp.dims
     dins = device_inputs(inp, DEV)
     p = binding.MlaProlog.from_dims(d)
-    assert p.kernel_names()[0] == "mla_compress_kernel", "four kernels are the default"
+    if p.kernel_names()[0] == "mla_compress_norm_kernel":  # the cluster schedule is this size's default
+        p.set_tuning(binding.TUNE_CLUSTER_NORM, 0)
+    assert p.kernel_names()[0] == "mla_compress_kernel"
     p.set_tuning(binding.TUNE_DECODE_FUSED, 1)
     assert p.kernel_names() == ["mla_decode_kernel"]
     a = alloc_outputs(d, DEV)
@@ -208,4 +210,74 @@ def test_fused_decode_kernel_matches_four_kernels(name):
         if x.dtype != torch.float32:
             x, y = x.view(torch.uint8), y.view(torch.uint8)
         assert torch.equal(x, y), k
+    p.close()
+
+
+V2L = wl.WORKLOADS["v2lite_decode"]
+
+
+@pytest.mark.parametrize("T", [1, 17, 64, 100, 128])
+def test_cluster_compression_parity(T):
+    """The compression and the norm in one thread-block cluster (partials
+    summed in distributed shared memory): parity with the oracle at every
+    owner split of the tokens, and the same outputs within the bar as the
+    split-K path."""
+    d = V2L.dims.with_T(T)
+    w = wl.Workload("v2l", d, positions="uniform")
+    inp = wl.make_inputs(w)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    p.set_tuning(binding.TUNE_CLUSTER_NORM, 1)
+    assert p.kernel_names()[0] == "mla_compress_norm_kernel", p.kernel_names()
+    a = alloc_outputs(d, DEV)
+    run_prolog(p, dins, a)
+    assert p.device_status() == 0
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin)
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t, ref[k], k)
+        assert a[k].guards_intact(), k
+    p.set_tuning(binding.TUNE_CLUSTER_NORM, 0)
+    assert p.kernel_names()[0] == "mla_compress_kernel"
+    b = alloc_outputs(d, DEV)
+    run_prolog(p, dins, b)
+    assert p.device_status() == 0
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t, b[k].t.view(torch.int16).cpu().numpy().view(np.uint16), k + " (split-K path)")
+    p.set_tuning(binding.TUNE_CLUSTER_NORM, 1)
+    c = alloc_outputs(d, DEV)
+    run_prolog(p, dins, c)
+    torch.cuda.synchronize()
+    for k in a:  # deterministic
+        assert torch.equal(a[k].t.view(torch.int16), c[k].t.view(torch.int16)), k
+    p.close()
+
+
+def test_cluster_compression_bad_positions():
+    d = V2L.dims.with_T(48)
+    w = wl.Workload("v2l", d, positions="uniform")
+    inp = wl.make_inputs(w)
+    inp.positions[7] = d.max_pos
+    inp.positions[40] = -3
+    dins = device_inputs(inp, DEV)
+    outs = alloc_outputs(d, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    p.set_tuning(binding.TUNE_CLUSTER_NORM, 1)
+    run_prolog(p, dins, outs)
+    assert p.device_status() & binding.STATUS_POSITION_RANGE
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin)
+    assert ref["bad_positions"] == 2
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(outs[k].t, ref[k], k)
+    for t in (7, 40):
+        assert not outs["out_k"].t[t].float().abs().sum().item()
+    p.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_q"])
+def test_cluster_compression_is_the_default_for_tiny_batches(name):
+    p = binding.MlaProlog.from_dims(wl.WORKLOADS[name].dims)
+    assert p.kernel_names()[0] == "mla_compress_norm_kernel"
+    p.close()
+    p = binding.MlaProlog.from_dims(V2L.dims)
+    assert p.kernel_names()[0] == "mla_compress_kernel"  # split-K measured faster at this size
     p.close()

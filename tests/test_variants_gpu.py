@@ -176,7 +176,7 @@ def test_fused_decode_kernel_matches_four_kernels(name, extra):
     inp = wl.make_inputs(w, d)
     dins = device_inputs(inp, DEV)
     p = binding.MlaProlog.from_dims(d)
-    p.set_tuning(binding.TUNE_DECODE_FUSED, 1)
+    p.set_tuning(binding.TUNE_DECODE_FUSED, 1)   # also turns the cluster compression off
     a = alloc_outputs(d, DEV)
     run_prolog(p, dins, a)
     assert p.device_status() == 0
@@ -205,7 +205,7 @@ def _slots(T: int, num_slots: int, seed: int) -> np.ndarray:
     return s
 
 
-def run_cached(d, inp, slots: np.ndarray, num_slots: int, fused: bool = False):
+def run_cached(d, inp, slots: np.ndarray, num_slots: int, fused: bool = False, cluster: bool = False):
     dins = device_inputs(inp, DEV)
     outs = alloc_outputs(d, DEV)
     cache = torch.full((num_slots, d.kv_lora_rank + d.rope_dim), CACHE_SENTINEL, dtype=torch.int16,
@@ -214,6 +214,8 @@ def run_cached(d, inp, slots: np.ndarray, num_slots: int, fused: bool = False):
     p = binding.MlaProlog.from_dims(d)
     if fused:
         p.set_tuning(binding.TUNE_DECODE_FUSED, 1)
+    if cluster:
+        p.set_tuning(binding.TUNE_CLUSTER_NORM, 1)
     p.run_cached(dins["x"], dins["gamma"], dins["W_a"], dins["W_b"], dins["positions"], dins["cos_sin"],
                  outs["out_k"].t, outs["out_v"].t, outs["out_kpe"].t,
                  outs["out_q_int8"].t if "out_q_int8" in outs else None,
@@ -324,3 +326,17 @@ def test_kv_cache_empty_batch_and_bad_arguments():
     assert L.mla_prolog_run_cached(p.handle, *([None] * 11), slots.data_ptr(), cache.data_ptr(), -1, None) == -1
     assert p.device_status() == 0
     p.close()
+
+
+@pytest.mark.parametrize("extra", [0, IL], ids=["rotate_half", "interleaved"])
+def test_kv_cache_write_cluster_compression(extra):
+    """The cache rows written by the cluster kernel's norm groups."""
+    w = wl.WORKLOADS["v2lite_decode"]
+    d = _with_flags(w.dims, extra)
+    inp = wl.make_inputs(w, d)
+    num_slots = 3 * d.T
+    slots = _slots(d.T, num_slots, 13)
+    status, outs, cache, normed = run_cached(d, inp, slots, num_slots, cluster=True)
+    assert status == 0
+    check_cache(d, inp, slots, cache, outs, normed)
+    _compare(d, inp, outs, None)
