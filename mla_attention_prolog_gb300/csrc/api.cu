@@ -87,6 +87,7 @@ struct mla_prolog {
     uint32_t* amax = nullptr;
     int* status = nullptr;
     int* job_table = nullptr;  // balanced expansion job lists (decode)
+    int* compress_table = nullptr;  // balanced compression job lists (prefill)
     int expand_grid = 0;
     // cooperative decode kernel (one launch for the whole pass)
     bool fused_ok = false;     // the dims and the device allow it
@@ -239,31 +240,23 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     std::vector<int> table;
     if (h->decode && njobs_b > sms) {
         const int nq = Lq > 0 ? d.num_heads : 0;
-        std::vector<std::pair<long long, int>> w;  // (-bytes, job) sorted: heaviest first
         const int ntiles = nq + cdiv(h->NKV, h->bn_kv), gn = 16;
+        std::vector<long long> cost;
         for (int j = 0; j < njobs_b; ++j) {
             // the job -> tile order of the kernel (groups of gn tiles, token tiles inside)
             const int g = j / (gn * h->m_tiles), r = j - g * gn * h->m_tiles;
             const int gw = ntiles - g * gn < gn ? ntiles - g * gn : gn;
             const int tile = g * gn + (r - (r / gw) * gw);
-            const long long bytes = tile < nq ? 2LL * (d.nope_dim + R) * Lq : 2LL * h->bn_kv * Lkv;
-            w.push_back({-bytes, j});
+            cost.push_back(tile < nq ? 2LL * (d.nope_dim + R) * Lq : 2LL * h->bn_kv * Lkv);
         }
-        std::sort(w.begin(), w.end());
-        const int G = sms;
-        std::vector<long long> load(G, 0);
-        std::vector<std::vector<int>> lists(G);
-        for (const auto& e : w) {
-            int best = 0;
-            for (int c = 1; c < G; ++c)
-                if (load[c] < load[best]) best = c;
-            load[best] -= e.first;
-            lists[best].push_back(e.second);
-        }
-        table.push_back(0);
-        for (int c = 0; c < G; ++c) table.push_back(table.back() + static_cast<int>(lists[c].size()));
-        for (int c = 0; c < G; ++c) table.insert(table.end(), lists[c].begin(), lists[c].end());
+        lpt_assign(cost, sms, &table);
     }
+    // Prefill compression: jobs of unequal size (ragged token and weight
+    // tiles) longest first, each to the least-loaded CTA.
+    std::vector<int> ctable;
+    const int njobs_a = cdiv(h->NA, h->bn_a) * h->m_tiles * h->splits_a;
+    if (!h->decode && njobs_a > sms)
+        lpt_assign(compress_job_bytes(d.T, h->NA, cdiv(d.D, kBK), h->bn_a, h->splits_a), sms, &ctable);
 
     // Workspace: partials | normed | q | amax | status | job table, each 256-byte aligned.
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
@@ -275,7 +268,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t b_amax = al(T * 4);
     const size_t b_stat = 1024;  // status word, then the cooperative kernel's counters
     const size_t b_tab = al(table.size() * sizeof(int));
-    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab;
+    const size_t b_ctab = al(ctable.size() * sizeof(int));
+    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab + b_ctab;
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
         delete h;
         return cuda_fail(e, "cudaMalloc(workspace)");
@@ -300,6 +294,15 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             cudaFree(h->ws);
             delete h;
             return cuda_fail(e, "cudaMemcpy(job table)");
+        }
+    }
+    if (!ctable.empty()) {
+        h->compress_table = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax + b_stat + b_tab);
+        if ((e = cudaMemcpy(h->compress_table, ctable.data(), ctable.size() * sizeof(int),
+                            cudaMemcpyHostToDevice)) != cudaSuccess) {
+            cudaFree(h->ws);
+            delete h;
+            return cuda_fail(e, "cudaMemcpy(compression job table)");
         }
     }
     const uint64_t Tm = d.T > 0 ? static_cast<uint64_t>(d.T) : 1;
@@ -414,6 +417,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pa.n_gamma = Lq + Lkv;
     pa.status = h->status;
     pa.timeout_ns = h->timeout_ns;
+    pa.job_table = h->compress_table;
 
     NormRopeParams pn{};
     pn.partials = h->partials;

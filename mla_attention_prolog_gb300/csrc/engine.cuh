@@ -508,10 +508,11 @@ struct RoleCounters {
     uint32_t loads = 0, consumed = 0, chain = 0;
 };
 
-// ---- compression phase: jobs j = first, first + stride, ... < njobs ------
+// ---- compression phase: this CTA's jobs (round robin or balanced table) ---
 //
-// Job j = (token tile, weight tile, K split).  Returns false when a wait gave
-// up (the CTA's abort flag is then raised).
+// Job j = (token tile, weight tile, K split).  `first` / `stride` are this
+// CTA's index and the grid size (they also split the L2 warm-up).  Returns
+// false when a wait gave up (the CTA's abort flag is then raised).
 template <int BN_MAX, int STAGES, int CBN>
 __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_x,
                                                const CUtensorMap* tm_wa, const CompressParams& p, RoleCounters& rc,
@@ -531,6 +532,7 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
         nkb = (split + 1) * p.kb_total / p.splits - kb0;
     };
     bool ok = true;
+    const CtaJobs jobs(p.job_table, njobs);
     if (warp == 0 && lane != 0 && p.prefetch_l2) {
         // Warm L2 with the small inputs the norm and expansion read (cos/sin
         // rows of this batch's positions, gamma): when they run, HBM queues
@@ -548,9 +550,9 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
         if (lane == 0) {
             prefetch_tensormap(tm_x);
             prefetch_tensormap(tm_wa);
-            for (int j = first; j < njobs; j += stride) {
+            for (int i = jobs.begin; i < jobs.end; ++i) {
                 int m0, n0, split, kb0, nkb;
-                job_of(j, m0, n0, split, kb0, nkb);
+                job_of(jobs[i], m0, n0, split, kb0, nkb);
                 if (!produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_x, tm_wa, m0, n0, kb0, nkb, p.bn, false,
                                                  p.timeout_ns, [] { return true; })) {
                     raise_abort(sm, p.status);
@@ -562,9 +564,9 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
-            for (int j = first; j < njobs && ok; j += stride) {
+            for (int i = jobs.begin; i < jobs.end && ok; ++i) {
                 int m0, n0, split, kb0, nkb;
-                job_of(j, m0, n0, split, kb0, nkb);
+                job_of(jobs[i], m0, n0, split, kb0, nkb);
                 for (int k = 0; k < nkb && ok; k += group, ++rc.chain)
                     ok = mma_chain<BN_MAX, STAGES>(sm, rc.consumed, rc.chain, nkb - k < group ? nkb - k : group,
                                                    tmem, idesc, p.timeout_ns);
@@ -577,9 +579,9 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
         const int half = ew >> 2;      // column half
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        for (int j = first; j < njobs && ok; j += stride) {
+        for (int i = jobs.begin; i < jobs.end && ok; ++i) {
             int m0, n0, split, kb0, nkb;
-            job_of(j, m0, n0, split, kb0, nkb);
+            job_of(jobs[i], m0, n0, split, kb0, nkb);
             // column pairs in packed f32x2 registers: half the drain instructions
             uint64_t acc[HALF / 2], cmp[HALF / 2];
 #pragma unroll

@@ -6,7 +6,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <utility>
+#include <vector>
 
 namespace mlap {
 
@@ -38,6 +40,7 @@ struct CompressParams {
     int n_gamma;
     int* status;
     uint64_t timeout_ns;
+    const int* job_table;  // balanced per-CTA job lists (null: round robin)
 };
 
 // Per-token reduction of the partials, BF16 cast, RMSNorm of c_q and c_kv,
@@ -264,6 +267,50 @@ struct Schedule {
     int bn_kv;            // expansion kv tile width
 };
 
+// Jobs of unequal cost over G CTAs, longest first, each to the least-loaded
+// CTA.  Returns the CTA loads in `load` and, when `table` is given, the job
+// table the kernels read: G + 1 start offsets, then every CTA's job ids.
+inline long long lpt_assign(const std::vector<long long>& cost, int G, std::vector<int>* table = nullptr) {
+    std::vector<std::pair<long long, int>> w;
+    w.reserve(cost.size());
+    for (size_t j = 0; j < cost.size(); ++j) w.push_back({-cost[j], static_cast<int>(j)});
+    std::sort(w.begin(), w.end());
+    std::vector<long long> load(G, 0);
+    std::vector<std::vector<int>> lists(G);
+    for (const auto& e : w) {
+        int best = 0;
+        for (int c = 1; c < G; ++c)
+            if (load[c] < load[best]) best = c;
+        load[best] -= e.first;
+        lists[best].push_back(e.second);
+    }
+    if (table) {
+        table->clear();
+        table->push_back(0);
+        for (int c = 0; c < G; ++c) table->push_back(table->back() + static_cast<int>(lists[c].size()));
+        for (int c = 0; c < G; ++c) table->insert(table->end(), lists[c].begin(), lists[c].end());
+    }
+    return *std::max_element(load.begin(), load.end());
+}
+
+// Operand bytes of each compression job, in the kernel's job order (token
+// tile, weight tile, K split): its K blocks x (the token rows of x + the
+// weight rows of its tile), 128 bytes per row per K block.
+inline std::vector<long long> compress_job_bytes(int T, int NA, int kb, int bn, int splits) {
+    const int m_tiles = cdiv_host(T, kBM), n_tiles = cdiv_host(NA, bn);
+    std::vector<long long> c;
+    c.reserve(static_cast<size_t>(m_tiles) * n_tiles * splits);
+    for (int m = 0; m < m_tiles; ++m)
+        for (int n = 0; n < n_tiles; ++n)
+            for (int sp = 0; sp < splits; ++sp) {
+                const int nkb = (sp + 1) * kb / splits - sp * kb / splits;
+                const int rows = T - m * kBM < kBM ? T - m * kBM : kBM;
+                const int width = NA - n * bn < bn ? NA - n * bn : bn;
+                c.push_back(static_cast<long long>(nkb) * 128 * (rows + width));
+            }
+    return c;
+}
+
 // T tokens, D model width, Lq / Lkv / R ranks, H heads of Dn + R (q) and
 // Dn + Dv (kv) columns, on a device with `sms` SMs.
 inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int Dn, int Dv, int sms) {
@@ -287,6 +334,18 @@ inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int D
             if (k < 1) k = 1;
             const int ctas = tiles * k <= sms ? tiles * k : 0;
             if (ctas > best) best = ctas, s.bn_a = bn, s.splits_a = k;
+        }
+    } else {
+        // Prefill: the split-K factor (1, 2 or 4) whose busiest CTA, jobs
+        // assigned longest first, finishes first -- its operand bytes at
+        // ~100 GB/s per SM, plus the extra FP32 partials written and read
+        // back by the norm at ~8 TB/s (both rates measured on GB300).
+        double best_us = 0.0;
+        for (int k = 1; k <= 4 && k <= kb_a / 4; k *= 2) {
+            const std::vector<long long> c = compress_job_bytes(T, NA, kb_a, 128, k);
+            const long long busiest = lpt_assign(c, sms);
+            const double us = busiest / 100e3 + (k - 1) * static_cast<double>(T) * NA * 8 / 8e6;
+            if (k == 1 || us < best_us) best_us = us, s.splits_a = k;
         }
     }
     // Accumulation chain length (K blocks) of the compression projection with

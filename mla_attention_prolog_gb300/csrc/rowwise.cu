@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
     if (t >= p.T) return;  // warp-uniform
     const int pos = p.positions[t];
     norm_token_warp(p, t, pos, p.cos_sin + static_cast<size_t>(pos >= 0 && pos < p.max_pos ? pos : 0) * p.R,
-                    p.gamma, p.partials + static_cast<size_t>(t) * p.NA, 0, 1,
+                    p.gamma, p.partials + static_cast<size_t>(t) * p.NA, static_cast<size_t>(p.T) * p.NA, p.splits,
                     wsm + static_cast<size_t>(warp) * (p.NA + p.R));
 }
 
@@ -91,7 +91,9 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
 
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
-    if (p.splits > 1)
+    // split-K partials of a decode batch: a wide CTA per token keeps every
+    // split's load in flight; prefill (many tokens): one warp per token
+    if (p.splits > 1 && p.T <= 2 * kBM)
         return launch_kernel(mla_norm_rope_kernel<512, 16>, dim3(p.T), dim3(512),
                              norm_token_smem_bytes(p.NA, p.R, p.Lq, p.Lkv), st, true, p);
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
