@@ -287,6 +287,15 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            Setting 1 turns MLA_TUNE_DECODE_FUSED off, and
  *                            the reverse. */
 #define MLA_TUNE_CLUSTER_NORM 4
+/*   MLA_TUNE_PAIR_EXPAND     1 (the default for prefill batches with a q
+ *                            path, where it measured faster): the
+ *                            expansion projections run on CTA pairs
+ *                            (tcgen05 cta_group::2, 256-token tiles, each SM
+ *                            streaming half of every weight tile); 0: one CTA
+ *                            per 128-token tile.  INVALID_ARG when 1 is not
+ *                            available (decode batches, or heads wider than
+ *                            256 columns). */
+#define MLA_TUNE_PAIR_EXPAND 6
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

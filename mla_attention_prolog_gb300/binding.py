@@ -39,6 +39,7 @@ TUNE_COMPRESS_GROUP = 1
 TUNE_COMPRESS_COMPENSATED = 2
 TUNE_DECODE_FUSED = 3
 TUNE_CLUSTER_NORM = 4
+TUNE_PAIR_EXPAND = 6
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -62,6 +62,8 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
+const char* const kPairKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
+                                                    "mla_expand_pair_kernel", "mla_quant_kernel"};
 const char* const kClusterKernelNames[3] = {"mla_compress_norm_kernel", "mla_expand_kernel", "mla_quant_kernel"};
 const char* const kFusedKernelName = "mla_decode_kernel";
 
@@ -95,6 +97,10 @@ struct mla_prolog {
     size_t decode_smem = 0;
     unsigned* sync = nullptr;  // its hand-over counters (kSyncWords words)
     uint64_t timeout_ns = 1000000000ull;
+    // prefill expansion on CTA pairs (cta_group::2, 256-token tiles)
+    bool pair_ok = false;
+    bool pair = false;
+    int pair_grid = 0, pair_m_tiles = 0;
     // compression + norm in one thread-block cluster (small decode batches)
     bool cluster_ok = false;   // the dims and the device allow it
     bool cluster = false;      // in use (tunable; on by default where allowed)
@@ -103,6 +109,7 @@ struct mla_prolog {
     GemmShape cluster_shape_b = GemmShape::Narrow;
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wa_c{}, tm_wqb{}, tm_wkvb{};
+    CUtensorMap tm_wqb2{}, tm_wkvb2{};  // half-tile weight boxes of the pair kernel
     const void* last_x = nullptr;
     const void* last_wa = nullptr;
     const void* last_wb = nullptr;
@@ -226,6 +233,20 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
                 break;
             }
             cudaGetLastError();
+        }
+        cudaGetLastError();
+    }
+    // Prefill: the expansion on CTA pairs (half of each weight tile per SM).
+    if (!h->decode && h->bn_kv == 256 && (Lq == 0 || (d.nope_dim + R <= 256 && (d.nope_dim + R) % 16 == 0))) {
+        int active = 0;
+        if (expand_pair_max_active(&active) == cudaSuccess && active >= 1) {
+            h->pair_ok = true;
+            // Measured on GB300: the V3 prefill expansion 1440 vs 1539 us on
+            // pairs; the KV-only V2-Lite prefill 28.0 vs 25.6 us (slower).
+            h->pair = Lq > 0;
+            h->pair_m_tiles = cdiv(d.T, 2 * kBM);
+            const int pjobs = ((Lq > 0 ? d.num_heads : 0) + cdiv(h->NKV, h->bn_kv)) * h->pair_m_tiles;
+            h->pair_grid = pjobs < sms / 2 ? pjobs : sms / 2;
         }
         cudaGetLastError();
     }
@@ -385,6 +406,16 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         } else {
             h->tm_wqb = h->tm_wkvb;
         }
+        if (h->pair_ok) {
+            if (!encode_bf16(&h->tm_wkvb2, wkvb, Lkv, h->NKV, Lkv, h->bn_kv / 2))
+                return cuda_fail(cudaErrorInvalidValue, "tensor map W_kv_b (pairs)");
+            if (Lq > 0) {
+                if (!encode_bf16(&h->tm_wqb2, wb, Lq, h->NQ, Lq, (d.nope_dim + R) / 2))
+                    return cuda_fail(cudaErrorInvalidValue, "tensor map W_q_b (pairs)");
+            } else {
+                h->tm_wqb2 = h->tm_wkvb2;
+            }
+        }
         h->last_wb = W_b;
     }
     const bool timed = h->n_events > 0;
@@ -542,9 +573,17 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
-    if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb, st)) !=
-        cudaSuccess)
+    if (h->pair) {
+        ExpandParams pp = pb;
+        pp.m_tiles = h->pair_m_tiles;
+        pp.job_table = nullptr;
+        if ((e = launch_expand_pair(h->pair_grid, h->tm_nq, h->tm_nkv, h->tm_wqb2, h->tm_wkvb2, pp, st)) !=
+            cudaSuccess)
+            return cuda_fail(e, "launch mla_expand_pair_kernel");
+    } else if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb,
+                                  st)) != cudaSuccess) {
         return cuda_fail(e, "launch mla_expand_kernel");
+    }
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if (pq.rows > 0) {
         if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
@@ -634,7 +673,9 @@ int32_t mla_prolog_kernel_count(mla_prolog_t h) {
 
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
     if (!h || i < 0 || i >= mla_prolog_kernel_count(h)) return "";
-    return h->fused ? kFusedKernelName : h->cluster ? kClusterKernelNames[i] : kKernelNames[i];
+    return h->fused ? kFusedKernelName
+           : h->cluster ? kClusterKernelNames[i]
+           : h->pair ? kPairKernelNames[i] : kKernelNames[i];
 }
 
 int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream) {
@@ -681,6 +722,11 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             h->fused = value == 1;
             if (h->fused) h->cluster = false;
             h->n_events = 0;  // the kernel count changed: re-arm the timing hook
+            return MLA_OK;
+        case MLA_TUNE_PAIR_EXPAND:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->pair_ok) return MLA_ERR_INVALID_ARG;
+            h->pair = value == 1;
             return MLA_OK;
         case MLA_TUNE_CLUSTER_NORM:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;

@@ -27,10 +27,12 @@
 namespace mlap {
 
 
-template <int BN_MAX, int STAGES>
+// CG = 2: a CTA pair (cta_group::2) -- each CTA holds its 128 rows of A and
+// half of the BN_MAX rows of B per stage.
+template <int BN_MAX, int STAGES, int CG = 1>
 struct Layout {
     static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BN_MAX * kBK * 2;
+    static constexpr int B_BYTES = BN_MAX / CG * kBK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int RING = STAGES * STAGE;
     // full[S], empty[S], acc_full[2], acc_empty[2], mma_done
@@ -49,9 +51,9 @@ struct Smem {
     volatile int* abort_flag;
 };
 
-template <int BN_MAX, int STAGES>
+template <int BN_MAX, int STAGES, int CG = 1>
 __device__ __forceinline__ Smem carve(uint8_t* raw_ptr) {
-    using L = Layout<BN_MAX, STAGES>;
+    using L = Layout<BN_MAX, STAGES, CG>;
     const uint32_t raw = smem_u32(raw_ptr);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     Smem s;
@@ -66,10 +68,13 @@ __device__ __forceinline__ Smem carve(uint8_t* raw_ptr) {
     return s;
 }
 
-// Barrier init, TMEM allocation; returns the TMEM base address.
-template <int BN_MAX, int STAGES>
+// Barrier init, TMEM allocation; returns the TMEM base address.  A pair
+// allocates the same columns in both CTAs and leaves through a cluster
+// barrier, so that every barrier of both CTAs exists before either uses it;
+// the even CTA's accumulator-empty barriers count both CTAs' epilogue warps.
+template <int BN_MAX, int STAGES, int CG = 1>
 __device__ __forceinline__ uint32_t gemm_setup(const Smem& sm, int epi_warps) {
-    using L = Layout<BN_MAX, STAGES>;
+    using L = Layout<BN_MAX, STAGES, CG>;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -78,30 +83,42 @@ __device__ __forceinline__ uint32_t gemm_setup(const Smem& sm, int epi_warps) {
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(sm.accf0 + 8 * b, 1);
-            mbar_init(sm.acce0 + 8 * b, epi_warps);
+            mbar_init(sm.acce0 + 8 * b, epi_warps * CG);
         }
         mbar_init(sm.done, 1);
         *sm.abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(sm.tmem_slot), L::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (CG == 2) {
+            tmem_alloc_pair(smem_u32(sm.tmem_slot), L::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(sm.tmem_slot), L::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync_all();
     tc_fence_after();
     return *sm.tmem_slot;
 }
 
-template <int BN_MAX, int STAGES>
+template <int BN_MAX, int STAGES, int CG = 1>
 __device__ __forceinline__ void gemm_teardown(const Smem& sm, uint32_t tmem) {
-    using L = Layout<BN_MAX, STAGES>;
+    using L = Layout<BN_MAX, STAGES, CG>;
     tc_fence_before();
     __syncthreads();
+    // a pair: no CTA frees TMEM or leaves while the other one's epilogue or
+    // the even CTA's MMAs (which read both CTAs' shared memory) still run
+    if constexpr (CG == 2) cluster_sync_all();
     if ((threadIdx.x >> 5) == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, L::TMEM_COLS);
+        if constexpr (CG == 2)
+            tmem_dealloc_pair(tmem, L::TMEM_COLS);
+        else
+            tmem_dealloc(tmem, L::TMEM_COLS);
     }
 }
 
@@ -117,12 +134,33 @@ __device__ __forceinline__ void raise_abort(const Smem& sm, int* status) {
 // same grid) the weight tiles of up to one ring pass are issued as their
 // slots free up, then `dep()` waits for the activations to exist, then the
 // activation tiles of those slots follow.
-template <int BN_MAX, int STAGES, class Dep>
+//
+// A pair (CG = 2): each CTA's producer loads its own halves into its own
+// ring -- A rows a_row + 128 * rank, B rows b_row + bn / 2 * rank -- and the
+// copies of both CTAs complete on the even CTA's full barrier, whose expected
+// byte count (both halves) only the even CTA sets.  Each CTA waits for its
+// slots on its own empty barrier (the MMA commit arrives on both).
+template <int BN_MAX, int STAGES, int CG = 1, class Dep>
 __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, const CUtensorMap* tmA,
                                             const CUtensorMap* tmB, int a_row, int b_row, int kb0, int nkb,
                                             int bn, bool weights_first, uint64_t timeout_ns, Dep&& dep) {
-    using L = Layout<BN_MAX, STAGES>;
-    const uint32_t tx = static_cast<uint32_t>(L::A_BYTES + bn * kBK * 2);
+    using L = Layout<BN_MAX, STAGES, CG>;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int b_rows = bn / CG;
+    const uint32_t tx = static_cast<uint32_t>(CG * (L::A_BYTES + b_rows * kBK * 2));
+    a_row += static_cast<int>(rank) * kBM;
+    b_row += static_cast<int>(rank) * b_rows;
+    auto full_bar = [&](int s) -> uint32_t {
+        if constexpr (CG == 2) return map_shared_rank(sm.full0 + 8 * s, 0);
+        return sm.full0 + 8 * s;
+    };
+    auto load = [&](uint32_t dst, const CUtensorMap* map, int s, int c0, int c1) {
+        if constexpr (CG == 2)
+            tma_load_2d_pair(dst, map, full_bar(s), c0, c1);
+        else
+            tma_load_2d(dst, map, full_bar(s), c0, c1);
+    };
     int i = 0;
     if (weights_first) {
         const int pre = nkb < STAGES ? nkb : STAGES;
@@ -130,15 +168,15 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
             const uint32_t l = loads + k;
             const int s = l % STAGES;
             if (!mbar_wait(sm.empty0 + 8 * s, ((l / STAGES) & 1) ^ 1, timeout_ns, sm.abort_flag)) return false;
-            mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
-            tma_load_2d(sm.base + s * L::STAGE + L::A_BYTES, tmB, sm.full0 + 8 * s, (kb0 + k) * kBK, b_row);
+            if (leader) mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
+            load(sm.base + s * L::STAGE + L::A_BYTES, tmB, s, (kb0 + k) * kBK, b_row);
         }
         // The weight tiles above are in flight: their slots must still be
         // completed (the activation tiles) even when the wait gives up.
         const bool dep_ok = dep();
         for (int k = 0; k < pre; ++k) {
             const int s = (loads + k) % STAGES;
-            tma_load_2d(sm.base + s * L::STAGE, tmA, sm.full0 + 8 * s, (kb0 + k) * kBK, a_row);
+            load(sm.base + s * L::STAGE, tmA, s, (kb0 + k) * kBK, a_row);
         }
         i = pre;
         loads += pre;
@@ -149,9 +187,9 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
         const uint32_t ph = (loads / STAGES) & 1;
         if (!mbar_wait(sm.empty0 + 8 * s, ph ^ 1, timeout_ns, sm.abort_flag)) return false;
         const uint32_t sa = sm.base + s * L::STAGE;
-        mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
-        tma_load_2d(sa, tmA, sm.full0 + 8 * s, (kb0 + i) * kBK, a_row);
-        tma_load_2d(sa + L::A_BYTES, tmB, sm.full0 + 8 * s, (kb0 + i) * kBK, b_row);
+        if (leader) mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
+        load(sa, tmA, s, (kb0 + i) * kBK, a_row);
+        load(sa + L::A_BYTES, tmB, s, (kb0 + i) * kBK, b_row);
     }
     return true;
 }
@@ -164,11 +202,13 @@ __device__ __forceinline__ void drain_loads(const Smem& sm, uint32_t loads, uint
 }
 
 // MMA issuer: one accumulation chain of nkb K blocks into TMEM buffer
-// (chain & 1), after the epilogue released that buffer's previous chain.
-template <int BN_MAX, int STAGES>
+// (chain & 1), after the epilogue released that buffer's previous chain.  A
+// pair's chain is issued by the even CTA (M = 256, idesc to match) and its
+// commits arrive on the barriers of both CTAs.
+template <int BN_MAX, int STAGES, int CG = 1>
 __device__ __forceinline__ bool mma_chain(const Smem& sm, uint32_t& consumed, uint32_t chain, int nkb,
                                           uint32_t tmem, uint32_t idesc, uint64_t timeout_ns) {
-    using L = Layout<BN_MAX, STAGES>;
+    using L = Layout<BN_MAX, STAGES, CG>;
     const uint32_t b = chain & 1;
     if (!mbar_wait(sm.acce0 + 8 * b, ((chain >> 1) & 1) ^ 1, timeout_ns, sm.abort_flag)) return false;
     tc_fence_after();
@@ -182,11 +222,21 @@ __device__ __forceinline__ bool mma_chain(const Smem& sm, uint32_t& consumed, ui
         const uint64_t ad = smem_desc_sw128(sa);
         const uint64_t bd = smem_desc_sw128(sa + L::A_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes of K per instruction
-            mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (i == 0 && kk == 0) ? 0u : 1u);
-        mma_commit(sm.empty0 + 8 * s);
+        for (int kk = 0; kk < kBK / 16; ++kk) {  // +32 bytes of K per instruction
+            if constexpr (CG == 2)
+                mma_bf16_pair(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (i == 0 && kk == 0) ? 0u : 1u);
+            else
+                mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (i == 0 && kk == 0) ? 0u : 1u);
+        }
+        if constexpr (CG == 2)
+            mma_commit_pair(sm.empty0 + 8 * s, 0x3);
+        else
+            mma_commit(sm.empty0 + 8 * s);
     }
-    mma_commit(sm.accf0 + 8 * b);
+    if constexpr (CG == 2)
+        mma_commit_pair(sm.accf0 + 8 * b, 0x3);
+    else
+        mma_commit(sm.accf0 + 8 * b);
     return true;
 }
 
@@ -198,11 +248,18 @@ __device__ __forceinline__ bool epi_acquire(const Smem& sm, uint32_t chain, uint
     return got;
 }
 
-// ... and hand the buffer back to the MMA warp (one arrival per warp).
+// ... and hand the buffer back to the MMA warp (one arrival per warp; a
+// pair's odd CTA arrives on the even CTA's barrier).
+template <int CG = 1>
 __device__ __forceinline__ void epi_release(const Smem& sm, uint32_t chain) {
     tc_fence_before();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(sm.acce0 + 8 * (chain & 1));
+    if ((threadIdx.x & 31) == 0) {
+        if (CG == 2 && cluster_ctarank() != 0)
+            mbar_arrive_cluster(map_shared_rank(sm.acce0 + 8 * (chain & 1), 0));
+        else
+            mbar_arrive(sm.acce0 + 8 * (chain & 1));
+    }
 }
 
 // ------------------------------------------------------- compression (x W_a^T)
@@ -480,23 +537,26 @@ __device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32
     }
 }
 
-// The jobs of this CTA: round robin over [0, njobs), or, when a balanced
+// The jobs of this CTA (of this CTA pair when CG = 2: both CTAs of a pair
+// run the same jobs): round robin over [0, njobs), or, when a balanced
 // table is given, entries [table[c], table[c + 1]) of the id list that
-// follows the gridDim.x + 1 start offsets.
+// follows the units + 1 start offsets.
 struct CtaJobs {
     const int* table;
+    int unit, units;
     int begin, end;
-    __device__ __forceinline__ CtaJobs(const int* t, int njobs) : table(t) {
+    __device__ __forceinline__ CtaJobs(const int* t, int njobs, int cg = 1)
+        : table(t), unit(static_cast<int>(blockIdx.x) / cg), units(static_cast<int>(gridDim.x) / cg) {
         if (t) {
-            begin = t[blockIdx.x];
-            end = t[blockIdx.x + 1];
+            begin = t[unit];
+            end = t[unit + 1];
         } else {
             begin = 0;
-            end = (njobs - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+            end = (njobs - unit + units - 1) / units;
         }
     }
     __device__ __forceinline__ int operator[](int i) const {
-        return table ? table[gridDim.x + 1 + i] : static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+        return table ? table[units + 1 + i] : unit + i * units;
     }
 };
 
@@ -634,13 +694,18 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
 // for them.  With `pdl` the phase opens a programmatic dependent launch and
 // the other roles also wait for the previous kernel right away (the
 // epilogue's amax updates must follow the norm kernel's clearing).
-template <int BN_MAX, int STAGES, class Dep>
+//
+// With CG = 2 the CTA pair runs one 256-token tile per job: token tile m
+// covers rows [256 m, 256 m + 256), this CTA's epilogue rows 128 * rank on.
+template <int BN_MAX, int STAGES, int CG = 1, class Dep>
 __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_aq,
                                              const CUtensorMap* tm_akv, const CUtensorMap* tm_bq,
                                              const CUtensorMap* tm_bkv, const ExpandParams& p, RoleCounters& rc,
                                              const CtaJobs& jobs, bool pdl, Dep&& dep) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Dn = p.Dn, R = p.R;
+    const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+    constexpr int TM = kBM * CG;  // token rows per job
     bool ok = true;
     if (pdl && warp != 0) pdl_wait();
     if (warp == 0) {
@@ -654,25 +719,25 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 expand_job(p, jobs[i], tile, m);
                 const bool first = i == jobs.begin;
                 ok = tile < p.nq_tiles
-                         ? produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_aq, tm_bq, m * kBM, tile * (Dn + R), 0, p.kb_q,
-                                                       Dn + R, first, p.timeout_ns, dep)
-                         : produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_akv, tm_bkv, m * kBM,
-                                                       (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
-                                                       p.timeout_ns, dep);
+                         ? produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_aq, tm_bq, m * TM, tile * (Dn + R), 0,
+                                                           p.kb_q, Dn + R, first, p.timeout_ns, dep)
+                         : produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_akv, tm_bkv, m * TM,
+                                                           (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
+                                                           p.timeout_ns, dep);
             }
             if (pdl && jobs.begin == jobs.end) pdl_wait();
             if (!ok) raise_abort(sm, p.status);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc_q = idesc_bf16_f32(kBM, Dn + R);
-            const uint32_t idesc_kv = idesc_bf16_f32(kBM, p.bn_kv);
+        if (lane == 0 && rank == 0) {  // a pair's MMAs are issued by its even CTA
+            const uint32_t idesc_q = idesc_bf16_f32(TM, Dn + R);
+            const uint32_t idesc_kv = idesc_bf16_f32(TM, p.bn_kv);
             for (int i = jobs.begin; i < jobs.end && ok; ++i, ++rc.chain) {
                 int tile, m;
                 expand_job(p, jobs[i], tile, m);
                 const bool q = tile < p.nq_tiles;
-                ok = mma_chain<BN_MAX, STAGES>(sm, rc.consumed, rc.chain, q ? p.kb_q : p.kb_kv, tmem,
-                                               q ? idesc_q : idesc_kv, p.timeout_ns);
+                ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, q ? p.kb_q : p.kb_kv, tmem,
+                                                   q ? idesc_q : idesc_kv, p.timeout_ns);
             }
             if (!ok) raise_abort(sm, p.status);
         }
@@ -687,7 +752,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             int tile, m;
             expand_job(p, jobs[i], tile, m);
             if (m != cur_m) {  // before waiting for the accumulator
-                load_row_ctx(p, m * kBM + row, ctx);
+                load_row_ctx(p, m * TM + rank * kBM + row, ctx);
                 cur_m = m;
             }
             if (!epi_acquire(sm, rc.chain, p.timeout_ns)) {
@@ -700,7 +765,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 expand_q_epilogue(p, tbase, ctx, tile, half_idx);
             else
                 expand_kv_epilogue(p, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx);
-            epi_release(sm, rc.chain);
+            epi_release<CG>(sm, rc.chain);
         }
     }
     return ok;
@@ -708,16 +773,22 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
 
 // Teardown after the last phase: no TMA copy may still be landing and no MMA
 // may still be running when TMEM is freed and the CTA leaves.
-template <int BN_MAX, int STAGES>
+// A pair: the even CTA's full barriers count both CTAs' copies and its
+// commits cover every MMA, so it alone drains and waits.
+template <int BN_MAX, int STAGES, int CG = 1>
 __device__ __forceinline__ void gemm_finish(const Smem& sm, uint32_t tmem, const RoleCounters& rc,
                                             uint64_t timeout_ns) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == 0 && lane == 0) drain_loads<STAGES>(sm, rc.loads, timeout_ns);
-    if (warp == 1 && lane == 0) {
-        mma_commit(sm.done);
+    const bool leader = CG == 1 || cluster_ctarank() == 0;
+    if (warp == 0 && lane == 0 && leader) drain_loads<STAGES>(sm, rc.loads, timeout_ns);
+    if (warp == 1 && lane == 0 && leader) {
+        if constexpr (CG == 2)
+            mma_commit_pair(sm.done, 0x1);
+        else
+            mma_commit(sm.done);
         mbar_wait(sm.done, 0, timeout_ns, nullptr);
     }
-    gemm_teardown<BN_MAX, STAGES>(sm, tmem);
+    gemm_teardown<BN_MAX, STAGES, CG>(sm, tmem);
 }
 
 }  // namespace mlap

@@ -39,6 +39,30 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
 
+// Prefill expansion on CTA pairs (cta_group::2): each job is a 256-token x
+// BN tile whose MMAs (M = 256) the even CTA issues; each CTA streams its own
+// 128 token rows and half of the weight tile, so an SM receives 16 KB of
+// activations + BN / 2 x 128 bytes of weights per K block instead of
+// 16 KB + BN x 128 bytes for the same tensor-core work.
+template <int BN_MAX, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kExpandThreads, 1)
+    mla_expand_pair_kernel(const __grid_constant__ CUtensorMap tm_aq,
+                           const __grid_constant__ CUtensorMap tm_akv,
+                           const __grid_constant__ CUtensorMap tm_bq,
+                           const __grid_constant__ CUtensorMap tm_bkv, const ExpandParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve<BN_MAX, STAGES, 2>(smem_raw);
+    const uint32_t tmem = gemm_setup<BN_MAX, STAGES, 2>(sm, kExpandEpiWarps);
+    pdl_launch_dependents();
+    RoleCounters rc;
+    const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles, 2);
+    expand_phase<BN_MAX, STAGES, 2>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true, [] {
+        pdl_wait();
+        return true;
+    });
+    gemm_finish<BN_MAX, STAGES, 2>(sm, tmem, rc, p.timeout_ns);
+}
+
 // ------------------------------------------------------------ self-test
 
 // One thread waits on a barrier phase that nothing completes; the bounded
@@ -59,6 +83,7 @@ using EWide = Layout<256, 4>;
 using EMid = Layout<192, 5>;
 using ENarrow = Layout<64, 4>;
 using EDeep = Layout<64, 8>;
+using EPair = Layout<256, 6, 2>;  // per CTA: 16 KB activations + 16 KB weights per stage
 using CWide = Layout<128, 6>;
 using CNarrow = Layout<64, 4>;
 
@@ -87,6 +112,9 @@ cudaError_t gemm_set_attributes() {
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EDeep::BYTES)))
         return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_pair_kernel<256, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  EPair::BYTES)))
+        return e;
     return cudaSuccess;
 }
 
@@ -113,6 +141,21 @@ cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq, const
                              tm_aq, tm_akv, tm_bq, tm_bkv, p);
     return launch_kernel(mla_expand_kernel<64, 4>, dim3(grid), dim3(kExpandThreads), ENarrow::BYTES, st, true,
                          tm_aq, tm_akv, tm_bq, tm_bkv, p);
+}
+
+cudaError_t expand_pair_max_active(int* clusters) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kExpandThreads);
+    cfg.dynamicSmemBytes = EPair::BYTES;
+    return cudaOccupancyMaxActiveClusters(clusters, mla_expand_pair_kernel<256, 6>, &cfg);
+}
+
+cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
+                               const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
+                               cudaStream_t st) {
+    return launch_kernel(mla_expand_pair_kernel<256, 6>, dim3(2 * pairs), dim3(kExpandThreads), EPair::BYTES, st,
+                         true, tm_aq, tm_akv, tm_bq, tm_bkv, p);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {

@@ -398,6 +398,13 @@ cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x,
 cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq,
                           const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
                           const CUtensorMap& tm_bkv, const ExpandParams& p, cudaStream_t st);
+// Prefill expansion on CTA pairs: 256-token tiles, kv tiles of 256 columns,
+// q heads of at most 256 columns; the B tensor maps' boxes are half a tile
+// (bn / 2 rows) and m_tiles counts 256-token tiles.
+cudaError_t expand_pair_max_active(int* clusters);
+cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
+                               const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
+                               cudaStream_t st);
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);

@@ -281,3 +281,50 @@ def test_cluster_compression_is_the_default_for_tiny_batches(name):
     p = binding.MlaProlog.from_dims(V2L.dims)
     assert p.kernel_names()[0] == "mla_compress_kernel"  # split-K measured faster at this size
     p.close()
+
+
+@pytest.mark.parametrize("name,T,extra", [
+    ("v2lite_prefill", 0, 0),
+    ("v2lite_prefill", 300, 0),                                      # the odd CTA of the last pair all out of range
+    ("v3_prefill", 640, 0),
+    ("v3_prefill", 385, wl.ROPE_INTERLEAVED | wl.Q_HEAD_NORM),
+], ids=["v2l_full", "v2l_T300", "v3_T640", "v3_T385_variants"])
+def test_pair_expansion_matches_single_cta(name, T, extra):
+    """Prefill runs the expansion on CTA pairs (tcgen05 cta_group::2, M = 256):
+    parity with the oracle, and the same outputs within the bar as the
+    one-CTA kernel (the accumulation order per output is the same, so they
+    are expected to agree bit for bit)."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    d = dataclasses.replace(d, flags=d.flags | extra)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    assert p.kernel_names()[2] == ("mla_expand_pair_kernel" if d.q_lora_rank else "mla_expand_kernel")
+    p.set_tuning(binding.TUNE_PAIR_EXPAND, 1)
+    assert p.kernel_names()[2] == "mla_expand_pair_kernel", p.kernel_names()
+    a = alloc_outputs(d, DEV)
+    run_prolog(p, dins, a)
+    assert p.device_status() == 0
+    p.set_tuning(binding.TUNE_PAIR_EXPAND, 0)
+    assert p.kernel_names()[2] == "mla_expand_kernel"
+    b = alloc_outputs(d, DEV)
+    run_prolog(p, dins, b)
+    assert p.device_status() == 0
+    torch.cuda.synchronize()
+    tok = np.unique(np.linspace(0, d.T - 1, min(d.T, 96)).astype(np.int32))
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t[sel], ref[k], k)
+        bf16_within(a[k].t, b[k].t.view(torch.int16).cpu().numpy().view(np.uint16), k + " vs one-CTA")
+    if d.q_lora_rank:
+        quant_within(a["out_q_int8"].t[sel], a["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+        quant_within(a["out_q_int8"].t, a["out_scale"].t, b["out_q_int8"].t.cpu().numpy(),
+                     b["out_scale"].t.cpu().numpy())
+    same = all(torch.equal(a[k].t.view(torch.uint8) if a[k].t.dtype != torch.float32 else a[k].t,
+                           b[k].t.view(torch.uint8) if b[k].t.dtype != torch.float32 else b[k].t) for k in a)
+    print(f"pair vs one-CTA outputs bit-identical: {same}")
+    for k, g in a.items():
+        assert g.guards_intact(), k
+    p.close()
