@@ -176,7 +176,9 @@ def kernel_work(d: wl.Dims, cache: bool = False):
         "mla_quant_kernel": 0,
     }
     assert sum(b.values()) == wl.algorithmic_bytes(d, cache)
-    # the expansion on CTA pairs does the expansion's work
+    # the kernels on CTA pairs do the work of their one-CTA counterparts
+    b["mla_compress_pair_kernel"] = b["mla_compress_kernel"]
+    f["mla_compress_pair_kernel"] = f["mla_compress_kernel"]
     b["mla_expand_pair_kernel"] = b["mla_expand_kernel"]
     f["mla_expand_pair_kernel"] = f["mla_expand_kernel"]
     # the cluster kernel runs the compression and the norm step

@@ -296,6 +296,13 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            available (decode batches, or heads wider than
  *                            256 columns). */
 #define MLA_TUNE_PAIR_EXPAND 6
+/*   MLA_TUNE_PAIR_COMPRESS   1: the compression projection runs on CTA pairs
+ *                            (256-token tiles of 128 weight rows, each SM
+ *                            streaming half of every weight tile); 0 (the
+ *                            default, measured faster): one CTA per
+ *                            128-token tile.  INVALID_ARG when 1 is not
+ *                            available (decode batches). */
+#define MLA_TUNE_PAIR_COMPRESS 7
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

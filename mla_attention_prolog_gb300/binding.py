@@ -40,6 +40,7 @@ TUNE_COMPRESS_COMPENSATED = 2
 TUNE_DECODE_FUSED = 3
 TUNE_CLUSTER_NORM = 4
 TUNE_PAIR_EXPAND = 6
+TUNE_PAIR_COMPRESS = 7
 
 
 class MlaPrologDims(ctypes.Structure):

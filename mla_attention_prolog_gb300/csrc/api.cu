@@ -62,8 +62,7 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
-const char* const kPairKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
-                                                    "mla_expand_pair_kernel", "mla_quant_kernel"};
+
 const char* const kClusterKernelNames[3] = {"mla_compress_norm_kernel", "mla_expand_kernel", "mla_quant_kernel"};
 const char* const kFusedKernelName = "mla_decode_kernel";
 
@@ -101,6 +100,11 @@ struct mla_prolog {
     bool pair_ok = false;
     bool pair = false;
     int pair_grid = 0, pair_m_tiles = 0;
+    // prefill compression on CTA pairs
+    bool cpair_ok = false;
+    bool cpair = false;
+    int cpair_grid = 0, cpair_m_tiles = 0, cpair_splits = 1;
+    int* cpair_table = nullptr;
     // compression + norm in one thread-block cluster (small decode batches)
     bool cluster_ok = false;   // the dims and the device allow it
     bool cluster = false;      // in use (tunable; on by default where allowed)
@@ -109,7 +113,7 @@ struct mla_prolog {
     GemmShape cluster_shape_b = GemmShape::Narrow;
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wa_c{}, tm_wqb{}, tm_wkvb{};
-    CUtensorMap tm_wqb2{}, tm_wkvb2{};  // half-tile weight boxes of the pair kernel
+    CUtensorMap tm_wqb2{}, tm_wkvb2{}, tm_wa2{};  // half-tile weight boxes of the pair kernels
     const void* last_x = nullptr;
     const void* last_wa = nullptr;
     const void* last_wb = nullptr;
@@ -250,6 +254,26 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         }
         cudaGetLastError();
     }
+    // Prefill: the compression on CTA pairs (half of each W_a tile per SM).
+    std::vector<int> cptable;
+    if (!h->decode && h->bn_a == 128) {
+        int active = 0;
+        if (compress_pair_max_active(&active) == cudaSuccess && active >= 1) {
+            const int kb = cdiv(d.D, kBK);
+            h->cpair_ok = true;
+            // Measured on GB300: slower on pairs (V3 prefill compression 831
+            // vs 640 us, V2-Lite 34.8 vs 30.3 us): its accumulators drain every
+            // 2-4 K blocks and each drain waits for both CTAs' epilogues.
+            h->cpair = false;
+            h->cpair_splits = prefill_compress_splits(d.T, h->NA, kb, sms, 2);
+            h->cpair_m_tiles = cdiv(d.T, 2 * kBM);
+            const int cjobs = cdiv(h->NA, h->bn_a) * h->cpair_m_tiles * h->cpair_splits;
+            h->cpair_grid = cjobs < sms / 2 ? cjobs : sms / 2;
+            if (cjobs > sms / 2)
+                lpt_assign(compress_job_bytes(d.T, h->NA, kb, h->bn_a, h->cpair_splits, 2), sms / 2, &cptable);
+        }
+        cudaGetLastError();
+    }
     if (h->cluster_ok) {
         h->cluster = h->cplan.est_us <= kClusterDefaultUs;
         h->cluster_expand_grid = njobs_b < sms - h->cluster_ctas ? njobs_b : sms - h->cluster_ctas;
@@ -282,7 +306,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // Workspace: partials | normed | q | amax | status | job table, each 256-byte aligned.
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t T = static_cast<size_t>(d.T);
-    const size_t b_part = al(static_cast<size_t>(h->splits_a) * T * h->NA * 4);
+    const int part_splits = h->cpair_splits > h->splits_a ? h->cpair_splits : h->splits_a;
+    const size_t b_part = al(static_cast<size_t>(part_splits) * T * h->NA * 4);
     const size_t b_norm = al(T * (Lq + Lkv) * 2);
     const bool per_head = (d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;  // no FP32 q round trip
     const size_t b_q = Lq > 0 && !per_head ? al(T * h->NQ * 4) : 0;
@@ -290,7 +315,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t b_stat = 1024;  // status word, then the cooperative kernel's counters
     const size_t b_tab = al(table.size() * sizeof(int));
     const size_t b_ctab = al(ctable.size() * sizeof(int));
-    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab + b_ctab;
+    const size_t b_cptab = al(cptable.size() * sizeof(int));
+    h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab + b_ctab + b_cptab;
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
         delete h;
         return cuda_fail(e, "cudaMalloc(workspace)");
@@ -315,6 +341,15 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             cudaFree(h->ws);
             delete h;
             return cuda_fail(e, "cudaMemcpy(job table)");
+        }
+    }
+    if (!cptable.empty()) {
+        h->cpair_table = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax + b_stat + b_tab + b_ctab);
+        if ((e = cudaMemcpy(h->cpair_table, cptable.data(), cptable.size() * sizeof(int),
+                            cudaMemcpyHostToDevice)) != cudaSuccess) {
+            cudaFree(h->ws);
+            delete h;
+            return cuda_fail(e, "cudaMemcpy(pair compression job table)");
         }
     }
     if (!ctable.empty()) {
@@ -389,6 +424,8 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     if (W_a != h->last_wa) {
         if (!encode_bf16(&h->tm_wa, W_a, d.D, h->NA, d.D, h->bn_a))
             return cuda_fail(cudaErrorInvalidValue, "tensor map W_a");
+        if (h->cpair_ok && !encode_bf16(&h->tm_wa2, W_a, d.D, h->NA, d.D, h->bn_a / 2))
+            return cuda_fail(cudaErrorInvalidValue, "tensor map W_a (pairs)");
         if (h->cluster_ok) {
             const int cgw = h->cplan.cgw;
             if (!encode_bf16(&h->tm_wa_c, W_a, d.D, h->NA, d.D, cgw <= 256 ? cgw : cgw / 2))
@@ -567,9 +604,18 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         return MLA_OK;
     }
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
-    if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
-        cudaSuccess)
+    if (h->cpair) {
+        CompressParams pp = pa;
+        pp.m_tiles = h->cpair_m_tiles;
+        pp.splits = h->cpair_splits;
+        pp.job_table = h->cpair_table;
+        pn.splits = h->cpair_splits;
+        if ((e = launch_compress_pair(h->cpair_grid, h->tm_x, h->tm_wa2, pp, st)) != cudaSuccess)
+            return cuda_fail(e, "launch mla_compress_pair_kernel");
+    } else if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
+               cudaSuccess) {
         return cuda_fail(e, "launch mla_compress_kernel");
+    }
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
@@ -673,9 +719,11 @@ int32_t mla_prolog_kernel_count(mla_prolog_t h) {
 
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
     if (!h || i < 0 || i >= mla_prolog_kernel_count(h)) return "";
-    return h->fused ? kFusedKernelName
-           : h->cluster ? kClusterKernelNames[i]
-           : h->pair ? kPairKernelNames[i] : kKernelNames[i];
+    if (h->fused) return kFusedKernelName;
+    if (h->cluster) return kClusterKernelNames[i];
+    if (i == 0 && h->cpair) return "mla_compress_pair_kernel";
+    if (i == 2 && h->pair) return "mla_expand_pair_kernel";
+    return kKernelNames[i];
 }
 
 int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream) {
@@ -722,6 +770,11 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             h->fused = value == 1;
             if (h->fused) h->cluster = false;
             h->n_events = 0;  // the kernel count changed: re-arm the timing hook
+            return MLA_OK;
+        case MLA_TUNE_PAIR_COMPRESS:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->cpair_ok) return MLA_ERR_INVALID_ARG;
+            h->cpair = value == 1;
             return MLA_OK;
         case MLA_TUNE_PAIR_EXPAND:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;

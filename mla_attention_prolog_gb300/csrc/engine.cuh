@@ -572,12 +572,15 @@ struct RoleCounters {
 //
 // Job j = (token tile, weight tile, K split).  `first` / `stride` are this
 // CTA's index and the grid size (they also split the L2 warm-up).  Returns
-// false when a wait gave up (the CTA's abort flag is then raised).
-template <int BN_MAX, int STAGES, int CBN>
+// false when a wait gave up (the CTA's abort flag is then raised).  With
+// CG = 2 a CTA pair runs each job on a 256-token tile (M = 256, the even CTA
+// issuing the MMAs), each CTA draining its own 128 rows.
+template <int BN_MAX, int STAGES, int CBN, int CG = 1>
 __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_x,
                                                const CUtensorMap* tm_wa, const CompressParams& p, RoleCounters& rc,
                                                int first, int stride) {
     constexpr int HALF = CBN / 2;  // columns per epilogue thread
+    const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_m = p.n_tiles * p.splits;
     const int njobs = p.m_tiles * per_m;
@@ -586,13 +589,13 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
         const int m = j / per_m, r = j - m * per_m;
         const int n = r / p.splits;
         split = r - n * p.splits;
-        m0 = m * kBM;
+        m0 = m * kBM * CG;
         n0 = n * p.bn;
         kb0 = split * p.kb_total / p.splits;
         nkb = (split + 1) * p.kb_total / p.splits - kb0;
     };
     bool ok = true;
-    const CtaJobs jobs(p.job_table, njobs);
+    const CtaJobs jobs(p.job_table, njobs, CG);
     if (warp == 0 && lane != 0 && p.prefetch_l2) {
         // Warm L2 with the small inputs the norm and expansion read (cos/sin
         // rows of this batch's positions, gamma): when they run, HBM queues
@@ -613,7 +616,7 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
             for (int i = jobs.begin; i < jobs.end; ++i) {
                 int m0, n0, split, kb0, nkb;
                 job_of(jobs[i], m0, n0, split, kb0, nkb);
-                if (!produce_job<BN_MAX, STAGES>(sm, rc.loads, tm_x, tm_wa, m0, n0, kb0, nkb, p.bn, false,
+                if (!produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_x, tm_wa, m0, n0, kb0, nkb, p.bn, false,
                                                  p.timeout_ns, [] { return true; })) {
                     raise_abort(sm, p.status);
                     ok = false;
@@ -622,14 +625,14 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kBM, p.bn);
+        if (lane == 0 && rank == 0) {  // a pair's MMAs are issued by its even CTA
+            const uint32_t idesc = idesc_bf16_f32(kBM * CG, p.bn);
             for (int i = jobs.begin; i < jobs.end && ok; ++i) {
                 int m0, n0, split, kb0, nkb;
                 job_of(jobs[i], m0, n0, split, kb0, nkb);
                 for (int k = 0; k < nkb && ok; k += group, ++rc.chain)
-                    ok = mma_chain<BN_MAX, STAGES>(sm, rc.consumed, rc.chain, nkb - k < group ? nkb - k : group,
-                                                   tmem, idesc, p.timeout_ns);
+                    ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, nkb - k < group ? nkb - k : group,
+                                                       tmem, idesc, p.timeout_ns);
             }
             if (!ok) raise_abort(sm, p.status);
         }
@@ -665,10 +668,10 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
                         }
                     }
                 }
-                epi_release(sm, rc.chain);
+                epi_release<CG>(sm, rc.chain);
             }
             if (!ok) break;
-            const int t = m0 + row;
+            const int t = m0 + rank * kBM + row;
             if (t < p.T) {
                 float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
 #pragma unroll

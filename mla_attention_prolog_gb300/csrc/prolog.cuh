@@ -296,19 +296,38 @@ inline long long lpt_assign(const std::vector<long long>& cost, int G, std::vect
 // Operand bytes of each compression job, in the kernel's job order (token
 // tile, weight tile, K split): its K blocks x (the token rows of x + the
 // weight rows of its tile), 128 bytes per row per K block.
-inline std::vector<long long> compress_job_bytes(int T, int NA, int kb, int bn, int splits) {
-    const int m_tiles = cdiv_host(T, kBM), n_tiles = cdiv_host(NA, bn);
+//
+// With CTA pairs (cg = 2) token tiles are 256 rows and the cost is that of the
+// busier CTA of the pair: up to 128 token rows and bn / 2 weight rows.
+inline std::vector<long long> compress_job_bytes(int T, int NA, int kb, int bn, int splits, int cg = 1) {
+    const int tm = kBM * cg;
+    const int m_tiles = cdiv_host(T, tm), n_tiles = cdiv_host(NA, bn);
     std::vector<long long> c;
     c.reserve(static_cast<size_t>(m_tiles) * n_tiles * splits);
     for (int m = 0; m < m_tiles; ++m)
         for (int n = 0; n < n_tiles; ++n)
             for (int sp = 0; sp < splits; ++sp) {
                 const int nkb = (sp + 1) * kb / splits - sp * kb / splits;
-                const int rows = T - m * kBM < kBM ? T - m * kBM : kBM;
+                const int rows = T - m * tm < kBM ? T - m * tm : kBM;
                 const int width = NA - n * bn < bn ? NA - n * bn : bn;
-                c.push_back(static_cast<long long>(nkb) * 128 * (rows + width));
+                c.push_back(static_cast<long long>(nkb) * 128 * (rows + (width + cg - 1) / cg));
             }
     return c;
+}
+
+// Prefill compression: the split-K factor (1, 2 or 4) whose busiest CTA,
+// jobs assigned longest first, finishes first -- its operand bytes at ~100
+// GB/s per SM, plus the extra FP32 partials written and read back by the
+// norm at ~8 TB/s (both rates measured on GB300).  cg = 2: CTA pairs.
+inline int prefill_compress_splits(int T, int NA, int kb, int sms, int cg) {
+    double best_us = 0.0;
+    int best = 1;
+    for (int k = 1; k <= 4 && k <= kb / 4; k *= 2) {
+        const long long busiest = lpt_assign(compress_job_bytes(T, NA, kb, 128, k, cg), sms / cg);
+        const double us = busiest / 100e3 + (k - 1) * static_cast<double>(T) * NA * 8 / 8e6;
+        if (k == 1 || us < best_us) best_us = us, best = k;
+    }
+    return best;
 }
 
 // T tokens, D model width, Lq / Lkv / R ranks, H heads of Dn + R (q) and
@@ -336,17 +355,7 @@ inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int D
             if (ctas > best) best = ctas, s.bn_a = bn, s.splits_a = k;
         }
     } else {
-        // Prefill: the split-K factor (1, 2 or 4) whose busiest CTA, jobs
-        // assigned longest first, finishes first -- its operand bytes at
-        // ~100 GB/s per SM, plus the extra FP32 partials written and read
-        // back by the norm at ~8 TB/s (both rates measured on GB300).
-        double best_us = 0.0;
-        for (int k = 1; k <= 4 && k <= kb_a / 4; k *= 2) {
-            const std::vector<long long> c = compress_job_bytes(T, NA, kb_a, 128, k);
-            const long long busiest = lpt_assign(c, sms);
-            const double us = busiest / 100e3 + (k - 1) * static_cast<double>(T) * NA * 8 / 8e6;
-            if (k == 1 || us < best_us) best_us = us, s.splits_a = k;
-        }
+        s.splits_a = prefill_compress_splits(T, NA, kb_a, sms, 1);
     }
     // Accumulation chain length (K blocks) of the compression projection with
     // TwoSum draining: measured on GB300 to keep INT8 code flips of the
@@ -402,6 +411,11 @@ cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq,
 // q heads of at most 256 columns; the B tensor maps' boxes are half a tile
 // (bn / 2 rows) and m_tiles counts 256-token tiles.
 cudaError_t expand_pair_max_active(int* clusters);
+cudaError_t compress_pair_max_active(int* clusters);
+// Prefill compression on CTA pairs: 256-token tiles of 128 weight rows (the
+// W_a tensor map's box is 64 rows), m_tiles counting 256-token tiles.
+cudaError_t launch_compress_pair(int pairs, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
+                                 const CompressParams& p, cudaStream_t st);
 cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
                                const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
                                cudaStream_t st);

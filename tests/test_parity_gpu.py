@@ -328,3 +328,46 @@ def test_pair_expansion_matches_single_cta(name, T, extra):
     for k, g in a.items():
         assert g.guards_intact(), k
     p.close()
+
+
+@pytest.mark.parametrize("name,T", [("v2lite_prefill", 0), ("v2lite_prefill", 300), ("v3_prefill", 640),
+                                    ("v3_prefill", 257)], ids=["v2l_full", "v2l_T300", "v3_T640", "v3_T257"])
+def test_pair_compression_matches_single_cta(name, T):
+    """The compression on CTA pairs (opt-in; M = 256, the odd CTA of a ragged
+    last tile has no token rows): parity with the oracle, and the
+    outputs within the bar of the one-CTA compression (bit-identical when both
+    use the same split-K factor)."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    assert p.kernel_names()[0] == "mla_compress_kernel"  # one CTA per tile measured faster
+    p.set_tuning(binding.TUNE_PAIR_COMPRESS, 1)
+    assert p.kernel_names()[0] == "mla_compress_pair_kernel", p.kernel_names()
+    a = alloc_outputs(d, DEV)
+    run_prolog(p, dins, a)
+    assert p.device_status() == 0
+    p.set_tuning(binding.TUNE_PAIR_COMPRESS, 0)
+    assert p.kernel_names()[0] == "mla_compress_kernel"
+    b = alloc_outputs(d, DEV)
+    run_prolog(p, dins, b)
+    assert p.device_status() == 0
+    torch.cuda.synchronize()
+    tok = np.unique(np.concatenate([np.linspace(0, d.T - 1, min(d.T, 96)).astype(np.int32), inp.boosted_rows[:8]]))
+    tok = tok.astype(np.int32)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t[sel], ref[k], k)
+        bf16_within(a[k].t, b[k].t.view(torch.int16).cpu().numpy().view(np.uint16), k + " vs one-CTA")
+    if d.q_lora_rank:
+        quant_within(a["out_q_int8"].t[sel], a["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+        quant_within(a["out_q_int8"].t, a["out_scale"].t, b["out_q_int8"].t.cpu().numpy(),
+                     b["out_scale"].t.cpu().numpy())
+    same = all(torch.equal(a[k].t.view(torch.uint8) if a[k].t.dtype != torch.float32 else a[k].t,
+                           b[k].t.view(torch.uint8) if b[k].t.dtype != torch.float32 else b[k].t) for k in a)
+    print(f"pair vs one-CTA compression outputs bit-identical: {same}")
+    for k, g in a.items():
+        assert g.guards_intact(), k
+    p.close()
