@@ -353,8 +353,7 @@ __device__ __forceinline__ void q_rope8(const ExpandParams& p, uint32_t tbase, b
 #pragma unroll
         for (int e = 0; e < 8; ++e) a[e] = v[2 * e], b[e] = v[2 * e + 1];
     } else {
-        tmem_ld8(tbase + Dn + i, a);
-        tmem_ld8(tbase + Dn + half + i, b);
+        tmem_ld8x2(tbase + Dn + i, tbase + Dn + half + i, a, b);
     }
     if (scaled) {
 #pragma unroll
@@ -402,6 +401,14 @@ __device__ __forceinline__ void q_nope16(uint32_t tbase, bool valid, int c, bool
     tmem_ld16(tbase + c, v);
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] = !valid ? 0.0f : scaled ? __fmul_rn(v[e], rstd) : v[e];
+}
+
+// Nope columns [c, c + 32) the same way, under one TMEM wait.
+__device__ __forceinline__ void q_nope32(uint32_t tbase, bool valid, int c, bool scaled, float rstd,
+                                         float (&v)[32]) {
+    tmem_ld32(tbase + c, v);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = !valid ? 0.0f : scaled ? __fmul_rn(v[e], rstd) : v[e];
 }
 
 // Symmetric INT8 code of one value: rint(v * inv) (ties to even), clamped to
@@ -482,7 +489,19 @@ __device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_
     float* qrow = p.qws + static_cast<size_t>(t) * p.NQ + static_cast<size_t>(h) * HD;
     float amax = 0.0f;
     if (half_idx == 0) {
-        for (int c = 0; c < Dn; c += 16) {
+        int c = 0;
+        for (; c + 32 <= Dn; c += 32) {
+            float v[32];
+            q_nope32(tbase, valid, c, scaled, rstd, v);
+            if (in) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+#pragma unroll
+                for (int e = 0; e < 32; e += 8)
+                    st_v8(qrow + c + e, v[e], v[e + 1], v[e + 2], v[e + 3], v[e + 4], v[e + 5], v[e + 6], v[e + 7]);
+            }
+        }
+        for (; c < Dn; c += 16) {
             float v[16];
             q_nope16(tbase, valid, c, scaled, rstd, v);
             if (in) {
@@ -514,9 +533,9 @@ __device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32
     const int Dn = p.Dn, R = p.R, HD = p.Dn + p.Dv;
     const int t = rc.t;
     const int hw = p.bn_kv / 2;
-    for (int c = half_idx * hw; c < (half_idx + 1) * hw; c += 16) {
-        float v[16];
-        tmem_ld16(tbase + c, v);
+    // 16 columns -> BF16 at K's nope slice or V (a 16-column group never
+    // straddles the two: Dn and Dv are multiples of 16)
+    auto store16 = [&](int c, const float* v) {
         const int n = n0 + c;
         if (rc.in && n < p.NKV) {
             const int h = n / HD;
@@ -534,6 +553,19 @@ __device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32
                 d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
         }
+    };
+    const int c1 = (half_idx + 1) * hw;
+    int c = half_idx * hw;
+    for (; c + 32 <= c1; c += 32) {  // two 16-column groups per TMEM wait
+        float v[32];
+        tmem_ld32(tbase + c, v);
+        store16(c, v);
+        store16(c + 16, v + 16);
+    }
+    for (; c < c1; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+        store16(c, v);
     }
 }
 
