@@ -235,7 +235,8 @@ int mla_prolog_selftest_wait_timeout(mla_prolog_t h, uint64_t timeout_ns, void* 
  */
 int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_events);
 
-/* Number of kernels one run launches, and the name of kernel i. */
+/* Number of kernels one run launches (with the current tuning), and the
+ * name of kernel i in launch order. */
 int32_t mla_prolog_kernel_count(mla_prolog_t h);
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i);
 

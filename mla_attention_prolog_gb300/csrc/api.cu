@@ -598,9 +598,10 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
                                h->tm_wkvb, pb, st)) != cudaSuccess)
             return cuda_fail(e, "launch mla_expand_kernel");
         if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
-        if (pq.rows > 0 && (e = launch_quant(pq, st, true)) != cudaSuccess)
-            return cuda_fail(e, "launch mla_quant_kernel");
-        if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        if (pq.rows > 0) {
+            if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
+            if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        }
         return MLA_OK;
     }
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
@@ -633,8 +634,8 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if (pq.rows > 0) {
         if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
+        if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     }
-    if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     return MLA_OK;
 }
 
@@ -713,8 +714,19 @@ int mla_prolog_set_timing_events(mla_prolog_t h, void* const* events, int32_t n_
     return MLA_OK;
 }
 
+namespace {
+// Whether a run launches the per-token quant kernel (no q path and the
+// per-head quant, which runs in the q epilogue, do without it).
+bool quant_kernel_runs(mla_prolog_t h) {
+    const bool per_head = (h->d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;
+    return h->d.q_lora_rank > 0 && !per_head;
+}
+}  // namespace
+
 int32_t mla_prolog_kernel_count(mla_prolog_t h) {
-    return h ? (h->fused ? 1 : h->cluster ? 3 : kKernelCount) : 0;
+    if (!h) return 0;
+    if (h->fused) return 1;
+    return (h->cluster ? 2 : 3) + (quant_kernel_runs(h) ? 1 : 0);
 }
 
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {

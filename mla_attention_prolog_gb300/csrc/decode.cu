@@ -33,8 +33,8 @@
 namespace mlap {
 
 constexpr int kDecodeThreads = kExpandThreads;  // 2 + 8 warps, as the standalone GEMM kernels
-constexpr int kDecodeEpiFirst = 64;             // the epilogue warps: threads [64, 320)
-constexpr int kDecodeEpiThreads = kDecodeThreads - kDecodeEpiFirst;
+constexpr int kDecodeEpiFirst = kEpiFirst;      // the epilogue warps: threads [64, 320)
+constexpr int kDecodeEpiThreads = kEpiThreads;
 constexpr int kDecodeBN = 192;                  // smem ring / TMEM sized for a 192-wide q head
 constexpr int kDecodeStages = 5;
 constexpr int kDecodeCompressBN = 128;          // compression tile width (drain registers)
@@ -43,28 +43,10 @@ constexpr size_t kDecodeNormOff = (DLayout::BYTES + 127) & ~static_cast<size_t>(
 static_assert(kCompressThreads == kDecodeThreads, "compression and expansion roles share the CTA shape");
 static_assert(kDecodeEpiThreads == 32 * kExpandEpiWarps, "the norm runs on the epilogue warps");
 
-// Epilogue-group arrival: every thread's earlier writes are made visible at
-// GPU scope, then one thread adds `n` with release semantics.  Returns the
-// AND of `ok` over the group, so that the group's next steps (and their
-// named barriers) stay uniform even when one warp's wait gave up.
-__device__ __forceinline__ bool epi_arrive(unsigned* counter, unsigned n, bool ok) {
-    __threadfence();
-    const bool all = named_bar_and(1, kDecodeEpiThreads, ok);
-    if (threadIdx.x == kDecodeEpiFirst) red_release_gpu_add(counter, n);
-    return all;
-}
-
-// Epilogue-group wait: one thread waits (bounded), the group follows.
-// Returns, uniformly over the group, whether the count was reached.
+// Epilogue-group wait with the decode kernel's limit and status word.
 __device__ __forceinline__ bool epi_wait(const unsigned* counter, unsigned target, const DecodeParams& p,
                                          const Smem& sm, int* ok_slot) {
-    if (threadIdx.x == kDecodeEpiFirst) {
-        const bool got = wait_counter(counter, target, p.timeout_ns, sm.abort_flag);
-        if (!got) atomicOr(p.status, kStatusWaitTimeout);
-        *ok_slot = got;
-    }
-    named_bar_sync(1, kDecodeEpiThreads);
-    return *ok_slot != 0;
+    return epi_wait(counter, target, p.timeout_ns, p.status, sm.abort_flag, ok_slot);
 }
 
 __global__ void __launch_bounds__(kDecodeThreads, 1)
@@ -112,6 +94,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p.b, rc, jobs, false, [&] {
             const bool got = wait_counter(p.sync + kSyncNormed, normed_target, p.timeout_ns, sm.abort_flag);
             if (!got) atomicOr(p.status, kStatusWaitTimeout);
+            fence_proxy_async_global();  // the normed rows were written with plain stores
             return got;
         });
     ok = ok && c_ok;

@@ -283,6 +283,38 @@ constexpr int kCompressThreads = 64 + 32 * kDrainEpiWarps;
 constexpr int kExpandEpiWarps = 8;  // two warps per TMEM lane quarter, one per column half
 constexpr int kExpandThreads = 64 + 32 * kExpandEpiWarps;
 
+// The epilogue warps as one thread group, threads [kEpiFirst, kExpandThreads),
+// synchronised on named barrier 1 while the producer and MMA warps work on.
+constexpr int kEpiFirst = 64;
+constexpr int kEpiThreads = kExpandThreads - kEpiFirst;
+
+// Epilogue-group arrival on a counter in global memory: the group meets at
+// a named barrier, then one thread adds `n` with release semantics at GPU
+// scope -- a release is cumulative, so it publishes every write the group
+// made before the barrier.  Returns the AND of `ok` over the group, so that
+// the group's next steps (and their named barriers) stay uniform even when
+// one warp's wait gave up.
+__device__ __forceinline__ bool epi_arrive(unsigned* counter, unsigned n, bool ok) {
+    const bool all = named_bar_and(1, kEpiThreads, ok);
+    if (threadIdx.x == kEpiFirst) red_release_gpu_add(counter, n);
+    return all;
+}
+
+// Epilogue-group wait: one thread waits (bounded) until the counter reaches
+// `target` (modulo 2^32), the group follows.  Returns, uniformly over the
+// group, whether the count was reached; a wait that gives up sets
+// kStatusWaitTimeout.  `ok_slot` is one int of shared memory.
+__device__ __forceinline__ bool epi_wait(const unsigned* counter, unsigned target, uint64_t timeout_ns, int* status,
+                                         const volatile int* abort_flag, int* ok_slot) {
+    if (threadIdx.x == kEpiFirst) {
+        const bool got = wait_counter(counter, target, timeout_ns, abort_flag);
+        if (!got) atomicOr(status, kStatusWaitTimeout);
+        *ok_slot = got;
+    }
+    named_bar_sync(1, kEpiThreads);
+    return *ok_slot != 0;
+}
+
 // Job j -> (tile, token tile).  Tiles [0, nq_tiles) are q heads, the rest kv
 // tiles.  Jobs go through the tiles in groups of group_n: all token tiles of
 // a group before the next group, so the weights of a group stay in L2 while

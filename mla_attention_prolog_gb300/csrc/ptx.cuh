@@ -28,6 +28,14 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Orders this thread's view of global memory (generic proxy: plain loads and
+// stores, and what it acquired from other threads) before its later TMA
+// accesses (async proxy) -- needed when a TMA load reads rows that other
+// threads of the same grid wrote with plain stores.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Makes the barrier initialisation visible to the async proxy (TMA, tcgen05).
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
