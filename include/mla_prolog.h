@@ -304,6 +304,15 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            128-token tile.  INVALID_ARG when 1 is not
  *                            available (decode batches). */
 #define MLA_TUNE_PAIR_COMPRESS 7
+/*   MLA_TUNE_TMA_STORE       1 (the default where the dims allow it: nope
+ *                            and value widths multiples of 32, and with the
+ *                            per-token quant a rope width of 32 or 64): the
+ *                            prefill expansion kernels write their kv outputs
+ *                            and FP32 q rows through shared memory with bulk
+ *                            tensor stores; 0: each thread stores its own
+ *                            row.  Same values either way.  INVALID_ARG when
+ *                            1 is not available. */
+#define MLA_TUNE_TMA_STORE 8
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

@@ -41,6 +41,7 @@ TUNE_DECODE_FUSED = 3
 TUNE_CLUSTER_NORM = 4
 TUNE_PAIR_EXPAND = 6
 TUNE_PAIR_COMPRESS = 7
+TUNE_TMA_STORE = 8
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -56,6 +56,21 @@ bool encode_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output tensor [rows, cols] (row pitch `row_bytes`) written by bulk tensor
+// stores in boxes of box_cols x 32 rows of 64 bytes, 64-byte swizzle.
+bool encode_store(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+                  uint64_t row_bytes, uint32_t box_cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_cols, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -114,6 +129,12 @@ struct mla_prolog {
     // tensor maps: workspace ones are fixed, caller ones are re-encoded when a pointer changes
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wa_c{}, tm_wqb{}, tm_wkvb{};
     CUtensorMap tm_wqb2{}, tm_wkvb2{}, tm_wa2{};  // half-tile weight boxes of the pair kernels
+    // the expansion epilogue's bulk tensor stores (kernels with a staging area)
+    bool ts_ok = false;     // the dims allow them
+    bool tma_store = false;  // in use (tunable)
+    OutTensorMaps tm_out{};  // q workspace (fixed), out_k / out_v (re-encoded per pointer)
+    const void* last_out_k = nullptr;
+    const void* last_out_v = nullptr;
     const void* last_x = nullptr;
     const void* last_wa = nullptr;
     const void* last_wb = nullptr;
@@ -365,6 +386,15 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     bool ok = encode_bf16(&h->tm_nkv, h->normed + Lq, Lkv, Tm, Lq + Lkv, kBM);
     if (Lq > 0) ok = ok && encode_bf16(&h->tm_nq, h->normed, Lq, Tm, Lq + Lkv, kBM);
     else h->tm_nq = h->tm_nkv;
+    // Bulk tensor stores in the expansion epilogue: 32-column BF16 groups
+    // that never straddle k_nope / value, and (per-token q path) a rope slice
+    // of 32 or 64 columns in 16-column boxes.
+    h->ts_ok = d.nope_dim % 32 == 0 && d.v_dim % 32 == 0 && h->bn_kv % 64 == 0 &&
+               (Lq == 0 || per_head || (R % 32 == 0 && R <= 64));
+    if (h->ts_ok && h->qws)
+        ok = ok && encode_store(&h->tm_out.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h->qws, h->NQ, Tm,
+                                static_cast<uint64_t>(h->NQ) * 4, 16);
+    h->tma_store = h->ts_ok;
     if (!ok) {
         cudaFree(h->ws);
         delete h;
@@ -454,6 +484,15 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
             }
         }
         h->last_wb = W_b;
+    }
+    if (h->ts_ok && (out_k != h->last_out_k || out_v != h->last_out_v)) {
+        const uint64_t HK = static_cast<uint64_t>(d.num_heads) * (d.nope_dim + R);
+        const uint64_t HV = static_cast<uint64_t>(d.num_heads) * d.v_dim;
+        if (!encode_store(&h->tm_out.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_k, HK, d.T, HK * 2, 32) ||
+            !encode_store(&h->tm_out.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out_v, HV, d.T, HV * 2, 32))
+            return cuda_fail(cudaErrorInvalidValue, "tensor map out_k / out_v");
+        h->last_out_k = out_k;
+        h->last_out_v = out_v;
     }
     const bool timed = h->n_events > 0;
     cudaError_t e;
@@ -549,6 +588,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pb.per_head = per_head;
     pb.q_codes = out_q_int8;
     pb.q_scale = out_scale;
+    pb.tma_store = h->tma_store ? 1 : 0;
 
     // the per-token quant kernel (the per-head quant runs in the q epilogue)
     QuantParams pq{h->qws, h->amax, Lq > 0 && !per_head ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
@@ -595,7 +635,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
             return cuda_fail(e, "launch mla_compress_norm_kernel");
         if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
         if ((e = launch_expand(h->cluster_shape_b, h->cluster_expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb,
-                               h->tm_wkvb, pb, st)) != cudaSuccess)
+                               h->tm_wkvb, h->tm_out, pb, st)) != cudaSuccess)
             return cuda_fail(e, "launch mla_expand_kernel");
         if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
         if (pq.rows > 0) {
@@ -624,10 +664,10 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         ExpandParams pp = pb;
         pp.m_tiles = h->pair_m_tiles;
         pp.job_table = nullptr;
-        if ((e = launch_expand_pair(h->pair_grid, h->tm_nq, h->tm_nkv, h->tm_wqb2, h->tm_wkvb2, pp, st)) !=
+        if ((e = launch_expand_pair(h->pair_grid, h->tm_nq, h->tm_nkv, h->tm_wqb2, h->tm_wkvb2, h->tm_out, pp, st)) !=
             cudaSuccess)
             return cuda_fail(e, "launch mla_expand_pair_kernel");
-    } else if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, pb,
+    } else if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, h->tm_out, pb,
                                   st)) != cudaSuccess) {
         return cuda_fail(e, "launch mla_expand_kernel");
     }
@@ -792,6 +832,11 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->pair_ok) return MLA_ERR_INVALID_ARG;
             h->pair = value == 1;
+            return MLA_OK;
+        case MLA_TUNE_TMA_STORE:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->ts_ok) return MLA_ERR_INVALID_ARG;
+            h->tma_store = value == 1;
             return MLA_OK;
         case MLA_TUNE_CLUSTER_NORM:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;

@@ -42,12 +42,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
         : "memory");
 }
 
-// Generic-proxy writes to shared memory become visible to the async proxy
-// (bulk copies) that reads them afterwards.
-__device__ __forceinline__ void fence_proxy_async_shared() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }

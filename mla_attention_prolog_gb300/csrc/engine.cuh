@@ -28,37 +28,41 @@ namespace mlap {
 
 
 // CG = 2: a CTA pair (cta_group::2) -- each CTA holds its 128 rows of A and
-// half of the BN_MAX rows of B per stage.
-template <int BN_MAX, int STAGES, int CG = 1>
+// half of the BN_MAX rows of B per stage.  EPI_STAGE bytes after the ring
+// (1 KB aligned) stage the expansion epilogue's bulk tensor stores.
+template <int BN_MAX, int STAGES, int CG = 1, int EPI_STAGE = 0>
 struct Layout {
     static constexpr int A_BYTES = kBM * kBK * 2;
     static constexpr int B_BYTES = BN_MAX / CG * kBK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int RING = STAGES * STAGE;
     // full[S], empty[S], acc_full[2], acc_empty[2], mma_done
-    static constexpr int MISC = RING + (2 * STAGES + 5) * 8;
+    static constexpr int MISC = RING + EPI_STAGE + (2 * STAGES + 5) * 8;
     static constexpr int BYTES = MISC + 16 + 1024;  // + slack to align the ring to 1 KB
     static constexpr uint32_t TMEM_COLS =
         2 * BN_MAX <= 32 ? 32 : 2 * BN_MAX <= 64 ? 64 : 2 * BN_MAX <= 128 ? 128 : 2 * BN_MAX <= 256 ? 256 : 512;
     static_assert(STAGE % 1024 == 0, "stages must keep 1 KB alignment for the swizzle atoms");
     static_assert(2 * BN_MAX <= 512, "two accumulators must fit in TMEM");
+    static_assert(EPI_STAGE % 1024 == 0, "the staging area keeps 1 KB alignment");
 };
 
 struct Smem {
-    uint32_t base;  // 1 KB aligned start of the ring
+    uint32_t base;   // 1 KB aligned start of the ring
+    uint32_t stage;  // the epilogue's store staging area (after the ring)
     uint32_t full0, empty0, accf0, acce0, done;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
 };
 
-template <int BN_MAX, int STAGES, int CG = 1>
+template <int BN_MAX, int STAGES, int CG = 1, int EPI_STAGE = 0>
 __device__ __forceinline__ Smem carve(uint8_t* raw_ptr) {
-    using L = Layout<BN_MAX, STAGES, CG>;
+    using L = Layout<BN_MAX, STAGES, CG, EPI_STAGE>;
     const uint32_t raw = smem_u32(raw_ptr);
     const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
     Smem s;
     s.base = raw + pad;
-    s.full0 = s.base + L::RING;
+    s.stage = s.base + L::RING;
+    s.full0 = s.stage + EPI_STAGE;
     s.empty0 = s.full0 + 8 * STAGES;
     s.accf0 = s.empty0 + 8 * STAGES;
     s.acce0 = s.accf0 + 16;
@@ -315,6 +319,62 @@ __device__ __forceinline__ bool epi_wait(const unsigned* counter, unsigned targe
     return *ok_slot != 0;
 }
 
+// ---- epilogue stores through shared memory --------------------------------
+//
+// Each epilogue warp owns two 2 KB slots of the staging area.  A slot holds
+// one box of an output tensor: the warp's 32 token rows x 64 bytes (16 FP32
+// or 32 BF16 columns), row r at byte 64 r with its 16-byte chunk j at chunk
+// j ^ ((r >> 1) & 3) -- the tensor map's 64-byte swizzle, under which the 32
+// lanes' 16-byte writes hit distinct banks eight rows at a time.  Lane 0
+// issues the tensor store of a filled slot; before a slot is filled again it
+// waits until the store issued from it two boxes earlier has read it.  The
+// store writes whole 64-byte row pieces and clips rows past the tensor's end.
+constexpr int kStoreSlotBytes = 32 * 64;
+constexpr int kStoreStageBytes = kExpandEpiWarps * 2 * kStoreSlotBytes;
+
+struct OutMaps {
+    const CUtensorMap* q = nullptr;  // FP32 q workspace [T][NQ], boxes of 16 columns x 32 rows
+    const CUtensorMap* k = nullptr;  // out_k [T][H (Dn + R)] BF16, boxes of 32 x 32
+    const CUtensorMap* v = nullptr;  // out_v [T][H Dv] BF16, boxes of 32 x 32
+};
+
+struct StoreRing {
+    uint32_t slots;  // this warp's two slots
+    uint32_t n;      // boxes issued so far
+};
+
+// One box at (x, y) (elements, rows) from this lane's 16 words of row y + lane.
+// Warp-uniform; a box whose rows all lie past the end (`issue` false) is
+// skipped.
+__device__ __forceinline__ void store_box(StoreRing& sr, const CUtensorMap* map, int x, int y, bool issue,
+                                          const uint32_t (&w)[16]) {
+    if (!issue) return;
+    const int lane = threadIdx.x & 31;
+    const uint32_t slot = sr.slots + (sr.n & 1u) * kStoreSlotBytes;
+    if (lane == 0) bulk_wait_read1();
+    __syncwarp();
+    const uint32_t row = slot + static_cast<uint32_t>(lane) * 64u;
+    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j)
+        st_shared_v4(row + ((j ^ sw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, slot, x, y);
+        bulk_commit();
+    }
+    ++sr.n;
+}
+
+__device__ __forceinline__ void store_box_f32(StoreRing& sr, const CUtensorMap* map, int x, int y, bool issue,
+                                              const float* v) {
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[e]);
+    store_box(sr, map, x, y, issue, w);
+}
+
 // Job j -> (tile, token tile).  Tiles [0, nq_tiles) are q heads, the rest kv
 // tiles.  Jobs go through the tiles in groups of group_n: all token tiles of
 // a group before the next group, so the weights of a group stay in L2 while
@@ -465,23 +525,27 @@ __device__ __forceinline__ uint32_t q_code4(const float* v, float inv) {
 //   per-(token, head) quant: amax of the head row (both warps, whole row),
 //     inv = 127/amax, codes rint(q * inv) clamped to +-127, scale amax/127,
 //     written straight from the epilogue (a zero row gives codes 0, scale 0).
+// The per-head RMSNorm's 1/rms of the whole head row (1 without the norm).
+// Whole warp (TMEM loads).
+__device__ __forceinline__ float q_head_rstd(const ExpandParams& p, uint32_t tbase) {
+    if (!p.head_norm) return 1.0f;
+    float ms = 0.0f;
+    for (int c = 0; c < p.Dn + p.R; c += 16) {
+        float v[16];
+        tmem_ld16(tbase + c, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ms = __fadd_rn(ms, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_hd));
+    }
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
+}
+
 __device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int h,
                                                   int half_idx) {
     const int Dn = p.Dn, R = p.R, HD = Dn + R, half = R / 2;
     const int t = rc.t;
     const bool in = rc.in, valid = rc.valid;
     const bool scaled = p.head_norm != 0;
-    float rstd = 1.0f;
-    if (scaled) {
-        float ms = 0.0f;
-        for (int c = 0; c < HD; c += 16) {
-            float v[16];
-            tmem_ld16(tbase + c, v);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ms = __fadd_rn(ms, __fmul_rn(__fmul_rn(v[e], v[e]), p.inv_hd));
-        }
-        rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, p.eps)));
-    }
+    const float rstd = q_head_rstd(p, tbase);
 
     if (p.per_head) {
         float amax = 0.0f;
@@ -598,6 +662,79 @@ __device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32
         float v[16];
         tmem_ld16(tbase + c, v);
         store16(c, v);
+    }
+}
+
+// The per-token q path through the store ring (R a multiple of 32, at most
+// 64): the same values as expand_q_epilogue, with the columns split evenly --
+// half 0 takes nope columns [0, ns), half 1 nope columns [ns, Dn) and the
+// rope slice, ns = min(Dn, (Dn + R) / 2 rounded down to 16).  y0 is the
+// warp's first token row.
+__device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, const OutMaps& om, StoreRing& sr,
+                                                     uint32_t tbase, const RowCtx& rc, int h, int half_idx, int y0) {
+    const int Dn = p.Dn, R = p.R, HD = Dn + R, half = R / 2;
+    const bool valid = rc.valid, issue = y0 < p.T;
+    const bool scaled = p.head_norm != 0;
+    const float rstd = q_head_rstd(p, tbase);
+    const int ns = (HD / 2) / 16 * 16 < Dn ? (HD / 2) / 16 * 16 : Dn;
+    const int c1 = half_idx ? Dn : ns;
+    const int x0 = h * HD;
+    float amax = 0.0f;
+    int c = half_idx ? ns : 0;
+    for (; c + 32 <= c1; c += 32) {
+        float v[32];
+        q_nope32(tbase, valid, c, scaled, rstd, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        store_box_f32(sr, om.q, x0 + c, y0, issue, v);
+        store_box_f32(sr, om.q, x0 + c + 16, y0, issue, v + 16);
+    }
+    for (; c < c1; c += 16) {
+        float v[16];
+        q_nope16(tbase, valid, c, scaled, rstd, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        store_box_f32(sr, om.q, x0 + c, y0, issue, v);
+    }
+    if (half_idx == 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 16) {
+            if (i < half) {  // warp-uniform
+                float o1[16], o2[16];
+                float a1[8], a2[8], b1[8], b2[8];
+                q_rope8(p, tbase, valid, i, scaled, rstd, rc.c + i, rc.s + i, a1, a2);
+                q_rope8(p, tbase, valid, i + 8, scaled, rstd, rc.c + i + 8, rc.s + i + 8, b1, b2);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o1[e] = a1[e], o1[8 + e] = b1[e], o2[e] = a2[e], o2[8 + e] = b2[e];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
+                store_box_f32(sr, om.q, x0 + Dn + i, y0, issue, o1);
+                store_box_f32(sr, om.q, x0 + Dn + half + i, y0, issue, o2);
+            }
+        }
+    }
+    if (valid) atomicMax(p.amax + rc.t, __float_as_uint(amax));
+}
+
+// The kv tile through the store ring (Dn, Dv multiples of 32, bn_kv a
+// multiple of 64): 32-column groups, each all k_nope or all value.
+__device__ __forceinline__ void expand_kv_epilogue_ts(const ExpandParams& p, const OutMaps& om, StoreRing& sr,
+                                                      uint32_t tbase, const RowCtx& rc, int n0, int half_idx, int y0) {
+    const int Dn = p.Dn, HD = p.Dn + p.Dv, hw = p.bn_kv / 2;
+    const bool issue = y0 < p.T;
+    for (int c = half_idx * hw; c < (half_idx + 1) * hw; c += 32) {
+        const int n = n0 + c;
+        if (n >= p.NKV) break;  // warp-uniform
+        float v[32];
+        tmem_ld32(tbase + c, v);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = rc.valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
+        const int h = n / HD, j = n - h * HD;
+        if (j < Dn)
+            store_box(sr, om.k, h * (Dn + p.R) + j, y0, issue, w);
+        else
+            store_box(sr, om.v, h * p.Dv + (j - Dn), y0, issue, w);
     }
 }
 
@@ -764,11 +901,13 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
 //
 // With CG = 2 the CTA pair runs one 256-token tile per job: token tile m
 // covers rows [256 m, 256 m + 256), this CTA's epilogue rows 128 * rank on.
-template <int BN_MAX, int STAGES, int CG = 1, class Dep>
+// With TS (a kernel with the store staging area) and p.tma_store the kv
+// tiles and the per-token q tiles leave through the store ring.
+template <int BN_MAX, int STAGES, int CG = 1, bool TS = false, class Dep>
 __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_aq,
                                              const CUtensorMap* tm_akv, const CUtensorMap* tm_bq,
                                              const CUtensorMap* tm_bkv, const ExpandParams& p, RoleCounters& rc,
-                                             const CtaJobs& jobs, bool pdl, Dep&& dep) {
+                                             const CtaJobs& jobs, bool pdl, const OutMaps& om, Dep&& dep) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Dn = p.Dn, R = p.R;
     const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -815,6 +954,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         int cur_m = -1;
         RowCtx ctx;
+        StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes, 0u};
         for (int i = jobs.begin; i < jobs.end; ++i, ++rc.chain) {
             int tile, m;
             expand_job(p, jobs[i], tile, m);
@@ -828,12 +968,19 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 break;
             }
             const uint32_t tbase = tmem + lane_off + (rc.chain & 1) * BN_MAX;
-            if (tile < p.nq_tiles)
+            const int y0 = m * TM + rank * kBM + quarter * 32;
+            if (TS && p.tma_store && tile >= p.nq_tiles)
+                expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx, y0);
+            else if (TS && p.tma_store && !p.per_head)
+                expand_q_epilogue_ts(p, om, sr, tbase, ctx, tile, half_idx, y0);
+            else if (tile < p.nq_tiles)
                 expand_q_epilogue(p, tbase, ctx, tile, half_idx);
             else
                 expand_kv_epilogue(p, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx);
             epi_release<CG>(sm, rc.chain);
         }
+        // every tensor store has written its box before the CTA leaves
+        if (TS && lane == 0) bulk_wait_all();
     }
     return ok;
 }

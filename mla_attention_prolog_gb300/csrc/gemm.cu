@@ -20,22 +20,28 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
     gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
 
-template <int BN_MAX, int STAGES>
+// TS: the kernel carries the epilogue's store staging area (the kv tiles and
+// the per-token q tiles leave through bulk tensor stores when p.tma_store).
+template <int BN_MAX, int STAGES, bool TS>
 __global__ void __launch_bounds__(kExpandThreads, 1)
     mla_expand_kernel(const __grid_constant__ CUtensorMap tm_aq,
                       const __grid_constant__ CUtensorMap tm_akv,
                       const __grid_constant__ CUtensorMap tm_bq,
-                      const __grid_constant__ CUtensorMap tm_bkv, const ExpandParams p) {
+                      const __grid_constant__ CUtensorMap tm_bkv,
+                      const __grid_constant__ CUtensorMap tm_oq,
+                      const __grid_constant__ CUtensorMap tm_ok,
+                      const __grid_constant__ CUtensorMap tm_ov, const ExpandParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve<BN_MAX, STAGES>(smem_raw);
+    const Smem sm = carve<BN_MAX, STAGES, 1, TS ? kStoreStageBytes : 0>(smem_raw);
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kExpandEpiWarps);
     pdl_launch_dependents();
     RoleCounters rc;
     const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles);
-    expand_phase<BN_MAX, STAGES>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true, [] {
-        pdl_wait();
-        return true;
-    });
+    expand_phase<BN_MAX, STAGES, 1, TS>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true,
+                                        OutMaps{&tm_oq, &tm_ok, &tm_ov}, [] {
+                                            pdl_wait();
+                                            return true;
+                                        });
     gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
 
@@ -65,17 +71,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kExpandThreads, 1)
     mla_expand_pair_kernel(const __grid_constant__ CUtensorMap tm_aq,
                            const __grid_constant__ CUtensorMap tm_akv,
                            const __grid_constant__ CUtensorMap tm_bq,
-                           const __grid_constant__ CUtensorMap tm_bkv, const ExpandParams p) {
+                           const __grid_constant__ CUtensorMap tm_bkv,
+                           const __grid_constant__ CUtensorMap tm_oq,
+                           const __grid_constant__ CUtensorMap tm_ok,
+                           const __grid_constant__ CUtensorMap tm_ov, const ExpandParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve<BN_MAX, STAGES, 2>(smem_raw);
+    const Smem sm = carve<BN_MAX, STAGES, 2, kStoreStageBytes>(smem_raw);
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES, 2>(sm, kExpandEpiWarps);
     pdl_launch_dependents();
     RoleCounters rc;
     const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles, 2);
-    expand_phase<BN_MAX, STAGES, 2>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true, [] {
-        pdl_wait();
-        return true;
-    });
+    expand_phase<BN_MAX, STAGES, 2, true>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true,
+                                          OutMaps{&tm_oq, &tm_ok, &tm_ov}, [] {
+                                              pdl_wait();
+                                              return true;
+                                          });
     gemm_finish<BN_MAX, STAGES, 2>(sm, tmem, rc, p.timeout_ns);
 }
 
@@ -95,11 +105,11 @@ __global__ void mla_wait_selftest_kernel(int* status, uint64_t timeout_ns) {
 
 // ------------------------------------------------------------ launchers
 
-using EWide = Layout<256, 4>;
+using EWide = Layout<256, 4, 1, kStoreStageBytes>;  // + the epilogue's store staging area
 using EMid = Layout<192, 5>;
 using ENarrow = Layout<64, 4>;
 using EDeep = Layout<64, 8>;
-using EPair = Layout<256, 6, 2>;  // per CTA: 16 KB activations + 16 KB weights per stage
+using EPair = Layout<256, 6, 2, kStoreStageBytes>;  // per CTA: 16 KB activations + 16 KB weights per stage
 using CPair = Layout<128, 8, 2>;  // per CTA: 16 KB activations + 8 KB weights per stage
 using CWide = Layout<128, 6>;
 using CNarrow = Layout<64, 4>;
@@ -117,16 +127,16 @@ cudaError_t gemm_set_attributes() {
     if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   CNarrow::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EWide::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<192, 5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<192, 5, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EMid::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   ENarrow::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_expand_kernel<64, 8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EDeep::BYTES)))
         return e;
     if ((e = cudaFuncSetAttribute(mla_expand_pair_kernel<256, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -148,19 +158,19 @@ cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x, cons
 }
 
 cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
-                          const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
-                          cudaStream_t st) {
+                          const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
+                          const ExpandParams& p, cudaStream_t st) {
     if (s == GemmShape::Wide)
-        return launch_kernel(mla_expand_kernel<256, 4>, dim3(grid), dim3(kExpandThreads), EWide::BYTES, st, true,
-                             tm_aq, tm_akv, tm_bq, tm_bkv, p);
+        return launch_kernel(mla_expand_kernel<256, 4, true>, dim3(grid), dim3(kExpandThreads), EWide::BYTES, st,
+                             true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
     if (s == GemmShape::Mid)
-        return launch_kernel(mla_expand_kernel<192, 5>, dim3(grid), dim3(kExpandThreads), EMid::BYTES, st, true,
-                             tm_aq, tm_akv, tm_bq, tm_bkv, p);
+        return launch_kernel(mla_expand_kernel<192, 5, false>, dim3(grid), dim3(kExpandThreads), EMid::BYTES, st,
+                             true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
     if (s == GemmShape::Deep)
-        return launch_kernel(mla_expand_kernel<64, 8>, dim3(grid), dim3(kExpandThreads), EDeep::BYTES, st, true,
-                             tm_aq, tm_akv, tm_bq, tm_bkv, p);
-    return launch_kernel(mla_expand_kernel<64, 4>, dim3(grid), dim3(kExpandThreads), ENarrow::BYTES, st, true,
-                         tm_aq, tm_akv, tm_bq, tm_bkv, p);
+        return launch_kernel(mla_expand_kernel<64, 8, false>, dim3(grid), dim3(kExpandThreads), EDeep::BYTES, st,
+                             true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
+    return launch_kernel(mla_expand_kernel<64, 4, false>, dim3(grid), dim3(kExpandThreads), ENarrow::BYTES, st,
+                         true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
 }
 
 cudaError_t expand_pair_max_active(int* clusters) {
@@ -186,10 +196,10 @@ cudaError_t launch_compress_pair(int pairs, const CUtensorMap& tm_x, const CUten
 }
 
 cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
-                               const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
-                               cudaStream_t st) {
+                               const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
+                               const ExpandParams& p, cudaStream_t st) {
     return launch_kernel(mla_expand_pair_kernel<256, 6>, dim3(2 * pairs), dim3(kExpandThreads), EPair::BYTES, st,
-                         true, tm_aq, tm_akv, tm_bq, tm_bkv, p);
+                         true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {

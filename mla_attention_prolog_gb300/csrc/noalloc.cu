@@ -248,7 +248,7 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pb.status = dstatus;
     pb.timeout_ns = timeout_ns;
     const int jobs_b = (pb.nq_tiles + pb.nkv_tiles) * m_tiles;
-    if (launch_expand(shape_b, jobs_b < sms ? jobs_b : sms, tm_nq, tm_nkv, tm_wqb, tm_wkvb, pb, st) != cudaSuccess)
+    if (launch_expand(shape_b, jobs_b < sms ? jobs_b : sms, tm_nq, tm_nkv, tm_wqb, tm_wkvb, OutTensorMaps{}, pb, st) != cudaSuccess)
         return set_error("launch mla_expand_kernel");
     if (Lq > 0) {
         QuantParams pq{qws, amax, d.T, NQ, NQ, out_q_int8, out_scale};

@@ -92,6 +92,10 @@ struct ExpandParams {
     int per_head;     // INT8 codes and one scale per (token, head) in the epilogue
     int8_t* q_codes;  // [T][H][Dn + R] (per_head)
     float* q_scale;   // [T][H] (per_head)
+    // Epilogue stores through shared memory and bulk tensor stores (the
+    // kernels built with a staging area; the kv tiles and the per-token q
+    // path): the output tensor maps are kernel parameters.
+    int tma_store;
 };
 
 struct QuantParams {
@@ -404,9 +408,17 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 cudaError_t gemm_set_attributes();
 cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x,
                             const CUtensorMap& tm_wa, const CompressParams& p, cudaStream_t st);
+// The expansion's output tensor maps for its bulk tensor stores (used when
+// ExpandParams::tma_store is set, by the kernels that stage stores): the FP32
+// q workspace in boxes of 16 columns x 32 rows, out_k and out_v in boxes of
+// 32 x 32, all with the 64-byte swizzle.
+struct OutTensorMaps {
+    CUtensorMap q, k, v;
+};
 cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq,
                           const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
-                          const CUtensorMap& tm_bkv, const ExpandParams& p, cudaStream_t st);
+                          const CUtensorMap& tm_bkv, const OutTensorMaps& om, const ExpandParams& p,
+                          cudaStream_t st);
 // Prefill expansion on CTA pairs: 256-token tiles, kv tiles of 256 columns,
 // q heads of at most 256 columns; the B tensor maps' boxes are half a tile
 // (bn / 2 rows) and m_tiles counts 256-token tiles.
@@ -417,8 +429,8 @@ cudaError_t compress_pair_max_active(int* clusters);
 cudaError_t launch_compress_pair(int pairs, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
                                  const CompressParams& p, cudaStream_t st);
 cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
-                               const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const ExpandParams& p,
-                               cudaStream_t st);
+                               const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
+                               const ExpandParams& p, cudaStream_t st);
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);

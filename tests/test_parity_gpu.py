@@ -371,3 +371,54 @@ def test_pair_compression_matches_single_cta(name, T):
     for k, g in a.items():
         assert g.guards_intact(), k
     p.close()
+
+
+@pytest.mark.parametrize("name,T,extra,pair", [
+    ("v2lite_prefill", 0, 0, 0),
+    ("v2lite_prefill", 300, 0, 0),                                    # last tile ragged, one warp's rows all past T
+    ("v3_prefill", 640, 0, 1),
+    ("v3_prefill", 385, wl.ROPE_INTERLEAVED | wl.Q_HEAD_NORM, 1),
+    ("v3_prefill", 300, wl.QUANT_PER_HEAD, 1),                        # kv tiles only through the store ring
+    ("v3_prefill", 385, 0, 0),                                        # one CTA per tile, q and kv tiles
+], ids=["v2l_full", "v2l_T300", "v3_T640", "v3_T385_variants", "v3_T300_per_head", "v3_T385_one_cta"])
+def test_tma_store_matches_thread_stores(name, T, extra, pair):
+    """The expansion epilogue's bulk tensor stores (the default where the dims
+    allow them) write the same bytes as per-thread stores, nothing outside
+    the outputs (guard bands intact), and stay within the bar of the oracle."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    d = dataclasses.replace(d, flags=d.flags | extra)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    if d.q_lora_rank:
+        p.set_tuning(binding.TUNE_PAIR_EXPAND, pair)
+    outs = []
+    for ts in (1, 0):
+        p.set_tuning(binding.TUNE_TMA_STORE, ts)
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    a, b = outs
+    _bits_equal(a, b)
+    tok = np.unique(np.linspace(0, d.T - 1, min(d.T, 64)).astype(np.int32))
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t[sel], ref[k], k)
+    if d.q_lora_rank:
+        quant_within(a["out_q_int8"].t[sel], a["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+    for o in outs:
+        for k, g in o.items():
+            assert g.guards_intact(), k
+    p.close()
+
+
+def _bits_equal(a, b):
+    for k in a:
+        x, y = a[k].t, b[k].t
+        if x.dtype != torch.float32:
+            x, y = x.view(torch.uint8), y.view(torch.uint8)
+        assert torch.equal(x, y), k
