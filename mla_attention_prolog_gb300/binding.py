@@ -42,6 +42,7 @@ TUNE_CLUSTER_NORM = 4
 TUNE_PAIR_EXPAND = 6
 TUNE_PAIR_COMPRESS = 7
 TUNE_TMA_STORE = 8
+TUNE_COMPRESS_TILE = 9
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -75,6 +75,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
+constexpr int kCompressTiles[3] = {128, 192, 256};  // prefill compression weight-tile widths
+constexpr int kPairCompressBN = 128;                // the compression pair kernel's tile width
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
 
@@ -104,6 +106,14 @@ struct mla_prolog {
     int* status = nullptr;
     int* job_table = nullptr;  // balanced expansion job lists (decode)
     int* compress_table = nullptr;  // balanced compression job lists (prefill)
+    // prefill compression: one plan per weight-tile width (128, 192, 256)
+    struct CompressTile {
+        int bn = 0;
+        GemmShape shape = GemmShape::Wide;
+        int splits = 1;
+        int* table = nullptr;
+    };
+    CompressTile ctile[3];
     int expand_grid = 0;
     // cooperative decode kernel (one launch for the whole pass)
     bool fused_ok = false;     // the dims and the device allow it
@@ -143,6 +153,22 @@ struct mla_prolog {
 };
 
 namespace {
+
+// Puts the prefill compression plan of weight-tile width `bn` in use; false
+// when there is none of that width.  The W_a tensor map is re-encoded (its
+// box is one tile high) on the next run.
+bool select_compress_tile(mla_prolog_t h, int bn) {
+    for (const auto& ct : h->ctile) {
+        if (ct.bn != bn || bn == 0) continue;
+        h->bn_a = ct.bn;
+        h->shape_a = ct.shape;
+        h->splits_a = ct.splits;
+        h->compress_table = ct.table;
+        h->last_wa = nullptr;
+        return true;
+    }
+    return false;
+}
 
 int check_dims(const mla_prolog_dims& d) {
     auto m16 = [](int v) { return v > 0 && v % 16 == 0; };
@@ -277,7 +303,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     }
     // Prefill: the compression on CTA pairs (half of each W_a tile per SM).
     std::vector<int> cptable;
-    if (!h->decode && h->bn_a == 128) {
+    if (!h->decode) {
         int active = 0;
         if (compress_pair_max_active(&active) == cudaSuccess && active >= 1) {
             const int kb = cdiv(d.D, kBK);
@@ -288,10 +314,11 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             h->cpair = false;
             h->cpair_splits = prefill_compress_splits(d.T, h->NA, kb, sms, 2);
             h->cpair_m_tiles = cdiv(d.T, 2 * kBM);
-            const int cjobs = cdiv(h->NA, h->bn_a) * h->cpair_m_tiles * h->cpair_splits;
+            const int cjobs = cdiv(h->NA, kPairCompressBN) * h->cpair_m_tiles * h->cpair_splits;
             h->cpair_grid = cjobs < sms / 2 ? cjobs : sms / 2;
             if (cjobs > sms / 2)
-                lpt_assign(compress_job_bytes(d.T, h->NA, kb, h->bn_a, h->cpair_splits, 2), sms / 2, &cptable);
+                lpt_assign(compress_job_bytes(d.T, h->NA, kb, kPairCompressBN, h->cpair_splits, 2), sms / 2,
+                           &cptable);
         }
         cudaGetLastError();
     }
@@ -317,17 +344,39 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         }
         lpt_assign(cost, sms, &table);
     }
-    // Prefill compression: jobs of unequal size (ragged token and weight
-    // tiles) longest first, each to the least-loaded CTA.
-    std::vector<int> ctable;
-    const int njobs_a = cdiv(h->NA, h->bn_a) * h->m_tiles * h->splits_a;
-    if (!h->decode && njobs_a > sms)
-        lpt_assign(compress_job_bytes(d.T, h->NA, cdiv(d.D, kBK), h->bn_a, h->splits_a), sms, &ctable);
+    // Prefill compression, for each weight-tile width: its split-K factor and
+    // its jobs (of unequal size: ragged token and weight tiles) longest
+    // first, each to the least-loaded CTA.
+    std::vector<int> ctable[3];
+    int part_splits = h->cpair_splits > h->splits_a ? h->cpair_splits : h->splits_a;
+    int ctile_default = 128;
+    if (!h->decode) {
+        const int kb = cdiv(d.D, kBK);
+        long long best = -1;
+        for (int i = 0; i < 3; ++i) {
+            auto& ct = h->ctile[i];
+            ct.bn = kCompressTiles[i];
+            ct.shape = ct.bn == 128 ? GemmShape::Wide : ct.bn == 192 ? GemmShape::Wide192 : GemmShape::Wide256;
+            ct.splits = prefill_compress_splits(d.T, h->NA, kb, sms, 1, ct.bn);
+            const auto cost = compress_job_bytes(d.T, h->NA, kb, ct.bn, ct.splits);
+            const long long busiest = lpt_assign(cost, sms, static_cast<int>(cost.size()) > sms ? &ctable[i] : nullptr);
+            if (ct.splits > part_splits) part_splits = ct.splits;
+            // Default: the wide tile (192 or 256) that needs no split-K and
+            // brings its busiest SM the fewest operand bytes, else 128.
+            // Measured on GB300 (step time): V3 prefill 16384 tokens 2441 /
+            // 2245 / 2173 us (128 / 192 / 256), V2-Lite prefill 4096 tokens
+            // 52.3 / 43.5 / 48.1 us (256 needs split-K 2 there), V3 prefill
+            // 385 tokens 109.5 / 127.3 / 120.0 us (the wide ones need split-K 4).
+            if (ct.bn > 128 && ct.splits == 1 && (best < 0 || busiest < best)) {
+                best = busiest;
+                ctile_default = ct.bn;
+            }
+        }
+    }
 
-    // Workspace: partials | normed | q | amax | status | job table, each 256-byte aligned.
+    // Workspace: partials | normed | q | amax | status | job tables, each 256-byte aligned.
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t T = static_cast<size_t>(d.T);
-    const int part_splits = h->cpair_splits > h->splits_a ? h->cpair_splits : h->splits_a;
     const size_t b_part = al(static_cast<size_t>(part_splits) * T * h->NA * 4);
     const size_t b_norm = al(T * (Lq + Lkv) * 2);
     const bool per_head = (d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;  // no FP32 q round trip
@@ -335,7 +384,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t b_amax = al(T * 4);
     const size_t b_stat = 1024;  // status word, then the cooperative kernel's counters
     const size_t b_tab = al(table.size() * sizeof(int));
-    const size_t b_ctab = al(ctable.size() * sizeof(int));
+    const size_t b_ctab = al(ctable[0].size() * sizeof(int)) + al(ctable[1].size() * sizeof(int)) +
+                          al(ctable[2].size() * sizeof(int));
     const size_t b_cptab = al(cptable.size() * sizeof(int));
     h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab + b_ctab + b_cptab;
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
@@ -373,15 +423,19 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             return cuda_fail(e, "cudaMemcpy(pair compression job table)");
         }
     }
-    if (!ctable.empty()) {
-        h->compress_table = reinterpret_cast<int*>(w + b_part + b_norm + b_q + b_amax + b_stat + b_tab);
-        if ((e = cudaMemcpy(h->compress_table, ctable.data(), ctable.size() * sizeof(int),
+    char* ct_base = w + b_part + b_norm + b_q + b_amax + b_stat + b_tab;
+    for (int i = 0; i < 3; ++i) {
+        if (ctable[i].empty()) continue;
+        h->ctile[i].table = reinterpret_cast<int*>(ct_base);
+        ct_base += al(ctable[i].size() * sizeof(int));
+        if ((e = cudaMemcpy(h->ctile[i].table, ctable[i].data(), ctable[i].size() * sizeof(int),
                             cudaMemcpyHostToDevice)) != cudaSuccess) {
             cudaFree(h->ws);
             delete h;
             return cuda_fail(e, "cudaMemcpy(compression job table)");
         }
     }
+    if (!h->decode) select_compress_tile(h, ctile_default);
     const uint64_t Tm = d.T > 0 ? static_cast<uint64_t>(d.T) : 1;
     bool ok = encode_bf16(&h->tm_nkv, h->normed + Lq, Lkv, Tm, Lq + Lkv, kBM);
     if (Lq > 0) ok = ok && encode_bf16(&h->tm_nq, h->normed, Lq, Tm, Lq + Lkv, kBM);
@@ -454,7 +508,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     if (W_a != h->last_wa) {
         if (!encode_bf16(&h->tm_wa, W_a, d.D, h->NA, d.D, h->bn_a))
             return cuda_fail(cudaErrorInvalidValue, "tensor map W_a");
-        if (h->cpair_ok && !encode_bf16(&h->tm_wa2, W_a, d.D, h->NA, d.D, h->bn_a / 2))
+        if (h->cpair_ok && !encode_bf16(&h->tm_wa2, W_a, d.D, h->NA, d.D, kPairCompressBN / 2))
             return cuda_fail(cudaErrorInvalidValue, "tensor map W_a (pairs)");
         if (h->cluster_ok) {
             const int cgw = h->cplan.cgw;
@@ -647,6 +701,8 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
     if (h->cpair) {
         CompressParams pp = pa;
+        pp.bn = kPairCompressBN;
+        pp.n_tiles = cdiv(h->NA, kPairCompressBN);
         pp.m_tiles = h->cpair_m_tiles;
         pp.splits = h->cpair_splits;
         pp.job_table = h->cpair_table;
@@ -833,6 +889,9 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value == 1 && !h->pair_ok) return MLA_ERR_INVALID_ARG;
             h->pair = value == 1;
             return MLA_OK;
+        case MLA_TUNE_COMPRESS_TILE:
+            if (h->decode || h->cluster || h->fused) return MLA_ERR_INVALID_ARG;
+            return select_compress_tile(h, value) ? MLA_OK : MLA_ERR_INVALID_ARG;
         case MLA_TUNE_TMA_STORE:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->ts_ok) return MLA_ERR_INVALID_ARG;

@@ -775,8 +775,11 @@ struct RoleCounters {
 // CTA's index and the grid size (they also split the L2 warm-up).  Returns
 // false when a wait gave up (the CTA's abort flag is then raised).  With
 // CG = 2 a CTA pair runs each job on a 256-token tile (M = 256, the even CTA
-// issuing the MMAs), each CTA draining its own 128 rows.
-template <int BN_MAX, int STAGES, int CBN, int CG = 1>
+// issuing the MMAs), each CTA draining its own 128 rows.  COMP = false drops
+// the TwoSum compensation registers (the drained chains are summed with plain
+// FP32 adds whatever p.compensated says), which leaves room for 256 columns
+// per tile.
+template <int BN_MAX, int STAGES, int CBN, int CG = 1, bool COMP = true>
 __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_x,
                                                const CUtensorMap* tm_wa, const CompressParams& p, RoleCounters& rc,
                                                int first, int stride) {
@@ -847,25 +850,44 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
             int m0, n0, split, kb0, nkb;
             job_of(jobs[i], m0, n0, split, kb0, nkb);
             // column pairs in packed f32x2 registers: half the drain instructions
-            uint64_t acc[HALF / 2], cmp[HALF / 2];
+            constexpr int NC = COMP ? HALF / 2 : 1;
+            uint64_t acc[HALF / 2], cmp[NC];
 #pragma unroll
-            for (int c = 0; c < HALF / 2; ++c) acc[c] = cmp[c] = 0ull;
+            for (int c = 0; c < HALF / 2; ++c) acc[c] = 0ull;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) cmp[c] = 0ull;
+            const bool comp = COMP && p.compensated;
+            constexpr bool LD32 = !COMP && HALF < 128;  // (no spills at 168 registers)
+            // 16 drained columns into the sums
+            auto drain16 = [&](int c, const float* v) {
+                if (comp) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2)
+                        two_sum_add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0], pk2(v[e], v[e + 1]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) acc[(c + e) / 2] = add2(acc[(c + e) / 2], pk2(v[e], v[e + 1]));
+                }
+            };
             for (int k = 0; k < nkb; k += group, ++rc.chain) {
                 if (!epi_acquire(sm, rc.chain, p.timeout_ns)) { ok = false; break; }
                 const uint32_t src = tmem + lane_off + (rc.chain & 1) * BN_MAX + half * HALF;
 #pragma unroll
-                for (int c = 0; c < HALF; c += 16) {
-                    if (half * HALF + c < p.bn) {  // warp-uniform
-                        float v[16];
-                        tmem_ld16(src + c, v);
-                        if (p.compensated) {
+                for (int c = 0; c < HALF; c += 32) {
+                    // warp-uniform: 32 columns under one wait where the registers allow
+                    if (LD32 && c + 32 <= HALF && half * HALF + c + 32 <= p.bn) {
+                        float v[32];
+                        tmem_ld32(src + c, v);
+                        drain16(c, v);
+                        drain16(c + 16, v + 16);
+                    } else {
 #pragma unroll
-                            for (int e = 0; e < 16; e += 2)
-                                two_sum_add2(acc[(c + e) / 2], cmp[(c + e) / 2], pk2(v[e], v[e + 1]));
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2)
-                                acc[(c + e) / 2] = add2(acc[(c + e) / 2], pk2(v[e], v[e + 1]));
+                        for (int c2 = c; c2 < c + 32 && c2 < HALF; c2 += 16) {
+                            if (half * HALF + c2 < p.bn) {
+                                float v[16];
+                                tmem_ld16(src + c2, v);
+                                drain16(c2, v);
+                            }
                         }
                     }
                 }
@@ -880,7 +902,9 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
                     if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA) {
                         float o[8];
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) upk2(add2(acc[(c + e) / 2], cmp[(c + e) / 2]), o[e], o[e + 1]);
+                        for (int e = 0; e < 8; e += 2)
+                            upk2(COMP ? add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0]) : acc[(c + e) / 2], o[e],
+                                 o[e + 1]);
                         st_v8(dst + c, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
                     }
                 }

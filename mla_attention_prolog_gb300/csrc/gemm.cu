@@ -7,7 +7,9 @@
 
 namespace mlap {
 
-template <int BN_MAX, int STAGES>
+// COMP: the drained chains may be summed with TwoSum (p.compensated); the
+// wide tiles sum them with plain FP32 adds.
+template <int BN_MAX, int STAGES, bool COMP>
 __global__ void __launch_bounds__(kCompressThreads, 1)
     mla_compress_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const __grid_constant__ CUtensorMap tm_wa, const CompressParams p) {
@@ -16,7 +18,7 @@ __global__ void __launch_bounds__(kCompressThreads, 1)
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kDrainEpiWarps);
     pdl_launch_dependents();
     RoleCounters rc;
-    compress_phase<BN_MAX, STAGES, BN_MAX>(sm, tmem, &tm_x, &tm_wa, p, rc, blockIdx.x, gridDim.x);
+    compress_phase<BN_MAX, STAGES, BN_MAX, 1, COMP>(sm, tmem, &tm_x, &tm_wa, p, rc, blockIdx.x, gridDim.x);
     gemm_finish<BN_MAX, STAGES>(sm, tmem, rc, p.timeout_ns);
 }
 
@@ -113,6 +115,8 @@ using EPair = Layout<256, 6, 2, kStoreStageBytes>;  // per CTA: 16 KB activation
 using CPair = Layout<128, 8, 2>;  // per CTA: 16 KB activations + 8 KB weights per stage
 using CWide = Layout<128, 6>;
 using CNarrow = Layout<64, 4>;
+using C192 = Layout<192, 5>;  // 16 KB activations + 24 KB weights per stage
+using C256 = Layout<256, 4>;  // 16 KB activations + 32 KB weights per stage
 
 int gemm_smem_bytes(GemmShape s) {
     return s == GemmShape::Wide ? EWide::BYTES : s == GemmShape::Mid ? EMid::BYTES
@@ -121,11 +125,17 @@ int gemm_smem_bytes(GemmShape s) {
 
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   CWide::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<64, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   CNarrow::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<192, 5, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  C192::BYTES)))
+        return e;
+    if ((e = cudaFuncSetAttribute(mla_compress_kernel<256, 4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  C256::BYTES)))
         return e;
     if ((e = cudaFuncSetAttribute(mla_expand_kernel<256, 4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EWide::BYTES)))
@@ -151,10 +161,16 @@ cudaError_t gemm_set_attributes() {
 cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
                             const CompressParams& p, cudaStream_t st) {
     if (s == GemmShape::Wide)
-        return launch_kernel(mla_compress_kernel<128, 6>, dim3(grid), dim3(kCompressThreads), CWide::BYTES, st,
+        return launch_kernel(mla_compress_kernel<128, 6, true>, dim3(grid), dim3(kCompressThreads), CWide::BYTES, st,
                              false, tm_x, tm_wa, p);
-    return launch_kernel(mla_compress_kernel<64, 4>, dim3(grid), dim3(kCompressThreads), CNarrow::BYTES, st, false,
-                         tm_x, tm_wa, p);
+    if (s == GemmShape::Wide192)
+        return launch_kernel(mla_compress_kernel<192, 5, false>, dim3(grid), dim3(kCompressThreads), C192::BYTES, st,
+                             false, tm_x, tm_wa, p);
+    if (s == GemmShape::Wide256)
+        return launch_kernel(mla_compress_kernel<256, 4, false>, dim3(grid), dim3(kCompressThreads), C256::BYTES, st,
+                             false, tm_x, tm_wa, p);
+    return launch_kernel(mla_compress_kernel<64, 4, true>, dim3(grid), dim3(kCompressThreads), CNarrow::BYTES, st,
+                         false, tm_x, tm_wa, p);
 }
 
 cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,

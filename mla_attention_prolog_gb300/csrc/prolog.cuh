@@ -258,7 +258,9 @@ constexpr int kDecodeMaxBN = 192;  // widest expansion tile the decode kernel ta
 // The narrow (decode) shapes use half the shared memory so that a compression
 // CTA and an expansion CTA fit on one SM and the expansion can start
 // streaming its weights while the compression is still running.
-enum class GemmShape { Wide, Mid, Narrow, Deep };
+// Kernel shapes: Wide / Mid / Narrow / Deep for both projections; Wide192 and
+// Wide256 are the compression's 192- and 256-column tiles (plain FP32 drain).
+enum class GemmShape { Wide, Mid, Narrow, Deep, Wide192, Wide256 };
 
 // Tile shapes and work split of one problem size, chosen on the host.
 struct Schedule {
@@ -322,12 +324,13 @@ inline std::vector<long long> compress_job_bytes(int T, int NA, int kb, int bn, 
 // Prefill compression: the split-K factor (1, 2 or 4) whose busiest CTA,
 // jobs assigned longest first, finishes first -- its operand bytes at ~100
 // GB/s per SM, plus the extra FP32 partials written and read back by the
-// norm at ~8 TB/s (both rates measured on GB300).  cg = 2: CTA pairs.
-inline int prefill_compress_splits(int T, int NA, int kb, int sms, int cg) {
+// norm at ~8 TB/s (both rates measured on GB300).  cg = 2: CTA pairs; bn:
+// the weight-tile width.
+inline int prefill_compress_splits(int T, int NA, int kb, int sms, int cg, int bn = 128) {
     double best_us = 0.0;
     int best = 1;
     for (int k = 1; k <= 4 && k <= kb / 4; k *= 2) {
-        const long long busiest = lpt_assign(compress_job_bytes(T, NA, kb, 128, k, cg), sms / cg);
+        const long long busiest = lpt_assign(compress_job_bytes(T, NA, kb, bn, k, cg), sms / cg);
         const double us = busiest / 100e3 + (k - 1) * static_cast<double>(T) * NA * 8 / 8e6;
         if (k == 1 || us < best_us) best_us = us, best = k;
     }

@@ -422,3 +422,36 @@ def _bits_equal(a, b):
         if x.dtype != torch.float32:
             x, y = x.view(torch.uint8), y.view(torch.uint8)
         assert torch.equal(x, y), k
+
+
+@pytest.mark.parametrize("name,T", [("v2lite_prefill", 0), ("v2lite_prefill", 300), ("v3_prefill", 640),
+                                    ("v3_prefill", 385)], ids=["v2l_full", "v2l_T300", "v3_T640", "v3_T385"])
+def test_compression_tile_widths(name, T):
+    """Every compression tile width (128 with TwoSum draining; 192 and 256 with
+    plain FP32 draining, ragged last weight tile at 256) within the bar of the
+    oracle, with the guard bands intact."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    tok = np.unique(np.concatenate([np.linspace(0, d.T - 1, min(d.T, 64)).astype(np.int32), inp.boosted_rows[:8]]))
+    tok = tok.astype(np.int32)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    for tile in (128, 192, 256):
+        p.set_tuning(binding.TUNE_COMPRESS_TILE, tile)
+        assert p.schedule()["bn_a"] == tile
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        torch.cuda.synchronize()
+        for k in ("out_k", "out_v", "out_kpe"):
+            bf16_within(o[k].t[sel], ref[k], f"{k} (tile {tile})")
+        if d.q_lora_rank:
+            quant_within(o["out_q_int8"].t[sel], o["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+        for k, g in o.items():
+            assert g.guards_intact(), k
+    with pytest.raises(binding.MlaPrologError):
+        p.set_tuning(binding.TUNE_COMPRESS_TILE, 160)
+    p.close()
