@@ -325,9 +325,10 @@ __device__ __forceinline__ bool epi_wait(const unsigned* counter, unsigned targe
 // one box of an output tensor: the warp's 32 token rows x 64 bytes (16 FP32
 // or 32 BF16 columns), row r at byte 64 r with its 16-byte chunk j at chunk
 // j ^ ((r >> 1) & 3) -- the tensor map's 64-byte swizzle, under which the 32
-// lanes' 16-byte writes hit distinct banks eight rows at a time.  Lane 0
-// issues the tensor store of a filled slot; before a slot is filled again it
-// waits until the store issued from it two boxes earlier has read it.  The
+// lanes' 16-byte writes hit distinct banks eight rows at a time.  The warp
+// fills both slots, makes them visible to the async proxy with one fence,
+// and lane 0 issues the two tensor stores as one bulk group; before the
+// slots are filled again lane 0 waits until that group has read them.  The
 // store writes whole 64-byte row pieces and clips rows past the tensor's end.
 constexpr int kStoreSlotBytes = 32 * 64;
 constexpr int kStoreStageBytes = kExpandEpiWarps * 2 * kStoreSlotBytes;
@@ -340,39 +341,46 @@ struct OutMaps {
 
 struct StoreRing {
     uint32_t slots;  // this warp's two slots
-    uint32_t n;      // boxes issued so far
 };
 
-// One box at (x, y) (elements, rows) from this lane's 16 words of row y + lane.
-// Warp-uniform; a box whose rows all lie past the end (`issue` false) is
-// skipped.
-__device__ __forceinline__ void store_box(StoreRing& sr, const CUtensorMap* map, int x, int y, bool issue,
-                                          const uint32_t (&w)[16]) {
-    if (!issue) return;
-    const int lane = threadIdx.x & 31;
-    const uint32_t slot = sr.slots + (sr.n & 1u) * kStoreSlotBytes;
-    if (lane == 0) bulk_wait_read1();
-    __syncwarp();
-    const uint32_t row = slot + static_cast<uint32_t>(lane) * 64u;
-    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+// This lane's 16 words of one box row into slot `slot`.
+__device__ __forceinline__ void stage_row(uint32_t slot, const uint32_t* w) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t row = slot + lane * 64u;
+    const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
     for (uint32_t j = 0; j < 4; ++j)
         st_shared_v4(row + ((j ^ sw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+// Boxes (m0, x0, y) and, when m1 is not null, (m1, x1, y) -- elements, rows
+// -- from this lane's words w0 / w1 of row y + lane.  Warp-uniform; boxes
+// whose rows all lie past the end (`issue` false) are skipped.
+__device__ __forceinline__ void store_boxes(const StoreRing& sr, const CUtensorMap* m0, int x0,
+                                            const CUtensorMap* m1, int x1, int y, bool issue, const uint32_t* w0,
+                                            const uint32_t* w1) {
+    if (!issue) return;
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) bulk_wait_read0();
+    __syncwarp();
+    stage_row(sr.slots, w0);
+    if (m1) stage_row(sr.slots + kStoreSlotBytes, w1);
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-        tma_store_2d(map, slot, x, y);
+        tma_store_2d(m0, sr.slots, x0, y);
+        if (m1) tma_store_2d(m1, sr.slots + kStoreSlotBytes, x1, y);
         bulk_commit();
     }
-    ++sr.n;
 }
 
-__device__ __forceinline__ void store_box_f32(StoreRing& sr, const CUtensorMap* map, int x, int y, bool issue,
-                                              const float* v) {
-    uint32_t w[16];
+// FP32 values: 16 per box.
+__device__ __forceinline__ void store_boxes_f32(const StoreRing& sr, const CUtensorMap* map, int x0, int x1,
+                                                bool two, int y, bool issue, const float* v0, const float* v1) {
+    uint32_t w0[16], w1[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[e]);
-    store_box(sr, map, x, y, issue, w);
+    for (int e = 0; e < 16; ++e) w0[e] = __float_as_uint(v0[e]), w1[e] = __float_as_uint(v1[e]);
+    store_boxes(sr, map, x0, two ? map : nullptr, x1, y, issue, w0, w1);
 }
 
 // Job j -> (tile, token tile).  Tiles [0, nq_tiles) are q heads, the rest kv
@@ -670,7 +678,7 @@ __device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32
 // half 0 takes nope columns [0, ns), half 1 nope columns [ns, Dn) and the
 // rope slice, ns = min(Dn, (Dn + R) / 2 rounded down to 16).  y0 is the
 // warp's first token row.
-__device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, const OutMaps& om, StoreRing& sr,
+__device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, const OutMaps& om, const StoreRing& sr,
                                                      uint32_t tbase, const RowCtx& rc, int h, int half_idx, int y0) {
     const int Dn = p.Dn, R = p.R, HD = Dn + R, half = R / 2;
     const bool valid = rc.valid, issue = y0 < p.T;
@@ -686,15 +694,14 @@ __device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, cons
         q_nope32(tbase, valid, c, scaled, rstd, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
-        store_box_f32(sr, om.q, x0 + c, y0, issue, v);
-        store_box_f32(sr, om.q, x0 + c + 16, y0, issue, v + 16);
+        store_boxes_f32(sr, om.q, x0 + c, x0 + c + 16, true, y0, issue, v, v + 16);
     }
     for (; c < c1; c += 16) {
         float v[16];
         q_nope16(tbase, valid, c, scaled, rstd, v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
-        store_box_f32(sr, om.q, x0 + c, y0, issue, v);
+        store_boxes_f32(sr, om.q, x0 + c, 0, false, y0, issue, v, v);
     }
     if (half_idx == 1) {
 #pragma unroll
@@ -708,8 +715,7 @@ __device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, cons
                 for (int e = 0; e < 8; ++e) o1[e] = a1[e], o1[8 + e] = b1[e], o2[e] = a2[e], o2[8 + e] = b2[e];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
-                store_box_f32(sr, om.q, x0 + Dn + i, y0, issue, o1);
-                store_box_f32(sr, om.q, x0 + Dn + half + i, y0, issue, o2);
+                store_boxes_f32(sr, om.q, x0 + Dn + i, x0 + Dn + half + i, true, y0, issue, o1, o2);
             }
         }
     }
@@ -718,23 +724,38 @@ __device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, cons
 
 // The kv tile through the store ring (Dn, Dv multiples of 32, bn_kv a
 // multiple of 64): 32-column groups, each all k_nope or all value.
-__device__ __forceinline__ void expand_kv_epilogue_ts(const ExpandParams& p, const OutMaps& om, StoreRing& sr,
+__device__ __forceinline__ void expand_kv_epilogue_ts(const ExpandParams& p, const OutMaps& om, const StoreRing& sr,
                                                       uint32_t tbase, const RowCtx& rc, int n0, int half_idx, int y0) {
     const int Dn = p.Dn, HD = p.Dn + p.Dv, hw = p.bn_kv / 2;
     const bool issue = y0 < p.T;
-    for (int c = half_idx * hw; c < (half_idx + 1) * hw; c += 32) {
+    // 32-column group at n: its output tensor and first element
+    auto dst = [&](int n, int& x) -> const CUtensorMap* {
+        const int h = n / HD, j = n - h * HD;
+        x = j < Dn ? h * (Dn + p.R) + j : h * p.Dv + (j - Dn);
+        return j < Dn ? om.k : om.v;
+    };
+    const int c1 = (half_idx + 1) * hw;
+    for (int c = half_idx * hw; c < c1; c += 64) {  // two 32-column groups per staging round
         const int n = n0 + c;
         if (n >= p.NKV) break;  // warp-uniform
+        const bool two = c + 32 < c1 && n + 32 < p.NKV;
         float v[32];
+        uint32_t w0[16], w1[16];
         tmem_ld32(tbase + c, v);
-        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = rc.valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
-        const int h = n / HD, j = n - h * HD;
-        if (j < Dn)
-            store_box(sr, om.k, h * (Dn + p.R) + j, y0, issue, w);
-        else
-            store_box(sr, om.v, h * p.Dv + (j - Dn), y0, issue, w);
+        for (int e = 0; e < 16; ++e) w0[e] = rc.valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
+        if (two) {
+            tmem_ld32(tbase + c + 32, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w1[e] = rc.valid ? pack_bf16x2(v[2 * e], v[2 * e + 1]) : 0u;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w1[e] = 0u;
+        }
+        int x0, x1 = 0;
+        const CUtensorMap* m0 = dst(n, x0);
+        const CUtensorMap* m1 = two ? dst(n + 32, x1) : nullptr;
+        store_boxes(sr, m0, x0, m1, x1, y0, issue, w0, w1);
     }
 }
 
@@ -978,7 +999,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         int cur_m = -1;
         RowCtx ctx;
-        StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes, 0u};
+        const StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes};
         for (int i = jobs.begin; i < jobs.end; ++i, ++rc.chain) {
             int tile, m;
             expand_job(p, jobs[i], tile, m);
