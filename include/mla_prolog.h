@@ -298,11 +298,12 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            256 columns). */
 #define MLA_TUNE_PAIR_EXPAND 6
 /*   MLA_TUNE_PAIR_COMPRESS   1: the compression projection runs on CTA pairs
- *                            (256-token tiles of 128 weight rows, each SM
- *                            streaming half of every weight tile); 0 (the
- *                            default, measured faster): one CTA per
- *                            128-token tile.  INVALID_ARG when 1 is not
- *                            available (decode batches). */
+ *                            (256-token tiles of 256 weight rows, each SM
+ *                            streaming half of every weight tile, plain FP32
+ *                            sums of the drained chains); 0 (the default,
+ *                            measured faster): one CTA per 128-token tile.
+ *                            INVALID_ARG when 1 is not available (decode
+ *                            batches). */
 #define MLA_TUNE_PAIR_COMPRESS 7
 /*   MLA_TUNE_TMA_STORE       1 (the default where the dims allow it: nope
  *                            and value widths multiples of 32, and with the
@@ -326,6 +327,15 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            cluster or cooperative paths) or another
  *                            width. */
 #define MLA_TUNE_COMPRESS_TILE 9
+/*   MLA_TUNE_L2_FETCH        decode batches: 1: once the compression kernel
+ *                            has issued its last operand loads it asks L2 to
+ *                            fetch the expansion weights W_b from HBM while
+ *                            it drains and the norm runs, so the expansion
+ *                            reads them from L2 (the default when W_b is at
+ *                            least 64 MB, where it measured faster); 0: the
+ *                            expansion streams them from HBM.  INVALID_ARG
+ *                            for prefill batches. */
+#define MLA_TUNE_L2_FETCH 10
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

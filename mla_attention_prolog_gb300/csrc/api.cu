@@ -76,7 +76,7 @@ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
 constexpr int kCompressTiles[3] = {128, 192, 256};  // prefill compression weight-tile widths
-constexpr int kPairCompressBN = 128;                // the compression pair kernel's tile width
+constexpr int kPairCompressBN = 256;                // the compression pair kernel's tile width
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
 
@@ -140,6 +140,7 @@ struct mla_prolog {
     CUtensorMap tm_nq{}, tm_nkv{}, tm_x{}, tm_wa{}, tm_wa_c{}, tm_wqb{}, tm_wkvb{};
     CUtensorMap tm_wqb2{}, tm_wkvb2{}, tm_wa2{};  // half-tile weight boxes of the pair kernels
     // the expansion epilogue's bulk tensor stores (kernels with a staging area)
+    bool l2_fetch = false;  // decode: the compression kernel fetches W_b into L2 (tunable)
     bool ts_ok = false;     // the dims allow them
     bool tma_store = false;  // in use (tunable)
     OutTensorMaps tm_out{};  // q workspace (fixed), out_k / out_v (re-encoded per pointer)
@@ -308,11 +309,13 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         if (compress_pair_max_active(&active) == cudaSuccess && active >= 1) {
             const int kb = cdiv(d.D, kBK);
             h->cpair_ok = true;
-            // Measured on GB300: slower on pairs (V3 prefill compression 831
-            // vs 640 us, V2-Lite 34.8 vs 30.3 us): its accumulators drain every
-            // 2-4 K blocks and each drain waits for both CTAs' epilogues.
+            // Measured on GB300: slower on pairs (256-wide tiles, plain FP32
+            // drain: V3 prefill step 2257 vs 2187 us, V2-Lite 47.4 vs 42.5
+            // us; 128-wide with TwoSum earlier: compression 831 vs 640 us):
+            // the accumulators drain every few K blocks and each drain waits
+            // for both CTAs' epilogues.
             h->cpair = false;
-            h->cpair_splits = prefill_compress_splits(d.T, h->NA, kb, sms, 2);
+            h->cpair_splits = prefill_compress_splits(d.T, h->NA, kb, sms, 2, kPairCompressBN);
             h->cpair_m_tiles = cdiv(d.T, 2 * kBM);
             const int cjobs = cdiv(h->NA, kPairCompressBN) * h->cpair_m_tiles * h->cpair_splits;
             h->cpair_grid = cjobs < sms / 2 ? cjobs : sms / 2;
@@ -449,6 +452,13 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         ok = ok && encode_store(&h->tm_out.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h->qws, h->NQ, Tm,
                                 static_cast<uint64_t>(h->NQ) * 4, 16);
     h->tma_store = h->ts_ok;
+    // Decode: W_b fetched into L2 behind the compression's last loads.
+    // Measured on GB300 (step time, weights from HBM every step): V3 decode
+    // (110 MB of W_b) 49.1 -> 48.1 us; V2-Lite decode (4 MB) 16.4 -> 18.6 us.
+    // Issued from the start of the compression instead, both were slower
+    // (56.9 / 20.3 us): the fetch delays the compression's own loads.
+    const uint64_t wb_bytes = (static_cast<uint64_t>(h->NQ) * Lq + static_cast<uint64_t>(h->NKV) * Lkv) * 2;
+    h->l2_fetch = h->decode && wb_bytes >= (64ull << 20);
     if (!ok) {
         cudaFree(h->ws);
         delete h;
@@ -579,6 +589,10 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pa.status = h->status;
     pa.timeout_ns = h->timeout_ns;
     pa.job_table = h->compress_table;
+    if (h->decode && h->l2_fetch) {
+        pa.l2_fetch = static_cast<const uint8_t*>(W_b);
+        pa.l2_fetch_bytes = (static_cast<uint64_t>(h->NQ) * Lq + static_cast<uint64_t>(h->NKV) * Lkv) * 2;
+    }
 
     NormRopeParams pn{};
     pn.partials = h->partials;
@@ -892,6 +906,11 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
         case MLA_TUNE_COMPRESS_TILE:
             if (h->decode || h->cluster || h->fused) return MLA_ERR_INVALID_ARG;
             return select_compress_tile(h, value) ? MLA_OK : MLA_ERR_INVALID_ARG;
+        case MLA_TUNE_L2_FETCH:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->decode) return MLA_ERR_INVALID_ARG;
+            h->l2_fetch = value == 1;
+            return MLA_OK;
         case MLA_TUNE_TMA_STORE:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->ts_ok) return MLA_ERR_INVALID_ARG;

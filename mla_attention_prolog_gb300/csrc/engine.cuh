@@ -849,6 +849,20 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
                 }
             }
         }
+        __syncwarp();
+        if (p.l2_fetch_bytes > 0) {
+            // Once this CTA's last operand load is issued, the expansion
+            // weights stream into L2 from HBM while the compression drains
+            // and the norm runs.
+            constexpr uint64_t kPiece = 32768;
+            const uint64_t pieces = (p.l2_fetch_bytes + kPiece - 1) / kPiece;
+            for (uint64_t k = static_cast<uint64_t>(first) * 32 + lane; k < pieces;
+                 k += 32ull * static_cast<uint64_t>(stride)) {
+                const uint64_t off = k * kPiece;
+                const uint64_t left = p.l2_fetch_bytes - off;
+                bulk_prefetch_l2(p.l2_fetch + off, static_cast<uint32_t>(left < kPiece ? left : kPiece));
+            }
+        }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {  // a pair's MMAs are issued by its even CTA
             const uint32_t idesc = idesc_bf16_f32(kBM * CG, p.bn);

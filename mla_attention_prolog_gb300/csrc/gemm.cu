@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 
 // Prefill compression on CTA pairs: each job is a 256-token x BN tile (M =
 // 256); each CTA streams its 128 token rows and BN / 2 weight rows per K
-// block and drains its own 128 rows' chains.
+// block and drains its own 128 rows' chains (plain FP32 sums, as the wide
+// one-CTA tiles).
 template <int BN_MAX, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompressThreads, 1)
     mla_compress_pair_kernel(const __grid_constant__ CUtensorMap tm_x,
@@ -59,7 +60,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kCompressThreads, 1)
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES, 2>(sm, kDrainEpiWarps);
     pdl_launch_dependents();
     RoleCounters rc;
-    compress_phase<BN_MAX, STAGES, BN_MAX, 2>(sm, tmem, &tm_x, &tm_wa, p, rc, blockIdx.x, gridDim.x);
+    compress_phase<BN_MAX, STAGES, BN_MAX, 2, false>(sm, tmem, &tm_x, &tm_wa, p, rc, blockIdx.x, gridDim.x);
     gemm_finish<BN_MAX, STAGES, 2>(sm, tmem, rc, p.timeout_ns);
 }
 
@@ -112,7 +113,7 @@ using EMid = Layout<192, 5>;
 using ENarrow = Layout<64, 4>;
 using EDeep = Layout<64, 8>;
 using EPair = Layout<256, 6, 2, kStoreStageBytes>;  // per CTA: 16 KB activations + 16 KB weights per stage
-using CPair = Layout<128, 8, 2>;  // per CTA: 16 KB activations + 8 KB weights per stage
+using CPair = Layout<256, 6, 2>;  // per CTA: 16 KB activations + 16 KB weights per stage
 using CWide = Layout<128, 6>;
 using CNarrow = Layout<64, 4>;
 using C192 = Layout<192, 5>;  // 16 KB activations + 24 KB weights per stage
@@ -152,7 +153,7 @@ cudaError_t gemm_set_attributes() {
     if ((e = cudaFuncSetAttribute(mla_expand_pair_kernel<256, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EPair::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_compress_pair_kernel<128, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_compress_pair_kernel<256, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   CPair::BYTES)))
         return e;
     return cudaSuccess;
@@ -202,12 +203,12 @@ cudaError_t compress_pair_max_active(int* clusters) {
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(kCompressThreads);
     cfg.dynamicSmemBytes = CPair::BYTES;
-    return cudaOccupancyMaxActiveClusters(clusters, mla_compress_pair_kernel<128, 8>, &cfg);
+    return cudaOccupancyMaxActiveClusters(clusters, mla_compress_pair_kernel<256, 6>, &cfg);
 }
 
 cudaError_t launch_compress_pair(int pairs, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
                                  const CompressParams& p, cudaStream_t st) {
-    return launch_kernel(mla_compress_pair_kernel<128, 8>, dim3(2 * pairs), dim3(kCompressThreads), CPair::BYTES, st,
+    return launch_kernel(mla_compress_pair_kernel<256, 6>, dim3(2 * pairs), dim3(kCompressThreads), CPair::BYTES, st,
                          false, tm_x, tm_wa, p);
 }
 

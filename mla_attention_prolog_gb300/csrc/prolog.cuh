@@ -41,6 +41,11 @@ struct CompressParams {
     int* status;
     uint64_t timeout_ns;
     const int* job_table;  // balanced per-CTA job lists (null: round robin)
+    // A byte range the kernel asks L2 to fetch from HBM while it runs (the
+    // expansion weights of a decode batch; null: none), in pieces of 32 KB
+    // issued by the producer warp's spare lanes.
+    const uint8_t* l2_fetch;
+    uint64_t l2_fetch_bytes;
 };
 
 // Per-token reduction of the partials, BF16 cast, RMSNorm of c_q and c_kv,

@@ -455,3 +455,31 @@ def test_compression_tile_widths(name, T):
     with pytest.raises(binding.MlaPrologError):
         p.set_tuning(binding.TUNE_COMPRESS_TILE, 160)
     p.close()
+
+
+@pytest.mark.parametrize("name", ["v3_decode", "v2lite_decode"])
+def test_l2_fetch_keeps_outputs(name):
+    """Fetching the expansion weights into L2 during the decode compression
+    changes no output bit; prefill handles refuse the switch."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    d = inp.dims
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    outs = []
+    for f in (1, 0):
+        p.set_tuning(binding.TUNE_L2_FETCH, f)
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    _bits_equal(outs[0], outs[1])
+    for o in outs:
+        for k, g in o.items():
+            assert g.guards_intact(), k
+    p.close()
+    q = binding.MlaProlog.from_dims(wl.WORKLOADS["v2lite_prefill"].dims.with_T(300))
+    with pytest.raises(binding.MlaPrologError):
+        q.set_tuning(binding.TUNE_L2_FETCH, 1)
+    q.close()
