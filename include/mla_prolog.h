@@ -336,6 +336,16 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            expansion streams them from HBM.  INVALID_ARG
  *                            for prefill batches. */
 #define MLA_TUNE_L2_FETCH 10
+/*   MLA_TUNE_Q_WIDE          prefill on CTA pairs with the per-token q path
+ *                            (rope width 64, nope width a multiple of 64, no
+ *                            per-head norm or quant): 1 (the default there,
+ *                            measured faster): q tiles of 256 columns that
+ *                            run across head boundaries (fewer operand bytes
+ *                            per tensor-core FLOP than one 192-column head
+ *                            per tile); 0: one head per tile.  Same values either way (the tensor
+ *                            stores must be on for 1 to take effect).
+ *                            INVALID_ARG when 1 is not available. */
+#define MLA_TUNE_Q_WIDE 11
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

@@ -44,6 +44,7 @@ TUNE_PAIR_COMPRESS = 7
 TUNE_TMA_STORE = 8
 TUNE_COMPRESS_TILE = 9
 TUNE_L2_FETCH = 10
+TUNE_Q_WIDE = 11
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -437,23 +437,23 @@ __device__ __forceinline__ void rope8(const float (&a)[8], const float (&b)[8], 
     }
 }
 
-// Rope pairs [i, i + 8) of q head's rope slice (TMEM columns Dn .. Dn + R of
-// this row): pair j is (Dn + j, Dn + R/2 + j), or, de-interleaved,
-// (Dn + 2j, Dn + 2j + 1); each value times rstd (the per-head norm) when
-// `scaled`, then rotated with (cc, ss).  Zero for a row whose position is
-// invalid.  Whole warp (TMEM loads).
-__device__ __forceinline__ void q_rope8(const ExpandParams& p, uint32_t tbase, bool valid, int i, bool scaled,
+// Rope pairs [i, i + 8) of a q head's rope slice, whose first column is the
+// TMEM address `tr` (a head's column Dn): pair j is (j, R/2 + j), or,
+// de-interleaved, (2j, 2j + 1); each value times rstd (the per-head norm)
+// when `scaled`, then rotated with (cc, ss).  Zero for a row whose position
+// is invalid.  Whole warp (TMEM loads).
+__device__ __forceinline__ void q_rope8(const ExpandParams& p, uint32_t tr, bool valid, int i, bool scaled,
                                         float rstd, const float* cc, const float* ss, float (&o1)[8],
                                         float (&o2)[8]) {
-    const int Dn = p.Dn, half = p.R / 2;
+    const int half = p.R / 2;
     float a[8], b[8];
     if (p.interleaved) {
         float v[16];
-        tmem_ld16(tbase + Dn + 2 * i, v);
+        tmem_ld16(tr + 2 * i, v);
 #pragma unroll
         for (int e = 0; e < 8; ++e) a[e] = v[2 * e], b[e] = v[2 * e + 1];
     } else {
-        tmem_ld8x2(tbase + Dn + i, tbase + Dn + half + i, a, b);
+        tmem_ld8x2(tr + i, tr + half + i, a, b);
     }
     if (scaled) {
 #pragma unroll
@@ -478,7 +478,7 @@ __device__ __forceinline__ void q_rope_chunks(const ExpandParams& p, uint32_t tb
         for (int i = 0; i < 32; i += 8) {
             if (i < half) {  // warp-uniform
                 float o1[8], o2[8];
-                q_rope8(p, tbase, rc.valid, i, scaled, rstd, rc.c + i, rc.s + i, o1, o2);
+                q_rope8(p, tbase + p.Dn, rc.valid, i, scaled, rstd, rc.c + i, rc.s + i, o1, o2);
                 f(i, o1, o2);
             }
         }
@@ -488,7 +488,7 @@ __device__ __forceinline__ void q_rope_chunks(const ExpandParams& p, uint32_t tb
             float cc[8], ss[8], o1[8], o2[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) cc[e] = cs[i + e], ss[e] = cs[half + i + e];
-            q_rope8(p, tbase, rc.valid, i, scaled, rstd, cc, ss, o1, o2);
+            q_rope8(p, tbase + p.Dn, rc.valid, i, scaled, rstd, cc, ss, o1, o2);
             f(i, o1, o2);
         }
     }
@@ -709,13 +709,58 @@ __device__ __forceinline__ void expand_q_epilogue_ts(const ExpandParams& p, cons
             if (i < half) {  // warp-uniform
                 float o1[16], o2[16];
                 float a1[8], a2[8], b1[8], b2[8];
-                q_rope8(p, tbase, valid, i, scaled, rstd, rc.c + i, rc.s + i, a1, a2);
-                q_rope8(p, tbase, valid, i + 8, scaled, rstd, rc.c + i + 8, rc.s + i + 8, b1, b2);
+                q_rope8(p, tbase + Dn, valid, i, scaled, rstd, rc.c + i, rc.s + i, a1, a2);
+                q_rope8(p, tbase + Dn, valid, i + 8, scaled, rstd, rc.c + i + 8, rc.s + i + 8, b1, b2);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o1[e] = a1[e], o1[8 + e] = b1[e], o2[e] = a2[e], o2[8 + e] = b2[e];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fmaxf(fabsf(o1[e]), fabsf(o2[e])));
                 store_boxes_f32(sr, om.q, x0 + Dn + i, x0 + Dn + half + i, true, y0, issue, o1, o2);
+            }
+        }
+    }
+    if (valid) atomicMax(p.amax + rc.t, __float_as_uint(amax));
+}
+
+// A q tile of kQWide columns starting at q column n0, across head
+// boundaries (see ExpandParams::q_wide): each warp takes 128 columns as two
+// 64-column pieces, either nope columns (copied) or one head's rope slice
+// (rotated), through the store ring; one amax update per row.
+__device__ __forceinline__ void expand_qw_epilogue_ts(const ExpandParams& p, const OutMaps& om, const StoreRing& sr,
+                                                      uint32_t tbase, const RowCtx& rc, int n0, int half_idx,
+                                                      int y0) {
+    const int Dn = p.Dn, HD = Dn + p.R;
+    const bool valid = rc.valid, issue = y0 < p.T;
+    float amax = 0.0f;
+#pragma unroll 1
+    for (int s = 0; s < 2; ++s) {
+        const int c = half_idx * (kQWide / 2) + s * 64;  // tile column
+        const int g = n0 + c;                            // q column
+        const int j = g - (g / HD) * HD;
+        if (j >= Dn) {  // one head's rope slice: [o1 | o2], 32 pairs
+#pragma unroll
+            for (int side = 0; side < 2; ++side) {
+                float o[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    float a1[8], a2[8];
+                    q_rope8(p, tbase + c, valid, i, false, 1.0f, rc.c + i, rc.s + i, a1, a2);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        o[i + e] = side ? a2[e] : a1[e];
+                        amax = fmaxf(amax, fabsf(o[i + e]));
+                    }
+                }
+                store_boxes_f32(sr, om.q, g + 32 * side, g + 32 * side + 16, true, y0, issue, o, o + 16);
+            }
+        } else {
+#pragma unroll
+            for (int h2 = 0; h2 < 64; h2 += 32) {
+                float v[32];
+                q_nope32(tbase, valid, c + h2, false, 1.0f, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+                store_boxes_f32(sr, om.q, g + h2, g + h2 + 16, true, y0, issue, v, v + 16);
             }
         }
     }
@@ -983,9 +1028,10 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 int tile, m;
                 expand_job(p, jobs[i], tile, m);
                 const bool first = i == jobs.begin;
+                const int bq = p.q_wide ? kQWide : Dn + R;  // q tile width
                 ok = tile < p.nq_tiles
-                         ? produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_aq, tm_bq, m * TM, tile * (Dn + R), 0,
-                                                           p.kb_q, Dn + R, first, p.timeout_ns, dep)
+                         ? produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_aq, tm_bq, m * TM, tile * bq, 0, p.kb_q,
+                                                           bq, first, p.timeout_ns, dep)
                          : produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_akv, tm_bkv, m * TM,
                                                            (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
                                                            p.timeout_ns, dep);
@@ -995,7 +1041,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {  // a pair's MMAs are issued by its even CTA
-            const uint32_t idesc_q = idesc_bf16_f32(TM, Dn + R);
+            const uint32_t idesc_q = idesc_bf16_f32(TM, p.q_wide ? kQWide : Dn + R);
             const uint32_t idesc_kv = idesc_bf16_f32(TM, p.bn_kv);
             for (int i = jobs.begin; i < jobs.end && ok; ++i, ++rc.chain) {
                 int tile, m;
@@ -1030,6 +1076,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             const int y0 = m * TM + rank * kBM + quarter * 32;
             if (TS && p.tma_store && tile >= p.nq_tiles)
                 expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx, y0);
+            else if (TS && p.q_wide)
+                expand_qw_epilogue_ts(p, om, sr, tbase, ctx, tile * kQWide, half_idx, y0);
             else if (TS && p.tma_store && !p.per_head)
                 expand_q_epilogue_ts(p, om, sr, tbase, ctx, tile, half_idx, y0);
             else if (tile < p.nq_tiles)

@@ -101,7 +101,14 @@ struct ExpandParams {
     // kernels built with a staging area; the kv tiles and the per-token q
     // path): the output tensor maps are kernel parameters.
     int tma_store;
+    // q tiles of kQWide columns that run across head boundaries (nq_tiles =
+    // NQ / kQWide) instead of one head per tile: the per-token q path through
+    // the store ring, R = 64 and Dn a multiple of 64, so every 64-column piece
+    // of a tile is nope columns or one head's whole rope slice.
+    int q_wide;
 };
+
+constexpr int kQWide = 256;
 
 struct QuantParams {
     const float* y;          // [rows][row_len]

@@ -483,3 +483,41 @@ def test_l2_fetch_keeps_outputs(name):
     with pytest.raises(binding.MlaPrologError):
         q.set_tuning(binding.TUNE_L2_FETCH, 1)
     q.close()
+
+
+@pytest.mark.parametrize("T,extra", [(640, 0), (385, wl.ROPE_INTERLEAVED), (0, 0)], ids=["T640", "T385_il", "full"])
+def test_wide_q_tiles_match_head_tiles(T, extra):
+    """q tiles of 256 columns across head boundaries (CTA pairs, per-token q
+    path) give the same bytes as one head per tile, within the bar of the
+    oracle, guard bands intact."""
+    w = wl.WORKLOADS["v3_prefill"]
+    d = w.dims.with_T(T) if T else w.dims
+    d = dataclasses.replace(d, flags=d.flags | extra)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    outs = []
+    for f in (1, 0):
+        p.set_tuning(binding.TUNE_Q_WIDE, f)
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    _bits_equal(outs[0], outs[1])
+    tok = np.unique(np.concatenate([np.linspace(0, d.T - 1, min(d.T, 48)).astype(np.int32), inp.boosted_rows[:4]]))
+    tok = tok.astype(np.int32)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    a = outs[0]
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t[sel], ref[k], k)
+    quant_within(a["out_q_int8"].t[sel], a["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+    for o in outs:
+        for k, g in o.items():
+            assert g.guards_intact(), k
+    p.close()
+    q = binding.MlaProlog.from_dims(dataclasses.replace(d, flags=d.flags | wl.QUANT_PER_HEAD))
+    with pytest.raises(binding.MlaPrologError):
+        q.set_tuning(binding.TUNE_Q_WIDE, 1)
+    q.close()
