@@ -391,6 +391,37 @@ int mla_prolog_workspace_bytes(mla_prolog_t h, size_t* bytes);
 int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a,
                         int32_t* bn_kv, int32_t* bn_q);
 
+/*
+ * The schedule mla_prolog_create() chooses for `dims` on a device with `sms`
+ * SMs, computed on the host without touching the GPU (the rules in one place,
+ * for tests and reports).  decode: 1 for the decode schedule (at most two
+ * 128-token tiles); bn_a, splits_a, group_a: the compression's weight-tile
+ * width (prefill: the default of MLA_TUNE_COMPRESS_TILE), split-K factor and
+ * accumulation-chain length in K blocks of 64; compress_jobs: its jobs (token
+ * tiles x weight tiles x splits); busiest_bytes: the operand bytes (token rows
+ * + weight rows, 128 bytes per row per K block) that the busiest CTA streams
+ * in the compression; bn_kv: the expansion's kv tile width.
+ * Errors: INVALID_ARG (a NULL pointer, sms < 1), UNSUPPORTED_DIMS as
+ * mla_prolog_create().
+ */
+typedef struct mla_prolog_plan_info {
+    int32_t decode, bn_a, splits_a, group_a, compress_jobs, bn_kv;
+    int64_t busiest_bytes;
+} mla_prolog_plan_info;
+int mla_prolog_plan(const mla_prolog_dims* dims, int32_t sms, mla_prolog_plan_info* out);
+
+/*
+ * Longest-processing-time assignment of n jobs of the given costs to `groups`
+ * workers, the way the kernels' balanced job tables are built: jobs by
+ * decreasing cost (ties by index), each to the least-loaded worker (the lowest
+ * index on a tie).  table (groups + 1 + n int32s, may be NULL): groups + 1
+ * start offsets, then the job indices of worker 0, worker 1, ...; *busiest
+ * (may be NULL): the largest worker load.  Host only.
+ * Errors: INVALID_ARG (n < 0, groups < 1, cost NULL with n > 0, a negative
+ * cost).
+ */
+int mla_prolog_lpt(const int64_t* cost, int32_t n, int32_t groups, int32_t* table, int64_t* busiest);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ EXPORTED = [
     "mla_prolog_set_wait_timeout", "mla_prolog_selftest_wait_timeout",
     "mla_prolog_set_timing_events", "mla_prolog_kernel_count", "mla_prolog_kernel_name",
     "mla_prolog_workspace_bytes", "mla_prolog_schedule", "mla_prolog_copy_tap", "mla_prolog_set_tuning",
-    "mla_prolog_run_noalloc", "mla_prolog_run_cached",
+    "mla_prolog_run_noalloc", "mla_prolog_run_cached", "mla_prolog_plan", "mla_prolog_lpt",
 ]
 TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
 TUNE_COMPRESS_GROUP = 1
@@ -51,6 +51,11 @@ class MlaPrologDims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "T", "D", "q_lora_rank", "kv_lora_rank", "rope_dim", "num_heads",
         "nope_dim", "v_dim", "max_pos")] + [("eps", ctypes.c_float), ("flags", ctypes.c_uint32)]
+
+
+class MlaPrologPlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "decode", "bn_a", "splits_a", "group_a", "compress_jobs", "bn_kv")] + [("busiest_bytes", ctypes.c_int64)]
 
 
 class MlaPrologError(RuntimeError):
@@ -95,6 +100,8 @@ def lib(path: Optional[str] = None):
     L.mla_prolog_set_tuning.argtypes = [V, I32, I32]
     L.mla_prolog_run_noalloc.argtypes = [P(MlaPrologDims)] + [V] * 13
     L.mla_prolog_run_cached.argtypes = [V] * 14 + [ctypes.c_int64, V]
+    L.mla_prolog_plan.argtypes = [P(MlaPrologDims), I32, P(MlaPrologPlanInfo)]
+    L.mla_prolog_lpt.argtypes = [P(ctypes.c_int64), I32, I32, P(I32), P(ctypes.c_int64)]
     for n in EXPORTED:
         if n not in ("mla_prolog_strerror", "mla_prolog_last_cuda_error", "mla_prolog_kernel_count",
                      "mla_prolog_kernel_name"):
@@ -271,3 +278,25 @@ def quant_rows(y: torch.Tensor, codes: torch.Tensor, scale: torch.Tensor, stream
             _ptr(codes, "codes", torch.int8, (rows, n), dev),
             _ptr(scale, "scale", torch.float32, (rows,), dev), _stream_ptr(stream)]
     _check(lib().mla_prolog_quant_rows(*args), "mla_prolog_quant_rows")
+
+
+def plan(d, sms: int) -> dict:
+    """The schedule the library chooses for dims `d` on `sms` SMs (host only)."""
+    dims = MlaPrologDims(d.T, d.D, d.q_lora_rank, d.kv_lora_rank, d.rope_dim, d.num_heads, d.nope_dim,
+                         d.v_dim, d.max_pos, d.eps, d.flags)
+    out = MlaPrologPlanInfo()
+    _check(lib().mla_prolog_plan(ctypes.byref(dims), sms, ctypes.byref(out)), "mla_prolog_plan")
+    return {n: getattr(out, n) for n, _ in MlaPrologPlanInfo._fields_}
+
+
+def lpt(cost: Sequence[int], groups: int):
+    """Longest-processing-time job assignment (host only): (per-worker job
+    lists, largest worker load)."""
+    n = len(cost)
+    c = (ctypes.c_int64 * max(n, 1))(*cost)
+    table = (ctypes.c_int32 * (groups + 1 + n))()
+    busiest = ctypes.c_int64(0)
+    _check(lib().mla_prolog_lpt(c, n, groups, table, ctypes.byref(busiest)), "mla_prolog_lpt")
+    offs = list(table[:groups + 1])
+    ids = list(table[groups + 1:])
+    return [ids[offs[g]:offs[g + 1]] for g in range(groups)], busiest.value

@@ -75,7 +75,6 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
-constexpr int kCompressTiles[3] = {128, 192, 256};  // prefill compression weight-tile widths
 constexpr int kPairCompressBN = 256;                // the compression pair kernel's tile width
 const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
                                                 "mla_expand_kernel", "mla_quant_kernel"};
@@ -357,26 +356,14 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     int part_splits = h->cpair_splits > h->splits_a ? h->cpair_splits : h->splits_a;
     int ctile_default = 128;
     if (!h->decode) {
-        const int kb = cdiv(d.D, kBK);
-        long long best = -1;
+        CompressTilePlan plans[3];
+        ctile_default = plan_compress_tiles(d.T, h->NA, cdiv(d.D, kBK), sms, plans, ctable);
         for (int i = 0; i < 3; ++i) {
             auto& ct = h->ctile[i];
-            ct.bn = kCompressTiles[i];
+            ct.bn = plans[i].bn;
             ct.shape = ct.bn == 128 ? GemmShape::Wide : ct.bn == 192 ? GemmShape::Wide192 : GemmShape::Wide256;
-            ct.splits = prefill_compress_splits(d.T, h->NA, kb, sms, 1, ct.bn);
-            const auto cost = compress_job_bytes(d.T, h->NA, kb, ct.bn, ct.splits);
-            const long long busiest = lpt_assign(cost, sms, static_cast<int>(cost.size()) > sms ? &ctable[i] : nullptr);
+            ct.splits = plans[i].splits;
             if (ct.splits > part_splits) part_splits = ct.splits;
-            // Default: the wide tile (192 or 256) that needs no split-K and
-            // brings its busiest SM the fewest operand bytes, else 128.
-            // Measured on GB300 (step time): V3 prefill 16384 tokens 2441 /
-            // 2245 / 2173 us (128 / 192 / 256), V2-Lite prefill 4096 tokens
-            // 52.3 / 43.5 / 48.1 us (256 needs split-K 2 there), V3 prefill
-            // 385 tokens 109.5 / 127.3 / 120.0 us (the wide ones need split-K 4).
-            if (ct.bn > 128 && ct.splits == 1 && (best < 0 || busiest < best)) {
-                best = busiest;
-                ctile_default = ct.bn;
-            }
         }
     }
 
@@ -965,7 +952,52 @@ int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a, int32_
     if (bn_a) *bn_a = h->cluster ? h->cplan.cgw : h->bn_a;
     if (splits_a) *splits_a = h->cluster ? h->cplan.ks : h->splits_a;
     if (bn_kv) *bn_kv = h->bn_kv;
-    if (bn_q) *bn_q = h->d.q_lora_rank > 0 ? h->d.nope_dim + h->d.rope_dim : 0;
+    if (bn_q)
+        *bn_q = h->d.q_lora_rank == 0              ? 0
+                : h->pair && h->q_wide && h->tma_store ? kQWide
+                                                       : h->d.nope_dim + h->d.rope_dim;
+    return MLA_OK;
+}
+
+int mla_prolog_plan(const mla_prolog_dims* dims, int32_t sms, mla_prolog_plan_info* out) {
+    if (!dims || !out || sms < 1) return MLA_ERR_INVALID_ARG;
+    const int rc = check_dims(*dims);
+    if (rc != MLA_OK) return rc;
+    const mla_prolog_dims& d = *dims;
+    const int Lq = d.q_lora_rank, Lkv = d.kv_lora_rank, R = d.rope_dim;
+    const int NA = Lq + Lkv + R, kb = cdiv(d.D, kBK);
+    const Schedule sc = plan_schedule(d.T, d.D, Lq, Lkv, R, d.num_heads, d.nope_dim, d.v_dim, sms);
+    int bn_a = sc.bn_a, splits = sc.splits_a;
+    if (!sc.decode) {
+        CompressTilePlan plans[3];
+        bn_a = plan_compress_tiles(d.T, NA, kb, sms, plans);
+        for (const auto& ct : plans)
+            if (ct.bn == bn_a) splits = ct.splits;
+    }
+    const auto cost = compress_job_bytes(d.T, NA, kb, bn_a, splits);
+    *out = mla_prolog_plan_info{};
+    out->decode = sc.decode ? 1 : 0;
+    out->bn_a = bn_a;
+    out->splits_a = splits;
+    out->group_a = sc.group_a;
+    out->compress_jobs = static_cast<int32_t>(cost.size());
+    out->bn_kv = sc.bn_kv;
+    out->busiest_bytes = cost.empty() ? 0 : lpt_assign(cost, sms);
+    return MLA_OK;
+}
+
+int mla_prolog_lpt(const int64_t* cost, int32_t n, int32_t groups, int32_t* table, int64_t* busiest) {
+    if (n < 0 || groups < 1 || (n > 0 && !cost)) return MLA_ERR_INVALID_ARG;
+    std::vector<long long> c(cost, cost + n);
+    for (long long v : c)
+        if (v < 0) return MLA_ERR_INVALID_ARG;
+    std::vector<int> t;
+    const long long b = n > 0 ? lpt_assign(c, groups, &t) : 0;
+    if (table) {
+        if (n == 0) t.assign(static_cast<size_t>(groups) + 1, 0);
+        std::copy(t.begin(), t.end(), table);
+    }
+    if (busiest) *busiest = b;
     return MLA_OK;
 }
 

@@ -349,6 +349,40 @@ inline int prefill_compress_splits(int T, int NA, int kb, int sms, int cg, int b
     return best;
 }
 
+// Prefill compression plans for each weight-tile width of
+// kCompressTileWidths: split-K factor and the operand bytes of the busiest
+// CTA (jobs longest first, each to the least-loaded CTA; the job tables into
+// `tables` when given and there are more jobs than CTAs).  Returns the
+// default width: the wide tile (192 or 256) that needs no split-K and brings
+// its busiest SM the fewest operand bytes, else 128.  Measured on GB300
+// (step time): V3 prefill 16384 tokens 2441 / 2245 / 2173 us (128 / 192 /
+// 256), V2-Lite prefill 4096 tokens 52.3 / 43.5 / 48.1 us (256 needs
+// split-K 2 there), V3 prefill 385 tokens 109.5 / 127.3 / 120.0 us (the
+// wide ones need split-K 4).
+constexpr int kCompressTileWidths[3] = {128, 192, 256};
+struct CompressTilePlan {
+    int bn, splits, jobs;
+    long long busiest;
+};
+inline int plan_compress_tiles(int T, int NA, int kb, int sms, CompressTilePlan (&out)[3],
+                               std::vector<int>* tables = nullptr) {
+    int def = 128;
+    long long best = -1;
+    for (int i = 0; i < 3; ++i) {
+        CompressTilePlan& ct = out[i];
+        ct.bn = kCompressTileWidths[i];
+        ct.splits = prefill_compress_splits(T, NA, kb, sms, 1, ct.bn);
+        const auto cost = compress_job_bytes(T, NA, kb, ct.bn, ct.splits);
+        ct.jobs = static_cast<int>(cost.size());
+        ct.busiest = lpt_assign(cost, sms, tables && ct.jobs > sms ? &tables[i] : nullptr);
+        if (ct.bn > 128 && ct.splits == 1 && (best < 0 || ct.busiest < best)) {
+            best = ct.busiest;
+            def = ct.bn;
+        }
+    }
+    return def;
+}
+
 // T tokens, D model width, Lq / Lkv / R ranks, H heads of Dn + R (q) and
 // Dn + Dv (kv) columns, on a device with `sms` SMs.
 inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int Dn, int Dv, int sms) {
