@@ -15,7 +15,10 @@ the launching stream after W warm-up replays.  Per-kernel durations come from
 a second graph of the same K steps with the library's timing hook on.
 `e2e` is the same metric through the public call with host buffers: each
 step copies x and positions from pinned host memory, runs, and copies every
-output back, all inside the timed region.
+output back, all inside the timed region -- pipelined as a serving loop
+would run it: copies in on one stream, the call on another, copies out on a
+third, over two device buffer sets, so step k+1's input copy and step k-1's
+output copy overlap step k's kernels.
 Under torchrun each rank runs its own replica of the workload (no collective
 on the data path); value = tokens of all ranks / max time over ranks.
 """
@@ -353,35 +356,52 @@ def run_gpu(args):
     per_kernel = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(G))
                   for j, n in enumerate(names) if n in active}
 
-    # e2e: host buffers through the public call
+    # e2e: host buffers through the public call, pipelined over two device sets
     pin = lambda t: t.cpu().pin_memory()
     hx, hpos = pin(base["x"]), pin(base["positions"])
     outs_h = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in sets[0].items()
               if (k.startswith("out_") or k == "kv_cache") and v is not None}
-    s0 = sets[0]
     h2d = hx.numel() * hx.element_size() + hpos.numel() * hpos.element_size()
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
-
-    def e2e_step():
-        s0["x"].copy_(hx, non_blocking=True)
-        s0["positions"].copy_(hpos, non_blocking=True)
-        one(s0)
-        for k, v in outs_h.items():
-            v.copy_(s0[k], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e2e_step()
-    stream.synchronize()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     K_e2e = min(K, 2000)
+    n_ev = K_e2e + args.warmup
+    ev_in = [torch.cuda.Event() for _ in range(n_ev)]
+    ev_run = [torch.cuda.Event() for _ in range(n_ev)]
+    ev_out = [torch.cuda.Event() for _ in range(n_ev)]
+
+    def e2e_steps(first, n):
+        for k in range(first, first + n):
+            s = sets[k % 2]
+            with torch.cuda.stream(s_in):  # set k % 2 is free once step k - 2 has run
+                if k >= 2:
+                    s_in.wait_event(ev_run[k - 2])
+                s["x"].copy_(hx, non_blocking=True)
+                s["positions"].copy_(hpos, non_blocking=True)
+                ev_in[k].record(s_in)
+            with torch.cuda.stream(stream):  # outputs of set k % 2 copied out by step k - 2
+                stream.wait_event(ev_in[k])
+                if k >= 2:
+                    stream.wait_event(ev_out[k - 2])
+                one(s)
+                ev_run[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[k])
+                for name, v in outs_h.items():
+                    v.copy_(s[name], non_blocking=True)
+                ev_out[k].record(s_out)
+
+    e2e_steps(0, args.warmup)
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(K_e2e):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    e2e_steps(args.warmup, K_e2e)
+    stream.wait_event(ev_out[n_ev - 1])
+    e1.record(stream)
+    torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     assert p.device_status(stream) == 0
     clk.__exit__(None, None, None)
