@@ -15,10 +15,12 @@ the launching stream after W warm-up replays.  Per-kernel durations come from
 a second graph of the same K steps with the library's timing hook on.
 `e2e` is the same metric through the public call with host buffers: each
 step copies x and positions from pinned host memory, runs, and copies every
-output back, all inside the timed region -- pipelined as a serving loop
-would run it: copies in on one stream, the call on another, copies out on a
-third, over two device buffer sets, so step k+1's input copy and step k-1's
-output copy overlap step k's kernels.
+output back, all inside the timed region.  When a step copies at least
+8 MB the loop is pipelined as a serving loop would run it: copies in on one
+stream, the call on another, copies out on a third, over two device buffer
+sets, so step k+1's input copy and step k-1's output copy overlap step k's
+kernels; below that the cross-stream events cost more than they hide and
+the steps run in order on one stream.
 Under torchrun each rank runs its own replica of the workload (no collective
 on the data path); value = tokens of all ranks / max time over ranks.
 """
@@ -363,7 +365,8 @@ def run_gpu(args):
               if (k.startswith("out_") or k == "kv_cache") and v is not None}
     h2d = hx.numel() * hx.element_size() + hpos.numel() * hpos.element_size()
     d2h = sum(v.numel() * v.element_size() for v in outs_h.values())
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    pipelined = h2d + d2h >= (8 << 20)
+    s_in, s_out = (torch.cuda.Stream(), torch.cuda.Stream()) if pipelined else (stream, stream)
     K_e2e = min(K, 2000)
     n_ev = K_e2e + args.warmup
     ev_in = [torch.cuda.Event() for _ in range(n_ev)]
@@ -371,6 +374,17 @@ def run_gpu(args):
     ev_out = [torch.cuda.Event() for _ in range(n_ev)]
 
     def e2e_steps(first, n):
+        if not pipelined:  # in order on one stream
+            s = sets[0]
+            with torch.cuda.stream(stream):
+                for k in range(first, first + n):
+                    s["x"].copy_(hx, non_blocking=True)
+                    s["positions"].copy_(hpos, non_blocking=True)
+                    one(s)
+                    for name, v in outs_h.items():
+                        v.copy_(s[name], non_blocking=True)
+                ev_out[first + n - 1].record(stream)
+            return
         for k in range(first, first + n):
             s = sets[k % 2]
             with torch.cuda.stream(s_in):  # set k % 2 is free once step k - 2 has run
@@ -446,7 +460,8 @@ def run_gpu(args):
         "whole_step": whole,
         "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
         "e2e": {"value": round(d.T * K_e2e * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K_e2e},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K_e2e,
+                "pipelined": pipelined},
         "gpu_launches": K * len(active),
         "clocks": clocks,
     }
