@@ -289,7 +289,30 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
         return;
     }
     float ssq_q = 0.0f, ssq_kv = 0.0f;
-    for (int i = lane * 4; i < NA; i += 128) {
+    // 4 columns -> BF16 row in shared memory and the sums of squares (chunk
+    // i / 4 on lane (i / 4) % 32, in increasing order: chunk_ssq)
+    auto take4 = [&](int i, float4 a) {
+        const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
+        *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
+        const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
+        if (i < Lq)
+            ssq_q = __fadd_rn(ssq_q, chunk_ssq(v, p.inv_lq));
+        else if (i < Lq + Lkv)
+            ssq_kv = __fadd_rn(ssq_kv, chunk_ssq(v, p.inv_lkv));
+    };
+    // One split: kB of the lane's loads in flight before any is used (the
+    // shared-memory stores would otherwise keep each load behind the last).
+    constexpr int kB = 6;
+    for (int i0 = lane * 4; splits == 1 && i0 < NA; i0 += 128 * kB) {
+        float4 a[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+            if (i0 + 128 * u < NA) a[u] = *reinterpret_cast<const float4*>(prow + i0 + 128 * u);
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+            if (i0 + 128 * u < NA) take4(i0 + 128 * u, a[u]);
+    }
+    for (int i = lane * 4; splits > 1 && i < NA; i += 128) {
         float4 a = *reinterpret_cast<const float4*>(prow + i), cmp = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int sp = 1; sp < splits; ++sp) {
             const float4 r = *reinterpret_cast<const float4*>(prow + sp * sstride + i);
@@ -298,16 +321,8 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
             two_sum_add(a.z, cmp.z, r.z);
             two_sum_add(a.w, cmp.w, r.w);
         }
-        if (splits > 1)
-            a = make_float4(__fadd_rn(a.x, cmp.x), __fadd_rn(a.y, cmp.y), __fadd_rn(a.z, cmp.z), __fadd_rn(a.w, cmp.w));
-        const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
-        *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
-        const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
-        // chunk i / 4 on lane (i / 4) % 32, in increasing order (chunk_ssq)
-        if (i < Lq)
-            ssq_q = __fadd_rn(ssq_q, chunk_ssq(v, p.inv_lq));
-        else if (i < Lq + Lkv)
-            ssq_kv = __fadd_rn(ssq_kv, chunk_ssq(v, p.inv_lkv));
+        a = make_float4(__fadd_rn(a.x, cmp.x), __fadd_rn(a.y, cmp.y), __fadd_rn(a.z, cmp.z), __fadd_rn(a.w, cmp.w));
+        take4(i, a);
     }
     ssq_q = lane_butterfly_sum(ssq_q);
     ssq_kv = lane_butterfly_sum(ssq_kv);
