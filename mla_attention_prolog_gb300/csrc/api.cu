@@ -714,6 +714,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         return MLA_OK;
     }
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
+    // one split: the compression writes the BF16 row and the norm reads it
     if (h->cpair) {
         CompressParams pp = pa;
         pp.bn = kPairCompressBN;
@@ -721,12 +722,17 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         pp.m_tiles = h->cpair_m_tiles;
         pp.splits = h->cpair_splits;
         pp.job_table = h->cpair_table;
+        pp.out_bf16 = pp.splits == 1;
         pn.splits = h->cpair_splits;
+        pn.in_bf16 = pp.out_bf16;
         if ((e = launch_compress_pair(h->cpair_grid, h->tm_x, h->tm_wa2, pp, st)) != cudaSuccess)
             return cuda_fail(e, "launch mla_compress_pair_kernel");
-    } else if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
-               cudaSuccess) {
-        return cuda_fail(e, "launch mla_compress_kernel");
+    } else {
+        pa.out_bf16 = pa.splits == 1;
+        pn.in_bf16 = pa.out_bf16;
+        if ((e = launch_compress(h->shape_a, jobs_a < h->sms ? jobs_a : h->sms, h->tm_x, h->tm_wa, pa, st)) !=
+            cudaSuccess)
+            return cuda_fail(e, "launch mla_compress_kernel");
     }
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");

@@ -975,7 +975,23 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
             }
             if (!ok) break;
             const int t = m0 + rank * kBM + row;
-            if (t < p.T) {
+            if (t < p.T && p.out_bf16) {  // one split: the BF16 row the norm reads
+                uint16_t* dst = reinterpret_cast<uint16_t*>(p.partials) + static_cast<size_t>(t) * p.NA + n0 +
+                                half * HALF;
+#pragma unroll
+                for (int c = 0; c < HALF; c += 8) {
+                    if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA) {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2)
+                            upk2(COMP ? add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0]) : acc[(c + e) / 2], o[e],
+                                 o[e + 1]);
+                        *reinterpret_cast<uint4*>(dst + c) = make_uint4(
+                            pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                            pack_bf16x2(o[6], o[7]));
+                    }
+                }
+            } else if (t < p.T) {
                 float* dst = p.partials + (static_cast<size_t>(split) * p.T + t) * p.NA + n0 + half * HALF;
 #pragma unroll
                 for (int c = 0; c < HALF; c += 8) {

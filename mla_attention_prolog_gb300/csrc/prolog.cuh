@@ -41,6 +41,9 @@ struct CompressParams {
     int* status;
     uint64_t timeout_ns;
     const int* job_table;  // balanced per-CTA job lists (null: round robin)
+    // One split (splits == 1): write the sums as the BF16 row the norm would
+    // round them to, [T][NA] BF16 in the partials buffer, instead of FP32.
+    int out_bf16;
     // A byte range the kernel asks L2 to fetch from HBM while it runs (the
     // expansion weights of a decode batch; null: none), in pieces of 32 KB
     // issued by the producer warp's spare lanes.
@@ -53,6 +56,7 @@ struct CompressParams {
 struct NormRopeParams {
     const float* partials;  // [splits][T][NA]
     int splits, T, NA, Lq, Lkv, R, H, Dn;
+    int in_bf16;            // one split written as BF16 [T][NA] (CompressParams::out_bf16)
     float inv_lq, inv_lkv, eps;
     const uint16_t* gamma;  // [Lq + Lkv]
     const int32_t* positions;

@@ -303,7 +303,20 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
     // One split: kB of the lane's loads in flight before any is used (the
     // shared-memory stores would otherwise keep each load behind the last).
     constexpr int kB = 6;
-    for (int i0 = lane * 4; splits == 1 && i0 < NA; i0 += 128 * kB) {
+    if (p.in_bf16) {  // the compression already rounded the row to BF16
+        const uint16_t* brow = reinterpret_cast<const uint16_t*>(prow);
+        for (int i0 = lane * 4; i0 < NA; i0 += 128 * kB) {
+            uint2 a[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+                if (i0 + 128 * u < NA) a[u] = *reinterpret_cast<const uint2*>(brow + i0 + 128 * u);
+#pragma unroll
+            for (int u = 0; u < kB; ++u)
+                if (i0 + 128 * u < NA)
+                    take4(i0 + 128 * u, make_float4(bf16_lo(a[u].x), bf16_hi(a[u].x), bf16_lo(a[u].y), bf16_hi(a[u].y)));
+        }
+    }
+    for (int i0 = lane * 4; splits == 1 && !p.in_bf16 && i0 < NA; i0 += 128 * kB) {
         float4 a[kB];
 #pragma unroll
         for (int u = 0; u < kB; ++u)

@@ -46,8 +46,12 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
     const int t = blockIdx.x * kNormWarpTokens + warp;
     if (t >= p.T) return;  // warp-uniform
     const int pos = p.positions[t];
+    // the row of token t: FP32 partials, or (in_bf16) the BF16 row, at element t * NA of its type
+    const float* prow = p.in_bf16 ? reinterpret_cast<const float*>(reinterpret_cast<const uint16_t*>(p.partials) +
+                                                                   static_cast<size_t>(t) * p.NA)
+                                  : p.partials + static_cast<size_t>(t) * p.NA;
     norm_token_warp(p, t, pos, p.cos_sin + static_cast<size_t>(pos >= 0 && pos < p.max_pos ? pos : 0) * p.R,
-                    p.gamma, p.partials + static_cast<size_t>(t) * p.NA, static_cast<size_t>(p.T) * p.NA, p.splits,
+                    p.gamma, prow, static_cast<size_t>(p.T) * p.NA, p.splits,
                     wsm + static_cast<size_t>(warp) * (p.NA + p.R));
 }
 
