@@ -154,7 +154,7 @@ class ClockSampler:
 
 # ------------------------------------------------------ per-kernel accounting
 
-def kernel_work(d: wl.Dims, cache: bool = False):
+def kernel_work(d: wl.Dims, cache: bool = False, names=()):
     """Algorithmic bytes and flops attributed to each kernel of one run.
 
     Bytes: every input a kernel must read once plus every output it must write
@@ -186,6 +186,13 @@ def kernel_work(d: wl.Dims, cache: bool = False):
     f["mla_compress_pair_kernel"] = f["mla_compress_kernel"]
     b["mla_expand_pair_kernel"] = b["mla_expand_kernel"]
     f["mla_expand_pair_kernel"] = f["mla_expand_kernel"]
+    if "mla_expand_kv_pair_kernel" in names:
+        # the kv tiles on their own pair kernel; the pair expansion keeps the q tiles
+        b_kv = 2 * d.n_kv * d.kv_lora_rank + 2 * T * H * Dn + 2 * T * H * Dv
+        b["mla_expand_kv_pair_kernel"] = b_kv
+        f["mla_expand_kv_pair_kernel"] = 2 * T * d.n_kv * d.kv_lora_rank
+        b["mla_expand_pair_kernel"] = b["mla_expand_kernel"] - b_kv
+        f["mla_expand_pair_kernel"] = 2 * T * d.n_q * d.q_lora_rank
     # the cluster kernel runs the compression and the norm step
     b["mla_compress_norm_kernel"] = b["mla_compress_kernel"] + b["mla_norm_rope_kernel"]
     f["mla_compress_norm_kernel"] = f["mla_compress_kernel"]
@@ -424,7 +431,7 @@ def run_gpu(args):
     tokens = d.T * K * world
     value = tokens / (ms_total / 1e3)
     peaks, peak_src = load_peaks()
-    kb, kf = kernel_work(d, cached)
+    kb, kf = kernel_work(d, cached, names)
     dom = max(per_kernel, key=per_kernel.get)
     dom_ms = per_kernel[dom]
     if w.bound == "tensor":

@@ -346,6 +346,19 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            stores must be on for 1 to take effect).
  *                            INVALID_ARG when 1 is not available. */
 #define MLA_TUNE_Q_WIDE 11
+/*   MLA_TUNE_KV_RESIDENT     prefill on CTA pairs with kv tiles of 256 columns
+ *                            and Lkv <= 512: 1 (the default when there are at
+ *                            least as many groups of 8 kv tiles x 256-token
+ *                            tiles as SMs, where it measured faster): the kv
+ *                            tiles run on their own kernel, which keeps a
+ *                            256-token tile's normed c_kv rows in shared
+ *                            memory and streams only the weights for a group
+ *                            of 8 kv tiles; 0: the kv
+ *                            tiles share the pair expansion kernel with the q
+ *                            tiles.  Same values either way (the tensor
+ *                            stores must be on for 1 to take effect).
+ *                            INVALID_ARG when 1 is not available. */
+#define MLA_TUNE_KV_RESIDENT 12
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

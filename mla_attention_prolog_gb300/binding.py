@@ -45,6 +45,7 @@ TUNE_TMA_STORE = 8
 TUNE_COMPRESS_TILE = 9
 TUNE_L2_FETCH = 10
 TUNE_Q_WIDE = 11
+TUNE_KV_RESIDENT = 12
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -74,10 +74,9 @@ bool encode_store(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-constexpr int kKernelCount = 4;  // most kernels one run launches (timing-hook events: + 1)
+constexpr int kKernelCount = 5;  // most kernels one run launches (timing-hook events: + 1)
+constexpr int kKvResGroup = 8;   // kv tiles per super-job of the kv-resident pair kernel
 constexpr int kPairCompressBN = 256;                // the compression pair kernel's tile width
-const char* const kKernelNames[kKernelCount] = {"mla_compress_kernel", "mla_norm_rope_kernel",
-                                                "mla_expand_kernel", "mla_quant_kernel"};
 
 const char* const kClusterKernelNames[3] = {"mla_compress_norm_kernel", "mla_expand_kernel", "mla_quant_kernel"};
 const char* const kFusedKernelName = "mla_decode_kernel";
@@ -141,6 +140,9 @@ struct mla_prolog {
     CUtensorMap tm_wqbw{};  // W_q_b in boxes of half a wide q tile (pairs with q_wide)
     bool q_wide_ok = false;  // pairs: q tiles of kQWide columns across heads possible
     bool q_wide = false;     // in use (tunable)
+    bool kvres_ok = false;   // pairs: kv tiles with the activations resident possible
+    bool kvres = false;      // in use (tunable)
+    int kvres_grid = 0;      // CTA pairs of that kernel
     // the expansion epilogue's bulk tensor stores (kernels with a staging area)
     bool l2_fetch = false;  // decode: the compression kernel fetches W_b into L2 (tunable)
     bool ts_ok = false;     // the dims allow them
@@ -160,6 +162,10 @@ namespace {
 // Puts the prefill compression plan of weight-tile width `bn` in use; false
 // when there is none of that width.  The W_a tensor map is re-encoded (its
 // box is one tile high) on the next run.
+// Whether the kv tiles run on the kv-resident pair kernel (with the pair
+// expansion): its epilogue writes through tensor stores.
+bool kvres_active(mla_prolog_t h) { return h->kvres && h->tma_store; }
+
 bool select_compress_tile(mla_prolog_t h, int bn) {
     for (const auto& ct : h->ctile) {
         if (ct.bn != bn || bn == 0) continue;
@@ -451,6 +457,22 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // 2191 -> 2066 us): 32 KB of operands per SM per 4.2 MFLOP K block
     // instead of 28 KB per 3.1 MFLOP, and a quarter fewer q jobs.
     h->q_wide = h->q_wide_ok;
+    // Pairs: the kv tiles on their own kernel with the normed c_kv rows of a
+    // 256-token tile resident in shared memory (K = Lkv <= 512).
+    if (h->pair_ok && h->ts_ok && Lkv <= 512 && Lkv % kBK == 0 && h->bn_kv == 256) {
+        int active = 0;
+        if (expand_kv_pair_max_active(&active) == cudaSuccess && active >= 1) {
+            h->kvres_ok = true;
+            const int n_sj = h->pair_m_tiles * cdiv(cdiv(h->NKV, h->bn_kv), kKvResGroup);
+            h->kvres_grid = n_sj < sms / 2 ? n_sj : sms / 2;
+            // Measured on GB300: V3 prefill step 2044 -> 2009 us (1024
+            // super-jobs), with the per-head quant 1872 -> 1827 us; V2-Lite
+            // prefill 42.4 -> 53.4 us (32 super-jobs for 76 pairs).  On when
+            // every pair gets at least two.
+            h->kvres = n_sj >= sms;
+        }
+        cudaGetLastError();
+    }
     // Decode: W_b fetched into L2 behind the compression's last loads.
     // Measured on GB300 (step time, weights from HBM every step): V3 decode
     // (110 MB of W_b) 49.1 -> 48.1 us; V2-Lite decode (4 MB) 16.4 -> 18.6 us.
@@ -737,29 +759,45 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
     if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+    int ev = 3;  // next timing-hook event
     if (h->pair) {
         ExpandParams pp = pb;
         pp.m_tiles = h->pair_m_tiles;
         pp.job_table = nullptr;
+        const bool kvres = kvres_active(h);
+        if (kvres) pp.nkv_tiles = 0;  // the kv tiles go to the kv-resident kernel
         const bool wide = h->q_wide && h->tma_store;
-        int grid = h->pair_grid;
         if (wide) {
             pp.q_wide = 1;
             pp.nq_tiles = h->NQ / kQWide;
-            const int jobs = (pp.nq_tiles + pp.nkv_tiles) * pp.m_tiles;
-            grid = jobs < h->sms / 2 ? jobs : h->sms / 2;
         }
-        if ((e = launch_expand_pair(grid, h->tm_nq, h->tm_nkv, wide ? h->tm_wqbw : h->tm_wqb2, h->tm_wkvb2, h->tm_out,
-                                    pp, st)) != cudaSuccess)
-            return cuda_fail(e, "launch mla_expand_pair_kernel");
-    } else if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, h->tm_out, pb,
-                                  st)) != cudaSuccess) {
-        return cuda_fail(e, "launch mla_expand_kernel");
+        const int jobs = (pp.nq_tiles + pp.nkv_tiles) * pp.m_tiles;
+        const int grid = jobs < h->sms / 2 ? jobs : h->sms / 2;
+        if (jobs > 0) {
+            if ((e = launch_expand_pair(grid, h->tm_nq, h->tm_nkv, wide ? h->tm_wqbw : h->tm_wqb2, h->tm_wkvb2,
+                                        h->tm_out, pp, st)) != cudaSuccess)
+                return cuda_fail(e, "launch mla_expand_pair_kernel");
+            if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        }
+        if (kvres) {
+            ExpandParams pk = pb;
+            pk.m_tiles = h->pair_m_tiles;
+            pk.nq_tiles = 0;
+            pk.job_table = nullptr;
+            if ((e = launch_expand_kv_pair(h->kvres_grid, h->tm_nkv, h->tm_wkvb2, h->tm_out, pk, kKvResGroup, st)) !=
+                cudaSuccess)
+                return cuda_fail(e, "launch mla_expand_kv_pair_kernel");
+            if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        }
+    } else {
+        if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, h->tm_out, pb,
+                               st)) != cudaSuccess)
+            return cuda_fail(e, "launch mla_expand_kernel");
+        if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     }
-    if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if (pq.rows > 0) {
         if ((e = launch_quant(pq, st, true)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
-        if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     }
     return MLA_OK;
 }
@@ -846,21 +884,39 @@ bool quant_kernel_runs(mla_prolog_t h) {
     const bool per_head = (h->d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;
     return h->d.q_lora_rank > 0 && !per_head;
 }
+
+// The kernels of the standard path (compression, norm, expansion, quant),
+// in launch order, with the current tuning; returns how many.
+int standard_kernels(mla_prolog_t h, const char* (&names)[kKernelCount]) {
+    int n = 0;
+    names[n++] = h->cpair ? "mla_compress_pair_kernel" : "mla_compress_kernel";
+    names[n++] = "mla_norm_rope_kernel";
+    if (h->pair && kvres_active(h)) {
+        if (h->d.q_lora_rank > 0) names[n++] = "mla_expand_pair_kernel";
+        names[n++] = "mla_expand_kv_pair_kernel";
+    } else {
+        names[n++] = h->pair ? "mla_expand_pair_kernel" : "mla_expand_kernel";
+    }
+    if (quant_kernel_runs(h)) names[n++] = "mla_quant_kernel";
+    return n;
+}
 }  // namespace
 
 int32_t mla_prolog_kernel_count(mla_prolog_t h) {
     if (!h) return 0;
     if (h->fused) return 1;
-    return (h->cluster ? 2 : 3) + (quant_kernel_runs(h) ? 1 : 0);
+    if (h->cluster) return 2 + (quant_kernel_runs(h) ? 1 : 0);
+    const char* names[kKernelCount];
+    return standard_kernels(h, names);
 }
 
 const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i) {
     if (!h || i < 0 || i >= mla_prolog_kernel_count(h)) return "";
     if (h->fused) return kFusedKernelName;
     if (h->cluster) return kClusterKernelNames[i];
-    if (i == 0 && h->cpair) return "mla_compress_pair_kernel";
-    if (i == 2 && h->pair) return "mla_expand_pair_kernel";
-    return kKernelNames[i];
+    const char* names[kKernelCount];
+    standard_kernels(h, names);
+    return names[i];
 }
 
 int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream) {
@@ -917,6 +973,7 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->pair_ok) return MLA_ERR_INVALID_ARG;
             h->pair = value == 1;
+            h->n_events = 0;
             return MLA_OK;
         case MLA_TUNE_COMPRESS_TILE:
             if (h->decode || h->cluster || h->fused) return MLA_ERR_INVALID_ARG;
@@ -931,10 +988,17 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value == 1 && !h->q_wide_ok) return MLA_ERR_INVALID_ARG;
             h->q_wide = value == 1;
             return MLA_OK;
+        case MLA_TUNE_KV_RESIDENT:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->kvres_ok) return MLA_ERR_INVALID_ARG;
+            h->kvres = value == 1;
+            h->n_events = 0;  // the kernel count may change: re-arm the timing hook
+            return MLA_OK;
         case MLA_TUNE_TMA_STORE:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->ts_ok) return MLA_ERR_INVALID_ARG;
             h->tma_store = value == 1;
+            h->n_events = 0;  // the kernel count may change: re-arm the timing hook
             return MLA_OK;
         case MLA_TUNE_CLUSTER_NORM:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;

@@ -1128,4 +1128,217 @@ __device__ __forceinline__ void gemm_finish(const Smem& sm, uint32_t tmem, const
     gemm_teardown<BN_MAX, STAGES, CG>(sm, tmem);
 }
 
+// ---- kv tiles of the prefill expansion on CTA pairs, activations resident --
+//
+// A kv tile has K = Lkv <= 512, so a pair's 256 token rows of normed c_kv
+// (128 KB per CTA) fit in shared memory.  A super-job (pair token tile m,
+// a group of kv tiles) loads them once and then streams only the weight
+// halves (16 KB per CTA per K block) through a 4-stage ring, one TMEM
+// accumulator chain per kv tile; the epilogue is the kv epilogue through the
+// store ring.  The next super-job's activation K block k is loaded as soon as
+// the last tile of the current one has consumed slot k, interleaved with the
+// first weight blocks, so the switch costs no pipeline drain.
+constexpr int kKvResKb = 8;              // resident K blocks (Lkv <= 8 * 64)
+constexpr int kKvResStages = 4;          // weight ring
+constexpr int kKvResA = kBM * kBK * 2;   // 16 KB: 128 token rows of one K block
+constexpr int kKvResB = 128 * kBK * 2;   // 16 KB: half of a 256-row weight tile
+
+struct KvResLayout {
+    static constexpr int B_OFF = kKvResKb * kKvResA;                  // 128 KB of activations first
+    static constexpr int STAGE_OFF = B_OFF + kKvResStages * kKvResB;  // then the ring (64 KB)
+    static constexpr int BAR_OFF = STAGE_OFF + kStoreStageBytes;      // then the store staging (32 KB)
+    // a_full[8], a_empty[8], b_full[4], b_empty[4], acc_full[2], acc_empty[2], done
+    static constexpr int MISC = BAR_OFF + (2 * kKvResKb + 2 * kKvResStages + 5) * 8;
+    static constexpr int BYTES = MISC + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
+};
+
+struct KvResSmem {
+    Smem s;  // ring = weight stages (full0 / empty0), stage, accumulator barriers, TMEM slot
+    uint32_t a, afull0, aempty0;
+};
+
+__device__ __forceinline__ KvResSmem kvres_carve(uint8_t* raw_ptr) {
+    using L = KvResLayout;
+    const uint32_t raw = smem_u32(raw_ptr);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+    KvResSmem k;
+    k.a = raw + pad;
+    k.s.base = k.a + L::B_OFF;
+    k.s.stage = k.a + L::STAGE_OFF;
+    k.afull0 = k.a + L::BAR_OFF;
+    k.aempty0 = k.afull0 + 8 * kKvResKb;
+    k.s.full0 = k.aempty0 + 8 * kKvResKb;
+    k.s.empty0 = k.s.full0 + 8 * kKvResStages;
+    k.s.accf0 = k.s.empty0 + 8 * kKvResStages;
+    k.s.acce0 = k.s.accf0 + 16;
+    k.s.done = k.s.acce0 + 16;
+    k.s.tmem_slot = reinterpret_cast<uint32_t*>(raw_ptr + pad + L::MISC);
+    k.s.abort_flag = reinterpret_cast<volatile int*>(raw_ptr + pad + L::MISC + 4);
+    return k;
+}
+
+__device__ __forceinline__ uint32_t kvres_setup(const KvResSmem& k) {
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kKvResKb; ++i) {
+            mbar_init(k.afull0 + 8 * i, 1);
+            mbar_init(k.aempty0 + 8 * i, 1);
+        }
+        for (int s = 0; s < kKvResStages; ++s) {
+            mbar_init(k.s.full0 + 8 * s, 1);
+            mbar_init(k.s.empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(k.s.accf0 + 8 * b, 1);
+            mbar_init(k.s.acce0 + 8 * b, kExpandEpiWarps * 2);
+        }
+        mbar_init(k.s.done, 1);
+        *k.s.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if ((threadIdx.x >> 5) == 1) {
+        tmem_alloc_pair(smem_u32(k.s.tmem_slot), KvResLayout::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    return *k.s.tmem_slot;
+}
+
+// Super-job sj -> (pair token tile m, first kv tile, tiles in the group).
+__device__ __forceinline__ void kvres_job(const ExpandParams& p, int group, int sj, int& m, int& t0, int& nt) {
+    const int ngroups = (p.nkv_tiles + group - 1) / group;
+    m = sj / ngroups;
+    t0 = (sj - m * ngroups) * group;
+    nt = p.nkv_tiles - t0 < group ? p.nkv_tiles - t0 : group;
+}
+
+// This pair's super-jobs: unit + i * units.  Returns false when a wait gave up.
+__device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t tmem, const CUtensorMap* tm_akv,
+                                                   const CUtensorMap* tm_bkv, const ExpandParams& p,
+                                                   const OutMaps& om, int group, RoleCounters& rc) {
+    const Smem& sm = k.s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool leader = rank == 0;
+    const int unit = static_cast<int>(blockIdx.x) / 2, units = static_cast<int>(gridDim.x) / 2;
+    const int n_sj = p.m_tiles * ((p.nkv_tiles + group - 1) / group);
+    const int kb = p.kb_kv;
+    bool ok = true;
+    pdl_wait();  // the normed rows come from the norm kernel; amax clearing precedes the epilogue
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tensormap(tm_akv);
+            prefetch_tensormap(tm_bkv);
+            uint32_t sjn = 0;
+            int a_last = 0;  // activation blocks issued for the latest super-job
+            auto b_load = [&](int tile, int kk) -> bool {
+                const uint32_t l = rc.loads;
+                const int s = static_cast<int>(l % kKvResStages);
+                if (!mbar_wait(sm.empty0 + 8 * s, ((l / kKvResStages) & 1) ^ 1, p.timeout_ns, sm.abort_flag))
+                    return false;
+                if (leader) mbar_arrive_expect_tx(sm.full0 + 8 * s, 2 * kKvResB);
+                tma_load_2d_pair(sm.base + s * kKvResB, tm_bkv, map_shared_rank(sm.full0 + 8 * s, 0), kk * kBK,
+                                 tile * 256 + rank * 128);
+                ++rc.loads;
+                return true;
+            };
+            for (int sj = unit; sj < n_sj && ok; sj += units, ++sjn) {
+                int m, t0, nt;
+                kvres_job(p, group, sj, m, t0, nt);
+                a_last = 0;
+                for (int kk = 0; kk < kb && ok; ++kk) {
+                    // activation block kk, once the previous super-job's last tile is done with it
+                    if (!mbar_wait(k.aempty0 + 8 * kk, (sjn & 1) ^ 1, p.timeout_ns, sm.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(k.afull0 + 8 * kk, 2 * kKvResA);
+                    tma_load_2d_pair(k.a + kk * kKvResA, tm_akv, map_shared_rank(k.afull0 + 8 * kk, 0), kk * kBK,
+                                     m * 256 + rank * 128);
+                    ++a_last;
+                    ok = b_load(t0, kk);
+                }
+                for (int h = 1; h < nt && ok; ++h)
+                    for (int kk = 0; kk < kb && ok; ++kk) ok = b_load(t0 + h, kk);
+            }
+            if (!ok) raise_abort(sm, p.status);
+            // no activation copy may still be landing when the CTA leaves: the
+            // last super-job's blocks (the leader's barriers count both CTAs)
+            // (the loop's increment also runs after an abort: super-job sjn - 1
+            // issued the latest blocks)
+            if (leader && sjn > 0)
+                for (int kk = 0; kk < a_last; ++kk)
+                    mbar_wait(k.afull0 + 8 * kk, (sjn - 1) & 1, p.timeout_ns, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            const uint32_t idesc = idesc_bf16_f32(256, 256);
+            uint32_t sjn = 0;
+            for (int sj = unit; sj < n_sj && ok; sj += units, ++sjn) {
+                int m, t0, nt;
+                kvres_job(p, group, sj, m, t0, nt);
+                for (int h = 0; h < nt && ok; ++h, ++rc.chain) {
+                    const uint32_t b = rc.chain & 1;
+                    if (!mbar_wait(sm.acce0 + 8 * b, ((rc.chain >> 1) & 1) ^ 1, p.timeout_ns, sm.abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dacc = tmem + b * 256;
+                    for (int kk = 0; kk < kb; ++kk, ++rc.consumed) {
+                        if (h == 0 && !mbar_wait(k.afull0 + 8 * kk, sjn & 1, p.timeout_ns, sm.abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const int s = static_cast<int>(rc.consumed % kKvResStages);
+                        if (!mbar_wait(sm.full0 + 8 * s, (rc.consumed / kKvResStages) & 1, p.timeout_ns,
+                                       sm.abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t ad = smem_desc_sw128(k.a + kk * kKvResA);
+                        const uint64_t bd = smem_desc_sw128(sm.base + s * kKvResB);
+#pragma unroll
+                        for (int q = 0; q < kBK / 16; ++q)
+                            mma_bf16_pair(dacc, ad + 2 * q, bd + 2 * q, idesc, (kk == 0 && q == 0) ? 0u : 1u);
+                        mma_commit_pair(sm.empty0 + 8 * s, 0x3);
+                        if (h == nt - 1) mma_commit_pair(k.aempty0 + 8 * kk, 0x3);
+                    }
+                    if (ok) mma_commit_pair(sm.accf0 + 8 * b, 0x3);
+                }
+            }
+            if (!ok) raise_abort(sm, p.status);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int half_idx = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes};
+        RowCtx ctx;
+        for (int sj = unit; sj < n_sj && ok; sj += units) {
+            int m, t0, nt;
+            kvres_job(p, group, sj, m, t0, nt);
+            load_row_ctx(p, m * 256 + rank * kBM + row, ctx);
+            const int y0 = m * 256 + rank * kBM + quarter * 32;
+            for (int h = 0; h < nt; ++h, ++rc.chain) {
+                if (!epi_acquire(sm, rc.chain, p.timeout_ns)) {
+                    if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
+                    ok = false;
+                    break;
+                }
+                const uint32_t tbase = tmem + lane_off + (rc.chain & 1) * 256;
+                expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (t0 + h) * p.bn_kv, half_idx, y0);
+                epi_release<2>(sm, rc.chain);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+    return ok;
+}
+
 }  // namespace mlap

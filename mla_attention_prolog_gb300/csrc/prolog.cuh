@@ -484,6 +484,12 @@ cudaError_t launch_compress_pair(int pairs, const CUtensorMap& tm_x, const CUten
 cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
                                const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
                                const ExpandParams& p, cudaStream_t st);
+// The kv tiles of the prefill expansion on CTA pairs with the normed c_kv
+// rows resident in shared memory (Lkv <= 512, 256-wide kv tiles, kv outputs
+// through tensor stores): super-jobs of `group` kv tiles per 256-token tile.
+cudaError_t expand_kv_pair_max_active(int* clusters);
+cudaError_t launch_expand_kv_pair(int pairs, const CUtensorMap& tm_akv, const CUtensorMap& tm_bkv,
+                                  const OutTensorMaps& om, const ExpandParams& p, int group, cudaStream_t st);
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);

@@ -521,3 +521,42 @@ def test_wide_q_tiles_match_head_tiles(T, extra):
     with pytest.raises(binding.MlaPrologError):
         q.set_tuning(binding.TUNE_Q_WIDE, 1)
     q.close()
+
+
+@pytest.mark.parametrize("name,T,extra", [("v3_prefill", 640, 0), ("v3_prefill", 385, wl.QUANT_PER_HEAD),
+                                          ("v2lite_prefill", 300, 0), ("v2lite_prefill", 0, 0)],
+                         ids=["v3_T640", "v3_T385_per_head", "v2l_T300", "v2l_full"])
+def test_kv_resident_matches_pair_kernel(name, T, extra):
+    """The kv tiles on the kv-resident pair kernel (activations loaded once per
+    group of kv tiles) give the same bytes as on the pair expansion kernel,
+    within the bar of the oracle, guard bands intact."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    d = dataclasses.replace(d, flags=d.flags | extra)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    p.set_tuning(binding.TUNE_PAIR_EXPAND, 1)
+    outs = []
+    for f in (1, 0):
+        p.set_tuning(binding.TUNE_KV_RESIDENT, f)
+        names = p.kernel_names()
+        assert ("mla_expand_kv_pair_kernel" in names) == bool(f), names
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    _bits_equal(outs[0], outs[1])
+    tok = np.unique(np.linspace(0, d.T - 1, min(d.T, 48)).astype(np.int32))
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    a = outs[0]
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(a[k].t[sel], ref[k], k)
+    if d.q_lora_rank:
+        quant_within(a["out_q_int8"].t[sel], a["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+    for o in outs:
+        for k, g in o.items():
+            assert g.guards_intact(), k
+    p.close()
