@@ -359,6 +359,16 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            stores must be on for 1 to take effect).
  *                            INVALID_ARG when 1 is not available. */
 #define MLA_TUNE_KV_RESIDENT 12
+/*   MLA_TUNE_QUANT_OVERLAP   with the kv-resident kernel and the per-token
+ *                            quant: 1 (the default): the quant kernel, which
+ *                            needs only the q tiles, runs on an internal
+ *                            low-priority stream beside the kv kernel (forked
+ *                            from and joined back to the caller's stream
+ *                            with events, which stream capture follows);
+ *                            0: after it on the caller's stream.  Not used
+ *                            while the timing hook is armed.  INVALID_ARG
+ *                            when 1 is not available. */
+#define MLA_TUNE_QUANT_OVERLAP 13
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

@@ -46,6 +46,7 @@ TUNE_COMPRESS_TILE = 9
 TUNE_L2_FETCH = 10
 TUNE_Q_WIDE = 11
 TUNE_KV_RESIDENT = 12
+TUNE_QUANT_OVERLAP = 13
 
 
 class MlaPrologDims(ctypes.Structure):

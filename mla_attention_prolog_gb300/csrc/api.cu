@@ -154,6 +154,11 @@ struct mla_prolog {
     const void* last_wa = nullptr;
     const void* last_wb = nullptr;
     cudaEvent_t events[kKernelCount + 1] = {};
+    // The per-token quant beside the kv-resident kernel: an internal
+    // low-priority stream, forked from and joined back to the caller's.
+    bool quant_overlap = false;  // in use (tunable; needs the kv-resident kernel)
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
     int n_events = 0;
 };
 
@@ -485,6 +490,20 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         delete h;
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(workspace)");
     }
+    if (h->kvres_ok && Lq > 0 && !per_head) {
+        int least = 0, greatest = 0;
+        if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
+            (e = cudaStreamCreateWithPriority(&h->side, cudaStreamNonBlocking, least)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h->fork_ev, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h->join_ev, cudaEventDisableTiming)) != cudaSuccess) {
+            if (h->side) cudaStreamDestroy(h->side);
+            if (h->fork_ev) cudaEventDestroy(h->fork_ev);
+            cudaFree(h->ws);
+            delete h;
+            return cuda_fail(e, "side stream for the quant");
+        }
+        h->quant_overlap = true;
+    }
     *out = h;
     return MLA_OK;
 }
@@ -495,6 +514,9 @@ int mla_prolog_destroy(mla_prolog_t h) {
     cudaGetDevice(&dev);
     if (dev != h->device) cudaSetDevice(h->device);
     cudaDeviceSynchronize();
+    if (h->side) cudaStreamDestroy(h->side);
+    if (h->fork_ev) cudaEventDestroy(h->fork_ev);
+    if (h->join_ev) cudaEventDestroy(h->join_ev);
     if (h->ws) cudaFree(h->ws);
     if (dev >= 0 && dev != h->device) cudaSetDevice(dev);
     delete h;
@@ -779,6 +801,15 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
                 return cuda_fail(e, "launch mla_expand_pair_kernel");
             if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
         }
+        // With the kv tiles on their own kernel the quant needs only the q
+        // tiles: it runs on the side stream beside the kv kernel (not with
+        // the timing hook, whose events time the kernels one after another).
+        const bool overlap = kvres && pq.rows > 0 && h->quant_overlap && h->side && !timed && jobs > 0;
+        if (overlap) {
+            if ((e = cudaEventRecord(h->fork_ev, st)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+            if ((e = cudaStreamWaitEvent(h->side, h->fork_ev, 0)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamWaitEvent(fork)");
+        }
         if (kvres) {
             ExpandParams pk = pb;
             pk.m_tiles = h->pair_m_tiles;
@@ -788,6 +819,13 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
                 cudaSuccess)
                 return cuda_fail(e, "launch mla_expand_kv_pair_kernel");
             if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+        }
+        if (overlap) {
+            if ((e = launch_quant(pq, h->side, false)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_kernel");
+            if ((e = cudaEventRecord(h->join_ev, h->side)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
+            if ((e = cudaStreamWaitEvent(st, h->join_ev, 0)) != cudaSuccess)
+                return cuda_fail(e, "cudaStreamWaitEvent(join)");
+            return MLA_OK;
         }
     } else {
         if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, h->tm_out, pb,
@@ -987,6 +1025,11 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->q_wide_ok) return MLA_ERR_INVALID_ARG;
             h->q_wide = value == 1;
+            return MLA_OK;
+        case MLA_TUNE_QUANT_OVERLAP:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && !h->side) return MLA_ERR_INVALID_ARG;
+            h->quant_overlap = value == 1;
             return MLA_OK;
         case MLA_TUNE_KV_RESIDENT:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
