@@ -560,3 +560,35 @@ def test_kv_resident_matches_pair_kernel(name, T, extra):
         for k, g in o.items():
             assert g.guards_intact(), k
     p.close()
+
+
+def test_quant_beside_kv_kernel_keeps_outputs():
+    """The per-token quant on the side stream beside the kv-resident kernel
+    (forked and joined with events, also inside a CUDA graph) writes the same
+    bytes as the quant after it, and the caller's stream sees them."""
+    w = wl.WORKLOADS["v3_prefill"]
+    d = w.dims.with_T(4096)  # enough (token tile, kv group) jobs for the kv-resident kernel
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    assert "mla_expand_kv_pair_kernel" in p.kernel_names(), p.kernel_names()
+    outs = []
+    for f in (1, 0):
+        p.set_tuning(binding.TUNE_QUANT_OVERLAP, f)
+        o = alloc_outputs(d, DEV)
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            run_prolog(p, dins, o)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                run_prolog(p, dins, o)
+            o["out_q_int8"].t.zero_()
+            g.replay()
+        st.synchronize()
+        assert p.device_status() == 0
+        outs.append(o)
+    _bits_equal(outs[0], outs[1])
+    for o in outs:
+        for k, gd in o.items():
+            assert gd.guards_intact(), k
+    p.close()
