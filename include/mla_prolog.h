@@ -369,6 +369,11 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            while the timing hook is armed.  INVALID_ARG
  *                            when 1 is not available. */
 #define MLA_TUNE_QUANT_OVERLAP 13
+/*   MLA_TUNE_KV_GROUP        kv tiles per super-job of the kv-resident kernel
+ *                            (1 .. the kv tile count; the default minimises
+ *                            the operand bytes of the busiest CTA pair).
+ *                            INVALID_ARG when that kernel is not available. */
+#define MLA_TUNE_KV_GROUP 14
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

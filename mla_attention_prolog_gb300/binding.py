@@ -47,6 +47,7 @@ TUNE_L2_FETCH = 10
 TUNE_Q_WIDE = 11
 TUNE_KV_RESIDENT = 12
 TUNE_QUANT_OVERLAP = 13
+TUNE_KV_GROUP = 14
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -75,7 +75,6 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kKernelCount = 5;  // most kernels one run launches (timing-hook events: + 1)
-constexpr int kKvResGroup = 8;   // kv tiles per super-job of the kv-resident pair kernel
 constexpr int kPairCompressBN = 256;                // the compression pair kernel's tile width
 
 const char* const kClusterKernelNames[3] = {"mla_compress_norm_kernel", "mla_expand_kernel", "mla_quant_kernel"};
@@ -142,6 +141,7 @@ struct mla_prolog {
     bool q_wide = false;     // in use (tunable)
     bool kvres_ok = false;   // pairs: kv tiles with the activations resident possible
     bool kvres = false;      // in use (tunable)
+    int kvres_group = 8;     // kv tiles per super-job (tunable)
     int kvres_grid = 0;      // CTA pairs of that kernel
     // the expansion epilogue's bulk tensor stores (kernels with a staging area)
     bool l2_fetch = false;  // decode: the compression kernel fetches W_b into L2 (tunable)
@@ -468,12 +468,14 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         int active = 0;
         if (expand_kv_pair_max_active(&active) == cudaSuccess && active >= 1) {
             h->kvres_ok = true;
-            const int n_sj = h->pair_m_tiles * cdiv(cdiv(h->NKV, h->bn_kv), kKvResGroup);
+            const int nkv_tiles = cdiv(h->NKV, h->bn_kv);
+            h->kvres_group = plan_kv_group(h->pair_m_tiles, nkv_tiles, sms / 2);
+            const int n_sj = h->pair_m_tiles * cdiv(nkv_tiles, h->kvres_group);
             h->kvres_grid = n_sj < sms / 2 ? n_sj : sms / 2;
-            // Measured on GB300: V3 prefill step 2044 -> 2009 us (1024
-            // super-jobs), with the per-head quant 1872 -> 1827 us; V2-Lite
-            // prefill 42.4 -> 53.4 us (32 super-jobs for 76 pairs).  On when
-            // every pair gets at least two.
+            // Measured on GB300 with groups of 8: V3 prefill step 2044 -> 2009
+            // us, with the per-head quant 1872 -> 1827 us.  On when every pair
+            // gets at least two super-jobs (the kv-only V2-Lite prefill runs
+            // one CTA per tile by default: 42.2 us, vs 41.5 us here).
             h->kvres = n_sj >= sms;
         }
         cudaGetLastError();
@@ -815,7 +817,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
             pk.m_tiles = h->pair_m_tiles;
             pk.nq_tiles = 0;
             pk.job_table = nullptr;
-            if ((e = launch_expand_kv_pair(h->kvres_grid, h->tm_nkv, h->tm_wkvb2, h->tm_out, pk, kKvResGroup, st)) !=
+            if ((e = launch_expand_kv_pair(h->kvres_grid, h->tm_nkv, h->tm_wkvb2, h->tm_out, pk, h->kvres_group, st)) !=
                 cudaSuccess)
                 return cuda_fail(e, "launch mla_expand_kv_pair_kernel");
             if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
@@ -1026,6 +1028,15 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value == 1 && !h->q_wide_ok) return MLA_ERR_INVALID_ARG;
             h->q_wide = value == 1;
             return MLA_OK;
+        case MLA_TUNE_KV_GROUP: {
+            if (value < 1 || !h->kvres_ok) return MLA_ERR_INVALID_ARG;
+            const int nkv_tiles = cdiv(h->NKV, h->bn_kv);
+            if (value > nkv_tiles) return MLA_ERR_INVALID_ARG;
+            h->kvres_group = value;
+            const int n_sj = h->pair_m_tiles * cdiv(nkv_tiles, value);
+            h->kvres_grid = n_sj < h->sms / 2 ? n_sj : h->sms / 2;
+            return MLA_OK;
+        }
         case MLA_TUNE_QUANT_OVERLAP:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
             if (value == 1 && !h->side) return MLA_ERR_INVALID_ARG;

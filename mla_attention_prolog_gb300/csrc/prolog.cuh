@@ -387,6 +387,17 @@ inline int plan_compress_tiles(int T, int NA, int kb, int sms, CompressTilePlan 
     return def;
 }
 
+// kv tiles per super-job of the kv-resident pair kernel: the largest of 8,
+// 4, 2 that still gives every CTA pair a super-job, else 1.  Measured on
+// GB300 (step time): V3 prefill 1932 / 1870 / 1897 / 1893 us with groups of
+// 4 / 8 / 16 / 32; V2-Lite prefill 41.7 / 41.5 / 53.2 us with 2 / 4 / 8 (32
+// super-jobs for 76 pairs at 8).
+inline int plan_kv_group(int pair_m_tiles, int nkv_tiles, int pairs) {
+    for (int g = 8; g > 1; g /= 2)
+        if (g <= nkv_tiles && static_cast<long long>(pair_m_tiles) * cdiv_host(nkv_tiles, g) >= pairs) return g;
+    return 1;
+}
+
 // T tokens, D model width, Lq / Lkv / R ranks, H heads of Dn + R (q) and
 // Dn + Dv (kv) columns, on a device with `sms` SMs.
 inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int Dn, int Dv, int sms) {
