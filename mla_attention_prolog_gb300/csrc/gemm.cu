@@ -139,11 +139,6 @@ using CNarrow = Layout<64, 4>;
 using C192 = Layout<192, 5>;  // 16 KB activations + 24 KB weights per stage
 using C256 = Layout<256, 4>;  // 16 KB activations + 32 KB weights per stage
 
-int gemm_smem_bytes(GemmShape s) {
-    return s == GemmShape::Wide ? EWide::BYTES : s == GemmShape::Mid ? EMid::BYTES
-                                : s == GemmShape::Deep ? EDeep::BYTES : ENarrow::BYTES;
-}
-
 cudaError_t gemm_set_attributes() {
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(mla_compress_kernel<128, 6, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

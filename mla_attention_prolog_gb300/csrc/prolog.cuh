@@ -448,7 +448,6 @@ inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int D
     return s;
 }
 
-int gemm_smem_bytes(GemmShape s);
 
 // Launches `kernel`; with `pdl` the launch may overlap the tail of the
 // previous kernel in the stream (programmatic dependent launch): the kernel
