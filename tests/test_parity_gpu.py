@@ -592,3 +592,58 @@ def test_quant_beside_kv_kernel_keeps_outputs():
         for k, gd in o.items():
             assert gd.guards_intact(), k
     p.close()
+
+
+# Unusual shapes for the prefill paths: smaller ranks, few heads, 64-wide nope
+# and value (two heads per 256-column kv tile), ragged token counts.
+_ODD_PREFILL = [
+    wl.Dims(T=700, D=1024, q_lora_rank=512, kv_lora_rank=256, rope_dim=64, num_heads=8, nope_dim=128,
+            v_dim=128, max_pos=4096, flags=wl.QUANT_Q),
+    wl.Dims(T=1100, D=768, q_lora_rank=256, kv_lora_rank=512, rope_dim=64, num_heads=16, nope_dim=64,
+            v_dim=64, max_pos=4096, flags=wl.QUANT_Q),
+]
+
+
+@pytest.mark.parametrize("d", _ODD_PREFILL, ids=["lkv256_h8", "dn64_h16"])
+def test_prefill_paths_on_unusual_shapes(d):
+    """Every prefill path on shapes other than the V2-Lite / V3 ones: the
+    compression tile widths, one head per q tile vs 256-column q tiles, kv
+    tiles on the pair kernel vs resident, the quant after vs beside the kv
+    kernel -- each within the bar of the oracle, the expansion variants bit
+    for bit equal, guard bands intact."""
+    w = wl.Workload("odd", d, positions="uniform", seed=3)
+    inp = wl.make_inputs(w)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    tok = np.unique(np.linspace(0, d.T - 1, 40).astype(np.int32))
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+
+    def run_and_check():
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        torch.cuda.synchronize()
+        for k in ("out_k", "out_v", "out_kpe"):
+            bf16_within(o[k].t[sel], ref[k], k)
+        quant_within(o["out_q_int8"].t[sel], o["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+        for k, g in o.items():
+            assert g.guards_intact(), k
+        return o
+
+    for tile in (128, 192, 256):
+        p.set_tuning(binding.TUNE_COMPRESS_TILE, tile)
+        run_and_check()
+    p.set_tuning(binding.TUNE_PAIR_EXPAND, 1)
+    base = None
+    for q_wide, kvres, overlap in ((0, 0, 0), (1, 0, 0), (1, 1, 0), (1, 1, 1), (0, 1, 1)):
+        p.set_tuning(binding.TUNE_Q_WIDE, q_wide)
+        p.set_tuning(binding.TUNE_KV_RESIDENT, kvres)
+        if kvres:
+            p.set_tuning(binding.TUNE_QUANT_OVERLAP, overlap)
+        o = run_and_check()
+        if base is None:
+            base = o
+        else:
+            _bits_equal(base, o)
+    p.close()
