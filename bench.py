@@ -78,6 +78,12 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def whole_job_tokens_per_s(tokens_per_rank: int, ms_max: float, world: int) -> float:
+    """Whole-job throughput: the tokens every rank processed over the slowest
+    rank's time (each rank runs its own replica; weak scaling)."""
+    return tokens_per_rank * world / (ms_max / 1e3)
+
+
 def barrier(world: int) -> None:
     if world > 1:
         import torch.distributed as dist
@@ -428,8 +434,7 @@ def run_gpu(args):
     clk.__exit__(None, None, None)
     clocks = clk.summary(t_wall0, t_wall1)
 
-    tokens = d.T * K * world
-    value = tokens / (ms_total / 1e3)
+    value = whole_job_tokens_per_s(d.T * K, ms_total, world)
     peaks, peak_src = load_peaks()
     kb, kf = kernel_work(d, cached, names)
     dom = max(per_kernel, key=per_kernel.get)
@@ -466,7 +471,7 @@ def run_gpu(args):
         "roofline": roof,
         "whole_step": whole,
         "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
-        "e2e": {"value": round(d.T * K_e2e * world / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(whole_job_tokens_per_s(d.T * K_e2e, e2e_ms, world), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K_e2e,
                 "pipelined": pipelined},
         "gpu_launches": K * len(active),
