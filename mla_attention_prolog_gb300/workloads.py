@@ -33,10 +33,12 @@ QUANT_Q = 1           # flag bits (the C header's MLA_PROLOG_*): INT8 quantisati
 ROPE_INTERLEAVED = 2  # rope slices de-interleaved before the rotate-half RoPE
 Q_HEAD_NORM = 4       # per-head RMSNorm (no gamma) of q before its RoPE
 QUANT_PER_HEAD = 8    # one q scale per (token, head) instead of per token
+W8A8 = 16             # INT8 weights and per-token INT8 activations in every projection
 
 # Variant names (benchmark and tests) -> flag bits; "cache" is the latent
 # KV-cache write of mla_prolog_run_cached, not a flag.
-VARIANTS = {"interleaved": ROPE_INTERLEAVED, "head_norm": Q_HEAD_NORM, "per_head": QUANT_PER_HEAD, "cache": 0}
+VARIANTS = {"interleaved": ROPE_INTERLEAVED, "head_norm": Q_HEAD_NORM, "per_head": QUANT_PER_HEAD, "cache": 0,
+            "w8a8": W8A8}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -80,6 +82,15 @@ class Dims:
     @property
     def quant_per_head(self) -> bool:
         return bool(self.flags & QUANT_PER_HEAD)
+
+    @property
+    def w8a8(self) -> bool:
+        return bool(self.flags & W8A8)
+
+    @property
+    def n_w_scales(self) -> int:
+        """Weight rows with a W8A8 scale: W_a, W_q_b (none without a q path), W_kv_b."""
+        return self.n_a + (self.n_q if self.q_lora_rank > 0 else 0) + self.n_kv
 
     @property
     def n_scales(self) -> int:
@@ -211,15 +222,51 @@ def make_inputs(wl: Workload, dims: Optional[Dims] = None, seed: Optional[int] =
     )
 
 
+@dataclasses.dataclass
+class W8A8Weights:
+    W_a: np.ndarray      # int8 [Lq+Lkv+R, D] codes, the layout of the BF16 W_a
+    W_b: np.ndarray      # int8 flat, the layout of the BF16 W_b
+    w_scale: np.ndarray  # float32 [n_w_scales]: W_a rows, W_q_b rows, W_kv_b rows
+
+    def sha256(self) -> str:
+        h = hashlib.sha256()
+        for a in (self.W_a, self.W_b, self.w_scale):
+            h.update(np.ascontiguousarray(a).tobytes())
+        return h.hexdigest()
+
+
+def make_w8a8_weights(wl: Workload, dims: Optional[Dims] = None, seed: Optional[int] = None) -> W8A8Weights:
+    """Seeded INT8 weights for the W8A8 projections, drawn on their own
+    generator (the BF16 inputs of the same seed are unchanged).
+
+    Codes are clamp(rint(N(0, 28)), -127, 127), the bell shape of a N(0, 0.02)
+    weight matrix stored with one scale per row (its largest entry near 4.5
+    standard deviations); each row's scale is 0.02 * 4.5 / 127 times U(0.8,
+    1.2).  Draw order: W_a codes, W_b codes, scales.
+    """
+    d = dims or wl.dims
+    g = torch.Generator("cpu").manual_seed((wl.seed if seed is None else seed) + 7919)
+    def codes(n):
+        return torch.clamp(torch.round(torch.randn((n,), generator=g, dtype=torch.float32) * 28.0), -127, 127)
+    wa = codes(d.n_a * d.D).to(torch.int8).numpy().reshape(d.n_a, d.D).copy()
+    wb = codes(d.w_b_elems).to(torch.int8).numpy().copy()
+    sc = (0.02 * 4.5 / 127.0) * (0.8 + 0.4 * torch.rand((d.n_w_scales,), generator=g, dtype=torch.float32))
+    return W8A8Weights(W_a=wa, W_b=wb, w_scale=sc.numpy().astype(np.float32).copy())
+
+
 # ---------------------------------------------------------------------------
 # Algorithmic work counts (inputs read once, outputs written once; GEMM flops).
 
 def algorithmic_bytes(d: Dims, cache: bool = False) -> int:
     """Every input read once + every output written once; with ``cache`` also
-    the slot indices read and the latent cache rows (Lkv + R BF16) written."""
+    the slot indices read and the latent cache rows (Lkv + R BF16) written.
+    W8A8 weights count one byte per code plus their FP32 row scales."""
     T = d.T
-    b = 2 * T * d.D + 2 * d.n_a * d.D + 2 * (d.q_lora_rank + d.kv_lora_rank)
-    b += 2 * d.w_b_elems + 4 * T + 4 * T * d.rope_dim  # positions + gathered cos/sin rows
+    wbytes = 1 if d.w8a8 else 2                            # INT8 or BF16 weights
+    b = 2 * T * d.D + wbytes * d.n_a * d.D + 2 * (d.q_lora_rank + d.kv_lora_rank)
+    b += wbytes * d.w_b_elems + 4 * T + 4 * T * d.rope_dim  # positions + gathered cos/sin rows
+    if d.w8a8:
+        b += 4 * d.n_w_scales                              # the weight rows' scales
     b += 2 * T * d.num_heads * (d.nope_dim + d.rope_dim)  # out_k
     b += 2 * T * d.num_heads * d.v_dim                    # out_v
     b += 2 * T * d.rope_dim                               # out_kpe

@@ -29,6 +29,7 @@ QUANT_Q = 1            # dims flags, the same bits as the C oracle's
 ROPE_INTERLEAVED = 2
 Q_HEAD_NORM = 4
 QUANT_PER_HEAD = 8
+W8A8 = 16
 
 
 class OracleDims(ctypes.Structure):
@@ -67,6 +68,13 @@ def lib():
         L.oracle_quant_row.argtypes = [P, ctypes.c_int, P, P]
         L.oracle_deinterleave.argtypes = [P, ctypes.c_int, P]
         L.oracle_rmsnorm_f32_row.argtypes = [P, ctypes.c_int, ctypes.c_float, P]
+        L.oracle_mla_prolog_w8a8.argtypes = [ctypes.POINTER(OracleDims)] + [P] * 7 + [P, ctypes.c_int32] + [P] * 12
+        L.oracle_mla_prolog_w8a8.restype = ctypes.c_int
+        L.oracle_dot_i8.argtypes = [P, P, ctypes.c_int]
+        L.oracle_dot_i8.restype = ctypes.c_int64
+        L.oracle_dequant.argtypes = [ctypes.c_int32, ctypes.c_float, ctypes.c_float]
+        L.oracle_dequant.restype = ctypes.c_float
+        L.oracle_project_w8a8.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_float, P, P]
         L.oracle_max_threads.restype = ctypes.c_int
         L.oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -125,6 +133,55 @@ def mla_prolog(d, x, gamma, W_a, W_b, positions, cos_sin,
                              _p(tok), ctypes.c_int32(n),
                              _p(out["out_k"]), _p(out["out_v"]), _p(out["out_kpe"]), _p(q8), _p(sc),
                              _p(c), _p(nrm), _p(q))
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    out["bad_positions"] = rc
+    return out
+
+
+def mla_prolog_w8a8(d, x, gamma, W_a, W_b, w_scale, positions, cos_sin,
+                    tokens: Optional[Sequence[int]] = None, taps: bool = False) -> Dict[str, np.ndarray]:
+    """The prolog with W8A8 projections (``d.flags`` has ``W8A8``).
+
+    ``W_a`` and ``W_b`` are INT8 codes in the layouts of the BF16 weights,
+    ``w_scale`` the FP32 scale of every weight row, [W_a rows; W_q_b rows
+    (none when q_lora_rank is 0); W_kv_b rows].  Outputs as
+    :func:`mla_prolog`; ``taps`` adds the x codes (``x_codes``, ``x_scale``)
+    and the normed rows' codes (``n_codes``, ``n_scale`` [n, 2] = c_q, c_kv)
+    to ``c``, ``normed`` (values before their quantisation) and ``q``.
+    """
+    L = lib()
+    tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    n = d.T if tok is None else len(tok)
+    H, Dn, Dv, R = d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
+    Lq, Lkv = d.q_lora_rank, d.kv_lora_rank
+    out = {
+        "out_k": np.zeros((n, H, Dn + R), np.uint16),
+        "out_v": np.zeros((n, H, Dv), np.uint16),
+        "out_kpe": np.zeros((n, R), np.uint16),
+    }
+    q8 = sc = None
+    if Lq > 0:
+        q8 = out["out_q_int8"] = np.zeros((n, H, Dn + R), np.int8)
+        sc = out["out_scale"] = np.zeros((n, H) if d.flags & QUANT_PER_HEAD else (n,), np.float32)
+    c = nrm = q = xc = xs = nc = ns = None
+    if taps:
+        c = out["c"] = np.zeros((n, Lq + Lkv + R), np.uint16)
+        nrm = out["normed"] = np.zeros((n, Lq + Lkv), np.uint16)
+        if Lq > 0:
+            q = out["q"] = np.zeros((n, H * (Dn + R)), np.float32)
+        xc = out["x_codes"] = np.zeros((n, d.D), np.int8)
+        xs = out["x_scale"] = np.zeros(n, np.float32)
+        nc = out["n_codes"] = np.zeros((n, Lq + Lkv), np.int8)
+        ns = out["n_scale"] = np.zeros((n, 2), np.float32)
+    arrs = [np.ascontiguousarray(x, np.uint16), np.ascontiguousarray(gamma, np.uint16),
+            np.ascontiguousarray(W_a, np.int8), np.ascontiguousarray(W_b, np.int8),
+            np.ascontiguousarray(w_scale, np.float32), np.ascontiguousarray(positions, np.int32),
+            np.ascontiguousarray(cos_sin, np.float32)]
+    dims = _dims(d)
+    rc = L.oracle_mla_prolog_w8a8(ctypes.byref(dims), *[_p(a) for a in arrs], _p(tok), ctypes.c_int32(n),
+                                  _p(out["out_k"]), _p(out["out_v"]), _p(out["out_kpe"]), _p(q8), _p(sc),
+                                  _p(c), _p(nrm), _p(q), _p(xc), _p(xs), _p(nc), _p(ns))
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
     out["bad_positions"] = rc
@@ -220,3 +277,23 @@ def quant_row(y: np.ndarray):
     scale = np.zeros(1, np.float32)
     lib().oracle_quant_row(_p(y), len(y), _p(codes), _p(scale))
     return codes, float(scale[0])
+
+
+def dot_i8(a: np.ndarray, w: np.ndarray) -> int:
+    a = np.ascontiguousarray(a, np.int8)
+    w = np.ascontiguousarray(w, np.int8)
+    return int(lib().oracle_dot_i8(_p(a), _p(w), len(a)))
+
+
+def dequant(y: int, a_scale: float, w_scale: float) -> float:
+    return float(lib().oracle_dequant(ctypes.c_int32(y), ctypes.c_float(a_scale), ctypes.c_float(w_scale)))
+
+
+def project_w8a8(a_codes: np.ndarray, W: np.ndarray, a_scale: float, w_scale: np.ndarray) -> np.ndarray:
+    a_codes = np.ascontiguousarray(a_codes, np.int8)
+    W = np.ascontiguousarray(W, np.int8)
+    w_scale = np.ascontiguousarray(w_scale, np.float32)
+    N, K = W.shape
+    out = np.zeros(N, np.float32)
+    lib().oracle_project_w8a8(_p(a_codes), _p(W), N, K, ctypes.c_float(a_scale), _p(w_scale), _p(out))
+    return out

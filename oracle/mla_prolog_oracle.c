@@ -35,7 +35,23 @@
  *     each (token, head) row of Dn + R values with its own scale (the quant
  *     formula of section 3.1 applied per head row).
  *
+ *   - W8A8 projections (oracle_mla_prolog_w8a8): the INT8 mode of the Linear
+ *     step (PyPTO-Gym AT-10 article, section 四, AT-09 "INT8 W8A8"):
+ *     the activation row is quantised per token with the formula above
+ *     (AT-05), the product is the exact integer sum of code x code
+ *     (int32 result; formed here in int64, which cannot overflow), and AT-06
+ *     turns it back into FP32 as ((float)y_int32 * a_scale) * w_scale, one
+ *     correctly rounded FP32 operation per step.  Every projection of the
+ *     prolog runs that way: x -> compression (then the BF16 cast the BF16
+ *     mode also has), the normed c_q / c_kv rows (after their BF16 cast) ->
+ *     q and KV expansion; with a quantised Linear the norm block becomes
+ *     RMSNorm + Linear + Quant (AT-11, V -> C -> V).
+ *
  * Readings where the pages are silent (also listed in the design notes):
+ *   - W8A8: one FP32 weight scale per output row of each weight matrix; the
+ *     quantised matmul input is the tensor the BF16 mode feeds to the
+ *     matmul (x; the normed rows after their BF16 cast); AT-06 multiplies
+ *     left to right: (y * a_scale) * w_scale;
  *   - a zero row (amax == 0) yields codes 0 and scale 0;
  *   - a position outside [0, max_pos) zero-fills every output of that token
  *     and is reported in the return value;
@@ -57,6 +73,7 @@
 #define ORACLE_ROPE_INTERLEAVED 2u
 #define ORACLE_Q_HEAD_NORM 4u
 #define ORACLE_QUANT_PER_HEAD 8u
+#define ORACLE_W8A8 16u
 
 typedef struct {
     int32_t T, D, q_lora_rank, kv_lora_rank, rope_dim, num_heads, nope_dim, v_dim, max_pos;
@@ -221,6 +238,42 @@ void oracle_quant_row(const float* y, int n, int8_t* codes, float* scale) {
     *scale = amax / 127.0f;
 }
 
+/* Exact integer product of two INT8 code rows of length K (the int32 matmul
+ * of the W8A8 Linear, PyPTO-Gym AT-10 article, section 四): the sum of
+ * code x code in int64, which holds it exactly for any K used here. */
+int64_t oracle_dot_i8(const int8_t* a, const int8_t* w_row, int K) {
+    int64_t acc = 0;
+    for (int k = 0; k < K; ++k) acc += (int64_t)a[k] * (int64_t)w_row[k];
+    return acc;
+}
+
+/* AT-06 dequantisation of one int32 product: FP32 (y * a_scale) * w_scale,
+ * the int32 -> FP32 conversion rounded to nearest. */
+float oracle_dequant(int32_t y, float a_scale, float w_scale) {
+    float f = (float)y;
+    float g = f * a_scale;
+    return g * w_scale;
+}
+
+/* One W8A8 projection of a quantised row: out[n] = AT-06(sum_k a[k] W[n,k],
+ * a_scale, w_scale[n]), n in [0, N), W INT8 codes in [N, K] layout. */
+void oracle_project_w8a8(const int8_t* a_codes, const int8_t* W, int N, int K, float a_scale,
+                         const float* w_scale, float* out) {
+    for (int n = 0; n < N; ++n)
+        out[n] = oracle_dequant((int32_t)oracle_dot_i8(a_codes, W + (size_t)n * K, K), a_scale, w_scale[n]);
+}
+
+/* The W8A8 operands and taps of one prolog run (NULL in the BF16 mode). */
+typedef struct {
+    const int8_t* W_a;     /* [NA, D] codes                                     */
+    const int8_t* W_b;     /* W_q_b [NQ, Lq] codes, then W_kv_b [NKV, Lkv]       */
+    const float* w_scale;  /* [NA + (Lq > 0 ? NQ : 0) + NKV]: one per weight row */
+    int8_t* x_codes;       /* taps (NULL to skip): x codes [n, D]               */
+    float* x_scale;        /*   x scales [n]                                    */
+    int8_t* n_codes;       /*   normed c_q | c_kv codes [n, Lq + Lkv]           */
+    float* n_scale;        /*   their scales [n, 2] = (c_q, c_kv)               */
+} oracle_w8a8;
+
 /* ------------------------------------------------------------ whole op -- */
 
 /*
@@ -236,15 +289,17 @@ void oracle_quant_row(const float* y, int n, int8_t* codes, float* scale) {
  * Returns the number of selected tokens whose position was out of range
  * (their outputs are zero-filled), or -1 on bad arguments.
  */
-int oracle_mla_prolog(const oracle_dims* d,
-                      const uint16_t* x, const uint16_t* gamma,
-                      const uint16_t* W_a, const uint16_t* W_b,
-                      const int32_t* positions, const float* cos_sin,
-                      const int32_t* tokens, int32_t n_tokens,
-                      uint16_t* out_k, uint16_t* out_v, uint16_t* out_kpe,
-                      int8_t* out_q_int8, float* out_scale,
-                      uint16_t* c_out, uint16_t* normed_out, float* q_out) {
-    if (!d || !x || !W_a || !positions || !cos_sin || !out_k || !out_v || !out_kpe) return -1;
+static int prolog(const oracle_dims* d,
+                  const uint16_t* x, const uint16_t* gamma,
+                  const uint16_t* W_a, const uint16_t* W_b, const oracle_w8a8* w8,
+                  const int32_t* positions, const float* cos_sin,
+                  const int32_t* tokens, int32_t n_tokens,
+                  uint16_t* out_k, uint16_t* out_v, uint16_t* out_kpe,
+                  int8_t* out_q_int8, float* out_scale,
+                  uint16_t* c_out, uint16_t* normed_out, float* q_out) {
+    if (!d || !x || !positions || !cos_sin || !out_k || !out_v || !out_kpe) return -1;
+    if (w8 ? (!w8->W_a || !w8->W_b || !w8->w_scale || W_a || W_b) : (!W_a || !W_b)) return -1;
+    if (((d->flags & ORACLE_W8A8) != 0) != (w8 != NULL)) return -1;
     const int T = d->T, D = d->D, Lq = d->q_lora_rank, Lkv = d->kv_lora_rank, R = d->rope_dim;
     const int H = d->num_heads, Dn = d->nope_dim, Dv = d->v_dim;
     const int NA = Lq + Lkv + R, NQ = H * (Dn + R);
@@ -255,12 +310,13 @@ int oracle_mla_prolog(const oracle_dims* d,
     if (T < 0 || D <= 0 || Lq < 0 || Lkv <= 0 || R <= 0 || (R & 1) || H <= 0 || Dn < 0 || Dv < 0)
         return -1;
     if ((Lq + Lkv) > 0 && !gamma) return -1;
-    if (Lq > 0 && (!W_b || !quant || !out_q_int8 || !out_scale)) return -1;
-    if (!W_b) return -1;
+    if (Lq > 0 && (!quant || !out_q_int8 || !out_scale)) return -1;
     const int n = tokens ? n_tokens : T;
     if (n < 0) return -1;
-    const uint16_t* W_qb = W_b;                          /* [NQ, Lq]  */
-    const uint16_t* W_kvb = W_b + (size_t)NQ * Lq;       /* [NKV, Lkv] */
+    const uint16_t* W_qb = W_b;                                   /* [NQ, Lq]  */
+    const uint16_t* W_kvb = W_b ? W_b + (size_t)NQ * Lq : NULL;  /* [NKV, Lkv] */
+    const int NKV = H * (Dn + Dv);
+    const int NQw = Lq > 0 ? NQ : 0;  /* rows of W_q_b */
     int bad = 0;
 
 #pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
@@ -270,8 +326,24 @@ int oracle_mla_prolog(const oracle_dims* d,
         uint16_t* ov = out_v + (size_t)j * H * Dv;
         uint16_t* okpe = out_kpe + (size_t)j * R;
         if (t < 0 || t >= T) { bad += 1; continue; }
+        /* W8A8, AT-05 on x: the per-token codes of the compression's input
+         * (they do not depend on the position). */
+        int8_t* xq = NULL;
+        float sx = 0.0f;
+        if (w8) {
+            float* xf = (float*)malloc(sizeof(float) * (size_t)D);
+            xq = (int8_t*)malloc((size_t)D);
+            for (int k = 0; k < D; ++k) xf[k] = bf16_to_f32(x[(size_t)t * D + k]);
+            oracle_quant_row(xf, D, xq, &sx);
+            if (w8->x_codes) memcpy(w8->x_codes + (size_t)j * D, xq, (size_t)D);
+            if (w8->x_scale) w8->x_scale[j] = sx;
+            free(xf);
+        }
         const int32_t pos = positions[t];
         if (pos < 0 || pos >= d->max_pos) {
+            free(xq);
+            if (w8 && w8->n_codes) memset(w8->n_codes + (size_t)j * (Lq + Lkv), 0, (size_t)(Lq + Lkv));
+            if (w8 && w8->n_scale) w8->n_scale[2 * j] = w8->n_scale[2 * j + 1] = 0.0f;
             memset(ok, 0, sizeof(uint16_t) * (size_t)H * (Dn + R));
             memset(ov, 0, sizeof(uint16_t) * (size_t)H * Dv);
             memset(okpe, 0, sizeof(uint16_t) * (size_t)R);
@@ -294,12 +366,34 @@ int oracle_mla_prolog(const oracle_dims* d,
         float* kpe_f = (float*)malloc(sizeof(float) * (size_t)R);
         float* kpe_r = (float*)malloc(sizeof(float) * (size_t)R);
 
-        /* Step 1: compression projection x . W_a^T, each output rounded to BF16. */
-        oracle_project_bf16(x + (size_t)t * D, W_a, NA, D, c);
+        /* Step 1: compression projection x . W_a^T, each output rounded to BF16
+         * (W8A8: the integer product of the codes, dequantised, then rounded). */
+        if (w8) {
+            float* cf = (float*)malloc(sizeof(float) * (size_t)NA);
+            oracle_project_w8a8(xq, w8->W_a, NA, D, sx, w8->w_scale, cf);
+            for (int i = 0; i < NA; ++i) c[i] = oracle_f32_to_bf16(cf[i]);
+            free(cf);
+        } else {
+            oracle_project_bf16(x + (size_t)t * D, W_a, NA, D, c);
+        }
         /* Step 2: split -- c_q = c[0, Lq), c_kv = c[Lq, Lq+Lkv), k_pe = c[Lq+Lkv, NA). */
         /* Step 3: RMSNorm of c_q and c_kv with their gammas, then BF16. */
         if (Lq > 0) oracle_rmsnorm_row(c, gamma, Lq, d->eps, NULL, nrm);
         oracle_rmsnorm_row(c + Lq, gamma + Lq, Lkv, d->eps, NULL, nrm + Lq);
+        /* W8A8 (AT-11): the normed BF16 rows c_q and c_kv, each quantised per
+         * token, are the expansions' inputs. */
+        int8_t* nq = NULL;
+        float sq = 0.0f, skv = 0.0f;
+        if (w8) {
+            float* nf = (float*)malloc(sizeof(float) * (size_t)(Lq + Lkv));
+            nq = (int8_t*)malloc((size_t)(Lq + Lkv));
+            for (int i = 0; i < Lq + Lkv; ++i) nf[i] = bf16_to_f32(nrm[i]);
+            if (Lq > 0) oracle_quant_row(nf, Lq, nq, &sq);
+            oracle_quant_row(nf + Lq, Lkv, nq + Lq, &skv);
+            if (w8->n_codes) memcpy(w8->n_codes + (size_t)j * (Lq + Lkv), nq, (size_t)(Lq + Lkv));
+            if (w8->n_scale) w8->n_scale[2 * j] = sq, w8->n_scale[2 * j + 1] = skv;
+            free(nf);
+        }
         /* Step 4 (k_pe RoPE): rotate-half in FP32 with this token's table row
          * (after the de-interleave in the interleaved variant). */
         for (int i = 0; i < R; ++i) kpe_f[i] = bf16_to_f32(c[Lq + Lkv + i]);
@@ -311,20 +405,33 @@ int oracle_mla_prolog(const oracle_dims* d,
         for (int i = 0; i < R; ++i) okpe[i] = oracle_f32_to_bf16(kpe_r[i]);
         /* Steps 5-7: KV expansion, split per head into k_nope | value, assemble
          * K = [k_nope | k_pe_rot] with the rotated k_pe shared by every head. */
+        float* kvf = NULL;
+        if (w8) {
+            kvf = (float*)malloc(sizeof(float) * (size_t)NKV);
+            oracle_project_w8a8(nq + Lq, w8->W_b + (size_t)NQw * Lq, NKV, Lkv, skv, w8->w_scale + NA + NQw, kvf);
+        }
         for (int h = 0; h < H; ++h) {
-            const uint16_t* Wh = W_kvb + (size_t)h * (Dn + Dv) * Lkv;
+            const uint16_t* Wh = w8 ? NULL : W_kvb + (size_t)h * (Dn + Dv) * Lkv;
             for (int i = 0; i < Dn; ++i)
-                ok[(size_t)h * (Dn + R) + i] = oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)i * Lkv, Lkv));
+                ok[(size_t)h * (Dn + R) + i] =
+                    w8 ? oracle_f32_to_bf16(kvf[(size_t)h * (Dn + Dv) + i])
+                       : oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)i * Lkv, Lkv));
             for (int i = 0; i < Dv; ++i)
-                ov[(size_t)h * Dv + i] = oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)(Dn + i) * Lkv, Lkv));
+                ov[(size_t)h * Dv + i] =
+                    w8 ? oracle_f32_to_bf16(kvf[(size_t)h * (Dn + Dv) + Dn + i])
+                       : oracle_f64_to_bf16(dot_bf16_f64(nrm + Lq, Wh + (size_t)(Dn + i) * Lkv, Lkv));
             for (int i = 0; i < R; ++i) ok[(size_t)h * (Dn + R) + Dn + i] = okpe[i];
         }
+        free(kvf);
         /* q path: expansion, (per-head RMSNorm,) RoPE on each head's rope
          * slice, INT8 quant per token (or per head row). */
         if (Lq > 0) {
             float* q = (float*)malloc(sizeof(float) * (size_t)NQ);
             float* hb = (float*)malloc(sizeof(float) * (size_t)(Dn + R));
-            oracle_project_f32(nrm, W_qb, NQ, Lq, q);
+            if (w8)
+                oracle_project_w8a8(nq, w8->W_b, NQ, Lq, sq, w8->w_scale + NA, q);
+            else
+                oracle_project_f32(nrm, W_qb, NQ, Lq, q);
             for (int h = 0; h < H; ++h) {
                 float* qh = q + (size_t)h * (Dn + R);
                 if (head_norm) {
@@ -351,9 +458,42 @@ int oracle_mla_prolog(const oracle_dims* d,
         }
         if (c_out) memcpy(c_out + (size_t)j * NA, c, sizeof(uint16_t) * (size_t)NA);
         if (normed_out) memcpy(normed_out + (size_t)j * (Lq + Lkv), nrm, sizeof(uint16_t) * (size_t)(Lq + Lkv));
-        free(c); free(nrm); free(kpe_f); free(kpe_r);
+        free(c); free(nrm); free(kpe_f); free(kpe_r); free(xq); free(nq);
     }
     return bad;
+}
+
+int oracle_mla_prolog(const oracle_dims* d,
+                      const uint16_t* x, const uint16_t* gamma,
+                      const uint16_t* W_a, const uint16_t* W_b,
+                      const int32_t* positions, const float* cos_sin,
+                      const int32_t* tokens, int32_t n_tokens,
+                      uint16_t* out_k, uint16_t* out_v, uint16_t* out_kpe,
+                      int8_t* out_q_int8, float* out_scale,
+                      uint16_t* c_out, uint16_t* normed_out, float* q_out) {
+    return prolog(d, x, gamma, W_a, W_b, NULL, positions, cos_sin, tokens, n_tokens, out_k, out_v, out_kpe,
+                  out_q_int8, out_scale, c_out, normed_out, q_out);
+}
+
+/*
+ * The prolog with W8A8 projections (dims flag ORACLE_W8A8): arguments as
+ * oracle_mla_prolog, with the INT8 weights and their row scales in place of
+ * the BF16 weights, and four more optional taps (x codes and scales, the
+ * normed rows' codes and scales; see oracle_w8a8).  normed_out still
+ * receives the normed BF16 values, before their quantisation.
+ */
+int oracle_mla_prolog_w8a8(const oracle_dims* d,
+                           const uint16_t* x, const uint16_t* gamma,
+                           const int8_t* W_a, const int8_t* W_b, const float* w_scale,
+                           const int32_t* positions, const float* cos_sin,
+                           const int32_t* tokens, int32_t n_tokens,
+                           uint16_t* out_k, uint16_t* out_v, uint16_t* out_kpe,
+                           int8_t* out_q_int8, float* out_scale,
+                           uint16_t* c_out, uint16_t* normed_out, float* q_out,
+                           int8_t* x_codes, float* x_scale, int8_t* n_codes, float* n_scale) {
+    const oracle_w8a8 w8 = {W_a, W_b, w_scale, x_codes, x_scale, n_codes, n_scale};
+    return prolog(d, x, gamma, NULL, NULL, &w8, positions, cos_sin, tokens, n_tokens, out_k, out_v, out_kpe,
+                  out_q_int8, out_scale, c_out, normed_out, q_out);
 }
 
 /* Threads OpenMP will use for the next parallel region (1 without OpenMP). */
