@@ -171,16 +171,20 @@ def kernel_work(d: wl.Dims, cache: bool = False, names=()):
     """
     T, H, Dn, Dv, R = d.T, d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
     q_out = (T * d.n_q + 4 * T * d.n_scales) if d.quant_q else 0
+    w8 = d.w8a8  # INT8 weights (1 byte) and their row scales; x is read by the x-quant kernel
+    nq_rows = d.n_q if d.q_lora_rank else 0
     b = {
-        "mla_compress_kernel": 2 * T * d.D + 2 * d.n_a * d.D,
+        "mla_quant_x_kernel": 2 * T * d.D if w8 else 0,
+        "mla_compress_kernel": (d.n_a * d.D + 4 * d.n_a) if w8 else 2 * T * d.D + 2 * d.n_a * d.D,
         "mla_norm_rope_kernel": 2 * (d.q_lora_rank + d.kv_lora_rank) + 4 * T + 4 * T * R
                                 + 2 * T * R + 2 * T * H * R
                                 + ((4 * T + 2 * T * (d.kv_lora_rank + R)) if cache else 0),
-        "mla_expand_kernel": 2 * d.w_b_elems + 2 * T * H * Dn + 2 * T * H * Dv
-                             + (q_out if d.quant_per_head else 0),
+        "mla_expand_kernel": (d.w_b_elems + 4 * (nq_rows + d.n_kv) if w8 else 2 * d.w_b_elems)
+                             + 2 * T * H * Dn + 2 * T * H * Dv + (q_out if d.quant_per_head else 0),
         "mla_quant_kernel": 0 if d.quant_per_head else q_out,
     }
     f = {
+        "mla_quant_x_kernel": 0,
         "mla_compress_kernel": 2 * T * d.n_a * d.D,
         "mla_norm_rope_kernel": 0,
         "mla_expand_kernel": 2 * T * (d.n_q * d.q_lora_rank + d.n_kv * d.kv_lora_rank),
@@ -253,14 +257,16 @@ def run_gpu(args):
     d = dataclasses.replace(d, flags=d.flags | sum(wl.VARIANTS[v] for v in variants))
     cached = "cache" in variants
     inp = wl.make_inputs(w, d)
+    ww = wl.make_w8a8_weights(w, d) if d.w8a8 else None
     H, Dn, Dv, R = d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
 
     def bf(a, shape):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).reshape(shape).to(dev)
 
-    base = dict(x=bf(inp.x, (d.T, d.D)), gamma=bf(inp.gamma, (-1,)), W_a=bf(inp.W_a, (d.n_a, d.D)),
-                W_b=bf(inp.W_b, (-1,)), positions=torch.from_numpy(inp.positions).to(dev),
-                cos_sin=torch.from_numpy(inp.cos_sin).to(dev))
+    # W8A8: the weights live in the handle (loaded once below), not in the sets
+    base = dict(x=bf(inp.x, (d.T, d.D)), gamma=bf(inp.gamma, (-1,)),
+                W_a=None if ww else bf(inp.W_a, (d.n_a, d.D)), W_b=None if ww else bf(inp.W_b, (-1,)),
+                positions=torch.from_numpy(inp.positions).to(dev), cos_sin=torch.from_numpy(inp.cos_sin).to(dev))
 
     def new_outputs():
         o = dict(out_k=torch.empty((d.T, H, Dn + R), dtype=torch.bfloat16, device=dev),
@@ -278,18 +284,22 @@ def run_gpu(args):
     if cached:
         base["slot_mapping"] = torch.from_numpy(
             np.random.default_rng(1).permutation(2 * d.T)[:d.T].astype(np.int32)).to(dev)
-    set_bytes = sum(t.numel() * t.element_size() for t in base.values())
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values() if t is not None)
     set_bytes += sum(t.numel() * t.element_size() for t in new_outputs().values() if t is not None)
     n_sets = max(2, -(-3 * L2_BYTES // set_bytes))
     n_sets = min(n_sets, max(2, int(8e9 // set_bytes)))
     sets = []
     for i in range(n_sets):
-        s = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        s = {k: (v if i == 0 or v is None else v.clone()) for k, v in base.items()}
         s.update(new_outputs())
         sets.append(s)
 
     clk = ClockSampler(local).__enter__()
     p = binding.MlaProlog.from_dims(d)
+    if ww is not None:
+        p.load_w8a8(torch.from_numpy(ww.W_a).to(dev), torch.from_numpy(ww.W_b).to(dev),
+                    torch.from_numpy(ww.w_scale).to(dev), stream=torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
     names = p.kernel_names()
     active = [n for n in names if n != "mla_quant_kernel" or (d.q_lora_rank and not d.quant_per_head)]
     stream = torch.cuda.Stream(device=dev)
@@ -459,7 +469,8 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "int8 x int8 -> int32 (on bf16 tensor cores)" if d.w8a8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": wname, "T": d.T, "D": d.D, "q_lora_rank": d.q_lora_rank,
                    "kv_lora_rank": d.kv_lora_rank, "rope_dim": d.rope_dim, "num_heads": d.num_heads,
                    "nope_dim": d.nope_dim, "v_dim": d.v_dim, "quant_q": d.quant_q, "flags": d.flags,
@@ -508,6 +519,17 @@ def oracle_sample(w: wl.Workload, max_tokens: int, dims=None):
     return inp, np.sort(rng.choice(T, max_tokens, replace=False)).astype(np.int32)
 
 
+def oracle_call(w: wl.Workload, inp: wl.Inputs, tok):
+    """One oracle pass over the sampled tokens (the W8A8 oracle for W8A8 dims)."""
+    import oracle
+    d = inp.dims
+    if d.w8a8:
+        ww = wl.make_w8a8_weights(w, d)
+        return lambda: oracle.mla_prolog_w8a8(d, inp.x, inp.gamma, ww.W_a, ww.W_b, ww.w_scale, inp.positions,
+                                              inp.cos_sin, tokens=tok)
+    return lambda: oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+
+
 def cpu_baseline(w: wl.Workload, seconds: float, dims=None):
     import oracle
     oracle.build()
@@ -517,10 +539,11 @@ def cpu_baseline(w: wl.Workload, seconds: float, dims=None):
     inp, tok = oracle_sample(w, max_tokens, dims)
     d = inp.dims
     n = d.T if tok is None else len(tok)
+    run = oracle_call(w, inp, tok)
     t0 = time.perf_counter()
     calls = 0
     while True:
-        oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+        run()
         calls += 1
         el = time.perf_counter() - t0
         if el >= seconds or el / calls * (calls + 1) > 3 * seconds:

@@ -93,6 +93,30 @@ extern "C" {
  * q_lora_rank > 0.
  */
 #define MLA_PROLOG_QUANT_PER_HEAD 0x8u
+/*
+ * W8A8 projections: the INT8 mode of the Linear step (PyPTO-Gym AT-10
+ * article, section 四, AT-09 "INT8 W8A8"): every projection takes its input
+ * row quantised per token (the formula of the q path: AT-05), multiplies
+ * INT8 codes by INT8 weight codes exactly (an int32 result), and
+ * dequantises it (AT-06) in FP32 as ((float)y * input_scale) * w_scale[row].
+ *   - compression: x (BF16) -> codes; the dequantised sums are rounded to
+ *     BF16 as in the BF16 mode;
+ *   - expansions: the normed c_q and c_kv rows (after their BF16 cast) are
+ *     quantised per token, each with its own scale (AT-11, RMSNorm + Linear
+ *     + Quant); k_nope and value are the dequantised sums rounded to BF16,
+ *     q the dequantised FP32 sums (then RoPE and the q quantisation).
+ * The weights live in the handle: load them once with
+ * mla_prolog_load_w8a8(), then call mla_prolog_run() / _run_cached() with
+ * W_a = W_b = NULL.  Extra size rules: Lq <= 2048 and Lkv <= 2048.  Not
+ * available through mla_prolog_run_noalloc().
+ *
+ * On sm_103a the tensor cores have no INT8 MMA kind, so the codes are kept
+ * as BF16 integers (exact) and multiplied on the BF16 path with FP32
+ * accumulation; accumulation chains are kept short enough (at most 1024 K
+ * per chain) that every partial sum is an integer below 2^24 and so exact,
+ * and chains are added in int32: the integer product is exact.
+ */
+#define MLA_PROLOG_W8A8 0x10u
 
 /*
  * Problem sizes, fixed for the life of a handle.
@@ -136,6 +160,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out);
  *                                             ordered [c_kv (Lkv) ; k_pe (R)]
  *   W_b        BF16, W_q_b [H(Dn+R), Lq] followed by W_kv_b [H(Dn+Dv), Lkv]
  *              (both [N, K] row-major; W_q_b empty when Lq = 0)
+ *              (W_a and W_b: NULL with MLA_PROLOG_W8A8, whose weights are
+ *              loaded into the handle by mla_prolog_load_w8a8)
  *   positions  int32 [T], each in [0, max_pos)
  *   cos_sin    FP32 [max_pos, R]: columns [0, R/2) = cos(p * theta_i),
  *              [R/2, R) = sin(p * theta_i)
@@ -180,6 +206,20 @@ int mla_prolog_run_cached(mla_prolog_t h,
                           int8_t* out_q_int8, float* out_scale,
                           const int32_t* slot_mapping, void* kv_cache, int64_t num_slots,
                           void* stream);
+
+/*
+ * W8A8 handles only: loads the INT8 weights into the handle (enqueued on
+ * `stream`; the inputs may be freed once the stream has passed this call).
+ *   W_a      int8 [Lq + Lkv + R, D]   codes, the layout of the BF16 W_a
+ *   W_b      int8                     codes, the layout of the BF16 W_b
+ *   w_scale  FP32 [Lq + Lkv + R + (Lq > 0 ? H(Dn+R) : 0) + H(Dn+Dv)]
+ *            one scale per weight row: W_a rows, then W_q_b rows, then
+ *            W_kv_b rows
+ * All device pointers; W_a and W_b 16-byte aligned.  The handle keeps the
+ * codes as BF16 integers (2 bytes per weight; see MLA_PROLOG_W8A8).
+ * Errors: INVALID_ARG (not a W8A8 handle, null or misaligned), CUDA.
+ */
+int mla_prolog_load_w8a8(mla_prolog_t h, const int8_t* W_a, const int8_t* W_b, const float* w_scale, void* stream);
 
 /* Frees the workspace and the handle.  NULL-safe.  Synchronises the device. */
 int mla_prolog_destroy(mla_prolog_t h);
@@ -255,6 +295,14 @@ const char* mla_prolog_kernel_name(mla_prolog_t h, int32_t i);
 #define MLA_TAP_NORMED 1
 #define MLA_TAP_Q      2
 #define MLA_TAP_AMAX   3
+/* W8A8 handles (with them MLA_TAP_NORMED holds the normed rows' INT8 codes,
+ * as BF16 integers):
+ *   MLA_TAP_X_CODES    BF16 [T, D]  x's per-token codes, as BF16 integers
+ *   MLA_TAP_X_SCALE    FP32 [T]     x's per-token scales
+ *   MLA_TAP_NORM_SCALE FP32 [T, 2]  scales of the normed (c_q, c_kv) codes */
+#define MLA_TAP_X_CODES    4
+#define MLA_TAP_X_SCALE    5
+#define MLA_TAP_NORM_SCALE 6
 int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, void* stream);
 
 /*

@@ -22,6 +22,7 @@ MLA_PROLOG_QUANT_Q = 1
 MLA_PROLOG_ROPE_INTERLEAVED = 2
 MLA_PROLOG_Q_HEAD_NORM = 4
 MLA_PROLOG_QUANT_PER_HEAD = 8
+MLA_PROLOG_W8A8 = 16
 STATUS_POSITION_RANGE = 0x1
 STATUS_WAIT_TIMEOUT = 0x2
 STATUS_SLOT_RANGE = 0x4
@@ -33,8 +34,10 @@ EXPORTED = [
     "mla_prolog_set_timing_events", "mla_prolog_kernel_count", "mla_prolog_kernel_name",
     "mla_prolog_workspace_bytes", "mla_prolog_schedule", "mla_prolog_copy_tap", "mla_prolog_set_tuning",
     "mla_prolog_run_noalloc", "mla_prolog_run_cached", "mla_prolog_plan", "mla_prolog_lpt",
+    "mla_prolog_load_w8a8",
 ]
 TAP_NORMED, TAP_Q, TAP_AMAX = 1, 2, 3
+TAP_X_CODES, TAP_X_SCALE, TAP_NORM_SCALE = 4, 5, 6
 TUNE_COMPRESS_GROUP = 1
 TUNE_COMPRESS_COMPENSATED = 2
 TUNE_DECODE_FUSED = 3
@@ -105,6 +108,7 @@ def lib(path: Optional[str] = None):
     L.mla_prolog_run_cached.argtypes = [V] * 14 + [ctypes.c_int64, V]
     L.mla_prolog_plan.argtypes = [P(MlaPrologDims), I32, P(MlaPrologPlanInfo)]
     L.mla_prolog_lpt.argtypes = [P(ctypes.c_int64), I32, I32, P(I32), P(ctypes.c_int64)]
+    L.mla_prolog_load_w8a8.argtypes = [V, V, V, V, V]
     for n in EXPORTED:
         if n not in ("mla_prolog_strerror", "mla_prolog_last_cuda_error", "mla_prolog_kernel_count",
                      "mla_prolog_kernel_name"):
@@ -182,6 +186,8 @@ class MlaProlog:
         bf = torch.bfloat16
         wb = H * (Dn + R) * Lq + H * (Dn + Dv) * Lkv
         scale_shape = (d.T, H) if d.flags & MLA_PROLOG_QUANT_PER_HEAD else (d.T,)
+        if d.flags & MLA_PROLOG_W8A8 and (W_a is not None or W_b is not None):
+            raise ValueError("a W8A8 handle takes its weights from load_w8a8: pass W_a = W_b = None")
         return [
             _ptr(x, "x", bf, (d.T, d.D), dev),
             _ptr(gamma, "gamma", bf, (Lq + Lkv,), dev),
@@ -214,6 +220,19 @@ class MlaProlog:
         slots = _ptr(slot_mapping, "slot_mapping", torch.int32, (d.T,), self.device)
         _check(lib().mla_prolog_run_cached(self.handle, *args, slots, cache, n, _stream_ptr(stream)),
                "mla_prolog_run_cached")
+
+    def load_w8a8(self, W_a, W_b, w_scale, stream=None) -> None:
+        """Loads INT8 weight codes (the layouts of the BF16 W_a and W_b) and
+        their FP32 row scales ([W_a rows; W_q_b rows; W_kv_b rows]) into a
+        W8A8 handle."""
+        d = self.dims
+        Lq, Lkv, R, H, Dn, Dv = d.q_lora_rank, d.kv_lora_rank, d.rope_dim, d.num_heads, d.nope_dim, d.v_dim
+        NQw = H * (Dn + R) if Lq > 0 else 0
+        wb = H * (Dn + R) * Lq + H * (Dn + Dv) * Lkv
+        a = _ptr(W_a, "W_a", torch.int8, (Lq + Lkv + R, d.D), self.device)
+        b = _ptr(W_b, "W_b", torch.int8, (wb,), self.device)
+        s = _ptr(w_scale, "w_scale", torch.float32, (Lq + Lkv + R + NQw + H * (Dn + Dv),), self.device)
+        _check(lib().mla_prolog_load_w8a8(self.handle, a, b, s, _stream_ptr(stream)), "mla_prolog_load_w8a8")
 
     def device_status(self, stream=None) -> int:
         v = ctypes.c_int32(0)
@@ -251,6 +270,12 @@ class MlaProlog:
             t = torch.empty((d.T, d.num_heads * (d.nope_dim + d.rope_dim)), dtype=torch.float32, device=self.device)
         elif which == TAP_AMAX:
             t = torch.empty((d.T,), dtype=torch.float32, device=self.device)
+        elif which == TAP_X_CODES:
+            t = torch.empty((d.T, d.D), dtype=torch.bfloat16, device=self.device)
+        elif which == TAP_X_SCALE:
+            t = torch.empty((d.T,), dtype=torch.float32, device=self.device)
+        elif which == TAP_NORM_SCALE:
+            t = torch.empty((d.T, 2), dtype=torch.float32, device=self.device)
         else:
             raise ValueError(which)
         _check(lib().mla_prolog_copy_tap(self.handle, which, t.data_ptr(), t.numel() * t.element_size(),

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmla_prolog.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["gemm.cu", "rowwise.cu", "decode.cu", "cluster.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["gemm.cu", "gemm_w8a8.cu", "rowwise.cu", "decode.cu", "cluster.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          f"-I{INCLUDE}"]

@@ -74,7 +74,7 @@ bool encode_store(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-constexpr int kKernelCount = 5;  // most kernels one run launches (timing-hook events: + 1)
+constexpr int kKernelCount = 6;  // most kernels one run launches (timing-hook events: + 1)
 constexpr int kPairCompressBN = 256;                // the compression pair kernel's tile width
 
 const char* const kClusterKernelNames[3] = {"mla_compress_norm_kernel", "mla_expand_kernel", "mla_quant_kernel"};
@@ -160,6 +160,19 @@ struct mla_prolog {
     cudaStream_t side = nullptr;
     cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
     int n_events = 0;
+    // W8A8 (MLA_PROLOG_W8A8): the weights as BF16 integers with their row
+    // scales (filled by mla_prolog_load_w8a8), x's codes and scales, and the
+    // normed rows' scales, in one allocation of their own.
+    bool w8a8 = false;
+    bool w8_loaded = false;
+    void* w8mem = nullptr;
+    uint16_t* wa16 = nullptr;
+    uint16_t* wb16 = nullptr;
+    float* wscale = nullptr;
+    uint16_t* xq = nullptr;
+    float* xscale = nullptr;
+    float* nscale = nullptr;
+    size_t wa_elems = 0, wb_elems = 0, n_wscale = 0;
 };
 
 namespace {
@@ -193,13 +206,16 @@ int check_dims(const mla_prolog_dims& d) {
     if (!std::isfinite(d.eps) || d.eps < 0.0f) return MLA_ERR_UNSUPPORTED_DIMS;
     const bool quant = (d.flags & MLA_PROLOG_QUANT_Q) != 0;
     const uint32_t known = MLA_PROLOG_QUANT_Q | MLA_PROLOG_ROPE_INTERLEAVED | MLA_PROLOG_Q_HEAD_NORM |
-                           MLA_PROLOG_QUANT_PER_HEAD;
+                           MLA_PROLOG_QUANT_PER_HEAD | MLA_PROLOG_W8A8;
     if ((d.flags & ~known) != 0) return MLA_ERR_INVALID_ARG;
     if (quant != (d.q_lora_rank > 0)) return MLA_ERR_INVALID_ARG;
     // the per-head norm and the per-head quant act on the q path
     if ((d.flags & (MLA_PROLOG_Q_HEAD_NORM | MLA_PROLOG_QUANT_PER_HEAD)) && d.q_lora_rank == 0)
         return MLA_ERR_INVALID_ARG;
     if (d.q_lora_rank > 0 && d.nope_dim + d.rope_dim > 256) return MLA_ERR_UNSUPPORTED_DIMS;
+    // W8A8: an expansion's K runs as at most two exact accumulation chains
+    if ((d.flags & MLA_PROLOG_W8A8) && (d.q_lora_rank > 2 * kW8ChainKb * kBK || d.kv_lora_rank > 2 * kW8ChainKb * kBK))
+        return MLA_ERR_UNSUPPORTED_DIMS;
     // 32-bit index headroom of the kernels' row arithmetic
     const double big = static_cast<double>(d.T) * d.num_heads * (d.nope_dim + d.rope_dim + d.v_dim);
     if (big > 4.0e9 || static_cast<double>(d.T) * d.D > 4.0e9) return MLA_ERR_UNSUPPORTED_DIMS;
@@ -319,7 +335,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     std::vector<int> cptable;
     if (!h->decode) {
         int active = 0;
-        if (compress_pair_max_active(&active) == cudaSuccess && active >= 1) {
+        if (!(d.flags & MLA_PROLOG_W8A8) && compress_pair_max_active(&active) == cudaSuccess && active >= 1) {
             const int kb = cdiv(d.D, kBK);
             h->cpair_ok = true;
             // Measured on GB300: slower on pairs (256-wide tiles, plain FP32
@@ -342,6 +358,15 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->cluster = h->cplan.est_us <= kClusterDefaultUs;
         h->cluster_expand_grid = njobs_b < sms - h->cluster_ctas ? njobs_b : sms - h->cluster_ctas;
         h->cluster_shape_b = h->shape_b == GemmShape::Narrow ? GemmShape::Deep : h->shape_b;
+    }
+    // W8A8 runs on the split-K / per-tile kernels, whose epilogues turn the
+    // exact integer accumulators into dequantised values; the cooperative,
+    // cluster and kv-resident kernels do not take it.
+    h->w8a8 = (d.flags & MLA_PROLOG_W8A8) != 0;
+    if (h->w8a8) {
+        h->fused_ok = h->fused = false;
+        h->cluster_ok = h->cluster = false;
+        if (h->group_a > kW8ChainKb) h->group_a = kW8ChainKb;
     }
     // A table is needed only when there are more jobs than SMs; the expansion
     // grid and the cooperative grid are then both one CTA per SM, so one
@@ -464,7 +489,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->q_wide = h->q_wide_ok;
     // Pairs: the kv tiles on their own kernel with the normed c_kv rows of a
     // 256-token tile resident in shared memory (K = Lkv <= 512).
-    if (h->pair_ok && h->ts_ok && Lkv <= 512 && Lkv % kBK == 0 && h->bn_kv == 256) {
+    if (h->pair_ok && h->ts_ok && Lkv <= 512 && Lkv % kBK == 0 && h->bn_kv == 256 && !h->w8a8) {
         int active = 0;
         if (expand_kv_pair_max_active(&active) == cudaSuccess && active >= 1) {
             h->kvres_ok = true;
@@ -492,6 +517,26 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         delete h;
         return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(workspace)");
     }
+    if (h->w8a8) {
+        const size_t NQw = Lq > 0 ? static_cast<size_t>(h->NQ) : 0;
+        h->wa_elems = static_cast<size_t>(h->NA) * d.D;
+        h->wb_elems = NQw * Lq + static_cast<size_t>(h->NKV) * Lkv;
+        h->n_wscale = h->NA + NQw + h->NKV;
+        const size_t b_wa = al(h->wa_elems * 2), b_wb = al(h->wb_elems * 2), b_ws = al(h->n_wscale * 4);
+        const size_t b_xq = al(T * d.D * 2), b_xs = al(T * 4), b_ns = al(T * 8);
+        if ((e = cudaMalloc(&h->w8mem, b_wa + b_wb + b_ws + b_xq + b_xs + b_ns)) != cudaSuccess) {
+            cudaFree(h->ws);
+            delete h;
+            return cuda_fail(e, "cudaMalloc(W8A8 weights)");
+        }
+        char* q = static_cast<char*>(h->w8mem);
+        h->wa16 = reinterpret_cast<uint16_t*>(q);
+        h->wb16 = reinterpret_cast<uint16_t*>(q + b_wa);
+        h->wscale = reinterpret_cast<float*>(q + b_wa + b_wb);
+        h->xq = reinterpret_cast<uint16_t*>(q + b_wa + b_wb + b_ws);
+        h->xscale = reinterpret_cast<float*>(q + b_wa + b_wb + b_ws + b_xq);
+        h->nscale = reinterpret_cast<float*>(q + b_wa + b_wb + b_ws + b_xq + b_xs);
+    }
     if (h->kvres_ok && Lq > 0 && !per_head) {
         int least = 0, greatest = 0;
         if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
@@ -501,6 +546,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             if (h->side) cudaStreamDestroy(h->side);
             if (h->fork_ev) cudaEventDestroy(h->fork_ev);
             cudaFree(h->ws);
+            if (h->w8mem) cudaFree(h->w8mem);
             delete h;
             return cuda_fail(e, "side stream for the quant");
         }
@@ -520,6 +566,7 @@ int mla_prolog_destroy(mla_prolog_t h) {
     if (h->fork_ev) cudaEventDestroy(h->fork_ev);
     if (h->join_ev) cudaEventDestroy(h->join_ev);
     if (h->ws) cudaFree(h->ws);
+    if (h->w8mem) cudaFree(h->w8mem);
     if (dev >= 0 && dev != h->device) cudaSetDevice(dev);
     delete h;
     return MLA_OK;
@@ -543,6 +590,11 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     const bool per_head = (d.flags & MLA_PROLOG_QUANT_PER_HEAD) != 0;
     if (cache && (!slot_mapping || !aligned(slot_mapping, 4) || !aligned(cache, 16) || num_slots < 0))
         return MLA_ERR_INVALID_ARG;
+    if (h->w8a8) {  // the weights live in the handle (mla_prolog_load_w8a8)
+        if (W_a || W_b || !h->w8_loaded) return MLA_ERR_INVALID_ARG;
+        W_a = h->wa16;
+        W_b = h->wb16;
+    }
     if (d.T == 0) return MLA_OK;
     const void* p16[] = {x, gamma, W_a, W_b, cos_sin, out_k, out_v, out_kpe};
     for (const void* p : p16)
@@ -556,9 +608,10 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const uint16_t* wb = static_cast<const uint16_t*>(W_b);
-    if (x != h->last_x) {
-        if (!encode_bf16(&h->tm_x, x, d.D, d.T, d.D, kBM)) return cuda_fail(cudaErrorInvalidValue, "tensor map x");
-        h->last_x = x;
+    const void* x_mma = h->w8a8 ? static_cast<const void*>(h->xq) : x;  // the compression's A operand
+    if (x_mma != h->last_x) {
+        if (!encode_bf16(&h->tm_x, x_mma, d.D, d.T, d.D, kBM)) return cuda_fail(cudaErrorInvalidValue, "tensor map x");
+        h->last_x = x_mma;
     }
     if (W_a != h->last_wa) {
         if (!encode_bf16(&h->tm_wa, W_a, d.D, h->NA, d.D, h->bn_a))
@@ -636,6 +689,9 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pa.status = h->status;
     pa.timeout_ns = h->timeout_ns;
     pa.job_table = h->compress_table;
+    pa.w8a8 = h->w8a8 ? 1 : 0;
+    pa.x_scale = h->xscale;
+    pa.w_scale = h->wscale;
     if (h->decode && h->l2_fetch) {
         pa.l2_fetch = static_cast<const uint8_t*>(W_b);
         pa.l2_fetch_bytes = (static_cast<uint64_t>(h->NQ) * Lq + static_cast<uint64_t>(h->NKV) * Lkv) * 2;
@@ -667,6 +723,10 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pn.cache = static_cast<uint16_t*>(cache);
     pn.slots = slot_mapping;
     pn.num_slots = num_slots;
+    pn.w8a8 = h->w8a8 ? 1 : 0;
+    pn.x_scale = h->xscale;
+    pn.w_scale = h->wscale;
+    pn.nscale = h->nscale;
 
     ExpandParams pb{};
     pb.T = d.T;
@@ -704,6 +764,10 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pb.q_codes = out_q_int8;
     pb.q_scale = out_scale;
     pb.tma_store = h->tma_store ? 1 : 0;
+    pb.w8a8 = h->w8a8 ? 1 : 0;
+    pb.a_scale = h->nscale;
+    pb.w_scale_q = h->wscale ? h->wscale + h->NA : nullptr;
+    pb.w_scale_kv = h->wscale ? h->wscale + h->NA + (Lq > 0 ? h->NQ : 0) : nullptr;
 
     // the per-token quant kernel (the per-head quant runs in the q epilogue)
     QuantParams pq{h->qws, h->amax, Lq > 0 && !per_head ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
@@ -759,6 +823,12 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         }
         return MLA_OK;
     }
+    int ev = 1;  // next timing-hook event
+    if (h->w8a8) {  // AT-05 on x: the compression's INT8 input
+        QuantXParams px{static_cast<const uint16_t*>(x), d.T, d.D, h->xq, h->xscale};
+        if ((e = launch_quant_x(px, st)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_x_kernel");
+        if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+    }
     const int jobs_a = pa.n_tiles * pa.m_tiles * pa.splits;
     // one split: the compression writes the BF16 row and the norm reads it
     if (h->cpair) {
@@ -780,10 +850,9 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
             cudaSuccess)
             return cuda_fail(e, "launch mla_compress_kernel");
     }
-    if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
+    if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if ((e = launch_norm_rope(pn, st)) != cudaSuccess) return cuda_fail(e, "launch mla_norm_rope_kernel");
-    if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
-    int ev = 3;  // next timing-hook event
+    if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     if (h->pair) {
         ExpandParams pp = pb;
         pp.m_tiles = h->pair_m_tiles;
@@ -889,6 +958,19 @@ int mla_prolog_quant_rows(const float* y, int32_t rows, int32_t row_len, int8_t*
     return e == cudaSuccess ? MLA_OK : cuda_fail(e, "launch mla_quant_kernel");
 }
 
+int mla_prolog_load_w8a8(mla_prolog_t h, const int8_t* W_a, const int8_t* W_b, const float* w_scale, void* stream) {
+    if (!h || !h->w8a8 || !W_a || !W_b || !w_scale) return MLA_ERR_INVALID_ARG;
+    if (!aligned(W_a, 16) || !aligned(W_b, 16) || !aligned(w_scale, 4)) return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if ((e = launch_widen_i8(W_a, h->wa16, h->wa_elems, st)) != cudaSuccess) return cuda_fail(e, "widen W_a");
+    if ((e = launch_widen_i8(W_b, h->wb16, h->wb_elems, st)) != cudaSuccess) return cuda_fail(e, "widen W_b");
+    if ((e = cudaMemcpyAsync(h->wscale, w_scale, h->n_wscale * 4, cudaMemcpyDefault, st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(w_scale)");
+    h->w8_loaded = true;
+    return MLA_OK;
+}
+
 int mla_prolog_set_wait_timeout(mla_prolog_t h, uint64_t timeout_ns) {
     if (!h || timeout_ns == 0) return MLA_ERR_INVALID_ARG;
     h->timeout_ns = timeout_ns;
@@ -929,6 +1011,7 @@ bool quant_kernel_runs(mla_prolog_t h) {
 // in launch order, with the current tuning; returns how many.
 int standard_kernels(mla_prolog_t h, const char* (&names)[kKernelCount]) {
     int n = 0;
+    if (h->w8a8) names[n++] = "mla_quant_x_kernel";
     names[n++] = h->cpair ? "mla_compress_pair_kernel" : "mla_compress_kernel";
     names[n++] = "mla_norm_rope_kernel";
     if (h->pair && kvres_active(h)) {
@@ -978,6 +1061,18 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
             src = h->qws ? h->amax : nullptr;
             n = T * 4;
             break;
+        case MLA_TAP_X_CODES:
+            src = h->xq;
+            n = T * d.D * 2;
+            break;
+        case MLA_TAP_X_SCALE:
+            src = h->xscale;
+            n = T * 4;
+            break;
+        case MLA_TAP_NORM_SCALE:
+            src = h->nscale;
+            n = T * 8;
+            break;
         default: return MLA_ERR_INVALID_ARG;
     }
     if (!src || bytes != n) return MLA_ERR_INVALID_ARG;
@@ -990,7 +1085,7 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
     if (!h) return MLA_ERR_INVALID_ARG;
     switch (key) {
         case MLA_TUNE_COMPRESS_GROUP:
-            if (value < 1 || value > 64) return MLA_ERR_INVALID_ARG;
+            if (value < 1 || value > (h->w8a8 ? kW8ChainKb : 64)) return MLA_ERR_INVALID_ARG;
             h->group_a = value;
             return MLA_OK;
         case MLA_TUNE_COMPRESS_COMPENSATED:

@@ -845,7 +845,7 @@ struct RoleCounters {
 // the TwoSum compensation registers (the drained chains are summed with plain
 // FP32 adds whatever p.compensated says), which leaves room for 256 columns
 // per tile.
-template <int BN_MAX, int STAGES, int CBN, int CG = 1, bool COMP = true>
+template <int BN_MAX, int STAGES, int CBN, int CG = 1, bool COMP = true, bool W8 = false>
 __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_x,
                                                const CUtensorMap* tm_wa, const CompressParams& p, RoleCounters& rc,
                                                int first, int stride) {
@@ -936,11 +936,21 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
             for (int c = 0; c < HALF / 2; ++c) acc[c] = 0ull;
 #pragma unroll
             for (int c = 0; c < NC; ++c) cmp[c] = 0ull;
-            const bool comp = COMP && p.compensated;
+            const bool comp = COMP && p.compensated && !W8;
             constexpr bool LD32 = !COMP && HALF < 128;  // (no spills at 168 registers)
-            // 16 drained columns into the sums
+            // 16 drained columns into the sums (W8A8: each chain's sums are
+            // exact integers, added in int32, two per register pair)
             auto drain16 = [&](int c, const float* v) {
-                if (comp) {
+                if constexpr (W8) {
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const uint64_t a = acc[(c + e) / 2];
+                        const uint32_t lo = static_cast<uint32_t>(a) + static_cast<uint32_t>(__float2int_rn(v[e]));
+                        const uint32_t hi =
+                            static_cast<uint32_t>(a >> 32) + static_cast<uint32_t>(__float2int_rn(v[e + 1]));
+                        acc[(c + e) / 2] = (static_cast<uint64_t>(hi) << 32) | lo;
+                    }
+                } else if (comp) {
 #pragma unroll
                     for (int e = 0; e < 16; e += 2)
                         two_sum_add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0], pk2(v[e], v[e + 1]));
@@ -982,10 +992,21 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
                 for (int c = 0; c < HALF; c += 8) {
                     if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA) {
                         float o[8];
+                        if constexpr (W8) {  // AT-06: ((float)y * x_scale) * w_scale
+                            const float sx = p.x_scale[t];
+                            const float* ws = p.w_scale + n0 + half * HALF + c;
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2)
-                            upk2(COMP ? add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0]) : acc[(c + e) / 2], o[e],
-                                 o[e + 1]);
+                            for (int e = 0; e < 8; e += 2) {
+                                const uint64_t a = acc[(c + e) / 2];
+                                o[e] = w8_dequant(static_cast<int>(static_cast<uint32_t>(a)), sx, ws[e]);
+                                o[e + 1] = w8_dequant(static_cast<int>(static_cast<uint32_t>(a >> 32)), sx, ws[e + 1]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2)
+                                upk2(COMP ? add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0]) : acc[(c + e) / 2],
+                                     o[e], o[e + 1]);
+                        }
                         *reinterpret_cast<uint4*>(dst + c) = make_uint4(
                             pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                             pack_bf16x2(o[6], o[7]));
@@ -998,9 +1019,14 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
                     if (half * HALF + c < p.bn && n0 + half * HALF + c < p.NA) {
                         float o[8];
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2)
-                            upk2(COMP ? add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0]) : acc[(c + e) / 2], o[e],
-                                 o[e + 1]);
+                        for (int e = 0; e < 8; e += 2) {
+                            if constexpr (W8)  // int32 partials, summed and dequantised by the norm
+                                o[e] = __uint_as_float(static_cast<uint32_t>(acc[(c + e) / 2])),
+                                o[e + 1] = __uint_as_float(static_cast<uint32_t>(acc[(c + e) / 2] >> 32));
+                            else
+                                upk2(COMP ? add2(acc[(c + e) / 2], cmp[COMP ? (c + e) / 2 : 0]) : acc[(c + e) / 2],
+                                     o[e], o[e + 1]);
+                        }
                         st_v8(dst + c, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
                     }
                 }
@@ -1009,6 +1035,35 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
         if (!ok && lane == 0) atomicOr(p.status, kStatusWaitTimeout);
     }
     return ok;
+}
+
+// ---- W8A8 expansion: exact integer accumulators -> dequantised values ----
+//
+// Every code is an integer of magnitude <= 127, exact in BF16, so the
+// tensor core's products are exact integers; a chain of at most kW8ChainKb
+// K blocks keeps every partial sum an integer below 2^24, where each FP32
+// add is exact.  A longer K runs as two chains into the two accumulator
+// buffers (b0 first half, b1 second half).  This warp converts its share of
+// the tile's columns in its lane quarter: y = int(b0) + int(b1), then
+// ((float)y * a_scale) * w_scale[n] back into b0, for the epilogue to read
+// as it reads a BF16-mode accumulator.  Columns past n_end (a ragged last
+// tile) get scale 0.  Whole warp.
+__device__ __forceinline__ void w8_dequant_tile(uint32_t tb0, uint32_t tb1, bool two, int width, int half_idx,
+                                                float a_scale, const float* w_scale, int n0, int n_end) {
+    const int hw = ((width + 31) / 32) * 16;  // columns per warp of the quarter, a multiple of 16
+    const int c0 = half_idx * hw, c1 = c0 + hw < width ? c0 + hw : width;
+    for (int c = c0; c < c1; c += 16) {
+        float v[16], u[16];
+        tmem_ld16(tb0 + c, v);
+        if (two) tmem_ld16(tb1 + c, u);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int y = __float2int_rn(v[e]) + (two ? __float2int_rn(u[e]) : 0);
+            const int n = n0 + c + e;
+            v[e] = w8_dequant(y, a_scale, n < n_end ? w_scale[n] : 0.0f);
+        }
+        tmem_st16(tb0 + c, v);
+    }
 }
 
 // ---- expansion phase: this CTA's jobs (round robin or balanced table) ----
@@ -1023,7 +1078,7 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
 // covers rows [256 m, 256 m + 256), this CTA's epilogue rows 128 * rank on.
 // With TS (a kernel with the store staging area) and p.tma_store the kv
 // tiles and the per-token q tiles leave through the store ring.
-template <int BN_MAX, int STAGES, int CG = 1, bool TS = false, class Dep>
+template <int BN_MAX, int STAGES, int CG = 1, bool TS = false, bool W8 = false, class Dep>
 __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_aq,
                                              const CUtensorMap* tm_akv, const CUtensorMap* tm_bq,
                                              const CUtensorMap* tm_bkv, const ExpandParams& p, RoleCounters& rc,
@@ -1059,12 +1114,22 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         if (lane == 0 && rank == 0) {  // a pair's MMAs are issued by its even CTA
             const uint32_t idesc_q = idesc_bf16_f32(TM, p.q_wide ? kQWide : Dn + R);
             const uint32_t idesc_kv = idesc_bf16_f32(TM, p.bn_kv);
-            for (int i = jobs.begin; i < jobs.end && ok; ++i, ++rc.chain) {
+            for (int i = jobs.begin; i < jobs.end && ok; ++i) {
                 int tile, m;
                 expand_job(p, jobs[i], tile, m);
                 const bool q = tile < p.nq_tiles;
-                ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, q ? p.kb_q : p.kb_kv, tmem,
-                                                   q ? idesc_q : idesc_kv, p.timeout_ns);
+                const int nkb = q ? p.kb_q : p.kb_kv;
+                if (W8 && nkb > kW8ChainKb) {  // W8A8: two exact chains, one per accumulator buffer
+                    ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, nkb / 2, tmem,
+                                                       q ? idesc_q : idesc_kv, p.timeout_ns) &&
+                         mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain + 1, nkb - nkb / 2, tmem,
+                                                       q ? idesc_q : idesc_kv, p.timeout_ns);
+                    rc.chain += 2;
+                } else {
+                    ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, nkb, tmem, q ? idesc_q : idesc_kv,
+                                                       p.timeout_ns);
+                    rc.chain += 1;
+                }
             }
             if (!ok) raise_abort(sm, p.status);
         }
@@ -1076,19 +1141,41 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         int cur_m = -1;
         RowCtx ctx;
         const StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes};
-        for (int i = jobs.begin; i < jobs.end; ++i, ++rc.chain) {
+        for (int i = jobs.begin; i < jobs.end; ++i) {
             int tile, m;
             expand_job(p, jobs[i], tile, m);
             if (m != cur_m) {  // before waiting for the accumulator
                 load_row_ctx(p, m * TM + rank * kBM + row, ctx);
                 cur_m = m;
             }
-            if (!epi_acquire(sm, rc.chain, p.timeout_ns)) {
+            const bool is_q = tile < p.nq_tiles;
+            const int chains = W8 && (is_q ? p.kb_q : p.kb_kv) > kW8ChainKb ? 2 : 1;
+            bool got = epi_acquire(sm, rc.chain, p.timeout_ns);
+            if (chains == 2) got = got && epi_acquire(sm, rc.chain + 1, p.timeout_ns);
+            const uint32_t tbase = tmem + lane_off + (rc.chain & 1) * BN_MAX;
+            if constexpr (W8) {
+                if (got) {
+                    const int t = ctx.t;
+                    const float as = t < p.T ? p.a_scale[2 * t + (is_q ? 0 : 1)] : 0.0f;
+                    const int bq = p.q_wide ? kQWide : Dn + R;
+                    if (is_q)
+                        w8_dequant_tile(tbase, tmem + lane_off + ((rc.chain + 1) & 1) * BN_MAX, chains == 2, bq,
+                                        half_idx, as, p.w_scale_q, tile * bq, p.NQ);
+                    else
+                        w8_dequant_tile(tbase, tmem + lane_off + ((rc.chain + 1) & 1) * BN_MAX, chains == 2,
+                                        p.bn_kv, half_idx, as, p.w_scale_kv, (tile - p.nq_tiles) * p.bn_kv, p.NKV);
+                }
+                // every warp's columns are converted before any warp reads the
+                // tile (the q epilogues read across the two column halves)
+                tc_fence_before();
+                got = named_bar_and(2, kEpiThreads, got);
+                tc_fence_after();
+            }
+            if (!got) {
                 if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
                 ok = false;
                 break;
             }
-            const uint32_t tbase = tmem + lane_off + (rc.chain & 1) * BN_MAX;
             const int y0 = m * TM + rank * kBM + quarter * 32;
             if (TS && p.tma_store && tile >= p.nq_tiles)
                 expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx, y0);
@@ -1101,6 +1188,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             else
                 expand_kv_epilogue(p, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx);
             epi_release<CG>(sm, rc.chain);
+            if (chains == 2) epi_release<CG>(sm, rc.chain + 1);
+            rc.chain += chains;
         }
         // every tensor store has written its box before the CTA leaves
         if (TS && lane == 0) bulk_wait_all();

@@ -49,6 +49,12 @@ struct CompressParams {
     // issued by the producer warp's spare lanes.
     const uint8_t* l2_fetch;
     uint64_t l2_fetch_bytes;
+    // W8A8: x and W_a hold INT8 codes as BF16 integers; each chain's sums are
+    // exact integers, added in int32, and leave as AT-06 dequantised BF16
+    // ((float)y * x_scale[t]) * w_scale[n] (one split) or as int32 partials.
+    int w8a8;
+    const float* x_scale;  // [T]
+    const float* w_scale;  // [NA]
 };
 
 // Per-token reduction of the partials, BF16 cast, RMSNorm of c_q and c_kv,
@@ -73,6 +79,13 @@ struct NormRopeParams {
     uint16_t* cache;
     const int32_t* slots;
     long long num_slots;
+    // W8A8: split-K partials are int32 (dequantised here with x_scale and
+    // w_scale), and the normed c_q and c_kv rows leave as per-token INT8
+    // codes (as BF16 integers) with their scales in nscale[t] = (c_q, c_kv).
+    int w8a8;
+    const float* x_scale;  // [T]
+    const float* w_scale;  // [NA]
+    float* nscale;         // [T][2]
 };
 
 // Expansion projections.  Tiles [0, nq_tiles) are q heads (one head of
@@ -110,9 +123,29 @@ struct ExpandParams {
     // the store ring, R = 64 and Dn a multiple of 64, so every 64-column piece
     // of a tile is nope columns or one head's whole rope slice.
     int q_wide;
+    // W8A8: the activations are INT8 codes (as BF16 integers) with a scale
+    // per token (a_scale[2t] for c_q, a_scale[2t + 1] for c_kv), the weights
+    // INT8 codes with one scale per output row.  The epilogue first turns
+    // the exact integer accumulator into ((float)y * a_scale) * w_scale.
+    int w8a8;
+    const float* a_scale;     // [T][2]
+    const float* w_scale_q;   // [NQ]
+    const float* w_scale_kv;  // [NKV]
 };
 
 constexpr int kQWide = 256;
+// W8A8: K blocks of one exact accumulation chain.  A chain of k blocks sums
+// 64 k products of magnitude <= 127^2, so every partial sum is an integer
+// below 2^24 (exact in FP32) while 64 k * 127^2 < 2^24, i.e. k <= 16.
+constexpr int kW8ChainKb = 16;
+
+// W8A8: per-token INT8 codes of a BF16 matrix (x), written as BF16 integers.
+struct QuantXParams {
+    const uint16_t* x;  // [rows][cols] BF16
+    int rows, cols;
+    uint16_t* codes;    // [rows][cols] BF16 integers in [-127, 127]
+    float* scale;       // [rows]
+};
 
 struct QuantParams {
     const float* y;          // [rows][row_len]
@@ -500,8 +533,22 @@ cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtens
 cudaError_t expand_kv_pair_max_active(int* clusters);
 cudaError_t launch_expand_kv_pair(int pairs, const CUtensorMap& tm_akv, const CUtensorMap& tm_bkv,
                                   const OutTensorMaps& om, const ExpandParams& p, int group, cudaStream_t st);
+// The W8A8 instantiations (gemm_w8a8.cu), chosen by the launchers above
+// when the parameters ask for W8A8.
+cudaError_t gemm_w8a8_set_attributes();
+cudaError_t launch_compress_w8(GemmShape s, int grid, const CUtensorMap& tm_x, const CUtensorMap& tm_wa,
+                               const CompressParams& p, cudaStream_t st);
+cudaError_t launch_expand_w8(GemmShape s, int grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
+                             const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
+                             const ExpandParams& p, cudaStream_t st);
+cudaError_t launch_expand_pair_w8(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
+                                  const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
+                                  const ExpandParams& p, cudaStream_t st);
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t st);
+// INT8 codes -> the same integers as BF16 (exact), n elements.
+cudaError_t launch_widen_i8(const int8_t* src, uint16_t* dst, size_t n, cudaStream_t st);
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st);
 
 }  // namespace mlap

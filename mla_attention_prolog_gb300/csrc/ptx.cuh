@@ -349,6 +349,23 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
         : "memory");
 }
 
+// Stores 16 consecutive 32-bit columns of this thread's TMEM lane (shape
+// 32x32b: lane i of the warp writes TMEM lane base + i) and waits until the
+// stores have completed.  Whole warp.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
 // Loads 16 consecutive FP32 columns of this warp's 32 TMEM lanes (one lane
 // per thread) and waits for them.  Whole warp, converged.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -500,5 +517,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// W8A8: symmetric INT8 codes of two values, rint(v * inv) (ties to even)
+// clamped to +-127, as two BF16 integers (exact); inv = 0 gives codes 0.
+__device__ __forceinline__ uint32_t code_bf16x2(float a, float b, float inv) {
+    int qa = __float2int_rn(__fmul_rn(a, inv));
+    int qb = __float2int_rn(__fmul_rn(b, inv));
+    qa = qa > 127 ? 127 : (qa < -127 ? -127 : qa);
+    qb = qb > 127 ? 127 : (qb < -127 ? -127 : qb);
+    return pack_bf16x2(static_cast<float>(qa), static_cast<float>(qb));
+}
+
+// W8A8 dequantisation of an exact integer product (AT-06): FP32
+// ((float)y * a_scale) * w_scale, each step correctly rounded.
+__device__ __forceinline__ float w8_dequant(int y, float a_scale, float w_scale) {
+    return __fmul_rn(__fmul_rn(__int2float_rn(y), a_scale), w_scale);
+}
 
 }  // namespace mlap

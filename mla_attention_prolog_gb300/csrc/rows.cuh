@@ -277,6 +277,7 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
     const int ndst = p.H + (cache_row ? 2 : 1);  // rope-slice destinations (kpe_dst)
     if (!valid) {
         if (lane == 0) atomicOr(p.status, kStatusPositionRange);
+        if (lane == 0 && p.w8a8) p.nscale[2 * t] = p.nscale[2 * t + 1] = 0.0f;
         const uint4 z = make_uint4(0, 0, 0, 0);
         for (int i = lane * 8; i < Lq + Lkv; i += 256) {
             *reinterpret_cast<uint4*>(nrow + i) = z;
@@ -325,7 +326,19 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
         for (int u = 0; u < kB; ++u)
             if (i0 + 128 * u < NA) take4(i0 + 128 * u, a[u]);
     }
-    for (int i = lane * 4; splits > 1 && i < NA; i += 128) {
+    for (int i = lane * 4; splits > 1 && p.w8a8 && i < NA; i += 128) {
+        // W8A8: exact int32 partials, summed exactly, then dequantised
+        int4 a = *reinterpret_cast<const int4*>(prow + i);
+        for (int sp = 1; sp < splits; ++sp) {
+            const int4 r = *reinterpret_cast<const int4*>(prow + sp * sstride + i);
+            a.x += r.x, a.y += r.y, a.z += r.z, a.w += r.w;
+        }
+        const float sx = p.x_scale[t];
+        const float4 ws = *reinterpret_cast<const float4*>(p.w_scale + i);
+        take4(i, make_float4(w8_dequant(a.x, sx, ws.x), w8_dequant(a.y, sx, ws.y), w8_dequant(a.z, sx, ws.z),
+                             w8_dequant(a.w, sx, ws.w)));
+    }
+    for (int i = lane * 4; splits > 1 && !p.w8a8 && i < NA; i += 128) {
         float4 a = *reinterpret_cast<const float4*>(prow + i), cmp = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int sp = 1; sp < splits; ++sp) {
             const float4 r = *reinterpret_cast<const float4*>(prow + sp * sstride + i);
@@ -342,6 +355,7 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
     const float rstd_q = Lq > 0 ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_q, p.eps))) : 0.0f;
     const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
     __syncwarp();
+    float amax_q = 0.0f, amax_kv = 0.0f;  // W8A8: max |normed| of c_q and c_kv
     for (int i = lane * 8; i < Lq + Lkv; i += 256) {
         const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
         const uint4 gv = *reinterpret_cast<const uint4*>(gamma + i);
@@ -349,15 +363,47 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
         const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
         const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
         uint32_t o[4];
+        float m = 0.0f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float y0 = __fmul_rn(__fmul_rn(bf16_lo(xs[e]), rstd), bf16_lo(gs[e]));
             const float y1 = __fmul_rn(__fmul_rn(bf16_hi(xs[e]), rstd), bf16_hi(gs[e]));
             o[e] = pack_bf16x2(y0, y1);
+            m = fmaxf(m, fmaxf(fabsf(bf16_lo(o[e])), fabsf(bf16_hi(o[e]))));
         }
         const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(nrow + i) = ov;
+        if (p.w8a8) {  // the normed values stay here until their codes are known
+            *reinterpret_cast<uint4*>(crow + i) = ov;
+            if (i < Lq)
+                amax_q = fmaxf(amax_q, m);
+            else
+                amax_kv = fmaxf(amax_kv, m);
+        } else {
+            *reinterpret_cast<uint4*>(nrow + i) = ov;
+        }
         if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
+    }
+    if (p.w8a8) {
+        // AT-11: the normed c_q and c_kv rows quantised per token, the
+        // expansions' INT8 inputs (each lane re-reads its own chunks)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            amax_q = fmaxf(amax_q, __shfl_xor_sync(0xffffffffu, amax_q, o));
+            amax_kv = fmaxf(amax_kv, __shfl_xor_sync(0xffffffffu, amax_kv, o));
+        }
+        const float inv_q = amax_q > 0.0f ? __fdiv_rn(127.0f, amax_q) : 0.0f;
+        const float inv_kv = amax_kv > 0.0f ? __fdiv_rn(127.0f, amax_kv) : 0.0f;
+        for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+            const uint4 yv = *reinterpret_cast<const uint4*>(crow + i);
+            const float inv = i < Lq ? inv_q : inv_kv;
+            *reinterpret_cast<uint4*>(nrow + i) =
+                make_uint4(code_bf16x2(bf16_lo(yv.x), bf16_hi(yv.x), inv), code_bf16x2(bf16_lo(yv.y), bf16_hi(yv.y), inv),
+                           code_bf16x2(bf16_lo(yv.z), bf16_hi(yv.z), inv), code_bf16x2(bf16_lo(yv.w), bf16_hi(yv.w), inv));
+        }
+        if (lane == 0) {
+            p.nscale[2 * t] = amax_q > 0.0f ? __fdiv_rn(amax_q, 127.0f) : 0.0f;
+            p.nscale[2 * t + 1] = amax_kv > 0.0f ? __fdiv_rn(amax_kv, 127.0f) : 0.0f;
+        }
     }
     const uint16_t* kp = crow + Lq + Lkv;
     for (int i = lane; i < half; i += 32) {

@@ -95,13 +95,81 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
     quant_span(p, row, c0, c1, amax, threadIdx.x, kQuantThreads);
 }
 
+// ------------------------------------------------------------ W8A8
+
+// One CTA per row of x: the per-token symmetric INT8 quantisation of the
+// BF16 row (amax = max |x|, inv = 127/amax, code = rint(x * inv) ties to
+// even, clamped to +-127, scale = amax/127, all correctly rounded FP32;
+// AT-05 in the PyPTO-Gym AT-10 article, section 四).  The codes are written
+// as BF16, which holds every integer of magnitude <= 127 exactly: the form
+// the BF16 tensor-core path multiplies.  A zero row gives codes 0, scale 0.
+constexpr int kQuantXThreads = 256;
+
+__global__ void __launch_bounds__(kQuantXThreads) mla_quant_x_kernel(const QuantXParams p) {
+    __shared__ float red[kQuantXThreads / 32];
+    const int row = blockIdx.x;
+    const uint16_t* x = p.x + static_cast<size_t>(row) * p.cols;
+    uint16_t* out = p.codes + static_cast<size_t>(row) * p.cols;
+    float m = 0.0f;
+    for (int i = threadIdx.x * 8; i < p.cols; i += kQuantXThreads * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(x + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[e])), fabsf(bf16_hi(w[e]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float amax = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kQuantXThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    for (int i = threadIdx.x * 8; i < p.cols; i += kQuantXThreads * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(x + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = code_bf16x2(bf16_lo(w[e]), bf16_hi(w[e]), inv);
+        *reinterpret_cast<uint4*>(out + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (threadIdx.x == 0) p.scale[row] = amax > 0.0f ? __fdiv_rn(amax, 127.0f) : 0.0f;
+}
+
+// INT8 weight codes -> BF16 integers, 16 per thread step.
+__global__ void __launch_bounds__(256) mla_widen_i8_kernel(const int8_t* src, uint16_t* dst, size_t n) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x * 16;
+    for (size_t i = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 16; i < n; i += stride) {
+        if (i + 16 <= n) {
+            const int4 v = *reinterpret_cast<const int4*>(src + i);
+            const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y),
+                                   static_cast<uint32_t>(v.z), static_cast<uint32_t>(v.w)};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float b0 = static_cast<float>(static_cast<int8_t>(w[e] & 0xFF));
+                const float b1 = static_cast<float>(static_cast<int8_t>((w[e] >> 8) & 0xFF));
+                const float b2 = static_cast<float>(static_cast<int8_t>((w[e] >> 16) & 0xFF));
+                const float b3 = static_cast<float>(static_cast<int8_t>(w[e] >> 24));
+                o[2 * e] = pack_bf16x2(b0, b1);
+                o[2 * e + 1] = pack_bf16x2(b2, b3);
+            }
+            *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + i + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+            for (size_t k = i; k < n; ++k)
+                dst[k] = static_cast<uint16_t>(pack_bf16x2(static_cast<float>(src[k]), 0.0f) & 0xFFFFu);
+        }
+    }
+}
+
 // ------------------------------------------------------------ launchers
 
 cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
     // split-K partials of a decode batch: a wide CTA per token keeps every
     // split's load in flight; prefill (many tokens): one warp per token
-    if (p.splits > 1 && p.T <= 2 * kBM)
+    if (p.splits > 1 && p.T <= 2 * kBM && !p.w8a8)
         return launch_kernel(mla_norm_rope_kernel<512, 16>, dim3(p.T), dim3(512),
                              norm_token_smem_bytes(p.NA, p.R, p.Lq, p.Lkv), st, true, p);
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
@@ -115,6 +183,19 @@ cudaError_t launch_quant(const QuantParams& p_in, cudaStream_t st, bool pdl) {
     p.chunk = p.amax ? kQuantChunk : p.row_len;
     const int chunks = (p.row_len + p.chunk - 1) / p.chunk;
     return launch_kernel(mla_quant_kernel, dim3(p.rows, chunks), dim3(kQuantThreads), 0, st, pdl, p);
+}
+
+cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t st) {
+    if (p.rows == 0) return cudaSuccess;
+    return launch_kernel(mla_quant_x_kernel, dim3(p.rows), dim3(kQuantXThreads), 0, st, false, p);
+}
+
+cudaError_t launch_widen_i8(const int8_t* src, uint16_t* dst, size_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const size_t threads = (n + 15) / 16;
+    const size_t blocks = std::min<size_t>((threads + 255) / 256, 152 * 8);
+    return launch_kernel(mla_widen_i8_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, false, src, dst,
+                         n);
 }
 
 }  // namespace mlap

@@ -57,7 +57,8 @@ def _dims(**kw):
     (dict(eps=float("nan")), -2), (dict(eps=-1.0), -2), (dict(q_lora_rank=24, flags=1), -2),
     (dict(q_lora_rank=64, flags=0), -1), (dict(flags=1), -1), (dict(flags=4), -1),
     (dict(q_lora_rank=64, flags=1, nope_dim=256, rope_dim=64), -2),
-    (dict(flags=8), -1), (dict(flags=2 | 4), -1), (dict(flags=16), -1),   # q variants without a q path
+    (dict(flags=8), -1), (dict(flags=2 | 4), -1), (dict(flags=32), -1),   # q variants without a q path; unknown
+    (dict(flags=16, kv_lora_rank=2064), -2), (dict(q_lora_rank=2064, flags=1 | 16), -2),  # W8A8: K <= 2048
     (dict(q_lora_rank=64, flags=1 | 32), -1), (dict(q_lora_rank=64, flags=8), -1),
 ])
 def test_create_rejects_bad_dims_without_touching_cuda(L, kw, code):

@@ -1,0 +1,224 @@
+"""GPU parity of the W8A8 prolog (MLA_PROLOG_W8A8) against the oracle.
+
+What is integer work, or FP32 work on exact integers in the same order on
+both sides, is compared bit for bit: x's per-token codes and scales, the
+rotated k_pe (from the exactly dequantised compression), and -- for every
+token whose normed-row codes and scales agree with the oracle's -- every
+output.  The normed rows themselves come out of an FP32 sum of squares whose
+order differs between the two sides (the BF16 mode's RMSNorm), so their
+codes may differ by one on a few elements; those tokens are held to the
+BF16 mode's bar for K and V and, for q, to their dequantised values (codes
+times scale) within 1e-2 of the row's largest magnitude.  A deterministic
+case with every code at +-127 checks the integer products at their largest
+magnitudes (past 2^24 in one chain).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import alloc_outputs, bf16_within, device_inputs
+from mla_attention_prolog_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    from mla_attention_prolog_gb300 import build
+    build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def _w8(name, T=None, **over):
+    w = wl.WORKLOADS[name]
+    d = dataclasses.replace(w.dims, flags=w.dims.flags | wl.W8A8, **over)
+    return w, (d.with_T(T) if T else d)
+
+
+def _run_gpu(d, inp, ww, cache=None):
+    dins = device_inputs(inp, DEV)
+    outs = alloc_outputs(d, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    p.load_w8a8(torch.from_numpy(ww.W_a).to(DEV), torch.from_numpy(ww.W_b).to(DEV),
+                torch.from_numpy(ww.w_scale).to(DEV))
+    args = (dins["x"], dins["gamma"], None, None, dins["positions"], dins["cos_sin"],
+            outs["out_k"].t, outs["out_v"].t, outs["out_kpe"].t,
+            outs["out_q_int8"].t if "out_q_int8" in outs else None,
+            outs["out_scale"].t if "out_scale" in outs else None)
+    if cache is None:
+        p.run(*args)
+    else:
+        p.run_cached(*args, cache[0], cache[1])
+    status = p.device_status()
+    taps = {
+        "x_codes": p.tap(binding.TAP_X_CODES).float().cpu().numpy(),
+        "x_scale": p.tap(binding.TAP_X_SCALE).cpu().numpy(),
+        "n_codes": p.tap(binding.TAP_NORMED).float().cpu().numpy(),
+        "n_scale": p.tap(binding.TAP_NORM_SCALE).cpu().numpy(),
+    }
+    names = p.kernel_names()
+    p.close()
+    for k, g in outs.items():
+        assert g.guards_intact(), f"{k}: write outside the buffer"
+    return status, outs, taps, names
+
+
+def _sample(T, n, seed=7):
+    if T <= n:
+        return None
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(np.arange(1, T - 1), n - 2, replace=False)
+    return np.array(sorted({0, T - 1} | set(int(i) for i in rest)), np.int32)
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16) if t.dtype == torch.bfloat16 else \
+        t.cpu().numpy()
+
+
+def check_w8a8(d, inp, ww, sample=384, n_code_frac=2e-3):
+    status, outs, taps, names = _run_gpu(d, inp, ww)
+    assert names[0] == "mla_quant_x_kernel"
+    tok = _sample(d.T, sample)
+    ref = oracle.mla_prolog_w8a8(d, inp.x, inp.gamma, ww.W_a, ww.W_b, ww.w_scale, inp.positions, inp.cos_sin,
+                                 tokens=tok, taps=True)
+    rows = np.arange(d.T) if tok is None else tok
+    sel = torch.from_numpy(rows.astype(np.int64)).to(DEV)
+    # x's codes and scales: bit-exact
+    assert np.array_equal(taps["x_codes"][rows], ref["x_codes"].astype(np.float32))
+    assert np.array_equal(taps["x_scale"][rows], ref["x_scale"])
+    # rotated k_pe: from the exact compression, same FP32 RoPE -> bit-exact
+    assert np.array_equal(_bits(outs["out_kpe"].t[sel]), ref["out_kpe"])
+    # normed-row codes: the RMSNorm's sum order may move a code by one
+    nc, nref = taps["n_codes"][rows], ref["n_codes"].astype(np.float32)
+    dq = np.abs(nc - nref)
+    assert dq.max() <= 1 and dq.mean() <= n_code_frac, (dq.max(), dq.mean())
+    ns = taps["n_scale"][rows]
+    rel = np.abs(ns - ref["n_scale"]) / np.maximum(ref["n_scale"], 1e-30)
+    assert np.all(rel <= 2.0 ** -7), rel.max()
+    same = np.all(nc == nref, axis=1) & np.all(ns == ref["n_scale"], axis=1)
+    assert same.mean() >= 0.5, f"only {same.mean():.2f} of the tokens have the oracle's normed codes"
+    ok_k, ok_v = _bits(outs["out_k"].t[sel]), _bits(outs["out_v"].t[sel])
+    assert np.array_equal(ok_k[same], ref["out_k"][same])
+    assert np.array_equal(ok_v[same], ref["out_v"][same])
+    bf16_within(outs["out_k"].t[sel], ref["out_k"], "out_k")
+    bf16_within(outs["out_v"].t[sel], ref["out_v"], "out_v")
+    if d.q_lora_rank:
+        qc, qs = outs["out_q_int8"].t[sel].cpu().numpy(), outs["out_scale"].t[sel].cpu().numpy()
+        assert np.array_equal(qc[same], ref["out_q_int8"][same])
+        assert np.array_equal(qs[same], ref["out_scale"][same])
+        # a normed code one off moves every q of the token a little, and with it
+        # the q scale and many codes: those tokens are held to the dequantised
+        # values, within 1e-2 of their row's largest magnitude
+        if (~same).any():
+            rq = ref["out_q_int8"][~same].astype(np.float64)
+            rs, gs = ref["out_scale"][~same].astype(np.float64), qs[~same].astype(np.float64)
+            if d.quant_per_head:
+                rs, gs = rs[..., None], gs[..., None]
+            else:
+                rs, gs = rs[:, None, None], gs[:, None, None]
+            want, got = rq * rs, qc[~same].astype(np.float64) * gs
+            assert np.all(np.abs(gs - rs) <= 1e-2 * rs)
+            assert np.all(np.abs(got - want) <= 1e-2 * 127 * rs)
+    return status, outs, ref, same
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 0), ("tiny_q", 0), ("v2lite_decode", 0), ("v2lite_prefill", 0),
+                                    ("v3_decode", 0), ("v3_decode", 200), ("v3_prefill", 1000),
+                                    ("v3_prefill", 0)])
+def test_w8a8_parity(name, T):
+    w, d = _w8(name, T)
+    inp = wl.make_inputs(w, d)
+    ww = wl.make_w8a8_weights(w, d)
+    status, _, _, same = check_w8a8(d, inp, ww, sample=256 if d.T > 4096 else 384)
+    print(f"{name} T={d.T}: {same.mean():.3f} of the tokens bit-exact end to end")
+    assert status == 0
+
+
+@pytest.mark.parametrize("extra", [wl.ROPE_INTERLEAVED, wl.QUANT_PER_HEAD, wl.Q_HEAD_NORM])
+def test_w8a8_q_variants(extra):
+    w, d = _w8("v3_prefill", 300)
+    d = dataclasses.replace(d, flags=d.flags | extra)
+    inp = wl.make_inputs(w, d)
+    same = check_w8a8(d, inp, wl.make_w8a8_weights(w, d))[3]
+    print(f"variant {extra}: {same.mean():.3f} of the tokens bit-exact end to end")
+
+
+@pytest.mark.parametrize("T", [130, 300])
+def test_w8a8_largest_codes_are_exact(T):
+    """Every code +-127 (x rows constant, every weight code 127, gamma 1):
+    the compression sums D 127^2 = 115,612,672 and the q expansion
+    Lq 127^2 = 24,774,144, past 2^24, so one FP32 accumulation chain would
+    round; the weight scales make the compression 2^26 exactly, so the norm
+    gives exactly 1.0 whatever its sum order, and every output is fixed."""
+    w, d = _w8("v3_prefill", T, num_heads=4, max_pos=T)
+    inp = wl.make_inputs(w, d)
+    x = np.full((d.T, d.D), 127.0, np.float32)
+    x[1::2] *= -1.0  # sign per row: codes +-127, x scale 1
+    bits = torch.tensor(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    one = np.full_like(inp.gamma, 0x3F80)  # BF16 1.0
+    inp = dataclasses.replace(inp, x=bits, gamma=one)
+    ww = wl.make_w8a8_weights(w, d)
+    s = np.float32(2.0 ** 26 / (d.D * 127 * 127))
+    ww = dataclasses.replace(ww, W_a=np.full_like(ww.W_a, 127), W_b=np.full_like(ww.W_b, 127),
+                             w_scale=np.full_like(ww.w_scale, s))
+    status, outs, taps, _ = _run_gpu(d, inp, ww)
+    ref = oracle.mla_prolog_w8a8(d, inp.x, inp.gamma, ww.W_a, ww.W_b, ww.w_scale, inp.positions, inp.cos_sin,
+                                 taps=True)
+    assert np.all(np.abs(ref["n_codes"]) == 127)
+    assert np.array_equal(taps["n_codes"], ref["n_codes"].astype(np.float32))
+    assert np.array_equal(taps["n_scale"], ref["n_scale"])
+    for k in ("out_k", "out_v", "out_kpe"):
+        assert np.array_equal(_bits(outs[k].t), ref[k]), k
+    assert np.array_equal(outs["out_q_int8"].t.cpu().numpy(), ref["out_q_int8"])
+    assert np.array_equal(outs["out_scale"].t.cpu().numpy(), ref["out_scale"])
+    assert status == 0
+
+
+def test_w8a8_cache_and_bad_positions():
+    w, d = _w8("v3_decode", 64)
+    inp = wl.make_inputs(w, d)
+    inp.positions[3] = d.max_pos
+    inp.positions[9] = -1
+    ww = wl.make_w8a8_weights(w, d)
+    slots = torch.arange(d.T, dtype=torch.int32, device=DEV).flip(0)
+    cache = torch.zeros((d.T + 5, d.kv_lora_rank + d.rope_dim), dtype=torch.bfloat16, device=DEV)
+    status, outs, taps, _ = _run_gpu(d, inp, ww, cache=(slots, cache))
+    assert status & binding.STATUS_POSITION_RANGE
+    ref = oracle.mla_prolog_w8a8(d, inp.x, inp.gamma, ww.W_a, ww.W_b, ww.w_scale, inp.positions, inp.cos_sin,
+                                 taps=True)
+    for t in (3, 9):
+        assert torch.count_nonzero(outs["out_k"].t[t]) == 0 and np.all(taps["n_scale"][t] == 0)
+    want = np.zeros((d.T + 5, d.kv_lora_rank + d.rope_dim), np.uint16)
+    oracle.scatter_kv_cache(want, slots.cpu().numpy(), ref["normed"], ref["out_kpe"], d.q_lora_rank)
+    bf16_within(cache, want, "kv_cache")
+
+
+def test_w8a8_run_needs_loaded_weights_and_null_pointers():
+    w, d = _w8("tiny")
+    p = binding.MlaProlog.from_dims(d)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    outs = alloc_outputs(d, DEV)
+    with pytest.raises(binding.MlaPrologError):  # nothing loaded yet
+        p.run(dins["x"], dins["gamma"], None, None, dins["positions"], dins["cos_sin"],
+              outs["out_k"].t, outs["out_v"].t, outs["out_kpe"].t)
+    with pytest.raises(ValueError):  # BF16 weights on a W8A8 handle
+        p.run(dins["x"], dins["gamma"], dins["W_a"], dins["W_b"], dins["positions"], dins["cos_sin"],
+              outs["out_k"].t, outs["out_v"].t, outs["out_kpe"].t)
+    d16 = dataclasses.replace(d, flags=0)
+    p16 = binding.MlaProlog.from_dims(d16)
+    ww = wl.make_w8a8_weights(w, d)
+    with pytest.raises(binding.MlaPrologError):  # not a W8A8 handle
+        p16.load_w8a8(torch.from_numpy(ww.W_a).to(DEV), torch.from_numpy(ww.W_b).to(DEV),
+                      torch.from_numpy(ww.w_scale).to(DEV))
+    p.close()
+    p16.close()
