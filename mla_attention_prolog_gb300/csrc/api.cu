@@ -172,6 +172,7 @@ struct mla_prolog {
     uint16_t* xq = nullptr;
     float* xscale = nullptr;
     float* nscale = nullptr;
+    uint32_t* w8_split = nullptr;  // per 128-token tile: the expansions' chain split marks
     size_t wa_elems = 0, wb_elems = 0, n_wscale = 0;
 };
 
@@ -523,8 +524,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->wb_elems = NQw * Lq + static_cast<size_t>(h->NKV) * Lkv;
         h->n_wscale = h->NA + NQw + h->NKV;
         const size_t b_wa = al(h->wa_elems * 2), b_wb = al(h->wb_elems * 2), b_ws = al(h->n_wscale * 4);
-        const size_t b_xq = al(T * d.D * 2), b_xs = al(T * 4), b_ns = al(T * 8);
-        if ((e = cudaMalloc(&h->w8mem, b_wa + b_wb + b_ws + b_xq + b_xs + b_ns)) != cudaSuccess) {
+        const size_t b_xq = al(T * d.D * 2), b_xs = al(T * 4), b_ns = al(T * 8), b_sp = al(h->m_tiles * 4 + 4);
+        if ((e = cudaMalloc(&h->w8mem, b_wa + b_wb + b_ws + b_xq + b_xs + b_ns + b_sp)) != cudaSuccess) {
             cudaFree(h->ws);
             delete h;
             return cuda_fail(e, "cudaMalloc(W8A8 weights)");
@@ -536,6 +537,13 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->xq = reinterpret_cast<uint16_t*>(q + b_wa + b_wb + b_ws);
         h->xscale = reinterpret_cast<float*>(q + b_wa + b_wb + b_ws + b_xq);
         h->nscale = reinterpret_cast<float*>(q + b_wa + b_wb + b_ws + b_xq + b_xs);
+        h->w8_split = reinterpret_cast<uint32_t*>(q + b_wa + b_wb + b_ws + b_xq + b_xs + b_ns);
+        if ((e = cudaMemset(h->w8_split, 0, b_sp)) != cudaSuccess) {
+            cudaFree(h->w8mem);
+            cudaFree(h->ws);
+            delete h;
+            return cuda_fail(e, "cudaMemset(W8A8 marks)");
+        }
     }
     if (h->kvres_ok && Lq > 0 && !per_head) {
         int least = 0, greatest = 0;
@@ -727,6 +735,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pn.x_scale = h->xscale;
     pn.w_scale = h->wscale;
     pn.nscale = h->nscale;
+    pn.w8_split = h->w8_split;
 
     ExpandParams pb{};
     pb.T = d.T;
@@ -768,6 +777,8 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pb.a_scale = h->nscale;
     pb.w_scale_q = h->wscale ? h->wscale + h->NA : nullptr;
     pb.w_scale_kv = h->wscale ? h->wscale + h->NA + (Lq > 0 ? h->NQ : 0) : nullptr;
+    pb.w8_split = h->w8_split;
+    pb.n_tiles128 = h->m_tiles;
 
     // the per-token quant kernel (the per-head quant runs in the q epilogue)
     QuantParams pq{h->qws, h->amax, Lq > 0 && !per_head ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
@@ -825,7 +836,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     }
     int ev = 1;  // next timing-hook event
     if (h->w8a8) {  // AT-05 on x: the compression's INT8 input
-        QuantXParams px{static_cast<const uint16_t*>(x), d.T, d.D, h->xq, h->xscale};
+        QuantXParams px{static_cast<const uint16_t*>(x), d.T, d.D, h->xq, h->xscale, h->w8_split, h->m_tiles};
         if ((e = launch_quant_x(px, st)) != cudaSuccess) return cuda_fail(e, "launch mla_quant_x_kernel");
         if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     }

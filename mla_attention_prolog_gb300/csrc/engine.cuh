@@ -1052,18 +1052,39 @@ __device__ __forceinline__ void w8_dequant_tile(uint32_t tb0, uint32_t tb1, bool
                                                 float a_scale, const float* w_scale, int n0, int n_end) {
     const int hw = ((width + 31) / 32) * 16;  // columns per warp of the quarter, a multiple of 16
     const int c0 = half_idx * hw, c1 = c0 + hw < width ? c0 + hw : width;
-    for (int c = c0; c < c1; c += 16) {
-        float v[16], u[16];
-        tmem_ld16(tb0 + c, v);
-        if (two) tmem_ld16(tb1 + c, u);
+    if (!two) {
+        for (int c = c0; c < c1; c += 16) {
+            float v[16];
+            tmem_ld16(tb0 + c, v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+            for (int e = 0; e < 16; ++e) {
+                const int n = n0 + c + e;
+                v[e] = w8_dequant(__float2int_rn(v[e]), a_scale, n < n_end ? w_scale[n] : 0.0f);
+            }
+            tmem_st16(tb0 + c, v);
+        }
+        return;
+    }
+    for (int c = c0; c < c1; c += 8) {  // 8 columns at a time: the epilogue's row context stays in registers
+        float v[8], u[8];
+        tmem_ld8x2(tb0 + c, two ? tb1 + c : tb0 + c, v, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
             const int y = __float2int_rn(v[e]) + (two ? __float2int_rn(u[e]) : 0);
             const int n = n0 + c + e;
             v[e] = w8_dequant(y, a_scale, n < n_end ? w_scale[n] : 0.0f);
         }
-        tmem_st16(tb0 + c, v);
+        tmem_st8(tb0 + c, v);
     }
+}
+
+// Whether the job of token tile m (CG 128-token tiles) runs its K as two
+// chains: a K longer than kW8ChainKb blocks and a tile the norm step marked.
+__device__ __forceinline__ bool w8_two_chains(const ExpandParams& p, int m, int cg, bool q) {
+    if ((q ? p.kb_q : p.kb_kv) <= kW8ChainKb) return false;
+    uint32_t bits = 0;
+    for (int i = m * cg; i < (m + 1) * cg && i < p.n_tiles128; ++i) bits |= p.w8_split[i];
+    return (bits & (q ? 1u : 2u)) != 0;
 }
 
 // ---- expansion phase: this CTA's jobs (round robin or balanced table) ----
@@ -1119,7 +1140,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 expand_job(p, jobs[i], tile, m);
                 const bool q = tile < p.nq_tiles;
                 const int nkb = q ? p.kb_q : p.kb_kv;
-                if (W8 && nkb > kW8ChainKb) {  // W8A8: two exact chains, one per accumulator buffer
+                if (W8 && w8_two_chains(p, m, CG, q)) {  // W8A8: two exact chains, one per accumulator buffer
                     ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, nkb / 2, tmem,
                                                        q ? idesc_q : idesc_kv, p.timeout_ns) &&
                          mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain + 1, nkb - nkb / 2, tmem,
@@ -1149,7 +1170,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 cur_m = m;
             }
             const bool is_q = tile < p.nq_tiles;
-            const int chains = W8 && (is_q ? p.kb_q : p.kb_kv) > kW8ChainKb ? 2 : 1;
+            const int chains = W8 && w8_two_chains(p, m, CG, is_q) ? 2 : 1;
             bool got = epi_acquire(sm, rc.chain, p.timeout_ns);
             if (chains == 2) got = got && epi_acquire(sm, rc.chain + 1, p.timeout_ns);
             const uint32_t tbase = tmem + lane_off + (rc.chain & 1) * BN_MAX;
@@ -1165,11 +1186,22 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                         w8_dequant_tile(tbase, tmem + lane_off + ((rc.chain + 1) & 1) * BN_MAX, chains == 2,
                                         p.bn_kv, half_idx, as, p.w_scale_kv, (tile - p.nq_tiles) * p.bn_kv, p.NKV);
                 }
-                // every warp's columns are converted before any warp reads the
-                // tile (the q epilogues read across the two column halves)
-                tc_fence_before();
-                got = named_bar_and(2, kEpiThreads, got);
-                tc_fence_after();
+                // Every warp's columns are converted before any warp reads
+                // them.  The store-ring epilogues (wide q tiles, kv tiles, and
+                // the per-token q tiles without the per-head norm) read only
+                // the columns this warp converted; the others read across the
+                // two column halves and meet first.
+                // (expand_q_epilogue_ts splits a head at min(Dn, (Dn + R) / 2):
+                // the pre-pass's split when Dn >= R, Dn + R a multiple of 32)
+                const bool own_cols =
+                    TS && (is_q ? (p.q_wide || (p.tma_store && !p.per_head && !p.head_norm && Dn >= R &&
+                                                (Dn + R) % 32 == 0))
+                                : p.tma_store != 0);
+                if (!own_cols) {
+                    tc_fence_before();
+                    got = named_bar_and(2, kEpiThreads, got);
+                    tc_fence_after();
+                }
             }
             if (!got) {
                 if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);

@@ -86,6 +86,7 @@ struct NormRopeParams {
     const float* x_scale;  // [T]
     const float* w_scale;  // [NA]
     float* nscale;         // [T][2]
+    uint32_t* w8_split;    // [ceil(T / 128)]: token tiles whose expansion K must split (w8_finish_token)
 };
 
 // Expansion projections.  Tiles [0, nq_tiles) are q heads (one head of
@@ -131,6 +132,11 @@ struct ExpandParams {
     const float* a_scale;     // [T][2]
     const float* w_scale_q;   // [NQ]
     const float* w_scale_kv;  // [NKV]
+    // Per 128-token tile: bit 0 / bit 1 set when the q / kv expansion of
+    // that tile runs as two exact chains (a K longer than kW8ChainKb blocks
+    // and some row's codes large enough to need it).
+    const uint32_t* w8_split;
+    int n_tiles128;
 };
 
 constexpr int kQWide = 256;
@@ -138,6 +144,10 @@ constexpr int kQWide = 256;
 // 64 k products of magnitude <= 127^2, so every partial sum is an integer
 // below 2^24 (exact in FP32) while 64 k * 127^2 < 2^24, i.e. k <= 16.
 constexpr int kW8ChainKb = 16;
+// W8A8: a token tile whose activation rows all have sum |code| <= this
+// bound needs no chain split whatever its K: every partial sum is then at
+// most 127 * 132104 = 16,777,208 < 2^24 in magnitude.
+constexpr uint32_t kW8SumLimit = 132104;
 
 // W8A8: per-token INT8 codes of a BF16 matrix (x), written as BF16 integers.
 struct QuantXParams {
@@ -145,6 +155,8 @@ struct QuantXParams {
     int rows, cols;
     uint16_t* codes;    // [rows][cols] BF16 integers in [-127, 127]
     float* scale;       // [rows]
+    uint32_t* w8_split;  // [n_split] cleared here for the norm step to mark
+    int n_split;
 };
 
 struct QuantParams {

@@ -349,6 +349,18 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
         : "memory");
 }
 
+// Stores 8 consecutive 32-bit columns of this thread's TMEM lane (shape
+// 32x32b) and waits until the stores have completed.  Whole warp.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+        : "memory");
+}
+
 // Stores 16 consecutive 32-bit columns of this thread's TMEM lane (shape
 // 32x32b: lane i of the warp writes TMEM lane base + i) and waits until the
 // stores have completed.  Whole warp.

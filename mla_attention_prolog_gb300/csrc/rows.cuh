@@ -37,6 +37,49 @@ __device__ __forceinline__ float lane_butterfly_sum(float v) {
     return v;
 }
 
+// ------------------------------------------------------------------ W8A8
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Codes of eight normed BF16 values (code_bf16x2), as BF16 integers.
+__device__ __forceinline__ uint4 codes_bf16x8(uint4 y, float inv) {
+    return make_uint4(code_bf16x2(bf16_lo(y.x), bf16_hi(y.x), inv), code_bf16x2(bf16_lo(y.y), bf16_hi(y.y), inv),
+                      code_bf16x2(bf16_lo(y.z), bf16_hi(y.z), inv), code_bf16x2(bf16_lo(y.w), bf16_hi(y.w), inv));
+}
+
+// Sum of |code| of eight codes held as BF16 integers.
+__device__ __forceinline__ uint32_t abs_sum_bf16x8(uint4 c) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t s = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        s += static_cast<uint32_t>(fabsf(bf16_lo(w[e]))) + static_cast<uint32_t>(fabsf(bf16_hi(w[e])));
+    return s;
+}
+
+// One token's normed-row scales (amax / 127, 0 for a zero row) and, where
+// a row's codes could drive an expansion's partial sums to 2^24 (sum |code|
+// * 127 >= 2^24, the largest weight code being 127), the mark that makes
+// the expansion split that token tile's K into two exact chains (bit 0: the
+// q expansion, bit 1: the kv expansion).
+__device__ __forceinline__ void w8_finish_token(const NormRopeParams& p, int t, float amax_q, float amax_kv,
+                                                uint32_t sum_q, uint32_t sum_kv) {
+    p.nscale[2 * t] = amax_q > 0.0f ? __fdiv_rn(amax_q, 127.0f) : 0.0f;
+    p.nscale[2 * t + 1] = amax_kv > 0.0f ? __fdiv_rn(amax_kv, 127.0f) : 0.0f;
+    const uint32_t bits = (sum_q > kW8SumLimit ? 1u : 0u) | (sum_kv > kW8SumLimit ? 2u : 0u);
+    if (bits) atomicOr(p.w8_split + t / kBM, bits);
+}
+
 // The latent KV-cache row of token t: null without a cache, for a negative
 // (padding) slot, and for a slot past the cache, which also sets
 // kStatusSlotRange (when `report`, i.e. from one thread of the token).
@@ -77,9 +120,9 @@ __host__ __device__ inline size_t norm_token_smem_bytes(int NA, int R, int Lq, i
 // of every chunk, BATCH loads in flight at a time, summed in split order
 // with TwoSum, rounded to BF16 into `crow`, chunk sums of x^2 / L into
 // `csum` (see chunk_ssq).
-template <int CPG, int BATCH, int NT>
+template <int CPG, int BATCH, int NT, bool W8 = false>
 __device__ __forceinline__ void norm_chunk_group(const NormRopeParams& p, const float* prow, int i0,
-                                                 uint16_t* crow, float* csum) {
+                                                 uint16_t* crow, float* csum, float sx = 0.0f) {
     constexpr int SPB = BATCH / CPG;  // splits per chunk and batch
     const size_t sstride = static_cast<size_t>(p.T) * p.NA;
     const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, splits = p.splits;
@@ -95,7 +138,16 @@ __device__ __forceinline__ void norm_chunk_group(const NormRopeParams& p, const 
         for (int u = 0; u < BATCH; ++u) {
             const int c = u / SPB, sp = s0 + u % SPB, i = i0 + c * NT * 4;
             if (sp < splits && i < NA) {
-                if (sp == 0) {
+                if constexpr (W8) {  // exact int32 partials: integer sums
+                    if (sp == 0) {
+                        acc[c] = r[u];
+                    } else {
+                        acc[c].x = __int_as_float(__float_as_int(acc[c].x) + __float_as_int(r[u].x));
+                        acc[c].y = __int_as_float(__float_as_int(acc[c].y) + __float_as_int(r[u].y));
+                        acc[c].z = __int_as_float(__float_as_int(acc[c].z) + __float_as_int(r[u].z));
+                        acc[c].w = __int_as_float(__float_as_int(acc[c].w) + __float_as_int(r[u].w));
+                    }
+                } else if (sp == 0) {
                     acc[c] = r[u];
                     cmp[c] = make_float4(0.f, 0.f, 0.f, 0.f);
                 } else {
@@ -111,8 +163,17 @@ __device__ __forceinline__ void norm_chunk_group(const NormRopeParams& p, const 
     for (int c = 0; c < CPG; ++c) {
         const int i = i0 + c * NT * 4;
         if (i < NA) {
-            const float4 a = make_float4(__fadd_rn(acc[c].x, cmp[c].x), __fadd_rn(acc[c].y, cmp[c].y),
-                                         __fadd_rn(acc[c].z, cmp[c].z), __fadd_rn(acc[c].w, cmp[c].w));
+            float4 a;
+            if constexpr (W8) {  // AT-06 on the integer sums
+                const float4 ws = *reinterpret_cast<const float4*>(p.w_scale + i);
+                a = make_float4(w8_dequant(__float_as_int(acc[c].x), sx, ws.x),
+                                w8_dequant(__float_as_int(acc[c].y), sx, ws.y),
+                                w8_dequant(__float_as_int(acc[c].z), sx, ws.z),
+                                w8_dequant(__float_as_int(acc[c].w), sx, ws.w));
+            } else {
+                a = make_float4(__fadd_rn(acc[c].x, cmp[c].x), __fadd_rn(acc[c].y, cmp[c].y),
+                                __fadd_rn(acc[c].z, cmp[c].z), __fadd_rn(acc[c].w, cmp[c].w));
+            }
             const uint32_t w0 = pack_bf16x2(a.x, a.y), w1 = pack_bf16x2(a.z, a.w);
             *reinterpret_cast<uint2*>(crow + i) = make_uint2(w0, w1);
             const float v[4] = {bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1)};
@@ -127,8 +188,10 @@ __device__ __forceinline__ void norm_chunk_group(const NormRopeParams& p, const 
 // + eps, sqrt, reciprocal, x * rstd, * gamma, BF16), rotate-half RoPE of
 // k_pe, and write the normed row, out_kpe, K's rope slice of every head and
 // (with a cache) the token's latent cache row [normed c_kv | k_pe_rot].
-// `crow` is norm_token_smem_bytes of shared memory, `red` 2 floats.
-template <int NT, int BATCH, int FIRST = 0>
+// `crow` is norm_token_smem_bytes of shared memory, `red` 2 floats (W8: 6
+// words; the integer split-K partials are summed exactly and dequantised,
+// and the normed rows leave as per-token codes, see norm_token_warp).
+template <int NT, int BATCH, int FIRST = 0, bool W8 = false>
 __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint16_t* crow, float* red) {
     constexpr int kNormThreads = NT;
     const int tid = static_cast<int>(threadIdx.x) - FIRST;
@@ -146,6 +209,7 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     const int ndst = p.H + (cache_row ? 2 : 1);  // rope-slice destinations (kpe_dst)
     if (!valid) {  // CTA-uniform
         if (tid == 0) atomicOr(p.status, kStatusPositionRange);
+        if (W8 && tid == 0) p.nscale[2 * t] = p.nscale[2 * t + 1] = 0.0f;
         const uint4 z = make_uint4(0, 0, 0, 0);
         for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) {
             *reinterpret_cast<uint4*>(nrow + i) = z;
@@ -176,12 +240,15 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     //    chunks go in groups whose loads (every split of up to two chunks,
     //    BATCH at most) are all in flight before the first sum.
     const float* prow = p.partials + static_cast<size_t>(t) * NA;
+    uint32_t* ured = reinterpret_cast<uint32_t*>(red) + 2;  // W8: max |normed| and sum |code| of c_q, c_kv
+    if (W8 && tid < 4) ured[tid] = 0u;
+    const float sx = W8 ? p.x_scale[t] : 0.0f;
     if (2 * p.splits <= BATCH) {
         for (int i0 = tid * 4; i0 < NA; i0 += 2 * kNormThreads * 4)
-            norm_chunk_group<2, BATCH, NT>(p, prow, i0, crow, csum);
+            norm_chunk_group<2, BATCH, NT, W8>(p, prow, i0, crow, csum, sx);
     } else {
         for (int i0 = tid * 4; i0 < NA; i0 += kNormThreads * 4)
-            norm_chunk_group<1, BATCH, NT>(p, prow, i0, crow, csum);
+            norm_chunk_group<1, BATCH, NT, W8>(p, prow, i0, crow, csum, sx);
     }
     group_sync<NT, FIRST>();  // also publishes crow
     if (tid < 32) {
@@ -204,6 +271,7 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
 
     // 2) y = bf16((x * rstd) * gamma) for c_q and c_kv, 8 columns per thread.
+    float amax_q = 0.0f, amax_kv = 0.0f;  // W8
     auto norm8 = [&](int i, const uint4 gv) {
         const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
         const float rstd = i < Lq ? rstd_q : rstd_kv;
@@ -217,7 +285,18 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
             o[e] = pack_bf16x2(y0, y1);
         }
         const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(nrow + i) = ov;
+        if constexpr (W8) {  // the normed values stay here until their codes are known
+            *reinterpret_cast<uint4*>(crow + i) = ov;
+            float m = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m = fmaxf(m, fmaxf(fabsf(bf16_lo(o[e])), fabsf(bf16_hi(o[e]))));
+            if (i < Lq)
+                amax_q = fmaxf(amax_q, m);
+            else
+                amax_kv = fmaxf(amax_kv, m);
+        } else {
+            *reinterpret_cast<uint4*>(nrow + i) = ov;
+        }
         if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
     };
 #pragma unroll
@@ -227,6 +306,35 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
     }
     for (int i = (tid + kGammaPre * kNormThreads) * 8; i < Lq + Lkv; i += kNormThreads * 8)
         norm8(i, *reinterpret_cast<const uint4*>(p.gamma + i));
+    if constexpr (W8) {
+        // AT-11: per-token codes of the normed c_q and c_kv rows (group-wide
+        // max |y| through shared memory: non-negative floats order as their bits)
+        amax_q = warp_max(amax_q);
+        amax_kv = warp_max(amax_kv);
+        if ((tid & 31) == 0) {
+            atomicMax(&ured[0], __float_as_uint(amax_q));
+            atomicMax(&ured[1], __float_as_uint(amax_kv));
+        }
+        group_sync<NT, FIRST>();
+        const float mq = __uint_as_float(ured[0]), mkv = __uint_as_float(ured[1]);
+        const float inv_q = mq > 0.0f ? __fdiv_rn(127.0f, mq) : 0.0f;
+        const float inv_kv = mkv > 0.0f ? __fdiv_rn(127.0f, mkv) : 0.0f;
+        uint32_t sq = 0, skv = 0;
+        for (int i = tid * 8; i < Lq + Lkv; i += kNormThreads * 8) {
+            const uint4 yv = *reinterpret_cast<const uint4*>(crow + i);
+            const uint4 cv = codes_bf16x8(yv, i < Lq ? inv_q : inv_kv);
+            *reinterpret_cast<uint4*>(nrow + i) = cv;
+            (i < Lq ? sq : skv) += abs_sum_bf16x8(cv);
+        }
+        sq = warp_sum(sq);
+        skv = warp_sum(skv);
+        if ((tid & 31) == 0) {
+            atomicAdd(&ured[2], sq);
+            atomicAdd(&ured[3], skv);
+        }
+        group_sync<NT, FIRST>();
+        if (tid == 0) w8_finish_token(p, t, mq, mkv, ured[2], ured[3]);
+    }
 
     // 3) k_pe RoPE (rotate-half) in FP32 with this token's cos/sin row; the
     //    interleaved variant pairs (2i, 2i + 1) and stores the pair at
@@ -393,17 +501,16 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
         }
         const float inv_q = amax_q > 0.0f ? __fdiv_rn(127.0f, amax_q) : 0.0f;
         const float inv_kv = amax_kv > 0.0f ? __fdiv_rn(127.0f, amax_kv) : 0.0f;
+        uint32_t sq = 0, skv = 0;
         for (int i = lane * 8; i < Lq + Lkv; i += 256) {
             const uint4 yv = *reinterpret_cast<const uint4*>(crow + i);
-            const float inv = i < Lq ? inv_q : inv_kv;
-            *reinterpret_cast<uint4*>(nrow + i) =
-                make_uint4(code_bf16x2(bf16_lo(yv.x), bf16_hi(yv.x), inv), code_bf16x2(bf16_lo(yv.y), bf16_hi(yv.y), inv),
-                           code_bf16x2(bf16_lo(yv.z), bf16_hi(yv.z), inv), code_bf16x2(bf16_lo(yv.w), bf16_hi(yv.w), inv));
+            const uint4 cv = codes_bf16x8(yv, i < Lq ? inv_q : inv_kv);
+            *reinterpret_cast<uint4*>(nrow + i) = cv;
+            (i < Lq ? sq : skv) += abs_sum_bf16x8(cv);
         }
-        if (lane == 0) {
-            p.nscale[2 * t] = amax_q > 0.0f ? __fdiv_rn(amax_q, 127.0f) : 0.0f;
-            p.nscale[2 * t + 1] = amax_kv > 0.0f ? __fdiv_rn(amax_kv, 127.0f) : 0.0f;
-        }
+        sq = warp_sum(sq);
+        skv = warp_sum(skv);
+        if (lane == 0) w8_finish_token(p, t, amax_q, amax_kv, sq, skv);
     }
     const uint16_t* kp = crow + Lq + Lkv;
     for (int i = lane; i < half; i += 32) {

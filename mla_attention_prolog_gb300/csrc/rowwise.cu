@@ -24,13 +24,13 @@ namespace mlap {
 // kernel: it waits for the partials, then lets the expansion kernel launch.
 // With split-K partials (decode) the CTA is wide and keeps every split's load
 // of its columns in flight at once: the step is latency bound.
-template <int NT, int BATCH>
+template <int NT, int BATCH, bool W8 = false>
 __global__ void __launch_bounds__(NT) mla_norm_rope_kernel(const NormRopeParams p) {
     extern __shared__ __align__(16) uint16_t crow[];  // BF16 row of C [NA], then rotated k_pe [R]
-    __shared__ float red[2];
+    __shared__ float red[6];
     pdl_wait();
     pdl_launch_dependents();
-    norm_token<NT, BATCH>(p, blockIdx.x, crow, red);
+    norm_token<NT, BATCH, 0, W8>(p, blockIdx.x, crow, red);
 }
 
 // Prefill variant (no split-K partials): one warp per token, eight tokens
@@ -108,6 +108,7 @@ constexpr int kQuantXThreads = 256;
 __global__ void __launch_bounds__(kQuantXThreads) mla_quant_x_kernel(const QuantXParams p) {
     __shared__ float red[kQuantXThreads / 32];
     const int row = blockIdx.x;
+    if (threadIdx.x == 0 && row < p.n_split) p.w8_split[row] = 0u;  // (rows >= tiles)
     const uint16_t* x = p.x + static_cast<size_t>(row) * p.cols;
     uint16_t* out = p.codes + static_cast<size_t>(row) * p.cols;
     float m = 0.0f;
@@ -169,9 +170,9 @@ cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
     if (p.T == 0) return cudaSuccess;
     // split-K partials of a decode batch: a wide CTA per token keeps every
     // split's load in flight; prefill (many tokens): one warp per token
-    if (p.splits > 1 && p.T <= 2 * kBM && !p.w8a8)
-        return launch_kernel(mla_norm_rope_kernel<512, 16>, dim3(p.T), dim3(512),
-                             norm_token_smem_bytes(p.NA, p.R, p.Lq, p.Lkv), st, true, p);
+    if (p.splits > 1 && p.T <= 2 * kBM)
+        return launch_kernel(p.w8a8 ? mla_norm_rope_kernel<512, 16, true> : mla_norm_rope_kernel<512, 16>, dim3(p.T),
+                             dim3(512), norm_token_smem_bytes(p.NA, p.R, p.Lq, p.Lkv), st, true, p);
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
     return launch_kernel(mla_norm_rope_warp_kernel, dim3((p.T + kNormWarpTokens - 1) / kNormWarpTokens),
                          dim3(32 * kNormWarpTokens), smem * kNormWarpTokens, st, true, p);

@@ -152,6 +152,17 @@ def test_w8a8_q_variants(extra):
     print(f"variant {extra}: {same.mean():.3f} of the tokens bit-exact end to end")
 
 
+@pytest.mark.parametrize("over", [dict(nope_dim=32, num_heads=8, D=1024, q_lora_rank=512, kv_lora_rank=256),
+                                  dict(nope_dim=64, rope_dim=32, v_dim=64, num_heads=16, D=2048)],
+                         ids=["dn32_r64", "dn64_r32"])
+def test_w8a8_unusual_shapes(over):
+    """Heads whose nope part is narrower than the rope slice (the q epilogue
+    then reads across the warps' column halves) and narrow heads."""
+    w, d = _w8("v3_prefill", 300, **over)
+    inp = wl.make_inputs(w, d)
+    check_w8a8(d, inp, wl.make_w8a8_weights(w, d))
+
+
 @pytest.mark.parametrize("T", [130, 300])
 def test_w8a8_largest_codes_are_exact(T):
     """Every code +-127 (x rows constant, every weight code 127, gamma 1):
