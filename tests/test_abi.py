@@ -97,8 +97,25 @@ def test_flag_bits_agree_across_header_binding_and_inputs():
     for name, py, w in (("QUANT_Q", binding.MLA_PROLOG_QUANT_Q, wl.QUANT_Q),
                         ("ROPE_INTERLEAVED", binding.MLA_PROLOG_ROPE_INTERLEAVED, wl.ROPE_INTERLEAVED),
                         ("Q_HEAD_NORM", binding.MLA_PROLOG_Q_HEAD_NORM, wl.Q_HEAD_NORM),
-                        ("QUANT_PER_HEAD", binding.MLA_PROLOG_QUANT_PER_HEAD, wl.QUANT_PER_HEAD)):
+                        ("QUANT_PER_HEAD", binding.MLA_PROLOG_QUANT_PER_HEAD, wl.QUANT_PER_HEAD),
+                        ("W8A8", binding.MLA_PROLOG_W8A8, wl.W8A8)):
         m = re.search(r"#define MLA_PROLOG_%s\s+(0x[0-9a-fA-F]+)u" % name, src)
         assert m and int(m.group(1), 16) == py == w, name
     m = re.search(r"#define MLA_STATUS_SLOT_RANGE\s+(0x[0-9a-fA-F]+)", src)
     assert m and int(m.group(1), 16) == binding.STATUS_SLOT_RANGE
+
+
+def test_oracle_flag_bits_match():
+    import oracle
+    from mla_attention_prolog_gb300 import workloads as wl
+    assert (oracle.QUANT_Q, oracle.ROPE_INTERLEAVED, oracle.Q_HEAD_NORM, oracle.QUANT_PER_HEAD, oracle.W8A8) == \
+        (wl.QUANT_Q, wl.ROPE_INTERLEAVED, wl.Q_HEAD_NORM, wl.QUANT_PER_HEAD, wl.W8A8)
+
+
+def test_w8a8_is_not_taken_by_the_noalloc_entry(L):
+    d = _dims(flags=16)
+    assert L.mla_prolog_run_noalloc(ctypes.byref(d), *([None] * 13)) == -1
+
+
+def test_w8a8_load_needs_a_handle(L):
+    assert L.mla_prolog_load_w8a8(None, None, None, None, None) == -1
