@@ -151,3 +151,23 @@ def test_plan_and_lpt_reject_bad_arguments():
     with pytest.raises(binding.MlaPrologError):
         binding.lpt([1, 2], 0)
     assert binding.lpt([], 3) == ([[], [], []], 0)
+
+
+def _constant(name):
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "mla_attention_prolog_gb300",
+                            "csrc", "prolog.cuh")).read()
+    return int(re.search(r"constexpr\s+\w+\s+%s\s*=\s*(\d+)\s*;" % name, src).group(1))
+
+
+def test_w8a8_exact_chain_bounds():
+    """The W8A8 integer products stay exact in FP32 accumulation: a chain of
+    kW8ChainKb K blocks of 64 codes sums at most 64 kW8ChainKb 127^2 < 2^24
+    in magnitude (one more block would pass it), and a row with
+    sum |code| <= kW8SumLimit keeps every partial sum below 2^24 against
+    weight codes of magnitude <= 127 (one more would not)."""
+    kb, lim, bk = _constant("kW8ChainKb"), _constant("kW8SumLimit"), _constant("kBK")
+    assert bk * kb * 127 ** 2 < 2 ** 24 <= bk * (kb + 1) * 127 ** 2
+    assert lim * 127 < 2 ** 24 <= (lim + 1) * 127
+    # a K of up to kW8ChainKb blocks never needs the mark: the largest possible sum |code| is within the limit
+    assert bk * kb * 127 <= lim
