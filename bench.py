@@ -560,12 +560,15 @@ def run_reference(args):
     import oracle
     oracle.build()
     w = wl.WORKLOADS[args.workload]
-    per_tok = wl.algorithmic_flops(w.dims) / w.dims.T
-    max_tokens = max(1, min(w.dims.T, int(1e10 / per_tok)))
-    inp, tok = oracle_sample(w, max_tokens)
+    variants = parse_variants(args.variant)  # the same config as the GPU arm's line
+    dims = w.dims if not args.tokens else w.dims.with_T(args.tokens)
+    dims = dataclasses.replace(dims, flags=dims.flags | sum(wl.VARIANTS[v] for v in variants))
+    per_tok = wl.algorithmic_flops(dims) / max(1, dims.T)
+    max_tokens = max(1, min(dims.T, int(1e10 / per_tok)))
+    inp, tok = oracle_sample(w, max_tokens, dims)
     d = inp.dims
     n = d.T if tok is None else len(tok)
-    call = lambda: oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    call = oracle_call(w, inp, tok)
     steps = args.steps or 10
     for _ in range(args.warmup):
         call()
@@ -576,8 +579,9 @@ def run_reference(args):
     v = n * steps / el
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64+f32",
-            "data": "synthetic", "config": {"workload": args.workload, "T": d.T},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int64+f32" if d.w8a8 else "f64+f32",
+            "data": "synthetic", "config": {"workload": "+".join([args.workload] + variants), "T": d.T},
             "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
                              "kind": "oracle", "sample": f"{n} of {d.T} tokens per step"},
             "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
