@@ -184,3 +184,42 @@ def test_flag_and_weights_must_agree():
     d16 = dataclasses.replace(d, flags=d.flags & ~wl.W8A8)
     with pytest.raises(ValueError):  # W8A8 entry without the flag
         oracle.mla_prolog_w8a8(d16, inp.x, inp.gamma, ww.W_a, ww.W_b, ww.w_scale, inp.positions, inp.cos_sin)
+
+
+def _f32_rn(q):
+    """The FP32 value nearest to the rational q (ties to even), by exact arithmetic."""
+    from fractions import Fraction
+    q = Fraction(q)
+    if q == 0:
+        return 0.0
+    lo = float(np.float32(float(q)))  # within one FP32 ulp of q
+    cands = sorted({lo, float(np.nextafter(np.float32(lo), np.float32(np.inf))),
+                    float(np.nextafter(np.float32(lo), np.float32(-np.inf)))})
+    best = min(cands, key=lambda c: (abs(Fraction(c) - q), int(np.array([c], np.float32).view(np.uint32)[0]) & 1))
+    return best
+
+
+def test_worked_example_by_hand():
+    """A projection worked by hand (AT-05, int32 matmul, AT-06):
+    x = (1, -0.5, 0.25, 2): amax 2, inv = 127/2 = 63.5 exactly, x * inv =
+    (63.5, -31.75, 15.875, 127) -> rint half-even (64, -32, 16, 127), scale
+    s_x = fl(2/127).  W rows (1, 2, 3, 4) and (-1, 0, 1, 0): integer sums
+    64 - 64 + 48 + 508 = 556 and -64 + 16 = -48.  Dequant with w_scale
+    (0.5, 0.25): fl(fl(556 * s_x) * 0.5), fl(fl(-48 * s_x) * 0.25)."""
+    from fractions import Fraction
+    x = np.array([1.0, -0.5, 0.25, 2.0], np.float32)
+    codes, s_x = oracle.quant_row(x)
+    assert codes.tolist() == [64, -32, 16, 127]
+    assert s_x == _f32_rn(Fraction(2, 127))
+    W = np.array([[1, 2, 3, 4], [-1, 0, 1, 0]], np.int8)
+    assert [oracle.dot_i8(codes, W[0]), oracle.dot_i8(codes, W[1])] == [556, -48]
+    y = oracle.project_w8a8(codes, W, s_x, np.array([0.5, 0.25], np.float32))
+    want = [_f32_rn(Fraction(_f32_rn(556 * Fraction(s_x))) * Fraction(1, 2)),
+            _f32_rn(Fraction(_f32_rn(-48 * Fraction(s_x))) * Fraction(1, 4))]
+    assert y.tolist() == want
+    # and it approximates the real-valued product x . W[n] * w_scale[n] within
+    # s_x / 2 * sum |W[n]| * w_scale[n] (rows 0 and 1: sum |W| = 10 and 2)
+    exact = [float(np.dot(x.astype(np.float64), W[0].astype(np.float64))) * 0.5,
+             float(np.dot(x.astype(np.float64), W[1].astype(np.float64))) * 0.25]
+    assert abs(y[0] - exact[0]) <= 0.5 * s_x * 10 * 0.5 + 1e-6
+    assert abs(y[1] - exact[1]) <= 0.5 * s_x * 2 * 0.25 + 1e-6
