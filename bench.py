@@ -5,8 +5,10 @@ One step = one pass of the whole prolog (compression projection, split,
 RMSNorm, RoPE, expansion projection, split/assemble, and the q path + INT8
 quant when the workload has one) over one batch of T tokens.
 
-Default workload: the DeepSeek-V2-Lite-shaped KV prolog decode (T=64).
-Other workloads: --workload {tiny,v2lite_decode,v2lite_prefill,v3_decode,v3_prefill}.
+Default workload: the DeepSeek-V3-shaped full prolog long prefill
+(T=16384, q path + per-token INT8 quant), the largest of the five
+configurations; the others are selected with
+--workload {tiny,v2lite_decode,v2lite_prefill,v3_decode,v3_prefill}.
 
 Timing: K steps are captured into one CUDA graph, each step on its own
 buffer set (inputs, weights and outputs), with enough sets that the sets
@@ -451,9 +453,12 @@ def run_gpu(args):
     dom_ms = per_kernel[dom]
     if w.bound == "tensor":
         ach = kf[dom] / (dom_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        # the burst peak for a kernel timed in a short loop, the sustained
+        # (power-capped) one for a kernel timed inside a seconds-long loop
+        long_loop = ms_total >= 1000.0 and "bf16_tflops_sustained" in peaks
+        peak = peaks["bf16_tflops_sustained"] if long_loop else peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": round(ach, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4)}
+                "frac": round(ach / peak, 4), "peak_kind": "sustained" if long_loop else "burst"}
     else:
         ach = kb[dom] / (dom_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -466,6 +471,13 @@ def run_gpu(args):
     whole = {"algorithmic_bytes": abytes, "algorithmic_flops": wl.algorithmic_flops(d),
              "hbm_frac": round(abytes / (ms_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
              "tc_frac": round(wl.algorithmic_flops(d) / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops"], 4)}
+    if "bf16_tflops_sustained" in peaks:
+        whole["tc_frac_of_sustained"] = round(
+            wl.algorithmic_flops(d) / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
+    if clocks.get("sm_mhz"):
+        # step time x median SM clock: compares runs taken at different
+        # (power-capped) clocks
+        whole["ms_x_sm_mhz"] = round(ms_step * clocks["sm_mhz"], 2)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -594,7 +606,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=0,
                     help="timed steps (default: about one second of steps)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="v2lite_decode", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default="v3_prefill", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T of the workload (small profiling cases; not a bench line)")

@@ -435,8 +435,14 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
  * in directly.  The scratch that a handle keeps in its workspace is instead a
  * static 32 MiB device array inside the library (each GPU that loads the
  * library holds it until the process exits); dims whose workspace would not
- * fit (split-K partials + normed rows + FP32 q rows + amax, i.e. decode-sized
- * batches) are rejected with MLA_ERR_UNSUPPORTED_DIMS before anything runs.
+ * fit (split-K partials + normed rows + FP32 q rows + amax) are rejected with
+ * MLA_ERR_UNSUPPORTED_DIMS before anything runs.  On a 152-SM GB300 that
+ * admits the V2-Lite KV shape up to about 10 000 tokens (decode and prefill
+ * schedules) and the V3 shape with its q path up to about 246 tokens; the
+ * exact limit follows from the schedule mla_prolog_plan() reports.  The
+ * kernels are a subset of mla_prolog_run()'s (no cluster, cooperative or
+ * CTA-pair kernels), so results agree with it within the parity tolerances,
+ * and bit for bit where both launch the same kernels.
  * `status` (device int32, may be NULL) receives the run's device status word
  * (MLA_STATUS_* bits).  Of the dims flags only MLA_PROLOG_QUANT_Q is taken
  * (the variant flags give MLA_ERR_INVALID_ARG).

@@ -11,8 +11,16 @@
 // loads the library holds its own copy of that array until the process
 // exits.  All calls on one device share it and it keeps the last call's
 // contents, so two calls whose kernels overlap on the same GPU (for example
-// on two streams) race on it.  The kernels are the ones mla_prolog_run()
-// launches, with the same schedule, so the outputs are the same.
+// on two streams) race on it.
+//
+// The math and the schedule rules are those of mla_prolog_run(), but this
+// entry launches only a subset of its kernels: the one-CTA split-K or wide
+// compression, the norm kernel, the one-CTA expansion and the quant kernel.
+// A handle may pick other kernels for the same dims (the cluster compression
+// + norm for tiny batches, CTA pairs for prefills with a q path), so results
+// agree with mla_prolog_run() within the parity tolerances; where both paths
+// launch the same kernels (the V2-Lite and V3 decode shapes, the V2-Lite
+// prefill shape) they agree bit for bit.
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -191,6 +199,13 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pa.n_gamma = Lq + Lkv;
     pa.status = dstatus;
     pa.timeout_ns = timeout_ns;
+    // As a handle does: a decode batch with large expansion weights asks L2
+    // to fetch W_b behind the compression's last operand loads.
+    const uint64_t wb_bytes = (static_cast<uint64_t>(NQ) * Lq + static_cast<uint64_t>(NKV) * Lkv) * 2;
+    if (decode && wb_bytes >= (64ull << 20)) {
+        pa.l2_fetch = static_cast<const uint8_t*>(W_b);
+        pa.l2_fetch_bytes = wb_bytes;
+    }
     const int jobs_a = pa.n_tiles * m_tiles * splits_a;
     if (launch_compress(shape_a, jobs_a < sms ? jobs_a : sms, tm_x, tm_wa, pa, st) != cudaSuccess)
         return set_error("launch mla_compress_kernel");

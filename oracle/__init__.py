@@ -68,7 +68,7 @@ def lib():
         L.oracle_quant_row.argtypes = [P, ctypes.c_int, P, P]
         L.oracle_deinterleave.argtypes = [P, ctypes.c_int, P]
         L.oracle_rmsnorm_f32_row.argtypes = [P, ctypes.c_int, ctypes.c_float, P]
-        L.oracle_mla_prolog_w8a8.argtypes = [ctypes.POINTER(OracleDims)] + [P] * 7 + [P, ctypes.c_int32] + [P] * 12
+        L.oracle_mla_prolog_w8a8.argtypes = [ctypes.POINTER(OracleDims)] + [P] * 7 + [P, ctypes.c_int32] + [P] * 14
         L.oracle_mla_prolog_w8a8.restype = ctypes.c_int
         L.oracle_dot_i8.argtypes = [P, P, ctypes.c_int]
         L.oracle_dot_i8.restype = ctypes.c_int64
@@ -140,7 +140,9 @@ def mla_prolog(d, x, gamma, W_a, W_b, positions, cos_sin,
 
 
 def mla_prolog_w8a8(d, x, gamma, W_a, W_b, w_scale, positions, cos_sin,
-                    tokens: Optional[Sequence[int]] = None, taps: bool = False) -> Dict[str, np.ndarray]:
+                    tokens: Optional[Sequence[int]] = None, taps: bool = False,
+                    given_codes: Optional[np.ndarray] = None,
+                    given_scale: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
     """The prolog with W8A8 projections (``d.flags`` has ``W8A8``).
 
     ``W_a`` and ``W_b`` are INT8 codes in the layouts of the BF16 weights,
@@ -149,6 +151,13 @@ def mla_prolog_w8a8(d, x, gamma, W_a, W_b, w_scale, positions, cos_sin,
     :func:`mla_prolog`; ``taps`` adds the x codes (``x_codes``, ``x_scale``)
     and the normed rows' codes (``n_codes``, ``n_scale`` [n, 2] = c_q, c_kv)
     to ``c``, ``normed`` (values before their quantisation) and ``q``.
+
+    ``given_codes`` [n, Lq + Lkv] int8 and ``given_scale`` [n, 2] float32
+    (rows compact like the outputs) replace the normed rows' codes and scales
+    that the expansion projections take: every later step then runs on them.
+    This checks a candidate whose normed codes legitimately differ from the
+    oracle's own (their RMSNorm sums in another order) step for step from
+    there on; the ``n_codes`` / ``n_scale`` taps still hold the oracle's own.
     """
     L = lib()
     tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
@@ -178,10 +187,18 @@ def mla_prolog_w8a8(d, x, gamma, W_a, W_b, w_scale, positions, cos_sin,
             np.ascontiguousarray(W_a, np.int8), np.ascontiguousarray(W_b, np.int8),
             np.ascontiguousarray(w_scale, np.float32), np.ascontiguousarray(positions, np.int32),
             np.ascontiguousarray(cos_sin, np.float32)]
+    gc = gs = None
+    if (given_codes is None) != (given_scale is None):
+        raise ValueError("given_codes and given_scale go together")
+    if given_codes is not None:
+        gc = np.ascontiguousarray(given_codes, np.int8)
+        gs = np.ascontiguousarray(given_scale, np.float32)
+        if gc.shape != (n, Lq + Lkv) or gs.shape != (n, 2):
+            raise ValueError(f"given codes {gc.shape} / scales {gs.shape} for {n} rows")
     dims = _dims(d)
     rc = L.oracle_mla_prolog_w8a8(ctypes.byref(dims), *[_p(a) for a in arrs], _p(tok), ctypes.c_int32(n),
                                   _p(out["out_k"]), _p(out["out_v"]), _p(out["out_kpe"]), _p(q8), _p(sc),
-                                  _p(c), _p(nrm), _p(q), _p(xc), _p(xs), _p(nc), _p(ns))
+                                  _p(c), _p(nrm), _p(q), _p(xc), _p(xs), _p(nc), _p(ns), _p(gc), _p(gs))
     if rc < 0:
         raise ValueError("oracle rejected its arguments")
     out["bad_positions"] = rc

@@ -47,7 +47,8 @@
  *     q and KV expansion; with a quantised Linear the norm block becomes
  *     RMSNorm + Linear + Quant (AT-11, V -> C -> V).
  *
- * Readings where the pages are silent (also listed in the design notes):
+ * Readings where the pages are silent (the pages fix none of these; each is
+ * the plainest reading that the passages cited above support):
  *   - W8A8: one FP32 weight scale per output row of each weight matrix; the
  *     quantised matmul input is the tensor the BF16 mode feeds to the
  *     matmul (x; the normed rows after their BF16 cast); AT-06 multiplies
@@ -272,6 +273,8 @@ typedef struct {
     float* x_scale;        /*   x scales [n]                                    */
     int8_t* n_codes;       /*   normed c_q | c_kv codes [n, Lq + Lkv]           */
     float* n_scale;        /*   their scales [n, 2] = (c_q, c_kv)               */
+    const int8_t* given_codes; /* optional [n, Lq + Lkv]: the expansions take   */
+    const float* given_scale;  /*   these codes and [n, 2] scales instead       */
 } oracle_w8a8;
 
 /* ------------------------------------------------------------ whole op -- */
@@ -392,6 +395,13 @@ static int prolog(const oracle_dims* d,
             oracle_quant_row(nf + Lq, Lkv, nq + Lq, &skv);
             if (w8->n_codes) memcpy(w8->n_codes + (size_t)j * (Lq + Lkv), nq, (size_t)(Lq + Lkv));
             if (w8->n_scale) w8->n_scale[2 * j] = sq, w8->n_scale[2 * j + 1] = skv;
+            /* Given codes (a candidate's own normed-row codes and scales):
+             * every step after the quantisation runs on them instead. */
+            if (w8->given_codes) {
+                memcpy(nq, w8->given_codes + (size_t)j * (Lq + Lkv), (size_t)(Lq + Lkv));
+                sq = w8->given_scale[2 * j];
+                skv = w8->given_scale[2 * j + 1];
+            }
             free(nf);
         }
         /* Step 4 (k_pe RoPE): rotate-half in FP32 with this token's table row
@@ -481,6 +491,14 @@ int oracle_mla_prolog(const oracle_dims* d,
  * the BF16 weights, and four more optional taps (x codes and scales, the
  * normed rows' codes and scales; see oracle_w8a8).  normed_out still
  * receives the normed BF16 values, before their quantisation.
+ *
+ * given_codes / given_scale (optional, compact by selected token like the
+ * outputs): normed-row codes [n, Lq + Lkv] and scales [n, 2] that the two
+ * expansion projections take in place of the oracle's own.  A candidate whose
+ * normed rows legitimately differ (the RMSNorm's FP32 sum of squares may run
+ * in another order) is then checked step for step after that point: the
+ * integer products, AT-06, RoPE, the split / assemble and the q quant.  The
+ * n_codes / n_scale taps still report the oracle's own codes.
  */
 int oracle_mla_prolog_w8a8(const oracle_dims* d,
                            const uint16_t* x, const uint16_t* gamma,
@@ -490,8 +508,10 @@ int oracle_mla_prolog_w8a8(const oracle_dims* d,
                            uint16_t* out_k, uint16_t* out_v, uint16_t* out_kpe,
                            int8_t* out_q_int8, float* out_scale,
                            uint16_t* c_out, uint16_t* normed_out, float* q_out,
-                           int8_t* x_codes, float* x_scale, int8_t* n_codes, float* n_scale) {
-    const oracle_w8a8 w8 = {W_a, W_b, w_scale, x_codes, x_scale, n_codes, n_scale};
+                           int8_t* x_codes, float* x_scale, int8_t* n_codes, float* n_scale,
+                           const int8_t* given_codes, const float* given_scale) {
+    if ((given_codes == NULL) != (given_scale == NULL)) return -1;
+    const oracle_w8a8 w8 = {W_a, W_b, w_scale, x_codes, x_scale, n_codes, n_scale, given_codes, given_scale};
     return prolog(d, x, gamma, NULL, NULL, &w8, positions, cos_sin, tokens, n_tokens, out_k, out_v, out_kpe,
                   out_q_int8, out_scale, c_out, normed_out, q_out);
 }

@@ -166,3 +166,25 @@ def test_scatter_kv_cache_rows_and_skips(oracle_lib):
             assert np.array_equal(cache[s, d.kv_lora_rank:], o["out_kpe"][j])
         else:
             assert np.all(cache[s] == 0xBEEF)
+
+
+def test_scatter_kv_cache_against_torch_index_copy(oracle_lib):
+    """An independent route to the same cache: torch's index_copy_ of the rows
+    [normed c_kv | k_pe_rot] at the valid slots (those in [0, num_slots));
+    padding (-1) and out-of-range slots are left out of the index list."""
+    d = _dims(T=40)
+    inp = wl.make_inputs(wl.Workload("v", d, positions="uniform"))
+    o = _run(oracle_lib, d, inp, taps=True)
+    num_slots, W = 64, d.kv_lora_rank + d.rope_dim
+    rng = np.random.default_rng(5)
+    slots = rng.permutation(num_slots + 8)[:d.T].astype(np.int32)  # distinct, some >= num_slots
+    slots[rng.choice(d.T, 6, replace=False)] = -1
+    cache = np.full((num_slots, W), 0xBEEF, np.uint16)
+    bad = oracle_lib.scatter_kv_cache(cache, slots, o["normed"], o["out_kpe"], d.q_lora_rank)
+    keep = (slots >= 0) & (slots < num_slots)
+    assert bad == int((slots >= num_slots).sum())
+    rows = torch.from_numpy(np.concatenate([o["normed"][:, d.q_lora_rank:], o["out_kpe"]], axis=1)
+                            .astype(np.int32))
+    want = torch.full((num_slots, W), 0xBEEF, dtype=torch.int32)
+    want.index_copy_(0, torch.from_numpy(slots[keep].astype(np.int64)), rows[torch.from_numpy(keep)])
+    assert np.array_equal(cache.astype(np.int32), want.numpy())

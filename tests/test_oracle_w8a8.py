@@ -223,3 +223,38 @@ def test_worked_example_by_hand():
              float(np.dot(x.astype(np.float64), W[1].astype(np.float64))) * 0.25]
     assert abs(y[0] - exact[0]) <= 0.5 * s_x * 10 * 0.5 + 1e-6
     assert abs(y[1] - exact[1]) <= 0.5 * s_x * 2 * 0.25 + 1e-6
+
+
+def test_given_codes_feed_the_expansions():
+    """The given-codes input (used to check a candidate's steps after its own
+    normed-row codes): the oracle's own codes give its own outputs bit for
+    bit; a code moved by one changes only that token's outputs, and its
+    k_nope and value are the AT-06 product of the moved codes, formed here
+    with numpy's integer dot, FP32 multiplies and torch's BF16 conversion."""
+    d, inp, ww = _case("tiny_q", T=6, max_pos=8)
+    own = _run(d, inp, ww)
+    again = _run(d, inp, ww, given_codes=own["n_codes"], given_scale=own["n_scale"])
+    for k in ("out_k", "out_v", "out_kpe", "out_q_int8", "out_scale"):
+        assert np.array_equal(again[k], own[k]), k
+    Lq, Lkv, H, Dn, Dv, R = d.q_lora_rank, d.kv_lora_rank, d.num_heads, d.nope_dim, d.v_dim, d.rope_dim
+    codes = own["n_codes"].copy()
+    j, k = 2, Lq + 5
+    codes[j, k] += 1 if codes[j, k] < 127 else -1
+    moved = _run(d, inp, ww, given_codes=codes, given_scale=own["n_scale"])
+    for t in range(d.T):
+        if t == j:
+            continue
+        for name in ("out_k", "out_v", "out_q_int8", "out_scale"):
+            assert np.array_equal(moved[name][t], own[name][t]), (name, t)
+    NQ = H * (Dn + R)
+    W_kv = ww.W_b[NQ * Lq:].reshape(H * (Dn + Dv), Lkv).astype(np.int64)
+    s_kv = ww.w_scale[d.n_a + NQ:]
+    acc = (W_kv @ codes[j, Lq:].astype(np.int64)).astype(np.float32)
+    kv = (acc * np.float32(own["n_scale"][j, 1])) * s_kv
+    kv = bf16_bits(kv).reshape(H, Dn + Dv)
+    assert np.array_equal(moved["out_k"][j][:, :Dn], kv[:, :Dn])
+    assert np.array_equal(moved["out_v"][j], kv[:, Dn:])
+    assert not np.array_equal(moved["out_v"][j], own["out_v"][j])
+    assert np.array_equal(moved["out_kpe"][j], own["out_kpe"][j])  # k_pe does not pass through the codes
+    with pytest.raises(ValueError):
+        _run(d, inp, ww, given_codes=codes)

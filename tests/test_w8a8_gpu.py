@@ -1,16 +1,17 @@
 """GPU parity of the W8A8 prolog (MLA_PROLOG_W8A8) against the oracle.
 
 What is integer work, or FP32 work on exact integers in the same order on
-both sides, is compared bit for bit: x's per-token codes and scales, the
-rotated k_pe (from the exactly dequantised compression), and -- for every
-token whose normed-row codes and scales agree with the oracle's -- every
-output.  The normed rows themselves come out of an FP32 sum of squares whose
-order differs between the two sides (the BF16 mode's RMSNorm), so their
-codes may differ by one on a few elements; those tokens are held to the
-BF16 mode's bar for K and V and, for q, to their dequantised values (codes
-times scale) within 1e-2 of the row's largest magnitude.  A deterministic
-case with every code at +-127 checks the integer products at their largest
-magnitudes (past 2^24 in one chain).
+both sides, is compared bit for bit: x's per-token codes and scales and the
+rotated k_pe (from the exactly dequantised compression).  The normed rows
+come out of an FP32 sum of squares whose order differs between the two
+sides (the BF16 mode's RMSNorm), so their codes may differ by one: they are
+held to the INT8 bar (<= 1 on <= 0.1 %), and at least 95 % of the tokens must
+carry exactly the oracle's codes.  From there on every token is checked step
+for step: the oracle, fed the kernel's own normed codes and scales, must give
+K, V, the q codes and the q scales bit for bit.  The outputs are also held to
+the parity bar against the oracle's own results (BF16 outputs, INT8 codes
+and scales).  A deterministic case with every code at +-127 checks the
+integer products at their largest magnitudes (past 2^24 in one chain).
 """
 import dataclasses
 
@@ -19,7 +20,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import alloc_outputs, bf16_within, device_inputs
+from helpers import alloc_outputs, bf16_within, device_inputs, quant_within
 from mla_attention_prolog_gb300 import binding, workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -84,7 +85,7 @@ def _bits(t):
         t.cpu().numpy()
 
 
-def check_w8a8(d, inp, ww, sample=384, n_code_frac=2e-3):
+def check_w8a8(d, inp, ww, sample=384):
     status, outs, taps, names = _run_gpu(d, inp, ww)
     assert names[0] == "mla_quant_x_kernel"
     tok = _sample(d.T, sample)
@@ -97,37 +98,34 @@ def check_w8a8(d, inp, ww, sample=384, n_code_frac=2e-3):
     assert np.array_equal(taps["x_scale"][rows], ref["x_scale"])
     # rotated k_pe: from the exact compression, same FP32 RoPE -> bit-exact
     assert np.array_equal(_bits(outs["out_kpe"].t[sel]), ref["out_kpe"])
-    # normed-row codes: the RMSNorm's sum order may move a code by one
+    # normed-row codes against the oracle's own: the RMSNorm's FP32 sum of
+    # squares runs in another order, which may move a BF16 normed value by an
+    # ulp and its code by one -- held to the INT8 bar (<= 1 on <= 0.1 %), the
+    # scale to one BF16 ulp of the row's largest magnitude
     nc, nref = taps["n_codes"][rows], ref["n_codes"].astype(np.float32)
     dq = np.abs(nc - nref)
-    assert dq.max() <= 1 and dq.mean() <= n_code_frac, (dq.max(), dq.mean())
+    assert dq.max() <= 1 and (dq > 0).mean() <= 1e-3, (dq.max(), (dq > 0).mean())
     ns = taps["n_scale"][rows]
     rel = np.abs(ns - ref["n_scale"]) / np.maximum(ref["n_scale"], 1e-30)
     assert np.all(rel <= 2.0 ** -7), rel.max()
     same = np.all(nc == nref, axis=1) & np.all(ns == ref["n_scale"], axis=1)
-    assert same.mean() >= 0.5, f"only {same.mean():.2f} of the tokens have the oracle's normed codes"
+    assert same.mean() >= 0.95, f"only {same.mean():.3f} of the tokens have the oracle's normed codes"
+    # every token, step for step from the kernel's own normed codes: the
+    # integer products, AT-06, RoPE, split / assemble and the q quant are
+    # then the same FP32 work in the same order on both sides -> bit-exact
+    given = oracle.mla_prolog_w8a8(d, inp.x, inp.gamma, ww.W_a, ww.W_b, ww.w_scale, inp.positions, inp.cos_sin,
+                                   tokens=tok, given_codes=nc.astype(np.int8), given_scale=ns)
     ok_k, ok_v = _bits(outs["out_k"].t[sel]), _bits(outs["out_v"].t[sel])
-    assert np.array_equal(ok_k[same], ref["out_k"][same])
-    assert np.array_equal(ok_v[same], ref["out_v"][same])
+    assert np.array_equal(ok_k, given["out_k"])
+    assert np.array_equal(ok_v, given["out_v"])
+    # and against the oracle's own results, within the parity bar
     bf16_within(outs["out_k"].t[sel], ref["out_k"], "out_k")
     bf16_within(outs["out_v"].t[sel], ref["out_v"], "out_v")
     if d.q_lora_rank:
-        qc, qs = outs["out_q_int8"].t[sel].cpu().numpy(), outs["out_scale"].t[sel].cpu().numpy()
-        assert np.array_equal(qc[same], ref["out_q_int8"][same])
-        assert np.array_equal(qs[same], ref["out_scale"][same])
-        # a normed code one off moves every q of the token a little, and with it
-        # the q scale and many codes: those tokens are held to the dequantised
-        # values, within 1e-2 of their row's largest magnitude
-        if (~same).any():
-            rq = ref["out_q_int8"][~same].astype(np.float64)
-            rs, gs = ref["out_scale"][~same].astype(np.float64), qs[~same].astype(np.float64)
-            if d.quant_per_head:
-                rs, gs = rs[..., None], gs[..., None]
-            else:
-                rs, gs = rs[:, None, None], gs[:, None, None]
-            want, got = rq * rs, qc[~same].astype(np.float64) * gs
-            assert np.all(np.abs(gs - rs) <= 1e-2 * rs)
-            assert np.all(np.abs(got - want) <= 1e-2 * 127 * rs)
+        qc, qs = outs["out_q_int8"].t[sel], outs["out_scale"].t[sel]
+        assert np.array_equal(qc.cpu().numpy(), given["out_q_int8"])
+        assert np.array_equal(qs.cpu().numpy(), given["out_scale"])
+        quant_within(qc, qs, ref["out_q_int8"], ref["out_scale"])
     return status, outs, ref, same
 
 
