@@ -13,9 +13,12 @@
 // contents, so two calls whose kernels overlap on the same GPU (for example
 // on two streams) race on it.
 //
-// The math and the schedule rules are those of mla_prolog_run(), but this
-// entry launches only a subset of its kernels: the one-CTA split-K or wide
-// compression, the norm kernel, the one-CTA expansion and the quant kernel.
+// The math and the schedule rules are those of mla_prolog_run() (the same
+// tile widths and split-K factors; jobs in round-robin order instead of the
+// handle's balanced job tables, which does not change any job's result),
+// but this entry launches only a subset of its kernels: the one-CTA split-K
+// or wide compression, the norm kernel, the one-CTA expansion and the quant
+// kernel.
 // A handle may pick other kernels for the same dims (the cluster compression
 // + norm for tiny batches, CTA pairs for prefills with a q path), so results
 // agree with mla_prolog_run() within the parity tolerances; where both paths
@@ -119,9 +122,18 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     if (rc != MLA_OK) return rc;
     const Schedule sc = plan_schedule(d.T, d.D, Lq, Lkv, R, H, d.nope_dim, d.v_dim, sms);
     const bool decode = sc.decode;
-    const GemmShape shape_a = sc.shape_a, shape_b = sc.shape_b;
-    const int bn_a = sc.bn_a, splits_a = sc.splits_a, bn_kv = sc.bn_kv, group_a = sc.group_a;
+    const GemmShape shape_b = sc.shape_b;
+    GemmShape shape_a = sc.shape_a;
+    int bn_a = sc.bn_a, splits_a = sc.splits_a;
+    const int bn_kv = sc.bn_kv, group_a = sc.group_a;
     const int kb_a = cdiv(d.D, kBK);
+    if (!decode) {  // the prefill compression tile a handle selects (jobs in round-robin order here)
+        CompressTilePlan plans[3];
+        bn_a = plan_compress_tiles(d.T, NA, kb_a, sms, plans);
+        for (const auto& ct : plans)
+            if (ct.bn == bn_a) splits_a = ct.splits;
+        shape_a = bn_a == 128 ? GemmShape::Wide : bn_a == 192 ? GemmShape::Wide192 : GemmShape::Wide256;
+    }
 
     // Scratch layout (same order as the handle's workspace) and its limit.
     const size_t T = static_cast<size_t>(d.T);

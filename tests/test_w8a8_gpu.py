@@ -9,8 +9,9 @@ held to the INT8 bar (<= 1 on <= 0.1 %), and at least 95 % of the tokens must
 carry exactly the oracle's codes.  From there on every token is checked step
 for step: the oracle, fed the kernel's own normed codes and scales, must give
 K, V, the q codes and the q scales bit for bit.  The outputs are also held to
-the parity bar against the oracle's own results (BF16 outputs, INT8 codes
-and scales).  A deterministic case with every code at +-127 checks the
+the parity bar against the oracle's own results (K and V for every token;
+the INT8 codes and scales for the tokens that carry the oracle's normed
+codes).  A deterministic case with every code at +-127 checks the
 integer products at their largest magnitudes (past 2^24 in one chain).
 """
 import dataclasses
@@ -118,14 +119,20 @@ def check_w8a8(d, inp, ww, sample=384):
     ok_k, ok_v = _bits(outs["out_k"].t[sel]), _bits(outs["out_v"].t[sel])
     assert np.array_equal(ok_k, given["out_k"])
     assert np.array_equal(ok_v, given["out_v"])
-    # and against the oracle's own results, within the parity bar
+    # and against the oracle's own results: K and V within the BF16 bar for
+    # every token; q within the INT8 bar for the tokens that carry the
+    # oracle's own normed codes (a token with a legitimately different normed
+    # row has another, equally valid q row -- one normed code moves a head's
+    # largest |q|, and so a per-head scale, by up to ~1e-3 -- and is held to
+    # the step-for-step check above instead)
     bf16_within(outs["out_k"].t[sel], ref["out_k"], "out_k")
     bf16_within(outs["out_v"].t[sel], ref["out_v"], "out_v")
     if d.q_lora_rank:
         qc, qs = outs["out_q_int8"].t[sel], outs["out_scale"].t[sel]
         assert np.array_equal(qc.cpu().numpy(), given["out_q_int8"])
         assert np.array_equal(qs.cpu().numpy(), given["out_scale"])
-        quant_within(qc, qs, ref["out_q_int8"], ref["out_scale"])
+        keep = torch.from_numpy(same).to(DEV)
+        quant_within(qc[keep], qs[keep], ref["out_q_int8"][same], ref["out_scale"][same])
     return status, outs, ref, same
 
 

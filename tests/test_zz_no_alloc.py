@@ -82,7 +82,7 @@ def _case(name, T=None, **over):
 # (workload, T, extra dims, bit-exact against mla_prolog_run)
 CASES = [
     ("tiny_q", None, {}, False),              # the handle runs the cluster compression here
-    ("tiny", 512, {"max_pos": 512}, False),   # prefill schedule, split-K compression
+    ("tiny", 512, {"max_pos": 512}, True),    # prefill schedule on a tiny shape
     ("v2lite_decode", None, {}, True),
     ("v2lite_prefill", 300, {}, True),         # prefill schedule with split-K
     ("v2lite_prefill", None, {}, True),        # the full V2-Lite prefill, T = 4096
