@@ -422,6 +422,16 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            the operand bytes of the busiest CTA pair).
  *                            INVALID_ARG when that kernel is not available. */
 #define MLA_TUNE_KV_GROUP 14
+/*   MLA_TUNE_L2_POLICY       L2 eviction priorities of the projections' bulk
+ *                            copies, an OR of: 1 the weight tiles load with
+ *                            the evict-last priority, 2 the activation tiles
+ *                            load with the evict-last priority, 4 the output
+ *                            tensor stores of the expansions write with the
+ *                            evict-first priority; 0 (the default): no
+ *                            priority hint on any copy.  Values are
+ *                            unchanged; only which lines L2 keeps.
+ *                            INVALID_ARG outside 0..7. */
+#define MLA_TUNE_L2_POLICY 15
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 
 /*

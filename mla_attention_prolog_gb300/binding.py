@@ -51,6 +51,7 @@ TUNE_Q_WIDE = 11
 TUNE_KV_RESIDENT = 12
 TUNE_QUANT_OVERLAP = 13
 TUNE_KV_GROUP = 14
+TUNE_L2_POLICY = 15
 
 
 class MlaPrologDims(ctypes.Structure):

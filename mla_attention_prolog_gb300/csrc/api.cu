@@ -142,6 +142,7 @@ struct mla_prolog {
     bool kvres_ok = false;   // pairs: kv tiles with the activations resident possible
     bool kvres = false;      // in use (tunable)
     int kvres_group = 8;     // kv tiles per super-job (tunable)
+    int l2_policy = 0;       // MLA_TUNE_L2_POLICY bits (kL2WeightsLast, kL2ActsLast, kL2StoresFirst)
     int kvres_grid = 0;      // CTA pairs of that kernel
     // the expansion epilogue's bulk tensor stores (kernels with a staging area)
     bool l2_fetch = false;  // decode: the compression kernel fetches W_b into L2 (tunable)
@@ -700,6 +701,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pa.w8a8 = h->w8a8 ? 1 : 0;
     pa.x_scale = h->xscale;
     pa.w_scale = h->wscale;
+    pa.l2_policy = h->l2_policy;
     if (h->decode && h->l2_fetch) {
         pa.l2_fetch = static_cast<const uint8_t*>(W_b);
         pa.l2_fetch_bytes = (static_cast<uint64_t>(h->NQ) * Lq + static_cast<uint64_t>(h->NKV) * Lkv) * 2;
@@ -779,6 +781,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
     pb.w_scale_kv = h->wscale ? h->wscale + h->NA + (Lq > 0 ? h->NQ : 0) : nullptr;
     pb.w8_split = h->w8_split;
     pb.n_tiles128 = h->m_tiles;
+    pb.l2_policy = h->l2_policy;
 
     // the per-token quant kernel (the per-head quant runs in the q epilogue)
     QuantParams pq{h->qws, h->amax, Lq > 0 && !per_head ? d.T : 0, h->NQ, h->NQ, out_q_int8, out_scale};
@@ -1159,6 +1162,10 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             if (value == 1 && !h->ts_ok) return MLA_ERR_INVALID_ARG;
             h->tma_store = value == 1;
             h->n_events = 0;  // the kernel count may change: re-arm the timing hook
+            return MLA_OK;
+        case MLA_TUNE_L2_POLICY:
+            if (value < 0 || value > 7) return MLA_ERR_INVALID_ARG;
+            h->l2_policy = value;
             return MLA_OK;
         case MLA_TUNE_CLUSTER_NORM:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;

@@ -147,7 +147,8 @@ __device__ __forceinline__ void raise_abort(const Smem& sm, int* status) {
 template <int BN_MAX, int STAGES, int CG = 1, class Dep>
 __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, const CUtensorMap* tmA,
                                             const CUtensorMap* tmB, int a_row, int b_row, int kb0, int nkb,
-                                            int bn, bool weights_first, uint64_t timeout_ns, Dep&& dep) {
+                                            int bn, bool weights_first, uint64_t timeout_ns, Dep&& dep,
+                                            uint64_t pol_a, uint64_t pol_b) {
     using L = Layout<BN_MAX, STAGES, CG>;
     const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
     const bool leader = rank == 0;
@@ -159,11 +160,11 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
         if constexpr (CG == 2) return map_shared_rank(sm.full0 + 8 * s, 0);
         return sm.full0 + 8 * s;
     };
-    auto load = [&](uint32_t dst, const CUtensorMap* map, int s, int c0, int c1) {
+    auto load = [&](uint32_t dst, const CUtensorMap* map, int s, int c0, int c1, uint64_t pol) {
         if constexpr (CG == 2)
-            tma_load_2d_pair(dst, map, full_bar(s), c0, c1);
+            tma_load_2d_pair_hint(dst, map, full_bar(s), c0, c1, pol);
         else
-            tma_load_2d(dst, map, full_bar(s), c0, c1);
+            tma_load_2d_hint(dst, map, full_bar(s), c0, c1, pol);
     };
     int i = 0;
     if (weights_first) {
@@ -173,14 +174,14 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
             const int s = l % STAGES;
             if (!mbar_wait(sm.empty0 + 8 * s, ((l / STAGES) & 1) ^ 1, timeout_ns, sm.abort_flag)) return false;
             if (leader) mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
-            load(sm.base + s * L::STAGE + L::A_BYTES, tmB, s, (kb0 + k) * kBK, b_row);
+            load(sm.base + s * L::STAGE + L::A_BYTES, tmB, s, (kb0 + k) * kBK, b_row, pol_b);
         }
         // The weight tiles above are in flight: their slots must still be
         // completed (the activation tiles) even when the wait gives up.
         const bool dep_ok = dep();
         for (int k = 0; k < pre; ++k) {
             const int s = (loads + k) % STAGES;
-            load(sm.base + s * L::STAGE, tmA, s, (kb0 + k) * kBK, a_row);
+            load(sm.base + s * L::STAGE, tmA, s, (kb0 + k) * kBK, a_row, pol_a);
         }
         i = pre;
         loads += pre;
@@ -192,8 +193,8 @@ __device__ __forceinline__ bool produce_job(const Smem& sm, uint32_t& loads, con
         if (!mbar_wait(sm.empty0 + 8 * s, ph ^ 1, timeout_ns, sm.abort_flag)) return false;
         const uint32_t sa = sm.base + s * L::STAGE;
         if (leader) mbar_arrive_expect_tx(sm.full0 + 8 * s, tx);
-        load(sa, tmA, s, (kb0 + i) * kBK, a_row);
-        load(sa + L::A_BYTES, tmB, s, (kb0 + i) * kBK, b_row);
+        load(sa, tmA, s, (kb0 + i) * kBK, a_row, pol_a);
+        load(sa + L::A_BYTES, tmB, s, (kb0 + i) * kBK, b_row, pol_b);
     }
     return true;
 }
@@ -340,7 +341,8 @@ struct OutMaps {
 };
 
 struct StoreRing {
-    uint32_t slots;  // this warp's two slots
+    uint32_t slots;   // this warp's two slots
+    uint64_t policy;  // L2 priority of the stored lines (0: none)
 };
 
 // This lane's 16 words of one box row into slot `slot`.
@@ -368,8 +370,8 @@ __device__ __forceinline__ void store_boxes(const StoreRing& sr, const CUtensorM
     fence_proxy_async_shared();
     __syncwarp();
     if (lane == 0) {
-        tma_store_2d(m0, sr.slots, x0, y);
-        if (m1) tma_store_2d(m1, sr.slots + kStoreSlotBytes, x1, y);
+        tma_store_2d_hint(m0, sr.slots, x0, y, sr.policy);
+        if (m1) tma_store_2d_hint(m1, sr.slots + kStoreSlotBytes, x1, y, sr.policy);
         bulk_commit();
     }
 }
@@ -883,11 +885,13 @@ __device__ __forceinline__ bool compress_phase(const Smem& sm, uint32_t tmem, co
         if (lane == 0) {
             prefetch_tensormap(tm_x);
             prefetch_tensormap(tm_wa);
+            const uint64_t pol_a = l2_policy(p.l2_policy & kL2ActsLast ? 1 : 0);
+            const uint64_t pol_w = l2_policy(p.l2_policy & kL2WeightsLast ? 1 : 0);
             for (int i = jobs.begin; i < jobs.end; ++i) {
                 int m0, n0, split, kb0, nkb;
                 job_of(jobs[i], m0, n0, split, kb0, nkb);
                 if (!produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_x, tm_wa, m0, n0, kb0, nkb, p.bn, false,
-                                                 p.timeout_ns, [] { return true; })) {
+                                                 p.timeout_ns, [] { return true; }, pol_a, pol_w)) {
                     raise_abort(sm, p.status);
                     ok = false;
                     break;
@@ -1116,6 +1120,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             prefetch_tensormap(tm_akv);
             prefetch_tensormap(tm_bq);
             prefetch_tensormap(tm_bkv);
+            const uint64_t pol_a = l2_policy(p.l2_policy & kL2ActsLast ? 1 : 0);
+            const uint64_t pol_w = l2_policy(p.l2_policy & kL2WeightsLast ? 1 : 0);
             for (int i = jobs.begin; i < jobs.end && ok; ++i) {
                 int tile, m;
                 expand_job(p, jobs[i], tile, m);
@@ -1123,10 +1129,10 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                 const int bq = p.q_wide ? kQWide : Dn + R;  // q tile width
                 ok = tile < p.nq_tiles
                          ? produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_aq, tm_bq, m * TM, tile * bq, 0, p.kb_q,
-                                                           bq, first, p.timeout_ns, dep)
+                                                           bq, first, p.timeout_ns, dep, pol_a, pol_w)
                          : produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_akv, tm_bkv, m * TM,
                                                            (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
-                                                           p.timeout_ns, dep);
+                                                           p.timeout_ns, dep, pol_a, pol_w);
             }
             if (pdl && jobs.begin == jobs.end) pdl_wait();
             if (!ok) raise_abort(sm, p.status);
@@ -1161,7 +1167,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         int cur_m = -1;
         RowCtx ctx;
-        const StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes};
+        const StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes,
+                           l2_policy(p.l2_policy & kL2StoresFirst ? 2 : 0)};
         for (int i = jobs.begin; i < jobs.end; ++i) {
             int tile, m;
             expand_job(p, jobs[i], tile, m);
@@ -1353,6 +1360,8 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
         if (lane == 0) {
             prefetch_tensormap(tm_akv);
             prefetch_tensormap(tm_bkv);
+            const uint64_t pol_w = l2_policy(p.l2_policy & kL2WeightsLast ? 1 : 0);
+            const uint64_t pol_a = l2_policy(p.l2_policy & kL2ActsLast ? 1 : 0);
             uint32_t sjn = 0;
             int a_last = 0;  // activation blocks issued for the latest super-job
             auto b_load = [&](int tile, int kk) -> bool {
@@ -1361,8 +1370,8 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
                 if (!mbar_wait(sm.empty0 + 8 * s, ((l / kKvResStages) & 1) ^ 1, p.timeout_ns, sm.abort_flag))
                     return false;
                 if (leader) mbar_arrive_expect_tx(sm.full0 + 8 * s, 2 * kKvResB);
-                tma_load_2d_pair(sm.base + s * kKvResB, tm_bkv, map_shared_rank(sm.full0 + 8 * s, 0), kk * kBK,
-                                 tile * 256 + rank * 128);
+                tma_load_2d_pair_hint(sm.base + s * kKvResB, tm_bkv, map_shared_rank(sm.full0 + 8 * s, 0),
+                                      kk * kBK, tile * 256 + rank * 128, pol_w);
                 ++rc.loads;
                 return true;
             };
@@ -1377,8 +1386,8 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(k.afull0 + 8 * kk, 2 * kKvResA);
-                    tma_load_2d_pair(k.a + kk * kKvResA, tm_akv, map_shared_rank(k.afull0 + 8 * kk, 0), kk * kBK,
-                                     m * 256 + rank * 128);
+                    tma_load_2d_pair_hint(k.a + kk * kKvResA, tm_akv, map_shared_rank(k.afull0 + 8 * kk, 0),
+                                          kk * kBK, m * 256 + rank * 128, pol_a);
                     ++a_last;
                     ok = b_load(t0, kk);
                 }
@@ -1439,7 +1448,8 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
         const int half_idx = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes};
+        StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes,
+                     l2_policy(p.l2_policy & kL2StoresFirst ? 2 : 0)};
         RowCtx ctx;
         for (int sj = unit; sj < n_sj && ok; sj += units) {
             int m, t0, nt;

@@ -55,6 +55,7 @@ struct CompressParams {
     int w8a8;
     const float* x_scale;  // [T]
     const float* w_scale;  // [NA]
+    int l2_policy;  // L2 eviction priority of the operand loads (kL2WeightsLast, kL2ActsLast)
 };
 
 // Per-token reduction of the partials, BF16 cast, RMSNorm of c_q and c_kv,
@@ -137,7 +138,13 @@ struct ExpandParams {
     // and some row's codes large enough to need it).
     const uint32_t* w8_split;
     int n_tiles128;
+    int l2_policy;  // L2 eviction priorities: kL2WeightsLast, kL2ActsLast, kL2StoresFirst
 };
+
+// Bits of CompressParams / ExpandParams::l2_policy (MLA_TUNE_L2_POLICY):
+// weight tiles and activation tiles loaded with the evict-last priority,
+// tensor stores of the outputs with the evict-first priority.
+constexpr int kL2WeightsLast = 1, kL2ActsLast = 2, kL2StoresFirst = 4;
 
 constexpr int kQWide = 256;
 // W8A8: K blocks of one exact accumulation chain.  A chain of k blocks sums

@@ -156,10 +156,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Same, with an L2 cache-policy hint (from createpolicy).
+// Same, with an L2 cache-policy hint (from createpolicy; 0: none).
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar, int32_t c0, int32_t c1,
                                                  uint64_t policy) {
+    if (policy == 0) {
+        tma_load_2d(dst, map, bar, c0, c1);
+        return;
+    }
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
@@ -173,6 +177,19 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
                  "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// Same, with an L2 cache-policy hint for the written lines (0: none).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                                  uint64_t policy) {
+    if (policy == 0) {
+        tma_store_2d(map, src, c0, c1);
+        return;
+    }
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "l"(policy)
                  : "memory");
 }
 
@@ -220,6 +237,14 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// A policy by name for the hinted copies: 1 evict last, 2 evict first; 0
+// gives 0, which the hinted copies take as "no hint" and issue the plain
+// instruction (an explicit evict-normal hint is not the same: it slowed the
+// decode expansion's activation loads on GB300).
+__device__ __forceinline__ uint64_t l2_policy(int which) {
+    return which == 1 ? policy_evict_last() : which == 2 ? policy_evict_first() : 0ull;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -325,6 +350,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Same, with an L2 cache-policy hint (from createpolicy; 0: none).
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                                      int32_t c1, uint64_t policy) {
+    if (policy == 0) {
+        tma_load_2d_pair(dst, map, bar, c0, c1);
+        return;
+    }
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
         : "memory");
 }
 

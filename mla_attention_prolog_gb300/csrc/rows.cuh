@@ -535,6 +535,7 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
 // threads (this one is `tid`): inv = 127/amax, rint(y*inv) ties to even,
 // clamp +-127, all correctly rounded; the chunk holding column 0 writes the
 // scale amax/127.  A zero row gives codes 0 and scale 0.
+template <int kB = 8>  // 16-byte loads in flight per thread
 __device__ __forceinline__ void quant_span(const QuantParams& p, int row, int c0, int c1, float amax, int tid,
                                            int nthr) {
     const float* y = p.y + static_cast<size_t>(row) * p.row_len;
@@ -545,8 +546,7 @@ __device__ __forceinline__ void quant_span(const QuantParams& p, int row, int c0
         return;
     }
     const float inv = __fdiv_rn(127.0f, amax);
-    // eight loads in flight per thread before any store
-    constexpr int kB = 8;
+    // kB loads in flight per thread before any store
     for (int i0 = c0 + tid * 4; i0 < c1; i0 += kB * nthr * 4) {
         float4 v[kB];
 #pragma unroll

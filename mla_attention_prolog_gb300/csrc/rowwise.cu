@@ -58,15 +58,18 @@ __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kerne
 // ---------------------------------------------------------------- quant
 
 constexpr int kQuantThreads = 256;
-// Elements per CTA when the amax is known: eight 16-byte loads in flight per
-// thread.  Measured on GB300 (V3 prefill, 16384 rows of 24576): 4096 -> 338
-// us, 8192 and 12288 -> 291 us (the copy rate), 16384 -> 343 us (a ragged
-// second chunk per row).
-constexpr int kQuantChunk = 8192;
+// Elements per CTA when the amax is known: one batch of KB 16-byte loads in
+// flight per thread, 256 * KB * 4 elements.  Measured on GB300 (V3 prefill,
+// 16384 rows of 24576, the kernel alone): 4096 -> 338 us, 8192 and 12288 ->
+// 291 us (the copy rate), 16384 -> 343 us (a ragged second chunk per row).
+// Beside the kv-resident kernel (one quant CTA per SM) 12 or 16 loads in
+// flight per thread measured no faster than 8.
+constexpr int kQuantLoads = 8;
 
 // blockIdx.x = row, blockIdx.y = chunk of the row.  With a known amax the
 // chunks of a row are independent; without one, one CTA takes the whole row
 // and first reduces max |y|.
+template <int KB>
 __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantParams p) {
     pdl_wait();
     const int row = blockIdx.x;
@@ -92,7 +95,7 @@ __global__ void __launch_bounds__(kQuantThreads) mla_quant_kernel(const QuantPar
         for (int w = 0; w < kQuantThreads / 32; ++w) m = fmaxf(m, red[w]);
         amax = m;
     }
-    quant_span(p, row, c0, c1, amax, threadIdx.x, kQuantThreads);
+    quant_span<KB>(p, row, c0, c1, amax, threadIdx.x, kQuantThreads);
 }
 
 // ------------------------------------------------------------ W8A8
@@ -181,9 +184,9 @@ cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
 cudaError_t launch_quant(const QuantParams& p_in, cudaStream_t st, bool pdl) {
     if (p_in.rows == 0) return cudaSuccess;
     QuantParams p = p_in;
-    p.chunk = p.amax ? kQuantChunk : p.row_len;
+    p.chunk = p.amax ? kQuantThreads * kQuantLoads * 4 : p.row_len;
     const int chunks = (p.row_len + p.chunk - 1) / p.chunk;
-    return launch_kernel(mla_quant_kernel, dim3(p.rows, chunks), dim3(kQuantThreads), 0, st, pdl, p);
+    return launch_kernel(mla_quant_kernel<kQuantLoads>, dim3(p.rows, chunks), dim3(kQuantThreads), 0, st, pdl, p);
 }
 
 cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t st) {

@@ -647,3 +647,31 @@ def test_prefill_paths_on_unusual_shapes(d):
         else:
             _bits_equal(base, o)
     p.close()
+
+
+@pytest.mark.parametrize("name,T", [("v3_prefill", 4096), ("v3_decode", 0), ("v2lite_prefill", 0),
+                                    ("v2lite_decode", 0)])
+def test_l2_policy_keeps_outputs(name, T):
+    """The L2 eviction priorities of the bulk copies (MLA_TUNE_L2_POLICY:
+    weights / activations evict last, output stores evict first) change only
+    which lines L2 keeps: every policy writes the same bytes; out-of-range
+    policies are refused."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    outs = []
+    for pol in (0, 1, 2, 4, 7):
+        p.set_tuning(binding.TUNE_L2_POLICY, pol)
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        _bits_equal(outs[0], o)
+    for bad in (-1, 8):
+        with pytest.raises(binding.MlaPrologError):
+            p.set_tuning(binding.TUNE_L2_POLICY, bad)
+    p.close()
