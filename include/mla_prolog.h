@@ -363,12 +363,13 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            1 is not available. */
 #define MLA_TUNE_TMA_STORE 8
 /*   MLA_TUNE_COMPRESS_TILE   prefill batches: the width of the compression
- *                            projection's weight tiles, 128, 192 or 256
- *                            columns.  Wider tiles bring fewer operand bytes
- *                            per tensor-core FLOP into each SM; the 192- and
- *                            256-wide kernels sum the drained chains with
- *                            plain FP32 adds (MLA_TUNE_COMPRESS_COMPENSATED
- *                            applies to 128-wide tiles).  Default: the wide
+ *                            projection's weight tiles, 128, 144, 192 or
+ *                            256 columns.  Wider tiles bring fewer operand
+ *                            bytes per tensor-core FLOP into each SM; the
+ *                            144-, 192- and 256-wide tiles sum the drained
+ *                            chains with plain FP32 adds
+ *                            (MLA_TUNE_COMPRESS_COMPENSATED applies to
+ *                            128-wide tiles).  Default: the wide
  *                            tile that needs no split-K and brings the
  *                            busiest SM the fewest operand bytes, else 128.
  *                            INVALID_ARG for decode batches (and the

@@ -110,7 +110,7 @@ struct mla_prolog {
         int splits = 1;
         int* table = nullptr;
     };
-    CompressTile ctile[3];
+    CompressTile ctile[kNumCompressTiles];
     int expand_grid = 0;
     // cooperative decode kernel (one launch for the whole pass)
     bool fused_ok = false;     // the dims and the device allow it
@@ -390,16 +390,16 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // Prefill compression, for each weight-tile width: its split-K factor and
     // its jobs (of unequal size: ragged token and weight tiles) longest
     // first, each to the least-loaded CTA.
-    std::vector<int> ctable[3];
+    std::vector<int> ctable[kNumCompressTiles];
     int part_splits = h->cpair_splits > h->splits_a ? h->cpair_splits : h->splits_a;
     int ctile_default = 128;
     if (!h->decode) {
-        CompressTilePlan plans[3];
+        CompressTilePlan plans[kNumCompressTiles];
         ctile_default = plan_compress_tiles(d.T, h->NA, cdiv(d.D, kBK), sms, plans, ctable);
-        for (int i = 0; i < 3; ++i) {
+        for (int i = 0; i < kNumCompressTiles; ++i) {
             auto& ct = h->ctile[i];
             ct.bn = plans[i].bn;
-            ct.shape = ct.bn == 128 ? GemmShape::Wide : ct.bn == 192 ? GemmShape::Wide192 : GemmShape::Wide256;
+            ct.shape = ct.bn == 128 ? GemmShape::Wide : ct.bn <= 192 ? GemmShape::Wide192 : GemmShape::Wide256;
             ct.splits = plans[i].splits;
             if (ct.splits > part_splits) part_splits = ct.splits;
         }
@@ -415,8 +415,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     const size_t b_amax = al(T * 4);
     const size_t b_stat = 1024;  // status word, then the cooperative kernel's counters
     const size_t b_tab = al(table.size() * sizeof(int));
-    const size_t b_ctab = al(ctable[0].size() * sizeof(int)) + al(ctable[1].size() * sizeof(int)) +
-                          al(ctable[2].size() * sizeof(int));
+    size_t b_ctab = 0;
+    for (const auto& t : ctable) b_ctab += al(t.size() * sizeof(int));
     const size_t b_cptab = al(cptable.size() * sizeof(int));
     h->ws_bytes = b_part + b_norm + b_q + b_amax + b_stat + b_tab + b_ctab + b_cptab;
     if ((e = cudaMalloc(&h->ws, h->ws_bytes)) != cudaSuccess) {
@@ -455,7 +455,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         }
     }
     char* ct_base = w + b_part + b_norm + b_q + b_amax + b_stat + b_tab;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < kNumCompressTiles; ++i) {
         if (ctable[i].empty()) continue;
         h->ctile[i].table = reinterpret_cast<int*>(ct_base);
         ct_base += al(ctable[i].size() * sizeof(int));
@@ -1206,7 +1206,7 @@ int mla_prolog_plan(const mla_prolog_dims* dims, int32_t sms, mla_prolog_plan_in
     const Schedule sc = plan_schedule(d.T, d.D, Lq, Lkv, R, d.num_heads, d.nope_dim, d.v_dim, sms);
     int bn_a = sc.bn_a, splits = sc.splits_a;
     if (!sc.decode) {
-        CompressTilePlan plans[3];
+        CompressTilePlan plans[kNumCompressTiles];
         bn_a = plan_compress_tiles(d.T, NA, kb, sms, plans);
         for (const auto& ct : plans)
             if (ct.bn == bn_a) splits = ct.splits;

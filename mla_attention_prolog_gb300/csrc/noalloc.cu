@@ -128,11 +128,11 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     const int bn_kv = sc.bn_kv, group_a = sc.group_a;
     const int kb_a = cdiv(d.D, kBK);
     if (!decode) {  // the prefill compression tile a handle selects (jobs in round-robin order here)
-        CompressTilePlan plans[3];
+        CompressTilePlan plans[kNumCompressTiles];
         bn_a = plan_compress_tiles(d.T, NA, kb_a, sms, plans);
         for (const auto& ct : plans)
             if (ct.bn == bn_a) splits_a = ct.splits;
-        shape_a = bn_a == 128 ? GemmShape::Wide : bn_a == 192 ? GemmShape::Wide192 : GemmShape::Wide256;
+        shape_a = bn_a == 128 ? GemmShape::Wide : bn_a <= 192 ? GemmShape::Wide192 : GemmShape::Wide256;
     }
 
     // Scratch layout (same order as the handle's workspace) and its limit.

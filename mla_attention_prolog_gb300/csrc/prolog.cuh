@@ -409,22 +409,25 @@ inline int prefill_compress_splits(int T, int NA, int kb, int sms, int cg, int b
 // kCompressTileWidths: split-K factor and the operand bytes of the busiest
 // CTA (jobs longest first, each to the least-loaded CTA; the job tables into
 // `tables` when given and there are more jobs than CTAs).  Returns the
-// default width: the wide tile (192 or 256) that needs no split-K and brings
-// its busiest SM the fewest operand bytes, else 128.  Measured on GB300
+// default width: the wide tile (144, 192 or 256) that needs no split-K and
+// brings its busiest SM the fewest operand bytes, else 128.  (A 144-wide
+// tile runs on the 192-wide kernel: 4 tiles of 144 cover the 576 rows of a
+// KV-only prolog with 33 % more jobs than 3 tiles of 192.)  Measured on GB300
 // (step time): V3 prefill 16384 tokens 2441 / 2245 / 2173 us (128 / 192 /
 // 256), V2-Lite prefill 4096 tokens 52.3 / 43.5 / 48.1 us (256 needs
 // split-K 2 there), V3 prefill 385 tokens 109.5 / 127.3 / 120.0 us (the
 // wide ones need split-K 4).
-constexpr int kCompressTileWidths[3] = {128, 192, 256};
+constexpr int kNumCompressTiles = 4;
+constexpr int kCompressTileWidths[kNumCompressTiles] = {128, 144, 192, 256};
 struct CompressTilePlan {
     int bn, splits, jobs;
     long long busiest;
 };
-inline int plan_compress_tiles(int T, int NA, int kb, int sms, CompressTilePlan (&out)[3],
+inline int plan_compress_tiles(int T, int NA, int kb, int sms, CompressTilePlan (&out)[kNumCompressTiles],
                                std::vector<int>* tables = nullptr) {
     int def = 128;
     long long best = -1;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < kNumCompressTiles; ++i) {
         CompressTilePlan& ct = out[i];
         ct.bn = kCompressTileWidths[i];
         ct.splits = prefill_compress_splits(T, NA, kb, sms, 1, ct.bn);

@@ -427,9 +427,9 @@ def _bits_equal(a, b):
 @pytest.mark.parametrize("name,T", [("v2lite_prefill", 0), ("v2lite_prefill", 300), ("v3_prefill", 640),
                                     ("v3_prefill", 385)], ids=["v2l_full", "v2l_T300", "v3_T640", "v3_T385"])
 def test_compression_tile_widths(name, T):
-    """Every compression tile width (128 with TwoSum draining; 192 and 256 with
-    plain FP32 draining, ragged last weight tile at 256) within the bar of the
-    oracle, with the guard bands intact."""
+    """Every compression tile width (128 with TwoSum draining; 144, 192 and
+    256 with plain FP32 draining, 144 on the 192-wide kernel, ragged last
+    weight tiles) within the bar of the oracle, with the guard bands intact."""
     w = wl.WORKLOADS[name]
     d = w.dims.with_T(T) if T else w.dims
     inp = wl.make_inputs(w, d)
@@ -439,7 +439,7 @@ def test_compression_tile_widths(name, T):
     tok = tok.astype(np.int32)
     ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
     sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
-    for tile in (128, 192, 256):
+    for tile in (128, 144, 192, 256):
         p.set_tuning(binding.TUNE_COMPRESS_TILE, tile)
         assert p.schedule()["bn_a"] == tile
         o = alloc_outputs(d, DEV)
@@ -631,7 +631,7 @@ def test_prefill_paths_on_unusual_shapes(d):
             assert g.guards_intact(), k
         return o
 
-    for tile in (128, 192, 256):
+    for tile in (128, 144, 192, 256):
         p.set_tuning(binding.TUNE_COMPRESS_TILE, tile)
         run_and_check()
     p.set_tuning(binding.TUNE_PAIR_EXPAND, 1)
