@@ -368,12 +368,13 @@ __device__ __forceinline__ void norm_token(const NormRopeParams& p, int t, uint1
 // cache row -- the arithmetic of norm_token, with the chunk sums of x^2 / L
 // on lane (i / 4) % 32 in increasing chunk order, so the bits agree with it
 // for equal partials.  `pos` is the token's position, `cs_row` its cos/sin
-// row (read only when pos is valid) and `gamma` the Lq + Lkv weights, from
+// row (read only when pos is valid; c_pre, s_pre: its entries lane and
+// R/2 + lane, loaded by the caller) and `gamma` the Lq + Lkv weights, from
 // global or shared memory.  `crow` is (NA + R) BF16 of this warp's shared
 // memory.
 __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, int pos, const float* cs_row,
                                                 const uint16_t* gamma, const float* prow, size_t sstride,
-                                                int splits, uint16_t* crow) {
+                                                int splits, uint16_t* crow, float c_pre, float s_pre) {
     const int lane = threadIdx.x & 31;
     const int NA = p.NA, Lq = p.Lq, Lkv = p.Lkv, R = p.R, half = R / 2;
     uint16_t* rot = crow + NA;
@@ -464,9 +465,8 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
     const float rstd_kv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ssq_kv, p.eps)));
     __syncwarp();
     float amax_q = 0.0f, amax_kv = 0.0f;  // W8A8: max |normed| of c_q and c_kv
-    for (int i = lane * 8; i < Lq + Lkv; i += 256) {
+    auto norm8 = [&](int i, const uint4 gv) {
         const uint4 xv = *reinterpret_cast<const uint4*>(crow + i);
-        const uint4 gv = *reinterpret_cast<const uint4*>(gamma + i);
         const float rstd = i < Lq ? rstd_q : rstd_kv;
         const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
         const uint32_t gs[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -490,7 +490,8 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
             *reinterpret_cast<uint4*>(nrow + i) = ov;
         }
         if (cache_row && i >= Lq) *reinterpret_cast<uint4*>(cache_row + (i - Lq)) = ov;
-    }
+    };
+    for (int i = lane * 8; i < Lq + Lkv; i += 256) norm8(i, *reinterpret_cast<const uint4*>(gamma + i));
     if (p.w8a8) {
         // AT-11: the normed c_q and c_kv rows quantised per token, the
         // expansions' INT8 inputs (each lane re-reads its own chunks)
@@ -518,7 +519,7 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
         kpe_pair(p.interleaved, i, half, j1, j2);
         const float x1 = __uint_as_float(static_cast<uint32_t>(kp[j1]) << 16);
         const float x2 = __uint_as_float(static_cast<uint32_t>(kp[j2]) << 16);
-        const float c = cs_row[i], s = cs_row[half + i];
+        const float c = i == lane ? c_pre : cs_row[i], s = i == lane ? s_pre : cs_row[half + i];
         const float o1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(-x2, s));
         const float o2 = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s));
         rot[i] = static_cast<uint16_t>(pack_bf16x2(o1, 0.0f) & 0xFFFFu);

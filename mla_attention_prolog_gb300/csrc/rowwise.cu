@@ -28,8 +28,11 @@ template <int NT, int BATCH, bool W8 = false>
 __global__ void __launch_bounds__(NT) mla_norm_rope_kernel(const NormRopeParams p) {
     extern __shared__ __align__(16) uint16_t crow[];  // BF16 row of C [NA], then rotated k_pe [R]
     __shared__ float red[6];
-    pdl_wait();
+    // The dependent expansion may start launching now: its CTAs prefetch their
+    // first weight tiles while this grid runs, and wait for it before reading
+    // the normed rows.
     pdl_launch_dependents();
+    pdl_wait();
     norm_token<NT, BATCH, 0, W8>(p, blockIdx.x, crow, red);
 }
 
@@ -38,21 +41,38 @@ __global__ void __launch_bounds__(NT) mla_norm_rope_kernel(const NormRopeParams 
 // barrier sits between the steps.  Same arithmetic as mla_norm_rope_kernel.
 constexpr int kNormWarpTokens = 8;
 
+// Shared memory: gamma (Lq + Lkv BF16, 16-byte aligned), then each warp's
+// BF16 row and rotated k_pe.  Everything that does not come from the
+// previous kernel (gamma, the token's position and its cos/sin pair) is
+// loaded before the dependency wait, so after it only the row's loads stand
+// between the wait and the first result.
 __global__ void __launch_bounds__(32 * kNormWarpTokens) mla_norm_rope_warp_kernel(const NormRopeParams p) {
     extern __shared__ __align__(16) uint16_t wsm[];
-    pdl_wait();
-    pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5;
+    pdl_launch_dependents();  // as in mla_norm_rope_kernel
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ng = p.Lq + p.Lkv, gpad = (ng + 7) & ~7;
+    for (int i = threadIdx.x * 8; i < ng; i += 32 * kNormWarpTokens * 8)
+        *reinterpret_cast<uint4*>(wsm + i) = *reinterpret_cast<const uint4*>(p.gamma + i);
     const int t = blockIdx.x * kNormWarpTokens + warp;
+    int pos = 0;
+    float c_pre = 0.0f, s_pre = 0.0f;
+    const float* cs_row = p.cos_sin;
+    if (t < p.T) {
+        pos = p.positions[t];
+        if (pos >= 0 && pos < p.max_pos) {
+            cs_row = p.cos_sin + static_cast<size_t>(pos) * p.R;
+            if (lane < p.R / 2) c_pre = cs_row[lane], s_pre = cs_row[p.R / 2 + lane];
+        }
+    }
+    __syncthreads();  // gamma staged
+    pdl_wait();
     if (t >= p.T) return;  // warp-uniform
-    const int pos = p.positions[t];
     // the row of token t: FP32 partials, or (in_bf16) the BF16 row, at element t * NA of its type
     const float* prow = p.in_bf16 ? reinterpret_cast<const float*>(reinterpret_cast<const uint16_t*>(p.partials) +
                                                                    static_cast<size_t>(t) * p.NA)
                                   : p.partials + static_cast<size_t>(t) * p.NA;
-    norm_token_warp(p, t, pos, p.cos_sin + static_cast<size_t>(pos >= 0 && pos < p.max_pos ? pos : 0) * p.R,
-                    p.gamma, prow, static_cast<size_t>(p.T) * p.NA, p.splits,
-                    wsm + static_cast<size_t>(warp) * (p.NA + p.R));
+    norm_token_warp(p, t, pos, cs_row, wsm, prow, static_cast<size_t>(p.T) * p.NA, p.splits,
+                    wsm + gpad + static_cast<size_t>(warp) * (p.NA + p.R), c_pre, s_pre);
 }
 
 // ---------------------------------------------------------------- quant
@@ -177,8 +197,9 @@ cudaError_t launch_norm_rope(const NormRopeParams& p, cudaStream_t st) {
         return launch_kernel(p.w8a8 ? mla_norm_rope_kernel<512, 16, true> : mla_norm_rope_kernel<512, 16>, dim3(p.T),
                              dim3(512), norm_token_smem_bytes(p.NA, p.R, p.Lq, p.Lkv), st, true, p);
     const size_t smem = static_cast<size_t>(p.NA + p.R) * sizeof(uint16_t);
+    const size_t gsmem = static_cast<size_t>((p.Lq + p.Lkv + 7) & ~7) * sizeof(uint16_t);
     return launch_kernel(mla_norm_rope_warp_kernel, dim3((p.T + kNormWarpTokens - 1) / kNormWarpTokens),
-                         dim3(32 * kNormWarpTokens), smem * kNormWarpTokens, st, true, p);
+                         dim3(32 * kNormWarpTokens), gsmem + smem * kNormWarpTokens, st, true, p);
 }
 
 cudaError_t launch_quant(const QuantParams& p_in, cudaStream_t st, bool pdl) {
