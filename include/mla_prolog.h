@@ -428,10 +428,12 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            the evict-last priority, 2 the activation tiles
  *                            load with the evict-last priority, 4 the output
  *                            tensor stores of the expansions write with the
- *                            evict-first priority; 0 (the default): no
- *                            priority hint on any copy.  Values are
- *                            unchanged; only which lines L2 keeps.
- *                            INVALID_ARG outside 0..7. */
+ *                            evict-first priority; 0: no priority hint on
+ *                            any copy.  Default: 1 for prefill batches (the
+ *                            kv expansion reads ~20 % fewer DRAM bytes), 0
+ *                            for decode batches.  Values are unchanged; only
+ *                            which lines L2 keeps.  INVALID_ARG outside
+ *                            0..7. */
 #define MLA_TUNE_L2_POLICY 15
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 

@@ -514,6 +514,11 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // (56.9 / 20.3 us): the fetch delays the compression's own loads.
     const uint64_t wb_bytes = (static_cast<uint64_t>(h->NQ) * Lq + static_cast<uint64_t>(h->NKV) * Lkv) * 2;
     h->l2_fetch = h->decode && wb_bytes >= (64ull << 20);
+    // Prefill: weight tiles loaded evict-last.  Measured on GB300 (ncu, V3
+    // prefill at full size): kv-resident kernel DRAM reads 459 -> 373 MB,
+    // 463 -> 443 us; q expansion 421 -> 404 MB, 747 -> 741 us; compression
+    // 546 -> 531 MB.  Decode batches measured no change and keep no hint.
+    h->l2_policy = h->decode ? 0 : kL2WeightsLast;
     if (!ok) {
         cudaFree(h->ws);
         delete h;
