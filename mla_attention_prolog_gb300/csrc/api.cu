@@ -361,9 +361,9 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         h->cluster_expand_grid = njobs_b < sms - h->cluster_ctas ? njobs_b : sms - h->cluster_ctas;
         h->cluster_shape_b = h->shape_b == GemmShape::Narrow ? GemmShape::Deep : h->shape_b;
     }
-    // W8A8 runs on the split-K / per-tile kernels, whose epilogues turn the
-    // exact integer accumulators into dequantised values; the cooperative,
-    // cluster and kv-resident kernels do not take it.
+    // W8A8 runs on the split-K / per-tile and pair kernels, whose epilogues
+    // turn the exact integer accumulators into dequantised values; the
+    // cooperative and cluster kernels do not take it.
     h->w8a8 = (d.flags & MLA_PROLOG_W8A8) != 0;
     if (h->w8a8) {
         h->fused_ok = h->fused = false;
@@ -491,7 +491,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     h->q_wide = h->q_wide_ok;
     // Pairs: the kv tiles on their own kernel with the normed c_kv rows of a
     // 256-token tile resident in shared memory (K = Lkv <= 512).
-    if (h->pair_ok && h->ts_ok && Lkv <= 512 && Lkv % kBK == 0 && h->bn_kv == 256 && !h->w8a8) {
+    if (h->pair_ok && h->ts_ok && Lkv <= 512 && Lkv % kBK == 0 && h->bn_kv == 256) {
         int active = 0;
         if (expand_kv_pair_max_active(&active) == cudaSuccess && active >= 1) {
             h->kvres_ok = true;

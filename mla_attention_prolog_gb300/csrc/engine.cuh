@@ -1344,9 +1344,15 @@ __device__ __forceinline__ void kvres_job(const ExpandParams& p, int group, int 
 }
 
 // This pair's super-jobs: unit + i * units.  Returns false when a wait gave up.
+// W8 (W8A8): the activations and weights are INT8 codes as BF16 integers; a
+// kv tile's K (Lkv <= 8 * 64) is one exact chain, and each epilogue warp
+// dequantises the columns it then stores (w8_dequant_tile) before the
+// unchanged kv epilogue reads them.
+template <bool W8 = false>
 __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t tmem, const CUtensorMap* tm_akv,
                                                    const CUtensorMap* tm_bkv, const ExpandParams& p,
                                                    const OutMaps& om, int group, RoleCounters& rc) {
+    static_assert(!W8 || kKvResKb <= kW8ChainKb, "a kv tile's K must be one exact W8A8 chain");
     const Smem& sm = k.s;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = static_cast<int>(cluster_ctarank());
@@ -1463,6 +1469,11 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
                     break;
                 }
                 const uint32_t tbase = tmem + lane_off + (rc.chain & 1) * 256;
+                if constexpr (W8) {  // this warp's columns, which only it stores
+                    const float as = ctx.t < p.T ? p.a_scale[2 * ctx.t + 1] : 0.0f;
+                    w8_dequant_tile(tbase, tbase, false, p.bn_kv, half_idx, as, p.w_scale_kv, (t0 + h) * p.bn_kv,
+                                    p.NKV);
+                }
                 expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (t0 + h) * p.bn_kv, half_idx, y0);
                 epi_release<2>(sm, rc.chain);
             }

@@ -7,26 +7,6 @@
 
 namespace mlap {
 
-// The kv tiles of the prefill expansion on CTA pairs with the activations
-// resident in shared memory (see expand_kvres_phase): super-jobs of `group`
-// kv tiles per pair token tile.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kExpandThreads, 1)
-    mla_expand_kv_pair_kernel(const __grid_constant__ CUtensorMap tm_akv,
-                              const __grid_constant__ CUtensorMap tm_bkv,
-                              const __grid_constant__ CUtensorMap tm_ok,
-                              const __grid_constant__ CUtensorMap tm_ov, const ExpandParams p, int group) {
-    extern __shared__ uint8_t smem_raw[];
-    const KvResSmem k = kvres_carve(smem_raw);
-    const uint32_t tmem = kvres_setup(k);
-    pdl_launch_dependents();
-    RoleCounters rc;
-    OutMaps om;
-    om.k = &tm_ok;
-    om.v = &tm_ov;
-    expand_kvres_phase(k, tmem, &tm_akv, &tm_bkv, p, om, group, rc);
-    gemm_finish<256, kKvResStages, 2>(k.s, tmem, rc, p.timeout_ns);
-}
-
 // ------------------------------------------------------------ self-test
 
 // One thread waits on a barrier phase that nothing completes; the bounded
@@ -72,7 +52,7 @@ cudaError_t gemm_set_attributes() {
     if ((e = cudaFuncSetAttribute(mla_expand_pair_kernel<256, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EPair::BYTES)))
         return e;
-    if ((e = cudaFuncSetAttribute(mla_expand_kv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(mla_expand_kv_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   KvResLayout::BYTES)))
         return e;
     if ((e = cudaFuncSetAttribute(mla_compress_pair_kernel<256, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -149,13 +129,14 @@ cudaError_t expand_kv_pair_max_active(int* clusters) {
     cfg.gridDim = dim3(2);
     cfg.blockDim = dim3(kExpandThreads);
     cfg.dynamicSmemBytes = KvResLayout::BYTES;
-    return cudaOccupancyMaxActiveClusters(clusters, mla_expand_kv_pair_kernel, &cfg);
+    return cudaOccupancyMaxActiveClusters(clusters, mla_expand_kv_pair_kernel<false>, &cfg);
 }
 
 cudaError_t launch_expand_kv_pair(int pairs, const CUtensorMap& tm_akv, const CUtensorMap& tm_bkv,
                                   const OutTensorMaps& om, const ExpandParams& p, int group, cudaStream_t st) {
-    return launch_kernel(mla_expand_kv_pair_kernel, dim3(2 * pairs), dim3(kExpandThreads), KvResLayout::BYTES, st,
-                         true, tm_akv, tm_bkv, om.k, om.v, p, group);
+    if (p.w8a8) return launch_expand_kv_pair_w8(pairs, tm_akv, tm_bkv, om, p, group, st);
+    return launch_kernel(mla_expand_kv_pair_kernel<false>, dim3(2 * pairs), dim3(kExpandThreads), KvResLayout::BYTES,
+                         st, true, tm_akv, tm_bkv, om.k, om.v, p, group);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t timeout_ns, cudaStream_t st) {

@@ -93,6 +93,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kExpandThreads, 1)
     gemm_finish<BN_MAX, STAGES, 2>(sm, tmem, rc, p.timeout_ns);
 }
 
+// The kv tiles of the prefill expansion on CTA pairs with the activations
+// resident in shared memory (see expand_kvres_phase): super-jobs of `group`
+// kv tiles per pair token tile.
+template <bool W8 = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kExpandThreads, 1)
+    mla_expand_kv_pair_kernel(const __grid_constant__ CUtensorMap tm_akv,
+                              const __grid_constant__ CUtensorMap tm_bkv,
+                              const __grid_constant__ CUtensorMap tm_ok,
+                              const __grid_constant__ CUtensorMap tm_ov, const ExpandParams p, int group) {
+    extern __shared__ uint8_t smem_raw[];
+    const KvResSmem k = kvres_carve(smem_raw);
+    const uint32_t tmem = kvres_setup(k);
+    pdl_launch_dependents();
+    RoleCounters rc;
+    OutMaps om;
+    om.k = &tm_ok;
+    om.v = &tm_ov;
+    expand_kvres_phase<W8>(k, tmem, &tm_akv, &tm_bkv, p, om, group, rc);
+    gemm_finish<256, kKvResStages, 2>(k.s, tmem, rc, p.timeout_ns);
+}
+
 // ------------------------------------------------------ shared-memory layouts
 
 using EWide = Layout<256, 4, 1, kStoreStageBytes>;  // + the epilogue's store staging area

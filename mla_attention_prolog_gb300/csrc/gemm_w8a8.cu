@@ -35,6 +35,9 @@ cudaError_t gemm_w8a8_set_attributes() {
     if ((e = cudaFuncSetAttribute(mla_expand_pair_kernel<256, 6, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   EPair::BYTES)))
         return e;
+    if ((e = cudaFuncSetAttribute(mla_expand_kv_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  KvResLayout::BYTES)))
+        return e;
     return cudaSuccess;
 }
 
@@ -74,6 +77,12 @@ cudaError_t launch_expand_pair_w8(int pairs, const CUtensorMap& tm_aq, const CUt
                                   const ExpandParams& p, cudaStream_t st) {
     return launch_kernel(mla_expand_pair_kernel<256, 6, true>, dim3(2 * pairs), dim3(kExpandThreads), EPair::BYTES,
                          st, true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
+}
+
+cudaError_t launch_expand_kv_pair_w8(int pairs, const CUtensorMap& tm_akv, const CUtensorMap& tm_bkv,
+                                     const OutTensorMaps& om, const ExpandParams& p, int group, cudaStream_t st) {
+    return launch_kernel(mla_expand_kv_pair_kernel<true>, dim3(2 * pairs), dim3(kExpandThreads), KvResLayout::BYTES,
+                         st, true, tm_akv, tm_bkv, om.k, om.v, p, group);
 }
 
 }  // namespace mlap

@@ -555,6 +555,8 @@ cudaError_t launch_expand_pair(int pairs, const CUtensorMap& tm_aq, const CUtens
 cudaError_t expand_kv_pair_max_active(int* clusters);
 cudaError_t launch_expand_kv_pair(int pairs, const CUtensorMap& tm_akv, const CUtensorMap& tm_bkv,
                                   const OutTensorMaps& om, const ExpandParams& p, int group, cudaStream_t st);
+cudaError_t launch_expand_kv_pair_w8(int pairs, const CUtensorMap& tm_akv, const CUtensorMap& tm_bkv,
+                                     const OutTensorMaps& om, const ExpandParams& p, int group, cudaStream_t st);
 // The W8A8 instantiations (gemm_w8a8.cu), chosen by the launchers above
 // when the parameters ask for W8A8.
 cudaError_t gemm_w8a8_set_attributes();

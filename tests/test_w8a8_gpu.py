@@ -238,3 +238,34 @@ def test_w8a8_run_needs_loaded_weights_and_null_pointers():
                       torch.from_numpy(ww.w_scale).to(DEV))
     p.close()
     p16.close()
+
+
+@pytest.mark.parametrize("T", [1000, 4096])
+def test_w8a8_kv_resident_matches_pair_kernel(T):
+    """The W8A8 kv tiles on the kv-resident pair kernel (normed c_kv codes
+    resident, one exact chain, each warp dequantising the columns it stores)
+    give the same bytes as on the pair expansion kernel; the quant beside
+    the kv kernel too."""
+    w, d = _w8("v3_prefill", T)
+    inp = wl.make_inputs(w, d)
+    ww = wl.make_w8a8_weights(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    p.load_w8a8(torch.from_numpy(ww.W_a).to(DEV), torch.from_numpy(ww.W_b).to(DEV),
+                torch.from_numpy(ww.w_scale).to(DEV))
+    got = []
+    for kvres, overlap in ((0, 0), (1, 0), (1, 1)):
+        p.set_tuning(binding.TUNE_KV_RESIDENT, kvres)
+        p.set_tuning(binding.TUNE_QUANT_OVERLAP, overlap)
+        assert ("mla_expand_kv_pair_kernel" in p.kernel_names()) == bool(kvres)
+        outs = alloc_outputs(d, DEV)
+        p.run(dins["x"], dins["gamma"], None, None, dins["positions"], dins["cos_sin"],
+              outs["out_k"].t, outs["out_v"].t, outs["out_kpe"].t, outs["out_q_int8"].t, outs["out_scale"].t)
+        assert p.device_status() == 0
+        for k, g in outs.items():
+            assert g.guards_intact(), k
+        got.append({k: _bits(g.t) for k, g in outs.items()})
+    p.close()
+    for other in got[1:]:
+        for k in got[0]:
+            assert np.array_equal(got[0][k], other[k]), k
