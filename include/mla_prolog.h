@@ -380,10 +380,9 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            has issued its last operand loads it asks L2 to
  *                            fetch the expansion weights W_b from HBM while
  *                            it drains and the norm runs, so the expansion
- *                            reads them from L2 (the default when W_b is at
- *                            least 64 MB, where it measured faster); 0: the
- *                            expansion streams them from HBM.  INVALID_ARG
- *                            for prefill batches. */
+ *                            reads them from L2; 0 (the default, measured
+ *                            faster): the expansion streams them from HBM.
+ *                            INVALID_ARG for prefill batches. */
 #define MLA_TUNE_L2_FETCH 10
 /*   MLA_TUNE_Q_WIDE          prefill on CTA pairs with the per-token q path
  *                            (rope width 64, nope width a multiple of 64, no

@@ -507,13 +507,14 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
         }
         cudaGetLastError();
     }
-    // Decode: W_b fetched into L2 behind the compression's last loads.
-    // Measured on GB300 (step time, weights from HBM every step): V3 decode
-    // (110 MB of W_b) 49.1 -> 48.1 us; V2-Lite decode (4 MB) 16.4 -> 18.6 us.
-    // Issued from the start of the compression instead, both were slower
-    // (56.9 / 20.3 us): the fetch delays the compression's own loads.
-    const uint64_t wb_bytes = (static_cast<uint64_t>(h->NQ) * Lq + static_cast<uint64_t>(h->NKV) * Lkv) * 2;
-    h->l2_fetch = h->decode && wb_bytes >= (64ull << 20);
+    // Decode: W_b fetched into L2 behind the compression's last loads (off
+    // by default).  First measured on GB300 at V3 decode (110 MB of W_b)
+    // 49.1 -> 48.1 us and V2-Lite decode (4 MB) 16.4 -> 18.6 us; with the
+    // norm kernels' early dependent launch the V3 decode measures 49.1 us
+    // without it and 50.5 us with it.  Issued from the compression's start,
+    // or by the norm kernel's CTAs at their start, it was slower still
+    // (56.9 / 57.1 us): the fetch delays that kernel's own loads.
+    h->l2_fetch = false;
     // Prefill: weight tiles loaded evict-last.  Measured on GB300 (ncu, V3
     // prefill at full size): kv-resident kernel DRAM reads 459 -> 373 MB,
     // 463 -> 443 us; q expansion 421 -> 404 MB, 747 -> 741 us; compression

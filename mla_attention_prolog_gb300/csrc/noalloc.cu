@@ -211,13 +211,6 @@ extern "C" int mla_prolog_run_noalloc(const mla_prolog_dims* dims, const void* x
     pa.n_gamma = Lq + Lkv;
     pa.status = dstatus;
     pa.timeout_ns = timeout_ns;
-    // As a handle does: a decode batch with large expansion weights asks L2
-    // to fetch W_b behind the compression's last operand loads.
-    const uint64_t wb_bytes = (static_cast<uint64_t>(NQ) * Lq + static_cast<uint64_t>(NKV) * Lkv) * 2;
-    if (decode && wb_bytes >= (64ull << 20)) {
-        pa.l2_fetch = static_cast<const uint8_t*>(W_b);
-        pa.l2_fetch_bytes = wb_bytes;
-    }
     const int jobs_a = pa.n_tiles * m_tiles * splits_a;
     if (launch_compress(shape_a, jobs_a < sms ? jobs_a : sms, tm_x, tm_wa, pa, st) != cudaSuccess)
         return set_error("launch mla_compress_kernel");
