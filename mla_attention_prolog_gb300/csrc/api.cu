@@ -352,7 +352,7 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             h->cpair_grid = cjobs < sms / 2 ? cjobs : sms / 2;
             if (cjobs > sms / 2)
                 lpt_assign(compress_job_bytes(d.T, h->NA, kb, kPairCompressBN, h->cpair_splits, 2), sms / 2,
-                           &cptable);
+                           &cptable, true);
         }
         cudaGetLastError();
     }

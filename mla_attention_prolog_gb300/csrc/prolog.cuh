@@ -342,9 +342,12 @@ struct Schedule {
 };
 
 // Jobs of unequal cost over G CTAs, longest first, each to the least-loaded
-// CTA.  Returns the CTA loads in `load` and, when `table` is given, the job
-// table the kernels read: G + 1 start offsets, then every CTA's job ids.
-inline long long lpt_assign(const std::vector<long long>& cost, int G, std::vector<int>* table = nullptr) {
+// CTA.  Returns the busiest CTA's load and, when `table` is given, the job
+// table the kernels read: G + 1 start offsets, then every CTA's job ids --
+// in the order assigned, or (by_index) each CTA's jobs in job-id order, so
+// that CTAs that progress alike work on neighbouring job ids at any time.
+inline long long lpt_assign(const std::vector<long long>& cost, int G, std::vector<int>* table = nullptr,
+                            bool by_index = false) {
     std::vector<std::pair<long long, int>> w;
     w.reserve(cost.size());
     for (size_t j = 0; j < cost.size(); ++j) w.push_back({-cost[j], static_cast<int>(j)});
@@ -358,6 +361,8 @@ inline long long lpt_assign(const std::vector<long long>& cost, int G, std::vect
         load[best] -= e.first;
         lists[best].push_back(e.second);
     }
+    if (by_index)
+        for (auto& l : lists) std::sort(l.begin(), l.end());
     if (table) {
         table->clear();
         table->push_back(0);
@@ -433,7 +438,7 @@ inline int plan_compress_tiles(int T, int NA, int kb, int sms, CompressTilePlan 
         ct.splits = prefill_compress_splits(T, NA, kb, sms, 1, ct.bn);
         const auto cost = compress_job_bytes(T, NA, kb, ct.bn, ct.splits);
         ct.jobs = static_cast<int>(cost.size());
-        ct.busiest = lpt_assign(cost, sms, tables && ct.jobs > sms ? &tables[i] : nullptr);
+        ct.busiest = lpt_assign(cost, sms, tables && ct.jobs > sms ? &tables[i] : nullptr, true);
         if (ct.bn > 128 && ct.splits == 1 && (best < 0 || ct.busiest < best)) {
             best = ct.busiest;
             def = ct.bn;
