@@ -123,7 +123,9 @@ extern "C" {
  * Size rules (else MLA_ERR_UNSUPPORTED_DIMS):
  *   D, Lkv, R, Dn, Dv  positive multiples of 16;  Lq = 0 or a multiple of 16;
  *   R <= 128;  Dn + R <= 256 when Lq > 0;  T >= 0;  H >= 1;  max_pos >= 1;
- *   eps finite and >= 0.
+ *   eps finite and >= 0;  T * H * (Dn + R + Dv) <= 4e9 and T * D <= 4e9 (the
+ *   kernels keep row offsets in 32 bits: the DeepSeek-V3 shapes take up to
+ *   T = 69 754 tokens per run).
  */
 typedef struct mla_prolog_dims {
     int32_t  T;            /* tokens per run (rows of x)                         */

@@ -84,6 +84,41 @@ def bf16_within(got_bf16: torch.Tensor, want_bits: np.ndarray, name: str) -> Non
                            f"{np.argwhere(bad)[0].tolist()} got {got[bad][0]} want {want[bad][0]}")
 
 
+def _bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """One unit in the last place of BF16 values (8 significand bits); 0 at 0."""
+    a = np.abs(x.astype(np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 2.0 ** (e - 7), 0.0)
+
+
+def rope_within(got_bf16: torch.Tensor, want_bits: np.ndarray, kpe_in_bits: np.ndarray, cos: np.ndarray,
+                sin: np.ndarray, interleaved: bool, name: str) -> None:
+    """Rotated k_pe rows (rotate-half layout [o1 | o2], last axis R; a head
+    axis before it is broadcast) within the BF16 bar widened by what a
+    one-ulp change of either BF16 input of the pair moves the output:
+    ulp(x1)|cos| + ulp(x2)|sin| for o1, ulp(x2)|cos| + ulp(x1)|sin| for o2.
+    The compression output is rounded to BF16 before the RoPE; where the
+    exact sum lies within the FP32 accumulation's error of a rounding
+    boundary, either neighbour is a correct rounding, and a pair whose
+    products nearly cancel turns that one ulp into more than the bar.
+    kpe_in_bits [n, R]: the oracle's BF16 k_pe; cos, sin [n, R/2]."""
+    n, R = kpe_in_bits.shape
+    half = R // 2
+    kin = wl.bf16_bits_to_f32(kpe_in_bits).astype(np.float64)
+    x1 = kin[:, 0::2] if interleaved else kin[:, :half]
+    x2 = kin[:, 1::2] if interleaved else kin[:, half:]
+    c, s = np.abs(cos.astype(np.float64)), np.abs(sin.astype(np.float64))
+    slack = np.concatenate([_bf16_ulp(x1) * c + _bf16_ulp(x2) * s, _bf16_ulp(x2) * c + _bf16_ulp(x1) * s], axis=1)
+    want = wl.bf16_bits_to_f32(want_bits).astype(np.float64)
+    got = got_bf16.float().cpu().numpy().reshape(want_bits.shape).astype(np.float64)
+    if want.ndim == 3:
+        slack = slack[:, None, :]
+    bad = ~(np.abs(got - want) <= 1e-2 + 1e-2 * np.abs(want) + slack)
+    assert not bad.any(), (f"{name}: {int(bad.sum())}/{bad.size} outside the rope bar; first at "
+                           f"{np.argwhere(bad)[0].tolist()} got {got[bad][0]} want {want[bad][0]}")
+
+
 def quant_within(codes: torch.Tensor, scale: torch.Tensor, want_codes: np.ndarray, want_scale: np.ndarray) -> None:
     """Scales relative <= 1e-3; INT8 codes differ by <= 1 on <= 0.1% of elements."""
     s = scale.cpu().numpy().reshape(want_scale.shape)

@@ -60,6 +60,7 @@ def _dims(**kw):
     (dict(flags=8), -1), (dict(flags=2 | 4), -1), (dict(flags=32), -1),   # q variants without a q path; unknown
     (dict(flags=16, kv_lora_rank=2064), -2), (dict(q_lora_rank=2064, flags=1 | 16), -2),  # W8A8: K <= 2048
     (dict(q_lora_rank=64, flags=1 | 32), -1), (dict(q_lora_rank=64, flags=8), -1),
+    (dict(T=2**27), -2), (dict(T=2**24), -2),  # T * H * (Dn + R + Dv) > 4e9; T * D > 4e9
 ])
 def test_create_rejects_bad_dims_without_touching_cuda(L, kw, code):
     h = ctypes.c_void_p()

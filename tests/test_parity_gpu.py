@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import alloc_outputs, bf16_within, device_inputs, quant_within, run_prolog
+from helpers import alloc_outputs, bf16_within, device_inputs, quant_within, rope_within, run_prolog
 from mla_attention_prolog_gb300 import binding, workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -38,6 +38,9 @@ def _sample(w: wl.Workload, inp: wl.Inputs, n: int):
         return None
     rng = np.random.default_rng(7)
     must = {0, T - 1} | set(int(i) for i in inp.boosted_rows)
+    n = max(n, len(must) + 16)  # every boosted row, and some others
+    if T <= n:
+        return None
     rest = rng.choice(np.setdiff1d(np.arange(T), np.array(sorted(must))), n - len(must), replace=False)
     return np.array(sorted(must | set(int(i) for i in rest)), np.int32)
 
@@ -53,11 +56,26 @@ def check_against_oracle(w: wl.Workload, dims=None, sample=512, positions=None):
     run_prolog(p, dins, outs)
     status = p.device_status()
     tok = _sample(w, inp, sample)
-    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok,
+                            taps=True)
     sel = slice(None) if tok is None else torch.from_numpy(tok.astype(np.int64)).to(DEV)
-    bf16_within(outs["out_k"].t[sel], ref["out_k"], "out_k")
+    Dn, R, H = d.nope_dim, d.rope_dim, d.num_heads
+    n = ref["out_kpe"].shape[0]
+    # K's nope columns and V to the BF16 bar; the rotated k_pe (K's rope
+    # slices, out_kpe) to that bar widened by a one-ulp rounding of its inputs
+    k_got = outs["out_k"].t[sel].reshape(n, H, Dn + R)
+    k_want = ref["out_k"].reshape(n, H, Dn + R)
+    bf16_within(k_got[:, :, :Dn], np.ascontiguousarray(k_want[:, :, :Dn]), "out_k nope")
     bf16_within(outs["out_v"].t[sel], ref["out_v"], "out_v")
-    bf16_within(outs["out_kpe"].t[sel], ref["out_kpe"], "out_kpe")
+    rows = np.arange(d.T) if tok is None else tok
+    pos = np.clip(inp.positions[rows], 0, d.max_pos - 1)
+    cs = inp.cos_sin[pos]
+    kpe_in = ref["c"][:, d.q_lora_rank + d.kv_lora_rank:]
+    il = bool(d.flags & wl.ROPE_INTERLEAVED)
+    rope_within(k_got[:, :, Dn:], np.ascontiguousarray(k_want[:, :, Dn:]), kpe_in, cs[:, :R // 2], cs[:, R // 2:],
+                il, "out_k rope")
+    rope_within(outs["out_kpe"].t[sel], ref["out_kpe"].reshape(n, R), kpe_in, cs[:, :R // 2], cs[:, R // 2:], il,
+                "out_kpe")
     if d.q_lora_rank:
         quant_within(outs["out_q_int8"].t[sel], outs["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
     for k, g in outs.items():
@@ -89,6 +107,19 @@ RAGGED = wl.Dims(T=300, D=512, q_lora_rank=64, kv_lora_rank=128, rope_dim=32, nu
 def test_ragged_parity(dims):
     w = wl.Workload("ragged", dims, positions="uniform")
     status, ref, _ = check_against_oracle(w)
+    assert status == 0 and ref["bad_positions"] == 0
+
+
+def test_v3_prefill_beyond_32bit_offsets():
+    """The largest batch tested: the V3 prolog at T = 65536 (4x the
+    workload, near its size rule T * H * (Dn + R + Dv) <= 4e9), where the
+    FP32 q workspace is 6.4 GB, so byte offsets pass 2^32, and out_k's pass
+    2^31 -- every output within the bar of the oracle on sampled tokens up
+    to the last one, guard bands intact."""
+    w = wl.WORKLOADS["v3_prefill"]
+    d = dataclasses.replace(w.dims.with_T(65536), max_pos=65536)
+    assert d.T * d.n_q * 4 > 2**32 and d.T * d.num_heads * (d.nope_dim + d.rope_dim) * 2 > 2**31
+    status, ref, _ = check_against_oracle(w, dims=d, sample=1024)
     assert status == 0 and ref["bad_positions"] == 0
 
 
