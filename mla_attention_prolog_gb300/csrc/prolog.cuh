@@ -485,10 +485,12 @@ inline Schedule plan_schedule(int T, int D, int Lq, int Lkv, int R, int H, int D
     } else {
         s.splits_a = prefill_compress_splits(T, NA, kb_a, sms, 1);
     }
-    // Accumulation chain length (K blocks) of the compression projection with
-    // TwoSum draining: measured on GB300 to keep INT8 code flips of the
-    // V3-shaped q path at 3-4.5e-4 (bar: 1e-3) at the lowest cost.
-    s.group_a = s.decode ? 2 : 4;
+    // Accumulation chain length (K blocks) of the compression projection:
+    // each drained chain costs the tensor core ~0.4 us, and longer chains
+    // flip more INT8 q codes.  Measured on GB300 (flips vs the oracle, bar
+    // 1e-3): V3 prefill 4.2e-4 / 5.8e-4 / 1.07e-3 at 4 / 8 / 16; V3 decode
+    // 3.2e-4 / 4.5e-4 / 9.95e-4 at 2 / 4 / 14, 50.4 / 49.8 / 49.0 us per step.
+    s.group_a = 4;
     // Expansion: prefill uses 256-wide kv tiles (one head of V2/V3); decode
     // without a q path uses the narrow kernel with enough tiles to cover the
     // SMs; decode with a q path puts one q head per tile (the 192-wide,

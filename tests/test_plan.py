@@ -59,7 +59,7 @@ def test_default_schedules(name, T, bn_a, splits):
     p = binding.plan(d, SMS)
     assert (p["bn_a"], p["splits_a"]) == (bn_a, splits), p
     assert p["decode"] == (cdiv(d.T, 128) <= 2)
-    assert p["group_a"] == (2 if p["decode"] else 4)
+    assert p["group_a"] == 4
 
 
 def _random_dims(rng):
