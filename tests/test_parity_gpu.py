@@ -123,6 +123,41 @@ def test_v3_prefill_beyond_32bit_offsets():
     assert status == 0 and ref["bad_positions"] == 0
 
 
+@pytest.mark.parametrize("name,T", [("v3_prefill", 640), ("v3_decode", 0), ("v2lite_prefill", 300)])
+def test_zero_rows_of_x(name, T):
+    """Tokens whose x row is all zero: C = 0, so the RMSNorm (eps > 0) gives
+    zero rows, K, V and the rotated k_pe are zero, q is zero and its amax 0
+    -- codes 0 and scale 0 (the quant step's zero row) -- while the other
+    tokens stay within the bar of the oracle."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    inp = wl.make_inputs(w, d)
+    zero = np.array([0, 1, d.T // 2, d.T - 1], np.int64)
+    x = inp.x.copy()
+    x[zero] = 0
+    inp = dataclasses.replace(inp, x=x)
+    dins = device_inputs(inp, DEV)
+    outs = alloc_outputs(d, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    run_prolog(p, dins, outs)
+    assert p.device_status() == 0
+    tok = np.unique(np.concatenate([zero, np.linspace(0, d.T - 1, 24).astype(np.int64)])).astype(np.int32)
+    ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok)
+    sel = torch.from_numpy(tok.astype(np.int64)).to(DEV)
+    for k in ("out_k", "out_v", "out_kpe"):
+        bf16_within(outs[k].t[sel], ref[k], k)
+        for t in zero:
+            assert not outs[k].t[int(t)].float().abs().sum().item(), (k, int(t))
+    if d.q_lora_rank:
+        quant_within(outs["out_q_int8"].t[sel], outs["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+        for t in zero:
+            assert not outs["out_q_int8"].t[int(t)].abs().sum().item()
+            assert outs["out_scale"].t[int(t)].item() == 0.0
+    for k, g in outs.items():
+        assert g.guards_intact(), k
+    p.close()
+
+
 def test_out_of_range_positions_zero_fill_and_status():
     d = dataclasses.replace(RAGGED, T=40)
     w = wl.Workload("badpos", d, positions="uniform")
