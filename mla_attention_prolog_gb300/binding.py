@@ -52,6 +52,7 @@ TUNE_KV_RESIDENT = 12
 TUNE_QUANT_OVERLAP = 13
 TUNE_KV_GROUP = 14
 TUNE_L2_POLICY = 15
+TUNE_KV_HALVES = 16
 
 
 class MlaPrologDims(ctypes.Structure):

@@ -112,6 +112,10 @@ struct mla_prolog {
     };
     CompressTile ctile[kNumCompressTiles];
     int expand_grid = 0;
+    // KV-only prefill on one CTA per tile: the last jobs as half tiles
+    // (ExpandParams::kv_halves; tunable)
+    int kv_halves = 0;
+    bool kv_halves_on = false;
     // cooperative decode kernel (one launch for the whole pass)
     bool fused_ok = false;     // the dims and the device allow it
     bool fused = false;        // in use (tunable)
@@ -284,6 +288,16 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // each to the least loaded CTA, so every SM streams about the same bytes.
     const int njobs_b = ((Lq > 0 ? d.num_heads : 0) + cdiv(h->NKV, h->bn_kv)) * h->m_tiles;
     h->expand_grid = njobs_b < sms ? njobs_b : sms;
+    // A KV-only prefill whose jobs leave a last round shorter than half the
+    // grid runs those jobs as half tiles (128 of 256 columns) on twice as
+    // many CTAs: measured on GB300, V2-Lite prefill (512 jobs, 152 SMs).
+    if (!h->decode && Lq == 0 && h->bn_kv % 128 == 0 && njobs_b > sms) {
+        const int r = njobs_b % sms;
+        if (r > 0 && 2 * r <= sms) {
+            h->kv_halves = r;
+            h->kv_halves_on = true;
+        }
+    }
     // The cooperative decode kernel takes one token tile, heads of at most
     // kDecodeMaxBN columns and needs one resident CTA per SM.
     if (h->m_tiles == 1 && h->bn_kv <= kDecodeMaxBN && (Lq == 0 || d.nope_dim + R <= kDecodeMaxBN)) {
@@ -650,9 +664,11 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
         } else {
             h->tm_wqb = h->tm_wkvb;
         }
-        if (h->pair_ok) {
+        if (h->pair_ok || h->kv_halves > 0) {  // boxes of bn_kv / 2 rows: pairs, half tiles
             if (!encode_bf16(&h->tm_wkvb2, wkvb, Lkv, h->NKV, Lkv, h->bn_kv / 2))
                 return cuda_fail(cudaErrorInvalidValue, "tensor map W_kv_b (pairs)");
+        }
+        if (h->pair_ok) {
             if (Lq > 0) {
                 if (h->q_wide_ok && !encode_bf16(&h->tm_wqbw, wb, Lq, h->NQ, Lq, kQWide / 2))
                     return cuda_fail(cudaErrorInvalidValue, "tensor map W_q_b (wide pairs)");
@@ -919,8 +935,9 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
             return MLA_OK;
         }
     } else {
+        pb.kv_halves = h->kv_halves_on ? h->kv_halves : 0;
         if ((e = launch_expand(h->shape_b, h->expand_grid, h->tm_nq, h->tm_nkv, h->tm_wqb, h->tm_wkvb, h->tm_out, pb,
-                               st)) != cudaSuccess)
+                               st, &h->tm_wkvb2)) != cudaSuccess)
             return cuda_fail(e, "launch mla_expand_kernel");
         if ((e = mark(ev++)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord(timing hook)");
     }
@@ -1172,6 +1189,11 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
         case MLA_TUNE_L2_POLICY:
             if (value < 0 || value > 7) return MLA_ERR_INVALID_ARG;
             h->l2_policy = value;
+            return MLA_OK;
+        case MLA_TUNE_KV_HALVES:
+            if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && h->kv_halves == 0) return MLA_ERR_INVALID_ARG;
+            h->kv_halves_on = value == 1;
             return MLA_OK;
         case MLA_TUNE_CLUSTER_NORM:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;

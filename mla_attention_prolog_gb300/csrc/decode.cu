@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // for every token's normed row (its weight tiles do not)
     const unsigned normed_target = run * static_cast<unsigned>(p.n.T);
     const bool c_ok = expand_phase<kDecodeBN, kDecodeStages>(
-        sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p.b, rc, jobs, false, OutMaps{}, [&] {
+        sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, &tm_bkv, p.b, rc, jobs, false, OutMaps{}, [&] {
             const bool got = wait_counter(p.sync + kSyncNormed, normed_target, p.timeout_ns, sm.abort_flag);
             if (!got) atomicOr(p.status, kStatusWaitTimeout);
             fence_proxy_async_global();  // the normed rows were written with plain stores

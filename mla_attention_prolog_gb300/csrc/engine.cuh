@@ -389,13 +389,35 @@ __device__ __forceinline__ void store_boxes_f32(const StoreRing& sr, const CUten
 // tiles.  Jobs go through the tiles in groups of group_n: all token tiles of
 // a group before the next group, so the weights of a group stay in L2 while
 // every token tile passes through them.
-__device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& tile, int& m_tile) {
+// With kv_halves, job ids from full - kv_halves on are half tiles: c0 is
+// the first column within the tile and width the columns the job covers.
+__device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& tile, int& m_tile, int& c0,
+                                           int& width) {
     const int ntiles = p.nq_tiles + p.nkv_tiles;
+    const int from = ntiles * p.m_tiles - p.kv_halves;
+    c0 = 0;
+    width = p.bn_kv;
+    if (p.kv_halves > 0 && j >= from) {
+        const int h = j - from;
+        j = from + h / 2;
+        width = p.bn_kv / 2;
+        c0 = (h & 1) * width;
+    }
     const int per_group = p.group_n * p.m_tiles;
     const int g = j / per_group, r = j - g * per_group;
     const int gw = ntiles - g * p.group_n < p.group_n ? ntiles - g * p.group_n : p.group_n;
     m_tile = r / gw;
     tile = g * p.group_n + (r - m_tile * gw);
+}
+
+__device__ __forceinline__ void expand_job(const ExpandParams& p, int j, int& tile, int& m_tile) {
+    int c0, width;
+    expand_job(p, j, tile, m_tile, c0, width);
+}
+
+// Jobs of the expansion (the half tiles count one each).
+__device__ __forceinline__ int expand_njobs(const ExpandParams& p) {
+    return (p.nq_tiles + p.nkv_tiles) * p.m_tiles + p.kv_halves;
 }
 
 // Per-row state of the expansion epilogue: the row's token, whether its
@@ -635,10 +657,10 @@ __device__ __forceinline__ void expand_q_epilogue(const ExpandParams& p, uint32_
 // into K's first Dn columns, value into out_v, both BF16.  Column half h
 // takes columns [h * bn / 2, (h + 1) * bn / 2).
 __device__ __forceinline__ void expand_kv_epilogue(const ExpandParams& p, uint32_t tbase, const RowCtx& rc, int n0,
-                                                   int half_idx) {
+                                                   int half_idx, int width) {
     const int Dn = p.Dn, R = p.R, HD = p.Dn + p.Dv;
     const int t = rc.t;
-    const int hw = p.bn_kv / 2;
+    const int hw = width / 2;
     // 16 columns -> BF16 at K's nope slice or V (a 16-column group never
     // straddles the two: Dn and Dv are multiples of 16)
     auto store16 = [&](int c, const float* v) {
@@ -772,8 +794,9 @@ __device__ __forceinline__ void expand_qw_epilogue_ts(const ExpandParams& p, con
 // The kv tile through the store ring (Dn, Dv multiples of 32, bn_kv a
 // multiple of 64): 32-column groups, each all k_nope or all value.
 __device__ __forceinline__ void expand_kv_epilogue_ts(const ExpandParams& p, const OutMaps& om, const StoreRing& sr,
-                                                      uint32_t tbase, const RowCtx& rc, int n0, int half_idx, int y0) {
-    const int Dn = p.Dn, HD = p.Dn + p.Dv, hw = p.bn_kv / 2;
+                                                      uint32_t tbase, const RowCtx& rc, int n0, int half_idx, int y0,
+                                                      int width) {
+    const int Dn = p.Dn, HD = p.Dn + p.Dv, hw = width / 2;
     const bool issue = y0 < p.T;
     // 32-column group at n: its output tensor and first element
     auto dst = [&](int n, int& x) -> const CUtensorMap* {
@@ -1106,8 +1129,9 @@ __device__ __forceinline__ bool w8_two_chains(const ExpandParams& p, int m, int 
 template <int BN_MAX, int STAGES, int CG = 1, bool TS = false, bool W8 = false, class Dep>
 __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, const CUtensorMap* tm_aq,
                                              const CUtensorMap* tm_akv, const CUtensorMap* tm_bq,
-                                             const CUtensorMap* tm_bkv, const ExpandParams& p, RoleCounters& rc,
-                                             const CtaJobs& jobs, bool pdl, const OutMaps& om, Dep&& dep) {
+                                             const CUtensorMap* tm_bkv, const CUtensorMap* tm_bkvh,
+                                             const ExpandParams& p, RoleCounters& rc, const CtaJobs& jobs, bool pdl,
+                                             const OutMaps& om, Dep&& dep) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Dn = p.Dn, R = p.R;
     const int rank = CG == 2 ? static_cast<int>(cluster_ctarank()) : 0;
@@ -1123,16 +1147,16 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             const uint64_t pol_a = l2_policy(p.l2_policy & kL2ActsLast ? 1 : 0);
             const uint64_t pol_w = l2_policy(p.l2_policy & kL2WeightsLast ? 1 : 0);
             for (int i = jobs.begin; i < jobs.end && ok; ++i) {
-                int tile, m;
-                expand_job(p, jobs[i], tile, m);
+                int tile, m, c0, w;
+                expand_job(p, jobs[i], tile, m, c0, w);
                 const bool first = i == jobs.begin;
                 const int bq = p.q_wide ? kQWide : Dn + R;  // q tile width
                 ok = tile < p.nq_tiles
                          ? produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_aq, tm_bq, m * TM, tile * bq, 0, p.kb_q,
                                                            bq, first, p.timeout_ns, dep, pol_a, pol_w)
-                         : produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_akv, tm_bkv, m * TM,
-                                                           (tile - p.nq_tiles) * p.bn_kv, 0, p.kb_kv, p.bn_kv, first,
-                                                           p.timeout_ns, dep, pol_a, pol_w);
+                         : produce_job<BN_MAX, STAGES, CG>(sm, rc.loads, tm_akv, w < p.bn_kv ? tm_bkvh : tm_bkv,
+                                                           m * TM, (tile - p.nq_tiles) * p.bn_kv + c0, 0, p.kb_kv, w,
+                                                           first, p.timeout_ns, dep, pol_a, pol_w);
             }
             if (pdl && jobs.begin == jobs.end) pdl_wait();
             if (!ok) raise_abort(sm, p.status);
@@ -1140,11 +1164,13 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {  // a pair's MMAs are issued by its even CTA
             const uint32_t idesc_q = idesc_bf16_f32(TM, p.q_wide ? kQWide : Dn + R);
-            const uint32_t idesc_kv = idesc_bf16_f32(TM, p.bn_kv);
+            const uint32_t idesc_kv_full = idesc_bf16_f32(TM, p.bn_kv);
+            const uint32_t idesc_kvh = idesc_bf16_f32(TM, p.bn_kv / 2);  // half tiles (kv_halves)
             for (int i = jobs.begin; i < jobs.end && ok; ++i) {
-                int tile, m;
-                expand_job(p, jobs[i], tile, m);
+                int tile, m, c0, w;
+                expand_job(p, jobs[i], tile, m, c0, w);
                 const bool q = tile < p.nq_tiles;
+                const uint32_t idesc_kv = w < p.bn_kv ? idesc_kvh : idesc_kv_full;
                 const int nkb = q ? p.kb_q : p.kb_kv;
                 if (W8 && w8_two_chains(p, m, CG, q)) {  // W8A8: two exact chains, one per accumulator buffer
                     ok = mma_chain<BN_MAX, STAGES, CG>(sm, rc.consumed, rc.chain, nkb / 2, tmem,
@@ -1170,8 +1196,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
         const StoreRing sr{sm.stage + static_cast<uint32_t>(warp - 2) * 2u * kStoreSlotBytes,
                            l2_policy(p.l2_policy & kL2StoresFirst ? 2 : 0)};
         for (int i = jobs.begin; i < jobs.end; ++i) {
-            int tile, m;
-            expand_job(p, jobs[i], tile, m);
+            int tile, m, c0, kv_w;
+            expand_job(p, jobs[i], tile, m, c0, kv_w);
             if (m != cur_m) {  // before waiting for the accumulator
                 load_row_ctx(p, m * TM + rank * kBM + row, ctx);
                 cur_m = m;
@@ -1191,7 +1217,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
                                         half_idx, as, p.w_scale_q, tile * bq, p.NQ);
                     else
                         w8_dequant_tile(tbase, tmem + lane_off + ((rc.chain + 1) & 1) * BN_MAX, chains == 2,
-                                        p.bn_kv, half_idx, as, p.w_scale_kv, (tile - p.nq_tiles) * p.bn_kv, p.NKV);
+                                        kv_w, half_idx, as, p.w_scale_kv, (tile - p.nq_tiles) * p.bn_kv + c0,
+                                        p.NKV);
                 }
                 // Every warp's columns are converted before any warp reads
                 // them.  The store-ring epilogues (wide q tiles, kv tiles, and
@@ -1217,7 +1244,8 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             }
             const int y0 = m * TM + rank * kBM + quarter * 32;
             if (TS && p.tma_store && tile >= p.nq_tiles)
-                expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx, y0);
+                expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv + c0, half_idx, y0,
+                                      kv_w);
             else if (TS && p.q_wide)
                 expand_qw_epilogue_ts(p, om, sr, tbase, ctx, tile * kQWide, half_idx, y0);
             else if (TS && p.tma_store && !p.per_head)
@@ -1225,7 +1253,7 @@ __device__ __forceinline__ bool expand_phase(const Smem& sm, uint32_t tmem, cons
             else if (tile < p.nq_tiles)
                 expand_q_epilogue(p, tbase, ctx, tile, half_idx);
             else
-                expand_kv_epilogue(p, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv, half_idx);
+                expand_kv_epilogue(p, tbase, ctx, (tile - p.nq_tiles) * p.bn_kv + c0, half_idx, kv_w);
             epi_release<CG>(sm, rc.chain);
             if (chains == 2) epi_release<CG>(sm, rc.chain + 1);
             rc.chain += chains;
@@ -1474,7 +1502,7 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
                     w8_dequant_tile(tbase, tbase, false, p.bn_kv, half_idx, as, p.w_scale_kv, (t0 + h) * p.bn_kv,
                                     p.NKV);
                 }
-                expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (t0 + h) * p.bn_kv, half_idx, y0);
+                expand_kv_epilogue_ts(p, om, sr, tbase, ctx, (t0 + h) * p.bn_kv, half_idx, y0, p.bn_kv);
                 epi_release<2>(sm, rc.chain);
             }
         }

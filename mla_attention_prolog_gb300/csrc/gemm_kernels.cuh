@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                       const __grid_constant__ CUtensorMap tm_akv,
                       const __grid_constant__ CUtensorMap tm_bq,
                       const __grid_constant__ CUtensorMap tm_bkv,
+                      const __grid_constant__ CUtensorMap tm_bkvh,
                       const __grid_constant__ CUtensorMap tm_oq,
                       const __grid_constant__ CUtensorMap tm_ok,
                       const __grid_constant__ CUtensorMap tm_ov, const ExpandParams p) {
@@ -39,8 +40,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const uint32_t tmem = gemm_setup<BN_MAX, STAGES>(sm, kExpandEpiWarps);
     pdl_launch_dependents();
     RoleCounters rc;
-    const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles);
-    expand_phase<BN_MAX, STAGES, 1, TS, W8>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true,
+    const CtaJobs jobs(p.job_table, expand_njobs(p));
+    expand_phase<BN_MAX, STAGES, 1, TS, W8>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, &tm_bkvh, p, rc, jobs, true,
                                         OutMaps{&tm_oq, &tm_ok, &tm_ov}, [] {
                                             pdl_wait();
                                             return true;
@@ -85,7 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kExpandThreads, 1)
     pdl_launch_dependents();
     RoleCounters rc;
     const CtaJobs jobs(p.job_table, (p.nq_tiles + p.nkv_tiles) * p.m_tiles, 2);
-    expand_phase<BN_MAX, STAGES, 2, true, W8>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, p, rc, jobs, true,
+    expand_phase<BN_MAX, STAGES, 2, true, W8>(sm, tmem, &tm_aq, &tm_akv, &tm_bq, &tm_bkv, &tm_bkv, p, rc, jobs, true,
                                           OutMaps{&tm_oq, &tm_ok, &tm_ov}, [] {
                                               pdl_wait();
                                               return true;

@@ -58,18 +58,19 @@ cudaError_t launch_compress_w8(GemmShape s, int grid, const CUtensorMap& tm_x, c
 
 cudaError_t launch_expand_w8(GemmShape s, int grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
                              const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
-                             const ExpandParams& p, cudaStream_t st) {
+                             const ExpandParams& p, cudaStream_t st, const CUtensorMap* tm_bkvh) {
+    const CUtensorMap& bkvh = tm_bkvh ? *tm_bkvh : tm_bkv;
     if (s == GemmShape::Wide)
         return launch_kernel(mla_expand_kernel<256, 4, true, true>, dim3(grid), dim3(kExpandThreads), EWide::BYTES,
-                             st, true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
+                             st, true, tm_aq, tm_akv, tm_bq, tm_bkv, bkvh, om.q, om.k, om.v, p);
     if (s == GemmShape::Mid)
         return launch_kernel(mla_expand_kernel<192, 5, false, true>, dim3(grid), dim3(kExpandThreads), EMid::BYTES,
-                             st, true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
+                             st, true, tm_aq, tm_akv, tm_bq, tm_bkv, bkvh, om.q, om.k, om.v, p);
     if (s == GemmShape::Deep)
         return launch_kernel(mla_expand_kernel<64, 8, false, true>, dim3(grid), dim3(kExpandThreads), EDeep::BYTES,
-                             st, true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
+                             st, true, tm_aq, tm_akv, tm_bq, tm_bkv, bkvh, om.q, om.k, om.v, p);
     return launch_kernel(mla_expand_kernel<64, 4, false, true>, dim3(grid), dim3(kExpandThreads), ENarrow::BYTES, st,
-                         true, tm_aq, tm_akv, tm_bq, tm_bkv, om.q, om.k, om.v, p);
+                         true, tm_aq, tm_akv, tm_bq, tm_bkv, bkvh, om.q, om.k, om.v, p);
 }
 
 cudaError_t launch_expand_pair_w8(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,

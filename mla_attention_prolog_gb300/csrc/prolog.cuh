@@ -139,6 +139,12 @@ struct ExpandParams {
     const uint32_t* w8_split;
     int n_tiles128;
     int l2_policy;  // L2 eviction priorities: kL2WeightsLast, kL2ActsLast, kL2StoresFirst
+    // A KV-only prolog on one CTA per tile: the last kv_halves jobs of the
+    // job order run as two jobs each over the columns [0, bn_kv / 2) and
+    // [bn_kv / 2, bn_kv) of their tile, appended after the others (job ids
+    // full - kv_halves .. full + kv_halves - 1), so that a last round of
+    // jobs shorter than the grid spreads over twice as many CTAs.
+    int kv_halves;
 };
 
 // Bits of CompressParams / ExpandParams::l2_policy (MLA_TUNE_L2_POLICY):
@@ -540,10 +546,12 @@ cudaError_t launch_compress(GemmShape s, int grid, const CUtensorMap& tm_x,
 struct OutTensorMaps {
     CUtensorMap q, k, v;
 };
+// tm_bkvh: W_kv_b in boxes of bn_kv / 2 rows, for the half tiles of
+// ExpandParams::kv_halves (null: no half tiles).
 cudaError_t launch_expand(GemmShape s, int grid, const CUtensorMap& tm_aq,
                           const CUtensorMap& tm_akv, const CUtensorMap& tm_bq,
                           const CUtensorMap& tm_bkv, const OutTensorMaps& om, const ExpandParams& p,
-                          cudaStream_t st);
+                          cudaStream_t st, const CUtensorMap* tm_bkvh = nullptr);
 // Prefill expansion on CTA pairs: 256-token tiles, kv tiles of 256 columns,
 // q heads of at most 256 columns; the B tensor maps' boxes are half a tile
 // (bn / 2 rows) and m_tiles counts 256-token tiles.
@@ -571,7 +579,7 @@ cudaError_t launch_compress_w8(GemmShape s, int grid, const CUtensorMap& tm_x, c
                                const CompressParams& p, cudaStream_t st);
 cudaError_t launch_expand_w8(GemmShape s, int grid, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
                              const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
-                             const ExpandParams& p, cudaStream_t st);
+                             const ExpandParams& p, cudaStream_t st, const CUtensorMap* tm_bkvh = nullptr);
 cudaError_t launch_expand_pair_w8(int pairs, const CUtensorMap& tm_aq, const CUtensorMap& tm_akv,
                                   const CUtensorMap& tm_bq, const CUtensorMap& tm_bkv, const OutTensorMaps& om,
                                   const ExpandParams& p, cudaStream_t st);

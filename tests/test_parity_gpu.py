@@ -660,6 +660,43 @@ def test_quant_beside_kv_kernel_keeps_outputs():
     p.close()
 
 
+@pytest.mark.parametrize("T,variant", [(0, 0), (4000, 0), (0, wl.W8A8)], ids=["full", "T4000", "w8a8"])
+def test_kv_half_tiles_keep_outputs(T, variant):
+    """The KV-only prefill's last round of jobs as half tiles (128 of 256
+    columns, MLA_TUNE_KV_HALVES, the default where 56 of 512 jobs would
+    otherwise run alone) writes the same bytes as whole tiles; the key is
+    refused where there is no such round."""
+    w = wl.WORKLOADS["v2lite_prefill"]
+    d = w.dims.with_T(T) if T else w.dims
+    d = dataclasses.replace(d, flags=d.flags | variant)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    if variant & wl.W8A8:
+        ww = wl.make_w8a8_weights(w, d)
+        p.load_w8a8(torch.from_numpy(ww.W_a).to(DEV), torch.from_numpy(ww.W_b).to(DEV),
+                    torch.from_numpy(ww.w_scale).to(DEV))
+        dins["W_a"] = dins["W_b"] = None
+    outs = []
+    for f in (1, 0, 1):
+        p.set_tuning(binding.TUNE_KV_HALVES, f)
+        o = alloc_outputs(d, DEV)
+        run_prolog(p, dins, o)
+        assert p.device_status() == 0
+        outs.append(o)
+    torch.cuda.synchronize()
+    _bits_equal(outs[0], outs[1])
+    _bits_equal(outs[0], outs[2])
+    for o in outs:
+        for k, g in o.items():
+            assert g.guards_intact(), k
+    p.close()
+    q = binding.MlaProlog.from_dims(w.dims.with_T(300))  # 48 jobs: no second round
+    with pytest.raises(binding.MlaPrologError):
+        q.set_tuning(binding.TUNE_KV_HALVES, 1)
+    q.close()
+
+
 # Unusual shapes for the prefill paths: smaller ranks, few heads, 64-wide nope
 # and value (two heads per 256-column kv tile), ragged token counts.
 _ODD_PREFILL = [
