@@ -436,12 +436,14 @@ int mla_prolog_copy_tap(mla_prolog_t h, int32_t which, void* dst, size_t bytes, 
  *                            which lines L2 keeps.  INVALID_ARG outside
  *                            0..7. */
 #define MLA_TUNE_L2_POLICY 15
-/*   MLA_TUNE_KV_HALVES       KV-only prefill on one CTA per tile, when the
- *                            jobs leave a last round shorter than half the
- *                            grid: 1 (the default there): those jobs run as
- *                            two half tiles each (bn_kv / 2 columns) on twice
- *                            as many CTAs; 0: as whole tiles.  Same values
- *                            either way.  INVALID_ARG when not available. */
+/*   MLA_TUNE_KV_HALVES       when the kv jobs leave a last round shorter
+ *                            than half the grid: 1 (the default there):
+ *                            those jobs run as two half jobs each on twice
+ *                            as many CTAs -- half tiles (bn_kv / 2 columns)
+ *                            for a KV-only prefill on one CTA per tile, half
+ *                            groups of kv tiles on the kv-resident kernel;
+ *                            0: whole.  Same values either way.  INVALID_ARG
+ *                            when not available. */
 #define MLA_TUNE_KV_HALVES 16
 int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value);
 

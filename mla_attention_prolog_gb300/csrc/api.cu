@@ -115,6 +115,7 @@ struct mla_prolog {
     // KV-only prefill on one CTA per tile: the last jobs as half tiles
     // (ExpandParams::kv_halves; tunable)
     int kv_halves = 0;
+    int kvres_halves = 0;  // the same for the kv-resident kernel's super-jobs
     bool kv_halves_on = false;
     // cooperative decode kernel (one launch for the whole pass)
     bool fused_ok = false;     // the dims and the device allow it
@@ -189,6 +190,18 @@ namespace {
 // Whether the kv tiles run on the kv-resident pair kernel (with the pair
 // expansion): its epilogue writes through tensor stores.
 bool kvres_active(mla_prolog_t h) { return h->kvres && h->tma_store; }
+
+// The kv-resident kernel's last round of super-jobs as half super-jobs when
+// that round is shorter than half the pairs and every group is whole.
+void plan_kvres_halves(mla_prolog_t h) {
+    const int nkv_tiles = cdiv(h->NKV, h->bn_kv);
+    const int n_sj = h->pair_m_tiles * cdiv(nkv_tiles, h->kvres_group);
+    const int r = h->kvres_grid > 0 ? n_sj % h->kvres_grid : 0;
+    h->kvres_halves = n_sj > h->kvres_grid && r > 0 && 2 * r <= h->kvres_grid && h->kvres_group >= 2 &&
+                              nkv_tiles % h->kvres_group == 0
+                          ? r
+                          : 0;
+}
 
 bool select_compress_tile(mla_prolog_t h, int bn) {
     for (const auto& ct : h->ctile) {
@@ -513,6 +526,8 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
             h->kvres_group = plan_kv_group(h->pair_m_tiles, nkv_tiles, sms / 2);
             const int n_sj = h->pair_m_tiles * cdiv(nkv_tiles, h->kvres_group);
             h->kvres_grid = n_sj < sms / 2 ? n_sj : sms / 2;
+            plan_kvres_halves(h);
+            if (h->kvres_halves > 0) h->kv_halves_on = true;
             // Measured on GB300 with groups of 8: V3 prefill step 2044 -> 2009
             // us, with the per-head quant 1872 -> 1827 us.  On when every pair
             // gets at least two super-jobs (the kv-only V2-Lite prefill runs
@@ -922,6 +937,7 @@ int run_pass(mla_prolog_t h, const void* x, const void* gamma, const void* W_a, 
             pk.m_tiles = h->pair_m_tiles;
             pk.nq_tiles = 0;
             pk.job_table = nullptr;
+            pk.kvres_halves = h->kv_halves_on ? h->kvres_halves : 0;
             if ((e = launch_expand_kv_pair(h->kvres_grid, h->tm_nkv, h->tm_wkvb2, h->tm_out, pk, h->kvres_group, st)) !=
                 cudaSuccess)
                 return cuda_fail(e, "launch mla_expand_kv_pair_kernel");
@@ -1167,6 +1183,7 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             h->kvres_group = value;
             const int n_sj = h->pair_m_tiles * cdiv(nkv_tiles, value);
             h->kvres_grid = n_sj < h->sms / 2 ? n_sj : h->sms / 2;
+            plan_kvres_halves(h);
             return MLA_OK;
         }
         case MLA_TUNE_QUANT_OVERLAP:
@@ -1192,7 +1209,7 @@ int mla_prolog_set_tuning(mla_prolog_t h, int32_t key, int32_t value) {
             return MLA_OK;
         case MLA_TUNE_KV_HALVES:
             if (value != 0 && value != 1) return MLA_ERR_INVALID_ARG;
-            if (value == 1 && h->kv_halves == 0) return MLA_ERR_INVALID_ARG;
+            if (value == 1 && h->kv_halves == 0 && h->kvres_halves == 0) return MLA_ERR_INVALID_ARG;
             h->kv_halves_on = value == 1;
             return MLA_OK;
         case MLA_TUNE_CLUSTER_NORM:

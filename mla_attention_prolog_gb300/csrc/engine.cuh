@@ -1366,9 +1366,20 @@ __device__ __forceinline__ uint32_t kvres_setup(const KvResSmem& k) {
 // Super-job sj -> (pair token tile m, first kv tile, tiles in the group).
 __device__ __forceinline__ void kvres_job(const ExpandParams& p, int group, int sj, int& m, int& t0, int& nt) {
     const int ngroups = (p.nkv_tiles + group - 1) / group;
+    const int from = p.m_tiles * ngroups - p.kvres_halves;
+    int half = -1;
+    if (p.kvres_halves > 0 && sj >= from) {  // half super-jobs (ExpandParams::kvres_halves)
+        half = (sj - from) & 1;
+        sj = from + (sj - from) / 2;
+    }
     m = sj / ngroups;
     t0 = (sj - m * ngroups) * group;
     nt = p.nkv_tiles - t0 < group ? p.nkv_tiles - t0 : group;
+    if (half >= 0) {
+        const int n0 = (nt + 1) / 2;
+        t0 += half ? n0 : 0;
+        nt = half ? nt - n0 : n0;
+    }
 }
 
 // This pair's super-jobs: unit + i * units.  Returns false when a wait gave up.
@@ -1386,7 +1397,7 @@ __device__ __forceinline__ bool expand_kvres_phase(const KvResSmem& k, uint32_t 
     const int rank = static_cast<int>(cluster_ctarank());
     const bool leader = rank == 0;
     const int unit = static_cast<int>(blockIdx.x) / 2, units = static_cast<int>(gridDim.x) / 2;
-    const int n_sj = p.m_tiles * ((p.nkv_tiles + group - 1) / group);
+    const int n_sj = p.m_tiles * ((p.nkv_tiles + group - 1) / group) + p.kvres_halves;
     const int kb = p.kb_kv;
     bool ok = true;
     pdl_wait();  // the normed rows come from the norm kernel; amax clearing precedes the epilogue

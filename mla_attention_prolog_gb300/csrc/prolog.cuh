@@ -145,6 +145,11 @@ struct ExpandParams {
     // full - kv_halves .. full + kv_halves - 1), so that a last round of
     // jobs shorter than the grid spreads over twice as many CTAs.
     int kv_halves;
+    // The same for the kv-resident pair kernel's super-jobs (a token tile and
+    // a group of kv tiles): its last kvres_halves super-jobs run as two
+    // super-jobs of half the group each, appended after the others (every
+    // group whole, of at least two tiles).
+    int kvres_halves;
 };
 
 // Bits of CompressParams / ExpandParams::l2_policy (MLA_TUNE_L2_POLICY):

@@ -660,13 +660,17 @@ def test_quant_beside_kv_kernel_keeps_outputs():
     p.close()
 
 
-@pytest.mark.parametrize("T,variant", [(0, 0), (4000, 0), (0, wl.W8A8)], ids=["full", "T4000", "w8a8"])
-def test_kv_half_tiles_keep_outputs(T, variant):
-    """The KV-only prefill's last round of jobs as half tiles (128 of 256
-    columns, MLA_TUNE_KV_HALVES, the default where 56 of 512 jobs would
-    otherwise run alone) writes the same bytes as whole tiles; the key is
-    refused where there is no such round."""
-    w = wl.WORKLOADS["v2lite_prefill"]
+@pytest.mark.parametrize("name,T,variant", [("v2lite_prefill", 0, 0), ("v2lite_prefill", 4000, 0),
+                                            ("v2lite_prefill", 0, wl.W8A8), ("v3_prefill", 4096, 0),
+                                            ("v3_prefill", 0, 0), ("v3_prefill", 4096, wl.W8A8)],
+                         ids=["v2l_full", "v2l_T4000", "v2l_w8a8", "v3_T4096", "v3_full", "v3_T4096_w8a8"])
+def test_kv_half_tiles_keep_outputs(name, T, variant):
+    """The last round of kv jobs as half jobs (MLA_TUNE_KV_HALVES): on the
+    KV-only prefill's one-CTA kernel half tiles (128 of 256 columns; 56 of
+    512 jobs would otherwise run alone), on the kv-resident pair kernel half
+    super-jobs (4 of 8 kv tiles; V3: 36 of 1024) -- the same bytes as whole
+    jobs; the key is refused where there is no such round."""
+    w = wl.WORKLOADS[name]
     d = w.dims.with_T(T) if T else w.dims
     d = dataclasses.replace(d, flags=d.flags | variant)
     inp = wl.make_inputs(w, d)
