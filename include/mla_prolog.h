@@ -505,12 +505,15 @@ int mla_prolog_schedule(mla_prolog_t h, int32_t* bn_a, int32_t* splits_a,
  * accumulation-chain length in K blocks of 64; compress_jobs: its jobs (token
  * tiles x weight tiles x splits); busiest_bytes: the operand bytes (token rows
  * + weight rows, 128 bytes per row per K block) that the busiest CTA streams
- * in the compression; bn_kv: the expansion's kv tile width.
+ * in the compression; bn_kv: the expansion's kv tile width; kv_halves: for
+ * a KV-only prefill, the last-round expansion jobs that run as two half
+ * tiles each (MLA_TUNE_KV_HALVES; 0: none).
  * Errors: INVALID_ARG (a NULL pointer, sms < 1), UNSUPPORTED_DIMS as
  * mla_prolog_create().
  */
 typedef struct mla_prolog_plan_info {
     int32_t decode, bn_a, splits_a, group_a, compress_jobs, bn_kv;
+    int32_t kv_halves;
     int64_t busiest_bytes;
 } mla_prolog_plan_info;
 int mla_prolog_plan(const mla_prolog_dims* dims, int32_t sms, mla_prolog_plan_info* out);

@@ -63,7 +63,8 @@ class MlaPrologDims(ctypes.Structure):
 
 class MlaPrologPlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
-        "decode", "bn_a", "splits_a", "group_a", "compress_jobs", "bn_kv")] + [("busiest_bytes", ctypes.c_int64)]
+        "decode", "bn_a", "splits_a", "group_a", "compress_jobs", "bn_kv", "kv_halves")] + \
+        [("busiest_bytes", ctypes.c_int64)]
 
 
 class MlaPrologError(RuntimeError):

@@ -196,10 +196,8 @@ bool kvres_active(mla_prolog_t h) { return h->kvres && h->tma_store; }
 void plan_kvres_halves(mla_prolog_t h) {
     const int nkv_tiles = cdiv(h->NKV, h->bn_kv);
     const int n_sj = h->pair_m_tiles * cdiv(nkv_tiles, h->kvres_group);
-    const int r = h->kvres_grid > 0 ? n_sj % h->kvres_grid : 0;
-    h->kvres_halves = n_sj > h->kvres_grid && r > 0 && 2 * r <= h->kvres_grid && h->kvres_group >= 2 &&
-                              nkv_tiles % h->kvres_group == 0
-                          ? r
+    h->kvres_halves = h->kvres_group >= 2 && nkv_tiles % h->kvres_group == 0
+                          ? plan_last_round_halves(n_sj, h->kvres_grid)
                           : 0;
 }
 
@@ -304,12 +302,9 @@ int mla_prolog_create(const mla_prolog_dims* dims, mla_prolog_t* out) {
     // A KV-only prefill whose jobs leave a last round shorter than half the
     // grid runs those jobs as half tiles (128 of 256 columns) on twice as
     // many CTAs: measured on GB300, V2-Lite prefill (512 jobs, 152 SMs).
-    if (!h->decode && Lq == 0 && h->bn_kv % 128 == 0 && njobs_b > sms) {
-        const int r = njobs_b % sms;
-        if (r > 0 && 2 * r <= sms) {
-            h->kv_halves = r;
-            h->kv_halves_on = true;
-        }
+    if (!h->decode && Lq == 0 && h->bn_kv % 128 == 0) {
+        h->kv_halves = plan_last_round_halves(njobs_b, sms);
+        h->kv_halves_on = h->kv_halves > 0;
     }
     // The cooperative decode kernel takes one token tile, heads of at most
     // kDecodeMaxBN columns and needs one resident CTA per SM.
@@ -1265,6 +1260,9 @@ int mla_prolog_plan(const mla_prolog_dims* dims, int32_t sms, mla_prolog_plan_in
     out->compress_jobs = static_cast<int32_t>(cost.size());
     out->bn_kv = sc.bn_kv;
     out->busiest_bytes = cost.empty() ? 0 : lpt_assign(cost, sms);
+    // a KV-only prefill's last expansion round as half tiles (one CTA per tile)
+    const int njobs_b = cdiv(d.num_heads * (d.nope_dim + d.v_dim), sc.bn_kv) * cdiv(d.T, kBM);
+    out->kv_halves = !sc.decode && Lq == 0 && sc.bn_kv % 128 == 0 ? plan_last_round_halves(njobs_b, sms) : 0;
     return MLA_OK;
 }
 

@@ -458,6 +458,16 @@ inline int plan_compress_tiles(int T, int NA, int kb, int sms, CompressTilePlan 
     return def;
 }
 
+// Jobs of a last round to run as two half jobs each on twice as many
+// workers: the remainder r of `jobs` over `grid` workers when there is more
+// than one round and 2 r workers are free in the last one, else 0 (the
+// busiest worker then does rounds - 1/2 jobs' work instead of rounds).
+inline int plan_last_round_halves(int jobs, int grid) {
+    if (grid <= 0 || jobs <= grid) return 0;
+    const int r = jobs % grid;
+    return r > 0 && 2 * r <= grid ? r : 0;
+}
+
 // kv tiles per super-job of the kv-resident pair kernel: the largest of 8,
 // 4, 2 that still gives every CTA pair a super-job, else 1.  Measured on
 // GB300 (step time): V3 prefill 1932 / 1870 / 1897 / 1893 us with groups of

@@ -171,3 +171,19 @@ def test_w8a8_exact_chain_bounds():
     assert lim * 127 < 2 ** 24 <= (lim + 1) * 127
     # a K of up to kW8ChainKb blocks never needs the mark: the largest possible sum |code| is within the limit
     assert bk * kb * 127 <= lim
+
+
+@pytest.mark.parametrize("name,T,sms,want", [
+    ("v2lite_prefill", 0, 152, 56),    # 512 jobs: 3 rounds + 56, which fit 112 CTAs as halves
+    ("v2lite_prefill", 0, 148, 68),    # 512 = 3 x 148 + 68
+    ("v2lite_prefill", 0, 132, 0),     # 512 = 3 x 132 + 116: 232 halves would not fit one round
+    ("v2lite_prefill", 300, 152, 0),   # 48 jobs: one round
+    ("v2lite_decode", 0, 152, 0),      # decode schedule
+    ("v3_prefill", 0, 152, 0),         # a q path: the pair kernels (the kv-resident kernel plans its own)
+])
+def test_last_round_half_tiles(name, T, sms, want):
+    """The KV-only prefill's last round of expansion jobs as half tiles: the
+    remainder of the jobs over the CTAs when it fits twice into the grid."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    assert binding.plan(d, sms)["kv_halves"] == want
