@@ -148,6 +148,29 @@ def test_w8a8_parity(name, T):
     assert status == 0
 
 
+@pytest.mark.parametrize("name,T", [("v3_decode", 0), ("v2lite_prefill", 300)])
+def test_w8a8_zero_rows_of_x(name, T):
+    """Tokens whose x row is zero: AT-05 gives scale 0 and codes 0, so the
+    compression, the normed rows and their codes (scale 0), K, V, k_pe and
+    q are zero -- every token compared with the oracle as in the parity
+    test, and the zero tokens' outputs exactly zero."""
+    w, d = _w8(name, T)
+    inp = wl.make_inputs(w, d)
+    zero = [0, d.T // 2, d.T - 1]
+    x = inp.x.copy()
+    x[zero] = 0
+    inp = dataclasses.replace(inp, x=x)
+    ww = wl.make_w8a8_weights(w, d)
+    status, outs, ref, _ = check_w8a8(d, inp, ww, sample=384)
+    assert status == 0
+    for t in zero:
+        for k in ("out_k", "out_v", "out_kpe"):
+            assert not outs[k].t[t].float().abs().sum().item(), (k, t)
+        if d.q_lora_rank:
+            assert not outs["out_q_int8"].t[t].abs().sum().item()
+            assert outs["out_scale"].t[t].item() == 0.0
+
+
 @pytest.mark.parametrize("extra", [wl.ROPE_INTERLEAVED, wl.QUANT_PER_HEAD, wl.Q_HEAD_NORM])
 def test_w8a8_q_variants(extra):
     w, d = _w8("v3_prefill", 300)
