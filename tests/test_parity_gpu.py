@@ -701,6 +701,41 @@ def test_kv_half_tiles_keep_outputs(name, T, variant):
     q.close()
 
 
+def test_kv_group_sizes_keep_outputs():
+    """The kv-resident kernel's super-job size (MLA_TUNE_KV_GROUP: 1, 2, 4,
+    8, 16 kv tiles per token tile; the last round's half super-jobs planned
+    again for each) writes the same bytes as the default; sizes outside
+    1 .. the kv tile count are refused."""
+    w = wl.WORKLOADS["v3_prefill"]
+    d = w.dims.with_T(4096)
+    inp = wl.make_inputs(w, d)
+    dins = device_inputs(inp, DEV)
+    p = binding.MlaProlog.from_dims(d)
+    assert "mla_expand_kv_pair_kernel" in p.kernel_names()
+    base = alloc_outputs(d, DEV)
+    run_prolog(p, dins, base)
+    assert p.device_status() == 0
+    for g in (1, 2, 4, 16, 8):
+        p.set_tuning(binding.TUNE_KV_GROUP, g)
+        for halves in (1, 0):
+            try:
+                p.set_tuning(binding.TUNE_KV_HALVES, halves)
+            except binding.MlaPrologError:
+                assert halves == 1  # this group size leaves no short last round
+                continue
+            o = alloc_outputs(d, DEV)
+            run_prolog(p, dins, o)
+            torch.cuda.synchronize()
+            assert p.device_status() == 0, (g, halves)
+            _bits_equal(base, o)
+            del o
+    n_tiles = d.num_heads * (d.nope_dim + d.v_dim) // 256
+    for bad in (0, n_tiles + 1):
+        with pytest.raises(binding.MlaPrologError):
+            p.set_tuning(binding.TUNE_KV_GROUP, bad)
+    p.close()
+
+
 # Unusual shapes for the prefill paths: smaller ranks, few heads, 64-wide nope
 # and value (two heads per 256-column kv tile), ragged token counts.
 _ODD_PREFILL = [
