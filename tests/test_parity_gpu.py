@@ -45,41 +45,48 @@ def _sample(w: wl.Workload, inp: wl.Inputs, n: int):
     return np.array(sorted(must | set(int(i) for i in rest)), np.int32)
 
 
-def check_against_oracle(w: wl.Workload, dims=None, sample=512, positions=None):
+def check_against_oracle(w: wl.Workload, dims=None, sample=512, positions=None, tunings=((),)):
+    """Runs the prolog once per entry of `tunings` (each a sequence of
+    (tuning key, value) pairs set on one handle, in order) and holds every
+    run to the oracle on the same sampled tokens."""
     inp = wl.make_inputs(w, dims)
     if positions is not None:
         inp.positions[:] = positions
     d = inp.dims
     dins = device_inputs(inp, DEV)
-    outs = alloc_outputs(d, DEV)
     p = binding.MlaProlog.from_dims(d)
-    run_prolog(p, dins, outs)
-    status = p.device_status()
     tok = _sample(w, inp, sample)
     ref = oracle.mla_prolog(d, inp.x, inp.gamma, inp.W_a, inp.W_b, inp.positions, inp.cos_sin, tokens=tok,
                             taps=True)
     sel = slice(None) if tok is None else torch.from_numpy(tok.astype(np.int64)).to(DEV)
     Dn, R, H = d.nope_dim, d.rope_dim, d.num_heads
     n = ref["out_kpe"].shape[0]
-    # K's nope columns and V to the BF16 bar; the rotated k_pe (K's rope
-    # slices, out_kpe) to that bar widened by a one-ulp rounding of its inputs
-    k_got = outs["out_k"].t[sel].reshape(n, H, Dn + R)
-    k_want = ref["out_k"].reshape(n, H, Dn + R)
-    bf16_within(k_got[:, :, :Dn], np.ascontiguousarray(k_want[:, :, :Dn]), "out_k nope")
-    bf16_within(outs["out_v"].t[sel], ref["out_v"], "out_v")
     rows = np.arange(d.T) if tok is None else tok
     pos = np.clip(inp.positions[rows], 0, d.max_pos - 1)
     cs = inp.cos_sin[pos]
     kpe_in = ref["c"][:, d.q_lora_rank + d.kv_lora_rank:]
     il = bool(d.flags & wl.ROPE_INTERLEAVED)
-    rope_within(k_got[:, :, Dn:], np.ascontiguousarray(k_want[:, :, Dn:]), kpe_in, cs[:, :R // 2], cs[:, R // 2:],
-                il, "out_k rope")
-    rope_within(outs["out_kpe"].t[sel], ref["out_kpe"].reshape(n, R), kpe_in, cs[:, :R // 2], cs[:, R // 2:], il,
-                "out_kpe")
-    if d.q_lora_rank:
-        quant_within(outs["out_q_int8"].t[sel], outs["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
-    for k, g in outs.items():
-        assert g.guards_intact(), f"{k}: write outside the buffer"
+    status = 0
+    for tune in tunings:
+        for key, value in tune:
+            p.set_tuning(key, value)
+        outs = alloc_outputs(d, DEV)
+        run_prolog(p, dins, outs)
+        status |= p.device_status()
+        # K's nope columns and V to the BF16 bar; the rotated k_pe (K's rope
+        # slices, out_kpe) to that bar widened by a one-ulp rounding of its inputs
+        k_got = outs["out_k"].t[sel].reshape(n, H, Dn + R)
+        k_want = ref["out_k"].reshape(n, H, Dn + R)
+        bf16_within(k_got[:, :, :Dn], np.ascontiguousarray(k_want[:, :, :Dn]), f"out_k nope {tune}")
+        bf16_within(outs["out_v"].t[sel], ref["out_v"], f"out_v {tune}")
+        rope_within(k_got[:, :, Dn:], np.ascontiguousarray(k_want[:, :, Dn:]), kpe_in, cs[:, :R // 2],
+                    cs[:, R // 2:], il, f"out_k rope {tune}")
+        rope_within(outs["out_kpe"].t[sel], ref["out_kpe"].reshape(n, R), kpe_in, cs[:, :R // 2], cs[:, R // 2:],
+                    il, f"out_kpe {tune}")
+        if d.q_lora_rank:
+            quant_within(outs["out_q_int8"].t[sel], outs["out_scale"].t[sel], ref["out_q_int8"], ref["out_scale"])
+        for k, g in outs.items():
+            assert g.guards_intact(), f"{k}: write outside the buffer"
     p.close()
     return status, ref, outs
 
@@ -121,6 +128,26 @@ def test_v3_prefill_beyond_32bit_offsets():
     assert d.T * d.n_q * 4 > 2**32 and d.T * d.num_heads * (d.nope_dim + d.rope_dim) * 2 > 2**31
     status, ref, _ = check_against_oracle(w, dims=d, sample=1024)
     assert status == 0 and ref["bad_positions"] == 0
+
+
+@pytest.mark.parametrize("name,T", [("v3_decode", 0), ("v3_prefill", 640), ("v2lite_prefill", 300)])
+def test_compression_chain_and_drain_settings(name, T):
+    """The compression's accumulation chain length (MLA_TUNE_COMPRESS_GROUP:
+    1, 2, 4, 8 K blocks) and its drained sums with or without TwoSum
+    (MLA_TUNE_COMPRESS_COMPENSATED) change rounding only: every setting
+    within the bar of the oracle on every token; out-of-range values are
+    refused."""
+    w = wl.WORKLOADS[name]
+    d = w.dims.with_T(T) if T else w.dims
+    G, C = binding.TUNE_COMPRESS_GROUP, binding.TUNE_COMPRESS_COMPENSATED
+    tunings = [((G, g), (C, c)) for g in (1, 2, 4, 8) for c in (0, 1)]
+    status, _, _ = check_against_oracle(w, dims=d, sample=d.T, tunings=tunings)
+    assert status == 0
+    p = binding.MlaProlog.from_dims(d)
+    for key, bad in ((G, 0), (G, 65), (C, 2)):
+        with pytest.raises(binding.MlaPrologError):
+            p.set_tuning(key, bad)
+    p.close()
 
 
 @pytest.mark.parametrize("name,T", [("v3_prefill", 640), ("v3_decode", 0), ("v2lite_prefill", 300)])
