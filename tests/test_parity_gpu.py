@@ -110,7 +110,10 @@ RAGGED = wl.Dims(T=300, D=512, q_lora_rank=64, kv_lora_rank=128, rope_dim=32, nu
                         nope_dim=128, v_dim=128, q_lora_rank=0, flags=0),   # decode, narrow kv tiles
     dataclasses.replace(RAGGED, T=96, D=2048, q_lora_rank=96, rope_dim=16, nope_dim=16, v_dim=16,
                         num_heads=7),                     # narrow heads, Lq not a multiple of 64
-], ids=["ragged300q", "T1", "T129", "prefill257", "decode200", "narrow_heads"])
+    dataclasses.replace(RAGGED, T=40, max_pos=1),         # one rope position: every token at 0, RoPE = identity
+    dataclasses.replace(RAGGED, num_heads=1),             # one head
+    dataclasses.replace(RAGGED, T=260, D=64),             # the hidden size one K block
+], ids=["ragged300q", "T1", "T129", "prefill257", "decode200", "narrow_heads", "max_pos1", "one_head", "D64"])
 def test_ragged_parity(dims):
     w = wl.Workload("ragged", dims, positions="uniform")
     status, ref, _ = check_against_oracle(w)
