@@ -526,6 +526,23 @@ __device__ __forceinline__ void norm_token_warp(const NormRopeParams& p, int t, 
         rot[i + half] = static_cast<uint16_t>(pack_bf16x2(o2, 0.0f) & 0xFFFFu);
     }
     __syncwarp();
+    if (32 % nchunk == 0) {
+        // Each lane keeps one 16-byte chunk c of the rotated row and writes
+        // it to every (32 / nchunk)-th head's rope slice from head lane /
+        // nchunk on, then out_kpe and the cache row (lanes below nchunk):
+        // the same bytes as the destination loop below, without its
+        // per-chunk division and destination choice.
+        const int c = lane % nchunk, step = 32 / nchunk;
+        const uint4 v = *reinterpret_cast<const uint4*>(rot + c * 8);
+        const size_t hstride = static_cast<size_t>(p.Dn + R);
+        uint16_t* dst = p.out_k + (static_cast<size_t>(t) * p.H + lane / nchunk) * hstride + p.Dn + c * 8;
+        for (int h = lane / nchunk; h < p.H; h += step, dst += step * hstride) *reinterpret_cast<uint4*>(dst) = v;
+        if (lane < nchunk) {
+            *reinterpret_cast<uint4*>(kpe_dst(p, t, p.H, c, cache_row)) = v;
+            if (cache_row) *reinterpret_cast<uint4*>(kpe_dst(p, t, p.H + 1, c, cache_row)) = v;
+        }
+        return;
+    }
     for (int k = lane; k < ndst * nchunk; k += 32) {
         const int h = k / nchunk, c = k - h * nchunk;
         *reinterpret_cast<uint4*>(kpe_dst(p, t, h, c, cache_row)) = *reinterpret_cast<const uint4*>(rot + c * 8);
